@@ -1,0 +1,76 @@
+"""Each oracle pin is shown to fail on the defect it guards.
+
+The verification list of the bloomery pages ("bloomery early V4.1 README")
+asks that a gate be seen failing on its defect before it is trusted.  Here a
+plausible mistake is planted in a copy of oracle.c (on the CPU, in a temporary
+directory; the committed oracle is never changed), the copy is compiled, and
+the pins that guard that step must reject it.
+"""
+from __future__ import annotations
+
+import os
+import tempfile
+
+import pytest
+
+import oracle
+from test_oracle_pins import PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, text to find, replacement, pins that must catch it)
+MUTANTS = [
+    ("fp16_exponent_bias", "expo - 15", "expo - 14", ["half_to_double", "q8_0_handbuilt"]),
+    ("q8_0_unsigned", "if (q >= 128) q -= 256;", "", ["q8_0_handbuilt"]),
+    ("q4k_nibbles_swapped", "(j % 2 == 0) ? (byte & 15) : (byte >> 4)",
+     "(j % 2 == 1) ? (byte & 15) : (byte >> 4)", ["q4_k_handbuilt"]),
+    ("q4k_min_dropped", "- dmin * (double)m;", ";", ["q4_k_handbuilt"]),
+    ("q4k_min_sign", "- dmin * (double)m;", "+ dmin * (double)m;", ["q4_k_handbuilt"]),
+    ("q4k_scale_high_bits", "((S[j - 4] >> 6) << 4)", "((S[j] >> 6) << 4)", ["q4_k_handbuilt"]),
+    ("q4k_min_high_bits", "((S[j] >> 6) << 4);", "((S[j - 4] >> 6) << 4);", ["q4_k_handbuilt"]),
+    ("q4k_block_stride", "row + b * 144", "row + b * 128", ["q4_k_multiblock_rows"]),
+    ("router_transposed", "(double)Wr[(int64_t)e * H + h]", "(double)Wr[(int64_t)h * E + e]",
+     ["router_integer"]),
+    ("topk_smallest", "if (sa != sb) return sa > sb;", "if (sa != sb) return sa < sb;",
+     ["softmax_topk_bruteforce", "sigmoid_group_bruteforce"]),
+    ("softmax_no_renorm", "if (renormalize) for (int j = 0; j < k; ++j) denom",
+     "if (0) for (int j = 0; j < k; ++j) denom", ["softmax_topk_bruteforce"]),
+    ("sigmoid_gates_use_bias", "denom += s[top[j]];", "denom += sel[top[j]];",
+     ["sigmoid_group_bruteforce"]),
+    ("group_score_top1", "int take = per < 2 ? per : 2;", "int take = 1;",
+     ["sigmoid_group_bruteforce", "sigmoid_group_special"]),
+    ("permute_unstable", "for (int64_t p = 0; p < P; ++p) {\n        int32_t i = cursor[ids[p]]++;",
+     "for (int64_t p = P - 1; p >= 0; --p) {\n        int32_t i = cursor[ids[p]]++;", ["permute_bruteforce"]),
+    ("silu_sign", "return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));", ["ffn_identity"]),
+    ("gate_up_swapped_in_h", "h[i] = silu(g) * u;", "h[i] = g * silu(u);", ["ffn_identity"]),
+    ("combine_drops_weights", "o[n] += w[(int64_t)t * k + j] * yp[n];", "o[n] += yp[n];",
+     ["dense_masked_equals_sparse"]),
+    ("shared_expert_dropped", "for (int n = 0; n < H; ++n) o[n] += ys[n];", "",
+     ["dense_masked_equals_sparse"]),
+    ("rmsnorm_no_mean", "sqrt(ss / H + eps)", "sqrt(ss + eps)", ["rmsnorm"]),
+    ("bf16_truncates", "double r = nearbyint(scaled);", "double r = trunc(scaled);", ["round_bf16"]),
+]
+
+
+def _build_mutant(name, find, repl, tmp):
+    src = open(SRC).read()
+    assert src.count(find) >= 1, f"mutation {name}: pattern not found"
+    mutated = src.replace(find, repl, 1)
+    path = os.path.join(tmp, f"{name}.c")
+    with open(path, "w") as f:
+        f.write(mutated)
+    return oracle.load(oracle.build(force=True, src=path, out=os.path.join(tmp, f"lib{name}.so")))
+
+
+@pytest.mark.parametrize("name,find,repl,pins", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pin_catches_mutant(name, find, repl, pins):
+    with tempfile.TemporaryDirectory() as tmp:
+        lib = _build_mutant(name, find, repl, tmp)
+        for pin in pins:
+            with pytest.raises((AssertionError, ValueError)):
+                PINS[pin](lib)
+
+
+def test_unmutated_oracle_passes_all_pins(olib):
+    for pin in PINS.values():
+        pin(olib)
