@@ -1,0 +1,213 @@
+/*
+ * moe_gb300.h -- C ABI of the GB300 (sm_103a) routed-expert MoE layer library.
+ *
+ * The layer: router logits -> softmax or sigmoid(+bias, group-limited) top-k
+ * with renormalised gates -> token-to-expert permutation with per-expert
+ * offsets -> per-expert SwiGLU FFN over GGUF block-quantized weights (Q4_K,
+ * Q8_0) -> gate-weighted combine, plus an optional unweighted shared expert.
+ *
+ * Where the operation comes from.  The bloomery pages describe an MoE engine
+ * whose routed experts run on the card over the stored GGUF quantization
+ * ("bloomery README 0.3.1", Status table, "Quant types" row), whose prompt
+ * batches run each expert over all its tokens at once ("bloomery V4.1
+ * README", feature list, "Batched prompts"), whose decode step is one CUDA
+ * graph ("bloomery README 0.3.1", "Why it is fast"), and whose router top-k
+ * ids are compared exactly against a CPU reference ("bloomery early V4.1
+ * README", "Oracle sets against ik_llama.cpp").  The pages print none of the
+ * arithmetic; each call below states the definition it implements.
+ *
+ * Conventions for every call
+ *  - Pointers marked (device) are CUDA device pointers owned by the caller;
+ *    (host) pointers are read during the call only.  The library never
+ *    allocates device memory and never synchronizes (except the two
+ *    *_read_device_status calls): each call enqueues kernels on `stream` and
+ *    returns, so every call can be captured in a CUDA graph.
+ *  - Arguments are validated on the host before any launch; a rejected call
+ *    launches nothing and returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED /
+ *    MOE_ERR_WORKSPACE.  A failed launch returns MOE_ERR_CUDA.  The reason
+ *    is readable with moe_last_error() (per host thread).
+ *  - Weight, activation, output and workspace pointers must be 16-byte
+ *    aligned; int32/fp32 routing arrays need 4-byte alignment.
+ *  - Weight matrices are GGUF block rows: [rows][cols / block] blocks, the
+ *    blocks running along the input dimension `cols`.  Q8_0: 34 bytes per 32
+ *    weights (fp16 d, 32 x int8 q; w = d*q).  Q4_K: 144 bytes per 256
+ *    weights (fp16 d, fp16 dmin, 12 bytes of packed 6-bit scales/mins for 8
+ *    sub-blocks of 32, 128 bytes of 4-bit q; w = d*sc_j*q - dmin*m_j).
+ *    For gate/up: rows = I, cols = H.  For down: rows = H, cols = I.
+ *    Expert e of a stacked tensor starts at data + e * expert_stride_bytes.
+ *  - Token-expert pairs: p = t*k + j for token t and its j-th chosen expert.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or mode */
+    MOE_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement */
+    MOE_ERR_WORKSPACE = 3,     /* workspace missing or smaller than the size query */
+    MOE_ERR_CUDA = 4,          /* a CUDA launch or runtime call failed */
+    MOE_ERR_DEVICE_CHECK = 5   /* a device-side check failed (see *_read_device_status) */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_Q8_0 = 2, MOE_Q4_K = 3 } moe_dtype;
+
+typedef enum { MOE_ROUTE_SOFTMAX = 0, MOE_ROUTE_SIGMOID_GROUP = 1 } moe_route_mode;
+
+/* One quantized weight tensor, possibly a stack of experts. */
+typedef struct {
+    moe_dtype qtype;             /* MOE_Q8_0 or MOE_Q4_K */
+    const void* data;            /* (device) 16-byte aligned */
+    int64_t rows, cols;          /* per expert; cols = input dimension */
+    int64_t expert_stride_bytes; /* bytes from expert e to e+1 (multiple of 16) */
+} moe_qmat;
+
+typedef struct {
+    moe_route_mode mode;
+    int n_experts;               /* E, 1..1024 */
+    int top_k;                   /* k, 1..min(E, 32) */
+    int n_groups;                /* sigmoid mode: G divides E, G <= 32 (softmax: ignored) */
+    int topk_groups;             /* sigmoid mode: groups kept, 1..G */
+    float routed_scale;          /* gates are multiplied by this (1.0 = none) */
+    int renormalize;             /* 1: gates renormalised over the chosen k */
+} moe_route_cfg;
+
+/* ---------------------------------------------------------------- steps */
+
+/*
+ * moe_route -- router logits and top-k gates for T tokens.
+ *   logits[t,e] = sum_h x[t,h] * W_router[e,h]          (fp32 accumulate)
+ *   softmax mode: the k largest logits (ties: lower id); gates = softmax over
+ *     those k (renormalize=1) or softmax over all E at those ids (0).
+ *   sigmoid-group mode: s = 1/(1+exp(-l)), sel = s + bias; groups of E/G
+ *     consecutive experts scored by the sum of their two largest sel; keep
+ *     the topk_groups best groups (ties: lower group); the k best sel inside
+ *     them; gates = s_j / sum s (renormalize=1) or s_j; the bias never enters
+ *     a gate.  Gates are then multiplied by routed_scale.
+ * Chosen ids are written in ascending expert id per token.
+ * x (device) [T][H] in x_type (MOE_F32 or MOE_BF16); W_router (device) fp32
+ * [E][H]; bias (device, nullable) fp32 [E]; logits_in (device, nullable)
+ * fp32 [T][E] replaces the router product; logits_out (device, nullable) fp32
+ * [T][E]; topk_ids (device) int32 [T][k]; topk_w (device) fp32 [T][k].
+ * T = 0 is a no-op.
+ */
+moe_status moe_route(const moe_route_cfg* cfg, const void* x, moe_dtype x_type, int T, int H,
+                     const float* W_router, const float* bias, const float* logits_in,
+                     float* logits_out, int32_t* topk_ids, float* topk_w, moe_stream_t stream);
+
+/*
+ * moe_permute -- group the P = T*k token-expert pairs by expert.
+ *   offsets[e] = number of pairs with id < e (E+1 entries, offsets[E] = P);
+ *   sorted_pairs lists p in ascending (expert, p) order (stable);
+ *   pair_pos[sorted_pairs[i]] = i.
+ * topk_ids (device) int32 [T][k], each in [0, E) (an out-of-range id sets the
+ * device status word in the workspace to MOE_ERR_DEVICE_CHECK and the pair is
+ * dropped); sorted_pairs, pair_pos (device) int32 [P]; offsets (device) int32
+ * [E+1]; workspace (device) of moe_permute_workspace_size() bytes.
+ */
+moe_status moe_permute_workspace_size(int T, int k, int E, size_t* bytes);
+moe_status moe_permute(const int32_t* topk_ids, int T, int k, int E, int32_t* sorted_pairs,
+                       int32_t* offsets, int32_t* pair_pos, void* workspace, size_t ws_bytes,
+                       moe_stream_t stream);
+
+/*
+ * moe_expert_ffn -- the SwiGLU experts over the grouped pairs.
+ *   for sorted position i with pair p = sorted_pairs[i], token t = p / k,
+ *   expert e (offsets[e] <= i < offsets[e+1]):
+ *   g = Wg[e] x_t, u = Wu[e] x_t, h = g/(1+exp(-g)) * u, y_pairs[i] = Wd[e] h.
+ * gate, up: rows I, cols H; down: rows H, cols I (host structs, device data).
+ * x (device) [T][H]; y_pairs (device) fp32 [T*k][H], row i = sorted position
+ * i.  With sorted_pairs = NULL and offsets = NULL (then E = 1, k = 1) the
+ * expert runs on every token in order, as a shared expert does.
+ * fp32 accumulation, fp32 h, for every T.
+ */
+moe_status moe_expert_ffn_workspace_size(int T, int k, int E, int H, int I, size_t* bytes);
+moe_status moe_expert_ffn(const moe_qmat* gate, const moe_qmat* up, const moe_qmat* down, int E,
+                          const void* x, moe_dtype x_type, int T, int H, int I,
+                          const int32_t* sorted_pairs, const int32_t* offsets, int k,
+                          float* y_pairs, void* workspace, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_combine -- out[t,n] = sum_{j<k} topk_w[t,j] * y_pairs[pair_pos[t*k+j], n]
+ *                           (+ shared_out[t,n]) (+ old out[t,n] if accumulate),
+ * summed in ascending j, then the shared term, then the old value: the same
+ * bits on every run.  y_pairs, shared_out (nullable), out: fp32 (device).
+ */
+moe_status moe_combine(const float* y_pairs, const float* topk_w, const int32_t* pair_pos, int T,
+                       int k, int H, const float* shared_out, int accumulate, float* out,
+                       moe_stream_t stream);
+
+/*
+ * moe_rmsnorm_bf16 -- u[t,h] = bf16( x[t,h] / sqrt(mean_h x[t,:]^2 + eps) * gamma[h] )
+ * (fp32 arithmetic, round to nearest even).  x fp32 [T][H], gamma fp32 [H],
+ * u bf16 [T][H] (device).  Used between stacked layers.
+ */
+moe_status moe_rmsnorm_bf16(const float* x, const float* gamma, int T, int H, float eps, void* u,
+                            moe_stream_t stream);
+
+/* ---------------------------------------------------------------- fused layer */
+
+typedef struct {
+    moe_route_cfg route;
+    int hidden;                   /* H */
+    int intermediate;             /* I of a routed expert */
+    moe_dtype x_type;             /* MOE_F32 or MOE_BF16 */
+    const float* W_router;        /* (device) fp32 [E][H] */
+    const float* bias;            /* (device, nullable) fp32 [E] */
+    moe_qmat gate, up, down;      /* routed experts, stacked over E */
+    int shared_intermediate;      /* I_s, 0 = no shared expert */
+    moe_qmat s_gate, s_up, s_down;/* shared expert (single matrices) */
+    int accumulate;               /* 1: out += layer(x) (a residual add); 0: out = layer(x) */
+    int tc_min_tokens;            /* T at or above this uses the tensor-core path (0 = default 128) */
+} moe_layer_desc;
+
+typedef struct moe_layer_plan moe_layer_plan;
+
+/* Validates the description once and keeps a host copy of it. */
+moe_status moe_layer_plan_create(const moe_layer_desc* desc, moe_layer_plan** plan);
+moe_status moe_layer_plan_destroy(moe_layer_plan* plan);
+/* Bytes of device workspace moe_layer needs for up to T tokens. */
+moe_status moe_layer_workspace_size(const moe_layer_plan* plan, int T, size_t* bytes);
+/*
+ * moe_layer -- the whole layer: route, permute, experts, combine (+ shared),
+ * for T tokens of x (device, [T][H] in desc->x_type) into out (device, fp32
+ * [T][H]).  Enqueued on `stream` with no host synchronization and no host
+ * read-back, so it can be captured in a CUDA graph; replays give the same
+ * bits as eager calls.  The expert path is chosen from T on the host:
+ * T < tc_min_tokens runs the fp32 dequant-GEMV kernels, larger T the
+ * tensor-core grouped GEMM (fp16 operands, fp32 accumulate).
+ */
+moe_status moe_layer(const moe_layer_plan* plan, const void* x, int T, float* out, void* workspace,
+                     size_t ws_bytes, moe_stream_t stream);
+/* Device pointers into a moe_layer workspace (any output may be NULL) to
+ * the last call's ids int32 [T][k], gates fp32 [T][k] and offsets int32
+ * [E+1]. */
+moe_status moe_layer_debug_views(const moe_layer_plan* plan, int T, void* workspace,
+                                 int32_t** topk_ids, float** topk_w, int32_t** offsets);
+
+/* Copies the device status word of a workspace (MOE_OK or a MOE_ERR_* code
+ * raised by a device-side check) to *code and clears it.  Synchronizes the
+ * stream first; call it outside graph capture. */
+moe_status moe_read_device_status(const moe_layer_plan* plan, int T, void* workspace, int32_t* code,
+                                  moe_stream_t stream);
+moe_status moe_permute_read_device_status(int T, int k, int E, void* workspace, int32_t* code,
+                                          moe_stream_t stream);
+
+/* The reason for the last non-MOE_OK status returned on this host thread. */
+const char* moe_last_error(void);
+/* Library version string. */
+const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,222 @@
+"""ctypes binding of the C ABI in include/moe_gb300.h (argument marshalling only).
+
+Every function keeps the C name and argument order.  Array arguments accept a
+torch tensor (its data_ptr() is passed), a raw integer device address, or
+None for a nullable pointer; `stream` defaults to torch's current CUDA stream.
+A non-MOE_OK status raises MoeError with the library's own message.  Nothing
+here computes any part of the layer: if the CUDA library cannot be loaded,
+every call fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+HEADER = os.path.join(os.path.dirname(HERE), "include", "moe_gb300.h")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE_CHECK = range(6)
+MOE_F32, MOE_BF16, MOE_Q8_0, MOE_Q4_K = range(4)
+MOE_ROUTE_SOFTMAX, MOE_ROUTE_SIGMOID_GROUP = range(2)
+
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
+                4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_CHECK"}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class moe_route_cfg(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int), ("n_experts", ctypes.c_int), ("top_k", ctypes.c_int),
+                ("n_groups", ctypes.c_int), ("topk_groups", ctypes.c_int), ("routed_scale", ctypes.c_float),
+                ("renormalize", ctypes.c_int)]
+
+
+class moe_qmat(ctypes.Structure):
+    _fields_ = [("qtype", ctypes.c_int), ("data", ctypes.c_void_p), ("rows", ctypes.c_int64),
+                ("cols", ctypes.c_int64), ("expert_stride_bytes", ctypes.c_int64)]
+
+
+class moe_layer_desc(ctypes.Structure):
+    _fields_ = [("route", moe_route_cfg), ("hidden", ctypes.c_int), ("intermediate", ctypes.c_int),
+                ("x_type", ctypes.c_int), ("W_router", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+                ("gate", moe_qmat), ("up", moe_qmat), ("down", moe_qmat),
+                ("shared_intermediate", ctypes.c_int), ("s_gate", moe_qmat), ("s_up", moe_qmat),
+                ("s_down", moe_qmat), ("accumulate", ctypes.c_int), ("tc_min_tokens", ctypes.c_int)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return os.path.join(HERE, "_build", "libmoe_gb300.so")
+
+
+def load(build_if_missing: bool = True):
+    """The loaded CUDA library (built in-tree on first use when missing)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if build_if_missing:
+                from . import build as _build
+                path = _build.build()
+            if not os.path.exists(path):
+                raise OSError(f"the CUDA library {path} is missing; run __graft_entry__.build()")
+            _lib = _declare(ctypes.CDLL(path))
+    return _lib
+
+
+def _declare(lib):
+    P, I, I64, S, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    PS = ctypes.POINTER(ctypes.c_size_t)
+    sig = {
+        "moe_route": [ctypes.POINTER(moe_route_cfg), P, I, I, I, P, P, P, P, P, P, P],
+        "moe_permute_workspace_size": [I, I, I, PS],
+        "moe_permute": [P, I, I, I, P, P, P, P, S, P],
+        "moe_expert_ffn_workspace_size": [I, I, I, I, I, PS],
+        "moe_expert_ffn": [ctypes.POINTER(moe_qmat)] * 3 + [I, P, I, I, I, I, P, P, I, P, P, S, P],
+        "moe_combine": [P, P, P, I, I, I, P, I, P, P],
+        "moe_rmsnorm_bf16": [P, P, I, I, F, P, P],
+        "moe_layer_plan_create": [ctypes.POINTER(moe_layer_desc), ctypes.POINTER(P)],
+        "moe_layer_plan_destroy": [P],
+        "moe_layer_workspace_size": [P, I, PS],
+        "moe_layer": [P, P, I, P, P, S, P],
+        "moe_layer_debug_views": [P, I, P, ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P)],
+        "moe_read_device_status": [P, I, P, ctypes.POINTER(ctypes.c_int32), P],
+        "moe_permute_read_device_status": [I, I, I, P, ctypes.POINTER(ctypes.c_int32), P],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.moe_last_error.argtypes = []
+    lib.moe_last_error.restype = ctypes.c_char_p
+    lib.moe_version.argtypes = []
+    lib.moe_version.restype = ctypes.c_char_p
+    del I64
+    return lib
+
+
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int):
+    if status != MOE_OK:
+        msg = load().moe_last_error().decode(errors="replace")
+        raise MoeError(status, msg)
+
+
+def qmat(qtype: int, data, rows: int, cols: int, expert_stride_bytes: int = 0) -> moe_qmat:
+    return moe_qmat(qtype, _p(data), rows, cols, expert_stride_bytes)
+
+
+def route_cfg(mode: int, n_experts: int, top_k: int, n_groups: int = 1, topk_groups: int = 1,
+              routed_scale: float = 1.0, renormalize: bool = True) -> moe_route_cfg:
+    return moe_route_cfg(mode, n_experts, top_k, n_groups, topk_groups, routed_scale, int(renormalize))
+
+
+# ------------------------------------------------------------------ calls (C names)
+
+def moe_route(cfg, x, x_type, T, H, W_router, bias, logits_in, logits_out, topk_ids, topk_w, stream=None):
+    _check(load().moe_route(ctypes.byref(cfg), _p(x), x_type, T, H, _p(W_router), _p(bias), _p(logits_in),
+                            _p(logits_out), _p(topk_ids), _p(topk_w), _stream(stream)))
+
+
+def moe_permute_workspace_size(T, k, E) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().moe_permute_workspace_size(T, k, E, ctypes.byref(n)))
+    return n.value
+
+
+def moe_permute(topk_ids, T, k, E, sorted_pairs, offsets, pair_pos, workspace, ws_bytes, stream=None):
+    _check(load().moe_permute(_p(topk_ids), T, k, E, _p(sorted_pairs), _p(offsets), _p(pair_pos),
+                              _p(workspace), ws_bytes, _stream(stream)))
+
+
+def moe_expert_ffn_workspace_size(T, k, E, H, I) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().moe_expert_ffn_workspace_size(T, k, E, H, I, ctypes.byref(n)))
+    return n.value
+
+
+def moe_expert_ffn(gate, up, down, E, x, x_type, T, H, I, sorted_pairs, offsets, k, y_pairs, workspace,
+                   ws_bytes, stream=None):
+    _check(load().moe_expert_ffn(ctypes.byref(gate), ctypes.byref(up), ctypes.byref(down), E, _p(x), x_type,
+                                 T, H, I, _p(sorted_pairs), _p(offsets), k, _p(y_pairs), _p(workspace),
+                                 ws_bytes, _stream(stream)))
+
+
+def moe_combine(y_pairs, topk_w, pair_pos, T, k, H, shared_out, accumulate, out, stream=None):
+    _check(load().moe_combine(_p(y_pairs), _p(topk_w), _p(pair_pos), T, k, H, _p(shared_out),
+                              int(accumulate), _p(out), _stream(stream)))
+
+
+def moe_rmsnorm_bf16(x, gamma, T, H, eps, u, stream=None):
+    _check(load().moe_rmsnorm_bf16(_p(x), _p(gamma), T, H, float(eps), _p(u), _stream(stream)))
+
+
+def moe_layer_plan_create(desc: moe_layer_desc) -> int:
+    h = ctypes.c_void_p(0)
+    _check(load().moe_layer_plan_create(ctypes.byref(desc), ctypes.byref(h)))
+    return h.value
+
+
+def moe_layer_plan_destroy(plan: int):
+    _check(load().moe_layer_plan_destroy(plan))
+
+
+def moe_layer_workspace_size(plan: int, T: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().moe_layer_workspace_size(plan, T, ctypes.byref(n)))
+    return n.value
+
+
+def moe_layer(plan, x, T, out, workspace, ws_bytes, stream=None):
+    _check(load().moe_layer(plan, _p(x), T, _p(out), _p(workspace), ws_bytes, _stream(stream)))
+
+
+def moe_layer_debug_views(plan, T, workspace):
+    a, b, c = ctypes.c_void_p(0), ctypes.c_void_p(0), ctypes.c_void_p(0)
+    _check(load().moe_layer_debug_views(plan, T, _p(workspace), ctypes.byref(a), ctypes.byref(b),
+                                        ctypes.byref(c)))
+    return a.value, b.value, c.value
+
+
+def moe_read_device_status(plan, T, workspace, stream=None) -> int:
+    code = ctypes.c_int32(0)
+    _check(load().moe_read_device_status(plan, T, _p(workspace), ctypes.byref(code), _stream(stream)))
+    return code.value
+
+
+def moe_permute_read_device_status(T, k, E, workspace, stream=None) -> int:
+    code = ctypes.c_int32(0)
+    _check(load().moe_permute_read_device_status(T, k, E, _p(workspace), ctypes.byref(code), _stream(stream)))
+    return code.value
+
+
+def moe_last_error() -> str:
+    return load().moe_last_error().decode(errors="replace")
+
+
+def moe_version() -> str:
+    return load().moe_version().decode()

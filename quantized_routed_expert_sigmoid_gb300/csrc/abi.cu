@@ -1,0 +1,414 @@
+// abi.cu -- the C ABI (include/moe_gb300.h): host-side validation, workspace
+// layout, and the order of launches for each call.  No device memory is
+// allocated here and no call synchronizes (the two status reads aside).
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+
+#include "internal.cuh"
+
+using namespace moe;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+moe_status fail(moe_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+moe_status cuda_fail(cudaError_t err, const char* what) {
+    return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(err));
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int64_t row_bytes(moe_dtype q, int64_t cols) {
+    if (q == MOE_Q4_K) return cols / kQ4KWeights * kQ4KBytes;
+    if (q == MOE_Q8_0) return cols / kQ80Weights * kQ80Bytes;
+    return -1;
+}
+
+moe_status check_qmat(const moe_qmat* m, const char* name, int64_t rows, int64_t cols, int E) {
+    if (!m) return fail(MOE_ERR_INVALID_ARG, "%s: NULL matrix", name);
+    if (m->qtype != MOE_Q4_K && m->qtype != MOE_Q8_0)
+        return fail(MOE_ERR_UNSUPPORTED, "%s: qtype %d (supported: Q8_0, Q4_K)", name, (int)m->qtype);
+    if (!m->data) return fail(MOE_ERR_INVALID_ARG, "%s: NULL data", name);
+    if (!aligned(m->data, 16)) return fail(MOE_ERR_INVALID_ARG, "%s: data not 16-byte aligned", name);
+    if (m->rows != rows || m->cols != cols)
+        return fail(MOE_ERR_INVALID_ARG, "%s: shape %lldx%lld, expected %lldx%lld", name, (long long)m->rows,
+                    (long long)m->cols, (long long)rows, (long long)cols);
+    const int blk = m->qtype == MOE_Q4_K ? kQ4KWeights : kQ80Weights;
+    if (cols % blk) return fail(MOE_ERR_INVALID_ARG, "%s: cols %lld not a multiple of %d", name, (long long)cols, blk);
+    const int64_t need = rows * row_bytes(m->qtype, cols);
+    if (E > 1 && (m->expert_stride_bytes < need || m->expert_stride_bytes % 16))
+        return fail(MOE_ERR_INVALID_ARG, "%s: expert stride %lld (need >= %lld, multiple of 16)", name,
+                    (long long)m->expert_stride_bytes, (long long)need);
+    return MOE_OK;
+}
+
+moe_status check_route_cfg(const moe_route_cfg* c) {
+    if (!c) return fail(MOE_ERR_INVALID_ARG, "route cfg is NULL");
+    if (c->n_experts < 1 || c->n_experts > kMaxExperts)
+        return fail(MOE_ERR_INVALID_ARG, "n_experts %d outside 1..%d", c->n_experts, kMaxExperts);
+    if (c->top_k < 1 || c->top_k > c->n_experts || c->top_k > kMaxTopK)
+        return fail(MOE_ERR_INVALID_ARG, "top_k %d outside 1..min(E, %d)", c->top_k, kMaxTopK);
+    if (c->mode == MOE_ROUTE_SIGMOID_GROUP) {
+        if (c->n_groups < 1 || c->n_groups > 32 || c->n_experts % c->n_groups)
+            return fail(MOE_ERR_INVALID_ARG, "n_groups %d must divide E and be <= 32", c->n_groups);
+        if (c->topk_groups < 1 || c->topk_groups > c->n_groups)
+            return fail(MOE_ERR_INVALID_ARG, "topk_groups %d outside 1..n_groups", c->topk_groups);
+        if (c->top_k > c->topk_groups * (c->n_experts / c->n_groups))
+            return fail(MOE_ERR_INVALID_ARG, "top_k %d exceeds the experts of the kept groups", c->top_k);
+    } else if (c->mode != MOE_ROUTE_SOFTMAX) {
+        return fail(MOE_ERR_INVALID_ARG, "unknown routing mode %d", (int)c->mode);
+    }
+    return MOE_OK;
+}
+
+struct FfnWs {
+    size_t h, total;
+};
+FfnWs ffn_ws(int T, int k, int I) {
+    FfnWs w;
+    w.h = 0;
+    w.total = align_up((size_t)T * k * I * sizeof(float), 256);
+    return w;
+}
+
+}  // namespace
+
+struct moe_layer_plan {
+    moe_layer_desc d;
+};
+
+namespace {
+
+// Workspace of moe_layer for T tokens (offsets in bytes, all 256-aligned).
+struct LayerWs {
+    size_t hdr, logits, ids, w, sorted, pair_pos, offsets, chunk, h, y, sh_h, sh_y, total;
+};
+
+LayerWs layer_ws(const moe_layer_desc& d, int T) {
+    const int E = d.route.n_experts, k = d.route.top_k, H = d.hidden, I = d.intermediate;
+    const size_t P = (size_t)T * k;
+    LayerWs w;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+    w.hdr = take(kHeaderBytes);
+    w.logits = take((size_t)T * E * 4);
+    w.ids = take(P * 4);
+    w.w = take(P * 4);
+    w.sorted = take(P * 4);
+    w.pair_pos = take(P * 4);
+    w.offsets = take((size_t)(E + 1) * 4);
+    w.chunk = take(permute_scratch_bytes(T, k, E));
+    w.h = take(P * I * 4);
+    w.y = take(P * H * 4);
+    const int Is = d.shared_intermediate;
+    w.sh_h = take(Is > 0 ? (size_t)T * Is * 4 : 0);
+    w.sh_y = take(Is > 0 ? (size_t)T * H * 4 : 0);
+    w.total = o;
+    return w;
+}
+
+template <typename T>
+T* at(void* base, size_t off) {
+    return reinterpret_cast<T*>(reinterpret_cast<char*>(base) + off);
+}
+
+moe_status run_ffn(const moe_qmat& gate, const moe_qmat& up, const moe_qmat& down, int E, const void* x,
+                   bool x_bf16, int T, int H, int I, const int32_t* sorted, const int32_t* offsets, int k,
+                   float* h, float* y, cudaStream_t s) {
+    GemvArgs g{};
+    g.qtype = gate.qtype;
+    g.gateup = true;
+    g.w0 = static_cast<const uint8_t*>(gate.data);
+    g.w1 = static_cast<const uint8_t*>(up.data);
+    g.expert_stride = gate.expert_stride_bytes;
+    g.rows = I;
+    g.K = H;
+    g.vin = x;
+    g.vin_bf16 = x_bf16;
+    g.sorted_pairs = sorted;
+    g.offsets = offsets;
+    g.E = E;
+    g.k = k;
+    g.n_pairs = T * k;
+    g.out = h;
+    cudaError_t err = launch_qgemv(g, s);
+    if (err != cudaSuccess) return cuda_fail(err, "gate/up kernel");
+    GemvArgs dn = g;
+    dn.qtype = down.qtype;
+    dn.gateup = false;
+    dn.w0 = static_cast<const uint8_t*>(down.data);
+    dn.w1 = nullptr;
+    dn.expert_stride = down.expert_stride_bytes;
+    dn.rows = H;
+    dn.K = I;
+    dn.vin = h;
+    dn.vin_bf16 = false;
+    dn.out = y;
+    err = launch_qgemv(dn, s);
+    if (err != cudaSuccess) return cuda_fail(err, "down kernel");
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_last_error(void) { return g_err; }
+const char* moe_version(void) { return "moe_gb300 0.1 (sm_103a)"; }
+
+moe_status moe_route(const moe_route_cfg* cfg, const void* x, moe_dtype x_type, int T, int H,
+                     const float* W_router, const float* bias, const float* logits_in, float* logits_out,
+                     int32_t* topk_ids, float* topk_w, moe_stream_t stream) {
+    moe_status st = check_route_cfg(cfg);
+    if (st) return st;
+    if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T = %d < 0", T);
+    if (T == 0) return MOE_OK;
+    if (!topk_ids || !topk_w) return fail(MOE_ERR_INVALID_ARG, "topk_ids / topk_w are NULL");
+    if (!aligned(topk_ids, 4) || !aligned(topk_w, 4)) return fail(MOE_ERR_INVALID_ARG, "ids/w not 4-byte aligned");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const float* logits = logits_in;
+    if (!logits_in) {
+        if (!logits_out) return fail(MOE_ERR_INVALID_ARG, "logits_out is needed when logits_in is NULL");
+        if (!x || !W_router) return fail(MOE_ERR_INVALID_ARG, "x / W_router are NULL");
+        if (x_type != MOE_F32 && x_type != MOE_BF16) return fail(MOE_ERR_UNSUPPORTED, "x_type %d", (int)x_type);
+        if (H < 4 || H % 32) return fail(MOE_ERR_INVALID_ARG, "H = %d must be a positive multiple of 32", H);
+        if (!aligned(x, 16) || !aligned(W_router, 16) || !aligned(logits_out, 4))
+            return fail(MOE_ERR_INVALID_ARG, "x / W_router must be 16-byte aligned");
+        cudaError_t err = launch_router_logits(x, x_type == MOE_BF16, T, H, W_router, cfg->n_experts,
+                                               logits_out, nullptr, s);
+        if (err != cudaSuccess) return cuda_fail(err, "router logits kernel");
+        logits = logits_out;
+    } else if (logits_out && logits_out != logits_in) {
+        cudaError_t err = cudaMemcpyAsync(logits_out, logits_in, sizeof(float) * (size_t)T * cfg->n_experts,
+                                          cudaMemcpyDeviceToDevice, s);
+        if (err != cudaSuccess) return cuda_fail(err, "logits copy");
+    }
+    cudaError_t err = launch_topk(*cfg, logits, bias, T, topk_ids, topk_w, nullptr, s);
+    if (err != cudaSuccess) return cuda_fail(err, "top-k kernel");
+    return MOE_OK;
+}
+
+moe_status moe_permute_workspace_size(int T, int k, int E, size_t* bytes) {
+    if (!bytes) return fail(MOE_ERR_INVALID_ARG, "bytes is NULL");
+    if (T < 0 || k < 1 || E < 1 || E > kMaxExperts) return fail(MOE_ERR_INVALID_ARG, "bad T/k/E");
+    *bytes = kHeaderBytes + permute_scratch_bytes(T, k, E);
+    return MOE_OK;
+}
+
+moe_status moe_permute(const int32_t* topk_ids, int T, int k, int E, int32_t* sorted_pairs, int32_t* offsets,
+                       int32_t* pair_pos, void* workspace, size_t ws_bytes, moe_stream_t stream) {
+    size_t need = 0;
+    moe_status st = moe_permute_workspace_size(T, k, E, &need);
+    if (st) return st;
+    if (!offsets) return fail(MOE_ERR_INVALID_ARG, "offsets is NULL");
+    if (T > 0 && (!topk_ids || !sorted_pairs || !pair_pos)) return fail(MOE_ERR_INVALID_ARG, "NULL array");
+    if ((int64_t)T * k > (int64_t)1 << 30) return fail(MOE_ERR_INVALID_ARG, "T*k too large");
+    if (!workspace || ws_bytes < need)
+        return fail(MOE_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace ? ws_bytes : 0, need);
+    if (!aligned(workspace, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    WsHeader* hdr = at<WsHeader>(workspace, 0);
+    cudaError_t err = cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s);
+    if (err != cudaSuccess) return cuda_fail(err, "workspace header reset");
+    err = launch_permute(topk_ids, T, k, E, sorted_pairs, offsets, pair_pos, hdr,
+                         at<int32_t>(workspace, kHeaderBytes), s);
+    if (err != cudaSuccess) return cuda_fail(err, "permute kernel");
+    return MOE_OK;
+}
+
+moe_status moe_permute_read_device_status(int T, int k, int E, void* workspace, int32_t* code,
+                                          moe_stream_t stream) {
+    (void)T; (void)k; (void)E;
+    if (!workspace || !code) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t err = cudaStreamSynchronize(s);
+    if (err == cudaSuccess) err = cudaMemcpy(code, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost);
+    if (err == cudaSuccess) err = cudaMemset(workspace, 0, sizeof(int32_t));
+    if (err != cudaSuccess) return cuda_fail(err, "status read");
+    return MOE_OK;
+}
+
+moe_status moe_expert_ffn_workspace_size(int T, int k, int E, int H, int I, size_t* bytes) {
+    (void)E; (void)H;
+    if (!bytes) return fail(MOE_ERR_INVALID_ARG, "bytes is NULL");
+    if (T < 0 || k < 1 || I < 1) return fail(MOE_ERR_INVALID_ARG, "bad T/k/I");
+    *bytes = ffn_ws(T, k, I).total;
+    return MOE_OK;
+}
+
+moe_status moe_expert_ffn(const moe_qmat* gate, const moe_qmat* up, const moe_qmat* down, int E, const void* x,
+                          moe_dtype x_type, int T, int H, int I, const int32_t* sorted_pairs,
+                          const int32_t* offsets, int k, float* y_pairs, void* workspace, size_t ws_bytes,
+                          moe_stream_t stream) {
+    if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T = %d < 0", T);
+    if (E < 1 || E > kMaxExperts || k < 1 || k > kMaxTopK) return fail(MOE_ERR_INVALID_ARG, "bad E/k");
+    if (H < 32 || I < 32) return fail(MOE_ERR_INVALID_ARG, "H/I too small");
+    moe_status st;
+    if ((st = check_qmat(gate, "gate", I, H, E)) || (st = check_qmat(up, "up", I, H, E)) ||
+        (st = check_qmat(down, "down", H, I, E)))
+        return st;
+    if (gate->qtype != up->qtype) return fail(MOE_ERR_UNSUPPORTED, "gate and up must share a qtype");
+    if (gate->expert_stride_bytes != up->expert_stride_bytes)
+        return fail(MOE_ERR_INVALID_ARG, "gate and up must share an expert stride");
+    if (x_type != MOE_F32 && x_type != MOE_BF16) return fail(MOE_ERR_UNSUPPORTED, "x_type %d", (int)x_type);
+    if ((sorted_pairs == nullptr) != (offsets == nullptr))
+        return fail(MOE_ERR_INVALID_ARG, "sorted_pairs and offsets must both be set or both be NULL");
+    if (!sorted_pairs && (E != 1 || k != 1))
+        return fail(MOE_ERR_INVALID_ARG, "the identity mapping needs E = 1 and k = 1");
+    if (T == 0) return MOE_OK;
+    if (!x || !y_pairs) return fail(MOE_ERR_INVALID_ARG, "x / y_pairs are NULL");
+    if (!aligned(x, 16) || !aligned(y_pairs, 16)) return fail(MOE_ERR_INVALID_ARG, "x / y_pairs not 16-byte aligned");
+    const FfnWs w = ffn_ws(T, k, I);
+    if (!workspace || ws_bytes < w.total)
+        return fail(MOE_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace ? ws_bytes : 0, w.total);
+    if (!aligned(workspace, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+    return run_ffn(*gate, *up, *down, E, x, x_type == MOE_BF16, T, H, I, sorted_pairs, offsets, k,
+                   at<float>(workspace, w.h), y_pairs, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_combine(const float* y_pairs, const float* topk_w, const int32_t* pair_pos, int T, int k, int H,
+                       const float* shared_out, int accumulate, float* out, moe_stream_t stream) {
+    if (T < 0 || k < 1 || H < 4 || H % 4) return fail(MOE_ERR_INVALID_ARG, "bad T/k/H");
+    if (T == 0) return MOE_OK;
+    if (!y_pairs || !topk_w || !pair_pos || !out) return fail(MOE_ERR_INVALID_ARG, "NULL array");
+    if (!aligned(y_pairs, 16) || !aligned(out, 16) || (shared_out && !aligned(shared_out, 16)))
+        return fail(MOE_ERR_INVALID_ARG, "y_pairs / shared_out / out not 16-byte aligned");
+    cudaError_t err = launch_combine(y_pairs, topk_w, pair_pos, T, k, H, shared_out, accumulate != 0, out,
+                                     reinterpret_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return cuda_fail(err, "combine kernel");
+    return MOE_OK;
+}
+
+moe_status moe_rmsnorm_bf16(const float* x, const float* gamma, int T, int H, float eps, void* u,
+                            moe_stream_t stream) {
+    if (T < 0 || H < 4 || H % 4) return fail(MOE_ERR_INVALID_ARG, "bad T/H");
+    if (T == 0) return MOE_OK;
+    if (!x || !gamma || !u) return fail(MOE_ERR_INVALID_ARG, "NULL array");
+    if (!aligned(x, 16) || !aligned(gamma, 16) || !aligned(u, 16))
+        return fail(MOE_ERR_INVALID_ARG, "x / gamma / u not 16-byte aligned");
+    if (!(eps >= 0.0f)) return fail(MOE_ERR_INVALID_ARG, "eps must be >= 0");
+    cudaError_t err = launch_rmsnorm_bf16(x, gamma, T, H, eps, u, reinterpret_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return cuda_fail(err, "rmsnorm kernel");
+    return MOE_OK;
+}
+
+moe_status moe_layer_plan_create(const moe_layer_desc* desc, moe_layer_plan** plan) {
+    if (!desc || !plan) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    *plan = nullptr;
+    const moe_layer_desc& d = *desc;
+    moe_status st = check_route_cfg(&d.route);
+    if (st) return st;
+    const int E = d.route.n_experts, H = d.hidden, I = d.intermediate;
+    if (H < 32 || H % 32 || I < 32) return fail(MOE_ERR_INVALID_ARG, "hidden %d / intermediate %d", H, I);
+    if (d.x_type != MOE_F32 && d.x_type != MOE_BF16) return fail(MOE_ERR_UNSUPPORTED, "x_type %d", (int)d.x_type);
+    if (!d.W_router || !aligned(d.W_router, 16)) return fail(MOE_ERR_INVALID_ARG, "W_router NULL or misaligned");
+    if (d.route.mode == MOE_ROUTE_SOFTMAX && d.bias)
+        return fail(MOE_ERR_INVALID_ARG, "a selection bias needs the sigmoid-group mode");
+    if ((st = check_qmat(&d.gate, "gate", I, H, E)) || (st = check_qmat(&d.up, "up", I, H, E)) ||
+        (st = check_qmat(&d.down, "down", H, I, E)))
+        return st;
+    if (d.gate.qtype != d.up.qtype || d.gate.expert_stride_bytes != d.up.expert_stride_bytes)
+        return fail(MOE_ERR_INVALID_ARG, "gate and up must share qtype and expert stride");
+    if (d.shared_intermediate < 0) return fail(MOE_ERR_INVALID_ARG, "shared_intermediate < 0");
+    if (d.shared_intermediate > 0) {
+        const int Is = d.shared_intermediate;
+        if ((st = check_qmat(&d.s_gate, "s_gate", Is, H, 1)) || (st = check_qmat(&d.s_up, "s_up", Is, H, 1)) ||
+            (st = check_qmat(&d.s_down, "s_down", H, Is, 1)))
+            return st;
+        if (d.s_gate.qtype != d.s_up.qtype) return fail(MOE_ERR_INVALID_ARG, "s_gate and s_up must share a qtype");
+    }
+    moe_layer_plan* p = new (std::nothrow) moe_layer_plan;
+    if (!p) return fail(MOE_ERR_INVALID_ARG, "out of host memory");
+    p->d = d;
+    if (p->d.tc_min_tokens <= 0) p->d.tc_min_tokens = 128;
+    *plan = p;
+    return MOE_OK;
+}
+
+moe_status moe_layer_plan_destroy(moe_layer_plan* plan) {
+    delete plan;
+    return MOE_OK;
+}
+
+moe_status moe_layer_workspace_size(const moe_layer_plan* plan, int T, size_t* bytes) {
+    if (!plan || !bytes) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T < 0");
+    *bytes = layer_ws(plan->d, T).total;
+    return MOE_OK;
+}
+
+moe_status moe_layer(const moe_layer_plan* plan, const void* x, int T, float* out, void* workspace,
+                     size_t ws_bytes, moe_stream_t stream) {
+    if (!plan) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+    if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T = %d < 0", T);
+    if (T == 0) return MOE_OK;
+    if ((int64_t)T * plan->d.route.top_k > (int64_t)1 << 30) return fail(MOE_ERR_INVALID_ARG, "T too large");
+    if (!x || !out) return fail(MOE_ERR_INVALID_ARG, "x / out are NULL");
+    if (!aligned(x, 16) || !aligned(out, 16)) return fail(MOE_ERR_INVALID_ARG, "x / out not 16-byte aligned");
+    const moe_layer_desc& d = plan->d;
+    const LayerWs w = layer_ws(d, T);
+    if (!workspace || ws_bytes < w.total)
+        return fail(MOE_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace ? ws_bytes : 0, w.total);
+    if (!aligned(workspace, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int E = d.route.n_experts, k = d.route.top_k, H = d.hidden, I = d.intermediate;
+    const bool xb = d.x_type == MOE_BF16;
+    WsHeader* hdr = at<WsHeader>(workspace, w.hdr);
+    float* logits = at<float>(workspace, w.logits);
+    int32_t* ids = at<int32_t>(workspace, w.ids);
+    float* gw = at<float>(workspace, w.w);
+    int32_t* sorted = at<int32_t>(workspace, w.sorted);
+    int32_t* ppos = at<int32_t>(workspace, w.pair_pos);
+    int32_t* offs = at<int32_t>(workspace, w.offsets);
+    cudaError_t err = launch_router_logits(x, xb, T, H, d.W_router, E, logits, hdr, s);
+    if (err != cudaSuccess) return cuda_fail(err, "router logits kernel");
+    err = launch_topk(d.route, logits, d.bias, T, ids, gw, nullptr, s);
+    if (err != cudaSuccess) return cuda_fail(err, "top-k kernel");
+    err = launch_permute(ids, T, k, E, sorted, offs, ppos, hdr, at<int32_t>(workspace, w.chunk), s);
+    if (err != cudaSuccess) return cuda_fail(err, "permute kernel");
+    float* y = at<float>(workspace, w.y);
+    moe_status st = run_ffn(d.gate, d.up, d.down, E, x, xb, T, H, I, sorted, offs, k,
+                            at<float>(workspace, w.h), y, s);
+    if (st) return st;
+    const float* shared = nullptr;
+    if (d.shared_intermediate > 0) {
+        float* sy = at<float>(workspace, w.sh_y);
+        st = run_ffn(d.s_gate, d.s_up, d.s_down, 1, x, xb, T, H, d.shared_intermediate, nullptr, nullptr, 1,
+                     at<float>(workspace, w.sh_h), sy, s);
+        if (st) return st;
+        shared = sy;
+    }
+    err = launch_combine(y, gw, ppos, T, k, H, shared, d.accumulate != 0, out, s);
+    if (err != cudaSuccess) return cuda_fail(err, "combine kernel");
+    return MOE_OK;
+}
+
+moe_status moe_layer_debug_views(const moe_layer_plan* plan, int T, void* workspace, int32_t** topk_ids,
+                                 float** topk_w, int32_t** offsets) {
+    if (!plan || !workspace) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    const LayerWs w = layer_ws(plan->d, T);
+    if (topk_ids) *topk_ids = at<int32_t>(workspace, w.ids);
+    if (topk_w) *topk_w = at<float>(workspace, w.w);
+    if (offsets) *offsets = at<int32_t>(workspace, w.offsets);
+    return MOE_OK;
+}
+
+moe_status moe_read_device_status(const moe_layer_plan* plan, int T, void* workspace, int32_t* code,
+                                  moe_stream_t stream) {
+    if (!plan || !workspace || !code) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    void* hdr = at<void>(workspace, layer_ws(plan->d, T).hdr);
+    return moe_permute_read_device_status(0, 1, 1, hdr, code, stream);
+}
+
+}  // extern "C"

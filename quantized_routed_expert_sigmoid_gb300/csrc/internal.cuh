@@ -1,0 +1,96 @@
+// internal.cuh -- declarations shared by the kernel translation units of the
+// GB300 MoE library.  Nothing here is part of the public C ABI
+// (include/moe_gb300.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_gb300.h"
+
+namespace moe {
+
+// GGUF block geometry.
+constexpr int kQ4KBytes = 144;     // fp16 d, fp16 dmin, 12 B scales/mins, 128 B quants
+constexpr int kQ4KWeights = 256;
+constexpr int kQ80Bytes = 34;      // fp16 d, 32 x int8
+constexpr int kQ80Weights = 32;
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kPermuteChunk = 1024;  // pairs per permute CTA
+
+// Workspace header: a status word (MOE_OK or an error code raised on the
+// device) and the arrival ticket of the permute's last-block scan.
+struct WsHeader {
+    int32_t status;
+    uint32_t ticket;
+};
+constexpr size_t kHeaderBytes = 256;
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- route
+cudaError_t launch_router_logits(const void* x, bool x_bf16, int T, int H, const float* W, int E,
+                                 float* logits, WsHeader* clear_hdr, cudaStream_t s);
+cudaError_t launch_topk(const moe_route_cfg& cfg, const float* logits, const float* bias, int T,
+                        int32_t* ids, float* w, WsHeader* clear_hdr, cudaStream_t s);
+
+// ---------------------------------------------------------------- permute
+size_t permute_scratch_bytes(int T, int k, int E);
+cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* sorted_pairs,
+                           int32_t* offsets, int32_t* pair_pos, WsHeader* hdr, int32_t* chunk_base,
+                           cudaStream_t s);
+
+// ---------------------------------------------------------------- decode GEMV experts
+// One launch computes, for every active expert e and each of its pairs, either
+//   GATEUP: h[i, r] = silu(Wg[e][r] . v_i) * (Wu[e][r] . v_i)      (rows r < I)
+//   DOWN  : y[i, n] = Wd[e][n] . v_i                               (rows n < H)
+// with v_i = x[sorted_pairs[i] / k] (GATEUP) or h[i] (DOWN).
+struct GemvArgs {
+    int qtype;                  // MOE_Q8_0 / MOE_Q4_K
+    bool gateup;
+    const uint8_t* w0;          // gate (GATEUP) or down (DOWN)
+    const uint8_t* w1;          // up (GATEUP) or NULL
+    int64_t expert_stride;      // bytes between experts
+    int rows;                   // output rows per expert
+    int K;                      // input length (row length in weights)
+    const void* vin;            // x [T][K] (bf16/fp32) or h [P][K] fp32
+    bool vin_bf16;
+    const int32_t* sorted_pairs;// NULL = identity (one expert, every row in order)
+    const int32_t* offsets;     // [E+1] or NULL
+    int E, k;
+    int n_pairs;                // P (or T for the identity case)
+    float* out;                 // h [P][rows] or y [P][rows], fp32
+};
+cudaError_t launch_qgemv(const GemvArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------- combine, norm
+cudaError_t launch_combine(const float* y_pairs, const float* w, const int32_t* pair_pos, int T, int k,
+                           int H, const float* shared_out, bool accumulate, float* out, cudaStream_t s);
+cudaError_t launch_rmsnorm_bf16(const float* x, const float* gamma, int T, int H, float eps, void* u,
+                                cudaStream_t s);
+
+// ---------------------------------------------------------------- tensor-core grouped GEMM
+struct GgemmArgs {
+    const uint8_t* wg;          // gate [E][I][H/256 blocks] Q4_K
+    const uint8_t* wu;          // up
+    const uint8_t* wd;          // down [E][H][I/256 blocks]
+    int64_t stride_gu, stride_d;
+    int E, k, H, I, T;
+    const void* x;              // [T][H] bf16 or fp32
+    bool x_bf16;
+    const int32_t* sorted_pairs;
+    const int32_t* offsets;
+    __half* x16;                // workspace: [T][H] fp16 copy of x
+    __half* h16;                // workspace: [P][I] fp16
+    float* y_pairs;             // [P][H] fp32
+    int32_t* tiles;             // workspace: tile list
+    WsHeader* hdr;
+};
+size_t ggemm_tile_list_bytes(int T, int k, int E, int I, int H);
+cudaError_t launch_ggemm(const GgemmArgs& a, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,92 @@
+"""Device-resident MoE layer: torch tensors in, one moe_layer call out.
+
+A convenience wrapper over the C ABI for callers that hold their weights in
+torch tensors.  It fills a moe_layer_desc from the tensors, creates the plan
+once, keeps a workspace buffer (torch memory) sized for the largest T seen,
+and calls moe_layer.  All arithmetic runs in the CUDA library.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _native as N
+
+_QT = {"q8_0": N.MOE_Q8_0, "q4_k": N.MOE_Q4_K}
+
+
+def row_bytes(qtype: int, cols: int) -> int:
+    return cols // 32 * 34 if qtype == N.MOE_Q8_0 else cols // 256 * 144
+
+
+class MoeLayer:
+    """gate/up: uint8 [E, I, rb(H)], down: uint8 [E, H, rb(I)] on the GPU."""
+
+    def __init__(self, *, mode: str, E: int, k: int, H: int, I: int, qtype: str, gate, up, down, W_router,
+                 bias=None, n_groups: int = 1, topk_groups: int = 1, scale: float = 1.0,
+                 renormalize: bool = True, x_dtype: str = "bf16", I_s: int = 0, shared_qtype: str = "q8_0",
+                 s_gate=None, s_up=None, s_down=None, accumulate: bool = False, tc_min_tokens: int = 0):
+        self.E, self.k, self.H, self.I = E, k, H, I
+        self.x_dtype = x_dtype
+        qt = _QT[qtype]
+        self._keep = [gate, up, down, W_router, bias, s_gate, s_up, s_down]
+        d = N.moe_layer_desc()
+        d.route = N.route_cfg(N.MOE_ROUTE_SIGMOID_GROUP if mode == "sigmoid_group" else N.MOE_ROUTE_SOFTMAX,
+                              E, k, n_groups, topk_groups, scale, renormalize)
+        d.hidden, d.intermediate = H, I
+        d.x_type = N.MOE_BF16 if x_dtype == "bf16" else N.MOE_F32
+        d.W_router = W_router.data_ptr()
+        d.bias = bias.data_ptr() if bias is not None else None
+        d.gate = N.qmat(qt, gate, I, H, I * row_bytes(qt, H))
+        d.up = N.qmat(qt, up, I, H, I * row_bytes(qt, H))
+        d.down = N.qmat(qt, down, H, I, H * row_bytes(qt, I))
+        d.shared_intermediate = I_s
+        if I_s > 0:
+            sq = _QT[shared_qtype]
+            d.s_gate = N.qmat(sq, s_gate, I_s, H, 0)
+            d.s_up = N.qmat(sq, s_up, I_s, H, 0)
+            d.s_down = N.qmat(sq, s_down, H, I_s, 0)
+        d.accumulate = int(accumulate)
+        d.tc_min_tokens = tc_min_tokens
+        self.desc = d
+        self.plan = N.moe_layer_plan_create(d)
+        self.ws = None
+        self.ws_T = -1
+
+    def workspace_bytes(self, T: int) -> int:
+        return N.moe_layer_workspace_size(self.plan, T)
+
+    def ensure_workspace(self, T: int, device=None):
+        if self.ws is None or T > self.ws_T:
+            nbytes = self.workspace_bytes(T)
+            self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+            self.ws_T = T
+        return self.ws
+
+    def __call__(self, x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty((T, self.H), dtype=torch.float32, device=x.device)
+        ws = self.ensure_workspace(T, x.device)
+        N.moe_layer(self.plan, x, T, out, ws, ws.numel(), stream)
+        return out
+
+    def debug_views(self, T: int):
+        """(ids [T,k] int32, gates [T,k] fp32, offsets [E+1] int32) of the last call, copied to the host."""
+        pi, pw, po = N.moe_layer_debug_views(self.plan, T, self.ws)
+        base = self.ws.data_ptr()
+        def view(ptr, n, dtype):
+            off = ptr - base
+            return self.ws[off:off + n * 4].view(dtype).clone().cpu()
+        return (view(pi, T * self.k, torch.int32).view(T, self.k), view(pw, T * self.k, torch.float32).view(T, self.k),
+                view(po, self.E + 1, torch.int32))
+
+    def device_status(self, T: int) -> int:
+        return N.moe_read_device_status(self.plan, T, self.ws)
+
+    def __del__(self):
+        try:
+            if getattr(self, "plan", None):
+                N.moe_layer_plan_destroy(self.plan)
+                self.plan = None
+        except Exception:
+            pass

@@ -1,0 +1,104 @@
+"""GPU parity of the fused layer (moe_layer through the C ABI) against the fp64 oracle.
+
+Routing ids and per-expert offsets must match bit for bit; the layer output
+must be within rel-L2 1e-4 of the oracle on the fp32 GEMV path.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import TOL_GEMV, make_layer, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_layer(tl, T, tol=TOL_GEMV, n_threads=8, tc_min_tokens=0):
+    layer = tl.moe_layer(tc_min_tokens=tc_min_tokens)
+    x = tl.x.cuda()
+    out = layer(x)
+    torch.cuda.synchronize()
+    ids, gw, offs = layer.debug_views(T)
+    spec = tl.spec()
+    ref = oracle.moe_layer(spec, tl.x.double().numpy(), n_threads=n_threads)
+    assert np.array_equal(ids.numpy(), ref["ids"]), "routing ids differ"
+    _, ref_off, _ = oracle.permute(ref["ids"], tl.shape.E)
+    assert np.array_equal(offs.numpy(), ref_off), "expert offsets differ"
+    assert np.allclose(gw.numpy(), ref["w"], rtol=1e-5, atol=1e-6), "gates differ"
+    err = rel_l2(out.cpu().numpy(), ref["out"])
+    assert err <= tol, f"rel-L2 {err:.3e} > {tol}"
+    assert layer.device_status(T) == 0
+    return layer, out, err
+
+
+@pytest.mark.parametrize("T", [1, 4, 9])
+def test_tiny_q8_0(T):
+    tl = make_layer(synth.TINY, 0, T, exact_all=True)
+    _check_layer(tl, T)
+
+
+@pytest.mark.parametrize("T", [1, 2])
+def test_decode_q4_k(T):
+    tl = make_layer(synth.DECODE, 2, T)
+    _check_layer(tl, T)
+
+
+def test_decode_q4_k_ragged_batch():
+    # 37 tokens: several tokens per expert, passes of 8 pairs plus a ragged tail
+    tl = make_layer(synth.DECODE, 21, 37)
+    _check_layer(tl, 37, tc_min_tokens=1 << 30)
+
+
+def test_deepseek_shape_decode_T2():
+    tl = make_layer(synth.DEEPSEEK, 4, 2)
+    _check_layer(tl, 2)
+
+
+def test_sigmoid_group_small_with_shared():
+    shape = synth.LayerShape(H=512, E=32, k=4, I=256, qtype=synth.Q4_K, mode="sigmoid_group", n_groups=4,
+                             topk_groups=2, scale=2.5, I_s=256, shared_qtype=synth.Q8_0, bias_std=0.1)
+    tl = make_layer(shape, 40, 11, exact_all=True)
+    _check_layer(tl, 11)
+
+
+def test_k_equals_E_every_expert_hit():
+    shape = synth.LayerShape(H=256, E=4, k=4, I=256, qtype=synth.Q4_K)
+    tl = make_layer(shape, 41, 5, exact_all=True)
+    _check_layer(tl, 5)
+
+
+def test_deterministic_and_graph_replay_bitwise():
+    tl = make_layer(synth.DECODE, 2, 2)
+    layer = tl.moe_layer()
+    x = tl.x.cuda()
+    out1 = layer(x).clone()
+    out2 = layer(x).clone()
+    assert torch.equal(out1, out2), "two eager runs differ"
+    out_g = torch.zeros_like(out1)
+    layer.ensure_workspace(2)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer(x, out=out_g)           # warm up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer(x, out=out_g)
+    out_g.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out_g, out1), "graph replay differs from eager"
+
+
+def test_accumulate_is_residual_add():
+    tl = make_layer(synth.TINY, 0, 4, exact_all=True)
+    plain = tl.moe_layer()(tl.x.cuda()).clone()
+    acc_layer = tl.moe_layer(accumulate=True)
+    base = torch.randn(4, synth.TINY.H, device="cuda")
+    out = base.clone()
+    acc_layer(tl.x.cuda(), out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, plain + base)
