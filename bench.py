@@ -1,0 +1,435 @@
+#!/usr/bin/env python3
+"""MoE-layer throughput on one GB300 (and N independent replicas under torchrun).
+
+Headline workload ("decode"): the decode MoE layer -- hidden 2048, 128 routed
+experts, top-8 softmax gates renormalised, expert intermediate 768, SwiGLU,
+Q4_K gate/up/down, fp32 router, bf16 activations -- at T = 1 token.  One step
+is one pass of the whole hot path (router GEMV + top-k, permute, gate/up +
+SwiGLU, down, combine) over L = 16 such layers with distinct weights, replayed
+as one captured CUDA graph.  The L layers touch ~360 MB of distinct weights per
+step, well above the 129 MB L2, so no layer's bytes are still cached when it
+runs again.  value = layer-token applications per second = T * L * steps / time.
+
+Other workloads (--workload): decode2 (T = 2), prefill (T = 4096, Zipf(1)
+popularity), deepseek (hidden 7168, 256 experts, sigmoid + bias group routing,
+shared Q8_0 expert, T = 2).
+
+--impl reference times the fp64 CPU oracle (the baseline the library is
+checked against) on the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+WORKLOADS = {
+    # name: (shape, T, layers in the chain, seed, description)
+    "decode": (synth.DECODE, 1, 16, 2,
+               "decode MoE layer T=1: H=2048 E=128 top-8 softmax I=768 Q4_K, bf16 x, 16 distinct layers per step"),
+    "decode2": (synth.DECODE, 2, 16, 2,
+                "decode MoE layer T=2: H=2048 E=128 top-8 softmax I=768 Q4_K, bf16 x, 16 distinct layers per step"),
+    "prefill": (synth.DECODE, 4096, 2, 3,
+                "prefill MoE layer T=4096: H=2048 E=128 top-8 softmax I=768 Q4_K, Zipf(1) popularity, 2 layers per step"),
+    "deepseek": (synth.DEEPSEEK, 2, 4, 4,
+                 "MoE layer T=2: H=7168 E=256 sigmoid+bias 8 groups/4 kept top-8 scale 2.5 I=2048 Q4_K, shared I=2048 Q8_0"),
+}
+
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        self.dev = device_index
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={CLOCK_QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[4:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for _, _, flags in rows:
+            for n, v in zip(names[1:], flags[1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ workload construction
+
+def build_layers(shape, T, L, seed, device):
+    from quantized_routed_expert_sigmoid_gb300 import MoeLayer
+    layers, xs = [], None
+    for l in range(L):
+        gate = synth.expert_stack(shape, seed, l, "gate", device)
+        up = synth.expert_stack(shape, seed, l, "up", device)
+        down = synth.expert_stack(shape, seed, l, "down", device)
+        Wr = synth.router_weight(shape, seed, l, device=device)
+        b = synth.bias(shape, seed, l, device=device)
+        sh = None
+        if shape.I_s > 0:
+            sh = [synth.expert_matrix(shape, seed, l, n, 0, device) for n in ("s_gate", "s_up", "s_down")]
+        layers.append(MoeLayer(mode=shape.mode, E=shape.E, k=shape.k, H=shape.H, I=shape.I, qtype=shape.qtype,
+                               gate=gate, up=up, down=down, W_router=Wr, bias=b, n_groups=shape.n_groups,
+                               topk_groups=shape.topk_groups, scale=shape.scale, renormalize=shape.renormalize,
+                               x_dtype=shape.x_dtype, I_s=shape.I_s, shared_qtype=shape.shared_qtype,
+                               s_gate=sh[0] if sh else None, s_up=sh[1] if sh else None,
+                               s_down=sh[2] if sh else None))
+    return layers
+
+
+def make_x(shape, T, seed, device, workload):
+    if workload == "prefill":
+        Wr = synth.router_weight(shape, seed, 0).numpy()
+        L = synth.zipf_target_logits(T, shape.E, shape.k, seed)
+        return synth.activations_for_logits(L, Wr, seed).to(device)
+    return synth.activations(T, shape.H, seed, shape.x_dtype, device="cpu").to(device)
+
+
+def algorithmic_bytes(shape, T, offsets_host):
+    """Distinct chosen experts' blocks + router weight + x in + out (one layer)."""
+    u = int(np.count_nonzero(np.diff(offsets_host)))
+    xb = T * shape.H * (2 if shape.x_dtype == "bf16" else 4)
+    b = u * synth.bytes_per_expert(shape) + shape.E * shape.H * 4 + xb + T * shape.H * 4
+    b += synth.shared_bytes(shape)
+    gu = u * 2 * shape.I * synth.row_bytes(shape.qtype, shape.H) + xb + T * shape.k * shape.I * 4
+    return b, gu, u
+
+
+def launches_per_layer(shape, T):
+    P = T * shape.k
+    n = 2 + (1 if P <= 1024 else 2) + 2 + 1          # logits, top-k, permute, gate/up, down, combine
+    if shape.I_s > 0:
+        n += 2
+    return n
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world):
+    import quantized_routed_expert_sigmoid_gb300 as moe
+    device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(device)
+    shape, T, L, seed, desc = WORKLOADS[args.workload]
+    layers = build_layers(shape, T, L, seed + 1000 * rank, device)
+    x = make_x(shape, T, seed + 1000 * rank, device, args.workload)
+    outs = [torch.empty(T, shape.H, dtype=torch.float32, device=device) for _ in range(L)]
+    for lay in layers:
+        lay.ensure_workspace(T, device)
+
+    def chain(stream=None):
+        for lay, o in zip(layers, outs):
+            lay(x, out=o, stream=stream)
+
+    chain()
+    torch.cuda.synchronize()
+    # one captured graph per step
+    s = torch.cuda.Stream(device=device)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        chain()
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        chain(stream=s)
+    torch.cuda.synchronize()
+
+    # per-layer routing facts (for algorithmic bytes)
+    per_layer = []
+    for lay in layers:
+        _, _, offs = lay.debug_views(T)
+        per_layer.append(algorithmic_bytes(shape, T, offs.numpy()))
+    layer_bytes = float(np.mean([p[0] for p in per_layer]))
+    gu_bytes = float(np.mean([p[1] for p in per_layer]))
+    u_mean = float(np.mean([p[2] for p in per_layer]))
+
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(device.index) as clk:
+        torch.cuda.synchronize()
+        ev0.record(s)
+        for _ in range(args.steps):
+            graph.replay()
+        ev1.record(s)
+        torch.cuda.synchronize()
+    t_ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        tt = torch.tensor([t_ms], device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_ms = float(tt.item())
+    ms_per_step = t_ms / args.steps
+    value = world * T * L * args.steps / (t_ms / 1e3)
+
+    # ---- the dominant kernel alone: L gate/up launches (one per layer) in one graph
+    gu_ms = None
+    try:
+        gu_ms = time_gateup(moe, layers, x, shape, T, device, args)
+    except Exception as exc:  # keep the headline even if this sub-measurement fails
+        print(f"gate/up timing skipped: {exc}", file=sys.stderr)
+
+    # ---- end to end through the public call, host buffers, copies inside the timed region
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty(L, T, shape.H, dtype=torch.float32).pin_memory()
+    x_dev = torch.empty_like(x)
+    out_stack = torch.empty(L, T, shape.H, dtype=torch.float32, device=device)
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        for i, lay in enumerate(layers):
+            lay(x_dev, out=out_stack[i])
+        out_host.copy_(out_stack, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(2):
+        e2e_step()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e = {"value": T * L / e2e_s * world, "unit": "tokens/s", "h2d_bytes_per_step": x.numel() * x.element_size(),
+           "d2h_bytes_per_step": out_stack.numel() * 4, "calls": "moe_layer x %d per step" % L}
+
+    hbm_peak, _, peak_kind = measured_peaks()
+    roof = None
+    if gu_ms is not None:
+        achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
+        roof = {"kernel": "qgemv_kernel (gate/up + SwiGLU)", "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                "peak_source": peak_kind, "bytes_per_launch": round(gu_bytes), "us_per_launch": round(gu_ms * 1e3, 3)}
+    layer_us = ms_per_step * 1e3 / L
+    result = {
+        "metric": "MoE-layer tokens/s (decode T=1,2 / prefill T=4096); % of HBM roofline",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": desc, "T": T, "layers_per_step": L, "H": shape.H, "E": shape.E, "k": shape.k,
+                   "I": shape.I, "qtype": shape.qtype, "l2": "inputs larger than L2 (distinct weights per layer)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "layer": {"us_per_layer": round(layer_us, 3), "algorithmic_bytes": round(layer_bytes),
+                  "GBps": round(layer_bytes / (layer_us * 1e-6) / 1e9, 1),
+                  "frac_hbm": round(layer_bytes / (layer_us * 1e-6) / 1e9 / hbm_peak, 4),
+                  "distinct_experts_mean": u_mean},
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": launches_per_layer(shape, T) * L * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.workload, layers[0], x, shape, T, budget_s=args.cpu_seconds)
+    return result
+
+
+def time_gateup(moe, layers, x, shape, T, device, args):
+    """Average duration of the gate/up kernel: one graph of L launches, replayed."""
+    k, E, H, I = shape.k, shape.E, shape.H, shape.I
+    P = T * k
+    routed = []
+    for lay in layers:
+        ids = torch.empty(T, k, dtype=torch.int32, device=device)
+        w = torch.empty(T, k, device=device)
+        lg = torch.empty(T, E, device=device)
+        moe.moe_route(lay.desc.route, x, lay.desc.x_type, T, H, lay.desc.W_router, lay.desc.bias, None, lg, ids, w)
+        sp = torch.empty(P, dtype=torch.int32, device=device)
+        pp = torch.empty(P, dtype=torch.int32, device=device)
+        off = torch.empty(E + 1, dtype=torch.int32, device=device)
+        nb = moe.moe_permute_workspace_size(T, k, E)
+        ws = torch.empty(nb, dtype=torch.uint8, device=device)
+        moe.moe_permute(ids, T, k, E, sp, off, pp, ws, nb)
+        h = torch.empty(P, I, device=device)
+        routed.append((lay, sp, off, h))
+    torch.cuda.synchronize()
+
+    def run(stream=None):
+        for lay, sp, off, h in routed:
+            moe.moe_expert_gateup(lay.desc.gate, lay.desc.up, E, x, lay.desc.x_type, T, H, I, sp, off, k, h,
+                                  stream)
+
+    s = torch.cuda.Stream(device=device)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        run(stream=s)
+    for _ in range(max(3, args.warmup)):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(10, args.steps)
+    e0.record(s)
+    for _ in range(reps):
+        g.replay()
+    e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (reps * len(routed))
+
+
+# ------------------------------------------------------------------ oracle (CPU baseline / reference arm)
+
+def oracle_layer_spec(shape, layer_tensors):
+    import oracle
+    gate, up, down, Wr, bias = layer_tensors
+    return oracle.LayerSpec(mode=oracle.ROUTE_SIGMOID_GROUP if shape.mode == "sigmoid_group" else oracle.ROUTE_SOFTMAX,
+                            E=shape.E, k=shape.k, H=shape.H, I=shape.I,
+                            qtype=oracle.Q4_K if shape.qtype == synth.Q4_K else oracle.Q8_0,
+                            gate=gate, up=up, down=down, Wr=Wr, bias=bias, n_groups=shape.n_groups,
+                            topk_groups=shape.topk_groups, renormalize=shape.renormalize, scale=shape.scale)
+
+
+def oracle_threads(workload):
+    return 1 if workload in ("decode", "decode2") else (os.cpu_count() or 1)
+
+
+def cpu_baseline(workload, layer, x, shape, T, budget_s=10.0):
+    """The oracle, as it stands, on a bounded sample of the same workload (host cores)."""
+    import oracle
+    gate, up, down = layer._keep[0], layer._keep[1], layer._keep[2]
+    Wr, b = layer._keep[3], layer._keep[4]
+    spec = oracle_layer_spec(shape, (gate.cpu().numpy(), up.cpu().numpy(), down.cpu().numpy(), Wr.cpu().numpy(),
+                                     None if b is None else b.cpu().numpy()))
+    if shape.I_s > 0:
+        sg, su, sd = layer._keep[5], layer._keep[6], layer._keep[7]
+        spec.shared_qtype, spec.I_s = oracle.Q8_0, shape.I_s
+        spec.s_gate, spec.s_up, spec.s_down = sg.cpu().numpy(), su.cpu().numpy(), sd.cpu().numpy()
+    xs = x.float().cpu().double().numpy()
+    n_sample = T if T <= 8 else 8                 # tokens per oracle call
+    threads = oracle_threads(workload)
+    times = []
+    t_start = time.perf_counter()
+    while time.perf_counter() - t_start < budget_s and len(times) < 200:
+        t0 = time.perf_counter()
+        oracle.moe_layer(spec, xs[:n_sample], n_threads=threads)
+        times.append(time.perf_counter() - t0)
+    per_call = statistics.median(times)
+    return {"value": round(n_sample / per_call, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(times)} oracle calls of {n_sample} token(s) of one layer of the same workload, "
+                      f"median {per_call * 1e3:.1f} ms per call"}
+
+
+def run_reference(args):
+    """The fp64 oracle timed on the host cores on this workload (no GPU)."""
+    import oracle
+    shape, T, L, seed, desc = WORKLOADS[args.workload]
+    tensors = (synth.expert_stack(shape, seed, 0, "gate").numpy(), synth.expert_stack(shape, seed, 0, "up").numpy(),
+               synth.expert_stack(shape, seed, 0, "down").numpy(), synth.router_weight(shape, seed, 0).numpy(),
+               None if shape.bias_std <= 0 else synth.bias(shape, seed, 0).numpy())
+    spec = oracle_layer_spec(shape, tensors)
+    if shape.I_s > 0:
+        spec.shared_qtype, spec.I_s = oracle.Q8_0, shape.I_s
+        spec.s_gate, spec.s_up, spec.s_down = [synth.expert_matrix(shape, seed, 0, n, 0).numpy()
+                                               for n in ("s_gate", "s_up", "s_down")]
+    x = make_x(shape, T, seed, "cpu", args.workload).float().double().numpy()
+    n_sample = T if T <= 8 else 8
+    threads = oracle_threads(args.workload)
+    for _ in range(args.warmup):
+        oracle.moe_layer(spec, x[:n_sample], n_threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.moe_layer(spec, x[:n_sample], n_threads=threads)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = n_sample / dt
+    return {"impl": "reference", "metric": "MoE-layer tokens/s (decode T=1,2 / prefill T=4096); % of HBM roofline",
+            "value": round(value, 3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "config": {"workload": desc, "T": T},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": f"each step: one oracle call on {n_sample} token(s) of one layer"},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    try:
+        result = run_ours(args, rank, world)
+        if rank == 0:
+            print(json.dumps(result), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -136,6 +136,20 @@ moe_status moe_expert_ffn(const moe_qmat* gate, const moe_qmat* up, const moe_qm
                           float* y_pairs, void* workspace, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * The two halves of moe_expert_ffn, for callers that keep h or time them:
+ * moe_expert_gateup writes h (device, fp32 [T*k][I], row i = sorted
+ * position i) = silu(Wg[e] x_t) * (Wu[e] x_t); moe_expert_down writes
+ * y_pairs[i] = Wd[e] h[i].  Same arguments and rules as moe_expert_ffn;
+ * each is exactly one kernel launch.
+ */
+moe_status moe_expert_gateup(const moe_qmat* gate, const moe_qmat* up, int E, const void* x, moe_dtype x_type,
+                             int T, int H, int I, const int32_t* sorted_pairs, const int32_t* offsets, int k,
+                             float* h, moe_stream_t stream);
+moe_status moe_expert_down(const moe_qmat* down, int E, const float* h, int T, int H, int I,
+                           const int32_t* sorted_pairs, const int32_t* offsets, int k, float* y_pairs,
+                           moe_stream_t stream);
+
+/*
  * moe_combine -- out[t,n] = sum_{j<k} topk_w[t,j] * y_pairs[pair_pos[t*k+j], n]
  *                           (+ shared_out[t,n]) (+ old out[t,n] if accumulate),
  * summed in ascending j, then the shared term, then the old value: the same

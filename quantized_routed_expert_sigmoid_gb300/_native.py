@@ -81,6 +81,8 @@ def _declare(lib):
         "moe_permute": [P, I, I, I, P, P, P, P, S, P],
         "moe_expert_ffn_workspace_size": [I, I, I, I, I, PS],
         "moe_expert_ffn": [ctypes.POINTER(moe_qmat)] * 3 + [I, P, I, I, I, I, P, P, I, P, P, S, P],
+        "moe_expert_gateup": [ctypes.POINTER(moe_qmat)] * 2 + [I, P, I, I, I, I, P, P, I, P, P],
+        "moe_expert_down": [ctypes.POINTER(moe_qmat), I, P, I, I, I, P, P, I, P, P],
         "moe_combine": [P, P, P, I, I, I, P, I, P, P],
         "moe_rmsnorm_bf16": [P, P, I, I, F, P, P],
         "moe_layer_plan_create": [ctypes.POINTER(moe_layer_desc), ctypes.POINTER(P)],
@@ -164,6 +166,16 @@ def moe_expert_ffn(gate, up, down, E, x, x_type, T, H, I, sorted_pairs, offsets,
     _check(load().moe_expert_ffn(ctypes.byref(gate), ctypes.byref(up), ctypes.byref(down), E, _p(x), x_type,
                                  T, H, I, _p(sorted_pairs), _p(offsets), k, _p(y_pairs), _p(workspace),
                                  ws_bytes, _stream(stream)))
+
+
+def moe_expert_gateup(gate, up, E, x, x_type, T, H, I, sorted_pairs, offsets, k, h, stream=None):
+    _check(load().moe_expert_gateup(ctypes.byref(gate), ctypes.byref(up), E, _p(x), x_type, T, H, I,
+                                    _p(sorted_pairs), _p(offsets), k, _p(h), _stream(stream)))
+
+
+def moe_expert_down(down, E, h, T, H, I, sorted_pairs, offsets, k, y_pairs, stream=None):
+    _check(load().moe_expert_down(ctypes.byref(down), E, _p(h), T, H, I, _p(sorted_pairs), _p(offsets), k,
+                                  _p(y_pairs), _stream(stream)))
 
 
 def moe_combine(y_pairs, topk_w, pair_pos, T, k, H, shared_out, accumulate, out, stream=None):

@@ -123,39 +123,44 @@ T* at(void* base, size_t off) {
     return reinterpret_cast<T*>(reinterpret_cast<char*>(base) + off);
 }
 
-moe_status run_ffn(const moe_qmat& gate, const moe_qmat& up, const moe_qmat& down, int E, const void* x,
-                   bool x_bf16, int T, int H, int I, const int32_t* sorted, const int32_t* offsets, int k,
-                   float* h, float* y, cudaStream_t s) {
+GemvArgs gemv_args(const moe_qmat& m0, const moe_qmat* m1, int E, const void* vin, bool vin_bf16, int rows,
+                   int K, const int32_t* sorted, const int32_t* offsets, int k, int n_pairs, float* out) {
     GemvArgs g{};
-    g.qtype = gate.qtype;
-    g.gateup = true;
-    g.w0 = static_cast<const uint8_t*>(gate.data);
-    g.w1 = static_cast<const uint8_t*>(up.data);
-    g.expert_stride = gate.expert_stride_bytes;
-    g.rows = I;
-    g.K = H;
-    g.vin = x;
-    g.vin_bf16 = x_bf16;
+    g.qtype = m0.qtype;
+    g.gateup = m1 != nullptr;
+    g.w0 = static_cast<const uint8_t*>(m0.data);
+    g.w1 = m1 ? static_cast<const uint8_t*>(m1->data) : nullptr;
+    g.expert_stride = m0.expert_stride_bytes;
+    g.rows = rows;
+    g.K = K;
+    g.vin = vin;
+    g.vin_bf16 = vin_bf16;
     g.sorted_pairs = sorted;
     g.offsets = offsets;
     g.E = E;
     g.k = k;
-    g.n_pairs = T * k;
-    g.out = h;
-    cudaError_t err = launch_qgemv(g, s);
+    g.n_pairs = n_pairs;
+    g.out = out;
+    return g;
+}
+
+moe_status check_ffn_common(int E, int k, int T, int H, int I, const int32_t* sorted_pairs, const int32_t* offsets) {
+    if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T = %d < 0", T);
+    if (E < 1 || E > kMaxExperts || k < 1 || k > kMaxTopK) return fail(MOE_ERR_INVALID_ARG, "bad E/k");
+    if (H < 32 || I < 32) return fail(MOE_ERR_INVALID_ARG, "H/I too small");
+    if ((sorted_pairs == nullptr) != (offsets == nullptr))
+        return fail(MOE_ERR_INVALID_ARG, "sorted_pairs and offsets must both be set or both be NULL");
+    if (!sorted_pairs && (E != 1 || k != 1))
+        return fail(MOE_ERR_INVALID_ARG, "the identity mapping needs E = 1 and k = 1");
+    return MOE_OK;
+}
+
+moe_status run_ffn(const moe_qmat& gate, const moe_qmat& up, const moe_qmat& down, int E, const void* x,
+                   bool x_bf16, int T, int H, int I, const int32_t* sorted, const int32_t* offsets, int k,
+                   float* h, float* y, cudaStream_t s) {
+    cudaError_t err = launch_qgemv(gemv_args(gate, &up, E, x, x_bf16, I, H, sorted, offsets, k, T * k, h), s);
     if (err != cudaSuccess) return cuda_fail(err, "gate/up kernel");
-    GemvArgs dn = g;
-    dn.qtype = down.qtype;
-    dn.gateup = false;
-    dn.w0 = static_cast<const uint8_t*>(down.data);
-    dn.w1 = nullptr;
-    dn.expert_stride = down.expert_stride_bytes;
-    dn.rows = H;
-    dn.K = I;
-    dn.vin = h;
-    dn.vin_bf16 = false;
-    dn.out = y;
-    err = launch_qgemv(dn, s);
+    err = launch_qgemv(gemv_args(down, nullptr, E, h, false, H, I, sorted, offsets, k, T * k, y), s);
     if (err != cudaSuccess) return cuda_fail(err, "down kernel");
     return MOE_OK;
 }
@@ -275,6 +280,38 @@ moe_status moe_expert_ffn(const moe_qmat* gate, const moe_qmat* up, const moe_qm
     if (!aligned(workspace, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace not 256-byte aligned");
     return run_ffn(*gate, *up, *down, E, x, x_type == MOE_BF16, T, H, I, sorted_pairs, offsets, k,
                    at<float>(workspace, w.h), y_pairs, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_expert_gateup(const moe_qmat* gate, const moe_qmat* up, int E, const void* x, moe_dtype x_type,
+                             int T, int H, int I, const int32_t* sorted_pairs, const int32_t* offsets, int k,
+                             float* h, moe_stream_t stream) {
+    moe_status st = check_ffn_common(E, k, T, H, I, sorted_pairs, offsets);
+    if (st) return st;
+    if ((st = check_qmat(gate, "gate", I, H, E)) || (st = check_qmat(up, "up", I, H, E))) return st;
+    if (gate->qtype != up->qtype || gate->expert_stride_bytes != up->expert_stride_bytes)
+        return fail(MOE_ERR_INVALID_ARG, "gate and up must share qtype and expert stride");
+    if (x_type != MOE_F32 && x_type != MOE_BF16) return fail(MOE_ERR_UNSUPPORTED, "x_type %d", (int)x_type);
+    if (T == 0) return MOE_OK;
+    if (!x || !h || !aligned(x, 16) || !aligned(h, 16)) return fail(MOE_ERR_INVALID_ARG, "x / h NULL or misaligned");
+    cudaError_t err = launch_qgemv(gemv_args(*gate, up, E, x, x_type == MOE_BF16, I, H, sorted_pairs, offsets, k,
+                                             T * k, h), reinterpret_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return cuda_fail(err, "gate/up kernel");
+    return MOE_OK;
+}
+
+moe_status moe_expert_down(const moe_qmat* down, int E, const float* h, int T, int H, int I,
+                           const int32_t* sorted_pairs, const int32_t* offsets, int k, float* y_pairs,
+                           moe_stream_t stream) {
+    moe_status st = check_ffn_common(E, k, T, H, I, sorted_pairs, offsets);
+    if (st) return st;
+    if ((st = check_qmat(down, "down", H, I, E))) return st;
+    if (T == 0) return MOE_OK;
+    if (!h || !y_pairs || !aligned(h, 16) || !aligned(y_pairs, 16))
+        return fail(MOE_ERR_INVALID_ARG, "h / y_pairs NULL or misaligned");
+    cudaError_t err = launch_qgemv(gemv_args(*down, nullptr, E, h, false, H, I, sorted_pairs, offsets, k, T * k,
+                                             y_pairs), reinterpret_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return cuda_fail(err, "down kernel");
+    return MOE_OK;
 }
 
 moe_status moe_combine(const float* y_pairs, const float* topk_w, const int32_t* pair_pos, int T, int k, int H,

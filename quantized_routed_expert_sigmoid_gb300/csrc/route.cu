@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(
             float v = (lane < G && !((keep >> lane) & 1u)) ? gs : -INFINITY;
             int id = (lane < G && !((keep >> lane) & 1u)) ? lane : 0x7fffffff;
             warp_argmax(v, id);
-            keep |= 1u << id;
+            if (id < 32) keep |= 1u << id;
         }
         for (int e = lane; e < E; e += 32)
             if (!((keep >> (e / per)) & 1u)) sel[e] = -INFINITY;
@@ -209,9 +209,11 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(
         int id = 0x7fffffff;
         for (int e = lane; e < E; e += 32) {
             const float c = sel[e];
-            if (c > v || (c == v && e < id)) { v = c; id = e; }
+            // any candidate beats none, so a non-finite row still yields an index in range
+            if (c > v || (c == v && e < id) || id == 0x7fffffff) { v = c; id = e; }
         }
         warp_argmax(v, id);
+        if (id >= E) id = 0;
         if (lane == r) { my_id = id; my_val = sv[id]; }
         if (lane == 0) sel[id] = -INFINITY;
         __syncwarp();

@@ -256,6 +256,21 @@ class ExpertBank:
                                 for n in ("s_gate", "s_up", "s_down"))
 
 
+def expert_stack(shape: LayerShape, seed: int, layer: int, which: str, device="cpu",
+                 chunk_rows: int = 1 << 17) -> torch.Tensor:
+    """All E experts of one matrix at once (a different stream from expert_matrix):
+    gate/up -> [E, I, rb(H)], down -> [E, H, rb(I)].  Drawn and encoded in row
+    chunks so the fp32 staging stays small."""
+    rows, K = (shape.I, shape.H) if which in ("gate", "up") else (shape.H, shape.I)
+    total = shape.E * rows
+    out = torch.empty((total, row_bytes(shape.qtype, K)), dtype=torch.uint8, device=device)
+    for i, r0 in enumerate(range(0, total, chunk_rows)):
+        n = min(chunk_rows, total - r0)
+        w = normal((n, K), shape.weight_std, derive_seed(seed, layer, TAGS[which], 1 << 30, i), device)
+        out[r0:r0 + n] = encode(shape.qtype, w)
+    return out.view(shape.E, rows, -1)
+
+
 # --------------------------------------------------------------------------- Zipf routing
 
 def zipf_target_logits(T: int, E: int, k: int, seed: int, alpha: float = 1.0, n_zero: int = 8,
