@@ -171,6 +171,9 @@ def run_ours(args, rank, world):
     device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(device)
     shape, T, L, seed, desc = WORKLOADS[args.workload]
+    if args.layers:
+        L = args.layers
+        desc = desc.replace("16 distinct layers", f"{L} distinct layers")
     layers = build_layers(shape, T, L, seed + 1000 * rank, device)
     x = make_x(shape, T, seed + 1000 * rank, device, args.workload)
     outs = [torch.empty(T, shape.H, dtype=torch.float32, device=device) for _ in range(L)]
@@ -209,12 +212,13 @@ def run_ours(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream(device)          # CUDAGraph.replay() launches on the current stream
     with ClockSampler(device.index) as clk:
         torch.cuda.synchronize()
-        ev0.record(s)
+        ev0.record(cur)
         for _ in range(args.steps):
             graph.replay()
-        ev1.record(s)
+        ev1.record(cur)
         torch.cuda.synchronize()
     t_ms = ev0.elapsed_time(ev1)
     if world > 1:
@@ -322,10 +326,11 @@ def time_gateup(moe, layers, x, shape, T, device, args):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     reps = max(10, args.steps)
-    e0.record(s)
+    cur = torch.cuda.current_stream(device)
+    e0.record(cur)
     for _ in range(reps):
         g.replay()
-    e1.record(s)
+    e1.record(cur)
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / (reps * len(routed))
 
@@ -412,6 +417,7 @@ def main():
     ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="override the layers per step (default per workload)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
