@@ -119,6 +119,28 @@ moe_status moe_permute(const int32_t* topk_ids, int T, int k, int E, int32_t* so
                        moe_stream_t stream);
 
 /*
+ * moe_permute_noalloc -- moe_permute for callers that cannot allocate device
+ * memory: code running where cudaMalloc is unavailable or forbidden (inside
+ * a host callback, under an allocator lock held by an embedding runtime, or
+ * in a process whose device memory is fully owned by another framework), or
+ * code that must not size and pass a workspace.  The bloomery pages have no
+ * counterpart of this call; it is a convenience of this library.
+ * Same inputs and outputs as moe_permute, no workspace: the scratch lives in
+ * a fixed 262,400-byte array inside the library that every GPU which loads
+ * the library keeps until the process exits.  Limit: T*k <= 65536 pairs
+ * (larger sizes return MOE_ERR_INVALID_ARG); E <= 1024 as for moe_permute.
+ * The first call on each device looks up that array's device address (with
+ * the device current); make that first call outside any stream capture.
+ * Every call on a device shares the array and zeroes its header first, so
+ * two calls whose kernels overlap on the GPU (different streams, no ordering)
+ * race: order them on one stream or with events.  Out-of-range ids are
+ * dropped (pair_pos = -1, offsets[E] < T*k); no status word is kept.
+ * Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ */
+moe_status moe_permute_noalloc(const int32_t* topk_ids, int T, int k, int E, int32_t* sorted_pairs,
+                               int32_t* offsets, int32_t* pair_pos, moe_stream_t stream);
+
+/*
  * moe_expert_ffn -- the SwiGLU experts over the grouped pairs.
  *   for sorted position i with pair p = sorted_pairs[i], token t = p / k,
  *   expert e (offsets[e] <= i < offsets[e+1]):

@@ -79,6 +79,7 @@ def _declare(lib):
         "moe_route": [ctypes.POINTER(moe_route_cfg), P, I, I, I, P, P, P, P, P, P, P],
         "moe_permute_workspace_size": [I, I, I, PS],
         "moe_permute": [P, I, I, I, P, P, P, P, S, P],
+        "moe_permute_noalloc": [P, I, I, I, P, P, P, P],
         "moe_expert_ffn_workspace_size": [I, I, I, I, I, PS],
         "moe_expert_ffn": [ctypes.POINTER(moe_qmat)] * 3 + [I, P, I, I, I, I, P, P, I, P, P, S, P],
         "moe_expert_gateup": [ctypes.POINTER(moe_qmat)] * 2 + [I, P, I, I, I, I, P, P, I, P, P],
@@ -153,6 +154,12 @@ def moe_permute_workspace_size(T, k, E) -> int:
 def moe_permute(topk_ids, T, k, E, sorted_pairs, offsets, pair_pos, workspace, ws_bytes, stream=None):
     _check(load().moe_permute(_p(topk_ids), T, k, E, _p(sorted_pairs), _p(offsets), _p(pair_pos),
                               _p(workspace), ws_bytes, _stream(stream)))
+
+
+def moe_permute_noalloc(topk_ids, T, k, E, sorted_pairs, offsets, pair_pos, stream=None):
+    """moe_permute without a workspace (fixed library scratch; T*k <= 65536)."""
+    _check(load().moe_permute_noalloc(_p(topk_ids), T, k, E, _p(sorted_pairs), _p(offsets), _p(pair_pos),
+                                      _stream(stream)))
 
 
 def moe_expert_ffn_workspace_size(T, k, E, H, I) -> int:

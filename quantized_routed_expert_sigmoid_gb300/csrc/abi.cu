@@ -84,6 +84,8 @@ FfnWs ffn_ws(int T, int k, int I) {
 
 }  // namespace
 
+moe_status moe::report(moe_status st, const char* msg) { return fail(st, "%s", msg); }
+
 struct moe_layer_plan {
     moe_layer_desc d;
 };

@@ -32,6 +32,9 @@ constexpr size_t kHeaderBytes = 256;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Records `msg` as this host thread's moe_last_error() text and returns `st`.
+moe_status report(moe_status st, const char* msg);
+
 // ---------------------------------------------------------------- route
 cudaError_t launch_router_logits(const void* x, bool x_bf16, int T, int H, const float* W, int E,
                                  float* logits, WsHeader* clear_hdr, cudaStream_t s);

@@ -10,6 +10,8 @@
 // offsets and per-chunk bases), then a stable scatter inside each chunk
 // (warp match for the rank inside a warp, per-warp counts for the rank
 // across warps).  A single chunk does both steps in one launch.
+#include <mutex>
+
 #include "internal.cuh"
 
 namespace moe {
@@ -177,3 +179,68 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* sor
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// moe_permute_noalloc: the same two-step permute, with its scratch (status
+// word, arrival ticket, per-chunk expert bases) in a fixed device array that
+// the library owns, so the caller passes only inputs and outputs.
+// ---------------------------------------------------------------------------
+namespace moe {
+namespace {
+
+constexpr int kNoallocMaxPairs = 65536;                            // T*k limit
+constexpr int kNoallocChunks = kNoallocMaxPairs / kPermuteChunk;   // 64 chunks
+constexpr size_t kNoallocWords = kHeaderBytes / sizeof(int32_t) + (size_t)kNoallocChunks * kMaxExperts;
+
+// 256 B header + 64 chunks x 1024 experts x 4 B = 262,400 bytes, held by every
+// GPU that loads the library until the process exits.
+static __device__ __align__(256) int32_t g_permute_scratch[kNoallocWords];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// The device address of g_permute_scratch on the current device, looked up
+// once per device (host code cannot use the symbol itself as an address).
+cudaError_t scratch_for_current_device(void** out) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_permute_scratch);
+        if (err != cudaSuccess) return err;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_permute_noalloc(const int32_t* topk_ids, int T, int k, int E, int32_t* sorted_pairs,
+                                          int32_t* offsets, int32_t* pair_pos, moe_stream_t stream) {
+    using namespace moe;
+    if (T < 0 || k < 1 || E < 1 || E > kMaxExperts) return report(MOE_ERR_INVALID_ARG, "bad T/k/E");
+    if ((int64_t)T * k > kNoallocMaxPairs)
+        return report(MOE_ERR_INVALID_ARG,
+                      "moe_permute_noalloc: T*k exceeds its fixed scratch limit of 65536 pairs; "
+                      "use moe_permute with a caller workspace");
+    if (!offsets) return report(MOE_ERR_INVALID_ARG, "offsets is NULL");
+    if (T > 0 && (!topk_ids || !sorted_pairs || !pair_pos)) return report(MOE_ERR_INVALID_ARG, "NULL array");
+    void* scratch = nullptr;
+    cudaError_t err = scratch_for_current_device(&scratch);
+    if (err != cudaSuccess) return report(MOE_ERR_CUDA, "moe_permute_noalloc: scratch lookup failed");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(scratch);
+    // status word and arrival ticket must start at zero on every call
+    err = cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s);
+    if (err != cudaSuccess) return report(MOE_ERR_CUDA, "moe_permute_noalloc: header reset failed");
+    int32_t* chunk_base = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(scratch) + kHeaderBytes);
+    err = launch_permute(topk_ids, T, k, E, sorted_pairs, offsets, pair_pos, hdr, chunk_base, s);
+    if (err != cudaSuccess) return report(MOE_ERR_CUDA, "moe_permute_noalloc: kernel launch failed");
+    return MOE_OK;
+}
