@@ -55,7 +55,8 @@ typedef enum {
     MOE_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement */
     MOE_ERR_WORKSPACE = 3,     /* workspace missing or smaller than the size query */
     MOE_ERR_CUDA = 4,          /* a CUDA launch or runtime call failed */
-    MOE_ERR_DEVICE_CHECK = 5   /* a device-side check failed (see *_read_device_status) */
+    MOE_ERR_DEVICE_CHECK = 5,  /* a device-side check failed (see *_read_device_status) */
+    MOE_ERR_TIMEOUT = 6        /* a bounded device-side wait ran out (see *_read_device_status) */
 } moe_status;
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_Q8_0 = 2, MOE_Q4_K = 3 } moe_dtype;

@@ -16,12 +16,13 @@ import threading
 HERE = os.path.dirname(os.path.abspath(__file__))
 HEADER = os.path.join(os.path.dirname(HERE), "include", "moe_gb300.h")
 
-MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE_CHECK = range(6)
+(MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE_CHECK,
+ MOE_ERR_TIMEOUT) = range(7)
 MOE_F32, MOE_BF16, MOE_Q8_0, MOE_Q4_K = range(4)
 MOE_ROUTE_SOFTMAX, MOE_ROUTE_SIGMOID_GROUP = range(2)
 
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
-                4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_CHECK"}
+                4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_CHECK", 6: "MOE_ERR_TIMEOUT"}
 
 
 class MoeError(RuntimeError):

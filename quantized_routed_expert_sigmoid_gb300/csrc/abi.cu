@@ -94,13 +94,28 @@ namespace {
 
 // Workspace of moe_layer for T tokens (offsets in bytes, all 256-aligned).
 struct LayerWs {
-    size_t hdr, logits, ids, w, sorted, pair_pos, offsets, chunk, h, y, sh_h, sh_y, total;
+    bool tc;                      // tensor-core path for this T
+    size_t hdr, logits, ids, w, sorted, pair_pos, offsets, chunk, h, y, sh_h, sh_y, x16, tiles, total;
 };
+
+bool use_tc(const moe_layer_desc& d, int T) {
+    if (T < d.tc_min_tokens) return false;
+    if (!tc_supported(d.gate.qtype, d.intermediate, d.hidden) || !tc_supported(d.down.qtype, d.hidden, d.intermediate))
+        return false;
+    if (d.gate.qtype != d.down.qtype) return false;
+    if (d.shared_intermediate > 0 &&
+        (!tc_supported(d.s_gate.qtype, d.shared_intermediate, d.hidden) ||
+         !tc_supported(d.s_down.qtype, d.hidden, d.shared_intermediate) || d.s_gate.qtype != d.s_down.qtype))
+        return false;
+    return true;
+}
 
 LayerWs layer_ws(const moe_layer_desc& d, int T) {
     const int E = d.route.n_experts, k = d.route.top_k, H = d.hidden, I = d.intermediate;
     const size_t P = (size_t)T * k;
     LayerWs w;
+    w.tc = use_tc(d, T);
+    const size_t hbytes = w.tc ? 2 : 4;   // h is fp16 on the tensor-core path, fp32 on the GEMV path
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
     w.hdr = take(kHeaderBytes);
@@ -111,11 +126,13 @@ LayerWs layer_ws(const moe_layer_desc& d, int T) {
     w.pair_pos = take(P * 4);
     w.offsets = take((size_t)(E + 1) * 4);
     w.chunk = take(permute_scratch_bytes(T, k, E));
-    w.h = take(P * I * 4);
+    w.h = take(P * I * hbytes);
     w.y = take(P * H * 4);
     const int Is = d.shared_intermediate;
-    w.sh_h = take(Is > 0 ? (size_t)T * Is * 4 : 0);
+    w.sh_h = take(Is > 0 ? (size_t)T * Is * hbytes : 0);
     w.sh_y = take(Is > 0 ? (size_t)T * H * 4 : 0);
+    w.x16 = take(w.tc ? (size_t)T * H * 2 : 0);
+    w.tiles = take(w.tc ? tc_tile_list_bytes(T, k, E) : 0);
     w.total = o;
     return w;
 }
@@ -417,16 +434,53 @@ moe_status moe_layer(const moe_layer_plan* plan, const void* x, int T, float* ou
     err = launch_permute(ids, T, k, E, sorted, offs, ppos, hdr, at<int32_t>(workspace, w.chunk), s);
     if (err != cudaSuccess) return cuda_fail(err, "permute kernel");
     float* y = at<float>(workspace, w.y);
-    moe_status st = run_ffn(d.gate, d.up, d.down, E, x, xb, T, H, I, sorted, offs, k,
-                            at<float>(workspace, w.h), y, s);
-    if (st) return st;
     const float* shared = nullptr;
-    if (d.shared_intermediate > 0) {
-        float* sy = at<float>(workspace, w.sh_y);
-        st = run_ffn(d.s_gate, d.s_up, d.s_down, 1, x, xb, T, H, d.shared_intermediate, nullptr, nullptr, 1,
-                     at<float>(workspace, w.sh_h), sy, s);
+    if (w.tc) {
+        TcFfnArgs a{};
+        a.qtype = d.gate.qtype;
+        a.wg = static_cast<const uint8_t*>(d.gate.data);
+        a.wu = static_cast<const uint8_t*>(d.up.data);
+        a.wd = static_cast<const uint8_t*>(d.down.data);
+        a.stride_gu = d.gate.expert_stride_bytes;
+        a.stride_d = d.down.expert_stride_bytes;
+        a.E = E; a.k = k; a.H = H; a.I = I; a.T = T;
+        a.identity = false;
+        a.x = x; a.x_bf16 = xb; a.convert_x = true;
+        a.sorted_pairs = sorted; a.offsets = offs;
+        a.x16 = at<__half>(workspace, w.x16);
+        a.h16 = at<__half>(workspace, w.h);
+        a.y = y;
+        a.tb_list = at<int4>(workspace, w.tiles);
+        a.hdr = hdr;
+        err = launch_tc_expert_ffn(a, s);
+        if (err != cudaSuccess) return cuda_fail(err, "tensor-core expert kernels");
+        if (d.shared_intermediate > 0) {
+            TcFfnArgs b = a;
+            b.qtype = d.s_gate.qtype;
+            b.wg = static_cast<const uint8_t*>(d.s_gate.data);
+            b.wu = static_cast<const uint8_t*>(d.s_up.data);
+            b.wd = static_cast<const uint8_t*>(d.s_down.data);
+            b.stride_gu = b.stride_d = 0;
+            b.E = 1; b.k = 1; b.I = d.shared_intermediate;
+            b.identity = true; b.convert_x = false;
+            b.sorted_pairs = nullptr; b.offsets = nullptr; b.tb_list = nullptr;
+            b.h16 = at<__half>(workspace, w.sh_h);
+            b.y = at<float>(workspace, w.sh_y);
+            err = launch_tc_expert_ffn(b, s);
+            if (err != cudaSuccess) return cuda_fail(err, "tensor-core shared expert kernels");
+            shared = b.y;
+        }
+    } else {
+        moe_status st = run_ffn(d.gate, d.up, d.down, E, x, xb, T, H, I, sorted, offs, k,
+                                at<float>(workspace, w.h), y, s);
         if (st) return st;
-        shared = sy;
+        if (d.shared_intermediate > 0) {
+            float* sy = at<float>(workspace, w.sh_y);
+            st = run_ffn(d.s_gate, d.s_up, d.s_down, 1, x, xb, T, H, d.shared_intermediate, nullptr, nullptr, 1,
+                         at<float>(workspace, w.sh_h), sy, s);
+            if (st) return st;
+            shared = sy;
+        }
     }
     err = launch_combine(y, gw, ppos, T, k, H, shared, d.accumulate != 0, out, s);
     if (err != cudaSuccess) return cuda_fail(err, "combine kernel");

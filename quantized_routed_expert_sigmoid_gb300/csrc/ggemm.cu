@@ -1,0 +1,591 @@
+// ggemm.cu -- grouped expert GEMM on the 5th-generation tensor cores (tcgen05).
+//
+// At prompt sizes the pages run "each expert over all its tokens at once" on
+// tensor cores ("bloomery V4.1 README", "Batched prompts"; "bloomery README
+// 0.3.1", "Why it is fast": prompts as tensor-core GEMMs).  Here each expert's
+// tokens form a dense GEMM against that expert's GGUF weights:
+//   GATEUP: h[i, r] = silu(Wg[e][r] . x_t) * (Wu[e][r] . x_t)     (fp16 out)
+//   DOWN  : y[i, n] = Wd[e][n] . h[i]                             (fp32 out)
+// Tile = 128 weight rows (MMA M) x up to 128 pairs of one expert (MMA N),
+// K in steps of 64.  Weights are dequantized from Q4_K / Q8_0 to fp16 in
+// shared memory (128-byte swizzled K-major tiles); token rows are gathered
+// with cp.async into the same layout; one thread issues tcgen05.mma with the
+// accumulators in TMEM (fp32); the epilogue reads TMEM with tcgen05.ld.
+// Persistent CTAs (one per SM) walk a device-built list of token blocks, so
+// the launch needs no host knowledge of the per-expert counts.
+//
+// Warp roles (288 threads): warps 0-7 stage operands (dequant + gather) and
+// run the epilogue; warp 8 owns TMEM and issues the MMAs.  Pipeline per
+// k-step g: producers wait until MMA(g-2) has finished (so A stage g%2 and B
+// stage (g+2)%4 are free), prefetch B(g+2) and the raw blocks of g+3 with
+// cp.async, dequantize g into A stage g%2, and arrive on full[g%4]; the MMA
+// warp waits full[g%4], issues 4 k-substeps, and commits to empty[g%4].
+// Every wait is bounded (globaltimer); on timeout the kernel records
+// MOE_ERR_TIMEOUT, drains its MMAs, frees TMEM and returns.
+#include "internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128, kBN = 128, kBK = 64;
+constexpr int kProducerWarps = 8;
+constexpr int kProducers = kProducerWarps * 32;
+constexpr int kThreadsTC = kProducers + 32;
+constexpr int kAStages = 2, kBStages = 4, kRawSlots = 4;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
+
+enum { kGateUp = 0, kDown = 1 };
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t gtime() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(su32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the completion of the phase with the given parity.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_test(b, parity)) return true;
+    const uint64_t t0 = gtime();
+    while (!mbar_test(b, parity)) {
+        if (*abort_flag) return false;
+        if (gtime() - t0 > kWaitLimitNs) { *abort_flag = 1; return false; }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(su32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(su32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;                 // leading-dimension offset (unused with this swizzle)
+    d |= (uint64_t)(1024 >> 4) << 32;       // stride between 8-row groups
+    d |= (uint64_t)1 << 46;                 // descriptor version
+    d |= (uint64_t)2 << 61;                 // 128-byte swizzle
+    return d;
+}
+// Instruction descriptor: D fp32, A and B fp16, both K-major, M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_f16(int n) {
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+}
+__device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(dtmem), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* b) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(b))
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float nib_f(uint32_t word, int b) {   // byte b (0..15 value) -> float, exact
+    return __int_as_float(__byte_perm(word, 0x4B00u, 0x5440u | (uint32_t)b)) - 8388608.0f;
+}
+__device__ __forceinline__ float s8_f(uint32_t word, int b) {    // signed byte b -> float, exact
+    return __int_as_float(__byte_perm(word ^ 0x80808080u, 0x4B00u, 0x5440u | (uint32_t)b)) - 8388736.0f;
+}
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t swz(int row, int ch) { return (uint32_t)(row * 128 + ((ch ^ (row & 7)) << 4)); }
+
+// scale and min of sub-block j (0..7) of a Q4_K block header (words y, z, w = scale bytes 0-11)
+__device__ __forceinline__ void q4k_scale_min(const uint4& hd, int j, float& fsc, float& fm) {
+    const float d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
+    const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
+    const int jj = j & 3;
+    const uint32_t by = (hd.y >> (8 * jj)) & 0xFFu, bz = (hd.z >> (8 * jj)) & 0xFFu, bw = (hd.w >> (8 * jj)) & 0xFFu;
+    uint32_t sc, m;
+    if (j < 4) { sc = by & 63u; m = bz & 63u; }
+    else { sc = (bw & 15u) | ((by >> 6) << 4); m = (bw >> 4) | ((bz >> 6) << 4); }
+    fsc = d * (float)sc;
+    fm = dmin * (float)m;
+}
+
+// Raw bytes staged per producer thread per k-step.
+template <int QT, int MODE>
+struct RawCfg {
+    static constexpr int kBytes = QT == MOE_Q4_K ? (MODE == kGateUp ? 48 : 32) : 80;
+};
+
+struct TileInfo {
+    int e, tok0, ntok, m0, n_inst;
+};
+
+struct TcParams {
+    const uint8_t* w0;           // gate (GATEUP) or down (DOWN) weights
+    const uint8_t* w1;           // up (GATEUP)
+    int64_t expert_stride;
+    int rows;                    // weight rows per expert (I for GATEUP, H for DOWN)
+    int K;                       // H for GATEUP, I for DOWN
+    int k;                       // top-k (token of pair = sorted_pairs[i] / k)
+    const __half* bsrc;          // x16 [T][K] (GATEUP) or h16 [P][K] (DOWN)
+    const int32_t* sorted_pairs; // GATEUP gather map (NULL: identity)
+    const int4* tb_list;         // [0].x = number of token blocks, then (e, tok0, ntok, 0); NULL: identity
+    int n_identity;              // identity mode: tokens
+    __half* h_out;               // GATEUP: [P][rows] fp16
+    float* y_out;                // DOWN: [P][rows] fp32
+    WsHeader* hdr;
+};
+
+// The full tile description for tile index t.
+__device__ __forceinline__ bool tile_at(const TcParams& p, int n_mb, int t, int n_tb, TileInfo& ti) {
+    const int tb = t / n_mb, mb = t - tb * n_mb;
+    if (tb >= n_tb) return false;
+    if (p.tb_list) {
+        const int4 v = p.tb_list[1 + tb];
+        ti.e = v.x; ti.tok0 = v.y; ti.ntok = v.z;
+    } else {
+        ti.e = 0; ti.tok0 = tb * kBN; ti.ntok = min(kBN, p.n_identity - ti.tok0);
+    }
+    ti.m0 = mb * kBM;
+    ti.n_inst = (ti.ntok + 15) & ~15;
+    return true;
+}
+
+template <int QT, int MODE>
+__global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+    constexpr int kAStageBytes = (MODE == kGateUp ? 2 : 1) * kBM * 128;
+    constexpr int kBStageBytes = kBN * 128;
+    constexpr int kRawBytes = RawCfg<QT, MODE>::kBytes;
+    constexpr int kRawSlotBytes = kProducers * kRawBytes;
+    constexpr uint32_t kTmemCols = MODE == kGateUp ? 2 * kBN : kBN;
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* sA = smem;
+    uint8_t* sB = sA + kAStages * kAStageBytes;
+    uint8_t* sRaw = sB + kBStages * kBStageBytes;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sRaw + kRawSlots * kRawSlotBytes);
+    uint64_t* full = bar;            // [4]
+    uint64_t* empty = bar + 4;       // [4]
+    uint64_t* accf = bar + 8;        // [1]
+    uint64_t* drain = bar + 9;       // [1]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 10);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 11);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int i = 0; i < 4; ++i) { mbar_init(&full[i], kProducers); mbar_init(&empty[i], 1); }
+        mbar_init(accf, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kProducerWarps) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                     "n"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_before();
+    __syncthreads();
+    tc_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int n_mb = p.rows / kBM;
+    const int n_tb = p.tb_list ? p.tb_list[0].x : (p.n_identity + kBN - 1) / kBN;
+    const int n_tiles = n_tb * n_mb;
+    const int nk = p.K / kBK;
+    const int nblk_row = QT == MOE_Q4_K ? p.K / kQ4KWeights : p.K / kQ80Weights;
+    const int64_t rb = (int64_t)nblk_row * (QT == MOE_Q4_K ? kQ4KBytes : kQ80Bytes);
+
+    if (warp < kProducerWarps) {
+        // ======================= producers + epilogue =======================
+        const int prow = tid & 127;                 // weight row within the tile
+        const int psel = tid >> 7;                  // GATEUP: matrix (0 gate, 1 up); DOWN: half of the k-step
+        uint32_t g = 0;                             // global k-step counter
+        int tile_iter = 0;
+        for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x, ++tile_iter) {
+            TileInfo ti;
+            if (!tile_at(p, n_mb, t, n_tb, ti)) break;
+            const uint8_t* wrow = (MODE == kGateUp && psel == 1 ? p.w1 : p.w0) + (int64_t)ti.e * p.expert_stride +
+                                  (int64_t)(ti.m0 + prow) * rb;
+            // rows of B this thread copies: r = tid/8 + 32*it, 16-byte chunk tid%8
+            const int bch = tid & 7;
+            int64_t brow[4];
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                const int r = (tid >> 3) + 32 * it;
+                int64_t src = -1;
+                if (r < ti.ntok) {
+                    const int i = ti.tok0 + r;
+                    if (MODE == kGateUp) src = p.sorted_pairs ? (int64_t)(p.sorted_pairs[i] / p.k) : (int64_t)i;
+                    else src = i;
+                }
+                brow[it] = src;
+            }
+            auto issue_b = [&](int kb, int stage) {
+                uint8_t* dst = sB + stage * kBStageBytes;
+#pragma unroll
+                for (int it = 0; it < 4; ++it) {
+                    const int r = (tid >> 3) + 32 * it;
+                    const __half* src = brow[it] >= 0 ? p.bsrc + brow[it] * p.K + kb * kBK + bch * 8 : p.bsrc;
+                    cp_async16(dst + swz(r, bch), src, brow[it] >= 0 ? 16u : 0u);
+                }
+            };
+            auto issue_raw = [&](int kb, int slot) {
+                uint8_t* dst = sRaw + slot * kRawSlotBytes + tid * kRawBytes;
+                if (QT == MOE_Q4_K) {
+                    const uint8_t* blk = wrow + (int64_t)(kb >> 2) * kQ4KBytes;
+                    cp_async16(dst, blk, 16u);                                    // header
+                    if (MODE == kGateUp) {
+                        cp_async16(dst + 16, blk + 16 + 32 * (kb & 3), 16u);
+                        cp_async16(dst + 32, blk + 32 + 32 * (kb & 3), 16u);
+                    } else {
+                        cp_async16(dst + 16, blk + 16 + 32 * (kb & 3) + 16 * psel, 16u);
+                    }
+                } else {
+                    const uint8_t* src = wrow + (int64_t)kb * 2 * kQ80Bytes;       // two blocks, 68 bytes
+#pragma unroll
+                    for (int w = 0; w < 17; ++w) cp_async4(dst + 4 * w, src + 4 * w);
+                }
+            };
+            // prologue: groups {raw0}, {B0, raw1}, {B1, raw2}
+            issue_raw(0, g % kRawSlots);
+            cp_commit();
+            if (nk > 0) issue_b(0, g % kBStages);
+            if (nk > 1) issue_raw(1, (g + 1) % kRawSlots);
+            cp_commit();
+            if (nk > 1) issue_b(1, (g + 1) % kBStages);
+            if (nk > 2) issue_raw(2, (g + 2) % kRawSlots);
+            cp_commit();
+
+            bool ok = true;
+            for (int kb = 0; kb < nk; ++kb, ++g) {
+                if (g >= 2 && !mbar_wait(&empty[(g + 2) & 3], ((g - 2) >> 2) & 1, abort_flag)) { ok = false; break; }
+                if (kb + 2 < nk) issue_b(kb + 2, (g + 2) % kBStages);
+                if (kb + 3 < nk) issue_raw(kb + 3, (g + 3) % kRawSlots);
+                cp_commit();
+                cp_wait<2>();
+                // ---- dequantize k-step kb into A stage g%2
+                const uint8_t* raw = sRaw + (g % kRawSlots) * kRawSlotBytes + tid * kRawBytes;
+                uint8_t* arow = sA + (g % kAStages) * kAStageBytes + (MODE == kGateUp ? psel * kBM * 128 : 0);
+                if (QT == MOE_Q4_K) {
+                    const uint4 hd = *reinterpret_cast<const uint4*>(raw);
+                    const int c = kb & 3;
+                    float fs0, fm0, fs1, fm1;
+                    q4k_scale_min(hd, 2 * c, fs0, fm0);
+                    q4k_scale_min(hd, 2 * c + 1, fs1, fm1);
+                    if (MODE == kGateUp) {
+                        const uint4 q0 = *reinterpret_cast<const uint4*>(raw + 16);
+                        const uint4 q1 = *reinterpret_cast<const uint4*>(raw + 32);
+                        const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch) {
+                            const bool hi = ch >= 4;
+                            const int wi = 2 * (ch & 3);
+                            const float fs = hi ? fs1 : fs0, fm = hi ? fm1 : fm0;
+                            uint32_t o[4];
+#pragma unroll
+                            for (int h2 = 0; h2 < 2; ++h2) {
+                                const uint32_t wv = qw[wi + h2];
+                                const uint32_t nb = hi ? ((wv >> 4) & 0x0F0F0F0Fu) : (wv & 0x0F0F0F0Fu);
+                                o[2 * h2] = pack_h2(fmaf(nib_f(nb, 0), fs, -fm), fmaf(nib_f(nb, 1), fs, -fm));
+                                o[2 * h2 + 1] = pack_h2(fmaf(nib_f(nb, 2), fs, -fm), fmaf(nib_f(nb, 3), fs, -fm));
+                            }
+                            *reinterpret_cast<uint4*>(arow + swz(prow, ch)) = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    } else {
+                        const uint4 q = *reinterpret_cast<const uint4*>(raw + 16);   // bytes 16*psel .. +15
+                        const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                        for (int part = 0; part < 4; ++part) {
+                            // chunk: low nibbles -> k = 16*psel + 8*part' ; high -> 32 + ...
+                            const bool hi = part >= 2;
+                            const int ch = (hi ? 4 : 0) + 2 * psel + (part & 1);
+                            const float fs = hi ? fs1 : fs0, fm = hi ? fm1 : fm0;
+                            uint32_t o[4];
+#pragma unroll
+                            for (int h2 = 0; h2 < 2; ++h2) {
+                                const uint32_t wv = qw[2 * (part & 1) + h2];
+                                const uint32_t nb = hi ? ((wv >> 4) & 0x0F0F0F0Fu) : (wv & 0x0F0F0F0Fu);
+                                o[2 * h2] = pack_h2(fmaf(nib_f(nb, 0), fs, -fm), fmaf(nib_f(nb, 1), fs, -fm));
+                                o[2 * h2 + 1] = pack_h2(fmaf(nib_f(nb, 2), fs, -fm), fmaf(nib_f(nb, 3), fs, -fm));
+                            }
+                            *reinterpret_cast<uint4*>(arow + swz(prow, ch)) = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                } else {
+                    // Q8_0: 68 bytes = d0, q0[32], d1, q1[32]
+                    uint32_t wv[17];
+#pragma unroll
+                    for (int w = 0; w < 17; ++w) wv[w] = reinterpret_cast<const uint32_t*>(raw)[w];
+                    const float d0 = __half2float(__ushort_as_half((unsigned short)(wv[0] & 0xFFFFu)));
+                    const float d1 = __half2float(__ushort_as_half((unsigned short)(wv[8] >> 16)));
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        if (MODE == kDown && (ch >> 2) != psel) continue;     // DOWN: this thread's block only
+                        const int b0 = ch < 4 ? 2 + 8 * ch : 36 + 8 * (ch - 4);
+                        const float d = ch < 4 ? d0 : d1;
+                        float v[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int off = b0 + i;
+                            v[i] = d * s8_f(wv[off >> 2], off & 3);
+                        }
+                        *reinterpret_cast<uint4*>(arow + swz(prow, ch)) =
+                            make_uint4(pack_h2(v[0], v[1]), pack_h2(v[2], v[3]), pack_h2(v[4], v[5]),
+                                       pack_h2(v[6], v[7]));
+                    }
+                }
+                fence_async_smem();
+                mbar_arrive(&full[g & 3]);
+            }
+            cp_wait_all();
+            if (!ok) break;
+            // ---- epilogue: wait for the accumulators of this tile
+            if (!mbar_wait(accf, tile_iter & 1, abort_flag)) break;
+            tc_after();
+            const int q = warp & 3, half = warp >> 2;
+            const int m = q * 32 + lane;
+            for (int c16 = half * 16; c16 < ti.n_inst; c16 += 32) {
+                uint32_t a[16];
+                tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c16, a);
+                if (MODE == kGateUp) {
+                    uint32_t u[16];
+                    tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(kBN + c16), u);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int col = c16 + j;
+                        if (col < ti.ntok) {
+                            const float gv = __uint_as_float(a[j]), uv = __uint_as_float(u[j]);
+                            const float hv = gv / (1.0f + expf(-gv)) * uv;
+                            p.h_out[(int64_t)(ti.tok0 + col) * p.rows + ti.m0 + m] = __float2half_rn(hv);
+                        }
+                    }
+                } else {
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int col = c16 + j;
+                        if (col < ti.ntok) p.y_out[(int64_t)(ti.tok0 + col) * p.rows + ti.m0 + m] = __uint_as_float(a[j]);
+                    }
+                }
+            }
+            tc_before();
+        }
+        cp_wait_all();
+    } else {
+        // ======================= MMA issuer (warp 8) =======================
+        uint32_t g = 0;
+        bool issued = false;
+        for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
+            TileInfo ti;
+            if (!tile_at(p, n_mb, t, n_tb, ti)) break;
+            const uint32_t idesc = idesc_f16(ti.n_inst);
+            bool ok = true;
+            for (int kb = 0; kb < nk; ++kb, ++g) {
+                if (!mbar_wait(&full[g & 3], (g >> 2) & 1, abort_flag)) { ok = false; break; }
+                tc_after();
+                if (lane == 0) {
+                    const uint32_t a0 = su32(sA + (g % kAStages) * kAStageBytes);
+                    const uint32_t b0 = su32(sB + (g % kBStages) * kBStageBytes);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t bd = sdesc(b0 + 32 * kk);
+                        mma_f16(tmem, sdesc(a0 + 32 * kk), bd, idesc, (kb | kk) != 0);
+                        if (MODE == kGateUp)
+                            mma_f16(tmem + kBN, sdesc(a0 + kBM * 128 + 32 * kk), bd, idesc, (kb | kk) != 0);
+                    }
+                    mma_commit(&empty[g & 3]);
+                    if (kb == nk - 1) mma_commit(accf);
+                }
+                issued = true;
+                __syncwarp();
+            }
+            if (!ok) break;
+        }
+        // drain: every MMA this thread issued has completed before TMEM is freed
+        if (issued) {
+            if (lane == 0) mma_commit(drain);
+            __syncwarp();
+            const uint64_t t0 = gtime();
+            while (!mbar_test(drain, 0)) {
+                if (gtime() - t0 > kWaitLimitNs) break;
+            }
+        }
+    }
+    if (*abort_flag && tid == 0) atomicCAS(&p.hdr->status, (int)MOE_OK, (int)MOE_ERR_TIMEOUT);
+    tc_before();
+    __syncthreads();
+    tc_after();
+    if (warp == kProducerWarps) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
+    }
+}
+
+// Token blocks of up to 128 pairs per expert: list[0].x = count, then (e, tok0, ntok, 0).
+__global__ void __launch_bounds__(1024) tile_list_kernel(const int32_t* __restrict__ offsets, int E,
+                                                         int4* __restrict__ list) {
+    __shared__ int warp_tot[32];
+    __shared__ int total;
+    const int e = threadIdx.x;
+    int n = 0, o0 = 0;
+    if (e < E) { o0 = offsets[e]; n = offsets[e + 1] - o0; }
+    const int nb = (n + kBN - 1) / kBN;
+    // block exclusive scan of nb
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = nb;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += v;
+    }
+    if (lane == 31) warp_tot[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        const int w = warp_tot[lane];
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += v;
+        }
+        warp_tot[lane] = wi - w;
+        if (lane == 31) total = wi;
+    }
+    __syncthreads();
+    const int base = inc - nb + warp_tot[warp];
+    for (int b = 0; b < nb; ++b) list[1 + base + b] = make_int4(e, o0 + b * kBN, min(kBN, n - b * kBN), 0);
+    if (threadIdx.x == 0) list[0] = make_int4(total, 0, 0, 0);
+}
+
+__global__ void to_half_kernel(const void* __restrict__ x, bool bf16, int64_t n, __half* __restrict__ out) {
+    const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (i >= n) return;
+    float v[4];
+    if (bf16) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(x) + i);
+        v[0] = __uint_as_float(raw.x << 16); v[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+        v[2] = __uint_as_float(raw.y << 16); v[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+    } else {
+        const float4 f = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(x) + i);
+        v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    }
+    *reinterpret_cast<uint2*>(out + i) = make_uint2(pack_h2(v[0], v[1]), pack_h2(v[2], v[3]));
+}
+
+template <int QT, int MODE>
+size_t tc_smem_bytes() {
+    constexpr int a = kAStages * (MODE == kGateUp ? 2 : 1) * kBM * 128;
+    constexpr int b = kBStages * kBN * 128;
+    constexpr int r = kRawSlots * kProducers * RawCfg<QT, MODE>::kBytes;
+    return (size_t)a + b + r + 128 + 1024;   // barriers + alignment slack
+}
+
+int num_sms() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 1;
+    }
+    return n;
+}
+
+template <int QT, int MODE>
+cudaError_t launch_tc(const TcParams& p, int max_tiles, cudaStream_t s) {
+    const size_t smem = tc_smem_bytes<QT, MODE>();
+    cudaError_t err = cudaFuncSetAttribute(tc_gemm_kernel<QT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)smem);
+    if (err != cudaSuccess) return err;
+    const int grid = max(1, min(num_sms(), max_tiles));
+    tc_gemm_kernel<QT, MODE><<<grid, kThreadsTC, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_tc_q(int qtype, const TcParams& p, int max_tiles, cudaStream_t s) {
+    return qtype == MOE_Q4_K ? launch_tc<MOE_Q4_K, MODE>(p, max_tiles, s) : launch_tc<MOE_Q8_0, MODE>(p, max_tiles, s);
+}
+
+}  // namespace
+
+size_t tc_tile_list_bytes(int T, int k, int E) {
+    const int64_t P = (int64_t)T * k;
+    return align_up((size_t)(1 + P / kBN + E + 1) * sizeof(int4), 256);
+}
+
+bool tc_supported(int qtype, int rows_gu, int K_gu) {
+    return (qtype == MOE_Q4_K || qtype == MOE_Q8_0) && rows_gu % kBM == 0 && K_gu % kBK == 0 &&
+           (qtype != MOE_Q4_K || K_gu % kQ4KWeights == 0);
+}
+
+cudaError_t launch_tc_expert_ffn(const TcFfnArgs& a, cudaStream_t s) {
+    cudaError_t err;
+    const int P = a.identity ? a.T : a.T * a.k;
+    if (P <= 0) return cudaSuccess;
+    // x -> fp16 copy (once per layer; the caller may share it between routed and shared experts)
+    if (a.convert_x) {
+        const int64_t n = (int64_t)a.T * a.H;
+        to_half_kernel<<<(unsigned)((n / 4 + 255) / 256), 256, 0, s>>>(a.x, a.x_bf16, n, a.x16);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    int max_tb;
+    if (!a.identity) {
+        tile_list_kernel<<<1, 1024, 0, s>>>(a.offsets, a.E, a.tb_list);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        max_tb = P / kBN + a.E;
+    } else {
+        max_tb = (P + kBN - 1) / kBN;
+    }
+    TcParams gu{};
+    gu.w0 = a.wg; gu.w1 = a.wu; gu.expert_stride = a.stride_gu; gu.rows = a.I; gu.K = a.H; gu.k = a.k;
+    gu.bsrc = a.x16; gu.sorted_pairs = a.identity ? nullptr : a.sorted_pairs;
+    gu.tb_list = a.identity ? nullptr : a.tb_list; gu.n_identity = a.identity ? a.T : 0;
+    gu.h_out = a.h16; gu.hdr = a.hdr;
+    if ((err = launch_tc_q<kGateUp>(a.qtype, gu, max_tb * (a.I / kBM), s)) != cudaSuccess) return err;
+    TcParams dn{};
+    dn.w0 = a.wd; dn.expert_stride = a.stride_d; dn.rows = a.H; dn.K = a.I; dn.k = a.k;
+    dn.bsrc = a.h16; dn.sorted_pairs = nullptr;
+    dn.tb_list = gu.tb_list; dn.n_identity = gu.n_identity;
+    dn.y_out = a.y; dn.hdr = a.hdr;
+    return launch_tc_q<kDown>(a.qtype, dn, max_tb * (a.H / kBM), s);
+}
+
+}  // namespace moe

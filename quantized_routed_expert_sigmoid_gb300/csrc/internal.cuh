@@ -77,23 +77,30 @@ cudaError_t launch_rmsnorm_bf16(const float* x, const float* gamma, int T, int H
                                 cudaStream_t s);
 
 // ---------------------------------------------------------------- tensor-core grouped GEMM
-struct GgemmArgs {
-    const uint8_t* wg;          // gate [E][I][H/256 blocks] Q4_K
-    const uint8_t* wu;          // up
-    const uint8_t* wd;          // down [E][H][I/256 blocks]
+// Expert FFN for many tokens per expert on tcgen05: gate/up + SwiGLU into an
+// fp16 h, then down into fp32 y (row i = sorted position i, or token i in the
+// identity mode used by a shared expert).
+struct TcFfnArgs {
+    int qtype;                  // MOE_Q4_K or MOE_Q8_0 (gate, up and down share it)
+    const uint8_t* wg;
+    const uint8_t* wu;
+    const uint8_t* wd;
     int64_t stride_gu, stride_d;
     int E, k, H, I, T;
+    bool identity;              // one expert over all T tokens in order
     const void* x;              // [T][H] bf16 or fp32
     bool x_bf16;
+    bool convert_x;             // write x16 from x first
     const int32_t* sorted_pairs;
     const int32_t* offsets;
-    __half* x16;                // workspace: [T][H] fp16 copy of x
-    __half* h16;                // workspace: [P][I] fp16
-    float* y_pairs;             // [P][H] fp32
-    int32_t* tiles;             // workspace: tile list
+    __half* x16;                // [T][H]
+    __half* h16;                // [P][I]
+    float* y;                   // [P][H]
+    int4* tb_list;              // token-block list (routed mode)
     WsHeader* hdr;
 };
-size_t ggemm_tile_list_bytes(int T, int k, int E, int I, int H);
-cudaError_t launch_ggemm(const GgemmArgs& a, cudaStream_t s);
+size_t tc_tile_list_bytes(int T, int k, int E);
+bool tc_supported(int qtype, int rows_gu, int K_gu);
+cudaError_t launch_tc_expert_ffn(const TcFfnArgs& a, cudaStream_t s);
 
 }  // namespace moe

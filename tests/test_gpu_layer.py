@@ -102,3 +102,98 @@ def test_accumulate_is_residual_add():
     acc_layer(tl.x.cuda(), out=out)
     torch.cuda.synchronize()
     assert torch.equal(out, plain + base)
+
+
+# ---------------------------------------------------------------- tensor-core path (T >= tc_min_tokens)
+
+def _check_sampled(tl, T, sample, tol, tc_min_tokens=0, n_threads=8):
+    """Whole-layer run on the GPU; routing ids of every token and the outputs of the
+    sampled tokens against the oracle (tokens are independent, so the oracle runs on
+    the sample alone)."""
+    layer = tl.moe_layer(tc_min_tokens=tc_min_tokens)
+    x = tl.x.cuda()
+    out = layer(x)
+    torch.cuda.synchronize()
+    ids, gw, offs = layer.debug_views(T)
+    from helpers import route_oracle
+    ref_ids, ref_w, _ = route_oracle(tl.shape, tl.x.double().numpy(), tl.Wr.numpy(),
+                                     None if tl.bias is None else tl.bias.numpy())
+    assert np.array_equal(ids.numpy(), ref_ids), "routing ids differ"
+    _, ref_off, _ = oracle.permute(ref_ids, tl.shape.E)
+    assert np.array_equal(offs.numpy(), ref_off), "expert offsets differ"
+    sample = np.asarray(sample)
+    need = sorted(set(ref_ids[sample].reshape(-1).tolist()))
+    assert set(need) <= tl.exact
+    ref = oracle.moe_layer(tl.spec(), tl.x[sample].double().numpy(), n_threads=n_threads)
+    err = rel_l2(out.cpu().numpy()[sample], ref["out"])
+    assert err <= tol, f"rel-L2 {err:.3e} > {tol}"
+    assert layer.device_status(T) == 0
+    return layer, out, err
+
+
+def test_tc_tiny_q8_0():
+    from helpers import TOL_TC
+    for T in (4, 9):
+        tl = make_layer(synth.TINY, 0, T, exact_all=True)
+        _check_sampled(tl, T, np.arange(T), TOL_TC, tc_min_tokens=1)
+
+
+def test_tc_decode_shape_ragged():
+    from helpers import TOL_TC
+    T = 300                                 # 2400 pairs: many token blocks, a ragged tail per expert
+    tl = make_layer(synth.DECODE, 30, T, exact_all=True)
+    _check_sampled(tl, T, np.arange(0, T, 13), TOL_TC)
+
+
+def test_tc_prefill_zipf_T4096():
+    from helpers import TOL_TC, SeededLayer
+    shape, seed, T = synth.DECODE, 3, 4096
+    Wr = synth.router_weight(shape, seed, 0)
+    L = synth.zipf_target_logits(T, shape.E, shape.k, seed)
+    x = synth.activations_for_logits(L, Wr.numpy(), seed)
+    from helpers import route_oracle, MIN_GAP
+    ids, _, gaps = route_oracle(shape, x.double().numpy(), Wr.numpy(), None)
+    assert gaps[:, 0].min() >= MIN_GAP
+    counts = np.bincount(ids.reshape(-1), minlength=shape.E)
+    assert (counts == 0).sum() >= 8 and counts.max() > 1000          # uneven, some experts empty
+    tl = SeededLayer(shape, seed, x, exact=None, Wr=Wr, bias=None)
+    _check_sampled(tl, T, np.arange(0, T, 257), TOL_TC)
+
+
+def test_tc_deepseek_shape_verify_T512():
+    from helpers import TOL_TC
+    T = 512
+    tl = make_layer(synth.DEEPSEEK, 4, T, exact_all=True)
+    _check_sampled(tl, T, np.arange(0, T, 43), TOL_TC)
+
+
+def test_tc_deterministic_and_graph_replay():
+    tl = make_layer(synth.DECODE, 31, 200, exact_all=True)
+    layer = tl.moe_layer()
+    x = tl.x.cuda()
+    o1 = layer(x).clone()
+    o2 = layer(x).clone()
+    assert torch.equal(o1, o2)
+    out_g = torch.zeros_like(o1)
+    layer.ensure_workspace(200)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer(x, out=out_g)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer(x, out=out_g)
+    out_g.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out_g, o1)
+
+
+def test_tc_matches_gemv_path():
+    """Same layer, same tokens: the tensor-core path stays within its tolerance of the GEMV path."""
+    from helpers import TOL_TC
+    tl = make_layer(synth.DECODE, 32, 160, exact_all=True)
+    o_tc = tl.moe_layer()(tl.x.cuda()).cpu().numpy()
+    o_gv = tl.moe_layer(tc_min_tokens=1 << 30)(tl.x.cuda()).cpu().numpy()
+    assert rel_l2(o_tc, o_gv) <= TOL_TC
