@@ -65,13 +65,14 @@ class SeededLayer:
         self.bank = synth.ExpertBank(shape, seed, layer, exact=exact, fill_device=device, out_device=device)
         self.exact = set(range(shape.E)) if exact is None else set(int(e) for e in exact)
 
-    def spec(self) -> oracle.LayerSpec:
+    def spec(self, experts=None) -> oracle.LayerSpec:
+        """Oracle view of the layer; only `experts` (default: all exact ones) carry their bytes."""
         s = self.shape
         rb_h, rb_i = synth.row_bytes(s.qtype, s.H), synth.row_bytes(s.qtype, s.I)
         gate = np.zeros((s.E, s.I, rb_h), np.uint8)
         up = np.zeros((s.E, s.I, rb_h), np.uint8)
         down = np.zeros((s.E, s.H, rb_i), np.uint8)
-        for e in sorted(self.exact):
+        for e in sorted(self.exact if experts is None else experts):
             gate[e] = self.bank.gate[e].cpu().numpy()
             up[e] = self.bank.up[e].cpu().numpy()
             down[e] = self.bank.down[e].cpu().numpy()

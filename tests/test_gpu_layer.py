@@ -124,7 +124,7 @@ def _check_sampled(tl, T, sample, tol, tc_min_tokens=0, n_threads=8):
     sample = np.asarray(sample)
     need = sorted(set(ref_ids[sample].reshape(-1).tolist()))
     assert set(need) <= tl.exact
-    ref = oracle.moe_layer(tl.spec(), tl.x[sample].double().numpy(), n_threads=n_threads)
+    ref = oracle.moe_layer(tl.spec(experts=need), tl.x[sample].double().numpy(), n_threads=n_threads)
     err = rel_l2(out.cpu().numpy()[sample], ref["out"])
     assert err <= tol, f"rel-L2 {err:.3e} > {tol}"
     assert layer.device_status(T) == 0
