@@ -44,6 +44,9 @@ WORKLOADS = {
                 "decode MoE layer T=2: H=2048 E=128 top-8 softmax I=768 Q4_K, bf16 x, 16 distinct layers per step"),
     "prefill": (synth.DECODE, 4096, 2, 3,
                 "prefill MoE layer T=4096: H=2048 E=128 top-8 softmax I=768 Q4_K, Zipf(1) popularity, 2 layers per step"),
+    "deepseek512": (synth.DEEPSEEK, 512, 2, 4,
+                    "MoE layer T=512 (verification batch): H=7168 E=256 sigmoid+bias 8 groups/4 kept top-8 scale 2.5 "
+                    "I=2048 Q4_K, shared I=2048 Q8_0, 2 layers per step"),
     "deepseek": (synth.DEEPSEEK, 2, 4, 4,
                  "MoE layer T=2: H=7168 E=256 sigmoid+bias 8 groups/4 kept top-8 scale 2.5 I=2048 Q4_K, shared I=2048 Q8_0"),
 }
@@ -117,15 +120,20 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ workload construction
 
-def build_layers(shape, T, L, seed, device):
+def build_layers(shape, T, L, seed, device, shared_router=False):
+    """L layers with distinct expert weights.  Router weights and biases are drawn on the
+    CPU (small) so that a workload built around them (the Zipf prefill) sees the same values;
+    shared_router gives every layer layer 0's router."""
     from quantized_routed_expert_sigmoid_gb300 import MoeLayer
-    layers, xs = [], None
+    layers = []
     for l in range(L):
         gate = synth.expert_stack(shape, seed, l, "gate", device)
         up = synth.expert_stack(shape, seed, l, "up", device)
         down = synth.expert_stack(shape, seed, l, "down", device)
-        Wr = synth.router_weight(shape, seed, l, device=device)
-        b = synth.bias(shape, seed, l, device=device)
+        lr = 0 if shared_router else l
+        Wr = synth.router_weight(shape, seed, lr).to(device)
+        b = synth.bias(shape, seed, lr)
+        b = None if b is None else b.to(device)
         sh = None
         if shape.I_s > 0:
             sh = [synth.expert_matrix(shape, seed, l, n, 0, device) for n in ("s_gate", "s_up", "s_down")]
@@ -174,7 +182,7 @@ def run_ours(args, rank, world):
     if args.layers:
         L = args.layers
         desc = desc.replace("16 distinct layers", f"{L} distinct layers")
-    layers = build_layers(shape, T, L, seed + 1000 * rank, device)
+    layers = build_layers(shape, T, L, seed + 1000 * rank, device, shared_router=(args.workload == "prefill"))
     x = make_x(shape, T, seed + 1000 * rank, device, args.workload)
     outs = [torch.empty(T, shape.H, dtype=torch.float32, device=device) for _ in range(L)]
     for lay in layers:
@@ -228,10 +236,14 @@ def run_ours(args, rank, world):
     ms_per_step = t_ms / args.steps
     value = world * T * L * args.steps / (t_ms / 1e3)
 
-    # ---- the dominant kernel alone: L gate/up launches (one per layer) in one graph
+    # ---- the dominant kernel alone (the routed gate/up + SwiGLU launch)
+    tc_path = T >= 128
     gu_ms = None
     try:
-        gu_ms = time_gateup(moe, layers, x, shape, T, device, args)
+        if tc_path:
+            gu_ms = time_gateup_events(moe, layers, x, outs, T, args)
+        else:
+            gu_ms = time_gateup(moe, layers, x, shape, T, device, args)
     except Exception as exc:  # keep the headline even if this sub-measurement fails
         print(f"gate/up timing skipped: {exc}", file=sys.stderr)
 
@@ -258,13 +270,21 @@ def run_ours(args, rank, world):
     e2e = {"value": T * L / e2e_s * world, "unit": "tokens/s", "h2d_bytes_per_step": x.numel() * x.element_size(),
            "d2h_bytes_per_step": out_stack.numel() * 4, "calls": "moe_layer x %d per step" % L}
 
-    hbm_peak, _, peak_kind = measured_peaks()
+    hbm_peak, tc_peak, peak_kind = measured_peaks()
     roof = None
-    if gu_ms is not None:
+    if gu_ms is not None and not tc_path:
         achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
         roof = {"kernel": "qgemv_kernel (gate/up + SwiGLU)", "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
                 "peak_source": peak_kind, "bytes_per_launch": round(gu_bytes), "us_per_launch": round(gu_ms * 1e3, 3)}
+    elif gu_ms is not None:
+        flops = 2.0 * T * shape.k * 2 * shape.H * shape.I
+        achieved = flops / (gu_ms * 1e-3) / 1e12
+        roof = {"kernel": "tc_gemm_kernel (tcgen05 gate/up + SwiGLU, fp16 operands, fp32 accumulate)",
+                "bound": "tensor", "achieved": round(achieved, 1), "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": round(achieved / tc_peak, 4), "traffic": None,
+                "peak_source": peak_kind + " (bf16 burst; fp16 runs at the bf16 rate)",
+                "flops_per_launch": flops, "us_per_launch": round(gu_ms * 1e3, 3)}
     layer_us = ms_per_step * 1e3 / L
     result = {
         "metric": "MoE-layer tokens/s (decode T=1,2 / prefill T=4096); % of HBM roofline",
@@ -286,6 +306,25 @@ def run_ours(args, rank, world):
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args.workload, layers[0], x, shape, T, budget_s=args.cpu_seconds)
     return result
+
+
+def time_gateup_events(moe, layers, x, outs, T, args):
+    """Average duration of the routed gate/up launch measured with CUDA events recorded
+    around it by moe_layer_timed (eager calls queued behind a short sleep so the host
+    is never the bottleneck)."""
+    import quantized_routed_expert_sigmoid_gb300._native as N
+    durations = []
+    rounds = max(3, min(args.steps, 10))
+    for _ in range(rounds):
+        evs = []
+        torch.cuda._sleep(20_000_000)
+        for lay, o in zip(layers, outs):
+            eb, ea = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            N.moe_layer_timed(lay.plan, x, T, o, lay.ws, lay.ws.numel(), None, eb, ea)
+            evs.append((eb, ea))
+        torch.cuda.synchronize()
+        durations += [eb.elapsed_time(ea) for eb, ea in evs]
+    return statistics.median(durations)
 
 
 def time_gateup(moe, layers, x, shape, T, device, args):

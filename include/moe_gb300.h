@@ -224,6 +224,13 @@ moe_status moe_layer_workspace_size(const moe_layer_plan* plan, int T, size_t* b
  */
 moe_status moe_layer(const moe_layer_plan* plan, const void* x, int T, float* out, void* workspace,
                      size_t ws_bytes, moe_stream_t stream);
+/* moe_layer that also records two caller-owned CUDA events (cudaEvent_t, may
+ * be NULL) on `stream` immediately before and after the launch of the routed
+ * gate/up kernel, so a caller can time that kernel alone.  Same results as
+ * moe_layer; meant for eager calls (not for graph capture). */
+moe_status moe_layer_timed(const moe_layer_plan* plan, const void* x, int T, float* out, void* workspace,
+                           size_t ws_bytes, moe_stream_t stream, void* ev_before_gateup, void* ev_after_gateup);
+
 /* Device pointers into a moe_layer workspace (any output may be NULL) to
  * the last call's ids int32 [T][k], gates fp32 [T][k] and offsets int32
  * [E+1]. */

@@ -91,6 +91,7 @@ def _declare(lib):
         "moe_layer_plan_destroy": [P],
         "moe_layer_workspace_size": [P, I, PS],
         "moe_layer": [P, P, I, P, P, S, P],
+        "moe_layer_timed": [P, P, I, P, P, S, P, P, P],
         "moe_layer_debug_views": [P, I, P, ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P)],
         "moe_read_device_status": [P, I, P, ctypes.POINTER(ctypes.c_int32), P],
         "moe_permute_read_device_status": [I, I, I, P, ctypes.POINTER(ctypes.c_int32), P],
@@ -213,6 +214,13 @@ def moe_layer_workspace_size(plan: int, T: int) -> int:
 
 def moe_layer(plan, x, T, out, workspace, ws_bytes, stream=None):
     _check(load().moe_layer(plan, _p(x), T, _p(out), _p(workspace), ws_bytes, _stream(stream)))
+
+
+def moe_layer_timed(plan, x, T, out, workspace, ws_bytes, stream=None, ev_before=None, ev_after=None):
+    """moe_layer recording torch.cuda.Event objects around the routed gate/up kernel."""
+    eb = ev_before.cuda_event if ev_before is not None else None
+    ea = ev_after.cuda_event if ev_after is not None else None
+    _check(load().moe_layer_timed(plan, _p(x), T, _p(out), _p(workspace), ws_bytes, _stream(stream), eb, ea))
 
 
 def moe_layer_debug_views(plan, T, workspace):

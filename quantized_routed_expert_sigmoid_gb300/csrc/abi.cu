@@ -406,6 +406,13 @@ moe_status moe_layer_workspace_size(const moe_layer_plan* plan, int T, size_t* b
 
 moe_status moe_layer(const moe_layer_plan* plan, const void* x, int T, float* out, void* workspace,
                      size_t ws_bytes, moe_stream_t stream) {
+    return moe_layer_timed(plan, x, T, out, workspace, ws_bytes, stream, nullptr, nullptr);
+}
+
+moe_status moe_layer_timed(const moe_layer_plan* plan, const void* x, int T, float* out, void* workspace,
+                           size_t ws_bytes, moe_stream_t stream, void* ev_before_gateup, void* ev_after_gateup) {
+    cudaEvent_t evb = static_cast<cudaEvent_t>(ev_before_gateup);
+    cudaEvent_t eva = static_cast<cudaEvent_t>(ev_after_gateup);
     if (!plan) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
     if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T = %d < 0", T);
     if (T == 0) return MOE_OK;
@@ -452,6 +459,8 @@ moe_status moe_layer(const moe_layer_plan* plan, const void* x, int T, float* ou
         a.y = y;
         a.tb_list = at<int4>(workspace, w.tiles);
         a.hdr = hdr;
+        a.ev_before_gateup = evb;
+        a.ev_after_gateup = eva;
         err = launch_tc_expert_ffn(a, s);
         if (err != cudaSuccess) return cuda_fail(err, "tensor-core expert kernels");
         if (d.shared_intermediate > 0) {
@@ -464,6 +473,7 @@ moe_status moe_layer(const moe_layer_plan* plan, const void* x, int T, float* ou
             b.E = 1; b.k = 1; b.I = d.shared_intermediate;
             b.identity = true; b.convert_x = false;
             b.sorted_pairs = nullptr; b.offsets = nullptr; b.tb_list = nullptr;
+            b.ev_before_gateup = b.ev_after_gateup = nullptr;
             b.h16 = at<__half>(workspace, w.sh_h);
             b.y = at<float>(workspace, w.sh_y);
             err = launch_tc_expert_ffn(b, s);
@@ -471,9 +481,14 @@ moe_status moe_layer(const moe_layer_plan* plan, const void* x, int T, float* ou
             shared = b.y;
         }
     } else {
-        moe_status st = run_ffn(d.gate, d.up, d.down, E, x, xb, T, H, I, sorted, offs, k,
-                                at<float>(workspace, w.h), y, s);
-        if (st) return st;
+        if (evb && (err = cudaEventRecord(evb, s)) != cudaSuccess) return cuda_fail(err, "event record");
+        err = launch_qgemv(gemv_args(d.gate, &d.up, E, x, xb, I, H, sorted, offs, k, T * k, at<float>(workspace, w.h)), s);
+        if (err != cudaSuccess) return cuda_fail(err, "gate/up kernel");
+        if (eva && (err = cudaEventRecord(eva, s)) != cudaSuccess) return cuda_fail(err, "event record");
+        err = launch_qgemv(gemv_args(d.down, nullptr, E, at<float>(workspace, w.h), false, H, I, sorted, offs, k,
+                                     T * k, y), s);
+        if (err != cudaSuccess) return cuda_fail(err, "down kernel");
+        moe_status st;
         if (d.shared_intermediate > 0) {
             float* sy = at<float>(workspace, w.sh_y);
             st = run_ffn(d.s_gate, d.s_up, d.s_down, 1, x, xb, T, H, d.shared_intermediate, nullptr, nullptr, 1,

@@ -579,7 +579,9 @@ cudaError_t launch_tc_expert_ffn(const TcFfnArgs& a, cudaStream_t s) {
     gu.bsrc = a.x16; gu.sorted_pairs = a.identity ? nullptr : a.sorted_pairs;
     gu.tb_list = a.identity ? nullptr : a.tb_list; gu.n_identity = a.identity ? a.T : 0;
     gu.h_out = a.h16; gu.hdr = a.hdr;
+    if (a.ev_before_gateup && (err = cudaEventRecord(a.ev_before_gateup, s)) != cudaSuccess) return err;
     if ((err = launch_tc_q<kGateUp>(a.qtype, gu, max_tb * (a.I / kBM), s)) != cudaSuccess) return err;
+    if (a.ev_after_gateup && (err = cudaEventRecord(a.ev_after_gateup, s)) != cudaSuccess) return err;
     TcParams dn{};
     dn.w0 = a.wd; dn.expert_stride = a.stride_d; dn.rows = a.H; dn.K = a.I; dn.k = a.k;
     dn.bsrc = a.h16; dn.sorted_pairs = nullptr;

@@ -98,6 +98,7 @@ struct TcFfnArgs {
     float* y;                   // [P][H]
     int4* tb_list;              // token-block list (routed mode)
     WsHeader* hdr;
+    cudaEvent_t ev_before_gateup, ev_after_gateup;   // optional timing events
 };
 size_t tc_tile_list_bytes(int T, int k, int E);
 bool tc_supported(int qtype, int rows_gu, int K_gu);
