@@ -47,6 +47,9 @@ WORKLOADS = {
     "deepseek512": (synth.DEEPSEEK, 512, 2, 4,
                     "MoE layer T=512 (verification batch): H=7168 E=256 sigmoid+bias 8 groups/4 kept top-8 scale 2.5 "
                     "I=2048 Q4_K, shared I=2048 Q8_0, 2 layers per step"),
+    "stack": (synth.DECODE, 1, 48, 5,
+              "48-layer stack captured as one CUDA graph: per layer RMSNorm (eps 1e-6) -> decode MoE layer "
+              "(H=2048 E=128 top-8 I=768 Q4_K) -> residual add, fp32 residual, bf16 layer input"),
     "deepseek": (synth.DEEPSEEK, 2, 4, 4,
                  "MoE layer T=2: H=7168 E=256 sigmoid+bias 8 groups/4 kept top-8 scale 2.5 I=2048 Q4_K, shared I=2048 Q8_0"),
 }
@@ -164,12 +167,14 @@ def algorithmic_bytes(shape, T, offsets_host):
     return b, gu, u
 
 
-def launches_per_layer(shape, T):
+def launches_per_layer(shape, T, stack=False):
     P = T * shape.k
     n = 2 + (1 if P <= 1024 else 2) + 2 + 1          # logits, top-k, permute, gate/up, down, combine
+    if T >= 128:
+        n += 2                                       # fp16 copy of x, token-block list
     if shape.I_s > 0:
         n += 2
-    return n
+    return n + (1 if stack else 0)                   # RMSNorm in the stack
 
 
 # ------------------------------------------------------------------ our arm
@@ -179,6 +184,10 @@ def run_ours(args, rank, world):
     device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(device)
     shape, T, L, seed, desc = WORKLOADS[args.workload]
+    if args.tokens:
+        T = args.tokens
+        desc = desc.replace("T=1:", f"T={T}:").replace("T=2:", f"T={T}:")
+    stack = args.workload == "stack"
     if args.layers:
         L = args.layers
         desc = desc.replace("16 distinct layers", f"{L} distinct layers")
@@ -187,8 +196,22 @@ def run_ours(args, rank, world):
     outs = [torch.empty(T, shape.H, dtype=torch.float32, device=device) for _ in range(L)]
     for lay in layers:
         lay.ensure_workspace(T, device)
+    if stack:
+        import quantized_routed_expert_sigmoid_gb300 as moe_mod
+        for lay in layers:              # the stack adds each layer into the residual stream
+            lay.desc.accumulate = 1
+            moe_mod.moe_layer_plan_destroy(lay.plan)
+            lay.plan = moe_mod.moe_layer_plan_create(lay.desc)
+        gammas = [synth.gamma(shape.H, seed, l).to(device) for l in range(L)]
+        resid = x.float().clone()
+        u = torch.empty(T, shape.H, dtype=torch.bfloat16, device=device)
 
     def chain(stream=None):
+        if stack:
+            for lay, gm in zip(layers, gammas):
+                moe.moe_rmsnorm_bf16(resid, gm, T, shape.H, 1e-6, u, stream)
+                lay(u, out=resid, stream=stream)
+            return
         for lay, o in zip(layers, outs):
             lay(x, out=o, stream=stream)
 
@@ -239,6 +262,8 @@ def run_ours(args, rank, world):
     # ---- the dominant kernel alone (the routed gate/up + SwiGLU launch)
     tc_path = T >= 128
     gu_ms = None
+    if stack:
+        x = u                           # the kernels' input in the stack: the bf16 normalised stream
     try:
         if tc_path:
             gu_ms = time_gateup_events(moe, layers, x, outs, T, args)
@@ -256,8 +281,15 @@ def run_ours(args, rank, world):
 
     def e2e_step():
         x_dev.copy_(x_host, non_blocking=True)
-        for i, lay in enumerate(layers):
-            lay(x_dev, out=out_stack[i])
+        if stack:
+            resid.copy_(x_dev)
+            for lay, gm in zip(layers, gammas):
+                moe.moe_rmsnorm_bf16(resid, gm, T, shape.H, 1e-6, u)
+                lay(u, out=resid)
+            out_stack[0].copy_(resid)
+        else:
+            for i, lay in enumerate(layers):
+                lay(x_dev, out=out_stack[i])
         out_host.copy_(out_stack, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
@@ -286,6 +318,9 @@ def run_ours(args, rank, world):
                 "peak_source": peak_kind + " (bf16 burst; fp16 runs at the bf16 rate)",
                 "flops_per_launch": flops, "us_per_launch": round(gu_ms * 1e3, 3)}
     layer_us = ms_per_step * 1e3 / L
+    extra = {}
+    if stack:
+        extra["stack_tokens_per_s"] = round(world * T * args.steps / (t_ms / 1e3), 1)
     result = {
         "metric": "MoE-layer tokens/s (decode T=1,2 / prefill T=4096); % of HBM roofline",
         "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -300,9 +335,10 @@ def run_ours(args, rank, world):
                   "distinct_experts_mean": u_mean},
         "roofline": roof,
         "e2e": e2e,
-        "gpu_launches": launches_per_layer(shape, T) * L * args.steps,
+        "gpu_launches": launches_per_layer(shape, T, stack) * L * args.steps,
         "clocks": clk.summary(),
     }
+    result.update(extra)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args.workload, layers[0], x, shape, T, budget_s=args.cpu_seconds)
     return result
@@ -320,6 +356,8 @@ def time_gateup_events(moe, layers, x, outs, T, args):
         torch.cuda._sleep(20_000_000)
         for lay, o in zip(layers, outs):
             eb, ea = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            eb.record()                  # torch creates the CUDA event on first record;
+            ea.record()                  # the library records both again around the kernel
             N.moe_layer_timed(lay.plan, x, T, o, lay.ws, lay.ws.numel(), None, eb, ea)
             evs.append((eb, ea))
         torch.cuda.synchronize()
@@ -457,6 +495,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="override the layers per step (default per workload)")
+    ap.add_argument("--tokens", type=int, default=0, help="override T (tokens per layer call)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
