@@ -169,6 +169,8 @@ def algorithmic_bytes(shape, T, offsets_host):
 
 def launches_per_layer(shape, T, stack=False):
     P = T * shape.k
+    if T <= 4 and P <= 64 and shape.E <= 256:
+        return 1 + (1 if stack else 0)                # the single-launch layer (+ RMSNorm)
     n = 2 + (1 if P <= 1024 else 2) + 2 + 1          # logits, top-k, permute, gate/up, down, combine
     if T >= 128:
         n += 2                                       # fp16 copy of x, token-block list
@@ -200,8 +202,7 @@ def run_ours(args, rank, world):
         import quantized_routed_expert_sigmoid_gb300 as moe_mod
         for lay in layers:              # the stack adds each layer into the residual stream
             lay.desc.accumulate = 1
-            moe_mod.moe_layer_plan_destroy(lay.plan)
-            lay.plan = moe_mod.moe_layer_plan_create(lay.desc)
+            lay.rebuild_plan()
         gammas = [synth.gamma(shape.H, seed, l).to(device) for l in range(L)]
         resid = x.float().clone()
         u = torch.empty(T, shape.H, dtype=torch.bfloat16, device=device)
@@ -261,11 +262,14 @@ def run_ours(args, rank, world):
 
     # ---- the dominant kernel alone (the routed gate/up + SwiGLU launch)
     tc_path = T >= 128
+    fused_path = T <= 4 and T * shape.k <= 64 and shape.E <= 256
     gu_ms = None
     if stack:
         x = u                           # the kernels' input in the stack: the bf16 normalised stream
     try:
-        if tc_path:
+        if fused_path:
+            gu_ms = None                # the layer is one kernel: its graph-timed duration is the layer's
+        elif tc_path:
             gu_ms = time_gateup_events(moe, layers, x, outs, T, args)
         else:
             gu_ms = time_gateup(moe, layers, x, shape, T, device, args)
@@ -304,7 +308,15 @@ def run_ours(args, rank, world):
 
     hbm_peak, tc_peak, peak_kind = measured_peaks()
     roof = None
-    if gu_ms is not None and not tc_path:
+    layer_us_ = ms_per_step * 1e3 / L
+    if fused_path:
+        achieved = layer_bytes / (layer_us_ * 1e-6) / 1e9
+        roof = {"kernel": "decode_layer_kernel (whole layer, one cooperative launch)", "bound": "hbm",
+                "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4), "traffic": None, "peak_source": peak_kind,
+                "bytes_per_launch": round(layer_bytes), "us_per_launch": round(layer_us_, 3),
+                "timing": "CUDA events around replays of one graph of L launches; per launch = total / (steps * L)"}
+    elif gu_ms is not None and not tc_path:
         achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
         roof = {"kernel": "qgemv_kernel (gate/up + SwiGLU)", "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,

@@ -47,7 +47,8 @@ class moe_layer_desc(ctypes.Structure):
                 ("x_type", ctypes.c_int), ("W_router", ctypes.c_void_p), ("bias", ctypes.c_void_p),
                 ("gate", moe_qmat), ("up", moe_qmat), ("down", moe_qmat),
                 ("shared_intermediate", ctypes.c_int), ("s_gate", moe_qmat), ("s_up", moe_qmat),
-                ("s_down", moe_qmat), ("accumulate", ctypes.c_int), ("tc_min_tokens", ctypes.c_int)]
+                ("s_down", moe_qmat), ("accumulate", ctypes.c_int), ("tc_min_tokens", ctypes.c_int),
+                ("decode_fused_off", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -90,6 +91,7 @@ def _declare(lib):
         "moe_layer_plan_create": [ctypes.POINTER(moe_layer_desc), ctypes.POINTER(P)],
         "moe_layer_plan_destroy": [P],
         "moe_layer_workspace_size": [P, I, PS],
+        "moe_layer_workspace_init": [P, I, P, P],
         "moe_layer": [P, P, I, P, P, S, P],
         "moe_layer_timed": [P, P, I, P, P, S, P, P, P],
         "moe_layer_debug_views": [P, I, P, ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P)],
@@ -210,6 +212,10 @@ def moe_layer_workspace_size(plan: int, T: int) -> int:
     n = ctypes.c_size_t(0)
     _check(load().moe_layer_workspace_size(plan, T, ctypes.byref(n)))
     return n.value
+
+
+def moe_layer_workspace_init(plan, T, workspace, stream=None):
+    _check(load().moe_layer_workspace_init(plan, T, _p(workspace), _stream(stream)))
 
 
 def moe_layer(plan, x, T, out, workspace, ws_bytes, stream=None):

@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <new>
+#include <vector>
 
 #include "internal.cuh"
 
@@ -88,6 +89,7 @@ moe_status moe::report(moe_status st, const char* msg) { return fail(st, "%s", m
 
 struct moe_layer_plan {
     moe_layer_desc d;
+    std::vector<void*> ready_ws;   // workspaces prepared by moe_layer_workspace_init
 };
 
 namespace {
@@ -434,7 +436,49 @@ moe_status moe_layer_timed(const moe_layer_plan* plan, const void* x, int T, flo
     int32_t* sorted = at<int32_t>(workspace, w.sorted);
     int32_t* ppos = at<int32_t>(workspace, w.pair_pos);
     int32_t* offs = at<int32_t>(workspace, w.offsets);
-    cudaError_t err = launch_router_logits(x, xb, T, H, d.W_router, E, logits, hdr, s);
+    cudaError_t err;
+    if (!w.tc) {
+        DecodeArgs da{};
+        da.route = d.route;
+        da.Wr = d.W_router;
+        da.bias = d.bias;
+        da.x = x;
+        da.x_bf16 = xb;
+        da.T = T; da.H = H; da.I = I;
+        da.qtype = d.gate.qtype;
+        da.wg = static_cast<const uint8_t*>(d.gate.data);
+        da.wu = static_cast<const uint8_t*>(d.up.data);
+        da.wd = static_cast<const uint8_t*>(d.down.data);
+        da.stride_gu = d.gate.expert_stride_bytes;
+        da.stride_d = d.down.expert_stride_bytes;
+        da.I_s = d.shared_intermediate;
+        if (da.I_s > 0) {
+            da.s_qtype = d.s_gate.qtype;
+            da.sg = static_cast<const uint8_t*>(d.s_gate.data);
+            da.su = static_cast<const uint8_t*>(d.s_up.data);
+            da.sd = static_cast<const uint8_t*>(d.s_down.data);
+        }
+        da.logits = logits; da.ids = ids; da.gw = gw; da.sorted = sorted; da.offsets = offs; da.pair_pos = ppos;
+        da.h = at<float>(workspace, w.h);
+        da.h_s = at<float>(workspace, w.sh_h);
+        da.out = out;
+        da.accumulate = d.accumulate != 0;
+        da.hdr = hdr;
+        const bool same_q = d.gate.qtype == d.up.qtype && d.gate.qtype == d.down.qtype &&
+                            (da.I_s == 0 || (d.s_gate.qtype == d.s_up.qtype && d.s_gate.qtype == d.s_down.qtype));
+        if (!plan->d.decode_fused_off && same_q && decode_fused_supported(da)) {
+            bool ready = false;
+            for (void* p : plan->ready_ws) ready = ready || p == workspace;
+            if (!ready)
+                return fail(MOE_ERR_WORKSPACE, "workspace not prepared: call moe_layer_workspace_init once on it");
+            if (evb && (err = cudaEventRecord(evb, s)) != cudaSuccess) return cuda_fail(err, "event record");
+            err = launch_decode_fused(da, s);
+            if (err != cudaSuccess) return cuda_fail(err, "fused decode kernel");
+            if (eva && (err = cudaEventRecord(eva, s)) != cudaSuccess) return cuda_fail(err, "event record");
+            return MOE_OK;
+        }
+    }
+    err = launch_router_logits(x, xb, T, H, d.W_router, E, logits, hdr, s);
     if (err != cudaSuccess) return cuda_fail(err, "router logits kernel");
     err = launch_topk(d.route, logits, d.bias, T, ids, gw, nullptr, s);
     if (err != cudaSuccess) return cuda_fail(err, "top-k kernel");
@@ -499,6 +543,18 @@ moe_status moe_layer_timed(const moe_layer_plan* plan, const void* x, int T, flo
     }
     err = launch_combine(y, gw, ppos, T, k, H, shared, d.accumulate != 0, out, s);
     if (err != cudaSuccess) return cuda_fail(err, "combine kernel");
+    return MOE_OK;
+}
+
+moe_status moe_layer_workspace_init(moe_layer_plan* plan, int T, void* workspace, moe_stream_t stream) {
+    if (!plan || !workspace) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    if (!aligned(workspace, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+    const LayerWs w = layer_ws(plan->d, T);
+    cudaError_t err = launch_init_header(at<WsHeader>(workspace, w.hdr), reinterpret_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return cuda_fail(err, "workspace init");
+    for (void* p : plan->ready_ws)
+        if (p == workspace) return MOE_OK;
+    plan->ready_ws.push_back(workspace);
     return MOE_OK;
 }
 

@@ -30,6 +30,15 @@ struct WsHeader {
 };
 constexpr size_t kHeaderBytes = 256;
 
+// Grid-barrier counters of the fused decode kernel, at byte 64 of the header.
+// moe_layer_workspace_init writes kDecodeMagic and zeroes the counters; the
+// kernel leaves them at zero when it finishes.
+struct DecodeSync {
+    uint32_t magic, bar1, bar2, done;
+};
+constexpr size_t kDecodeSyncOffset = 64;
+constexpr uint32_t kDecodeMagic = 0x4D4F4531u;
+
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Records `msg` as this host thread's moe_last_error() text and returns `st`.
@@ -75,6 +84,40 @@ cudaError_t launch_combine(const float* y_pairs, const float* w, const int32_t* 
                            int H, const float* shared_out, bool accumulate, float* out, cudaStream_t s);
 cudaError_t launch_rmsnorm_bf16(const float* x, const float* gamma, int T, int H, float eps, void* u,
                                 cudaStream_t s);
+
+// ---------------------------------------------------------------- fused decode layer
+// The whole layer for a few tokens in one cooperative persistent launch.
+struct DecodeArgs {
+    moe_route_cfg route;
+    const float* Wr;
+    const float* bias;
+    const void* x;
+    bool x_bf16;
+    int T, H, I;
+    int qtype;
+    const uint8_t* wg;
+    const uint8_t* wu;
+    const uint8_t* wd;
+    int64_t stride_gu, stride_d;
+    int I_s, s_qtype;
+    const uint8_t* sg;
+    const uint8_t* su;
+    const uint8_t* sd;
+    float* logits;
+    int32_t* ids;
+    float* gw;
+    int32_t* sorted;
+    int32_t* offsets;
+    int32_t* pair_pos;
+    float* h;
+    float* h_s;
+    float* out;
+    bool accumulate;
+    WsHeader* hdr;
+};
+bool decode_fused_supported(const DecodeArgs& a);
+cudaError_t launch_init_header(WsHeader* hdr, cudaStream_t s);
+cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s);
 
 // ---------------------------------------------------------------- tensor-core grouped GEMM
 // Expert FFN for many tokens per expert on tcgen05: gate/up + SwiGLU into an

@@ -1,0 +1,264 @@
+// qdot.cuh -- per-lane dequant-dot of quantized rows against staged fp32 vectors.
+//
+// One warp reads 4 weight rows at a time; per warp iteration every lane covers
+// 32 weights of each row: Q4_K one 16-byte quant chunk (8 lanes per 256-weight
+// super-block: w = d*sc_j*q - dmin*m_j), Q8_0 one 34-byte block (w = d*q).
+// The vectors are staged in shared memory in exactly the order of that walk
+// (float4 slot (it*8 + i4)*32 + lane), so every lane reads 16 bytes at a time
+// without bank conflicts, and for Q4_K each lane also finds the sums of its two
+// 16-element halves (the min term).  Used by the decode GEMV kernels and the
+// fused decode-layer kernel.
+#pragma once
+
+#include "internal.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ float qd_byte_to_float(uint32_t word, int b) {
+    // 0x4B0000bb is 2^23 + bb as an fp32; subtracting 2^23 leaves bb exactly.
+    return __int_as_float(__byte_perm(word, 0x4B00u, 0x5440u | (uint32_t)b)) - 8388608.0f;
+}
+// Same for a byte that holds int8 + 128: leaves the signed value exactly.
+__device__ __forceinline__ float qd_sbyte_to_float(uint32_t word, int b) {
+    return __int_as_float(__byte_perm(word, 0x4B00u, 0x5440u | (uint32_t)b)) - 8388736.0f;
+}
+__device__ __forceinline__ uint32_t qd_ldg_u16(const uint8_t* p) {
+    return __ldg(reinterpret_cast<const unsigned short*>(p));
+}
+
+template <int QT>
+struct Walk;
+
+// Q4_K: lane l of iteration it covers super-block it*4 + l/8, quant chunk l%8.
+template <>
+struct Walk<MOE_Q4_K> {
+    static constexpr int kBlockWeights = kQ4KWeights;
+    static constexpr int kBlockBytes = kQ4KBytes;
+    static constexpr int kBlocksPerIter = 4;
+    __device__ static int blk(int it, int lane) { return it * 4 + (lane >> 3); }
+    // element offset inside the row of the first of the 4 values of slot i4
+    __device__ static int pos(int it, int lane, int i4) {
+        const int ch = lane & 7, c = ch >> 1, half = ch & 1, hi = i4 >> 2;
+        return blk(it, lane) * 256 + 64 * c + 32 * hi + 16 * half + 4 * (i4 & 3);
+    }
+};
+
+// Q8_0: lane l of iteration it covers block it*32 + l.
+template <>
+struct Walk<MOE_Q8_0> {
+    static constexpr int kBlockWeights = kQ80Weights;
+    static constexpr int kBlockBytes = kQ80Bytes;
+    static constexpr int kBlocksPerIter = 32;
+    __device__ static int blk(int it, int lane) { return it * 32 + lane; }
+    __device__ static int pos(int it, int lane, int i4) { return blk(it, lane) * 32 + 4 * i4; }
+};
+
+template <int QT>
+__host__ __device__ inline int walk_iters(int K) {
+    const int nblk = K / (QT == MOE_Q4_K ? kQ4KWeights : kQ80Weights);
+    const int bpi = QT == MOE_Q4_K ? 4 : 32;
+    return (nblk + bpi - 1) / bpi;
+}
+
+__device__ __forceinline__ float4 qd_load_vec4(const void* v, bool bf16, int64_t idx) {
+    float4 out;
+    if (bf16) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(v) + idx);
+        out.x = __uint_as_float(raw.x << 16);
+        out.y = __uint_as_float(raw.x & 0xFFFF0000u);
+        out.z = __uint_as_float(raw.y << 16);
+        out.w = __uint_as_float(raw.y & 0xFFFF0000u);
+    } else {
+        out = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(v) + idx);
+    }
+    return out;
+}
+
+// Stage one length-K vector (src: bf16 or fp32, global) into xs (iters*256 float4
+// slots, walk order) with threads [tid0, tid0+nthr).  Call qd_stage_sums after a
+// barrier for Q4_K.  `coherent` reads through L2 (data written by other CTAs).
+template <int QT>
+__device__ __forceinline__ void qd_stage(const void* src, bool bf16, bool coherent, int K, int iters, float4* xs,
+                                         int tid, int nthr) {
+    const int nblk = K / Walk<QT>::kBlockWeights;
+    for (int s = tid; s < iters * 256; s += nthr) {
+        const int it = s >> 8, i4 = (s >> 5) & 7, ln = s & 31;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (Walk<QT>::blk(it, ln) < nblk) {
+            const int p = Walk<QT>::pos(it, ln, i4);
+            if (coherent && !bf16) v = __ldcg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + p));
+            else v = qd_load_vec4(src, bf16, p);
+        }
+        xs[s] = v;
+    }
+}
+
+// 16-element half sums of each lane's slice (Q4_K min term): xsum[it*32 + lane].
+__device__ __forceinline__ void qd_stage_sums(const float4* xs, float2* xsum, int iters, int tid, int nthr) {
+    for (int r = tid; r < iters * 32; r += nthr) {
+        const int it = r >> 5, ln = r & 31;
+        const float4* base = xs + it * 256 + ln;
+        float lo = 0.f, hi = 0.f;
+#pragma unroll
+        for (int i4 = 0; i4 < 4; ++i4) {
+            const float4 v = base[i4 * 32];
+            lo += (v.x + v.y) + (v.z + v.w);
+            const float4 u = base[(i4 + 4) * 32];
+            hi += (u.x + u.y) + (u.z + u.w);
+        }
+        xsum[r] = make_float2(lo, hi);
+    }
+}
+
+// acc[r][t] += lane's part of row r . vector t, for 4 rows and nt <= NT staged vectors.
+// Vector t lives at xs + t*vstride (float4 slots) and xsum + t*sstride.  Rows may be
+// NULL (skipped, accumulators untouched).
+template <int QT, int NT>
+__device__ __forceinline__ void qd_rows4(const uint8_t* const (&rowp)[4], int nblk, int iters, const float4* xs,
+                                         int vstride, const float2* xsum, int sstride, int nt, int lane,
+                                         float (&acc)[4][NT], const int* vidx = nullptr) {
+    for (int it = 0; it < iters; ++it) {
+        const int b = Walk<QT>::blk(it, lane);
+        if (b >= nblk) continue;
+        if (QT == MOE_Q4_K) {
+            const int ch = lane & 7, jj = (ch >> 1) & 1, upper = ch >> 2;
+            uint4 q[4], hd[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                if (rowp[r]) {
+                    const uint8_t* bp = rowp[r] + (int64_t)b * kQ4KBytes;
+                    hd[r] = __ldg(reinterpret_cast<const uint4*>(bp));
+                    q[r] = __ldg(reinterpret_cast<const uint4*>(bp + 16 + 16 * ch));
+                } else {
+                    hd[r] = make_uint4(0, 0, 0, 0);
+                    q[r] = make_uint4(0, 0, 0, 0);
+                }
+            }
+            float fsc[4][2], fm[4][2];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float d = __half2float(__ushort_as_half((unsigned short)(hd[r].x & 0xFFFFu)));
+                const float dmin = __half2float(__ushort_as_half((unsigned short)(hd[r].x >> 16)));
+#pragma unroll
+                for (int s = 0; s < 2; ++s) {
+                    const int j = 2 * jj + s;
+                    const uint32_t by = (hd[r].y >> (8 * j)) & 0xFFu;
+                    const uint32_t bz = (hd[r].z >> (8 * j)) & 0xFFu;
+                    const uint32_t bw = (hd[r].w >> (8 * j)) & 0xFFu;
+                    uint32_t sc, m;
+                    if (!upper) { sc = by & 63u; m = bz & 63u; }
+                    else { sc = (bw & 15u) | ((by >> 6) << 4); m = (bw >> 4) | ((bz >> 6) << 4); }
+                    fsc[r][s] = d * (float)sc;
+                    fm[r][s] = dmin * (float)m;
+                }
+            }
+            const float4* xb = xs + it * 256 + lane;
+            const float2* xsb = xsum + it * 32 + lane;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                if (t < nt) {
+                    float dl[4], dh[4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) { dl[r] = 0.f; dh[r] = 0.f; }
+#pragma unroll
+                    const size_t vt = (size_t)(vidx ? vidx[t] : t);
+                    for (int w4 = 0; w4 < 4; ++w4) {
+                        const float4 xl = xb[vt * vstride + w4 * 32];
+                        const float4 xh = xb[vt * vstride + (w4 + 4) * 32];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const uint32_t word = w4 == 0 ? q[r].x : w4 == 1 ? q[r].y : w4 == 2 ? q[r].z : q[r].w;
+                            const uint32_t lo = word & 0x0F0F0F0Fu, hi = (word >> 4) & 0x0F0F0F0Fu;
+                            dl[r] = fmaf(qd_byte_to_float(lo, 0), xl.x, dl[r]);
+                            dl[r] = fmaf(qd_byte_to_float(lo, 1), xl.y, dl[r]);
+                            dl[r] = fmaf(qd_byte_to_float(lo, 2), xl.z, dl[r]);
+                            dl[r] = fmaf(qd_byte_to_float(lo, 3), xl.w, dl[r]);
+                            dh[r] = fmaf(qd_byte_to_float(hi, 0), xh.x, dh[r]);
+                            dh[r] = fmaf(qd_byte_to_float(hi, 1), xh.y, dh[r]);
+                            dh[r] = fmaf(qd_byte_to_float(hi, 2), xh.z, dh[r]);
+                            dh[r] = fmaf(qd_byte_to_float(hi, 3), xh.w, dh[r]);
+                        }
+                    }
+                    const float2 sx = xsb[vt * sstride];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        float v = fsc[r][0] * dl[r];
+                        v = fmaf(fsc[r][1], dh[r], v);
+                        v = fmaf(-fm[r][0], sx.x, v);
+                        v = fmaf(-fm[r][1], sx.y, v);
+                        acc[r][t] += v;
+                    }
+                }
+            }
+        } else {
+            uint32_t qw[4][8];
+            float dd[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                if (rowp[r]) {
+                    const uint8_t* bp = rowp[r] + (int64_t)b * kQ80Bytes;
+                    dd[r] = __half2float(__ushort_as_half((unsigned short)qd_ldg_u16(bp)));
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        const uint32_t lo16 = qd_ldg_u16(bp + 2 + 4 * w);
+                        const uint32_t hi16 = qd_ldg_u16(bp + 4 + 4 * w);
+                        qw[r][w] = (lo16 | (hi16 << 16)) ^ 0x80808080u;   // int8 + 128 as bytes
+                    }
+                } else {
+                    dd[r] = 0.f;
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) qw[r][w] = 0x80808080u;
+                }
+            }
+            const float4* xb = xs + it * 256 + lane;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                if (t < nt) {
+                    float dt[4] = {0.f, 0.f, 0.f, 0.f};
+                    const size_t vt = (size_t)(vidx ? vidx[t] : t);
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        const float4 xv = xb[vt * vstride + w * 32];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            dt[r] = fmaf(qd_sbyte_to_float(qw[r][w], 0), xv.x, dt[r]);
+                            dt[r] = fmaf(qd_sbyte_to_float(qw[r][w], 1), xv.y, dt[r]);
+                            dt[r] = fmaf(qd_sbyte_to_float(qw[r][w], 2), xv.z, dt[r]);
+                            dt[r] = fmaf(qd_sbyte_to_float(qw[r][w], 3), xv.w, dt[r]);
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) acc[r][t] = fmaf(dd[r], dt[r], acc[r][t]);
+                }
+            }
+        }
+    }
+}
+
+// Butterfly sum of every accumulator across the warp (fixed order: same bits on every run).
+template <int NT>
+__device__ __forceinline__ void qd_warp_reduce(float (&acc)[4][NT]) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            float v = acc[r][t];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            acc[r][t] = v;
+        }
+}
+
+// acc[r][t] selected by runtime (r, t) without dynamic register indexing.
+template <int NT>
+__device__ __forceinline__ float qd_pick(const float (&acc)[4][NT], int r, int t) {
+    float v = 0.f;
+#pragma unroll
+    for (int tt = 0; tt < NT; ++tt)
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr)
+            if (tt == t && rr == r) v = acc[rr][tt];
+    return v;
+}
+
+}  // namespace moe

@@ -15,6 +15,7 @@
 #include <math.h>
 
 #include "internal.cuh"
+#include "route_common.cuh"
 
 namespace moe {
 namespace {
@@ -133,117 +134,23 @@ __global__ void __launch_bounds__(256) logits_tiled_kernel(const void* __restric
     }
 }
 
-// (value, id) arg-max across the warp: larger value first, then lower id.
-__device__ __forceinline__ void warp_argmax(float& v, int& id) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-        const int oid = __shfl_xor_sync(0xffffffffu, id, o);
-        if (ov > v || (ov == v && oid < id)) { v = ov; id = oid; }
-    }
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
 constexpr int kTopkWarps = 4;
 
 // One warp per token.  Shared memory per warp: sel[E] and s[E].
-__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(
-    int mode, int E, int k, int G, int Gk, float scale, int renorm, const float* __restrict__ logits,
-    const float* __restrict__ bias, int T, int32_t* __restrict__ ids, float* __restrict__ wout, WsHeader* hdr) {
+__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(RouteCfgDev c, const float* __restrict__ logits,
+                                                               const float* __restrict__ bias, int T,
+                                                               int32_t* __restrict__ ids, float* __restrict__ wout,
+                                                               WsHeader* hdr) {
     extern __shared__ float sm[];
     if (hdr && blockIdx.x == 0 && threadIdx.x == 0) {
         hdr->status = MOE_OK;
         hdr->ticket = 0u;
     }
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int warp = threadIdx.x >> 5;
     const int t = blockIdx.x * kTopkWarps + warp;
     if (t >= T) return;
-    float* sel = sm + (size_t)warp * 2 * E;
-    float* sv = sel + E;
-    const float* lrow = logits + (int64_t)t * E;
-    const bool sig = (mode == MOE_ROUTE_SIGMOID_GROUP);
-    for (int e = lane; e < E; e += 32) {
-        const float l = lrow[e];
-        if (sig) {
-            const float s = 1.0f / (1.0f + expf(-l));
-            sv[e] = s;
-            sel[e] = s + (bias ? bias[e] : 0.0f);
-        } else {
-            sv[e] = l;
-            sel[e] = l;
-        }
-    }
-    __syncwarp();
-    if (sig) {
-        const int per = E / G;
-        float gs = -INFINITY;
-        if (lane < G) {
-            float b1 = -INFINITY, b2 = -INFINITY;
-            for (int i = 0; i < per; ++i) {
-                const float v = sel[lane * per + i];
-                if (v > b1) { b2 = b1; b1 = v; } else if (v > b2) { b2 = v; }
-            }
-            gs = per >= 2 ? b1 + b2 : b1;
-        }
-        uint32_t keep = 0u;
-        for (int r = 0; r < Gk; ++r) {
-            float v = (lane < G && !((keep >> lane) & 1u)) ? gs : -INFINITY;
-            int id = (lane < G && !((keep >> lane) & 1u)) ? lane : 0x7fffffff;
-            warp_argmax(v, id);
-            if (id < 32) keep |= 1u << id;
-        }
-        for (int e = lane; e < E; e += 32)
-            if (!((keep >> (e / per)) & 1u)) sel[e] = -INFINITY;
-        __syncwarp();
-    }
-    // k rounds of arg-max over sel; lane r keeps the r-th pick.
-    int my_id = 0x7fffffff;
-    float my_val = 0.f;
-    for (int r = 0; r < k; ++r) {
-        float v = -INFINITY;
-        int id = 0x7fffffff;
-        for (int e = lane; e < E; e += 32) {
-            const float c = sel[e];
-            // any candidate beats none, so a non-finite row still yields an index in range
-            if (c > v || (c == v && e < id) || id == 0x7fffffff) { v = c; id = e; }
-        }
-        warp_argmax(v, id);
-        if (id >= E) id = 0;
-        if (lane == r) { my_id = id; my_val = sv[id]; }
-        if (lane == 0) sel[id] = -INFINITY;
-        __syncwarp();
-    }
-    // Gates.
-    float num = 0.f, den;
-    if (sig) {
-        num = lane < k ? my_val : 0.f;
-        den = renorm ? warp_sum(num) : 1.0f;
-    } else {
-        const float m = __shfl_sync(0xffffffffu, my_val, 0);  // the first pick is the largest logit
-        num = lane < k ? expf(my_val - m) : 0.f;
-        if (renorm) {
-            den = warp_sum(num);
-        } else {
-            float part = 0.f;
-            for (int e = lane; e < E; e += 32) part += expf(lrow[e] - m);
-            den = warp_sum(part);
-        }
-    }
-    // Ascending id order: the rank of my id among the k picks.
-    int rank = 0;
-    for (int j = 0; j < k; ++j) {
-        const int oid = __shfl_sync(0xffffffffu, my_id, j);
-        rank += (oid < my_id) ? 1 : 0;
-    }
-    if (lane < k) {
-        ids[(int64_t)t * k + rank] = my_id;
-        wout[(int64_t)t * k + rank] = scale * (num / den);
-    }
+    float* sel = sm + (size_t)warp * 2 * c.E;
+    warp_topk(c, logits + (int64_t)t * c.E, bias, sel, sel + c.E, ids + (int64_t)t * c.k, wout + (int64_t)t * c.k);
 }
 
 }  // namespace
@@ -267,11 +174,15 @@ cudaError_t launch_topk(const moe_route_cfg& cfg, const float* logits, const flo
     const int E = cfg.n_experts;
     const size_t smem = (size_t)kTopkWarps * 2 * E * sizeof(float);
     // E <= 1024 keeps this at or below 32 KB: no opt-in needed.
-    const int G = cfg.mode == MOE_ROUTE_SIGMOID_GROUP ? cfg.n_groups : 1;
-    const int Gk = cfg.mode == MOE_ROUTE_SIGMOID_GROUP ? cfg.topk_groups : 1;
-    topk_kernel<<<(T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, smem, s>>>(
-        (int)cfg.mode, E, cfg.top_k, G, Gk, cfg.routed_scale, cfg.renormalize, logits, bias, T, ids, w,
-        clear_hdr);
+    RouteCfgDev c;
+    c.mode = (int)cfg.mode;
+    c.E = E;
+    c.k = cfg.top_k;
+    c.G = cfg.mode == MOE_ROUTE_SIGMOID_GROUP ? cfg.n_groups : 1;
+    c.Gk = cfg.mode == MOE_ROUTE_SIGMOID_GROUP ? cfg.topk_groups : 1;
+    c.renorm = cfg.renormalize;
+    c.scale = cfg.routed_scale;
+    topk_kernel<<<(T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, smem, s>>>(c, logits, bias, T, ids, w, clear_hdr);
     return cudaGetLastError();
 }
 

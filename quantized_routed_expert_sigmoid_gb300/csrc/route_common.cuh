@@ -1,0 +1,120 @@
+// route_common.cuh -- one token's top-k selection and gates, done by one warp.
+// Shared by the routing kernel and the fused decode kernel (both compute the
+// same definition; see route.cu for it).
+#pragma once
+
+#include <math.h>
+
+#include "internal.cuh"
+
+namespace moe {
+
+// (value, id) arg-max across the warp: larger value first, then lower id.
+__device__ __forceinline__ void warp_argmax(float& v, int& id) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+        const int oid = __shfl_xor_sync(0xffffffffu, id, o);
+        if (ov > v || (ov == v && oid < id)) { v = ov; id = oid; }
+    }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+struct RouteCfgDev {
+    int mode, E, k, G, Gk, renorm;
+    float scale;
+};
+
+// The whole warp selects token `lrow`'s k experts and writes them in ascending id
+// order to ids[0..k) with their gates w[0..k).  sel, sv: 2*E floats of per-warp
+// shared memory.  lrow is read through L2 (it may have been written by other CTAs
+// of the same grid).
+__device__ __forceinline__ void warp_topk(const RouteCfgDev& c, const float* lrow, const float* bias, float* sel,
+                                          float* sv, int32_t* ids, float* w) {
+    const int lane = threadIdx.x & 31;
+    const int E = c.E, k = c.k;
+    const bool sig = (c.mode == MOE_ROUTE_SIGMOID_GROUP);
+    for (int e = lane; e < E; e += 32) {
+        const float l = __ldcg(lrow + e);
+        if (sig) {
+            const float s = 1.0f / (1.0f + expf(-l));
+            sv[e] = s;
+            sel[e] = s + (bias ? bias[e] : 0.0f);
+        } else {
+            sv[e] = l;
+            sel[e] = l;
+        }
+    }
+    __syncwarp();
+    if (sig) {
+        const int per = E / c.G;
+        float gs = -INFINITY;
+        if (lane < c.G) {
+            float b1 = -INFINITY, b2 = -INFINITY;
+            for (int i = 0; i < per; ++i) {
+                const float v = sel[lane * per + i];
+                if (v > b1) { b2 = b1; b1 = v; } else if (v > b2) { b2 = v; }
+            }
+            gs = per >= 2 ? b1 + b2 : b1;
+        }
+        uint32_t keep = 0u;
+        for (int r = 0; r < c.Gk; ++r) {
+            float v = (lane < c.G && !((keep >> lane) & 1u)) ? gs : -INFINITY;
+            int id = (lane < c.G && !((keep >> lane) & 1u)) ? lane : 0x7fffffff;
+            warp_argmax(v, id);
+            if (id < 32) keep |= 1u << id;
+        }
+        for (int e = lane; e < E; e += 32)
+            if (!((keep >> (e / per)) & 1u)) sel[e] = -INFINITY;
+        __syncwarp();
+    }
+    // k rounds of arg-max over sel; lane r keeps the r-th pick.
+    int my_id = 0x7fffffff;
+    float my_val = 0.f;
+    for (int r = 0; r < k; ++r) {
+        float v = -INFINITY;
+        int id = 0x7fffffff;
+        for (int e = lane; e < E; e += 32) {
+            const float cand = sel[e];
+            // any candidate beats none, so a non-finite row still yields an index in range
+            if (cand > v || (cand == v && e < id) || id == 0x7fffffff) { v = cand; id = e; }
+        }
+        warp_argmax(v, id);
+        if (id >= E) id = 0;
+        if (lane == r) { my_id = id; my_val = sv[id]; }
+        if (lane == 0) sel[id] = -INFINITY;
+        __syncwarp();
+    }
+    float num = 0.f, den;
+    if (sig) {
+        num = lane < k ? my_val : 0.f;
+        den = c.renorm ? warp_sum(num) : 1.0f;
+    } else {
+        const float m = __shfl_sync(0xffffffffu, my_val, 0);  // the first pick is the largest logit
+        num = lane < k ? expf(my_val - m) : 0.f;
+        if (c.renorm) {
+            den = warp_sum(num);
+        } else {
+            float part = 0.f;
+            for (int e = lane; e < E; e += 32) part += expf(__ldcg(lrow + e) - m);
+            den = warp_sum(part);
+        }
+    }
+    int rank = 0;
+    for (int j = 0; j < k; ++j) {
+        const int oid = __shfl_sync(0xffffffffu, my_id, j);
+        rank += (oid < my_id) ? 1 : 0;
+    }
+    if (lane < k) {
+        ids[rank] = my_id;
+        w[rank] = c.scale * (num / den);
+    }
+    __syncwarp();
+}
+
+}  // namespace moe

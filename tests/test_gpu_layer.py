@@ -197,3 +197,43 @@ def test_tc_matches_gemv_path():
     o_tc = tl.moe_layer()(tl.x.cuda()).cpu().numpy()
     o_gv = tl.moe_layer(tc_min_tokens=1 << 30)(tl.x.cuda()).cpu().numpy()
     assert rel_l2(o_tc, o_gv) <= TOL_TC
+
+
+# ---------------------------------------------------------------- single-launch decode layer (T <= 4)
+
+def _fused_vs_separate(tl, T):
+    """The single-launch layer and the separate kernels give the same bits and ids."""
+    fused = tl.moe_layer()
+    sep = tl.moe_layer()
+    sep.desc.decode_fused_off = 1
+    sep.rebuild_plan()
+    x = tl.x.cuda()
+    o_f = fused(x).clone()
+    o_s = sep(x).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(o_f, o_s), "fused decode layer differs from the separate kernels"
+    for a, b in zip(fused.debug_views(T), sep.debug_views(T)):
+        assert torch.equal(a, b)
+    assert fused.device_status(T) == 0
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
+def test_fused_decode_matches_separate_kernels(T):
+    _fused_vs_separate(make_layer(synth.DECODE, 50 + T, T), T)
+
+
+def test_fused_decode_deepseek_shape_and_tiny():
+    _fused_vs_separate(make_layer(synth.DEEPSEEK, 60, 2), 2)
+    _fused_vs_separate(make_layer(synth.TINY, 61, 3, exact_all=True), 3)
+
+
+def test_fused_decode_needs_prepared_workspace():
+    import quantized_routed_expert_sigmoid_gb300 as moe
+    tl = make_layer(synth.TINY, 62, 1, exact_all=True)
+    layer = tl.moe_layer()
+    nbytes = layer.workspace_bytes(1)
+    raw = torch.empty(nbytes, dtype=torch.uint8, device="cuda")     # never prepared
+    out = torch.empty(1, synth.TINY.H, device="cuda")
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_layer(layer.plan, tl.x.cuda(), 1, out, raw, nbytes)
+    assert ei.value.status == moe.MOE_ERR_WORKSPACE
