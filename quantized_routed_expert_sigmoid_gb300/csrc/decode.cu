@@ -163,7 +163,7 @@ __device__ __forceinline__ void down_unit(const uint8_t* d, int n0, int K, int i
     }
 }
 
-template <int QR, int QS>
+template <int QR, int QS, int NT>
 __global__ void __launch_bounds__(kDT, 1) decode_layer_kernel(const __grid_constant__ DecodeParams p) {
     extern __shared__ __align__(16) uint8_t dsm[];
     __shared__ int32_t s_ids[kDMaxP];
@@ -311,22 +311,22 @@ __global__ void __launch_bounds__(kDT, 1) decode_layer_kernel(const __grid_const
             if (unit < units_r) {
                 const int a = unit / upe, r0 = (unit - a * upe) * 2;
                 const int e = s_act_e[a], st = s_act_start[a], n = s_act_n[a];
-                int vidx[kDMaxT], orow[kDMaxT];
+                int vidx[NT], orow[NT];
 #pragma unroll
-                for (int t = 0; t < kDMaxT; ++t) {
+                for (int t = 0; t < NT; ++t) {
                     const int pos = st + min(t, n - 1);
                     vidx[t] = s_sorted[pos] / k;        // token of the pair
                     orow[t] = pos;                      // h row = sorted position
                 }
-                gateup_unit<QR, kDMaxT>(p.wg + (int64_t)e * p.stride_gu, p.wu + (int64_t)e * p.stride_gu, r0, H,
+                gateup_unit<QR, NT>(p.wg + (int64_t)e * p.stride_gu, p.wu + (int64_t)e * p.stride_gu, r0, H,
                                         p.it_H_r, xs_r, xsum_r, vidx, n, lane, p.h, orow, I);
             } else {
                 const int r0 = (unit - units_r) * 2;
-                int vidx[kDMaxT], orow[kDMaxT];
+                int vidx[NT], orow[NT];
 #pragma unroll
-                for (int t = 0; t < kDMaxT; ++t) { vidx[t] = min(t, T - 1); orow[t] = min(t, T - 1); }
+                for (int t = 0; t < NT; ++t) { vidx[t] = min(t, T - 1); orow[t] = min(t, T - 1); }
                 const float4* xsrc = QS == QR ? xs_r : xs_s;
-                gateup_unit<QS, kDMaxT>(p.sg, p.su, r0, H, p.it_H_s, xsrc, xsum_s, vidx, T, lane, p.h_s, orow,
+                gateup_unit<QS, NT>(p.sg, p.su, r0, H, p.it_H_s, xsrc, xsum_s, vidx, T, lane, p.h_s, orow,
                                         p.I_s);
             }
         }
@@ -338,12 +338,8 @@ __global__ void __launch_bounds__(kDT, 1) decode_layer_kernel(const __grid_const
         float4* hs_s = reinterpret_cast<float4*>(dsm + p.off_hs_s);
         float2* hsum_s = reinterpret_cast<float2*>(dsm + p.off_hsum_s);
         const int slots_I_r = p.it_I_r * 256, slots_Is_s = p.it_Is_s * 256;
-        for (int i = 0; i < P; ++i)
-            qd_stage<QR>(p.h + (int64_t)i * I, false, true, I, p.it_I_r, hs_r + (size_t)i * slots_I_r, tid, kDT);
-        if (has_shared)
-            for (int t = 0; t < T; ++t)
-                qd_stage<QS>(p.h_s + (int64_t)t * p.I_s, false, true, p.I_s, p.it_Is_s, hs_s + (size_t)t * slots_Is_s,
-                             tid, kDT);
+        qd_stage_many_f32<QR>(p.h, I, P, I, p.it_I_r, hs_r, tid, kDT);
+        if (has_shared) qd_stage_many_f32<QS>(p.h_s, p.I_s, T, p.I_s, p.it_Is_s, hs_s, tid, kDT);
         __syncthreads();
         if (QR == MOE_Q4_K)
             for (int i = 0; i < P; ++i) qd_stage_sums(hs_r + (size_t)i * slots_I_r, hsum_r + i * p.it_I_r * 32, p.it_I_r, tid, kDT);
@@ -357,16 +353,16 @@ __global__ void __launch_bounds__(kDT, 1) decode_layer_kernel(const __grid_const
             const int a = unit / (g1 - g0), g = g0 + (unit - a * (g1 - g0));
             if (a < nact) {
                 const int st = s_act_start[a], n = s_act_n[a];
-                int vidx[kDMaxT], ycol[kDMaxT];
+                int vidx[NT], ycol[NT];
 #pragma unroll
-                for (int t = 0; t < kDMaxT; ++t) { vidx[t] = st + min(t, n - 1); ycol[t] = st + min(t, n - 1); }
-                down_unit<QR, kDMaxT>(p.wd + (int64_t)s_act_e[a] * p.stride_d, 4 * g, I, p.it_I_r, hs_r, hsum_r,
+                for (int t = 0; t < NT; ++t) { vidx[t] = st + min(t, n - 1); ycol[t] = st + min(t, n - 1); }
+                down_unit<QR, NT>(p.wd + (int64_t)s_act_e[a] * p.stride_d, 4 * g, I, p.it_I_r, hs_r, hsum_r,
                                       vidx, n, lane, ybuf, ycol, nrows, nbase);
             } else {
-                int vidx[kDMaxT], ycol[kDMaxT];
+                int vidx[NT], ycol[NT];
 #pragma unroll
-                for (int t = 0; t < kDMaxT; ++t) { vidx[t] = min(t, T - 1); ycol[t] = P + min(t, T - 1); }
-                down_unit<QS, kDMaxT>(p.sd, 4 * g, p.I_s, p.it_Is_s, hs_s, hsum_s, vidx, T, lane, ybuf, ycol, nrows,
+                for (int t = 0; t < NT; ++t) { vidx[t] = min(t, T - 1); ycol[t] = P + min(t, T - 1); }
+                down_unit<QS, NT>(p.sd, 4 * g, p.I_s, p.it_Is_s, hs_s, hsum_s, vidx, T, lane, ybuf, ycol, nrows,
                                       nbase);
             }
         }
@@ -409,9 +405,9 @@ __global__ void init_header_kernel(WsHeader* hdr) {
 
 int g_num_sms = 0;
 
-template <int QR, int QS>
-cudaError_t launch_q(const DecodeParams& p, size_t smem, cudaStream_t s) {
-    cudaError_t err = cudaFuncSetAttribute(decode_layer_kernel<QR, QS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <int QR, int QS, int NT>
+cudaError_t launch_nt(const DecodeParams& p, size_t smem, cudaStream_t s) {
+    cudaError_t err = cudaFuncSetAttribute(decode_layer_kernel<QR, QS, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)smem);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
@@ -424,7 +420,15 @@ cudaError_t launch_q(const DecodeParams& p, size_t smem, cudaStream_t s) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_layer_kernel<QR, QS>, p);
+    return cudaLaunchKernelEx(&cfg, decode_layer_kernel<QR, QS, NT>, p);
+}
+
+// NT = the largest number of a token batch's pairs one expert can hold (<= T), rounded up.
+template <int QR, int QS>
+cudaError_t launch_q(const DecodeParams& p, size_t smem, cudaStream_t s) {
+    if (p.T == 1) return launch_nt<QR, QS, 1>(p, smem, s);
+    if (p.T == 2) return launch_nt<QR, QS, 2>(p, smem, s);
+    return launch_nt<QR, QS, 4>(p, smem, s);
 }
 
 struct Layout {

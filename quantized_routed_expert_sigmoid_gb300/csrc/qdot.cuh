@@ -93,6 +93,36 @@ __device__ __forceinline__ void qd_stage(const void* src, bool bf16, bool cohere
     }
 }
 
+// Stage n vectors at once (vector i from base + i*row_elems, fp32, written by other
+// CTAs: read through L2) into xs + i*iters*256: every load is issued before any store.
+template <int QT>
+__device__ __forceinline__ void qd_stage_many_f32(const float* base, int64_t row_elems, int n, int K, int iters,
+                                                  float4* xs, int tid, int nthr) {
+    const int nblk = K / Walk<QT>::kBlockWeights;
+    const int per = iters * 256;
+    const int total = n * per;
+    constexpr int kB = 8;                             // loads in flight per thread
+    for (int s0 = tid; s0 < total; s0 += kB * nthr) {
+        float4 v[kB];
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+            const int s = s0 + b * nthr;
+            v[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (s < total) {
+                const int i = s / per, r = s - i * per;
+                const int it = r >> 8, i4 = (r >> 5) & 7, ln = r & 31;
+                if (Walk<QT>::blk(it, ln) < nblk)
+                    v[b] = __ldcg(reinterpret_cast<const float4*>(base + (int64_t)i * row_elems + Walk<QT>::pos(it, ln, i4)));
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+            const int s = s0 + b * nthr;
+            if (s < total) xs[s] = v[b];
+        }
+    }
+}
+
 // 16-element half sums of each lane's slice (Q4_K min term): xsum[it*32 + lane].
 __device__ __forceinline__ void qd_stage_sums(const float4* xs, float2* xsum, int iters, int tid, int nthr) {
     for (int r = tid; r < iters * 32; r += nthr) {
@@ -160,8 +190,8 @@ __device__ __forceinline__ void qd_rows4(const uint8_t* const (&rowp)[4], int nb
                     float dl[4], dh[4];
 #pragma unroll
                     for (int r = 0; r < 4; ++r) { dl[r] = 0.f; dh[r] = 0.f; }
-#pragma unroll
                     const size_t vt = (size_t)(vidx ? vidx[t] : t);
+#pragma unroll
                     for (int w4 = 0; w4 < 4; ++w4) {
                         const float4 xl = xb[vt * vstride + w4 * 32];
                         const float4 xh = xb[vt * vstride + (w4 + 4) * 32];
