@@ -143,7 +143,18 @@ __device__ __forceinline__ void qd_stage_sums(const float4* xs, float2* xsum, in
 // acc[r][t] += lane's part of row r . vector t, for 4 rows and nt <= NT staged vectors.
 // Vector t lives at xs + t*vstride (float4 slots) and xsum + t*sstride.  Rows may be
 // NULL (skipped, accumulators untouched).
-template <int QT, int NT>
+template <bool kSmemRows>
+__device__ __forceinline__ uint4 qd_ld16(const uint8_t* p) {
+    if (kSmemRows) return *reinterpret_cast<const uint4*>(p);
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
+template <bool kSmemRows>
+__device__ __forceinline__ uint32_t qd_ld2(const uint8_t* p) {
+    if (kSmemRows) return *reinterpret_cast<const unsigned short*>(p);
+    return qd_ldg_u16(p);
+}
+
+template <int QT, int NT, bool kSmemRows = false>
 __device__ __forceinline__ void qd_rows4(const uint8_t* const (&rowp)[4], int nblk, int iters, const float4* xs,
                                          int vstride, const float2* xsum, int sstride, int nt, int lane,
                                          float (&acc)[4][NT], const int* vidx = nullptr) {
@@ -157,8 +168,8 @@ __device__ __forceinline__ void qd_rows4(const uint8_t* const (&rowp)[4], int nb
             for (int r = 0; r < 4; ++r) {
                 if (rowp[r]) {
                     const uint8_t* bp = rowp[r] + (int64_t)b * kQ4KBytes;
-                    hd[r] = __ldg(reinterpret_cast<const uint4*>(bp));
-                    q[r] = __ldg(reinterpret_cast<const uint4*>(bp + 16 + 16 * ch));
+                    hd[r] = qd_ld16<kSmemRows>(bp);
+                    q[r] = qd_ld16<kSmemRows>(bp + 16 + 16 * ch);
                 } else {
                     hd[r] = make_uint4(0, 0, 0, 0);
                     q[r] = make_uint4(0, 0, 0, 0);
@@ -227,11 +238,11 @@ __device__ __forceinline__ void qd_rows4(const uint8_t* const (&rowp)[4], int nb
             for (int r = 0; r < 4; ++r) {
                 if (rowp[r]) {
                     const uint8_t* bp = rowp[r] + (int64_t)b * kQ80Bytes;
-                    dd[r] = __half2float(__ushort_as_half((unsigned short)qd_ldg_u16(bp)));
+                    dd[r] = __half2float(__ushort_as_half((unsigned short)qd_ld2<kSmemRows>(bp)));
 #pragma unroll
                     for (int w = 0; w < 8; ++w) {
-                        const uint32_t lo16 = qd_ldg_u16(bp + 2 + 4 * w);
-                        const uint32_t hi16 = qd_ldg_u16(bp + 4 + 4 * w);
+                        const uint32_t lo16 = qd_ld2<kSmemRows>(bp + 2 + 4 * w);
+                        const uint32_t hi16 = qd_ld2<kSmemRows>(bp + 4 + 4 * w);
                         qw[r][w] = (lo16 | (hi16 << 16)) ^ 0x80808080u;   // int8 + 128 as bytes
                     }
                 } else {

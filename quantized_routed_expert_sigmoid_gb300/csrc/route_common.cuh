@@ -73,21 +73,29 @@ __device__ __forceinline__ void warp_topk(const RouteCfgDev& c, const float* lro
             if (!((keep >> (e / per)) & 1u)) sel[e] = -INFINITY;
         __syncwarp();
     }
-    // k rounds of arg-max over sel; lane r keeps the r-th pick.
+    // k rounds of arg-max over sel (larger first, ties to the lower id); lane r keeps the
+    // r-th pick.  Scores become order-preserving unsigned keys (-0 folded into +0) so each
+    // round is two warp reductions; a taken expert gets key 0, below every score.
     int my_id = 0x7fffffff;
     float my_val = 0.f;
+    for (int e = lane; e < E; e += 32) {
+        const uint32_t u = __float_as_uint(sel[e] + 0.0f);
+        reinterpret_cast<uint32_t*>(sel)[e] = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    }
+    __syncwarp();
+    const uint32_t* key = reinterpret_cast<const uint32_t*>(sel);
     for (int r = 0; r < k; ++r) {
-        float v = -INFINITY;
-        int id = 0x7fffffff;
+        uint32_t best = 0u;
+        int bid = 0x7fffffff;
         for (int e = lane; e < E; e += 32) {
-            const float cand = sel[e];
-            // any candidate beats none, so a non-finite row still yields an index in range
-            if (cand > v || (cand == v && e < id) || id == 0x7fffffff) { v = cand; id = e; }
+            const uint32_t kv = key[e];
+            if (kv > best || bid == 0x7fffffff) { best = kv; bid = e; }   // ascending e: ties keep the lower id
         }
-        warp_argmax(v, id);
+        const uint32_t top = __reduce_max_sync(0xffffffffu, best);
+        int id = (int)__reduce_min_sync(0xffffffffu, best == top ? (uint32_t)bid : 0x7fffffffu);
         if (id >= E) id = 0;
         if (lane == r) { my_id = id; my_val = sv[id]; }
-        if (lane == 0) sel[id] = -INFINITY;
+        if (lane == 0) reinterpret_cast<uint32_t*>(sel)[id] = 0u;
         __syncwarp();
     }
     float num = 0.f, den;
