@@ -229,14 +229,8 @@ __global__ void __launch_bounds__(kDT, 1) decode_layer_kernel(const __grid_const
                 qd_stage<QS>(src, xb, false, H, p.it_H_s, xs_s + (size_t)t * slots_H_s, tid, kCons);
         }
         if (grid_barrier(&p.sync->bar1, (uint32_t)G, abort_flag)) {
-            if (QR == MOE_Q4_K)
-                for (int t = 0; t < T; ++t)
-                    qd_stage_sums(xs_r + (size_t)t * slots_H_r, xsum_r + t * p.it_H_r * 32, p.it_H_r, tid, kCons);
-            if (has_shared && QS == MOE_Q4_K) {
-                const float4* xsrc = QS == QR ? xs_r : xs_s;
-                for (int t = 0; t < T; ++t)
-                    qd_stage_sums(xsrc + (size_t)t * slots_H_s, xsum_s + t * p.it_H_s * 32, p.it_H_s, tid, kCons);
-            }
+            if (QR == MOE_Q4_K) qd_stage_sums_many(xs_r, xsum_r, T, p.it_H_r, tid, kCons);
+            if (has_shared && QS == MOE_Q4_K) qd_stage_sums_many(QS == QR ? xs_r : xs_s, xsum_s, T, p.it_H_s, tid, kCons);
             // -------------------------------------------------------- routing (every CTA)
             if (warp < T) {
                 float* sel = reinterpret_cast<float*>(dsm + p.off_topk) + warp * 2 * E;
@@ -405,13 +399,8 @@ __global__ void __launch_bounds__(kDT, 1) decode_layer_kernel(const __grid_const
                 qd_stage_many_f32<QR>(p.h, I, P, I, p.it_I_r, hs_r, tid, kCons);
                 if (has_shared) qd_stage_many_f32<QS>(p.h_s, p.I_s, T, p.I_s, p.it_Is_s, hs_s, tid, kCons);
                 cons_sync();
-                if (QR == MOE_Q4_K)
-                    for (int i = 0; i < P; ++i)
-                        qd_stage_sums(hs_r + (size_t)i * slots_I_r, hsum_r + i * p.it_I_r * 32, p.it_I_r, tid, kCons);
-                if (has_shared && QS == MOE_Q4_K)
-                    for (int t = 0; t < T; ++t)
-                        qd_stage_sums(hs_s + (size_t)t * slots_Is_s, hsum_s + t * p.it_Is_s * 32, p.it_Is_s, tid,
-                                      kCons);
+                if (QR == MOE_Q4_K) qd_stage_sums_many(hs_r, hsum_r, P, p.it_I_r, tid, kCons);
+                if (has_shared && QS == MOE_Q4_K) qd_stage_sums_many(hs_s, hsum_s, T, p.it_Is_s, tid, kCons);
                 cons_sync();
                 // ---- phase 2: unit u (>= n1) is consumed by warp u % kDW as well
                 const int ustart = n1 + ((warp - n1 % kDW) + kDW) % kDW;

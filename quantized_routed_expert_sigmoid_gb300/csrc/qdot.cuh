@@ -81,15 +81,29 @@ template <int QT>
 __device__ __forceinline__ void qd_stage(const void* src, bool bf16, bool coherent, int K, int iters, float4* xs,
                                          int tid, int nthr) {
     const int nblk = K / Walk<QT>::kBlockWeights;
-    for (int s = tid; s < iters * 256; s += nthr) {
-        const int it = s >> 8, i4 = (s >> 5) & 7, ln = s & 31;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (Walk<QT>::blk(it, ln) < nblk) {
-            const int p = Walk<QT>::pos(it, ln, i4);
-            if (coherent && !bf16) v = __ldcg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + p));
-            else v = qd_load_vec4(src, bf16, p);
+    constexpr int kB = 8;                             // loads in flight per thread before any store
+    for (int s0 = tid; s0 < iters * 256; s0 += kB * nthr) {
+        float4 v[kB];
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+            const int s = s0 + b * nthr;
+            v[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (s < iters * 256) {
+                const int it = s >> 8, i4 = (s >> 5) & 7, ln = s & 31;
+                if (Walk<QT>::blk(it, ln) < nblk) {
+                    const int p = Walk<QT>::pos(it, ln, i4);
+                    if (coherent && !bf16)
+                        v[b] = __ldcg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + p));
+                    else
+                        v[b] = qd_load_vec4(src, bf16, p);
+                }
+            }
         }
-        xs[s] = v;
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+            const int s = s0 + b * nthr;
+            if (s < iters * 256) xs[s] = v[b];
+        }
     }
 }
 
@@ -120,6 +134,26 @@ __device__ __forceinline__ void qd_stage_many_f32(const float* base, int64_t row
             const int s = s0 + b * nthr;
             if (s < total) xs[s] = v[b];
         }
+    }
+}
+
+// Half sums of n consecutive staged vectors at once (vector i at xs + i*iters*256,
+// sums at xsum + i*iters*32).
+__device__ __forceinline__ void qd_stage_sums_many(const float4* xs, float2* xsum, int n, int iters, int tid,
+                                                   int nthr) {
+    for (int r = tid; r < n * iters * 32; r += nthr) {
+        const int i = r / (iters * 32), rr = r - i * iters * 32;
+        const int it = rr >> 5, ln = rr & 31;
+        const float4* base = xs + (size_t)i * iters * 256 + it * 256 + ln;
+        float lo = 0.f, hi = 0.f;
+#pragma unroll
+        for (int i4 = 0; i4 < 4; ++i4) {
+            const float4 v = base[i4 * 32];
+            lo += (v.x + v.y) + (v.z + v.w);
+            const float4 u = base[(i4 + 4) * 32];
+            hi += (u.x + u.y) + (u.z + u.w);
+        }
+        xsum[r] = make_float2(lo, hi);
     }
 }
 

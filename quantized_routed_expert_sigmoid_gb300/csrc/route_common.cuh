@@ -39,15 +39,29 @@ __device__ __forceinline__ void warp_topk(const RouteCfgDev& c, const float* lro
     const int lane = threadIdx.x & 31;
     const int E = c.E, k = c.k;
     const bool sig = (c.mode == MOE_ROUTE_SIGMOID_GROUP);
-    for (int e = lane; e < E; e += 32) {
-        const float l = __ldcg(lrow + e);
-        if (sig) {
-            const float s = 1.0f / (1.0f + expf(-l));
-            sv[e] = s;
-            sel[e] = s + (bias ? bias[e] : 0.0f);
-        } else {
-            sv[e] = l;
-            sel[e] = l;
+    // all loads of a chunk are issued before its stores (the shared-memory stores could
+    // otherwise alias the global loads and serialise one L2 round trip per element)
+    for (int e0 = 0; e0 < E; e0 += 8 * 32) {
+        float l[8], b[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = e0 + i * 32 + lane;
+            l[i] = e < E ? __ldcg(lrow + e) : 0.f;
+            b[i] = (sig && bias && e < E) ? __ldg(bias + e) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = e0 + i * 32 + lane;
+            if (e < E) {
+                if (sig) {
+                    const float s = 1.0f / (1.0f + expf(-l[i]));
+                    sv[e] = s;
+                    sel[e] = s + b[i];
+                } else {
+                    sv[e] = l[i];
+                    sel[e] = l[i];
+                }
+            }
         }
     }
     __syncwarp();
