@@ -221,16 +221,29 @@ __global__ void __launch_bounds__(kDT, 1) decode_layer_kernel(const __grid_const
             cons_sync();
         }
         // stage x for phase 1 (an input: no dependency on other CTAs)
-        for (int t = 0; t < T; ++t) {
-            const void* src = xb ? (const void*)(reinterpret_cast<const __nv_bfloat16*>(p.x) + (int64_t)t * H)
-                                 : (const void*)(reinterpret_cast<const float*>(p.x) + (int64_t)t * H);
-            qd_stage<QR>(src, xb, false, H, p.it_H_r, xs_r + (size_t)t * slots_H_r, tid, kCons);
-            if (has_shared && QS != QR)
-                qd_stage<QS>(src, xb, false, H, p.it_H_s, xs_s + (size_t)t * slots_H_s, tid, kCons);
+        if (QR == MOE_Q4_K) {
+            qd4_stage(p.x, xb, false, H, T, nullptr, H, reinterpret_cast<uint4*>(xs_r),
+                      reinterpret_cast<float4*>(xsum_r), tid, kCons);
+        } else {
+            for (int t = 0; t < T; ++t) {
+                const void* src = xb ? (const void*)(reinterpret_cast<const __nv_bfloat16*>(p.x) + (int64_t)t * H)
+                                     : (const void*)(reinterpret_cast<const float*>(p.x) + (int64_t)t * H);
+                qd_stage<QR>(src, xb, false, H, p.it_H_r, xs_r + (size_t)t * slots_H_r, tid, kCons);
+            }
+        }
+        if (has_shared && QS != QR) {
+            if (QS == MOE_Q4_K) {
+                qd4_stage(p.x, xb, false, H, T, nullptr, H, reinterpret_cast<uint4*>(xs_s),
+                          reinterpret_cast<float4*>(xsum_s), tid, kCons);
+            } else {
+                for (int t = 0; t < T; ++t) {
+                    const void* src = xb ? (const void*)(reinterpret_cast<const __nv_bfloat16*>(p.x) + (int64_t)t * H)
+                                         : (const void*)(reinterpret_cast<const float*>(p.x) + (int64_t)t * H);
+                    qd_stage<QS>(src, xb, false, H, p.it_H_s, xs_s + (size_t)t * slots_H_s, tid, kCons);
+                }
+            }
         }
         if (grid_barrier(&p.sync->bar1, (uint32_t)G, abort_flag)) {
-            if (QR == MOE_Q4_K) qd_stage_sums_many(xs_r, xsum_r, T, p.it_H_r, tid, kCons);
-            if (has_shared && QS == MOE_Q4_K) qd_stage_sums_many(QS == QR ? xs_r : xs_s, xsum_s, T, p.it_H_s, tid, kCons);
             // -------------------------------------------------------- routing (every CTA)
             if (warp < T) {
                 float* sel = reinterpret_cast<float*>(dsm + p.off_topk) + warp * 2 * E;
@@ -356,8 +369,12 @@ __global__ void __launch_bounds__(kDT, 1) decode_layer_kernel(const __grid_const
                     const uint8_t* rowp[4] = {base, base + rbH_r, base + 2 * rbH_r, base + 3 * rbH_r};
 #pragma unroll
                     for (int t = 0; t < NT; ++t) vidx[t] = s_sorted[st + min(t, n - 1)] / k;
-                    qd_rows4<QR, NT, true>(rowp, H / Walk<QR>::kBlockWeights, p.it_H_r, xs_r, slots_H_r, xsum_r,
-                                           p.it_H_r * 32, n, lane, acc, vidx);
+                    if (QR == MOE_Q4_K)
+                        qd4_rows4<NT, true>(rowp, H / kQ4KWeights, reinterpret_cast<const uint4*>(xs_r),
+                                            reinterpret_cast<const float4*>(xsum_r), n, lane, acc, vidx);
+                    else
+                        qd_rows4<QR, NT, true>(rowp, H / Walk<QR>::kBlockWeights, p.it_H_r, xs_r, slots_H_r, xsum_r,
+                                               p.it_H_r * 32, n, lane, acc, vidx);
                     qd_warp_reduce<NT>(acc);
                     if (lane < 2 * NT) {
                         const int t = lane >> 1, ri = lane & 1;
@@ -372,8 +389,13 @@ __global__ void __launch_bounds__(kDT, 1) decode_layer_kernel(const __grid_const
 #pragma unroll
                     for (int t = 0; t < NT; ++t) vidx[t] = min(t, T - 1);
                     const float4* xsrc = QS == QR ? xs_r : xs_s;
-                    qd_rows4<QS, NT, true>(rowp, H / Walk<QS>::kBlockWeights, p.it_H_s, xsrc, slots_H_s, xsum_s,
-                                           p.it_H_s * 32, T, lane, acc, vidx);
+                    const float2* xssrc = QS == QR ? xsum_r : xsum_s;
+                    if (QS == MOE_Q4_K)
+                        qd4_rows4<NT, true>(rowp, H / kQ4KWeights, reinterpret_cast<const uint4*>(xsrc),
+                                            reinterpret_cast<const float4*>(xssrc), T, lane, acc, vidx);
+                    else
+                        qd_rows4<QS, NT, true>(rowp, H / Walk<QS>::kBlockWeights, p.it_H_s, xsrc, slots_H_s, xssrc,
+                                               p.it_H_s * 32, T, lane, acc, vidx);
                     qd_warp_reduce<NT>(acc);
                     if (lane < 2 * NT) {
                         const int t = lane >> 1, ri = lane & 1;
@@ -396,11 +418,18 @@ __global__ void __launch_bounds__(kDT, 1) decode_layer_kernel(const __grid_const
                 float4* hs_s = reinterpret_cast<float4*>(dsm + p.off_hs_s);
                 float2* hsum_s = reinterpret_cast<float2*>(dsm + p.off_hsum_s);
                 const int slots_I_r = p.it_I_r * 256, slots_Is_s = p.it_Is_s * 256;
-                qd_stage_many_f32<QR>(p.h, I, P, I, p.it_I_r, hs_r, tid, kCons);
-                if (has_shared) qd_stage_many_f32<QS>(p.h_s, p.I_s, T, p.I_s, p.it_Is_s, hs_s, tid, kCons);
-                cons_sync();
-                if (QR == MOE_Q4_K) qd_stage_sums_many(hs_r, hsum_r, P, p.it_I_r, tid, kCons);
-                if (has_shared && QS == MOE_Q4_K) qd_stage_sums_many(hs_s, hsum_s, T, p.it_Is_s, tid, kCons);
+                if (QR == MOE_Q4_K)
+                    qd4_stage(p.h, false, true, I, P, nullptr, I, reinterpret_cast<uint4*>(hs_r),
+                              reinterpret_cast<float4*>(hsum_r), tid, kCons);
+                else
+                    qd_stage_many_f32<QR>(p.h, I, P, I, p.it_I_r, hs_r, tid, kCons);
+                if (has_shared) {
+                    if (QS == MOE_Q4_K)
+                        qd4_stage(p.h_s, false, true, p.I_s, T, nullptr, p.I_s, reinterpret_cast<uint4*>(hs_s),
+                                  reinterpret_cast<float4*>(hsum_s), tid, kCons);
+                    else
+                        qd_stage_many_f32<QS>(p.h_s, p.I_s, T, p.I_s, p.it_Is_s, hs_s, tid, kCons);
+                }
                 cons_sync();
                 // ---- phase 2: unit u (>= n1) is consumed by warp u % kDW as well
                 const int ustart = n1 + ((warp - n1 % kDW) + kDW) % kDW;
@@ -421,15 +450,23 @@ __global__ void __launch_bounds__(kDT, 1) decode_layer_kernel(const __grid_const
 #pragma unroll
                         for (int t = 0; t < NT; ++t) { vidx[t] = st + min(t, nt - 1); ycol[t] = vidx[t]; }
                         const uint8_t* rowp[4] = {base, base + rbI_r, base + 2 * rbI_r, base + 3 * rbI_r};
-                        qd_rows4<QR, NT, true>(rowp, I / Walk<QR>::kBlockWeights, p.it_I_r, hs_r, slots_I_r, hsum_r,
-                                               p.it_I_r * 32, nt, lane, acc, vidx);
+                        if (QR == MOE_Q4_K)
+                            qd4_rows4<NT, true>(rowp, I / kQ4KWeights, reinterpret_cast<const uint4*>(hs_r),
+                                                reinterpret_cast<const float4*>(hsum_r), nt, lane, acc, vidx);
+                        else
+                            qd_rows4<QR, NT, true>(rowp, I / Walk<QR>::kBlockWeights, p.it_I_r, hs_r, slots_I_r,
+                                                   hsum_r, p.it_I_r * 32, nt, lane, acc, vidx);
                     } else {
                         nt = T;
 #pragma unroll
                         for (int t = 0; t < NT; ++t) { vidx[t] = min(t, T - 1); ycol[t] = P + vidx[t]; }
                         const uint8_t* rowp[4] = {base, base + rbIs_s, base + 2 * rbIs_s, base + 3 * rbIs_s};
-                        qd_rows4<QS, NT, true>(rowp, p.I_s / Walk<QS>::kBlockWeights, p.it_Is_s, hs_s, slots_Is_s,
-                                               hsum_s, p.it_Is_s * 32, nt, lane, acc, vidx);
+                        if (QS == MOE_Q4_K)
+                            qd4_rows4<NT, true>(rowp, p.I_s / kQ4KWeights, reinterpret_cast<const uint4*>(hs_s),
+                                                reinterpret_cast<const float4*>(hsum_s), nt, lane, acc, vidx);
+                        else
+                            qd_rows4<QS, NT, true>(rowp, p.I_s / Walk<QS>::kBlockWeights, p.it_Is_s, hs_s, slots_Is_s,
+                                                   hsum_s, p.it_Is_s * 32, nt, lane, acc, vidx);
                     }
                     qd_warp_reduce<NT>(acc);
                     if (lane < 4 * NT) {
@@ -544,16 +581,20 @@ Layout layout(const DecodeArgs& a, int n_slots) {
     L.it_I_r = iters_for(a.qtype, a.I);
     L.it_H_s = sh ? iters_for(a.s_qtype, a.H) : 0;
     L.it_Is_s = sh ? iters_for(a.s_qtype, a.I_s) : 0;
+    // staged vectors: Q4_K as 24-bit integer planes (X: 16 uint4 per 64 values, XS: 1 float4 per 64),
+    // Q8_0 as fp32 in walk order (xs) with per-lane half sums (xsum)
+    auto xs_bytes = [](int q, int K, int it) { return q == MOE_Q4_K ? (size_t)qd4_groups(K) * 256 : (size_t)it * 4096; };
+    auto xsum_bytes = [](int q, int K, int it) { return q == MOE_Q4_K ? (size_t)qd4_groups(K) * 16 : (size_t)it * 256; };
     size_t o1 = 0;                     // phase 1 staging
-    L.off_xs_r = (int)o1; o1 += (size_t)T * L.it_H_r * 256 * 16;
-    L.off_xsum_r = (int)o1; o1 += (size_t)T * L.it_H_r * 32 * 8;
-    L.off_xs_s = (int)o1; o1 += (sh && a.s_qtype != a.qtype) ? (size_t)T * L.it_H_s * 256 * 16 : 0;
-    L.off_xsum_s = (int)o1; o1 += sh ? (size_t)T * L.it_H_s * 32 * 8 : 0;
+    L.off_xs_r = (int)o1; o1 += (size_t)T * xs_bytes(a.qtype, a.H, L.it_H_r);
+    L.off_xsum_r = (int)o1; o1 += (size_t)T * xsum_bytes(a.qtype, a.H, L.it_H_r);
+    L.off_xs_s = (int)o1; o1 += (sh && a.s_qtype != a.qtype) ? (size_t)T * xs_bytes(a.s_qtype, a.H, L.it_H_s) : 0;
+    L.off_xsum_s = (int)o1; o1 += (sh && a.s_qtype != a.qtype) ? (size_t)T * xsum_bytes(a.s_qtype, a.H, L.it_H_s) : 0;
     size_t o2 = 0;                     // phase 2 staging (same region)
-    L.off_hs_r = (int)o2; o2 += (size_t)P * L.it_I_r * 256 * 16;
-    L.off_hsum_r = (int)o2; o2 += (size_t)P * L.it_I_r * 32 * 8;
-    L.off_hs_s = (int)o2; o2 += sh ? (size_t)T * L.it_Is_s * 256 * 16 : 0;
-    L.off_hsum_s = (int)o2; o2 += sh ? (size_t)T * L.it_Is_s * 32 * 8 : 0;
+    L.off_hs_r = (int)o2; o2 += (size_t)P * xs_bytes(a.qtype, a.I, L.it_I_r);
+    L.off_hsum_r = (int)o2; o2 += (size_t)P * xsum_bytes(a.qtype, a.I, L.it_I_r);
+    L.off_hs_s = (int)o2; o2 += sh ? (size_t)T * xs_bytes(a.s_qtype, a.I_s, L.it_Is_s) : 0;
+    L.off_hsum_s = (int)o2; o2 += sh ? (size_t)T * xsum_bytes(a.s_qtype, a.I_s, L.it_Is_s) : 0;
     size_t o = align_up(o1 > o2 ? o1 : o2, 1024);
     int64_t sb = std::max<int64_t>(4 * rbytes_host(a.qtype, a.H), 4 * rbytes_host(a.qtype, a.I));
     if (sh) sb = std::max<int64_t>(sb, std::max(4 * rbytes_host(a.s_qtype, a.H), 4 * rbytes_host(a.s_qtype, a.I_s)));

@@ -336,4 +336,164 @@ __device__ __forceinline__ float qd_pick(const float (&acc)[4][NT], int r, int t
     return v;
 }
 
+
+// ============================================================================
+// Q4_K against 24-bit integer activations (the path both GEMV kernels use).
+//
+// A row is walked in groups of 64 weights: group g = (super-block b, quant group
+// c), i.e. 32 quant bytes holding sub-blocks 2c (low nibbles) and 2c+1 (high
+// nibbles).  One lane takes one (row, group) item, so it decodes its two
+// sub-block scales once per 64 weights.  Each activation sub-block of 32 values
+// is scaled to 24-bit integers, x24 = round(x * (2^23-1) / max|x|), stored as
+// three byte planes (signed high byte, then two unsigned bytes); the lane
+// multiplies its 4-bit codes with dp4a (exact integer sums), recombines the
+// planes and applies the scales in fp32:
+//   dot_j = (65536*sum(q*hi) + 256*sum(q*mid) + sum(q*lo)) * sx_j
+//   row . x += d*sc_j*dot_j - dmin*m_j*sum(x over sub-block j)
+// The 24-bit rounding is far below fp32 accumulation noise (2^-23 of the block
+// maximum per value).
+// Staged vector layout (G = K/64 groups): X[q*G + g] (q = 0..15) holds the
+// planes {hi, mid, lo, 0} of 4 values: q < 8 values 4q.. of sub-block 2c,
+// q >= 8 values 4(q-8).. of sub-block 2c+1; XS[g] = {sx_lo, sx_hi, sum_lo, sum_hi}.
+// ============================================================================
+
+__host__ __device__ inline int qd4_groups(int K) { return K / 64; }
+// bytes of one staged vector
+__host__ __device__ inline size_t qd4_vec_bytes(int K) { return (size_t)qd4_groups(K) * 17 * 16; }
+
+__device__ __forceinline__ int qd_dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int qd_dp4a_uu(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Stage n vectors (vector i at src + row*row_elems, bf16 or fp32; `coherent` reads
+// fp32 through L2) into X + i*16*G, XS + i*G.  One task = one 32-value sub-block.
+// rows (nullable): vector i is source row rows[i] instead of row i.
+__device__ __forceinline__ void qd4_stage(const void* src, bool bf16, bool coherent, int64_t row_elems, int n,
+                                          const int* rows, int K, uint4* X, float4* XS, int tid, int nthr) {
+    const int G = qd4_groups(K);
+    const int tasks = n * G * 2;
+    for (int s = tid; s < tasks; s += nthr) {
+        const int i = s / (2 * G), r = s - i * 2 * G, g = r >> 1, hh = r & 1;
+        const int64_t row = rows ? rows[i] : i;
+        const int64_t e0 = row * row_elems + (g >> 2) * 256 + (2 * (g & 3) + hh) * 32;
+        float v[32];
+        if (bf16) {
+            const uint4* p4 = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(src) + e0);
+            uint4 raw[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) raw[j] = p4[j];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+                for (int h2 = 0; h2 < 4; ++h2) {
+                    v[8 * j + 2 * h2] = __uint_as_float(w[h2] << 16);
+                    v[8 * j + 2 * h2 + 1] = __uint_as_float(w[h2] & 0xFFFF0000u);
+                }
+            }
+        } else {
+            const float4* p4 = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + e0);
+            float4 raw[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) raw[j] = coherent ? __ldcg(p4 + j) : p4[j];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                v[4 * j] = raw[j].x; v[4 * j + 1] = raw[j].y; v[4 * j + 2] = raw[j].z; v[4 * j + 3] = raw[j].w;
+            }
+        }
+        float m = 0.f, sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) { m = fmaxf(m, fabsf(v[j])); sum += v[j]; }
+        const float inv = m > 0.f ? 8388607.0f / m : 0.f;
+        const float sx = m / 8388607.0f;
+        uint4* Xi = X + (size_t)i * 16 * G;
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {
+            uint32_t hw = 0, mw = 0, lw = 0;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                int x24 = __float2int_rn(v[4 * q8 + b] * inv);
+                x24 = max(-8388607, min(8388607, x24));
+                hw |= ((uint32_t)(x24 >> 16) & 0xFFu) << (8 * b);
+                mw |= ((uint32_t)(x24 >> 8) & 0xFFu) << (8 * b);
+                lw |= ((uint32_t)x24 & 0xFFu) << (8 * b);
+            }
+            Xi[(hh * 8 + q8) * G + g] = make_uint4(hw, mw, lw, 0u);
+        }
+        float* xsf = reinterpret_cast<float*>(XS + (size_t)i * G + g);
+        xsf[hh] = sx;
+        xsf[2 + hh] = sum;
+    }
+}
+
+// acc[r][t] += row r . vector vidx[t] (t < nt) for 4 Q4_K rows of nblk super-blocks.
+// Rows may be NULL (skipped).  Vector v lives at X + v*16*G, XS + v*G.
+template <int NT, bool kSmemRows = false>
+__device__ __forceinline__ void qd4_rows4(const uint8_t* const (&rowp)[4], int nblk, const uint4* X,
+                                          const float4* XS, int nt, int lane, float (&acc)[4][NT],
+                                          const int* vidx = nullptr) {
+    const int G = nblk * 4;
+    for (int item = lane; item < 4 * G; item += 32) {
+        const int r = item / G, g = item - r * G;
+        const uint8_t* rp = r == 0 ? rowp[0] : r == 1 ? rowp[1] : r == 2 ? rowp[2] : rowp[3];
+        if (!rp) continue;
+        const int b = g >> 2, c = g & 3;
+        const uint8_t* blk = rp + (int64_t)b * kQ4KBytes;
+        const uint4 hd = qd_ld16<kSmemRows>(blk);
+        const uint4 q0 = qd_ld16<kSmemRows>(blk + 16 + 32 * c);
+        const uint4 q1 = qd_ld16<kSmemRows>(blk + 32 + 32 * c);
+        // scales of sub-blocks 2c and 2c+1
+        const float d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
+        const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
+        float fs[2], fm[2];
+#pragma unroll
+        for (int s2 = 0; s2 < 2; ++s2) {
+            const int j = 2 * c + s2, jj = j & 3;
+            const uint32_t by = (hd.y >> (8 * jj)) & 0xFFu, bz = (hd.z >> (8 * jj)) & 0xFFu, bw = (hd.w >> (8 * jj)) & 0xFFu;
+            uint32_t sc, m;
+            if (j < 4) { sc = by & 63u; m = bz & 63u; }
+            else { sc = (bw & 15u) | ((by >> 6) << 4); m = (bw >> 4) | ((bz >> 6) << 4); }
+            fs[s2] = d * (float)sc;
+            fm[s2] = dmin * (float)m;
+        }
+        const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            if (t < nt) {
+                const int v = vidx ? vidx[t] : t;
+                const uint4* Xv = X + (size_t)v * 16 * G + g;
+                int ah0 = 0, am0 = 0, al0 = 0, ah1 = 0, am1 = 0, al1 = 0;
+#pragma unroll
+                for (int qd = 0; qd < 8; ++qd) {
+                    const uint32_t ql = qw[qd] & 0x0F0F0F0Fu, qh = (qw[qd] >> 4) & 0x0F0F0F0Fu;
+                    const uint4 xl = Xv[qd * G], xh = Xv[(8 + qd) * G];
+                    ah0 = qd_dp4a_us(ql, xl.x, ah0);
+                    am0 = qd_dp4a_uu(ql, xl.y, am0);
+                    al0 = qd_dp4a_uu(ql, xl.z, al0);
+                    ah1 = qd_dp4a_us(qh, xh.x, ah1);
+                    am1 = qd_dp4a_uu(qh, xh.y, am1);
+                    al1 = qd_dp4a_uu(qh, xh.z, al1);
+                }
+                const float4 xs = XS[(size_t)v * G + g];
+                const float d0 = fmaf((float)ah0, 65536.0f, fmaf((float)am0, 256.0f, (float)al0)) * xs.x;
+                const float d1 = fmaf((float)ah1, 65536.0f, fmaf((float)am1, 256.0f, (float)al1)) * xs.y;
+                float part = fs[0] * d0;
+                part = fmaf(fs[1], d1, part);
+                part = fmaf(-fm[0], xs.z, part);
+                part = fmaf(-fm[1], xs.w, part);
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr)
+                    if (rr == r) acc[rr][t] += part;
+            }
+        }
+    }
+}
+
 }  // namespace moe

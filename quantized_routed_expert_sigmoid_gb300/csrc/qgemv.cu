@@ -67,8 +67,57 @@ __global__ void __launch_bounds__(kThreads) qgemv_kernel(GemvArgs a, int iters, 
     const int n_units = a.rows / (GATEUP ? 2 : 4);
     const int slots = iters * 256;
 
+    __shared__ int s_rows[NT];
     for (int pb = 0; pb < n_tot; pb += NT) {
         const int nt = min(NT, n_tot - pb);
+        if (QT == MOE_Q4_K) {
+            // ---- stage the activation vectors as 24-bit integer planes (qdot.cuh)
+            uint4* X = reinterpret_cast<uint4*>(xs);
+            float4* XS = reinterpret_cast<float4*>(X + (size_t)NT * 16 * qd4_groups(a.K));
+            if (threadIdx.x < nt) {
+                const int i = start + pb + threadIdx.x;
+                s_rows[threadIdx.x] = (GATEUP && a.sorted_pairs) ? a.sorted_pairs[i] / a.k : i;
+            }
+            __syncthreads();
+            qd4_stage(a.vin, a.vin_bf16, false, a.K, nt, s_rows, a.K, X, XS, threadIdx.x, kThreads);
+            __syncthreads();
+            for (int ui = 0; ui < units_per_warp; ++ui) {
+                const int unit = (blockIdx.x * kWarps + warp) * units_per_warp + ui;
+                if (unit >= n_units) break;
+                const uint8_t* rowp[4];
+                if (GATEUP) {
+                    const int r0 = unit * 2;
+                    rowp[0] = w0 + (int64_t)r0 * rb;
+                    rowp[1] = w0 + (int64_t)(r0 + 1) * rb;
+                    rowp[2] = w1 + (int64_t)r0 * rb;
+                    rowp[3] = w1 + (int64_t)(r0 + 1) * rb;
+                } else {
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) rowp[r] = w0 + (int64_t)(unit * 4 + r) * rb;
+                }
+                float acc[4][NT];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) acc[r][t] = 0.f;
+                qd4_rows4<NT>(rowp, nblk, X, XS, nt, lane, acc);
+                qd_warp_reduce<NT>(acc);
+                if (GATEUP) {
+                    if (lane < 2 * NT) {
+                        const int t = lane >> 1, ri = lane & 1;
+                        if (t < nt) {
+                            const float g = qd_pick<NT>(acc, ri, t), u = qd_pick<NT>(acc, 2 + ri, t);
+                            a.out[(int64_t)(start + pb + t) * a.rows + unit * 2 + ri] = g / (1.0f + expf(-g)) * u;
+                        }
+                    }
+                } else if (lane < 4 * NT) {
+                    const int t = lane >> 2, ri = lane & 3;
+                    if (t < nt) a.out[(int64_t)(start + pb + t) * a.rows + unit * 4 + ri] = qd_pick<NT>(acc, ri, t);
+                }
+            }
+            __syncthreads();
+            continue;
+        }
         // ---- stage the activation vectors of pairs start+pb .. +nt in walk order
         for (int t = 0; t < nt; ++t) {
             const int i = start + pb + t;
@@ -124,7 +173,8 @@ __global__ void __launch_bounds__(kThreads) qgemv_kernel(GemvArgs a, int iters, 
 
 template <int QT, bool GU, int NT>
 cudaError_t launch_one(const GemvArgs& a, int iters, int grid_y, cudaStream_t s) {
-    const size_t smem = (size_t)NT * iters * 256 * sizeof(float4) + (size_t)NT * iters * 32 * sizeof(float2);
+    const size_t smem = QT == MOE_Q4_K ? (size_t)NT * qd4_vec_bytes(a.K)
+                                       : (size_t)NT * iters * 256 * sizeof(float4) + (size_t)NT * iters * 32 * sizeof(float2);
     if (smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(qgemv_kernel<QT, GU, NT>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -155,8 +205,9 @@ cudaError_t launch_qgemv(const GemvArgs& a, cudaStream_t s) {
     // Tokens per pass: at most the pairs one expert can hold (distinct ids per
     // token: <= tokens), at most 8, and a staged tile of at most ~64 KB.
     const int per_expert_max = a.sorted_pairs ? (a.n_pairs / a.k) : a.n_pairs;
+    const size_t per_vec = a.qtype == MOE_Q4_K ? qd4_vec_bytes(a.K) : (size_t)iters * 4096;
     int nt = 8;
-    while (nt > 1 && ((size_t)nt * iters * 4096 > 64 * 1024 || nt / 2 >= per_expert_max)) nt /= 2;
+    while (nt > 1 && ((size_t)nt * per_vec > 64 * 1024 || nt / 2 >= per_expert_max)) nt /= 2;
     const int grid_y = a.offsets ? (a.n_pairs < a.E ? a.n_pairs : a.E) : 1;
     if (a.qtype == MOE_Q4_K)
         return a.gateup ? launch_nt<MOE_Q4_K, true>(a, nt, iters, grid_y, s)
