@@ -123,7 +123,7 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ workload construction
 
-def build_layers(shape, T, L, seed, device, shared_router=False):
+def build_layers(shape, T, L, seed, device, shared_router=False, decode_fused=True):
     """L layers with distinct expert weights.  Router weights and biases are drawn on the
     CPU (small) so that a workload built around them (the Zipf prefill) sees the same values;
     shared_router gives every layer layer 0's router."""
@@ -145,7 +145,7 @@ def build_layers(shape, T, L, seed, device, shared_router=False):
                                topk_groups=shape.topk_groups, scale=shape.scale, renormalize=shape.renormalize,
                                x_dtype=shape.x_dtype, I_s=shape.I_s, shared_qtype=shape.shared_qtype,
                                s_gate=sh[0] if sh else None, s_up=sh[1] if sh else None,
-                               s_down=sh[2] if sh else None))
+                               s_down=sh[2] if sh else None, decode_fused=decode_fused))
     return layers
 
 
@@ -193,7 +193,8 @@ def run_ours(args, rank, world):
     if args.layers:
         L = args.layers
         desc = desc.replace("16 distinct layers", f"{L} distinct layers")
-    layers = build_layers(shape, T, L, seed + 1000 * rank, device, shared_router=(args.workload == "prefill"))
+    layers = build_layers(shape, T, L, seed + 1000 * rank, device, shared_router=(args.workload == "prefill"),
+                          decode_fused=not args.separate_decode)
     x = make_x(shape, T, seed + 1000 * rank, device, args.workload)
     outs = [torch.empty(T, shape.H, dtype=torch.float32, device=device) for _ in range(L)]
     for lay in layers:
@@ -261,8 +262,9 @@ def run_ours(args, rank, world):
     value = world * T * L * args.steps / (t_ms / 1e3)
 
     # ---- the dominant kernel alone (the routed gate/up + SwiGLU launch)
-    tc_path = T >= 128
-    fused_path = T <= 4 and T * shape.k <= 64 and shape.E <= 256
+    path = layers[0].path(T)           # which kernels the library runs for this T
+    tc_path = path == "tensor"
+    fused_path = path == "fused_decode"
     gu_ms = None
     if stack:
         x = u                           # the kernels' input in the stack: the bf16 normalised stream
@@ -340,7 +342,7 @@ def run_ours(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": desc, "T": T, "layers_per_step": L, "H": shape.H, "E": shape.E, "k": shape.k,
                    "I": shape.I, "qtype": shape.qtype, "l2": "inputs larger than L2 (distinct weights per layer)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU", "path": path},
         "layer": {"us_per_layer": round(layer_us, 3), "algorithmic_bytes": round(layer_bytes),
                   "GBps": round(layer_bytes / (layer_us * 1e-6) / 1e9, 1),
                   "frac_hbm": round(layer_bytes / (layer_us * 1e-6) / 1e9 / hbm_peak, 4),
@@ -508,6 +510,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="override the layers per step (default per workload)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (tokens per layer call)")
+    ap.add_argument("--separate-decode", action="store_true",
+                    help="decode sizes: run the separate route/permute/GEMV/combine kernels, not the single-launch layer")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -221,6 +221,18 @@ moe_status moe_layer_workspace_size(const moe_layer_plan* plan, int T, size_t* b
  * workspace header; this call sets them up.  moe_layer refuses a workspace
  * that was not prepared with MOE_ERR_WORKSPACE. */
 moe_status moe_layer_workspace_init(moe_layer_plan* plan, int T, void* workspace, moe_stream_t stream);
+/* Which kernels moe_layer runs for T tokens with this plan (T >= 1):
+ *   MOE_PATH_GEMV         route, permute, dequant-GEMV experts and combine as
+ *                         separate launches (fp32 accumulation);
+ *   MOE_PATH_FUSED_DECODE the whole layer as one cooperative launch (same
+ *                         arithmetic as MOE_PATH_GEMV, same bits);
+ *   MOE_PATH_TENSOR       route and permute, then the tcgen05 grouped GEMM
+ *                         (fp16 operands, fp32 accumulation) and combine.
+ * Host-only; reads nothing on the device. */
+#define MOE_PATH_GEMV 0
+#define MOE_PATH_FUSED_DECODE 1
+#define MOE_PATH_TENSOR 2
+moe_status moe_layer_path(const moe_layer_plan* plan, int T, int* path);
 /*
  * moe_layer -- the whole layer: route, permute, experts, combine (+ shared),
  * for T tokens of x (device, [T][H] in desc->x_type) into out (device, fp32

@@ -92,6 +92,7 @@ def _declare(lib):
         "moe_layer_plan_destroy": [P],
         "moe_layer_workspace_size": [P, I, PS],
         "moe_layer_workspace_init": [P, I, P, P],
+        "moe_layer_path": [P, I, ctypes.POINTER(ctypes.c_int)],
         "moe_layer": [P, P, I, P, P, S, P],
         "moe_layer_timed": [P, P, I, P, P, S, P, P, P],
         "moe_layer_debug_views": [P, I, P, ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P)],
@@ -216,6 +217,17 @@ def moe_layer_workspace_size(plan: int, T: int) -> int:
 
 def moe_layer_workspace_init(plan, T, workspace, stream=None):
     _check(load().moe_layer_workspace_init(plan, T, _p(workspace), _stream(stream)))
+
+
+MOE_PATH_GEMV, MOE_PATH_FUSED_DECODE, MOE_PATH_TENSOR = 0, 1, 2
+PATH_NAMES = {MOE_PATH_GEMV: "gemv", MOE_PATH_FUSED_DECODE: "fused_decode", MOE_PATH_TENSOR: "tensor"}
+
+
+def moe_layer_path(plan, T):
+    """Which kernels moe_layer runs for T tokens: one of the MOE_PATH_* values."""
+    v = ctypes.c_int(-1)
+    _check(load().moe_layer_path(plan, T, ctypes.byref(v)))
+    return v.value
 
 
 def moe_layer(plan, x, T, out, workspace, ws_bytes, stream=None):

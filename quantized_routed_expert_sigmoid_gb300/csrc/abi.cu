@@ -112,6 +112,38 @@ bool use_tc(const moe_layer_desc& d, int T) {
     return true;
 }
 
+// The shape-level fields of the single-launch decode layer (no buffers yet).
+DecodeArgs decode_shape_args(const moe_layer_desc& d, int T) {
+    DecodeArgs da{};
+    da.route = d.route;
+    da.Wr = d.W_router;
+    da.bias = d.bias;
+    da.T = T; da.H = d.hidden; da.I = d.intermediate;
+    da.qtype = d.gate.qtype;
+    da.wg = static_cast<const uint8_t*>(d.gate.data);
+    da.wu = static_cast<const uint8_t*>(d.up.data);
+    da.wd = static_cast<const uint8_t*>(d.down.data);
+    da.stride_gu = d.gate.expert_stride_bytes;
+    da.stride_d = d.down.expert_stride_bytes;
+    da.I_s = d.shared_intermediate;
+    if (da.I_s > 0) {
+        da.s_qtype = d.s_gate.qtype;
+        da.sg = static_cast<const uint8_t*>(d.s_gate.data);
+        da.su = static_cast<const uint8_t*>(d.s_up.data);
+        da.sd = static_cast<const uint8_t*>(d.s_down.data);
+    }
+    return da;
+}
+
+// True when moe_layer runs T tokens as the single-launch decode layer.
+bool fused_decode_applies(const moe_layer_desc& d, int T) {
+    if (d.decode_fused_off || use_tc(d, T)) return false;
+    const bool same_q = d.gate.qtype == d.up.qtype && d.gate.qtype == d.down.qtype &&
+                        (d.shared_intermediate == 0 ||
+                         (d.s_gate.qtype == d.s_up.qtype && d.s_gate.qtype == d.s_down.qtype));
+    return same_q && decode_chain_supported(decode_shape_args(d, T));
+}
+
 LayerWs layer_ws(const moe_layer_desc& d, int T) {
     const int E = d.route.n_experts, k = d.route.top_k, H = d.hidden, I = d.intermediate;
     const size_t P = (size_t)T * k;
@@ -406,6 +438,15 @@ moe_status moe_layer_workspace_size(const moe_layer_plan* plan, int T, size_t* b
     return MOE_OK;
 }
 
+moe_status moe_layer_path(const moe_layer_plan* plan, int T, int* path) {
+    if (!plan || !path) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    if (T < 1) return fail(MOE_ERR_INVALID_ARG, "T = %d < 1", T);
+    if (use_tc(plan->d, T)) *path = MOE_PATH_TENSOR;
+    else if (fused_decode_applies(plan->d, T)) *path = MOE_PATH_FUSED_DECODE;
+    else *path = MOE_PATH_GEMV;
+    return MOE_OK;
+}
+
 moe_status moe_layer(const moe_layer_plan* plan, const void* x, int T, float* out, void* workspace,
                      size_t ws_bytes, moe_stream_t stream) {
     return moe_layer_timed(plan, x, T, out, workspace, ws_bytes, stream, nullptr, nullptr);
@@ -437,46 +478,24 @@ moe_status moe_layer_timed(const moe_layer_plan* plan, const void* x, int T, flo
     int32_t* ppos = at<int32_t>(workspace, w.pair_pos);
     int32_t* offs = at<int32_t>(workspace, w.offsets);
     cudaError_t err;
-    if (!w.tc) {
-        DecodeArgs da{};
-        da.route = d.route;
-        da.Wr = d.W_router;
-        da.bias = d.bias;
+    if (!w.tc && fused_decode_applies(d, T)) {
+        DecodeArgs da = decode_shape_args(d, T);
         da.x = x;
         da.x_bf16 = xb;
-        da.T = T; da.H = H; da.I = I;
-        da.qtype = d.gate.qtype;
-        da.wg = static_cast<const uint8_t*>(d.gate.data);
-        da.wu = static_cast<const uint8_t*>(d.up.data);
-        da.wd = static_cast<const uint8_t*>(d.down.data);
-        da.stride_gu = d.gate.expert_stride_bytes;
-        da.stride_d = d.down.expert_stride_bytes;
-        da.I_s = d.shared_intermediate;
-        if (da.I_s > 0) {
-            da.s_qtype = d.s_gate.qtype;
-            da.sg = static_cast<const uint8_t*>(d.s_gate.data);
-            da.su = static_cast<const uint8_t*>(d.s_up.data);
-            da.sd = static_cast<const uint8_t*>(d.s_down.data);
-        }
         da.logits = logits; da.ids = ids; da.gw = gw; da.sorted = sorted; da.offsets = offs; da.pair_pos = ppos;
         da.h = at<float>(workspace, w.h);
         da.h_s = at<float>(workspace, w.sh_h);
         da.out = out;
         da.accumulate = d.accumulate != 0;
         da.hdr = hdr;
-        const bool same_q = d.gate.qtype == d.up.qtype && d.gate.qtype == d.down.qtype &&
-                            (da.I_s == 0 || (d.s_gate.qtype == d.s_up.qtype && d.s_gate.qtype == d.s_down.qtype));
-        if (!plan->d.decode_fused_off && same_q && decode_fused_supported(da)) {
-            bool ready = false;
-            for (void* p : plan->ready_ws) ready = ready || p == workspace;
-            if (!ready)
-                return fail(MOE_ERR_WORKSPACE, "workspace not prepared: call moe_layer_workspace_init once on it");
-            if (evb && (err = cudaEventRecord(evb, s)) != cudaSuccess) return cuda_fail(err, "event record");
-            err = launch_decode_fused(da, s);
-            if (err != cudaSuccess) return cuda_fail(err, "fused decode kernel");
-            if (eva && (err = cudaEventRecord(eva, s)) != cudaSuccess) return cuda_fail(err, "event record");
-            return MOE_OK;
-        }
+        bool ready = false;
+        for (void* p : plan->ready_ws) ready = ready || p == workspace;
+        if (!ready) return fail(MOE_ERR_WORKSPACE, "workspace not prepared: call moe_layer_workspace_init once on it");
+        if (evb && (err = cudaEventRecord(evb, s)) != cudaSuccess) return cuda_fail(err, "event record");
+        err = launch_decode_chain(da, s);
+        if (err != cudaSuccess) return cuda_fail(err, "decode chain kernels");
+        if (eva && (err = cudaEventRecord(eva, s)) != cudaSuccess) return cuda_fail(err, "event record");
+        return MOE_OK;
     }
     err = launch_router_logits(x, xb, T, H, d.W_router, E, logits, hdr, s);
     if (err != cudaSuccess) return cuda_fail(err, "router logits kernel");

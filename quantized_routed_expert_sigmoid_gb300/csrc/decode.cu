@@ -122,6 +122,15 @@ __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t b
                  : "memory");
 }
 
+// Requests [src, src + bytes) into L2 without waiting (a hint: no completion, no
+// fault on the weight tensors it is given).  src and bytes are 16-byte multiples.
+__device__ __forceinline__ void prefetch_l2(const uint8_t* src, int64_t bytes) {
+    for (int64_t o = 0; o < bytes; o += 65536) {
+        const uint32_t n = (uint32_t)(bytes - o < 65536 ? bytes - o : 65536);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src + o), "r"(n) : "memory");
+    }
+}
+
 // The consumers of every CTA meet here.  Returns false on timeout.
 __device__ bool grid_barrier(uint32_t* ctr, uint32_t target, volatile int* abort_flag) {
     cons_sync();
@@ -303,6 +312,43 @@ __global__ void __launch_bounds__(kDT, 1) decode_layer_kernel(const __grid_const
         if (warp == kDW) {
             // ======================================================== producer
             if (lane == 0) {
+                // The ring holds NS units; the rest of the CTA's slice is requested into L2
+                // now, so every weight byte of the layer is in flight at once and the ring's
+                // later copies are L2 hits.  Consecutive units of one expert are contiguous
+                // rows: one prefetch per run and matrix (pieces of at most 64 KB).
+                for (int u = NS; u < n1;) {
+                    const int q = q0 + u;
+                    const uint8_t *gp, *upp;
+                    int64_t rb;
+                    int qend, r0;
+                    if (q < nact * half_r) {
+                        const int a = q / half_r;
+                        qend = min(q0 + n1, (a + 1) * half_r);
+                        r0 = 2 * (q - a * half_r);
+                        gp = p.wg + (int64_t)s_act_e[a] * p.stride_gu;
+                        upp = p.wu + (int64_t)s_act_e[a] * p.stride_gu;
+                        rb = rbH_r;
+                    } else {
+                        qend = q0 + n1;
+                        r0 = 2 * (q - nact * half_r);
+                        gp = p.sg;
+                        upp = p.su;
+                        rb = rbH_s;
+                    }
+                    const int64_t nb = 2 * (int64_t)(qend - q) * rb;
+                    prefetch_l2(gp + r0 * rb, nb);
+                    prefetch_l2(upp + r0 * rb, nb);
+                    u = qend - q0;
+                }
+                for (int u = max(NS, n1); u < n_units;) {
+                    const int v = u - n1, a = v / ng, gi = v - a * ng;
+                    const uint8_t* d;
+                    int64_t rb;
+                    if (a < nact) { d = p.wd + (int64_t)s_act_e[a] * p.stride_d; rb = rbI_r; }
+                    else { d = p.sd; rb = rbIs_s; }
+                    prefetch_l2(d + (int64_t)4 * (g0 + gi) * rb, (int64_t)4 * (ng - gi) * rb);
+                    u = n1 + (a + 1) * ng;
+                }
                 int issued = 0;
                 for (int u = 0; u < n_units; ++u) {
                     const int slot = u % NS;

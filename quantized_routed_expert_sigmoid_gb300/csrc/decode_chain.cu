@@ -1,0 +1,652 @@
+// decode_chain.cu -- the MoE layer at T <= 4 tokens as three chained launches.
+//
+// The pages run a decode step as one captured CUDA graph with the routed
+// experts on the card ("bloomery README 0.3.1", "Why it is fast").  At a few
+// tokens a layer reads ~22 MB (hidden 2048) to ~450 MB (hidden 7168) of expert
+// weights; what costs time is the chain of dependent steps (router logits ->
+// the chosen experts' gate/up -> their down rows), each of which must see the
+// previous one complete.  The three kernels are launched with programmatic
+// dependent launch: a kernel starts while the one before it still runs, does
+// what does not depend on it (router rows into registers, the activations
+// staged), then waits (griddepcontrol.wait) for it to complete.
+//
+//   K1 logits   one CTA per expert row: the T router logits of that expert.
+//   K2 gate/up  every CTA selects the top-k of the T tokens itself (identical
+//               results everywhere; CTA 0 publishes them), then a persistent
+//               grid runs (active expert, row pair) units: each warp requests
+//               all the weight bytes of its units at once (per-lane cp.async
+//               into a two-slot ring in shared memory) and computes
+//               h = silu(gate . x) * (up . x) as they land; the shared
+//               expert's rows follow.  Each CTA also requests its share of the
+//               chosen down rows into L2.
+//   K3 down     one CTA per block of output rows: its down rows of every pair
+//               go to shared memory while h is staged, then the dot products,
+//               the gate-weighted combine in fixed order (+ shared, + residual).
+// Dot products use the integer Q4_K walk of qdot.cuh; every reduction has a
+// fixed order, so a replay gives the same bits.
+#include <algorithm>
+
+#include "internal.cuh"
+#include "qdot.cuh"
+#include "route_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kCMaxT = 4;
+constexpr int kCMaxP = 64;
+constexpr int kCMaxE = 256;
+constexpr int kK1Threads = 128;
+constexpr int kK3Threads = 256;
+constexpr int kK1MaxVec = 16;              // float4 of a router row per K1 thread: H <= 8192
+constexpr int kSlotU4 = 4 * 3 * 32;        // ring slot: 4 rows x 3 uint4 x 32 lanes
+constexpr int kK2MaxWarps = 16;
+
+struct ChainParams {
+    RouteCfgDev rc;
+    const float* Wr;
+    const float* bias;
+    const void* x;
+    int x_bf16;
+    int T, H, I;
+    const uint8_t* wg;
+    const uint8_t* wu;
+    const uint8_t* wd;
+    int64_t stride_gu, stride_d;
+    int I_s, s_q8;                          // shared expert: intermediate, 1 if Q8_0 (else Q4_K)
+    const uint8_t* sg;
+    const uint8_t* su;
+    const uint8_t* sd;
+    float* logits;
+    int32_t* ids;
+    float* gw;
+    int32_t* sorted;
+    int32_t* offsets;
+    int32_t* pair_pos;
+    float* h;
+    float* h_s;
+    float* out;
+    int accumulate;
+    WsHeader* hdr;
+    int it_H_s, it_Is_s;                    // Q8_0 walk iterations of the shared expert
+    int k2_warps;                           // K2 warps per CTA (<= kK2MaxWarps)
+    int k2_off_xs_s, k2_off_ring;           // K2 dynamic shared-memory offsets (bytes)
+    int rows_per_cta;                       // K3 output rows per CTA (multiple of 8)
+    int k3_prefetch;                        // K3 copies its down rows to shared memory
+    int k3_off_hs_s, k3_off_y, k3_off_w;    // K3 dynamic shared-memory offsets (bytes)
+};
+
+// The routing every K2 CTA derives from the logits (shared memory).
+struct CtaRoute {
+    int32_t ids[kCMaxP], sorted[kCMaxP], ppos[kCMaxP], tok[kCMaxP];
+    float w[kCMaxP];
+    int act_e[kCMaxP], act_start[kCMaxP], act_n[kCMaxP];
+    int nact;
+    float sel[kCMaxT][2 * kCMaxE];
+};
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void prefetch_l2(const uint8_t* src, int64_t bytes) {
+    for (int64_t o = 0; o < bytes; o += 65536) {
+        const uint32_t n = (uint32_t)(bytes - o < 65536 ? bytes - o : 65536);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src + o), "r"(n) : "memory");
+    }
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+// Every thread of the CTA calls this.  Warp t < T selects token t's experts from the
+// logits (read through L2: another grid wrote them); warp 0 then orders the pairs by
+// expert (stable) and lists the active experts with their runs of sorted positions.
+__device__ void cta_route(const ChainParams& p, CtaRoute& R) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int E = p.rc.E, k = p.rc.k, P = p.T * k;
+    if (warp < p.T)
+        warp_topk(p.rc, p.logits + (int64_t)warp * E, p.bias, R.sel[warp], R.sel[warp] + E, R.ids + warp * k,
+                  R.w + warp * k);
+    __syncthreads();
+    if (warp == 0) {
+        for (int i = lane; i < P; i += 32) {
+            const int ei = R.ids[i];
+            int rank = 0;
+            for (int j = 0; j < P; ++j) {
+                const int ej = R.ids[j];
+                rank += (ej < ei || (ej == ei && j < i)) ? 1 : 0;
+            }
+            R.sorted[rank] = i;
+            R.ppos[i] = rank;
+        }
+        __syncwarp();
+        const int i0 = lane, i1 = lane + 32;
+        const bool f0 = i0 < P && (i0 == 0 || R.ids[R.sorted[i0]] != R.ids[R.sorted[i0 - 1]]);
+        const bool f1 = i1 < P && (R.ids[R.sorted[i1]] != R.ids[R.sorted[i1 - 1]]);
+        const unsigned lo = __ballot_sync(0xffffffffu, f0), hi = __ballot_sync(0xffffffffu, f1);
+        const unsigned below = (1u << lane) - 1u;
+        // the next run's start after position q (or P)
+        const unsigned long long runs = ((unsigned long long)hi << 32) | lo;
+        auto next_start = [&](int q) {
+            const unsigned long long rest = q >= 63 ? 0ull : (runs >> (q + 1)) << (q + 1);
+            return rest ? __ffsll((long long)rest) - 1 : P;
+        };
+        if (f0) {
+            const int a = __popc(lo & below);
+            R.act_e[a] = R.ids[R.sorted[i0]];
+            R.act_start[a] = i0;
+            R.act_n[a] = next_start(i0) - i0;
+        }
+        if (f1) {
+            const int a = __popc(lo) + __popc(hi & below);
+            R.act_e[a] = R.ids[R.sorted[i1]];
+            R.act_start[a] = i1;
+            R.act_n[a] = next_start(i1) - i1;
+        }
+        for (int i = lane; i < P; i += 32) R.tok[i] = R.sorted[i] / k;
+        if (lane == 0) R.nact = __popc(lo) + __popc(hi);
+    }
+    __syncthreads();
+}
+
+// ============================================================================ K1: router logits
+__global__ void __launch_bounds__(kK1Threads) chain_logits_kernel(const __grid_constant__ ChainParams p) {
+    __shared__ float s_part[kK1Threads / 32][kCMaxT];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int e = blockIdx.x, E = p.rc.E, T = p.T, H = p.H;
+    const int n4 = H / 4;
+    // the router row: a weight, independent of the launches before this one
+    float4 w[kK1MaxVec];
+#pragma unroll
+    for (int i = 0; i < kK1MaxVec; ++i) {
+        const int j = tid + i * kK1Threads;
+        w[i] = j < n4 ? __ldg(reinterpret_cast<const float4*>(p.Wr + (int64_t)e * H) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    pdl_wait();                                   // x and the workspace belong to the launches before
+    pdl_launch_dependents();
+    if (e == 0 && tid == 0) p.hdr->status = MOE_OK;
+    const bool xb = p.x_bf16 != 0;
+    float acc[kCMaxT];
+#pragma unroll
+    for (int t = 0; t < kCMaxT; ++t) acc[t] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kK1MaxVec; ++i) {
+        const int j = tid + i * kK1Threads;
+        if (j < n4) {
+#pragma unroll
+            for (int t = 0; t < kCMaxT; ++t) {
+                if (t < T) {
+                    const float4 xv = qd_load_vec4(p.x, xb, (int64_t)t * H + 4 * j);
+                    acc[t] = fmaf(w[i].x, xv.x, acc[t]);
+                    acc[t] = fmaf(w[i].y, xv.y, acc[t]);
+                    acc[t] = fmaf(w[i].z, xv.z, acc[t]);
+                    acc[t] = fmaf(w[i].w, xv.w, acc[t]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < kCMaxT; ++t) {
+        const float v = warp_sum(acc[t]);
+        if (lane == 0) s_part[warp][t] = v;
+    }
+    __syncthreads();
+    if (tid < T) {
+        float s = 0.f;
+#pragma unroll
+        for (int wi = 0; wi < kK1Threads / 32; ++wi) s += s_part[wi][tid];
+        p.logits[(int64_t)tid * E + e] = s;
+    }
+}
+
+// ============================================================================ K2: routing + gate/up
+// Routed units: (active expert a, row pair rp) = rows 2rp, 2rp+1 of gate and up, split
+// into chunks of 32 groups (64 weights each; lane = group in the chunk).  Warp w of the
+// grid takes units w, w + W, ...; every chunk of its units streams through the warp's
+// two ring slots (each lane copies and later reads only its own 16-byte pieces).
+template <int NT, bool kSharedQ8>
+__global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const __grid_constant__ ChainParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ CtaRoute R;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nthr = blockDim.x;
+    const int T = p.T, H = p.H, I = p.I, k = p.rc.k, E = p.rc.E, P = T * k;
+    const int G = qd4_groups(H);
+    const bool has_shared = p.I_s > 0;
+    uint4* X = reinterpret_cast<uint4*>(smem);
+    float4* XS = reinterpret_cast<float4*>(X + (size_t)T * 16 * G);
+    float4* xs_s = reinterpret_cast<float4*>(smem + p.k2_off_xs_s);
+    uint4* ring = reinterpret_cast<uint4*>(smem + p.k2_off_ring) + (size_t)warp * 2 * kSlotU4;
+    const bool xb = p.x_bf16 != 0;
+    // ---- x is the input of the whole chain: stage it before waiting
+    qd4_stage_par(p.x, xb, false, H, T, nullptr, H, X, XS, tid, nthr);
+    if (kSharedQ8 && has_shared) {
+        const int slots = p.it_H_s * 256;
+        for (int t = 0; t < T; ++t) {
+            const void* src = xb ? (const void*)(reinterpret_cast<const __nv_bfloat16*>(p.x) + (int64_t)t * H)
+                                 : (const void*)(reinterpret_cast<const float*>(p.x) + (int64_t)t * H);
+            qd_stage<MOE_Q8_0>(src, xb, false, H, p.it_H_s, xs_s + (size_t)t * slots, tid, nthr);
+        }
+    }
+    pdl_wait();                                   // the logits of K1
+    pdl_launch_dependents();
+    cta_route(p, R);
+    const int nact = R.nact;
+    const int64_t rbH = (int64_t)(H / kQ4KWeights) * kQ4KBytes;
+    const int half_I = I / 2;
+    const int nch = (G + 31) / 32;
+    const int Ur = nact * half_I;
+    const int Us = has_shared ? p.I_s / 2 : 0;
+    const int W = gridDim.x * (nthr / 32);
+    const int wg = blockIdx.x * (nthr / 32) + warp;
+    const int my_units = wg < Ur ? (Ur - wg + W - 1) / W : 0;
+    const int n_items = my_units * nch;
+
+    auto unit_rows = [&](int u, const uint8_t* (&rowp)[4]) {
+        const int a = u / half_I, r0 = 2 * (u - a * half_I);
+        const uint8_t* gb = p.wg + (int64_t)R.act_e[a] * p.stride_gu + r0 * rbH;
+        const uint8_t* ub = p.wu + (int64_t)R.act_e[a] * p.stride_gu + r0 * rbH;
+        rowp[0] = gb; rowp[1] = ub; rowp[2] = gb + rbH; rowp[3] = ub + rbH;
+    };
+    auto issue = [&](int item) {
+        if (item < n_items) {
+            const int u = wg + (item / nch) * W, ch = item - (item / nch) * nch;
+            const int g = ch * 32 + lane;
+            if (g < G) {
+                const uint8_t* rowp[4];
+                unit_rows(u, rowp);
+                uint4* sl = ring + (item & 1) * kSlotU4 + lane;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const uint8_t* blk = rowp[r] + (int64_t)(g >> 2) * kQ4KBytes;
+                    cp_async16(sl + (r * 3 + 0) * 32, blk);
+                    cp_async16(sl + (r * 3 + 1) * 32, blk + 16 + 32 * (g & 3));
+                    cp_async16(sl + (r * 3 + 2) * 32, blk + 32 + 32 * (g & 3));
+                }
+            }
+        }
+        cp_async_commit();
+    };
+    // all of this warp's first two chunks go out before anything else
+    issue(0);
+    issue(1);
+    // ---- this CTA's share of the chosen down rows (and the shared expert's) into L2
+    {
+        const int rows0 = (int)((int64_t)blockIdx.x * H / gridDim.x), rows1 = (int)((int64_t)(blockIdx.x + 1) * H / gridDim.x);
+        const int64_t rbI = (int64_t)(I / kQ4KWeights) * kQ4KBytes;
+        if (warp == 0 && lane < nact && rows1 > rows0)
+            prefetch_l2(p.wd + (int64_t)R.act_e[lane] * p.stride_d + rows0 * rbI, (int64_t)(rows1 - rows0) * rbI);
+        if (warp == 0 && lane == 31 && has_shared && rows1 > rows0) {
+            const int64_t rbS = p.s_q8 ? (int64_t)(p.I_s / kQ80Weights) * kQ80Bytes
+                                       : (int64_t)(p.I_s / kQ4KWeights) * kQ4KBytes;
+            if ((rbS % 16) == 0) prefetch_l2(p.sd + rows0 * rbS, (int64_t)(rows1 - rows0) * rbS);
+        }
+    }
+    // ---- CTA 0 publishes the routing (the down kernel and the debug views read it)
+    if (blockIdx.x == 0) {
+        for (int i = tid; i < P; i += nthr) {
+            p.ids[i] = R.ids[i];
+            p.gw[i] = R.w[i];
+            p.sorted[i] = R.sorted[i];
+            p.pair_pos[i] = R.ppos[i];
+        }
+        for (int e = tid; e <= E; e += nthr) {
+            int cnt = 0;
+            for (int i = 0; i < P; ++i) cnt += R.ids[i] < e ? 1 : 0;
+            p.offsets[e] = cnt;
+        }
+    }
+    // ---- routed units through the ring
+    float acc[4][NT];
+    int n = 0, st = 0;
+    int vidx[NT];
+    for (int item = 0; item < n_items; ++item) {
+        cp_async_wait<1>();                        // this item's group has landed (the next may be in flight)
+        const int u = wg + (item / nch) * W, ch = item - (item / nch) * nch;
+        if (ch == 0) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int t = 0; t < NT; ++t) acc[r][t] = 0.f;
+            const int a = u / half_I;
+            st = R.act_start[a];
+            n = R.act_n[a];
+#pragma unroll
+            for (int t = 0; t < NT; ++t) vidx[t] = R.tok[st + min(t, n - 1)];
+        }
+        const int g = ch * 32 + lane;
+        if (g < G) {
+            const uint4* sl = ring + (item & 1) * kSlotU4 + lane;
+            uint4 hd[4], q0[4], q1[4];
+            const bool live[4] = {true, true, true, true};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                hd[r] = sl[(r * 3 + 0) * 32];
+                q0[r] = sl[(r * 3 + 1) * 32];
+                q1[r] = sl[(r * 3 + 2) * 32];
+            }
+            qd4_group_math<NT, 4>(hd, q0, q1, live, 0, g, G, X, XS, n, acc, vidx);
+        }
+        issue(item + 2);                           // refills the slot just read
+        if (ch == nch - 1) {
+            qd_warp_reduce<NT>(acc);
+            if (lane < 2 * NT) {
+                const int t = lane >> 1, ri = lane & 1;
+                if (t < n) {
+                    const int a = u / half_I, r0 = 2 * (u - a * half_I);
+                    const float gv = qd_pick<NT>(acc, 2 * ri, t), uv = qd_pick<NT>(acc, 2 * ri + 1, t);
+                    p.h[(int64_t)(st + t) * I + r0 + ri] = silu_mul(gv, uv);
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();
+    // ---- the shared expert's row pairs (direct loads)
+    for (int u = wg + my_units * W; u < Ur + Us; u += W) {
+        if (u < Ur) continue;
+        float sacc[4][NT];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int t = 0; t < NT; ++t) sacc[r][t] = 0.f;
+        const int r0 = 2 * (u - Ur);
+        int sv[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) sv[t] = min(t, T - 1);
+        if (kSharedQ8) {
+            const int64_t rbS = (int64_t)(H / kQ80Weights) * kQ80Bytes;
+            const uint8_t* const rowp[4] = {p.sg + r0 * rbS, p.sg + (r0 + 1) * rbS, p.su + r0 * rbS,
+                                            p.su + (r0 + 1) * rbS};
+            qd_rows4<MOE_Q8_0, NT, false>(rowp, H / kQ80Weights, p.it_H_s, xs_s, p.it_H_s * 256,
+                                          reinterpret_cast<const float2*>(xs_s), 0, T, lane, sacc, sv);
+        } else {
+            const uint8_t* const rowp[4] = {p.sg + r0 * rbH, p.sg + (r0 + 1) * rbH, p.su + r0 * rbH,
+                                            p.su + (r0 + 1) * rbH};
+            qd4_rows4<NT, false>(rowp, H / kQ4KWeights, X, XS, T, lane, sacc, sv);
+        }
+        qd_warp_reduce<NT>(sacc);
+        if (lane < 2 * NT) {
+            const int t = lane >> 1, ri = lane & 1;
+            if (t < T) {
+                const float gv = qd_pick<NT>(sacc, ri, t), uv = qd_pick<NT>(sacc, 2 + ri, t);
+                p.h_s[(int64_t)t * p.I_s + r0 + ri] = silu_mul(gv, uv);
+            }
+        }
+    }
+}
+
+// ============================================================================ K3: down + combine
+// CTA c owns output rows [c*R, c*R + R).  Tasks: (pair s, 8 rows) with lane = 4*row + sub
+// and sub taking groups sub, sub+4, ...; then the shared expert's rows 4 at a time.
+template <int NT, bool kSharedQ8>
+__global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_constant__ ChainParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ int32_t s_e[kCMaxP], s_pos[kCMaxP];
+    __shared__ float s_w[kCMaxP];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int T = p.T, H = p.H, I = p.I, k = p.rc.k, P = T * k;
+    const int GI = qd4_groups(I);
+    const int R = p.rows_per_cta, n0 = blockIdx.x * R;
+    const bool has_shared = p.I_s > 0;
+    const int64_t rbI = (int64_t)(I / kQ4KWeights) * kQ4KBytes;
+    uint4* HX = reinterpret_cast<uint4*>(smem);
+    float4* HXS = reinterpret_cast<float4*>(HX + (size_t)P * 16 * GI);
+    float* ybuf = reinterpret_cast<float*>(smem + p.k3_off_y);          // [P + T][R]
+    uint8_t* wbuf = smem + p.k3_off_w;                                   // [P][R][rbI] when prefetching
+    pdl_wait();                                   // h and the routing of K2
+    pdl_launch_dependents();
+    for (int i = tid; i < P; i += kK3Threads) {
+        s_e[i] = __ldcg(p.ids + i);
+        s_pos[i] = __ldcg(p.pair_pos + i);
+        s_w[i] = __ldcg(p.gw + i);
+    }
+    __syncthreads();
+    // ---- the CTA's down rows of every pair to shared memory (in flight while h is staged)
+    const int nrows = min(R, H - n0);
+    if (p.k3_prefetch) {
+        const int per_row = (int)(rbI / 16);
+        const int total = P * nrows * per_row;
+        for (int c = tid; c < total; c += kK3Threads) {
+            const int s = c / (nrows * per_row), rem = c - s * nrows * per_row;
+            const int r = rem / per_row, o = rem - r * per_row;
+            cp_async16(wbuf + ((int64_t)s * R + r) * rbI + 16 * o,
+                       p.wd + (int64_t)s_e[s] * p.stride_d + (int64_t)(n0 + r) * rbI + 16 * o);
+        }
+        cp_async_commit();
+    }
+    // ---- stage every pair's h (row pair_pos[s] of h) and the shared expert's h_s
+    qd4_stage_par(p.h, false, true, I, P, s_pos, I, HX, HXS, tid, kK3Threads);
+    if (has_shared) {
+        if (kSharedQ8) {
+            float4* hs = reinterpret_cast<float4*>(smem + p.k3_off_hs_s);
+            qd_stage_many_f32<MOE_Q8_0>(p.h_s, p.I_s, T, p.I_s, p.it_Is_s, hs, tid, kK3Threads);
+        } else {
+            uint4* SX = reinterpret_cast<uint4*>(smem + p.k3_off_hs_s);
+            float4* SXS = reinterpret_cast<float4*>(SX + (size_t)T * 16 * qd4_groups(p.I_s));
+            qd4_stage_par(p.h_s, false, true, p.I_s, T, nullptr, p.I_s, SX, SXS, tid, kK3Threads);
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    const int nsub = R / 8;
+    const int n_routed = P * nsub;
+    const int n_shared = has_shared ? R / 4 : 0;
+    for (int task = warp; task < n_routed + n_shared; task += kK3Threads / 32) {
+        if (task < n_routed) {
+            const int s = task / nsub, sb = task - s * nsub;
+            const int row = lane >> 2, sub = lane & 3;
+            const int rl = 8 * sb + row, n = n0 + rl;
+            float acc[4][1] = {{0.f}, {0.f}, {0.f}, {0.f}};
+            const uint4* Xs = HX + (size_t)s * 16 * GI;
+            const float4* XSs = HXS + (size_t)s * GI;
+            if (p.k3_prefetch) {
+                const uint8_t* const rowp[4] = {n < H ? wbuf + ((int64_t)s * R + rl) * rbI : nullptr, nullptr, nullptr,
+                                                nullptr};
+                for (int g = sub; g < GI; g += 4) qd4_group<1, 1, true>(rowp, 0, g, GI, Xs, XSs, 1, acc, nullptr);
+            } else {
+                const uint8_t* const rowp[4] = {n < H ? p.wd + (int64_t)s_e[s] * p.stride_d + (int64_t)n * rbI : nullptr,
+                                                nullptr, nullptr, nullptr};
+                for (int g = sub; g < GI; g += 4) qd4_group<1, 1, false>(rowp, 0, g, GI, Xs, XSs, 1, acc, nullptr);
+            }
+            float v = acc[0][0];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            if (sub == 0) ybuf[s * R + rl] = v;
+        } else {
+            const int q = task - n_routed;
+            const int nb = n0 + 4 * q;
+            float acc[4][NT];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int t = 0; t < NT; ++t) acc[r][t] = 0.f;
+            int vidx[NT];
+#pragma unroll
+            for (int t = 0; t < NT; ++t) vidx[t] = min(t, T - 1);
+            if (kSharedQ8) {
+                const int64_t rbS = (int64_t)(p.I_s / kQ80Weights) * kQ80Bytes;
+                const uint8_t* rowp[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) rowp[r] = nb + r < H ? p.sd + (int64_t)(nb + r) * rbS : nullptr;
+                const float4* hs = reinterpret_cast<const float4*>(smem + p.k3_off_hs_s);
+                qd_rows4<MOE_Q8_0, NT, false>(rowp, p.I_s / kQ80Weights, p.it_Is_s, hs, p.it_Is_s * 256,
+                                              reinterpret_cast<const float2*>(hs), 0, T, lane, acc, vidx);
+            } else {
+                const int64_t rbS = (int64_t)(p.I_s / kQ4KWeights) * kQ4KBytes;
+                const uint8_t* rowp[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) rowp[r] = nb + r < H ? p.sd + (int64_t)(nb + r) * rbS : nullptr;
+                const uint4* SX = reinterpret_cast<const uint4*>(smem + p.k3_off_hs_s);
+                const float4* SXS = reinterpret_cast<const float4*>(SX + (size_t)T * 16 * qd4_groups(p.I_s));
+                qd4_rows4<NT, false>(rowp, p.I_s / kQ4KWeights, SX, SXS, T, lane, acc, vidx);
+            }
+            qd_warp_reduce<NT>(acc);
+            if (lane < 4 * NT) {
+                const int t = lane >> 2, ri = lane & 3;
+                if (t < T) ybuf[(P + t) * R + 4 * q + ri] = qd_pick<NT>(acc, ri, t);
+            }
+        }
+    }
+    __syncthreads();
+    // ---- combine: out[t][n] = ((sum_j w_tj * y_(t,j)[n]) + shared) (+ old out)
+    for (int idx = tid; idx < T * R; idx += kK3Threads) {
+        const int t = idx / R, nl = idx - t * R, n = n0 + nl;
+        if (n >= H) continue;
+        float acc = 0.f;
+        for (int j = 0; j < k; ++j) acc = fmaf(s_w[t * k + j], ybuf[(t * k + j) * R + nl], acc);
+        if (has_shared) acc += ybuf[(P + t) * R + nl];
+        float* o = p.out + (int64_t)t * H + n;
+        if (p.accumulate) acc += *o;
+        *o = acc;
+    }
+}
+
+// ============================================================================ host side
+struct ChainLayout {
+    size_t k2_smem, k3_smem;
+    int k2_warps, k2_off_xs_s, k2_off_ring;
+    int k3_prefetch, k3_off_hs_s, k3_off_y, k3_off_w;
+    int it_H_s, it_Is_s, rows_per_cta;
+};
+
+int g_sms = 0;
+
+int sm_count() {
+    if (g_sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    return g_sms;
+}
+
+constexpr size_t kChainSmemCap = 200 * 1024;   // dynamic; the kernels' static shared memory is < 12 KB
+
+ChainLayout chain_layout(const DecodeArgs& a) {
+    ChainLayout L{};
+    const int T = a.T, P = a.T * a.route.top_k, H = a.H, I = a.I;
+    const bool sh = a.I_s > 0, q8 = sh && a.s_qtype == MOE_Q8_0;
+    L.it_H_s = q8 ? walk_iters<MOE_Q8_0>(H) : 0;
+    L.it_Is_s = q8 ? walk_iters<MOE_Q8_0>(a.I_s) : 0;
+    // K2: staged x, then two ring slots per warp; as many warps as fit (at most 16)
+    size_t o = (size_t)T * qd4_vec_bytes(H);
+    L.k2_off_xs_s = (int)align_up(o, 16);
+    o = L.k2_off_xs_s + (q8 ? (size_t)T * L.it_H_s * 4096 : 0);
+    L.k2_off_ring = (int)align_up(o, 16);
+    const size_t per_warp = (size_t)2 * kSlotU4 * 16;
+    int warps = kK2MaxWarps;
+    while (warps > 1 && L.k2_off_ring + warps * per_warp > kChainSmemCap) --warps;
+    L.k2_warps = warps;
+    L.k2_smem = L.k2_off_ring + warps * per_warp;
+    // K3: about two CTAs per SM, 8-row multiples
+    const int sms = std::max(1, sm_count());
+    int R = (H + 2 * sms - 1) / (2 * sms);
+    R = std::max(8, (R + 7) / 8 * 8);
+    L.rows_per_cta = R;
+    o = (size_t)P * qd4_vec_bytes(I);
+    L.k3_off_hs_s = (int)align_up(o, 16);
+    if (sh) o = L.k3_off_hs_s + (q8 ? (size_t)T * L.it_Is_s * 4096 : (size_t)T * qd4_vec_bytes(a.I_s));
+    L.k3_off_y = (int)align_up(o, 16);
+    o = L.k3_off_y + (size_t)(P + T) * R * 4;
+    L.k3_off_w = (int)align_up(o, 16);
+    const size_t wbytes = (size_t)P * R * (size_t)(I / kQ4KWeights) * kQ4KBytes;
+    L.k3_prefetch = L.k3_off_w + wbytes <= kChainSmemCap ? 1 : 0;
+    L.k3_smem = L.k3_off_w + (L.k3_prefetch ? wbytes : 0);
+    return L;
+}
+
+template <int NT, bool Q8>
+cudaError_t launch_chain_nt(const ChainParams& p, const ChainLayout& L, int E, cudaStream_t s) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t err;
+    cfg.gridDim = dim3(E);
+    cfg.blockDim = dim3(kK1Threads);
+    cfg.dynamicSmemBytes = 0;
+    if ((err = cudaLaunchKernelEx(&cfg, chain_logits_kernel, p)) != cudaSuccess) return err;
+    if ((err = cudaFuncSetAttribute(chain_gateup_kernel<NT, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)L.k2_smem)) != cudaSuccess)
+        return err;
+    cfg.gridDim = dim3(sm_count());
+    cfg.blockDim = dim3(L.k2_warps * 32);
+    cfg.dynamicSmemBytes = L.k2_smem;
+    if ((err = cudaLaunchKernelEx(&cfg, chain_gateup_kernel<NT, Q8>, p)) != cudaSuccess) return err;
+    if ((err = cudaFuncSetAttribute(chain_down_kernel<NT, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)L.k3_smem)) != cudaSuccess)
+        return err;
+    cfg.gridDim = dim3((p.H + L.rows_per_cta - 1) / L.rows_per_cta);
+    cfg.blockDim = dim3(kK3Threads);
+    cfg.dynamicSmemBytes = L.k3_smem;
+    return cudaLaunchKernelEx(&cfg, chain_down_kernel<NT, Q8>, p);
+}
+
+ChainParams chain_params(const DecodeArgs& a, const ChainLayout& L) {
+    ChainParams p{};
+    p.rc.mode = (int)a.route.mode;
+    p.rc.E = a.route.n_experts;
+    p.rc.k = a.route.top_k;
+    p.rc.G = a.route.mode == MOE_ROUTE_SIGMOID_GROUP ? a.route.n_groups : 1;
+    p.rc.Gk = a.route.mode == MOE_ROUTE_SIGMOID_GROUP ? a.route.topk_groups : 1;
+    p.rc.renorm = a.route.renormalize;
+    p.rc.scale = a.route.routed_scale;
+    p.Wr = a.Wr; p.bias = a.bias; p.x = a.x; p.x_bf16 = a.x_bf16 ? 1 : 0;
+    p.T = a.T; p.H = a.H; p.I = a.I;
+    p.wg = a.wg; p.wu = a.wu; p.wd = a.wd;
+    p.stride_gu = a.stride_gu; p.stride_d = a.stride_d;
+    p.I_s = a.I_s; p.s_q8 = (a.I_s > 0 && a.s_qtype == MOE_Q8_0) ? 1 : 0;
+    p.sg = a.sg; p.su = a.su; p.sd = a.sd;
+    p.logits = a.logits; p.ids = a.ids; p.gw = a.gw; p.sorted = a.sorted; p.offsets = a.offsets;
+    p.pair_pos = a.pair_pos;
+    p.h = a.h; p.h_s = a.h_s; p.out = a.out; p.accumulate = a.accumulate ? 1 : 0;
+    p.hdr = a.hdr;
+    p.it_H_s = L.it_H_s; p.it_Is_s = L.it_Is_s;
+    p.k2_warps = L.k2_warps; p.k2_off_xs_s = L.k2_off_xs_s; p.k2_off_ring = L.k2_off_ring;
+    p.rows_per_cta = L.rows_per_cta; p.k3_prefetch = L.k3_prefetch;
+    p.k3_off_hs_s = L.k3_off_hs_s; p.k3_off_y = L.k3_off_y; p.k3_off_w = L.k3_off_w;
+    return p;
+}
+
+}  // namespace
+
+bool decode_chain_supported(const DecodeArgs& a) {
+    if (sm_count() <= 0) return false;
+    const int P = a.T * a.route.top_k;
+    if (a.T < 1 || a.T > kCMaxT || P > kCMaxP || a.route.n_experts > kCMaxE) return false;
+    if (a.qtype != MOE_Q4_K) return false;
+    if (a.H % kQ4KWeights || a.I % kQ4KWeights || a.H / 4 > kK1MaxVec * kK1Threads) return false;
+    if (a.I_s > 0) {
+        if (a.s_qtype == MOE_Q8_0) {
+            if (a.I_s % kQ80Weights || a.H % kQ80Weights || a.I_s % 2) return false;
+        } else if (a.s_qtype == MOE_Q4_K) {
+            if (a.I_s % kQ4KWeights) return false;
+        } else {
+            return false;
+        }
+    }
+    if ((a.stride_gu % 16) || (a.stride_d % 16)) return false;
+    const ChainLayout L = chain_layout(a);
+    return L.k2_warps >= 4 && L.k2_smem <= kChainSmemCap && L.k3_smem <= kChainSmemCap;
+}
+
+cudaError_t launch_decode_chain(const DecodeArgs& a, cudaStream_t s) {
+    const ChainLayout L = chain_layout(a);
+    const ChainParams p = chain_params(a, L);
+    const int E = a.route.n_experts;
+    const bool q8 = p.s_q8 != 0;
+    switch (a.T) {
+        case 1: return q8 ? launch_chain_nt<1, true>(p, L, E, s) : launch_chain_nt<1, false>(p, L, E, s);
+        case 2: return q8 ? launch_chain_nt<2, true>(p, L, E, s) : launch_chain_nt<2, false>(p, L, E, s);
+        default: return q8 ? launch_chain_nt<4, true>(p, L, E, s) : launch_chain_nt<4, false>(p, L, E, s);
+    }
+}
+
+}  // namespace moe

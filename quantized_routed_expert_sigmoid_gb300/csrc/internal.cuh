@@ -116,6 +116,9 @@ struct DecodeArgs {
     WsHeader* hdr;
 };
 bool decode_fused_supported(const DecodeArgs& a);
+// The same layer as three launches chained by programmatic dependent launch (decode_chain.cu).
+bool decode_chain_supported(const DecodeArgs& a);
+cudaError_t launch_decode_chain(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_init_header(WsHeader* hdr, cudaStream_t s);
 cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s);
 

@@ -433,66 +433,184 @@ __device__ __forceinline__ void qd4_stage(const void* src, bool bf16, bool coher
     }
 }
 
+// Same layout as qd4_stage, eight threads per 32-value sub-block (4 values each, max
+// and sum by butterfly within the 8), four loads in flight per thread.  nthr must
+// be a multiple of 32; every thread of [0, nthr) must call it.
+__device__ __forceinline__ void qd4_stage_par(const void* src, bool bf16, bool coherent, int64_t row_elems, int n,
+                                              const int* rows, int K, uint4* X, float4* XS, int tid, int nthr) {
+    const int G = qd4_groups(K);
+    const int total = n * G * 16;
+    constexpr int kU = 4;
+    for (int base = 0; base < total; base += kU * nthr) {
+        float4 v[kU];
+#pragma unroll
+        for (int j = 0; j < kU; ++j) {
+            const int s = base + j * nthr + tid;
+            v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (s < total) {
+                const int i = s / (16 * G), r = s - i * 16 * G;
+                const int sb = r >> 3, q8 = r & 7, g = sb >> 1, hh = sb & 1;
+                const int64_t row = rows ? rows[i] : i;
+                const int64_t e = row * row_elems + (g >> 2) * 256 + (2 * (g & 3) + hh) * 32 + 4 * q8;
+                if (bf16) {
+                    const uint2 raw = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(src) + e);
+                    v[j] = make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                                       __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
+                } else {
+                    const float4* p4 = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + e);
+                    v[j] = coherent ? __ldcg(p4) : *p4;
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kU; ++j) {
+            const int s = base + j * nthr + tid;
+            float m = fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w)));
+            float sum = (v[j].x + v[j].y) + (v[j].z + v[j].w);
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            }
+            if (s < total) {
+                const int i = s / (16 * G), r = s - i * 16 * G;
+                const int sb = r >> 3, q8 = r & 7, g = sb >> 1, hh = sb & 1;
+                const float inv = m > 0.f ? 8388607.0f / m : 0.f;
+                const float vv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+                uint32_t hw = 0, mw = 0, lw = 0;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    int x24 = __float2int_rn(vv[b] * inv);
+                    x24 = max(-8388607, min(8388607, x24));
+                    hw |= ((uint32_t)(x24 >> 16) & 0xFFu) << (8 * b);
+                    mw |= ((uint32_t)(x24 >> 8) & 0xFFu) << (8 * b);
+                    lw |= ((uint32_t)x24 & 0xFFu) << (8 * b);
+                }
+                X[(size_t)i * 16 * G + (hh * 8 + q8) * G + g] = make_uint4(hw, mw, lw, 0u);
+                if (q8 == 0) {
+                    float* xsf = reinterpret_cast<float*>(XS + (size_t)i * G + g);
+                    xsf[hh] = m / 8388607.0f;
+                    xsf[2 + hh] = sum;
+                }
+            }
+        }
+    }
+}
+
+// Scales of sub-blocks 2c and 2c+1 of a Q4_K block header.
+__device__ __forceinline__ void qd4_scales(const uint4& hd, int c, float (&fs)[2], float (&fm)[2]) {
+    const float d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
+    const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
+#pragma unroll
+    for (int s2 = 0; s2 < 2; ++s2) {
+        const int j = 2 * c + s2, jj = j & 3;
+        const uint32_t by = (hd.y >> (8 * jj)) & 0xFFu, bz = (hd.z >> (8 * jj)) & 0xFFu, bw = (hd.w >> (8 * jj)) & 0xFFu;
+        uint32_t sc, m;
+        if (j < 4) { sc = by & 63u; m = bz & 63u; }
+        else { sc = (bw & 15u) | ((by >> 6) << 4); m = (bw >> 4) | ((bz >> 6) << 4); }
+        fs[s2] = d * (float)sc;
+        fm[s2] = dmin * (float)m;
+    }
+}
+
+// One lane, one group g (64 weights: sub-blocks 2c, 2c+1 of super-block g/4, c = g%4),
+// RPL rows whose bytes are already loaded: hd = the 16-byte block header, q0/q1 = the
+// 32 quant bytes of the group.  acc[r0 + i][t] += row i . vector vidx[t] (t < nt); the
+// activation planes of the group are read once and serve every row.
+template <int NT, int RPL>
+__device__ __forceinline__ void qd4_group_math(const uint4 (&hd)[RPL], const uint4 (&q0)[RPL], const uint4 (&q1)[RPL],
+                                               const bool (&live)[RPL], int r0, int g, int G, const uint4* X,
+                                               const float4* XS, int nt, float (&acc)[4][NT], const int* vidx) {
+    const int c = g & 3;
+    uint32_t qw[RPL][8];
+    float fs[RPL][2], fm[RPL][2];
+#pragma unroll
+    for (int i = 0; i < RPL; ++i) {
+        qw[i][0] = q0[i].x; qw[i][1] = q0[i].y; qw[i][2] = q0[i].z; qw[i][3] = q0[i].w;
+        qw[i][4] = q1[i].x; qw[i][5] = q1[i].y; qw[i][6] = q1[i].z; qw[i][7] = q1[i].w;
+        qd4_scales(hd[i], c, fs[i], fm[i]);
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        if (t < nt) {
+            const int v = vidx ? vidx[t] : t;
+            const uint4* Xv = X + (size_t)v * 16 * G + g;
+            int ah[RPL][2], am[RPL][2], al[RPL][2];
+#pragma unroll
+            for (int i = 0; i < RPL; ++i) ah[i][0] = ah[i][1] = am[i][0] = am[i][1] = al[i][0] = al[i][1] = 0;
+#pragma unroll
+            for (int qd = 0; qd < 8; ++qd) {
+                const uint4 xl = Xv[qd * G], xh = Xv[(8 + qd) * G];
+#pragma unroll
+                for (int i = 0; i < RPL; ++i) {
+                    const uint32_t ql = qw[i][qd] & 0x0F0F0F0Fu, qh = (qw[i][qd] >> 4) & 0x0F0F0F0Fu;
+                    ah[i][0] = qd_dp4a_us(ql, xl.x, ah[i][0]);
+                    am[i][0] = qd_dp4a_uu(ql, xl.y, am[i][0]);
+                    al[i][0] = qd_dp4a_uu(ql, xl.z, al[i][0]);
+                    ah[i][1] = qd_dp4a_us(qh, xh.x, ah[i][1]);
+                    am[i][1] = qd_dp4a_uu(qh, xh.y, am[i][1]);
+                    al[i][1] = qd_dp4a_uu(qh, xh.z, al[i][1]);
+                }
+            }
+            const float4 xs = XS[(size_t)v * G + g];
+#pragma unroll
+            for (int i = 0; i < RPL; ++i) {
+                if (live[i]) {
+                    const float d0 = fmaf((float)ah[i][0], 65536.0f, fmaf((float)am[i][0], 256.0f, (float)al[i][0])) * xs.x;
+                    const float d1 = fmaf((float)ah[i][1], 65536.0f, fmaf((float)am[i][1], 256.0f, (float)al[i][1])) * xs.y;
+                    float part = fs[i][0] * d0;
+                    part = fmaf(fs[i][1], d1, part);
+                    part = fmaf(-fm[i][0], xs.z, part);
+                    part = fmaf(-fm[i][1], xs.w, part);
+#pragma unroll
+                    for (int rr = 0; rr < 4; ++rr)
+                        if (rr == r0 + i) acc[rr][t] += part;
+                }
+            }
+        }
+    }
+}
+
+// qd4_group_math with the rows' bytes read here (rows r0..r0+RPL-1 of rowp; NULL rows skipped).
+template <int NT, int RPL, bool kSmemRows>
+__device__ __forceinline__ void qd4_group(const uint8_t* const (&rowp)[4], int r0, int g, int G, const uint4* X,
+                                          const float4* XS, int nt, float (&acc)[4][NT], const int* vidx) {
+    const int b = g >> 2, c = g & 3;
+    uint4 hd[RPL], q0[RPL], q1[RPL];
+    bool live[RPL];
+#pragma unroll
+    for (int i = 0; i < RPL; ++i) {
+        const uint8_t* rp = rowp[r0 + i];
+        live[i] = rp != nullptr;
+        if (live[i]) {
+            const uint8_t* blk = rp + (int64_t)b * kQ4KBytes;
+            hd[i] = qd_ld16<kSmemRows>(blk);
+            q0[i] = qd_ld16<kSmemRows>(blk + 16 + 32 * c);
+            q1[i] = qd_ld16<kSmemRows>(blk + 32 + 32 * c);
+        } else {
+            hd[i] = q0[i] = q1[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    qd4_group_math<NT, RPL>(hd, q0, q1, live, r0, g, G, X, XS, nt, acc, vidx);
+}
+
 // acc[r][t] += row r . vector vidx[t] (t < nt) for 4 Q4_K rows of nblk super-blocks.
-// Rows may be NULL (skipped).  Vector v lives at X + v*16*G, XS + v*G.
+// Rows may be NULL (skipped).  Vector v lives at X + v*16*G, XS + v*G.  Lanes split
+// into row subsets so that every lane reuses one group's activations over 4, 2 or 1
+// rows (long rows: 4; 12-23 groups: 2; shorter: 1).
 template <int NT, bool kSmemRows = false>
 __device__ __forceinline__ void qd4_rows4(const uint8_t* const (&rowp)[4], int nblk, const uint4* X,
                                           const float4* XS, int nt, int lane, float (&acc)[4][NT],
                                           const int* vidx = nullptr) {
     const int G = nblk * 4;
-    for (int item = lane; item < 4 * G; item += 32) {
-        const int r = item / G, g = item - r * G;
-        const uint8_t* rp = r == 0 ? rowp[0] : r == 1 ? rowp[1] : r == 2 ? rowp[2] : rowp[3];
-        if (!rp) continue;
-        const int b = g >> 2, c = g & 3;
-        const uint8_t* blk = rp + (int64_t)b * kQ4KBytes;
-        const uint4 hd = qd_ld16<kSmemRows>(blk);
-        const uint4 q0 = qd_ld16<kSmemRows>(blk + 16 + 32 * c);
-        const uint4 q1 = qd_ld16<kSmemRows>(blk + 32 + 32 * c);
-        // scales of sub-blocks 2c and 2c+1
-        const float d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
-        const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
-        float fs[2], fm[2];
-#pragma unroll
-        for (int s2 = 0; s2 < 2; ++s2) {
-            const int j = 2 * c + s2, jj = j & 3;
-            const uint32_t by = (hd.y >> (8 * jj)) & 0xFFu, bz = (hd.z >> (8 * jj)) & 0xFFu, bw = (hd.w >> (8 * jj)) & 0xFFu;
-            uint32_t sc, m;
-            if (j < 4) { sc = by & 63u; m = bz & 63u; }
-            else { sc = (bw & 15u) | ((by >> 6) << 4); m = (bw >> 4) | ((bz >> 6) << 4); }
-            fs[s2] = d * (float)sc;
-            fm[s2] = dmin * (float)m;
-        }
-        const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            if (t < nt) {
-                const int v = vidx ? vidx[t] : t;
-                const uint4* Xv = X + (size_t)v * 16 * G + g;
-                int ah0 = 0, am0 = 0, al0 = 0, ah1 = 0, am1 = 0, al1 = 0;
-#pragma unroll
-                for (int qd = 0; qd < 8; ++qd) {
-                    const uint32_t ql = qw[qd] & 0x0F0F0F0Fu, qh = (qw[qd] >> 4) & 0x0F0F0F0Fu;
-                    const uint4 xl = Xv[qd * G], xh = Xv[(8 + qd) * G];
-                    ah0 = qd_dp4a_us(ql, xl.x, ah0);
-                    am0 = qd_dp4a_uu(ql, xl.y, am0);
-                    al0 = qd_dp4a_uu(ql, xl.z, al0);
-                    ah1 = qd_dp4a_us(qh, xh.x, ah1);
-                    am1 = qd_dp4a_uu(qh, xh.y, am1);
-                    al1 = qd_dp4a_uu(qh, xh.z, al1);
-                }
-                const float4 xs = XS[(size_t)v * G + g];
-                const float d0 = fmaf((float)ah0, 65536.0f, fmaf((float)am0, 256.0f, (float)al0)) * xs.x;
-                const float d1 = fmaf((float)ah1, 65536.0f, fmaf((float)am1, 256.0f, (float)al1)) * xs.y;
-                float part = fs[0] * d0;
-                part = fmaf(fs[1], d1, part);
-                part = fmaf(-fm[0], xs.z, part);
-                part = fmaf(-fm[1], xs.w, part);
-#pragma unroll
-                for (int rr = 0; rr < 4; ++rr)
-                    if (rr == r) acc[rr][t] += part;
-            }
-        }
+    if (G >= 24) {
+        for (int g = lane; g < G; g += 32) qd4_group<NT, 4, kSmemRows>(rowp, 0, g, G, X, XS, nt, acc, vidx);
+    } else if (G >= 12) {
+        const int rs = lane >> 4;
+        for (int g = lane & 15; g < G; g += 16) qd4_group<NT, 2, kSmemRows>(rowp, 2 * rs, g, G, X, XS, nt, acc, vidx);
+    } else {
+        const int rs = lane >> 3;
+        for (int g = lane & 7; g < G; g += 8) qd4_group<NT, 1, kSmemRows>(rowp, rs, g, G, X, XS, nt, acc, vidx);
     }
 }
 

@@ -34,8 +34,9 @@ struct RouteCfgDev {
 // order to ids[0..k) with their gates w[0..k).  sel, sv: 2*E floats of per-warp
 // shared memory.  lrow is read through L2 (it may have been written by other CTAs
 // of the same grid).
-__device__ __forceinline__ void warp_topk(const RouteCfgDev& c, const float* lrow, const float* bias, float* sel,
-                                          float* sv, int32_t* ids, float* w) {
+template <int kSlots>
+__device__ __forceinline__ void warp_topk_n(const RouteCfgDev& c, const float* lrow, const float* bias, float* sel,
+                                            float* sv, int32_t* ids, float* w) {
     const int lane = threadIdx.x & 31;
     const int E = c.E, k = c.k;
     const bool sig = (c.mode == MOE_ROUTE_SIGMOID_GROUP);
@@ -88,30 +89,36 @@ __device__ __forceinline__ void warp_topk(const RouteCfgDev& c, const float* lro
         __syncwarp();
     }
     // k rounds of arg-max over sel (larger first, ties to the lower id); lane r keeps the
-    // r-th pick.  Scores become order-preserving unsigned keys (-0 folded into +0) so each
-    // round is two warp reductions; a taken expert gets key 0, below every score.
-    int my_id = 0x7fffffff;
-    float my_val = 0.f;
-    for (int e = lane; e < E; e += 32) {
-        const uint32_t u = __float_as_uint(sel[e] + 0.0f);
-        reinterpret_cast<uint32_t*>(sel)[e] = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    // r-th pick.  Scores become order-preserving unsigned keys (-0 folded into +0) held in
+    // registers (element lane + 32*i in slot i); a round is a lane-local scan and two warp
+    // reductions, and a taken expert's key becomes 0, below every score.
+    uint32_t kv[kSlots];                              // E <= 32 * kSlots
+#pragma unroll
+    for (int i = 0; i < kSlots; ++i) {
+        const int e = lane + 32 * i;
+        uint32_t key = 0u;
+        if (e < E) {
+            const uint32_t u = __float_as_uint(sel[e] + 0.0f);
+            key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+        }
+        kv[i] = key;
     }
-    __syncwarp();
-    const uint32_t* key = reinterpret_cast<const uint32_t*>(sel);
+    int my_id = 0x7fffffff;
     for (int r = 0; r < k; ++r) {
         uint32_t best = 0u;
         int bid = 0x7fffffff;
-        for (int e = lane; e < E; e += 32) {
-            const uint32_t kv = key[e];
-            if (kv > best || bid == 0x7fffffff) { best = kv; bid = e; }   // ascending e: ties keep the lower id
-        }
+#pragma unroll
+        for (int i = 0; i < kSlots; ++i)
+            if (kv[i] > best) { best = kv[i]; bid = lane + 32 * i; }   // ascending id: ties keep the lower
         const uint32_t top = __reduce_max_sync(0xffffffffu, best);
         int id = (int)__reduce_min_sync(0xffffffffu, best == top ? (uint32_t)bid : 0x7fffffffu);
         if (id >= E) id = 0;
-        if (lane == r) { my_id = id; my_val = sv[id]; }
-        if (lane == 0) reinterpret_cast<uint32_t*>(sel)[id] = 0u;
-        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < kSlots; ++i)
+            if (lane + 32 * i == id) kv[i] = 0u;
+        if (lane == r) my_id = id;
     }
+    const float my_val = lane < k ? sv[my_id] : 0.f;
     float num = 0.f, den;
     if (sig) {
         num = lane < k ? my_val : 0.f;
@@ -137,6 +144,14 @@ __device__ __forceinline__ void warp_topk(const RouteCfgDev& c, const float* lro
         w[rank] = c.scale * (num / den);
     }
     __syncwarp();
+}
+
+// Same, with the key registers sized for E (E <= 1024).
+__device__ __forceinline__ void warp_topk(const RouteCfgDev& c, const float* lrow, const float* bias, float* sel,
+                                          float* sv, int32_t* ids, float* w) {
+    if (c.E <= 128) warp_topk_n<4>(c, lrow, bias, sel, sv, ids, w);
+    else if (c.E <= 256) warp_topk_n<8>(c, lrow, bias, sel, sv, ids, w);
+    else warp_topk_n<32>(c, lrow, bias, sel, sv, ids, w);
 }
 
 }  // namespace moe

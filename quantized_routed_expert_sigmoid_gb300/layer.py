@@ -54,6 +54,10 @@ class MoeLayer:
         self.ws = None
         self.ws_T = -1
 
+    def path(self, T: int) -> str:
+        """Which kernels a call with T tokens runs: "gemv", "fused_decode" or "tensor"."""
+        return N.PATH_NAMES[N.moe_layer_path(self.plan, T)]
+
     def workspace_bytes(self, T: int) -> int:
         return N.moe_layer_workspace_size(self.plan, T)
 

@@ -199,41 +199,53 @@ def test_tc_matches_gemv_path():
     assert rel_l2(o_tc, o_gv) <= TOL_TC
 
 
-# ---------------------------------------------------------------- single-launch decode layer (T <= 4)
+# ---------------------------------------------------------------- chained decode kernels (T <= 4)
 
-def _fused_vs_separate(tl, T):
-    """The single-launch layer and the separate kernels give the same bits and ids."""
-    fused = tl.moe_layer()
+def _chain_vs_separate(tl, T):
+    """The chained decode kernels and the separate kernels: same routing, same pair
+    lists; outputs equal up to summation order (both accumulate in fp32)."""
+    chain = tl.moe_layer()
     sep = tl.moe_layer()
     sep.desc.decode_fused_off = 1
     sep.rebuild_plan()
+    assert chain.path(T) == "fused_decode" and sep.path(T) == "gemv"
     x = tl.x.cuda()
-    o_f = fused(x).clone()
+    o_c = chain(x).clone()
     o_s = sep(x).clone()
     torch.cuda.synchronize()
-    assert torch.equal(o_f, o_s), "fused decode layer differs from the separate kernels"
-    for a, b in zip(fused.debug_views(T), sep.debug_views(T)):
-        assert torch.equal(a, b)
-    assert fused.device_status(T) == 0
+    (ids_c, gw_c, off_c), (ids_s, gw_s, off_s) = chain.debug_views(T), sep.debug_views(T)
+    assert torch.equal(ids_c, ids_s) and torch.equal(off_c, off_s)
+    # the router logits are summed in another order: gates agree to rounding
+    assert torch.allclose(gw_c, gw_s, rtol=1e-5, atol=0)
+    err = rel_l2(o_c.cpu().numpy(), o_s.cpu().double().numpy())
+    assert err <= 2e-6, f"chain vs separate kernels: rel-L2 {err:.3e}"
+    assert chain.device_status(T) == 0
 
 
 @pytest.mark.parametrize("T", [1, 2, 3, 4])
-def test_fused_decode_matches_separate_kernels(T):
-    _fused_vs_separate(make_layer(synth.DECODE, 50 + T, T), T)
+def test_decode_chain_matches_separate_kernels(T):
+    _chain_vs_separate(make_layer(synth.DECODE, 50 + T, T), T)
 
 
-def test_fused_decode_deepseek_shape_and_tiny():
-    _fused_vs_separate(make_layer(synth.DEEPSEEK, 60, 2), 2)
-    _fused_vs_separate(make_layer(synth.TINY, 61, 3, exact_all=True), 3)
+def test_decode_chain_deepseek_shape():
+    _chain_vs_separate(make_layer(synth.DEEPSEEK, 60, 2), 2)
 
 
-def test_fused_decode_needs_prepared_workspace():
+def test_decode_chain_q4k_shared_expert():
+    shape = synth.LayerShape(H=512, E=32, k=4, I=256, qtype=synth.Q4_K, mode="sigmoid_group", n_groups=4,
+                             topk_groups=2, scale=2.5, I_s=512, shared_qtype=synth.Q4_K, bias_std=0.1)
+    tl = make_layer(shape, 63, 3, exact_all=True)
+    _chain_vs_separate(tl, 3)
+    _check_layer(tl, 3)
+
+
+def test_decode_chain_needs_prepared_workspace():
     import quantized_routed_expert_sigmoid_gb300 as moe
-    tl = make_layer(synth.TINY, 62, 1, exact_all=True)
+    tl = make_layer(synth.DECODE, 62, 1)
     layer = tl.moe_layer()
     nbytes = layer.workspace_bytes(1)
     raw = torch.empty(nbytes, dtype=torch.uint8, device="cuda")     # never prepared
-    out = torch.empty(1, synth.TINY.H, device="cuda")
+    out = torch.empty(1, synth.DECODE.H, device="cuda")
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_layer(layer.plan, tl.x.cuda(), 1, out, raw, nbytes)
     assert ei.value.status == moe.MOE_ERR_WORKSPACE
