@@ -13,18 +13,20 @@
 //   K1 logits   one CTA per expert row: the T router logits of that expert.
 //   K2 gate/up  every CTA selects the top-k of the T tokens itself (identical
 //               results everywhere; CTA 0 publishes them), then a persistent
-//               grid runs (active expert, row pair) units: each warp requests
-//               all the weight bytes of its units at once (per-lane cp.async
-//               into a two-slot ring in shared memory) and computes
+//               grid runs (active expert, row pair) units: each warp streams
+//               its units' rows through a two-slot ring in shared memory (bulk
+//               copies, one mbarrier per slot) and computes
 //               h = silu(gate . x) * (up . x) as they land; the shared
 //               expert's rows follow.  Each CTA also requests its share of the
 //               chosen down rows into L2.
 //   K3 down     one CTA per block of output rows: its down rows of every pair
-//               go to shared memory while h is staged, then the dot products,
-//               the gate-weighted combine in fixed order (+ shared, + residual).
+//               go to shared memory (one bulk copy per pair) while h is
+//               staged, then the dot products and the gate-weighted combine in
+//               fixed order (+ shared, + residual).
 // Dot products use the integer Q4_K walk of qdot.cuh; every reduction has a
 // fixed order, so a replay gives the same bits.
 #include <algorithm>
+#include <type_traits>
 
 #include "internal.cuh"
 #include "qdot.cuh"
@@ -39,7 +41,9 @@ constexpr int kCMaxE = 256;
 constexpr int kK1Threads = 128;
 constexpr int kK3Threads = 256;
 constexpr int kK1MaxVec = 16;              // float4 of a router row per K1 thread: H <= 8192
-constexpr int kSlotU4 = 4 * 3 * 32;        // ring slot: 4 rows x 3 uint4 x 32 lanes
+constexpr int kChunkBlocks = 8;            // ring item: 8 Q4_K blocks (32 groups) of 4 rows
+constexpr int kSlotBytes = 4 * kChunkBlocks * kQ4KBytes;
+constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kK2MaxWarps = 16;
 
 struct ChainParams {
@@ -93,14 +97,60 @@ __device__ __forceinline__ void prefetch_l2(const uint8_t* src, int64_t bytes) {
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src + o), "r"(n) : "memory");
     }
 }
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+__device__ __forceinline__ float4 ld_nc_v4(const float4* q) {
+    float4 v;
+    asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(q));
+    return v;
+}
+__device__ __forceinline__ uint32_t smem_u32(const void* q) { return (uint32_t)__cvta_generic_to_shared(q); }
+__device__ __forceinline__ uint64_t gtime() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    // the suspend-time hint lets the warp sleep until the phase completes (or ~0.1 ms pass)
+    asm volatile("{\n .reg .pred q;\n mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2, %3;\n selp.u32 %0, 1, 0, q;\n}\n"
+                 : "=r"(ok)
+                 : "r"(smem_u32(b)), "r"(parity), "r"(100000u)
+                 : "memory");
+    return ok != 0;
+}
+// Waits for the phase of parity `parity` to complete; false after kWaitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
+    if (mbar_test(b, parity)) return true;
+    const uint64_t t0 = gtime();
+    while (!mbar_test(b, parity))
+        if (gtime() - t0 > kWaitNs) return false;
+    return true;
+}
+constexpr int kCluster = 8;                 // K3 CTAs per cluster (they share the staged h)
+__device__ __forceinline__ int cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return (int)r;
+}
+// Stores v at the address of *a in the shared memory of cluster CTA `peer`.
+__device__ __forceinline__ void st_peer(const uint4* a, int peer, const uint4& v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(a)), "r"(peer));
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
                  : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// A bulk copy global -> shared whose bytes complete the transaction count of bar.
+__device__ __forceinline__ void bulk_to_smem(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
 
 // Every thread of the CTA calls this.  Warp t < T selects token t's experts from the
 // logits (read through L2: another grid wrote them); warp 0 then orders the pairs by
@@ -160,11 +210,13 @@ __global__ void __launch_bounds__(kK1Threads) chain_logits_kernel(const __grid_c
     const int e = blockIdx.x, E = p.rc.E, T = p.T, H = p.H;
     const int n4 = H / 4;
     // the router row: a weight, independent of the launches before this one
+    // (volatile loads: issued here, ahead of the wait, not moved past it)
     float4 w[kK1MaxVec];
 #pragma unroll
     for (int i = 0; i < kK1MaxVec; ++i) {
         const int j = tid + i * kK1Threads;
-        w[i] = j < n4 ? __ldg(reinterpret_cast<const float4*>(p.Wr + (int64_t)e * H) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        w[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j < n4) w[i] = ld_nc_v4(reinterpret_cast<const float4*>(p.Wr + (int64_t)e * H) + j);
     }
     pdl_wait();                                   // x and the workspace belong to the launches before
     pdl_launch_dependents();
@@ -208,7 +260,7 @@ __global__ void __launch_bounds__(kK1Threads) chain_logits_kernel(const __grid_c
 // into chunks of 32 groups (64 weights each; lane = group in the chunk).  Warp w of the
 // grid takes units w, w + W, ...; every chunk of its units streams through the warp's
 // two ring slots (each lane copies and later reads only its own 16-byte pieces).
-template <int NT, bool kSharedQ8>
+template <int NT, int kSh>
 __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const __grid_constant__ ChainParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ CtaRoute R;
@@ -216,15 +268,22 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
     const int nthr = blockDim.x;
     const int T = p.T, H = p.H, I = p.I, k = p.rc.k, E = p.rc.E, P = T * k;
     const int G = qd4_groups(H);
-    const bool has_shared = p.I_s > 0;
+    constexpr bool has_shared = kSh != 0;
     uint4* X = reinterpret_cast<uint4*>(smem);
     float4* XS = reinterpret_cast<float4*>(X + (size_t)T * 16 * G);
     float4* xs_s = reinterpret_cast<float4*>(smem + p.k2_off_xs_s);
-    uint4* ring = reinterpret_cast<uint4*>(smem + p.k2_off_ring) + (size_t)warp * 2 * kSlotU4;
+    uint8_t* ring = smem + p.k2_off_ring + (size_t)warp * 2 * kSlotBytes;
+    __shared__ __align__(8) uint64_t s_bar[kK2MaxWarps][2];
+    if (lane == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar[warp][0])) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar[warp][1])) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
     const bool xb = p.x_bf16 != 0;
     // ---- x is the input of the whole chain: stage it before waiting
     qd4_stage_par(p.x, xb, false, H, T, nullptr, H, X, XS, tid, nthr);
-    if (kSharedQ8 && has_shared) {
+    if (kSh == 2) {
         const int slots = p.it_H_s * 256;
         for (int t = 0; t < T; ++t) {
             const void* src = xb ? (const void*)(reinterpret_cast<const __nv_bfloat16*>(p.x) + (int64_t)t * H)
@@ -252,26 +311,24 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
         const uint8_t* ub = p.wu + (int64_t)R.act_e[a] * p.stride_gu + r0 * rbH;
         rowp[0] = gb; rowp[1] = ub; rowp[2] = gb + rbH; rowp[3] = ub + rbH;
     };
+    const int nblk = H / kQ4KWeights;
+    // lane 0 puts item `item` (its 4 rows' blocks [8*ch, 8*ch + 8)) into slot item & 1
     auto issue = [&](int item) {
-        if (item < n_items) {
-            const int u = wg + (item / nch) * W, ch = item - (item / nch) * nch;
-            const int g = ch * 32 + lane;
-            if (g < G) {
-                const uint8_t* rowp[4];
-                unit_rows(u, rowp);
-                uint4* sl = ring + (item & 1) * kSlotU4 + lane;
+        if (lane != 0 || item >= n_items) return;
+        const int u = wg + (item / nch) * W, ch = item - (item / nch) * nch;
+        const int b0 = ch * kChunkBlocks, nb = min(kChunkBlocks, nblk - b0);
+        const uint32_t bytes = (uint32_t)nb * kQ4KBytes;
+        const uint8_t* rowp[4];
+        unit_rows(u, rowp);
+        uint8_t* dst = ring + (item & 1) * kSlotBytes;
+        uint64_t* bar = &s_bar[warp][item & 1];
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(4 * bytes)
+                     : "memory");
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const uint8_t* blk = rowp[r] + (int64_t)(g >> 2) * kQ4KBytes;
-                    cp_async16(sl + (r * 3 + 0) * 32, blk);
-                    cp_async16(sl + (r * 3 + 1) * 32, blk + 16 + 32 * (g & 3));
-                    cp_async16(sl + (r * 3 + 2) * 32, blk + 32 + 32 * (g & 3));
-                }
-            }
-        }
-        cp_async_commit();
+        for (int r = 0; r < 4; ++r)
+            bulk_to_smem(dst + r * kChunkBlocks * kQ4KBytes, rowp[r] + (int64_t)b0 * kQ4KBytes, bytes, bar);
     };
-    // all of this warp's first two chunks go out before anything else
+    // this warp's first two items go out before anything else
     issue(0);
     issue(1);
     // ---- this CTA's share of the chosen down rows (and the shared expert's) into L2
@@ -304,8 +361,10 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
     float acc[4][NT];
     int n = 0, st = 0;
     int vidx[NT];
-    for (int item = 0; item < n_items; ++item) {
-        cp_async_wait<1>();                        // this item's group has landed (the next may be in flight)
+    bool ok = true;
+    int item = 0;
+    for (; item < n_items; ++item) {
+        if (!mbar_wait(&s_bar[warp][item & 1], (uint32_t)(item >> 1) & 1u)) { ok = false; break; }
         const int u = wg + (item / nch) * W, ch = item - (item / nch) * nch;
         if (ch == 0) {
 #pragma unroll
@@ -320,18 +379,21 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
         }
         const int g = ch * 32 + lane;
         if (g < G) {
-            const uint4* sl = ring + (item & 1) * kSlotU4 + lane;
+            const uint8_t* blk = ring + (item & 1) * kSlotBytes + (lane >> 2) * kQ4KBytes;
+            const int c = lane & 3;
             uint4 hd[4], q0[4], q1[4];
             const bool live[4] = {true, true, true, true};
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
-                hd[r] = sl[(r * 3 + 0) * 32];
-                q0[r] = sl[(r * 3 + 1) * 32];
-                q1[r] = sl[(r * 3 + 2) * 32];
+                const uint8_t* rb = blk + r * kChunkBlocks * kQ4KBytes;
+                hd[r] = *reinterpret_cast<const uint4*>(rb);
+                q0[r] = *reinterpret_cast<const uint4*>(rb + 16 + 32 * c);
+                q1[r] = *reinterpret_cast<const uint4*>(rb + 32 + 32 * c);
             }
             qd4_group_math<NT, 4>(hd, q0, q1, live, 0, g, G, X, XS, n, acc, vidx);
         }
-        issue(item + 2);                           // refills the slot just read
+        __syncwarp();                              // every lane is done with the slot
+        issue(item + 2);
         if (ch == nch - 1) {
             qd_warp_reduce<NT>(acc);
             if (lane < 2 * NT) {
@@ -344,8 +406,17 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
             }
         }
     }
-    cp_async_wait<0>();
+    if (!ok) {
+        // a copy never completed: report it, and let no copy land after the CTA exits
+        if (lane == 0) {
+            atomicExch(&p.hdr->status, (int)MOE_ERR_TIMEOUT);
+            for (int i = item; i < min(item + 2, n_items); ++i) mbar_wait(&s_bar[warp][i & 1], (uint32_t)(i >> 1) & 1u);
+        }
+        __syncwarp();
+        return;
+    }
     // ---- the shared expert's row pairs (direct loads)
+    if constexpr (has_shared) {
     for (int u = wg + my_units * W; u < Ur + Us; u += W) {
         if (u < Ur) continue;
         float sacc[4][NT];
@@ -357,7 +428,7 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
         int sv[NT];
 #pragma unroll
         for (int t = 0; t < NT; ++t) sv[t] = min(t, T - 1);
-        if (kSharedQ8) {
+        if (kSh == 2) {
             const int64_t rbS = (int64_t)(H / kQ80Weights) * kQ80Bytes;
             const uint8_t* const rowp[4] = {p.sg + r0 * rbS, p.sg + (r0 + 1) * rbS, p.su + r0 * rbS,
                                             p.su + (r0 + 1) * rbS};
@@ -377,21 +448,23 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
             }
         }
     }
+    }
 }
 
 // ============================================================================ K3: down + combine
 // CTA c owns output rows [c*R, c*R + R).  Tasks: (pair s, 8 rows) with lane = 4*row + sub
 // and sub taking groups sub, sub+4, ...; then the shared expert's rows 4 at a time.
-template <int NT, bool kSharedQ8>
+template <int NT, int kSh>
 __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_constant__ ChainParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ int32_t s_e[kCMaxP], s_pos[kCMaxP];
     __shared__ float s_w[kCMaxP];
+    __shared__ __align__(8) uint64_t s_wbar;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = p.T, H = p.H, I = p.I, k = p.rc.k, P = T * k;
     const int GI = qd4_groups(I);
     const int R = p.rows_per_cta, n0 = blockIdx.x * R;
-    const bool has_shared = p.I_s > 0;
+    constexpr bool has_shared = kSh != 0;
     const int64_t rbI = (int64_t)(I / kQ4KWeights) * kQ4KBytes;
     uint4* HX = reinterpret_cast<uint4*>(smem);
     float4* HXS = reinterpret_cast<float4*>(HX + (size_t)P * 16 * GI);
@@ -399,39 +472,79 @@ __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_con
     uint8_t* wbuf = smem + p.k3_off_w;                                   // [P][R][rbI] when prefetching
     pdl_wait();                                   // h and the routing of K2
     pdl_launch_dependents();
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_wbar)) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
     for (int i = tid; i < P; i += kK3Threads) {
         s_e[i] = __ldcg(p.ids + i);
         s_pos[i] = __ldcg(p.pair_pos + i);
         s_w[i] = __ldcg(p.gw + i);
     }
     __syncthreads();
-    // ---- the CTA's down rows of every pair to shared memory (in flight while h is staged)
+    // ---- the CTA's down rows of every pair to shared memory (in flight while h is staged):
+    // rows n0.. of one expert are contiguous, one bulk copy per pair
     const int nrows = min(R, H - n0);
-    if (p.k3_prefetch) {
-        const int per_row = (int)(rbI / 16);
-        const int total = P * nrows * per_row;
-        for (int c = tid; c < total; c += kK3Threads) {
-            const int s = c / (nrows * per_row), rem = c - s * nrows * per_row;
-            const int r = rem / per_row, o = rem - r * per_row;
-            cp_async16(wbuf + ((int64_t)s * R + r) * rbI + 16 * o,
-                       p.wd + (int64_t)s_e[s] * p.stride_d + (int64_t)(n0 + r) * rbI + 16 * o);
-        }
-        cp_async_commit();
+    if (p.k3_prefetch && tid == 0 && nrows > 0) {
+        const uint32_t bytes = (uint32_t)(nrows * rbI);
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&s_wbar)), "r"(P * bytes)
+                     : "memory");
+        for (int s = 0; s < P; ++s)
+            bulk_to_smem(wbuf + (int64_t)s * R * rbI, p.wd + (int64_t)s_e[s] * p.stride_d + (int64_t)n0 * rbI, bytes,
+                         &s_wbar);
     }
-    // ---- stage every pair's h (row pair_pos[s] of h) and the shared expert's h_s
-    qd4_stage_par(p.h, false, true, I, P, s_pos, I, HX, HXS, tid, kK3Threads);
-    if (has_shared) {
-        if (kSharedQ8) {
-            float4* hs = reinterpret_cast<float4*>(smem + p.k3_off_hs_s);
-            qd_stage_many_f32<MOE_Q8_0>(p.h_s, p.I_s, T, p.I_s, p.it_Is_s, hs, tid, kK3Threads);
-        } else {
-            uint4* SX = reinterpret_cast<uint4*>(smem + p.k3_off_hs_s);
-            float4* SXS = reinterpret_cast<float4*>(SX + (size_t)T * 16 * qd4_groups(p.I_s));
-            qd4_stage_par(p.h_s, false, true, p.I_s, T, nullptr, p.I_s, SX, SXS, tid, kK3Threads);
-        }
+    // ---- stage every pair's h (row pair_pos[s] of h) and the shared expert's h_s.  The CTAs
+    // of a cluster split the vectors (rank r takes s = r, r + kCluster, ...), stage them,
+    // and write the planes into every CTA of the cluster.
+    const int rank = cluster_rank();
+    for (int s = rank; s < P; s += kCluster)
+        qd4_stage_par(p.h, false, true, I, 1, &s_pos[s], I, HX + (size_t)s * 16 * GI, HXS + (size_t)s * GI, tid,
+                      kK3Threads);
+    uint4* SX = reinterpret_cast<uint4*>(smem + p.k3_off_hs_s);
+    const int GS = kSh == 1 ? qd4_groups(p.I_s) : 1;
+    float4* SXS = reinterpret_cast<float4*>(SX + (size_t)T * 16 * GS);
+    if constexpr (kSh == 2) {
+        float4* hs = reinterpret_cast<float4*>(smem + p.k3_off_hs_s);
+        qd_stage_many_f32<MOE_Q8_0>(p.h_s, p.I_s, T, p.I_s, p.it_Is_s, hs, tid, kK3Threads);
+    } else if constexpr (kSh == 1) {
+        for (int t = rank; t < T; t += kCluster)
+            qd4_stage_par(p.h_s + (int64_t)t * p.I_s, false, true, p.I_s, 1, nullptr, p.I_s, SX + (size_t)t * 16 * GS,
+                          SXS + (size_t)t * GS, tid, kK3Threads);
     }
-    cp_async_wait<0>();
     __syncthreads();
+    {
+        const int per_x = 16 * GI, per_s = GI;        // uint4 / float4 per staged vector
+        for (int s = rank; s < P; s += kCluster) {
+            for (int i = tid; i < per_x + per_s; i += kK3Threads) {
+                uint4* a = i < per_x ? HX + (size_t)s * per_x + i
+                                     : reinterpret_cast<uint4*>(HXS + (size_t)s * per_s + (i - per_x));
+                const uint4 v = *a;
+                for (int q = 1; q < kCluster; ++q) st_peer(a, (rank + q) % kCluster, v);
+            }
+        }
+        if constexpr (kSh == 1) {
+            const int sx_x = 16 * GS, sx_s = GS;
+            for (int t = rank; t < T; t += kCluster) {
+                for (int i = tid; i < sx_x + sx_s; i += kK3Threads) {
+                    uint4* a = i < sx_x ? SX + (size_t)t * sx_x + i
+                                        : reinterpret_cast<uint4*>(SXS + (size_t)t * sx_s + (i - sx_x));
+                    const uint4 v = *a;
+                    for (int q = 1; q < kCluster; ++q) st_peer(a, (rank + q) % kCluster, v);
+                }
+            }
+        }
+    }
+    cluster_sync();                                   // every plane of every vector is in every CTA
+    const bool landed = !p.k3_prefetch || nrows <= 0 || mbar_wait(&s_wbar, 0u);
+    if (__syncthreads_or(!landed)) {
+        // the copies did not complete in time: report it; let none land after the CTA exits
+        if (tid == 0) {
+            atomicExch(&p.hdr->status, (int)MOE_ERR_TIMEOUT);
+            mbar_wait(&s_wbar, 0u);
+        }
+        __syncthreads();
+        return;
+    }
     const int nsub = R / 8;
     const int n_routed = P * nsub;
     const int n_shared = has_shared ? R / 4 : 0;
@@ -456,7 +569,7 @@ __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_con
             v += __shfl_xor_sync(0xffffffffu, v, 1);
             v += __shfl_xor_sync(0xffffffffu, v, 2);
             if (sub == 0) ybuf[s * R + rl] = v;
-        } else {
+        } else if constexpr (has_shared) {
             const int q = task - n_routed;
             const int nb = n0 + 4 * q;
             float acc[4][NT];
@@ -467,7 +580,7 @@ __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_con
             int vidx[NT];
 #pragma unroll
             for (int t = 0; t < NT; ++t) vidx[t] = min(t, T - 1);
-            if (kSharedQ8) {
+            if (kSh == 2) {
                 const int64_t rbS = (int64_t)(p.I_s / kQ80Weights) * kQ80Bytes;
                 const uint8_t* rowp[4];
 #pragma unroll
@@ -480,8 +593,6 @@ __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_con
                 const uint8_t* rowp[4];
 #pragma unroll
                 for (int r = 0; r < 4; ++r) rowp[r] = nb + r < H ? p.sd + (int64_t)(nb + r) * rbS : nullptr;
-                const uint4* SX = reinterpret_cast<const uint4*>(smem + p.k3_off_hs_s);
-                const float4* SXS = reinterpret_cast<const float4*>(SX + (size_t)T * 16 * qd4_groups(p.I_s));
                 qd4_rows4<NT, false>(rowp, p.I_s / kQ4KWeights, SX, SXS, T, lane, acc, vidx);
             }
             qd_warp_reduce<NT>(acc);
@@ -536,8 +647,8 @@ ChainLayout chain_layout(const DecodeArgs& a) {
     size_t o = (size_t)T * qd4_vec_bytes(H);
     L.k2_off_xs_s = (int)align_up(o, 16);
     o = L.k2_off_xs_s + (q8 ? (size_t)T * L.it_H_s * 4096 : 0);
-    L.k2_off_ring = (int)align_up(o, 16);
-    const size_t per_warp = (size_t)2 * kSlotU4 * 16;
+    L.k2_off_ring = (int)align_up(o, 128);
+    const size_t per_warp = (size_t)2 * kSlotBytes;
     int warps = kK2MaxWarps;
     while (warps > 1 && L.k2_off_ring + warps * per_warp > kChainSmemCap) --warps;
     L.k2_warps = warps;
@@ -559,7 +670,7 @@ ChainLayout chain_layout(const DecodeArgs& a) {
     return L;
 }
 
-template <int NT, bool Q8>
+template <int NT, int Q8>
 cudaError_t launch_chain_nt(const ChainParams& p, const ChainLayout& L, int E, cudaStream_t s) {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -583,9 +694,18 @@ cudaError_t launch_chain_nt(const ChainParams& p, const ChainLayout& L, int E, c
     if ((err = cudaFuncSetAttribute(chain_down_kernel<NT, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)L.k3_smem)) != cudaSuccess)
         return err;
-    cfg.gridDim = dim3((p.H + L.rows_per_cta - 1) / L.rows_per_cta);
+    const int n3 = (p.H + L.rows_per_cta - 1) / L.rows_per_cta;
+    cfg.gridDim = dim3((n3 + kCluster - 1) / kCluster * kCluster);
     cfg.blockDim = dim3(kK3Threads);
     cfg.dynamicSmemBytes = L.k3_smem;
+    cudaLaunchAttribute attr3[2];
+    attr3[0] = attr[0];
+    attr3[1].id = cudaLaunchAttributeClusterDimension;
+    attr3[1].val.clusterDim.x = kCluster;
+    attr3[1].val.clusterDim.y = 1;
+    attr3[1].val.clusterDim.z = 1;
+    cfg.attrs = attr3;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, chain_down_kernel<NT, Q8>, p);
 }
 
@@ -641,11 +761,16 @@ cudaError_t launch_decode_chain(const DecodeArgs& a, cudaStream_t s) {
     const ChainLayout L = chain_layout(a);
     const ChainParams p = chain_params(a, L);
     const int E = a.route.n_experts;
-    const bool q8 = p.s_q8 != 0;
+    const int sh = a.I_s <= 0 ? 0 : p.s_q8 ? 2 : 1;
+    auto go = [&](auto nt) -> cudaError_t {
+        constexpr int NT = decltype(nt)::value;
+        return sh == 0 ? launch_chain_nt<NT, 0>(p, L, E, s) : sh == 1 ? launch_chain_nt<NT, 1>(p, L, E, s)
+                                                                       : launch_chain_nt<NT, 2>(p, L, E, s);
+    };
     switch (a.T) {
-        case 1: return q8 ? launch_chain_nt<1, true>(p, L, E, s) : launch_chain_nt<1, false>(p, L, E, s);
-        case 2: return q8 ? launch_chain_nt<2, true>(p, L, E, s) : launch_chain_nt<2, false>(p, L, E, s);
-        default: return q8 ? launch_chain_nt<4, true>(p, L, E, s) : launch_chain_nt<4, false>(p, L, E, s);
+        case 1: return go(std::integral_constant<int, 1>{});
+        case 2: return go(std::integral_constant<int, 2>{});
+        default: return go(std::integral_constant<int, 4>{});
     }
 }
 

@@ -433,23 +433,33 @@ __device__ __forceinline__ void qd4_stage(const void* src, bool bf16, bool coher
     }
 }
 
-// Same layout as qd4_stage, eight threads per 32-value sub-block (4 values each, max
-// and sum by butterfly within the 8), four loads in flight per thread.  nthr must
-// be a multiple of 32; every thread of [0, nthr) must call it.
+// Same layout as qd4_stage.  Work is split in chunks of 32 values (4 sub-blocks of 8
+// threads, 4 values per thread, max and sum by butterfly within the 8); warp w of nw
+// takes chunks w, w + nw, ... with four chunks' loads in flight.  Every lane of every
+// warp in [0, nw) must call it.
 __device__ __forceinline__ void qd4_stage_par(const void* src, bool bf16, bool coherent, int64_t row_elems, int n,
                                               const int* rows, int K, uint4* X, float4* XS, int tid, int nthr) {
     const int G = qd4_groups(K);
-    const int total = n * G * 16;
+    const int lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
+    const int cpv = G / 2;                            // chunks per vector (G = K/64 is a multiple of 4)
+    const int total = n * cpv;
     constexpr int kU = 4;
-    for (int base = 0; base < total; base += kU * nthr) {
+    const int sbl = lane >> 3, q8 = lane & 7;         // sub-block within the chunk, quad within it
+    for (int c0 = warp; c0 < total; c0 += kU * nw) {
         float4 v[kU];
+        int iv[kU], sbv[kU];
 #pragma unroll
         for (int j = 0; j < kU; ++j) {
-            const int s = base + j * nthr + tid;
+            const int c = c0 + j * nw;
             v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (s < total) {
-                const int i = s / (16 * G), r = s - i * 16 * G;
-                const int sb = r >> 3, q8 = r & 7, g = sb >> 1, hh = sb & 1;
+            iv[j] = -1;
+            sbv[j] = 0;
+            if (c < total) {
+                const int i = c / cpv;
+                const int sb = (c - i * cpv) * 4 + sbl;   // sub-block index 0..2G-1 in the vector
+                iv[j] = i;
+                sbv[j] = sb;
+                const int g = sb >> 1, hh = sb & 1;
                 const int64_t row = rows ? rows[i] : i;
                 const int64_t e = row * row_elems + (g >> 2) * 256 + (2 * (g & 3) + hh) * 32 + 4 * q8;
                 if (bf16) {
@@ -464,7 +474,7 @@ __device__ __forceinline__ void qd4_stage_par(const void* src, bool bf16, bool c
         }
 #pragma unroll
         for (int j = 0; j < kU; ++j) {
-            const int s = base + j * nthr + tid;
+            if (c0 + j * nw >= total) break;              // warp-uniform
             float m = fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w)));
             float sum = (v[j].x + v[j].y) + (v[j].z + v[j].w);
 #pragma unroll
@@ -472,45 +482,50 @@ __device__ __forceinline__ void qd4_stage_par(const void* src, bool bf16, bool c
                 m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
                 sum += __shfl_xor_sync(0xffffffffu, sum, o);
             }
-            if (s < total) {
-                const int i = s / (16 * G), r = s - i * 16 * G;
-                const int sb = r >> 3, q8 = r & 7, g = sb >> 1, hh = sb & 1;
-                const float inv = m > 0.f ? 8388607.0f / m : 0.f;
-                const float vv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-                uint32_t hw = 0, mw = 0, lw = 0;
+            const int i = iv[j], sb = sbv[j], g = sb >> 1, hh = sb & 1;
+            const float inv = m > 0.f ? 8388607.0f / m : 0.f;
+            const float vv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+            uint32_t hw = 0, mw = 0, lw = 0;
 #pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    int x24 = __float2int_rn(vv[b] * inv);
-                    x24 = max(-8388607, min(8388607, x24));
-                    hw |= ((uint32_t)(x24 >> 16) & 0xFFu) << (8 * b);
-                    mw |= ((uint32_t)(x24 >> 8) & 0xFFu) << (8 * b);
-                    lw |= ((uint32_t)x24 & 0xFFu) << (8 * b);
-                }
-                X[(size_t)i * 16 * G + (hh * 8 + q8) * G + g] = make_uint4(hw, mw, lw, 0u);
-                if (q8 == 0) {
-                    float* xsf = reinterpret_cast<float*>(XS + (size_t)i * G + g);
-                    xsf[hh] = m / 8388607.0f;
-                    xsf[2 + hh] = sum;
-                }
+            for (int b = 0; b < 4; ++b) {
+                int x24 = __float2int_rn(vv[b] * inv);
+                x24 = max(-8388607, min(8388607, x24));
+                hw |= ((uint32_t)(x24 >> 16) & 0xFFu) << (8 * b);
+                mw |= ((uint32_t)(x24 >> 8) & 0xFFu) << (8 * b);
+                lw |= ((uint32_t)x24 & 0xFFu) << (8 * b);
+            }
+            X[(size_t)i * 16 * G + (hh * 8 + q8) * G + g] = make_uint4(hw, mw, lw, 0u);
+            if (q8 == 0) {
+                float* xsf = reinterpret_cast<float*>(XS + (size_t)i * G + g);
+                xsf[hh] = m / 8388607.0f;
+                xsf[2 + hh] = sum;
             }
         }
     }
 }
 
-// Scales of sub-blocks 2c and 2c+1 of a Q4_K block header.
+// Exact float of an integer 0 <= v < 2^23 (2^23 + v as fp32 bit pattern, minus 2^23).
+__device__ __forceinline__ float qd_small_u2f(uint32_t v) { return __uint_as_float(0x4B000000u | v) - 8388608.0f; }
+
+// Scales of sub-blocks 2c and 2c+1 of a Q4_K block header: fs = d*sc_j, fm = dmin*m_j.
+// Sub-blocks 0..3 keep sc and m in the low 6 bits of bytes 0..3 / 4..7 of the 12 scale
+// bytes; sub-blocks 4..7 take their low 4 bits from the nibbles of bytes 8..11 and the
+// top 2 bits from bits 6..7 of bytes 0..3 / 4..7.  Both sub-blocks of the pair come out
+// of one 16-bit window of each scale word.
 __device__ __forceinline__ void qd4_scales(const uint4& hd, int c, float (&fs)[2], float (&fm)[2]) {
     const float d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
     const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
-#pragma unroll
-    for (int s2 = 0; s2 < 2; ++s2) {
-        const int j = 2 * c + s2, jj = j & 3;
-        const uint32_t by = (hd.y >> (8 * jj)) & 0xFFu, bz = (hd.z >> (8 * jj)) & 0xFFu, bw = (hd.w >> (8 * jj)) & 0xFFu;
-        uint32_t sc, m;
-        if (j < 4) { sc = by & 63u; m = bz & 63u; }
-        else { sc = (bw & 15u) | ((by >> 6) << 4); m = (bw >> 4) | ((bz >> 6) << 4); }
-        fs[s2] = d * (float)sc;
-        fm[s2] = dmin * (float)m;
-    }
+    const int sh = (c & 1) * 16;
+    const uint32_t y = hd.y >> sh, z = hd.z >> sh, w = hd.w >> sh;
+    const uint32_t sc_lo = y & 0x3F3Fu, m_lo = z & 0x3F3Fu;
+    const uint32_t sc_hi = (w & 0x0F0Fu) | ((y >> 2) & 0x3030u);
+    const uint32_t m_hi = ((w >> 4) & 0x0F0Fu) | ((z >> 2) & 0x3030u);
+    const bool upper = c >= 2;
+    const uint32_t sc = upper ? sc_hi : sc_lo, m = upper ? m_hi : m_lo;
+    fs[0] = d * qd_small_u2f(sc & 0xFFu);
+    fs[1] = d * qd_small_u2f(sc >> 8);
+    fm[0] = dmin * qd_small_u2f(m & 0xFFu);
+    fm[1] = dmin * qd_small_u2f(m >> 8);
 }
 
 // One lane, one group g (64 weights: sub-blocks 2c, 2c+1 of super-block g/4, c = g%4),

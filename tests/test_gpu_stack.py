@@ -24,12 +24,33 @@ N_LAYERS = 48
 EPS = 1e-6
 
 
-def _oracle_chain(layers, shape, x):
-    """The oracle's own chain from x (fp64), returning x after every layer."""
+def _bf16_neighbours(u):
+    """The two bf16 values around each element of u (fp64), and the midpoint between them."""
+    f = np.abs(u).astype(np.float32)
+    lo_bits = f.view(np.uint32) & np.uint32(0xFFFF0000)
+    lo = lo_bits.view(np.float32).astype(np.float64)
+    hi = (lo_bits + np.uint32(0x10000)).view(np.float32).astype(np.float64)
+    return lo, hi, 0.5 * (lo + hi)
+
+
+def _round_other_way(u, rel=1e-6):
+    """bf16(u), except that elements within rel of a rounding midpoint take the other
+    neighbour: a computation of u in lower precision may land on either side there."""
+    r = np.vectorize(oracle.round_bf16)(u)
+    lo, hi, mid = _bf16_neighbours(u)
+    amb = np.abs(np.abs(u) - mid) <= rel * np.abs(u)
+    other = np.where(np.abs(r) == lo, hi, lo) * np.sign(u)
+    return np.where(amb, other, r)
+
+
+def _oracle_chain(layers, shape, x, flip_rel=0.0):
+    """The oracle's own chain from x (fp64), returning x after every layer.  flip_rel > 0
+    rounds the RMSNorm outputs that sit within flip_rel of a bf16 rounding midpoint the
+    other way (the rounding a less precise RMSNorm may legitimately take)."""
     xs = []
     for L in layers:
         u = oracle.rmsnorm(x, L["gamma"].numpy(), EPS)
-        u = np.vectorize(oracle.round_bf16)(u)
+        u = _round_other_way(u, flip_rel) if flip_rel > 0 else np.vectorize(oracle.round_bf16)(u)
         x = x + oracle.moe_layer(L["spec"], u, n_threads=8)["out"]
         xs.append(x)
     return xs
@@ -98,14 +119,18 @@ def test_stack_48_layers_graph(T):
     The stack is a deep residual chain whose bf16 rounding of each layer's input
     is a discontinuous step, so tiny differences grow with depth.  The bound on
     the GPU's distance from the oracle after layer l is derived from the oracle
-    alone: the oracle chain is rerun from an input perturbed by 1e-6 (relative),
-    and its own divergence after layer l, times 10, plus the single-layer
-    tolerance, is the allowed distance.
+    alone, from two reruns of its chain: one from an input perturbed by 1e-6
+    (relative), and one that rounds every RMSNorm output lying within 1e-6 of a
+    bf16 rounding midpoint to the other neighbour (the GPU computes RMSNorm in
+    fp32, so such elements may round either way).  The larger of the two
+    divergences after layer l, times 10, plus the single-layer tolerance, is the
+    allowed distance.
     """
     shape, x0, layers, x_ref = _build_stack(T)
     rng = np.random.default_rng(7)
     x0_64 = x0.double().numpy()
     pert = _oracle_chain(layers, shape, x0_64 * (1.0 + 1e-6 * rng.standard_normal(x0_64.shape)))
+    flip = _oracle_chain(layers, shape, x0_64, flip_rel=1e-6)
     mls, x, run = _gpu_stack(shape, x0, layers, T)
     # eager, layer by layer: the GPU chain next to the oracle chain (never fed into it)
     import quantized_routed_expert_sigmoid_gb300 as moe
@@ -119,7 +144,7 @@ def test_stack_48_layers_graph(T):
         ids, _, _ = m.debug_views(T)
         assert np.array_equal(ids.numpy(), L["ids"]), f"layer {l}: routing ids differ"
         err = rel_l2(x.cpu().numpy(), L["x_after"])
-        self_div = rel_l2(pert[l], L["x_after"])
+        self_div = max(rel_l2(pert[l], L["x_after"]), rel_l2(flip[l], L["x_after"]))
         drift.append((err, self_div))
         assert err <= 1e-4 + 10 * self_div, f"layer {l}: rel-L2 {err:.3e}, oracle self-divergence {self_div:.3e}"
     eager_final = x.clone()
