@@ -20,6 +20,7 @@ checked against) on the same workload, on the host cores.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -66,6 +67,29 @@ def measured_peaks():
             d = json.load(f)
         return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
     return 6800.0, 1900.0, "fallback"
+
+
+def sources_digest(files):
+    """sha1 over the given library sources (paths relative to the package's csrc/)."""
+    h = hashlib.sha1()
+    for f in files:
+        with open(os.path.join(ROOT, "quantized_routed_expert_sigmoid_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(kernel, args):
+    """DRAM bytes per launch of `kernel` on this workload from the committed ncu summary
+    (profiles/traffic.json), or None when there is none or the kernel's sources changed
+    since the counters were taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            entry = json.load(f).get(f"{kernel} {args.workload}")
+        if entry and sources_digest(entry["sources"]) == entry["sources_sha1"]:
+            return entry["dram_bytes_per_launch"]
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
 
 
 # ------------------------------------------------------------------ clocks
@@ -123,7 +147,7 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ workload construction
 
-def build_layers(shape, T, L, seed, device, shared_router=False, decode_fused=True):
+def build_layers(shape, T, L, seed, device, shared_router=False, decode_chain=True):
     """L layers with distinct expert weights.  Router weights and biases are drawn on the
     CPU (small) so that a workload built around them (the Zipf prefill) sees the same values;
     shared_router gives every layer layer 0's router."""
@@ -145,7 +169,7 @@ def build_layers(shape, T, L, seed, device, shared_router=False, decode_fused=Tr
                                topk_groups=shape.topk_groups, scale=shape.scale, renormalize=shape.renormalize,
                                x_dtype=shape.x_dtype, I_s=shape.I_s, shared_qtype=shape.shared_qtype,
                                s_gate=sh[0] if sh else None, s_up=sh[1] if sh else None,
-                               s_down=sh[2] if sh else None, decode_fused=decode_fused))
+                               s_down=sh[2] if sh else None, decode_chain=decode_chain))
     return layers
 
 
@@ -167,10 +191,10 @@ def algorithmic_bytes(shape, T, offsets_host):
     return b, gu, u
 
 
-def launches_per_layer(shape, T, stack=False):
+def launches_per_layer(shape, T, stack=False, path=None):
     P = T * shape.k
-    if T <= 4 and P <= 64 and shape.E <= 256:
-        return 1 + (1 if stack else 0)                # the single-launch layer (+ RMSNorm)
+    if path == "decode_chain":
+        return 3 + (1 if stack else 0)                # logits, routing + gate/up, down + combine (+ RMSNorm)
     n = 2 + (1 if P <= 1024 else 2) + 2 + 1          # logits, top-k, permute, gate/up, down, combine
     if T >= 128:
         n += 2                                       # fp16 copy of x, token-block list
@@ -194,7 +218,7 @@ def run_ours(args, rank, world):
         L = args.layers
         desc = desc.replace("16 distinct layers", f"{L} distinct layers")
     layers = build_layers(shape, T, L, seed + 1000 * rank, device, shared_router=(args.workload == "prefill"),
-                          decode_fused=not args.separate_decode)
+                          decode_chain=not args.separate_decode)
     x = make_x(shape, T, seed + 1000 * rank, device, args.workload)
     outs = [torch.empty(T, shape.H, dtype=torch.float32, device=device) for _ in range(L)]
     for lay in layers:
@@ -264,14 +288,12 @@ def run_ours(args, rank, world):
     # ---- the dominant kernel alone (the routed gate/up + SwiGLU launch)
     path = layers[0].path(T)           # which kernels the library runs for this T
     tc_path = path == "tensor"
-    fused_path = path == "fused_decode"
+    chain_path = path == "decode_chain"
     gu_ms = None
     if stack:
         x = u                           # the kernels' input in the stack: the bf16 normalised stream
     try:
-        if fused_path:
-            gu_ms = None                # the layer is one kernel: its graph-timed duration is the layer's
-        elif tc_path:
+        if tc_path or chain_path:
             gu_ms = time_gateup_events(moe, layers, x, outs, T, args)
         else:
             gu_ms = time_gateup(moe, layers, x, shape, T, device, args)
@@ -311,13 +333,15 @@ def run_ours(args, rank, world):
     hbm_peak, tc_peak, peak_kind = measured_peaks()
     roof = None
     layer_us_ = ms_per_step * 1e3 / L
-    if fused_path:
-        achieved = layer_bytes / (layer_us_ * 1e-6) / 1e9
-        roof = {"kernel": "decode_layer_kernel (whole layer, one cooperative launch)", "bound": "hbm",
+    if gu_ms is not None and chain_path:
+        # routing + gate/up (+ the shared expert's gate/up rows) of the chain
+        cb = gu_bytes + (2 * shape.I_s * synth.row_bytes(shape.shared_qtype, shape.H) if shape.I_s > 0 else 0)
+        achieved = cb / (gu_ms * 1e-3) / 1e9
+        roof = {"kernel": "chain_gateup_kernel (routing + gate/up + SwiGLU)", "bound": "hbm",
                 "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                "frac": round(achieved / hbm_peak, 4), "traffic": None, "peak_source": peak_kind,
-                "bytes_per_launch": round(layer_bytes), "us_per_launch": round(layer_us_, 3),
-                "timing": "CUDA events around replays of one graph of L launches; per launch = total / (steps * L)"}
+                "frac": round(achieved / hbm_peak, 4), "traffic": profiled_traffic("chain_gateup_kernel", args),
+                "peak_source": peak_kind, "bytes_per_launch": round(cb), "us_per_launch": round(gu_ms * 1e3, 3),
+                "timing": "CUDA events recorded around the gate/up launch, eager calls"}
     elif gu_ms is not None and not tc_path:
         achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
         roof = {"kernel": "qgemv_kernel (gate/up + SwiGLU)", "bound": "hbm", "achieved": round(achieved, 1),
@@ -349,7 +373,7 @@ def run_ours(args, rank, world):
                   "distinct_experts_mean": u_mean},
         "roofline": roof,
         "e2e": e2e,
-        "gpu_launches": launches_per_layer(shape, T, stack) * L * args.steps,
+        "gpu_launches": launches_per_layer(shape, T, stack, path) * L * args.steps,
         "clocks": clk.summary(),
     }
     result.update(extra)

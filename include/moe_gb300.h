@@ -204,7 +204,7 @@ typedef struct {
     moe_qmat s_gate, s_up, s_down;/* shared expert (single matrices) */
     int accumulate;               /* 1: out += layer(x) (a residual add); 0: out = layer(x) */
     int tc_min_tokens;            /* T at or above this uses the tensor-core path (0 = default 128) */
-    int decode_fused_off;         /* 1: never use the single-launch decode kernel (T <= 4) */
+    int decode_chain_off;         /* 1: never use the chained decode kernels (T <= 4) */
 } moe_layer_desc;
 
 typedef struct moe_layer_plan moe_layer_plan;
@@ -214,23 +214,17 @@ moe_status moe_layer_plan_create(const moe_layer_desc* desc, moe_layer_plan** pl
 moe_status moe_layer_plan_destroy(moe_layer_plan* plan);
 /* Bytes of device workspace moe_layer needs for up to T tokens. */
 moe_status moe_layer_workspace_size(const moe_layer_plan* plan, int T, size_t* bytes);
-/* Prepares a workspace for moe_layer with this plan (enqueued on stream; call
- * once after allocating it, outside graph capture, and again after a call
- * reported a device-side error).  At T <= 4 moe_layer runs the whole layer as
- * one cooperative launch whose grid barriers keep their counters in the
- * workspace header; this call sets them up.  moe_layer refuses a workspace
- * that was not prepared with MOE_ERR_WORKSPACE. */
-moe_status moe_layer_workspace_init(moe_layer_plan* plan, int T, void* workspace, moe_stream_t stream);
 /* Which kernels moe_layer runs for T tokens with this plan (T >= 1):
  *   MOE_PATH_GEMV         route, permute, dequant-GEMV experts and combine as
  *                         separate launches (fp32 accumulation);
- *   MOE_PATH_FUSED_DECODE the whole layer as one cooperative launch (same
- *                         arithmetic as MOE_PATH_GEMV, same bits);
+ *   MOE_PATH_DECODE_CHAIN the whole layer as three launches chained by
+ *                         programmatic dependent launch (router logits; routing
+ *                         + gate/up; down + combine), fp32 accumulation;
  *   MOE_PATH_TENSOR       route and permute, then the tcgen05 grouped GEMM
  *                         (fp16 operands, fp32 accumulation) and combine.
  * Host-only; reads nothing on the device. */
 #define MOE_PATH_GEMV 0
-#define MOE_PATH_FUSED_DECODE 1
+#define MOE_PATH_DECODE_CHAIN 1
 #define MOE_PATH_TENSOR 2
 moe_status moe_layer_path(const moe_layer_plan* plan, int T, int* path);
 /*
@@ -238,18 +232,17 @@ moe_status moe_layer_path(const moe_layer_plan* plan, int T, int* path);
  * for T tokens of x (device, [T][H] in desc->x_type) into out (device, fp32
  * [T][H]).  Enqueued on `stream` with no host synchronization and no host
  * read-back, so it can be captured in a CUDA graph; replays give the same
- * bits as eager calls.  The expert path is chosen from T on the host:
- * T <= 4 (T*k <= 64, E <= 256) runs one cooperative kernel for the whole
- * layer, T < tc_min_tokens the fp32 dequant-GEMV kernels (both fp32
- * accumulate, identical results), larger T the tensor-core grouped GEMM
- * (fp16 operands, fp32 accumulate).
+ * bits as eager calls.  The expert path is chosen from T on the host
+ * (moe_layer_path tells which): T <= 4 (T*k <= 64, E <= 256, Q4_K routed
+ * experts) the chained decode kernels, T < tc_min_tokens the fp32
+ * dequant-GEMV kernels (both fp32 accumulate), larger T the tensor-core
+ * grouped GEMM (fp16 operands, fp32 accumulate).
  */
 moe_status moe_layer(const moe_layer_plan* plan, const void* x, int T, float* out, void* workspace,
                      size_t ws_bytes, moe_stream_t stream);
 /* moe_layer that also records two caller-owned CUDA events (cudaEvent_t, may
  * be NULL) on `stream` immediately before and after the launch of the routed
- * gate/up kernel (the whole single-launch layer at T <= 4), so a caller can
- * time that kernel alone.  Same results as
+ * gate/up kernel, so a caller can time that kernel alone.  Same results as
  * moe_layer; meant for eager calls (not for graph capture). */
 moe_status moe_layer_timed(const moe_layer_plan* plan, const void* x, int T, float* out, void* workspace,
                            size_t ws_bytes, moe_stream_t stream, void* ev_before_gateup, void* ev_after_gateup);

@@ -48,7 +48,7 @@ class moe_layer_desc(ctypes.Structure):
                 ("gate", moe_qmat), ("up", moe_qmat), ("down", moe_qmat),
                 ("shared_intermediate", ctypes.c_int), ("s_gate", moe_qmat), ("s_up", moe_qmat),
                 ("s_down", moe_qmat), ("accumulate", ctypes.c_int), ("tc_min_tokens", ctypes.c_int),
-                ("decode_fused_off", ctypes.c_int)]
+                ("decode_chain_off", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -91,7 +91,6 @@ def _declare(lib):
         "moe_layer_plan_create": [ctypes.POINTER(moe_layer_desc), ctypes.POINTER(P)],
         "moe_layer_plan_destroy": [P],
         "moe_layer_workspace_size": [P, I, PS],
-        "moe_layer_workspace_init": [P, I, P, P],
         "moe_layer_path": [P, I, ctypes.POINTER(ctypes.c_int)],
         "moe_layer": [P, P, I, P, P, S, P],
         "moe_layer_timed": [P, P, I, P, P, S, P, P, P],
@@ -215,12 +214,8 @@ def moe_layer_workspace_size(plan: int, T: int) -> int:
     return n.value
 
 
-def moe_layer_workspace_init(plan, T, workspace, stream=None):
-    _check(load().moe_layer_workspace_init(plan, T, _p(workspace), _stream(stream)))
-
-
-MOE_PATH_GEMV, MOE_PATH_FUSED_DECODE, MOE_PATH_TENSOR = 0, 1, 2
-PATH_NAMES = {MOE_PATH_GEMV: "gemv", MOE_PATH_FUSED_DECODE: "fused_decode", MOE_PATH_TENSOR: "tensor"}
+MOE_PATH_GEMV, MOE_PATH_DECODE_CHAIN, MOE_PATH_TENSOR = 0, 1, 2
+PATH_NAMES = {MOE_PATH_GEMV: "gemv", MOE_PATH_DECODE_CHAIN: "decode_chain", MOE_PATH_TENSOR: "tensor"}
 
 
 def moe_layer_path(plan, T):

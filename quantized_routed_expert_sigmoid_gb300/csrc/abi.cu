@@ -89,7 +89,6 @@ moe_status moe::report(moe_status st, const char* msg) { return fail(st, "%s", m
 
 struct moe_layer_plan {
     moe_layer_desc d;
-    std::vector<void*> ready_ws;   // workspaces prepared by moe_layer_workspace_init
 };
 
 namespace {
@@ -112,7 +111,7 @@ bool use_tc(const moe_layer_desc& d, int T) {
     return true;
 }
 
-// The shape-level fields of the single-launch decode layer (no buffers yet).
+// The shape-level fields of the chained decode kernels (no buffers yet).
 DecodeArgs decode_shape_args(const moe_layer_desc& d, int T) {
     DecodeArgs da{};
     da.route = d.route;
@@ -135,9 +134,9 @@ DecodeArgs decode_shape_args(const moe_layer_desc& d, int T) {
     return da;
 }
 
-// True when moe_layer runs T tokens as the single-launch decode layer.
-bool fused_decode_applies(const moe_layer_desc& d, int T) {
-    if (d.decode_fused_off || use_tc(d, T)) return false;
+// True when moe_layer runs T tokens as the chained decode kernels.
+bool decode_chain_applies(const moe_layer_desc& d, int T) {
+    if (d.decode_chain_off || use_tc(d, T)) return false;
     const bool same_q = d.gate.qtype == d.up.qtype && d.gate.qtype == d.down.qtype &&
                         (d.shared_intermediate == 0 ||
                          (d.s_gate.qtype == d.s_up.qtype && d.s_gate.qtype == d.s_down.qtype));
@@ -442,7 +441,7 @@ moe_status moe_layer_path(const moe_layer_plan* plan, int T, int* path) {
     if (!plan || !path) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
     if (T < 1) return fail(MOE_ERR_INVALID_ARG, "T = %d < 1", T);
     if (use_tc(plan->d, T)) *path = MOE_PATH_TENSOR;
-    else if (fused_decode_applies(plan->d, T)) *path = MOE_PATH_FUSED_DECODE;
+    else if (decode_chain_applies(plan->d, T)) *path = MOE_PATH_DECODE_CHAIN;
     else *path = MOE_PATH_GEMV;
     return MOE_OK;
 }
@@ -478,7 +477,7 @@ moe_status moe_layer_timed(const moe_layer_plan* plan, const void* x, int T, flo
     int32_t* ppos = at<int32_t>(workspace, w.pair_pos);
     int32_t* offs = at<int32_t>(workspace, w.offsets);
     cudaError_t err;
-    if (!w.tc && fused_decode_applies(d, T)) {
+    if (!w.tc && decode_chain_applies(d, T)) {
         DecodeArgs da = decode_shape_args(d, T);
         da.x = x;
         da.x_bf16 = xb;
@@ -488,13 +487,8 @@ moe_status moe_layer_timed(const moe_layer_plan* plan, const void* x, int T, flo
         da.out = out;
         da.accumulate = d.accumulate != 0;
         da.hdr = hdr;
-        bool ready = false;
-        for (void* p : plan->ready_ws) ready = ready || p == workspace;
-        if (!ready) return fail(MOE_ERR_WORKSPACE, "workspace not prepared: call moe_layer_workspace_init once on it");
-        if (evb && (err = cudaEventRecord(evb, s)) != cudaSuccess) return cuda_fail(err, "event record");
-        err = launch_decode_chain(da, s);
+        err = launch_decode_chain(da, s, evb, eva);
         if (err != cudaSuccess) return cuda_fail(err, "decode chain kernels");
-        if (eva && (err = cudaEventRecord(eva, s)) != cudaSuccess) return cuda_fail(err, "event record");
         return MOE_OK;
     }
     err = launch_router_logits(x, xb, T, H, d.W_router, E, logits, hdr, s);
@@ -562,18 +556,6 @@ moe_status moe_layer_timed(const moe_layer_plan* plan, const void* x, int T, flo
     }
     err = launch_combine(y, gw, ppos, T, k, H, shared, d.accumulate != 0, out, s);
     if (err != cudaSuccess) return cuda_fail(err, "combine kernel");
-    return MOE_OK;
-}
-
-moe_status moe_layer_workspace_init(moe_layer_plan* plan, int T, void* workspace, moe_stream_t stream) {
-    if (!plan || !workspace) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
-    if (!aligned(workspace, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace not 256-byte aligned");
-    const LayerWs w = layer_ws(plan->d, T);
-    cudaError_t err = launch_init_header(at<WsHeader>(workspace, w.hdr), reinterpret_cast<cudaStream_t>(stream));
-    if (err != cudaSuccess) return cuda_fail(err, "workspace init");
-    for (void* p : plan->ready_ws)
-        if (p == workspace) return MOE_OK;
-    plan->ready_ws.push_back(workspace);
     return MOE_OK;
 }
 

@@ -671,7 +671,8 @@ ChainLayout chain_layout(const DecodeArgs& a) {
 }
 
 template <int NT, int Q8>
-cudaError_t launch_chain_nt(const ChainParams& p, const ChainLayout& L, int E, cudaStream_t s) {
+cudaError_t launch_chain_nt(const ChainParams& p, const ChainLayout& L, int E, cudaStream_t s, cudaEvent_t evb,
+                            cudaEvent_t eva) {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -684,6 +685,7 @@ cudaError_t launch_chain_nt(const ChainParams& p, const ChainLayout& L, int E, c
     cfg.blockDim = dim3(kK1Threads);
     cfg.dynamicSmemBytes = 0;
     if ((err = cudaLaunchKernelEx(&cfg, chain_logits_kernel, p)) != cudaSuccess) return err;
+    if (evb && (err = cudaEventRecord(evb, s)) != cudaSuccess) return err;
     if ((err = cudaFuncSetAttribute(chain_gateup_kernel<NT, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)L.k2_smem)) != cudaSuccess)
         return err;
@@ -691,6 +693,7 @@ cudaError_t launch_chain_nt(const ChainParams& p, const ChainLayout& L, int E, c
     cfg.blockDim = dim3(L.k2_warps * 32);
     cfg.dynamicSmemBytes = L.k2_smem;
     if ((err = cudaLaunchKernelEx(&cfg, chain_gateup_kernel<NT, Q8>, p)) != cudaSuccess) return err;
+    if (eva && (err = cudaEventRecord(eva, s)) != cudaSuccess) return err;
     if ((err = cudaFuncSetAttribute(chain_down_kernel<NT, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)L.k3_smem)) != cudaSuccess)
         return err;
@@ -757,15 +760,15 @@ bool decode_chain_supported(const DecodeArgs& a) {
     return L.k2_warps >= 4 && L.k2_smem <= kChainSmemCap && L.k3_smem <= kChainSmemCap;
 }
 
-cudaError_t launch_decode_chain(const DecodeArgs& a, cudaStream_t s) {
+cudaError_t launch_decode_chain(const DecodeArgs& a, cudaStream_t s, cudaEvent_t evb, cudaEvent_t eva) {
     const ChainLayout L = chain_layout(a);
     const ChainParams p = chain_params(a, L);
     const int E = a.route.n_experts;
     const int sh = a.I_s <= 0 ? 0 : p.s_q8 ? 2 : 1;
     auto go = [&](auto nt) -> cudaError_t {
         constexpr int NT = decltype(nt)::value;
-        return sh == 0 ? launch_chain_nt<NT, 0>(p, L, E, s) : sh == 1 ? launch_chain_nt<NT, 1>(p, L, E, s)
-                                                                       : launch_chain_nt<NT, 2>(p, L, E, s);
+        return sh == 0 ? launch_chain_nt<NT, 0>(p, L, E, s, evb, eva) : sh == 1 ? launch_chain_nt<NT, 1>(p, L, E, s, evb, eva)
+                                                                       : launch_chain_nt<NT, 2>(p, L, E, s, evb, eva);
     };
     switch (a.T) {
         case 1: return go(std::integral_constant<int, 1>{});

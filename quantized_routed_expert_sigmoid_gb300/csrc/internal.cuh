@@ -30,14 +30,6 @@ struct WsHeader {
 };
 constexpr size_t kHeaderBytes = 256;
 
-// Grid-barrier counters of the fused decode kernel, at byte 64 of the header.
-// moe_layer_workspace_init writes kDecodeMagic and zeroes the counters; the
-// kernel leaves them at zero when it finishes.
-struct DecodeSync {
-    uint32_t magic, bar1, bar2, done;
-};
-constexpr size_t kDecodeSyncOffset = 64;
-constexpr uint32_t kDecodeMagic = 0x4D4F4531u;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -85,8 +77,8 @@ cudaError_t launch_combine(const float* y_pairs, const float* w, const int32_t* 
 cudaError_t launch_rmsnorm_bf16(const float* x, const float* gamma, int T, int H, float eps, void* u,
                                 cudaStream_t s);
 
-// ---------------------------------------------------------------- fused decode layer
-// The whole layer for a few tokens in one cooperative persistent launch.
+// ---------------------------------------------------------------- decode layer (T <= 4)
+// The whole layer for a few tokens: shapes, weights and workspace buffers.
 struct DecodeArgs {
     moe_route_cfg route;
     const float* Wr;
@@ -115,12 +107,11 @@ struct DecodeArgs {
     bool accumulate;
     WsHeader* hdr;
 };
-bool decode_fused_supported(const DecodeArgs& a);
-// The same layer as three launches chained by programmatic dependent launch (decode_chain.cu).
+// The layer as three launches chained by programmatic dependent launch (decode_chain.cu).
 bool decode_chain_supported(const DecodeArgs& a);
-cudaError_t launch_decode_chain(const DecodeArgs& a, cudaStream_t s);
-cudaError_t launch_init_header(WsHeader* hdr, cudaStream_t s);
-cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s);
+// evb / eva (nullable): events recorded around the gate/up launch.
+cudaError_t launch_decode_chain(const DecodeArgs& a, cudaStream_t s, cudaEvent_t evb = nullptr,
+                                cudaEvent_t eva = nullptr);
 
 // ---------------------------------------------------------------- tensor-core grouped GEMM
 // Expert FFN for many tokens per expert on tcgen05: gate/up + SwiGLU into an

@@ -25,7 +25,7 @@ class MoeLayer:
                  bias=None, n_groups: int = 1, topk_groups: int = 1, scale: float = 1.0,
                  renormalize: bool = True, x_dtype: str = "bf16", I_s: int = 0, shared_qtype: str = "q8_0",
                  s_gate=None, s_up=None, s_down=None, accumulate: bool = False, tc_min_tokens: int = 0,
-                 decode_fused: bool = True):
+                 decode_chain: bool = True):
         self.E, self.k, self.H, self.I = E, k, H, I
         self.x_dtype = x_dtype
         qt = _QT[qtype]
@@ -48,14 +48,14 @@ class MoeLayer:
             d.s_down = N.qmat(sq, s_down, H, I_s, 0)
         d.accumulate = int(accumulate)
         d.tc_min_tokens = tc_min_tokens
-        d.decode_fused_off = 0 if decode_fused else 1
+        d.decode_chain_off = 0 if decode_chain else 1
         self.desc = d
         self.plan = N.moe_layer_plan_create(d)
         self.ws = None
         self.ws_T = -1
 
     def path(self, T: int) -> str:
-        """Which kernels a call with T tokens runs: "gemv", "fused_decode" or "tensor"."""
+        """Which kernels a call with T tokens runs: "gemv", "decode_chain" or "tensor"."""
         return N.PATH_NAMES[N.moe_layer_path(self.plan, T)]
 
     def workspace_bytes(self, T: int) -> int:
@@ -66,7 +66,6 @@ class MoeLayer:
             nbytes = self.workspace_bytes(T)
             self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
             self.ws_T = T
-            N.moe_layer_workspace_init(self.plan, T, self.ws)
         return self.ws
 
     def __call__(self, x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
@@ -88,11 +87,9 @@ class MoeLayer:
                 view(po, self.E + 1, torch.int32))
 
     def rebuild_plan(self):
-        """Re-create the plan after editing self.desc (the workspace is prepared again)."""
+        """Re-create the plan after editing self.desc."""
         N.moe_layer_plan_destroy(self.plan)
         self.plan = N.moe_layer_plan_create(self.desc)
-        if self.ws is not None:
-            N.moe_layer_workspace_init(self.plan, self.ws_T, self.ws)
 
     def device_status(self, T: int) -> int:
         return N.moe_read_device_status(self.plan, T, self.ws)

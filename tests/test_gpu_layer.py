@@ -206,9 +206,9 @@ def _chain_vs_separate(tl, T):
     lists; outputs equal up to summation order (both accumulate in fp32)."""
     chain = tl.moe_layer()
     sep = tl.moe_layer()
-    sep.desc.decode_fused_off = 1
+    sep.desc.decode_chain_off = 1
     sep.rebuild_plan()
-    assert chain.path(T) == "fused_decode" and sep.path(T) == "gemv"
+    assert chain.path(T) == "decode_chain" and sep.path(T) == "gemv"
     x = tl.x.cuda()
     o_c = chain(x).clone()
     o_s = sep(x).clone()
@@ -237,15 +237,3 @@ def test_decode_chain_q4k_shared_expert():
     tl = make_layer(shape, 63, 3, exact_all=True)
     _chain_vs_separate(tl, 3)
     _check_layer(tl, 3)
-
-
-def test_decode_chain_needs_prepared_workspace():
-    import quantized_routed_expert_sigmoid_gb300 as moe
-    tl = make_layer(synth.DECODE, 62, 1)
-    layer = tl.moe_layer()
-    nbytes = layer.workspace_bytes(1)
-    raw = torch.empty(nbytes, dtype=torch.uint8, device="cuda")     # never prepared
-    out = torch.empty(1, synth.DECODE.H, device="cuda")
-    with pytest.raises(moe.MoeError) as ei:
-        moe.moe_layer(layer.plan, tl.x.cuda(), 1, out, raw, nbytes)
-    assert ei.value.status == moe.MOE_ERR_WORKSPACE
