@@ -27,14 +27,20 @@
 namespace moe {
 namespace {
 
-constexpr int kBM = 128, kBN = 128, kBK = 64;
+constexpr int kBM = 128, kBK = 64;
+constexpr int kBNMin = 128;                       // token-block width bound used to size the tile list
 constexpr int kProducerWarps = 8;
 constexpr int kProducers = kProducerWarps * 32;
 constexpr int kThreadsTC = kProducers + 32;
-constexpr int kAStages = 2, kBStages = 4, kRawSlots = 4;
+constexpr int kAStages = 2, kBStages = 4, kRawSlots = 2;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
 
 enum { kGateUp = 0, kDown = 1 };
+
+// Token-block width (MMA N) per weight type: 256 for Q4_K (each dequantized weight tile
+// feeds twice the MMA work), 128 for Q8_0 (its raw blocks need the shared memory).
+template <int QT>
+__host__ __device__ constexpr int tc_bn() { return QT == MOE_Q4_K ? 256 : 128; }
 
 // ---------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -53,10 +59,12 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
 }
 __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
     uint32_t ok;
+    // the suspend-time hint lets a waiting warp sleep (until the phase completes or ~0.1 ms
+    // pass) instead of spinning through issue slots the working warps need
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(su32(b)), "r"(parity)
+        : "r"(su32(b)), "r"(parity), "r"(100000u)
         : "memory");
     return ok != 0;
 }
@@ -132,6 +140,34 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 __device__ __forceinline__ uint32_t swz(int row, int ch) { return (uint32_t)(row * 128 + ((ch ^ (row & 7)) << 4)); }
 
 // scale and min of sub-block j (0..7) of a Q4_K block header (words y, z, w = scale bytes 0-11)
+// Eight fp16 weights of one Q4_K word into two 16-byte halves of a chunk: the low nibbles of
+// bytes b0..b3 are elements 0..3 of sub-block 2c, the high nibbles elements 0..3 of 2c+1.
+// A nibble q placed under the fp16 exponent of 1024 reads as 1024 + q (low nibble) or
+// 1024 + 16q (high nibble, left in place); one exact subtraction leaves q (or 16q), and one
+// fp16 FMA applies the sub-block's scale (s, or s/16) and min: w = s*q - m.
+struct Q4H2 {
+    __half2 s_lo, m_lo, s_hi, m_hi;       // m already negated
+};
+__device__ __forceinline__ Q4H2 q4h2_consts(float fs0, float fm0, float fs1, float fm1) {
+    Q4H2 c;
+    c.s_lo = __float2half2_rn(fs0);
+    c.m_lo = __float2half2_rn(-fm0);
+    c.s_hi = __float2half2_rn(fs1 * 0.0625f);
+    c.m_hi = __float2half2_rn(-fm1);
+    return c;
+}
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+// w -> (lo: elements 0,1 | 2,3 of sub-block 2c) and (hi: the same of 2c+1), as fp16 pairs
+__device__ __forceinline__ void q4_word_h2(uint32_t w, const Q4H2& c, uint32_t (&lo)[2], uint32_t (&hi)[2]) {
+    const __half2 k1024 = __float2half2_rn(1024.0f);
+    const uint32_t t01 = __byte_perm(w, 0u, 0x4140u);        // [b0, 0, b1, 0]
+    const uint32_t t23 = __byte_perm(w, 0u, 0x4342u);        // [b2, 0, b3, 0]
+    lo[0] = h2u(__hfma2(__hsub2(u2h((t01 & 0x000F000Fu) | 0x64006400u), k1024), c.s_lo, c.m_lo));
+    lo[1] = h2u(__hfma2(__hsub2(u2h((t23 & 0x000F000Fu) | 0x64006400u), k1024), c.s_lo, c.m_lo));
+    hi[0] = h2u(__hfma2(__hsub2(u2h((t01 & 0x00F000F0u) | 0x64006400u), k1024), c.s_hi, c.m_hi));
+    hi[1] = h2u(__hfma2(__hsub2(u2h((t23 & 0x00F000F0u) | 0x64006400u), k1024), c.s_hi, c.m_hi));
+}
 __device__ __forceinline__ void q4k_scale_min(const uint4& hd, int j, float& fsc, float& fm) {
     const float d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
     const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
@@ -165,6 +201,7 @@ struct TcParams {
     const int32_t* sorted_pairs; // GATEUP gather map (NULL: identity)
     const int4* tb_list;         // [0].x = number of token blocks, then (e, tok0, ntok, 0); NULL: identity
     int n_identity;              // identity mode: tokens
+    int bn;                      // token-block width of the list (tc_bn)
     __half* h_out;               // GATEUP: [P][rows] fp16
     float* y_out;                // DOWN: [P][rows] fp32
     WsHeader* hdr;
@@ -178,7 +215,7 @@ __device__ __forceinline__ bool tile_at(const TcParams& p, int n_mb, int t, int 
         const int4 v = p.tb_list[1 + tb];
         ti.e = v.x; ti.tok0 = v.y; ti.ntok = v.z;
     } else {
-        ti.e = 0; ti.tok0 = tb * kBN; ti.ntok = min(kBN, p.n_identity - ti.tok0);
+        ti.e = 0; ti.tok0 = tb * p.bn; ti.ntok = min(p.bn, p.n_identity - ti.tok0);
     }
     ti.m0 = mb * kBM;
     ti.n_inst = (ti.ntok + 15) & ~15;
@@ -188,10 +225,11 @@ __device__ __forceinline__ bool tile_at(const TcParams& p, int n_mb, int t, int 
 template <int QT, int MODE>
 __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
     constexpr int kAStageBytes = (MODE == kGateUp ? 2 : 1) * kBM * 128;
-    constexpr int kBStageBytes = kBN * 128;
+    constexpr int BN = tc_bn<QT>();
+    constexpr int kBStageBytes = BN * 128;
     constexpr int kRawBytes = RawCfg<QT, MODE>::kBytes;
     constexpr int kRawSlotBytes = kProducers * kRawBytes;
-    constexpr uint32_t kTmemCols = MODE == kGateUp ? 2 * kBN : kBN;
+    constexpr uint32_t kTmemCols = MODE == kGateUp ? 2 * BN : BN;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -226,7 +264,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
     const uint32_t tmem = *tmem_slot;
 
     const int n_mb = p.rows / kBM;
-    const int n_tb = p.tb_list ? p.tb_list[0].x : (p.n_identity + kBN - 1) / kBN;
+    const int n_tb = p.tb_list ? p.tb_list[0].x : (p.n_identity + BN - 1) / BN;
     const int n_tiles = n_tb * n_mb;
     const int nk = p.K / kBK;
     const int nblk_row = QT == MOE_Q4_K ? p.K / kQ4KWeights : p.K / kQ80Weights;
@@ -244,10 +282,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
             const uint8_t* wrow = (MODE == kGateUp && psel == 1 ? p.w1 : p.w0) + (int64_t)ti.e * p.expert_stride +
                                   (int64_t)(ti.m0 + prow) * rb;
             // rows of B this thread copies: r = tid/8 + 32*it, 16-byte chunk tid%8
+            constexpr int kBIt = BN / 32;
             const int bch = tid & 7;
-            int64_t brow[4];
+            int64_t brow[kBIt];
 #pragma unroll
-            for (int it = 0; it < 4; ++it) {
+            for (int it = 0; it < kBIt; ++it) {
                 const int r = (tid >> 3) + 32 * it;
                 int64_t src = -1;
                 if (r < ti.ntok) {
@@ -259,11 +298,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
             }
             auto issue_b = [&](int kb, int stage) {
                 uint8_t* dst = sB + stage * kBStageBytes;
+                // rows past the block's tokens only feed accumulator columns that are never read
 #pragma unroll
-                for (int it = 0; it < 4; ++it) {
+                for (int it = 0; it < kBIt; ++it) {
                     const int r = (tid >> 3) + 32 * it;
-                    const __half* src = brow[it] >= 0 ? p.bsrc + brow[it] * p.K + kb * kBK + bch * 8 : p.bsrc;
-                    cp_async16(dst + swz(r, bch), src, brow[it] >= 0 ? 16u : 0u);
+                    if (brow[it] >= 0) cp_async16(dst + swz(r, bch), p.bsrc + brow[it] * p.K + kb * kBK + bch * 8, 16u);
                 }
             };
             auto issue_raw = [&](int kb, int slot) {
@@ -283,23 +322,22 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
                     for (int w = 0; w < 17; ++w) cp_async4(dst + 4 * w, src + 4 * w);
                 }
             };
-            // prologue: groups {raw0}, {B0, raw1}, {B1, raw2}
+            // prologue: groups {raw0, B0}, {raw1, B1}; the group of step kb + 2 is issued right
+            // after step kb's dequantization, into the raw slot it has just read
             issue_raw(0, g % kRawSlots);
-            cp_commit();
             if (nk > 0) issue_b(0, g % kBStages);
-            if (nk > 1) issue_raw(1, (g + 1) % kRawSlots);
             cp_commit();
-            if (nk > 1) issue_b(1, (g + 1) % kBStages);
-            if (nk > 2) issue_raw(2, (g + 2) % kRawSlots);
+            if (nk > 1) {
+                issue_raw(1, (g + 1) % kRawSlots);
+                issue_b(1, (g + 1) % kBStages);
+            }
             cp_commit();
 
             bool ok = true;
             for (int kb = 0; kb < nk; ++kb, ++g) {
+                // A stage g%2 and B stage (g+2)%4 were last read by MMA(g-2)
                 if (g >= 2 && !mbar_wait(&empty[(g + 2) & 3], ((g - 2) >> 2) & 1, abort_flag)) { ok = false; break; }
-                if (kb + 2 < nk) issue_b(kb + 2, (g + 2) % kBStages);
-                if (kb + 3 < nk) issue_raw(kb + 3, (g + 3) % kRawSlots);
-                cp_commit();
-                cp_wait<2>();
+                cp_wait<1>();                        // raw(kb) and B(kb) have landed
                 // ---- dequantize k-step kb into A stage g%2
                 const uint8_t* raw = sRaw + (g % kRawSlots) * kRawSlotBytes + tid * kRawBytes;
                 uint8_t* arow = sA + (g % kAStages) * kAStageBytes + (MODE == kGateUp ? psel * kBM * 128 : 0);
@@ -309,43 +347,33 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
                     float fs0, fm0, fs1, fm1;
                     q4k_scale_min(hd, 2 * c, fs0, fm0);
                     q4k_scale_min(hd, 2 * c + 1, fs1, fm1);
+                    const Q4H2 hc = q4h2_consts(fs0, fm0, fs1, fm1);
                     if (MODE == kGateUp) {
                         const uint4 q0 = *reinterpret_cast<const uint4*>(raw + 16);
                         const uint4 q1 = *reinterpret_cast<const uint4*>(raw + 32);
                         const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                        // chunk ch < 4: elements 8ch.. of sub-block 2c (low nibbles of words 2ch, 2ch+1);
+                        // chunk 4 + ch: the same elements of 2c+1 (high nibbles)
 #pragma unroll
-                        for (int ch = 0; ch < 8; ++ch) {
-                            const bool hi = ch >= 4;
-                            const int wi = 2 * (ch & 3);
-                            const float fs = hi ? fs1 : fs0, fm = hi ? fm1 : fm0;
-                            uint32_t o[4];
-#pragma unroll
-                            for (int h2 = 0; h2 < 2; ++h2) {
-                                const uint32_t wv = qw[wi + h2];
-                                const uint32_t nb = hi ? ((wv >> 4) & 0x0F0F0F0Fu) : (wv & 0x0F0F0F0Fu);
-                                o[2 * h2] = pack_h2(fmaf(nib_f(nb, 0), fs, -fm), fmaf(nib_f(nb, 1), fs, -fm));
-                                o[2 * h2 + 1] = pack_h2(fmaf(nib_f(nb, 2), fs, -fm), fmaf(nib_f(nb, 3), fs, -fm));
-                            }
-                            *reinterpret_cast<uint4*>(arow + swz(prow, ch)) = make_uint4(o[0], o[1], o[2], o[3]);
+                        for (int ch = 0; ch < 4; ++ch) {
+                            uint32_t la[2], ha[2], lb[2], hb[2];
+                            q4_word_h2(qw[2 * ch], hc, la, ha);
+                            q4_word_h2(qw[2 * ch + 1], hc, lb, hb);
+                            *reinterpret_cast<uint4*>(arow + swz(prow, ch)) = make_uint4(la[0], la[1], lb[0], lb[1]);
+                            *reinterpret_cast<uint4*>(arow + swz(prow, 4 + ch)) = make_uint4(ha[0], ha[1], hb[0], hb[1]);
                         }
                     } else {
                         const uint4 q = *reinterpret_cast<const uint4*>(raw + 16);   // bytes 16*psel .. +15
                         const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+                        // words 0,1: elements 16*psel + 0..7 (chunk 2*psel), words 2,3: + 8..15 (chunk 2*psel+1)
 #pragma unroll
-                        for (int part = 0; part < 4; ++part) {
-                            // chunk: low nibbles -> k = 16*psel + 8*part' ; high -> 32 + ...
-                            const bool hi = part >= 2;
-                            const int ch = (hi ? 4 : 0) + 2 * psel + (part & 1);
-                            const float fs = hi ? fs1 : fs0, fm = hi ? fm1 : fm0;
-                            uint32_t o[4];
-#pragma unroll
-                            for (int h2 = 0; h2 < 2; ++h2) {
-                                const uint32_t wv = qw[2 * (part & 1) + h2];
-                                const uint32_t nb = hi ? ((wv >> 4) & 0x0F0F0F0Fu) : (wv & 0x0F0F0F0Fu);
-                                o[2 * h2] = pack_h2(fmaf(nib_f(nb, 0), fs, -fm), fmaf(nib_f(nb, 1), fs, -fm));
-                                o[2 * h2 + 1] = pack_h2(fmaf(nib_f(nb, 2), fs, -fm), fmaf(nib_f(nb, 3), fs, -fm));
-                            }
-                            *reinterpret_cast<uint4*>(arow + swz(prow, ch)) = make_uint4(o[0], o[1], o[2], o[3]);
+                        for (int part = 0; part < 2; ++part) {
+                            uint32_t la[2], ha[2], lb[2], hb[2];
+                            q4_word_h2(qw[2 * part], hc, la, ha);
+                            q4_word_h2(qw[2 * part + 1], hc, lb, hb);
+                            const int ch = 2 * psel + part;
+                            *reinterpret_cast<uint4*>(arow + swz(prow, ch)) = make_uint4(la[0], la[1], lb[0], lb[1]);
+                            *reinterpret_cast<uint4*>(arow + swz(prow, 4 + ch)) = make_uint4(ha[0], ha[1], hb[0], hb[1]);
                         }
                     }
                 } else {
@@ -373,6 +401,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
                 }
                 fence_async_smem();
                 mbar_arrive(&full[g & 3]);
+                if (kb + 2 < nk) {
+                    issue_raw(kb + 2, g % kRawSlots);
+                    issue_b(kb + 2, (g + 2) % kBStages);
+                }
+                cp_commit();
             }
             cp_wait_all();
             if (!ok) break;
@@ -386,14 +419,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
                 tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c16, a);
                 if (MODE == kGateUp) {
                     uint32_t u[16];
-                    tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(kBN + c16), u);
+                    tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(BN + c16), u);
                     tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int col = c16 + j;
                         if (col < ti.ntok) {
                             const float gv = __uint_as_float(a[j]), uv = __uint_as_float(u[j]);
-                            const float hv = gv / (1.0f + expf(-gv)) * uv;
+                            const float hv = gv * __frcp_rn(1.0f + __expf(-gv)) * uv;
                             p.h_out[(int64_t)(ti.tok0 + col) * p.rows + ti.m0 + m] = __float2half_rn(hv);
                         }
                     }
@@ -429,7 +462,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
                         const uint64_t bd = sdesc(b0 + 32 * kk);
                         mma_f16(tmem, sdesc(a0 + 32 * kk), bd, idesc, (kb | kk) != 0);
                         if (MODE == kGateUp)
-                            mma_f16(tmem + kBN, sdesc(a0 + kBM * 128 + 32 * kk), bd, idesc, (kb | kk) != 0);
+                            mma_f16(tmem + BN, sdesc(a0 + kBM * 128 + 32 * kk), bd, idesc, (kb | kk) != 0);
                     }
                     mma_commit(&empty[g & 3]);
                     if (kb == nk - 1) mma_commit(accf);
@@ -458,15 +491,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
     }
 }
 
-// Token blocks of up to 128 pairs per expert: list[0].x = count, then (e, tok0, ntok, 0).
-__global__ void __launch_bounds__(1024) tile_list_kernel(const int32_t* __restrict__ offsets, int E,
+// Token blocks of up to bn pairs per expert: list[0].x = count, then (e, tok0, ntok, 0).
+__global__ void __launch_bounds__(1024) tile_list_kernel(const int32_t* __restrict__ offsets, int E, int bn,
                                                          int4* __restrict__ list) {
     __shared__ int warp_tot[32];
     __shared__ int total;
     const int e = threadIdx.x;
     int n = 0, o0 = 0;
     if (e < E) { o0 = offsets[e]; n = offsets[e + 1] - o0; }
-    const int nb = (n + kBN - 1) / kBN;
+    const int nb = (n + bn - 1) / bn;
     // block exclusive scan of nb
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int inc = nb;
@@ -490,7 +523,7 @@ __global__ void __launch_bounds__(1024) tile_list_kernel(const int32_t* __restri
     }
     __syncthreads();
     const int base = inc - nb + warp_tot[warp];
-    for (int b = 0; b < nb; ++b) list[1 + base + b] = make_int4(e, o0 + b * kBN, min(kBN, n - b * kBN), 0);
+    for (int b = 0; b < nb; ++b) list[1 + base + b] = make_int4(e, o0 + b * bn, min(bn, n - b * bn), 0);
     if (threadIdx.x == 0) list[0] = make_int4(total, 0, 0, 0);
 }
 
@@ -512,7 +545,7 @@ __global__ void to_half_kernel(const void* __restrict__ x, bool bf16, int64_t n,
 template <int QT, int MODE>
 size_t tc_smem_bytes() {
     constexpr int a = kAStages * (MODE == kGateUp ? 2 : 1) * kBM * 128;
-    constexpr int b = kBStages * kBN * 128;
+    constexpr int b = kBStages * tc_bn<QT>() * 128;
     constexpr int r = kRawSlots * kProducers * RawCfg<QT, MODE>::kBytes;
     return (size_t)a + b + r + 128 + 1024;   // barriers + alignment slack
 }
@@ -548,7 +581,7 @@ cudaError_t launch_tc_q(int qtype, const TcParams& p, int max_tiles, cudaStream_
 
 size_t tc_tile_list_bytes(int T, int k, int E) {
     const int64_t P = (int64_t)T * k;
-    return align_up((size_t)(1 + P / kBN + E + 1) * sizeof(int4), 256);
+    return align_up((size_t)(1 + P / kBNMin + E + 1) * sizeof(int4), 256);
 }
 
 bool tc_supported(int qtype, int rows_gu, int K_gu) {
@@ -566,18 +599,19 @@ cudaError_t launch_tc_expert_ffn(const TcFfnArgs& a, cudaStream_t s) {
         to_half_kernel<<<(unsigned)((n / 4 + 255) / 256), 256, 0, s>>>(a.x, a.x_bf16, n, a.x16);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
+    const int bn = a.qtype == MOE_Q4_K ? tc_bn<MOE_Q4_K>() : tc_bn<MOE_Q8_0>();
     int max_tb;
     if (!a.identity) {
-        tile_list_kernel<<<1, 1024, 0, s>>>(a.offsets, a.E, a.tb_list);
+        tile_list_kernel<<<1, 1024, 0, s>>>(a.offsets, a.E, bn, a.tb_list);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
-        max_tb = P / kBN + a.E;
+        max_tb = P / bn + a.E;
     } else {
-        max_tb = (P + kBN - 1) / kBN;
+        max_tb = (P + bn - 1) / bn;
     }
     TcParams gu{};
     gu.w0 = a.wg; gu.w1 = a.wu; gu.expert_stride = a.stride_gu; gu.rows = a.I; gu.K = a.H; gu.k = a.k;
     gu.bsrc = a.x16; gu.sorted_pairs = a.identity ? nullptr : a.sorted_pairs;
-    gu.tb_list = a.identity ? nullptr : a.tb_list; gu.n_identity = a.identity ? a.T : 0;
+    gu.tb_list = a.identity ? nullptr : a.tb_list; gu.n_identity = a.identity ? a.T : 0; gu.bn = bn;
     gu.h_out = a.h16; gu.hdr = a.hdr;
     if (a.ev_before_gateup && (err = cudaEventRecord(a.ev_before_gateup, s)) != cudaSuccess) return err;
     if ((err = launch_tc_q<kGateUp>(a.qtype, gu, max_tb * (a.I / kBM), s)) != cudaSuccess) return err;
@@ -585,7 +619,7 @@ cudaError_t launch_tc_expert_ffn(const TcFfnArgs& a, cudaStream_t s) {
     TcParams dn{};
     dn.w0 = a.wd; dn.expert_stride = a.stride_d; dn.rows = a.H; dn.K = a.I; dn.k = a.k;
     dn.bsrc = a.h16; dn.sorted_pairs = nullptr;
-    dn.tb_list = gu.tb_list; dn.n_identity = gu.n_identity;
+    dn.tb_list = gu.tb_list; dn.n_identity = gu.n_identity; dn.bn = bn;
     dn.y_out = a.y; dn.hdr = a.hdr;
     return launch_tc_q<kDown>(a.qtype, dn, max_tb * (a.H / kBM), s);
 }
