@@ -96,7 +96,8 @@ namespace {
 // Workspace of moe_layer for T tokens (offsets in bytes, all 256-aligned).
 struct LayerWs {
     bool tc;                      // tensor-core path for this T
-    size_t hdr, logits, ids, w, sorted, pair_pos, offsets, chunk, h, y, sh_h, sh_y, x16, tiles, total;
+    size_t hdr, logits, ids, w, sorted, pair_pos, offsets, chunk, h, y, sh_h, sh_y, x16, tiles, wsplit, total;
+    bool router_tc;               // router logits on the tensor cores
 };
 
 bool use_tc(const moe_layer_desc& d, int T) {
@@ -166,6 +167,8 @@ LayerWs layer_ws(const moe_layer_desc& d, int T) {
     w.sh_y = take(Is > 0 ? (size_t)T * H * 4 : 0);
     w.x16 = take(w.tc ? (size_t)T * H * 2 : 0);
     w.tiles = take(w.tc ? tc_tile_list_bytes(T, k, E) : 0);
+    w.router_tc = router_tc_supported(T, H, E, d.x_type == MOE_BF16);
+    w.wsplit = take(w.router_tc ? router_tc_split_bytes(H, E) : 0);
     w.total = o;
     return w;
 }
@@ -491,7 +494,8 @@ moe_status moe_layer_timed(const moe_layer_plan* plan, const void* x, int T, flo
         if (err != cudaSuccess) return cuda_fail(err, "decode chain kernels");
         return MOE_OK;
     }
-    err = launch_router_logits(x, xb, T, H, d.W_router, E, logits, hdr, s);
+    err = w.router_tc ? launch_router_tc(x, T, H, d.W_router, E, logits, at<void>(workspace, w.wsplit), hdr, s)
+                      : launch_router_logits(x, xb, T, H, d.W_router, E, logits, hdr, s);
     if (err != cudaSuccess) return cuda_fail(err, "router logits kernel");
     err = launch_topk(d.route, logits, d.bias, T, ids, gw, nullptr, s);
     if (err != cudaSuccess) return cuda_fail(err, "top-k kernel");

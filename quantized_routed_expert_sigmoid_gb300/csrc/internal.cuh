@@ -39,6 +39,12 @@ moe_status report(moe_status st, const char* msg);
 // ---------------------------------------------------------------- route
 cudaError_t launch_router_logits(const void* x, bool x_bf16, int T, int H, const float* W, int E,
                                  float* logits, WsHeader* clear_hdr, cudaStream_t s);
+// Router logits on the tensor cores (router_tc.cu): x bf16, W split into three bf16 parts
+// in w3 (router_tc_split_bytes(H, E) of device memory).
+bool router_tc_supported(int T, int H, int E, bool x_bf16);
+size_t router_tc_split_bytes(int H, int E);
+cudaError_t launch_router_tc(const void* x, int T, int H, const float* W, int E, float* logits, void* w3,
+                             WsHeader* clear_hdr, cudaStream_t s);
 cudaError_t launch_topk(const moe_route_cfg& cfg, const float* logits, const float* bias, int T,
                         int32_t* ids, float* w, WsHeader* clear_hdr, cudaStream_t s);
 
