@@ -96,7 +96,7 @@ namespace {
 // Workspace of moe_layer for T tokens (offsets in bytes, all 256-aligned).
 struct LayerWs {
     bool tc;                      // tensor-core path for this T
-    size_t hdr, logits, ids, w, sorted, pair_pos, offsets, chunk, h, y, sh_h, sh_y, x16, tiles, wsplit, total;
+    size_t hdr, logits, ids, w, sorted, pair_pos, offsets, chunk, h, y, sh_h, sh_y, x16, tiles, wsplit, hq, hq_s, total;
     bool router_tc;               // router logits on the tensor cores
 };
 
@@ -169,6 +169,9 @@ LayerWs layer_ws(const moe_layer_desc& d, int T) {
     w.tiles = take(w.tc ? tc_tile_list_bytes(T, k, E) : 0);
     w.router_tc = router_tc_supported(T, H, E, d.x_type == MOE_BF16);
     w.wsplit = take(w.router_tc ? router_tc_split_bytes(H, E) : 0);
+    const bool chain = decode_chain_applies(d, T);
+    w.hq = take(chain ? P * (size_t)(I / 64) * 272 : 0);
+    w.hq_s = take(chain && Is > 0 ? (size_t)T * (Is / 64) * 272 : 0);
     w.total = o;
     return w;
 }
@@ -487,6 +490,8 @@ moe_status moe_layer_timed(const moe_layer_plan* plan, const void* x, int T, flo
         da.logits = logits; da.ids = ids; da.gw = gw; da.sorted = sorted; da.offsets = offs; da.pair_pos = ppos;
         da.h = at<float>(workspace, w.h);
         da.h_s = at<float>(workspace, w.sh_h);
+        da.hq = at<uint8_t>(workspace, w.hq);
+        da.hq_s = at<uint8_t>(workspace, w.hq_s);
         da.out = out;
         da.accumulate = d.accumulate != 0;
         da.hdr = hdr;

@@ -67,8 +67,9 @@ struct ChainParams {
     int32_t* sorted;
     int32_t* offsets;
     int32_t* pair_pos;
-    float* h;
-    float* h_s;
+    uint8_t* hq;                            // [P][272 * I/64]: h of each pair (sorted position) as staged planes
+    uint8_t* hq_s;                          // [T][272 * I_s/64]: the shared expert's h (Q4_K shared expert)
+    float* h_s;                             // [T][I_s] fp32: the shared expert's h (Q8_0 shared expert)
     float* out;
     int accumulate;
     WsHeader* hdr;
@@ -98,6 +99,34 @@ __device__ __forceinline__ void prefetch_l2(const uint8_t* src, int64_t bytes) {
     }
 }
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+// One warp stages the 32 consecutive values v (lane = element) of sub-block sb of a vector
+// of G groups into dst: the layout qd4_stage gives a staged vector (X: 16 x G uint4 of byte
+// planes {hi, mid, lo, 0} of 4 values, then XS: G float4 {scale lo, scale hi, sum lo, sum hi}).
+__device__ __forceinline__ void warp_stage_subblock(float v, uint8_t* dst, int G, int sb, int lane) {
+    float m = fabsf(v), sum = v;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    }
+    const float inv = m > 0.f ? 8388607.0f / m : 0.f;
+    int x24 = __float2int_rn(v * inv);
+    x24 = max(-8388607, min(8388607, x24));
+    uint32_t hb = ((uint32_t)x24 >> 16) & 0xFFu, mb = ((uint32_t)x24 >> 8) & 0xFFu, lb = (uint32_t)x24 & 0xFFu;
+#pragma unroll
+    for (int b = 1; b < 4; ++b) {
+        hb |= __shfl_down_sync(0xffffffffu, ((uint32_t)x24 >> 16) & 0xFFu, b) << (8 * b);
+        mb |= __shfl_down_sync(0xffffffffu, ((uint32_t)x24 >> 8) & 0xFFu, b) << (8 * b);
+        lb |= __shfl_down_sync(0xffffffffu, (uint32_t)x24 & 0xFFu, b) << (8 * b);
+    }
+    const int g = sb >> 1, hh = sb & 1;
+    if ((lane & 3) == 0) reinterpret_cast<uint4*>(dst)[(hh * 8 + (lane >> 2)) * G + g] = make_uint4(hb, mb, lb, 0u);
+    if (lane == 0) {
+        float* xs = reinterpret_cast<float*>(dst + (size_t)16 * G * 16) + 4 * g;
+        xs[hh] = m / 8388607.0f;
+        xs[2 + hh] = sum;
+    }
+}
 __device__ __forceinline__ float4 ld_nc_v4(const float4* q) {
     float4 v;
     asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(q));
@@ -125,24 +154,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
     while (!mbar_test(b, parity))
         if (gtime() - t0 > kWaitNs) return false;
     return true;
-}
-constexpr int kCluster = 8;                 // K3 CTAs per cluster (they share the staged h)
-__device__ __forceinline__ int cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return (int)r;
-}
-// Stores v at the address of *a in the shared memory of cluster CTA `peer`.
-__device__ __forceinline__ void st_peer(const uint4* a, int peer, const uint4& v) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(a)), "r"(peer));
-    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
-                 : "memory");
-}
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 // A bulk copy global -> shared whose bytes complete the transaction count of bar.
 __device__ __forceinline__ void bulk_to_smem(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -357,14 +368,25 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
             p.offsets[e] = cnt;
         }
     }
-    // ---- routed units through the ring
+    // ---- routed units through the ring.  The 16 warps of a CTA take 16 consecutive row pairs
+    // of one expert in each round: 32 rows of h, one staged sub-block, which the CTA stages
+    // itself (the values meet in shared memory) and writes out for the down kernel.  Every
+    // warp runs the same rounds, so the barrier below is reached uniformly, also after a
+    // copy that timed out (the warp then stops computing and issuing, not looping).
+    __shared__ float s_hq[2][kCMaxT][32];
+    const int vb = 272 * qd4_groups(I);            // bytes of one staged vector of h
     float acc[4][NT];
     int n = 0, st = 0;
     int vidx[NT];
     bool ok = true;
-    int item = 0;
-    for (; item < n_items; ++item) {
-        if (!mbar_wait(&s_bar[warp][item & 1], (uint32_t)(item >> 1) & 1u)) { ok = false; break; }
+    int round = 0, waited = 0, issued = min(2, n_items);
+    for (int item = 0; item < n_items; ++item) {
+        const bool have = ok && mbar_wait(&s_bar[warp][item & 1], (uint32_t)(item >> 1) & 1u);
+        if (ok && !have) {
+            ok = false;
+            if (lane == 0) atomicExch(&p.hdr->status, (int)MOE_ERR_TIMEOUT);
+        }
+        if (have) waited = item + 1;
         const int u = wg + (item / nch) * W, ch = item - (item / nch) * nch;
         if (ch == 0) {
 #pragma unroll
@@ -378,7 +400,7 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
             for (int t = 0; t < NT; ++t) vidx[t] = R.tok[st + min(t, n - 1)];
         }
         const int g = ch * 32 + lane;
-        if (g < G) {
+        if (have && g < G) {
             const uint8_t* blk = ring + (item & 1) * kSlotBytes + (lane >> 2) * kQ4KBytes;
             const int c = lane & 3;
             uint4 hd[4], q0[4], q1[4];
@@ -393,28 +415,32 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
             qd4_group_math<NT, 4>(hd, q0, q1, live, 0, g, G, X, XS, n, acc, vidx);
         }
         __syncwarp();                              // every lane is done with the slot
-        issue(item + 2);
+        if (ok && item + 2 < n_items) {
+            issue(item + 2);
+            issued = item + 3;
+        }
         if (ch == nch - 1) {
             qd_warp_reduce<NT>(acc);
+            const int a = u / half_I, r0 = 2 * (u - a * half_I);
             if (lane < 2 * NT) {
                 const int t = lane >> 1, ri = lane & 1;
                 if (t < n) {
-                    const int a = u / half_I, r0 = 2 * (u - a * half_I);
                     const float gv = qd_pick<NT>(acc, 2 * ri, t), uv = qd_pick<NT>(acc, 2 * ri + 1, t);
-                    p.h[(int64_t)(st + t) * I + r0 + ri] = silu_mul(gv, uv);
+                    s_hq[round & 1][t][(r0 & 31) + ri] = silu_mul(gv, uv);
                 }
             }
+            __syncthreads();
+            if (warp < n)
+                warp_stage_subblock(s_hq[round & 1][warp][lane], p.hq + (size_t)(st + warp) * vb, qd4_groups(I), r0 >> 5,
+                                    lane);
+            ++round;
         }
     }
-    if (!ok) {
-        // a copy never completed: report it, and let no copy land after the CTA exits
-        if (lane == 0) {
-            atomicExch(&p.hdr->status, (int)MOE_ERR_TIMEOUT);
-            for (int i = item; i < min(item + 2, n_items); ++i) mbar_wait(&s_bar[warp][i & 1], (uint32_t)(i >> 1) & 1u);
-        }
-        __syncwarp();
-        return;
+    if (!ok && lane == 0) {
+        // let no copy land after the CTA exits: wait (bounded) for the ones still in flight
+        for (int i = waited; i < issued; ++i) mbar_wait(&s_bar[warp][i & 1], (uint32_t)(i >> 1) & 1u);
     }
+    __syncwarp();
     // ---- the shared expert's row pairs (direct loads)
     if constexpr (has_shared) {
     for (int u = wg + my_units * W; u < Ur + Us; u += W) {
@@ -440,12 +466,27 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
             qd4_rows4<NT, false>(rowp, H / kQ4KWeights, X, XS, T, lane, sacc, sv);
         }
         qd_warp_reduce<NT>(sacc);
-        if (lane < 2 * NT) {
-            const int t = lane >> 1, ri = lane & 1;
-            if (t < T) {
-                const float gv = qd_pick<NT>(sacc, ri, t), uv = qd_pick<NT>(sacc, 2 + ri, t);
-                p.h_s[(int64_t)t * p.I_s + r0 + ri] = silu_mul(gv, uv);
+        if constexpr (kSh == 2) {
+            if (lane < 2 * NT) {
+                const int t = lane >> 1, ri = lane & 1;
+                if (t < T) {
+                    const float gv = qd_pick<NT>(sacc, ri, t), uv = qd_pick<NT>(sacc, 2 + ri, t);
+                    p.h_s[(int64_t)t * p.I_s + r0 + ri] = silu_mul(gv, uv);
+                }
             }
+        } else {
+            if (lane < 2 * NT) {
+                const int t = lane >> 1, ri = lane & 1;
+                if (t < T) {
+                    const float gv = qd_pick<NT>(sacc, ri, t), uv = qd_pick<NT>(sacc, 2 + ri, t);
+                    s_hq[round & 1][t][(r0 & 31) + ri] = silu_mul(gv, uv);
+                }
+            }
+            __syncthreads();
+            if (warp < T)
+                warp_stage_subblock(s_hq[round & 1][warp][lane], p.hq_s + (size_t)warp * 272 * qd4_groups(p.I_s),
+                                    qd4_groups(p.I_s), r0 >> 5, lane);
+            ++round;
         }
     }
     }
@@ -466,10 +507,13 @@ __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_con
     const int R = p.rows_per_cta, n0 = blockIdx.x * R;
     constexpr bool has_shared = kSh != 0;
     const int64_t rbI = (int64_t)(I / kQ4KWeights) * kQ4KBytes;
-    uint4* HX = reinterpret_cast<uint4*>(smem);
-    float4* HXS = reinterpret_cast<float4*>(HX + (size_t)P * 16 * GI);
+    const int vb = 272 * GI;                                             // bytes of one staged h vector
+    uint8_t* hsm = smem;                                                 // [P][vb]: h of pair s, staged
     float* ybuf = reinterpret_cast<float*>(smem + p.k3_off_y);          // [P + T][R]
     uint8_t* wbuf = smem + p.k3_off_w;                                   // [P][R][rbI] when prefetching
+    uint4* SX = reinterpret_cast<uint4*>(smem + p.k3_off_hs_s);          // Q4_K shared expert: [T][16 GS] uint4
+    const int GS = kSh == 1 ? qd4_groups(p.I_s) : 1;
+    float4* SXS = reinterpret_cast<float4*>(SX + (size_t)T * 16 * GS);   // then [T][GS] float4
     pdl_wait();                                   // h and the routing of K2
     pdl_launch_dependents();
     if (tid == 0) {
@@ -482,60 +526,37 @@ __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_con
         s_w[i] = __ldcg(p.gw + i);
     }
     __syncthreads();
-    // ---- the CTA's down rows of every pair to shared memory (in flight while h is staged):
-    // rows n0.. of one expert are contiguous, one bulk copy per pair
+    // ---- bulk copies into shared memory, all completing on one mbarrier: the CTA's down rows
+    // of every pair (rows n0.. of one expert are contiguous: one copy per pair), and every
+    // pair's h, which the gate/up kernel wrote already staged (one copy per pair)
     const int nrows = min(R, H - n0);
-    if (p.k3_prefetch && tid == 0 && nrows > 0) {
-        const uint32_t bytes = (uint32_t)(nrows * rbI);
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&s_wbar)), "r"(P * bytes)
+    const bool wcopy = p.k3_prefetch && nrows > 0;
+    if (tid == 0) {
+        uint32_t total = (uint32_t)P * vb;
+        if (wcopy) total += (uint32_t)(P * nrows * rbI);
+        if (kSh == 1) total += (uint32_t)T * 272 * GS;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&s_wbar)), "r"(total)
                      : "memory");
-        for (int s = 0; s < P; ++s)
-            bulk_to_smem(wbuf + (int64_t)s * R * rbI, p.wd + (int64_t)s_e[s] * p.stride_d + (int64_t)n0 * rbI, bytes,
-                         &s_wbar);
     }
-    // ---- stage every pair's h (row pair_pos[s] of h) and the shared expert's h_s.  The CTAs
-    // of a cluster split the vectors (rank r takes s = r, r + kCluster, ...), stage them,
-    // and write the planes into every CTA of the cluster.
-    const int rank = cluster_rank();
-    for (int s = rank; s < P; s += kCluster)
-        qd4_stage_par(p.h, false, true, I, 1, &s_pos[s], I, HX + (size_t)s * 16 * GI, HXS + (size_t)s * GI, tid,
-                      kK3Threads);
-    uint4* SX = reinterpret_cast<uint4*>(smem + p.k3_off_hs_s);
-    const int GS = kSh == 1 ? qd4_groups(p.I_s) : 1;
-    float4* SXS = reinterpret_cast<float4*>(SX + (size_t)T * 16 * GS);
-    if constexpr (kSh == 2) {
+    if (warp == 0 && wcopy) {
+        for (int s = lane; s < P; s += 32)
+            bulk_to_smem(wbuf + (int64_t)s * R * rbI, p.wd + (int64_t)s_e[s] * p.stride_d + (int64_t)n0 * rbI,
+                         (uint32_t)(nrows * rbI), &s_wbar);
+    } else if (warp == 1) {
+        for (int s = lane; s < P; s += 32)
+            bulk_to_smem(hsm + (size_t)s * vb, p.hq + (size_t)s_pos[s] * vb, (uint32_t)vb, &s_wbar);
+    } else if (warp == 2 && kSh == 1) {
+        for (int t = lane; t < T; t += 32) {
+            const uint8_t* src = p.hq_s + (size_t)t * 272 * GS;
+            bulk_to_smem(SX + (size_t)t * 16 * GS, src, (uint32_t)(256 * GS), &s_wbar);
+            bulk_to_smem(SXS + (size_t)t * GS, src + 256 * GS, (uint32_t)(16 * GS), &s_wbar);
+        }
+    }
+    if constexpr (kSh == 2) {                          // Q8_0 shared expert: its h is fp32
         float4* hs = reinterpret_cast<float4*>(smem + p.k3_off_hs_s);
         qd_stage_many_f32<MOE_Q8_0>(p.h_s, p.I_s, T, p.I_s, p.it_Is_s, hs, tid, kK3Threads);
-    } else if constexpr (kSh == 1) {
-        for (int t = rank; t < T; t += kCluster)
-            qd4_stage_par(p.h_s + (int64_t)t * p.I_s, false, true, p.I_s, 1, nullptr, p.I_s, SX + (size_t)t * 16 * GS,
-                          SXS + (size_t)t * GS, tid, kK3Threads);
     }
-    __syncthreads();
-    {
-        const int per_x = 16 * GI, per_s = GI;        // uint4 / float4 per staged vector
-        for (int s = rank; s < P; s += kCluster) {
-            for (int i = tid; i < per_x + per_s; i += kK3Threads) {
-                uint4* a = i < per_x ? HX + (size_t)s * per_x + i
-                                     : reinterpret_cast<uint4*>(HXS + (size_t)s * per_s + (i - per_x));
-                const uint4 v = *a;
-                for (int q = 1; q < kCluster; ++q) st_peer(a, (rank + q) % kCluster, v);
-            }
-        }
-        if constexpr (kSh == 1) {
-            const int sx_x = 16 * GS, sx_s = GS;
-            for (int t = rank; t < T; t += kCluster) {
-                for (int i = tid; i < sx_x + sx_s; i += kK3Threads) {
-                    uint4* a = i < sx_x ? SX + (size_t)t * sx_x + i
-                                        : reinterpret_cast<uint4*>(SXS + (size_t)t * sx_s + (i - sx_x));
-                    const uint4 v = *a;
-                    for (int q = 1; q < kCluster; ++q) st_peer(a, (rank + q) % kCluster, v);
-                }
-            }
-        }
-    }
-    cluster_sync();                                   // every plane of every vector is in every CTA
-    const bool landed = !p.k3_prefetch || nrows <= 0 || mbar_wait(&s_wbar, 0u);
+    const bool landed = mbar_wait(&s_wbar, 0u);
     if (__syncthreads_or(!landed)) {
         // the copies did not complete in time: report it; let none land after the CTA exits
         if (tid == 0) {
@@ -554,8 +575,8 @@ __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_con
             const int row = lane >> 2, sub = lane & 3;
             const int rl = 8 * sb + row, n = n0 + rl;
             float acc[4][1] = {{0.f}, {0.f}, {0.f}, {0.f}};
-            const uint4* Xs = HX + (size_t)s * 16 * GI;
-            const float4* XSs = HXS + (size_t)s * GI;
+            const uint4* Xs = reinterpret_cast<const uint4*>(hsm + (size_t)s * vb);
+            const float4* XSs = reinterpret_cast<const float4*>(hsm + (size_t)s * vb + 256 * GI);
             if (p.k3_prefetch) {
                 const uint8_t* const rowp[4] = {n < H ? wbuf + ((int64_t)s * R + rl) * rbI : nullptr, nullptr, nullptr,
                                                 nullptr};
@@ -697,18 +718,9 @@ cudaError_t launch_chain_nt(const ChainParams& p, const ChainLayout& L, int E, c
     if ((err = cudaFuncSetAttribute(chain_down_kernel<NT, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)L.k3_smem)) != cudaSuccess)
         return err;
-    const int n3 = (p.H + L.rows_per_cta - 1) / L.rows_per_cta;
-    cfg.gridDim = dim3((n3 + kCluster - 1) / kCluster * kCluster);
+    cfg.gridDim = dim3((p.H + L.rows_per_cta - 1) / L.rows_per_cta);
     cfg.blockDim = dim3(kK3Threads);
     cfg.dynamicSmemBytes = L.k3_smem;
-    cudaLaunchAttribute attr3[2];
-    attr3[0] = attr[0];
-    attr3[1].id = cudaLaunchAttributeClusterDimension;
-    attr3[1].val.clusterDim.x = kCluster;
-    attr3[1].val.clusterDim.y = 1;
-    attr3[1].val.clusterDim.z = 1;
-    cfg.attrs = attr3;
-    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, chain_down_kernel<NT, Q8>, p);
 }
 
@@ -729,7 +741,7 @@ ChainParams chain_params(const DecodeArgs& a, const ChainLayout& L) {
     p.sg = a.sg; p.su = a.su; p.sd = a.sd;
     p.logits = a.logits; p.ids = a.ids; p.gw = a.gw; p.sorted = a.sorted; p.offsets = a.offsets;
     p.pair_pos = a.pair_pos;
-    p.h = a.h; p.h_s = a.h_s; p.out = a.out; p.accumulate = a.accumulate ? 1 : 0;
+    p.hq = a.hq; p.hq_s = a.hq_s; p.h_s = a.h_s; p.out = a.out; p.accumulate = a.accumulate ? 1 : 0;
     p.hdr = a.hdr;
     p.it_H_s = L.it_H_s; p.it_Is_s = L.it_Is_s;
     p.k2_warps = L.k2_warps; p.k2_off_xs_s = L.k2_off_xs_s; p.k2_off_ring = L.k2_off_ring;
@@ -757,7 +769,7 @@ bool decode_chain_supported(const DecodeArgs& a) {
     }
     if ((a.stride_gu % 16) || (a.stride_d % 16)) return false;
     const ChainLayout L = chain_layout(a);
-    return L.k2_warps >= 4 && L.k2_smem <= kChainSmemCap && L.k3_smem <= kChainSmemCap;
+    return L.k2_warps == kK2MaxWarps && L.k2_smem <= kChainSmemCap && L.k3_smem <= kChainSmemCap;
 }
 
 cudaError_t launch_decode_chain(const DecodeArgs& a, cudaStream_t s, cudaEvent_t evb, cudaEvent_t eva) {

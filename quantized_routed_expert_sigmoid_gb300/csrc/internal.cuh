@@ -109,6 +109,8 @@ struct DecodeArgs {
     int32_t* pair_pos;
     float* h;
     float* h_s;
+    uint8_t* hq;                  // chain: every pair's h, staged (272 * I/64 bytes per pair)
+    uint8_t* hq_s;                // chain: the Q4_K shared expert's h, staged (T vectors)
     float* out;
     bool accumulate;
     WsHeader* hdr;

@@ -227,8 +227,17 @@ def test_decode_chain_matches_separate_kernels(T):
     _chain_vs_separate(make_layer(synth.DECODE, 50 + T, T), T)
 
 
-def test_decode_chain_deepseek_shape():
-    _chain_vs_separate(make_layer(synth.DEEPSEEK, 60, 2), 2)
+def test_decode_chain_q8_shared_expert():
+    shape = synth.LayerShape(H=2048, E=64, k=4, I=768, qtype=synth.Q4_K, mode="sigmoid_group", n_groups=8,
+                             topk_groups=4, scale=2.5, I_s=512, shared_qtype=synth.Q8_0, bias_std=0.1)
+    tl = make_layer(shape, 60, 2, exact_all=True)
+    _chain_vs_separate(tl, 2)
+    _check_layer(tl, 2)
+
+
+def test_deepseek_shape_decode_takes_gemv_path():
+    # hidden 7168 leaves the gate/up kernel fewer than 16 warps: the layer runs the GEMV kernels
+    assert make_layer(synth.DEEPSEEK, 60, 2).moe_layer().path(2) == "gemv"
 
 
 def test_decode_chain_q4k_shared_expert():
