@@ -167,7 +167,9 @@ LayerWs layer_ws(const moe_layer_desc& d, int T) {
     w.sh_y = take(Is > 0 ? (size_t)T * H * 4 : 0);
     w.x16 = take(w.tc ? (size_t)T * H * 2 : 0);
     w.tiles = take(w.tc ? tc_tile_list_bytes(T, k, E) : 0);
-    w.router_tc = router_tc_supported(T, H, E, d.x_type == MOE_BF16);
+    // tensor-core router logits only on the tensor-core path: their fp32 accumulation inside the
+    // MMA is within that path's tolerance, not within the GEMV path's
+    w.router_tc = w.tc && router_tc_supported(T, H, E, d.x_type == MOE_BF16);
     w.wsplit = take(w.router_tc ? router_tc_split_bytes(H, E) : 0);
     const bool chain = decode_chain_applies(d, T);
     w.hq = take(chain ? P * (size_t)(I / 64) * 272 : 0);
@@ -213,12 +215,30 @@ moe_status check_ffn_common(int E, int k, int T, int H, int I, const int32_t* so
     return MOE_OK;
 }
 
+// Routed gate/up (h fp32 [P][I]) and down (y fp32 [P][H]): the segmented persistent kernels
+// when the shape allows them (routed experts with a permutation), else the per-expert GEMV.
+cudaError_t routed_gateup(const moe_qmat& gate, const moe_qmat& up, int E, const void* x, bool x_bf16, int T, int H,
+                          int I, const int32_t* sorted, const int32_t* offsets, int k, float* h, WsHeader* hdr,
+                          cudaStream_t s) {
+    if (sorted && offsets && gate.qtype == up.qtype && seg_gemv_supported(gate.qtype, E, H, I))
+        return launch_seg_gemv(true, x, x_bf16, sorted, offsets, E, k, H, I, static_cast<const uint8_t*>(gate.data),
+                               static_cast<const uint8_t*>(up.data), gate.expert_stride_bytes, h, hdr, T, s);
+    return launch_qgemv(gemv_args(gate, &up, E, x, x_bf16, I, H, sorted, offsets, k, T * k, h), s);
+}
+cudaError_t routed_down(const moe_qmat& down, int E, const float* h, int T, int H, int I, const int32_t* sorted,
+                        const int32_t* offsets, int k, float* y, WsHeader* hdr, cudaStream_t s) {
+    if (sorted && offsets && seg_gemv_supported(down.qtype, E, H, I))
+        return launch_seg_gemv(false, h, false, sorted, offsets, E, k, I, H, static_cast<const uint8_t*>(down.data),
+                               nullptr, down.expert_stride_bytes, y, hdr, T, s);
+    return launch_qgemv(gemv_args(down, nullptr, E, h, false, H, I, sorted, offsets, k, T * k, y), s);
+}
+
 moe_status run_ffn(const moe_qmat& gate, const moe_qmat& up, const moe_qmat& down, int E, const void* x,
                    bool x_bf16, int T, int H, int I, const int32_t* sorted, const int32_t* offsets, int k,
-                   float* h, float* y, cudaStream_t s) {
-    cudaError_t err = launch_qgemv(gemv_args(gate, &up, E, x, x_bf16, I, H, sorted, offsets, k, T * k, h), s);
+                   float* h, float* y, cudaStream_t s, WsHeader* hdr = nullptr) {
+    cudaError_t err = routed_gateup(gate, up, E, x, x_bf16, T, H, I, sorted, offsets, k, h, hdr, s);
     if (err != cudaSuccess) return cuda_fail(err, "gate/up kernel");
-    err = launch_qgemv(gemv_args(down, nullptr, E, h, false, H, I, sorted, offsets, k, T * k, y), s);
+    err = routed_down(down, E, h, T, H, I, sorted, offsets, k, y, hdr, s);
     if (err != cudaSuccess) return cuda_fail(err, "down kernel");
     return MOE_OK;
 }
@@ -351,8 +371,8 @@ moe_status moe_expert_gateup(const moe_qmat* gate, const moe_qmat* up, int E, co
     if (x_type != MOE_F32 && x_type != MOE_BF16) return fail(MOE_ERR_UNSUPPORTED, "x_type %d", (int)x_type);
     if (T == 0) return MOE_OK;
     if (!x || !h || !aligned(x, 16) || !aligned(h, 16)) return fail(MOE_ERR_INVALID_ARG, "x / h NULL or misaligned");
-    cudaError_t err = launch_qgemv(gemv_args(*gate, up, E, x, x_type == MOE_BF16, I, H, sorted_pairs, offsets, k,
-                                             T * k, h), reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t err = routed_gateup(*gate, *up, E, x, x_type == MOE_BF16, T, H, I, sorted_pairs, offsets, k, h,
+                                    nullptr, reinterpret_cast<cudaStream_t>(stream));
     if (err != cudaSuccess) return cuda_fail(err, "gate/up kernel");
     return MOE_OK;
 }
@@ -366,8 +386,8 @@ moe_status moe_expert_down(const moe_qmat* down, int E, const float* h, int T, i
     if (T == 0) return MOE_OK;
     if (!h || !y_pairs || !aligned(h, 16) || !aligned(y_pairs, 16))
         return fail(MOE_ERR_INVALID_ARG, "h / y_pairs NULL or misaligned");
-    cudaError_t err = launch_qgemv(gemv_args(*down, nullptr, E, h, false, H, I, sorted_pairs, offsets, k, T * k,
-                                             y_pairs), reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t err = routed_down(*down, E, h, T, H, I, sorted_pairs, offsets, k, y_pairs, nullptr,
+                                  reinterpret_cast<cudaStream_t>(stream));
     if (err != cudaSuccess) return cuda_fail(err, "down kernel");
     return MOE_OK;
 }
@@ -548,11 +568,10 @@ moe_status moe_layer_timed(const moe_layer_plan* plan, const void* x, int T, flo
         }
     } else {
         if (evb && (err = cudaEventRecord(evb, s)) != cudaSuccess) return cuda_fail(err, "event record");
-        err = launch_qgemv(gemv_args(d.gate, &d.up, E, x, xb, I, H, sorted, offs, k, T * k, at<float>(workspace, w.h)), s);
+        err = routed_gateup(d.gate, d.up, E, x, xb, T, H, I, sorted, offs, k, at<float>(workspace, w.h), hdr, s);
         if (err != cudaSuccess) return cuda_fail(err, "gate/up kernel");
         if (eva && (err = cudaEventRecord(eva, s)) != cudaSuccess) return cuda_fail(err, "event record");
-        err = launch_qgemv(gemv_args(d.down, nullptr, E, at<float>(workspace, w.h), false, H, I, sorted, offs, k,
-                                     T * k, y), s);
+        err = routed_down(d.down, E, at<float>(workspace, w.h), T, H, I, sorted, offs, k, y, hdr, s);
         if (err != cudaSuccess) return cuda_fail(err, "down kernel");
         moe_status st;
         if (d.shared_intermediate > 0) {

@@ -76,6 +76,12 @@ struct GemvArgs {
     float* out;                 // h [P][rows] or y [P][rows], fp32
 };
 cudaError_t launch_qgemv(const GemvArgs& a, cudaStream_t s);
+// Routed experts' gate/up (h fp32 [P][I]) or down (y fp32 [P][H]) for a few tokens per
+// expert: persistent CTAs over contiguous unit ranges, bulk-copy ring (gemv_seg.cu).
+bool seg_gemv_supported(int qtype, int E, int H, int I);
+cudaError_t launch_seg_gemv(bool gateup, const void* vin, bool vin_bf16, const int32_t* sorted_pairs,
+                            const int32_t* offsets, int E, int k, int K, int rows, const uint8_t* w0, const uint8_t* w1,
+                            int64_t expert_stride, float* out, WsHeader* hdr, int max_tokens, cudaStream_t s);
 
 // ---------------------------------------------------------------- combine, norm
 cudaError_t launch_combine(const float* y_pairs, const float* w, const int32_t* pair_pos, int T, int k,

@@ -12,6 +12,8 @@
 // takes 4 weight rows at a time (gate/up: 2 rows of each matrix) so one read
 // of the staged activations feeds four rows (see qdot.cuh for the walk).
 // Reductions run in a fixed order: the same bits on every run.
+#include <algorithm>
+
 #include "internal.cuh"
 #include "qdot.cuh"
 
@@ -21,8 +23,16 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 
+// Requests [src, src + bytes) into L2 (a hint; 16-byte multiples, pieces of at most 64 KB).
+__device__ __forceinline__ void prefetch_rows_l2(const uint8_t* src, int64_t bytes) {
+    for (int64_t o = 0; o < bytes; o += 65536) {
+        const uint32_t n = (uint32_t)(bytes - o < 65536 ? bytes - o : 65536);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src + o), "r"(n) : "memory");
+    }
+}
+
 template <int QT, bool GATEUP, int NT>
-__global__ void __launch_bounds__(kThreads) qgemv_kernel(GemvArgs a, int iters, int units_per_warp) {
+__global__ void __launch_bounds__(kThreads, 2) qgemv_kernel(GemvArgs a, int iters, int units_per_warp) {
     extern __shared__ float4 xs[];                    // [NT][iters*256] float4
     float2* xsum = reinterpret_cast<float2*>(xs + (size_t)NT * iters * 256);  // [NT][iters*32]
     __shared__ int s_e, s_start, s_n;
@@ -66,6 +76,16 @@ __global__ void __launch_bounds__(kThreads) qgemv_kernel(GemvArgs a, int iters, 
     const uint8_t* w1 = GATEUP ? a.w1 + (int64_t)e * a.expert_stride : nullptr;
     const int n_units = a.rows / (GATEUP ? 2 : 4);
     const int slots = iters * 256;
+    // this CTA's weight rows (contiguous: units_per_warp units of every warp) into L2 before staging
+    if (threadIdx.x == 0) {
+        const int u0 = blockIdx.x * kWarps * units_per_warp;
+        const int u1 = min(n_units, u0 + kWarps * units_per_warp);
+        const int rpu = GATEUP ? 2 : 4;
+        if (u1 > u0 && (rb % 16) == 0) {
+            prefetch_rows_l2(w0 + (int64_t)u0 * rpu * rb, (int64_t)(u1 - u0) * rpu * rb);
+            if (GATEUP) prefetch_rows_l2(w1 + (int64_t)u0 * rpu * rb, (int64_t)(u1 - u0) * rpu * rb);
+        }
+    }
 
     __shared__ int s_rows[NT];
     for (int pb = 0; pb < n_tot; pb += NT) {
@@ -79,7 +99,7 @@ __global__ void __launch_bounds__(kThreads) qgemv_kernel(GemvArgs a, int iters, 
                 s_rows[threadIdx.x] = (GATEUP && a.sorted_pairs) ? a.sorted_pairs[i] / a.k : i;
             }
             __syncthreads();
-            qd4_stage(a.vin, a.vin_bf16, false, a.K, nt, s_rows, a.K, X, XS, threadIdx.x, kThreads);
+            qd4_stage_par(a.vin, a.vin_bf16, false, a.K, nt, s_rows, a.K, X, XS, threadIdx.x, kThreads);
             __syncthreads();
             for (int ui = 0; ui < units_per_warp; ++ui) {
                 const int unit = (blockIdx.x * kWarps + warp) * units_per_warp + ui;
@@ -180,8 +200,13 @@ cudaError_t launch_one(const GemvArgs& a, int iters, int grid_y, cudaStream_t s)
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
     }
+    // units per warp: enough that the grid is about two waves of two CTAs per SM
     const int n_units = a.rows / (GU ? 2 : 4);
-    const int upw = 1;
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t target_warps = (int64_t)kWarps * 4 * (sms > 0 ? sms : 152);
+    const int upw = (int)std::max<int64_t>(1, ((int64_t)n_units * grid_y + target_warps - 1) / target_warps);
     const int grid_x = (n_units + kWarps * upw - 1) / (kWarps * upw);
     qgemv_kernel<QT, GU, NT><<<dim3(grid_x, grid_y), kThreads, smem, s>>>(a, iters, upw);
     return cudaGetLastError();

@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(RouteCfgDev c, co
 cudaError_t launch_router_logits(const void* x, bool x_bf16, int T, int H, const float* W, int E,
                                  float* logits, WsHeader* clear_hdr, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
-    if (T <= 32) {
+    if (T < 128) {                                   // one CTA per (expert row, 4 tokens): enough CTAs
         dim3 grid(E, (T + kSmallTT - 1) / kSmallTT);
         logits_small_kernel<<<grid, 256, 0, s>>>(x, x_bf16, T, H, W, E, logits, clear_hdr);
     } else {

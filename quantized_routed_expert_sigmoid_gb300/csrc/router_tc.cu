@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kRThreads, 1) router_tc_kernel(const __grid_co
 }  // namespace
 
 bool router_tc_supported(int T, int H, int E, bool x_bf16) {
-    return x_bf16 && T >= 128 && H % kRK == 0 && E % 4 == 0 && E <= 1024;
+    return x_bf16 && T > 32 && H % kRK == 0 && E % 4 == 0 && E <= 1024;
 }
 
 size_t router_tc_split_bytes(int H, int E) { return (size_t)3 * E * H * sizeof(__nv_bfloat16); }
