@@ -420,14 +420,15 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
             issued = item + 3;
         }
         if (ch == nch - 1) {
-            qd_warp_reduce<NT>(acc);
+            // rows 0, 1 = gate, up of row r0; rows 2, 3 = gate, up of row r0 + 1
+            constexpr int sh = qd_red_shift<NT>();
+            const float gv = qd_warp_reduce_t<NT>(acc);
+            const float uv = __shfl_xor_sync(0xffffffffu, gv, NT << sh);
             const int a = u / half_I, r0 = 2 * (u - a * half_I);
-            if (lane < 2 * NT) {
-                const int t = lane >> 1, ri = lane & 1;
-                if (t < n) {
-                    const float gv = qd_pick<NT>(acc, 2 * ri, t), uv = qd_pick<NT>(acc, 2 * ri + 1, t);
-                    s_hq[round & 1][t][(r0 & 31) + ri] = silu_mul(gv, uv);
-                }
+            {
+                const int i = lane >> sh, r = i / NT, t = i - r * NT;
+                if ((r & 1) == 0 && (lane & ((1 << sh) - 1)) == 0 && t < n)
+                    s_hq[round & 1][t][(r0 & 31) + (r >> 1)] = silu_mul(gv, uv);
             }
             __syncthreads();
             if (warp < n)
@@ -465,23 +466,16 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
                                             p.su + (r0 + 1) * rbH};
             qd4_rows4<NT, false>(rowp, H / kQ4KWeights, X, XS, T, lane, sacc, sv);
         }
-        qd_warp_reduce<NT>(sacc);
+        // rows 0, 1 = gate of rows r0, r0 + 1; rows 2, 3 = up of the same rows
+        constexpr int sh = qd_red_shift<NT>();
+        const float gv = qd_warp_reduce_t<NT>(sacc);
+        const float uv = __shfl_xor_sync(0xffffffffu, gv, (2 * NT) << sh);
+        const int si = lane >> sh, sr = si / NT, st_ = si - sr * NT;
+        const bool s_lead = sr < 2 && (lane & ((1 << sh) - 1)) == 0 && st_ < T;
         if constexpr (kSh == 2) {
-            if (lane < 2 * NT) {
-                const int t = lane >> 1, ri = lane & 1;
-                if (t < T) {
-                    const float gv = qd_pick<NT>(sacc, ri, t), uv = qd_pick<NT>(sacc, 2 + ri, t);
-                    p.h_s[(int64_t)t * p.I_s + r0 + ri] = silu_mul(gv, uv);
-                }
-            }
+            if (s_lead) p.h_s[(int64_t)st_ * p.I_s + r0 + sr] = silu_mul(gv, uv);
         } else {
-            if (lane < 2 * NT) {
-                const int t = lane >> 1, ri = lane & 1;
-                if (t < T) {
-                    const float gv = qd_pick<NT>(sacc, ri, t), uv = qd_pick<NT>(sacc, 2 + ri, t);
-                    s_hq[round & 1][t][(r0 & 31) + ri] = silu_mul(gv, uv);
-                }
-            }
+            if (s_lead) s_hq[round & 1][st_][(r0 & 31) + sr] = silu_mul(gv, uv);
             __syncthreads();
             if (warp < T)
                 warp_stage_subblock(s_hq[round & 1][warp][lane], p.hq_s + (size_t)warp * 272 * qd4_groups(p.I_s),
@@ -616,11 +610,10 @@ __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_con
                 for (int r = 0; r < 4; ++r) rowp[r] = nb + r < H ? p.sd + (int64_t)(nb + r) * rbS : nullptr;
                 qd4_rows4<NT, false>(rowp, p.I_s / kQ4KWeights, SX, SXS, T, lane, acc, vidx);
             }
-            qd_warp_reduce<NT>(acc);
-            if (lane < 4 * NT) {
-                const int t = lane >> 2, ri = lane & 3;
-                if (t < T) ybuf[(P + t) * R + 4 * q + ri] = qd_pick<NT>(acc, ri, t);
-            }
+            constexpr int sh = qd_red_shift<NT>();
+            const float v = qd_warp_reduce_t<NT>(acc);
+            const int i = lane >> sh, ri = i / NT, t = i - ri * NT;
+            if ((lane & ((1 << sh) - 1)) == 0 && t < T) ybuf[(P + t) * R + 4 * q + ri] = v;
         }
     }
     __syncthreads();

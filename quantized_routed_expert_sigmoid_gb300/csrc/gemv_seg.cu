@@ -242,15 +242,13 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_gateup_kernel(const __grid_c
                 __syncwarp();
                 issue(item + 2);
                 if (ch == nch - 1) {
-                    qd_warp_reduce<NT>(acc);
-                    const int r0 = 2 * u;
-                    if (lane < 2 * NT) {
-                        const int t = lane >> 1, ri = lane & 1;
-                        if (t < nt) {
-                            const float gv = qd_pick<NT>(acc, 2 * ri, t), uv = qd_pick<NT>(acc, 2 * ri + 1, t);
-                            p.out[(int64_t)(st + pb + t) * I + r0 + ri] = gv / (1.0f + expf(-gv)) * uv;
-                        }
-                    }
+                    // rows 0, 1 = gate, up of row 2u; rows 2, 3 = gate, up of row 2u + 1
+                    constexpr int sh = qd_red_shift<NT>();
+                    const float gv = qd_warp_reduce_t<NT>(acc);
+                    const float uv = __shfl_xor_sync(0xffffffffu, gv, NT << sh);
+                    const int i = lane >> sh, r = i / NT, t = i - r * NT;
+                    if ((r & 1) == 0 && (lane & ((1 << sh) - 1)) == 0 && t < nt)
+                        p.out[(int64_t)(st + pb + t) * I + 2 * u + (r >> 1)] = gv / (1.0f + expf(-gv)) * uv;
                 }
             }
             // the items of this pass are all consumed (or, after a timeout, waited for below)

@@ -324,6 +324,39 @@ __device__ __forceinline__ void qd_warp_reduce(float (&acc)[4][NT]) {
         }
 }
 
+// Transposed warp sum of acc[4][NT] (NT = 1, 2, 4 or 8).  Each halving step sends one half
+// of the lane's entries to the partner lane and keeps the other, so the 4*NT sums cost
+// 4*NT - 1 shuffles plus the butterfly steps left over, not 4*NT*5.  Afterwards lane L
+// holds the warp total of entry i = L >> qd_red_shift<NT>() of acc, i = r * NT + t, and
+// the 2^shift lanes sharing i hold the same value.
+template <int NT>
+__host__ __device__ constexpr int qd_red_shift() { return NT >= 8 ? 0 : NT == 4 ? 1 : NT == 2 ? 2 : 3; }
+
+template <int NT>
+__device__ __forceinline__ float qd_warp_reduce_t(const float (&acc)[4][NT]) {
+    constexpr int V = 4 * NT;
+    float v[V];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) v[r * NT + t] = acc[r][t];
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int n = V, o = 16; n > 1; n >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float keep = up ? v[i + n / 2] : v[i];
+            const float send = up ? v[i] : v[i + n / 2];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    float s = v[0];
+#pragma unroll
+    for (int o = (1 << qd_red_shift<NT>()) >> 1; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    return s;
+}
+
 // acc[r][t] selected by runtime (r, t) without dynamic register indexing.
 template <int NT>
 __device__ __forceinline__ float qd_pick(const float (&acc)[4][NT], int r, int t) {
@@ -350,6 +383,10 @@ __device__ __forceinline__ float qd_pick(const float (&acc)[4][NT], int r, int t
 // planes and applies the scales in fp32:
 //   dot_j = (65536*sum(q*hi) + 256*sum(q*mid) + sum(q*lo)) * sx_j
 //   row . x += d*sc_j*dot_j - dmin*m_j*sum(x over sub-block j)
+// The high nibbles enter dp4a unshifted (byte = 16 q), so their sums are 16x the
+// codes' sums and the factor 1/16 joins the sub-block scale (exact).  The high and
+// middle plane sums are joined in integers (|256*hi + mid| < 2^31, and < 2^24 for
+// the low nibbles) before the one conversion to fp32.
 // The 24-bit rounding is far below fp32 accumulation noise (2^-23 of the block
 // maximum per value).
 // Staged vector layout (G = K/64 groups): X[q*G + g] (q = 0..15) holds the
@@ -544,6 +581,7 @@ __device__ __forceinline__ void qd4_group_math(const uint4 (&hd)[RPL], const uin
         qw[i][0] = q0[i].x; qw[i][1] = q0[i].y; qw[i][2] = q0[i].z; qw[i][3] = q0[i].w;
         qw[i][4] = q1[i].x; qw[i][5] = q1[i].y; qw[i][6] = q1[i].z; qw[i][7] = q1[i].w;
         qd4_scales(hd[i], c, fs[i], fm[i]);
+        fs[i][1] *= 0.0625f;                       // the high nibbles' sums carry a factor 16
     }
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
@@ -558,7 +596,7 @@ __device__ __forceinline__ void qd4_group_math(const uint4 (&hd)[RPL], const uin
                 const uint4 xl = Xv[qd * G], xh = Xv[(8 + qd) * G];
 #pragma unroll
                 for (int i = 0; i < RPL; ++i) {
-                    const uint32_t ql = qw[i][qd] & 0x0F0F0F0Fu, qh = (qw[i][qd] >> 4) & 0x0F0F0F0Fu;
+                    const uint32_t ql = qw[i][qd] & 0x0F0F0F0Fu, qh = qw[i][qd] & 0xF0F0F0F0u;
                     ah[i][0] = qd_dp4a_us(ql, xl.x, ah[i][0]);
                     am[i][0] = qd_dp4a_uu(ql, xl.y, am[i][0]);
                     al[i][0] = qd_dp4a_uu(ql, xl.z, al[i][0]);
@@ -571,8 +609,8 @@ __device__ __forceinline__ void qd4_group_math(const uint4 (&hd)[RPL], const uin
 #pragma unroll
             for (int i = 0; i < RPL; ++i) {
                 if (live[i]) {
-                    const float d0 = fmaf((float)ah[i][0], 65536.0f, fmaf((float)am[i][0], 256.0f, (float)al[i][0])) * xs.x;
-                    const float d1 = fmaf((float)ah[i][1], 65536.0f, fmaf((float)am[i][1], 256.0f, (float)al[i][1])) * xs.y;
+                    const float d0 = fmaf((float)(ah[i][0] * 256 + am[i][0]), 256.0f, (float)al[i][0]) * xs.x;
+                    const float d1 = fmaf((float)(ah[i][1] * 256 + am[i][1]), 256.0f, (float)al[i][1]) * xs.y;
                     float part = fs[i][0] * d0;
                     part = fmaf(fs[i][1], d1, part);
                     part = fmaf(-fm[i][0], xs.z, part);

@@ -31,6 +31,24 @@ __device__ __forceinline__ void prefetch_rows_l2(const uint8_t* src, int64_t byt
     }
 }
 
+// Sum a unit's acc over the warp and store it.  Gate/up: rows 0, 1 = gate of the unit's
+// rows 2 unit, 2 unit + 1, rows 2, 3 = up of the same rows -> h[t][row] = SiLU(gate) * up;
+// down: rows 0..3 -> y[t][4 unit + r].
+template <int NT, bool GATEUP>
+__device__ __forceinline__ void qd_store_units(const float (&acc)[4][NT], int lane, int nt, float* out, int rows,
+                                               int unit) {
+    constexpr int sh = qd_red_shift<NT>();
+    const float v = qd_warp_reduce_t<NT>(acc);
+    const int i = lane >> sh, r = i / NT, t = i - r * NT;
+    const bool lead = (lane & ((1 << sh) - 1)) == 0 && t < nt;
+    if (GATEUP) {
+        const float u = __shfl_xor_sync(0xffffffffu, v, (2 * NT) << sh);
+        if (lead && r < 2) out[(int64_t)t * rows + unit * 2 + r] = v / (1.0f + expf(-v)) * u;
+    } else if (lead) {
+        out[(int64_t)t * rows + unit * 4 + r] = v;
+    }
+}
+
 template <int QT, bool GATEUP, int NT>
 __global__ void __launch_bounds__(kThreads, 2) qgemv_kernel(GemvArgs a, int iters, int units_per_warp) {
     extern __shared__ float4 xs[];                    // [NT][iters*256] float4
@@ -121,19 +139,7 @@ __global__ void __launch_bounds__(kThreads, 2) qgemv_kernel(GemvArgs a, int iter
 #pragma unroll
                     for (int t = 0; t < NT; ++t) acc[r][t] = 0.f;
                 qd4_rows4<NT>(rowp, nblk, X, XS, nt, lane, acc);
-                qd_warp_reduce<NT>(acc);
-                if (GATEUP) {
-                    if (lane < 2 * NT) {
-                        const int t = lane >> 1, ri = lane & 1;
-                        if (t < nt) {
-                            const float g = qd_pick<NT>(acc, ri, t), u = qd_pick<NT>(acc, 2 + ri, t);
-                            a.out[(int64_t)(start + pb + t) * a.rows + unit * 2 + ri] = g / (1.0f + expf(-g)) * u;
-                        }
-                    }
-                } else if (lane < 4 * NT) {
-                    const int t = lane >> 2, ri = lane & 3;
-                    if (t < nt) a.out[(int64_t)(start + pb + t) * a.rows + unit * 4 + ri] = qd_pick<NT>(acc, ri, t);
-                }
+                qd_store_units<NT, GATEUP>(acc, lane, nt, a.out + (int64_t)(start + pb) * a.rows, a.rows, unit);
             }
             __syncthreads();
             continue;
@@ -173,19 +179,7 @@ __global__ void __launch_bounds__(kThreads, 2) qgemv_kernel(GemvArgs a, int iter
 #pragma unroll
                 for (int t = 0; t < NT; ++t) acc[r][t] = 0.f;
             qd_rows4<QT, NT>(rowp, nblk, iters, xs, slots, xsum, iters * 32, nt, lane, acc);
-            qd_warp_reduce<NT>(acc);
-            if (GATEUP) {
-                if (lane < 2 * NT) {
-                    const int t = lane >> 1, ri = lane & 1;
-                    if (t < nt) {
-                        const float g = qd_pick<NT>(acc, ri, t), u = qd_pick<NT>(acc, 2 + ri, t);
-                        a.out[(int64_t)(start + pb + t) * a.rows + unit * 2 + ri] = g / (1.0f + expf(-g)) * u;
-                    }
-                }
-            } else if (lane < 4 * NT) {
-                const int t = lane >> 2, ri = lane & 3;
-                if (t < nt) a.out[(int64_t)(start + pb + t) * a.rows + unit * 4 + ri] = qd_pick<NT>(acc, ri, t);
-            }
+            qd_store_units<NT, GATEUP>(acc, lane, nt, a.out + (int64_t)(start + pb) * a.rows, a.rows, unit);
         }
         __syncthreads();
     }

@@ -2,9 +2,10 @@
 
 Each layer is the decode-shaped layer (hidden 2048, 128 experts, top-8, I=768,
 Q4_K).  The oracle runs its own chain in fp64 (it never sees a GPU value);
-routing ids must match at every layer, the first layer must meet the
-single-layer tolerance, and the drift after every later layer must stay within
-a bound the oracle measures for itself (see the test).  A layer whose routing margin
+routing ids must match at every layer whose routing the oracle's own reruns
+leave unchanged, the first layer must meet the single-layer tolerance, and the
+drift after every later layer must stay within a bound the oracle measures for
+itself (see the test).  A layer whose routing margin
 (measured on the oracle chain) falls below 1e-3 gets its router redrawn from a
 new seed before the chain continues.
 """
@@ -44,16 +45,28 @@ def _round_other_way(u, rel=1e-6):
 
 
 def _oracle_chain(layers, shape, x, flip_rel=0.0):
-    """The oracle's own chain from x (fp64), returning x after every layer.  flip_rel > 0
-    rounds the RMSNorm outputs that sit within flip_rel of a bf16 rounding midpoint the
-    other way (the rounding a less precise RMSNorm may legitimately take)."""
-    xs = []
+    """The oracle's own chain from x (fp64), returning x and the routing ids after every
+    layer.  flip_rel > 0 rounds the RMSNorm outputs that sit within flip_rel of a bf16
+    rounding midpoint the other way (the rounding a less precise RMSNorm may legitimately
+    take)."""
+    xs, ids = [], []
     for L in layers:
         u = oracle.rmsnorm(x, L["gamma"].numpy(), EPS)
         u = _round_other_way(u, flip_rel) if flip_rel > 0 else np.vectorize(oracle.round_bf16)(u)
-        x = x + oracle.moe_layer(L["spec"], u, n_threads=8)["out"]
+        r = oracle.moe_layer(L["spec"], u, n_threads=8)
+        x = x + r["out"]
         xs.append(x)
-    return xs
+        ids.append(r["ids"])
+    return xs, ids
+
+
+def _first_rerouted(layers, *id_chains):
+    """First layer at which any rerun of the oracle chain routes differently from the
+    reference chain (len(layers) if none does)."""
+    for l, L in enumerate(layers):
+        if any(not np.array_equal(ch[l], L["ids"]) for ch in id_chains):
+            return l
+    return len(layers)
 
 
 def _build_stack(T, seed=5, n_layers=N_LAYERS):
@@ -114,7 +127,7 @@ def _gpu_stack(shape, x0, layers, T):
 
 @pytest.mark.parametrize("T", [1, 2])
 def test_stack_48_layers_graph(T):
-    """Ids bit-exact at every layer; per-layer drift within a bound the oracle sets for itself.
+    """Ids bit-exact where the oracle's routing is decided; drift within a bound the oracle sets.
 
     The stack is a deep residual chain whose bf16 rounding of each layer's input
     is a discontinuous step, so tiny differences grow with depth.  The bound on
@@ -124,13 +137,20 @@ def test_stack_48_layers_graph(T):
     bf16 rounding midpoint to the other neighbour (the GPU computes RMSNorm in
     fp32, so such elements may round either way).  The larger of the two
     divergences after layer l, times 10, plus the single-layer tolerance, is the
-    allowed distance.
+    allowed distance.  The same reruns say how far down the routing is decided: from
+    the first layer at which either of them picks other experts than the reference
+    chain, a 1e-6 change of the input already reroutes the oracle itself, so from there
+    on only the drift bound applies (the reference keeps a 1e-3 margin on its own
+    inputs, but the drift of any chain grows with depth).  At least the first 32 layers
+    must stay decided, so the test keeps checking ids over two thirds of the stack.
     """
     shape, x0, layers, x_ref = _build_stack(T)
     rng = np.random.default_rng(7)
     x0_64 = x0.double().numpy()
-    pert = _oracle_chain(layers, shape, x0_64 * (1.0 + 1e-6 * rng.standard_normal(x0_64.shape)))
-    flip = _oracle_chain(layers, shape, x0_64, flip_rel=1e-6)
+    pert, pert_ids = _oracle_chain(layers, shape, x0_64 * (1.0 + 1e-6 * rng.standard_normal(x0_64.shape)))
+    flip, flip_ids = _oracle_chain(layers, shape, x0_64, flip_rel=1e-6)
+    decided = _first_rerouted(layers, pert_ids, flip_ids)
+    assert decided >= 32, f"the oracle's own reruns reroute at layer {decided}"
     mls, x, run = _gpu_stack(shape, x0, layers, T)
     # eager, layer by layer: the GPU chain next to the oracle chain (never fed into it)
     import quantized_routed_expert_sigmoid_gb300 as moe
@@ -142,7 +162,8 @@ def test_stack_48_layers_graph(T):
         m(u, out=x)
         torch.cuda.synchronize()
         ids, _, _ = m.debug_views(T)
-        assert np.array_equal(ids.numpy(), L["ids"]), f"layer {l}: routing ids differ"
+        if l < decided:
+            assert np.array_equal(ids.numpy(), L["ids"]), f"layer {l}: routing ids differ"
         err = rel_l2(x.cpu().numpy(), L["x_after"])
         self_div = max(rel_l2(pert[l], L["x_after"]), rel_l2(flip[l], L["x_after"]))
         drift.append((err, self_div))
@@ -162,8 +183,9 @@ def test_stack_48_layers_graph(T):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(x, eager_final), "graph replay differs from the eager chain"
-    for l, (m, L) in enumerate(zip(mls, layers)):
+    for l, (m, L) in enumerate(zip(mls[:decided], layers)):
         ids, _, _ = m.debug_views(T)
         assert np.array_equal(ids.numpy(), L["ids"]), f"replay, layer {l}: routing ids differ"
-    print("stack drift (gpu vs oracle, oracle self-divergence) per 8 layers:",
+    print(f"routing decided through layer {decided - 1};",
+          "stack drift (gpu vs oracle, oracle self-divergence) per 8 layers:",
           [(f"{a:.1e}", f"{b:.1e}") for a, b in drift[::8]], "final", f"{drift[-1][0]:.2e}")
