@@ -22,6 +22,9 @@
 // warp waits full[g%4], issues 4 k-substeps, and commits to empty[g%4].
 // Every wait is bounded (globaltimer); on timeout the kernel records
 // MOE_ERR_TIMEOUT, drains its MMAs, frees TMEM and returns.
+#include <algorithm>
+#include <cuda.h>   // CUtensorMap and its enums (the encoder is fetched from the driver at run time)
+
 #include "internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -32,7 +35,6 @@ constexpr int kBM = 128, kBK = 64;
 constexpr int kBNMin = 128;                       // token-block width bound used to size the tile list
 constexpr int kProducerWarps = 8;
 constexpr int kProducers = kProducerWarps * 32;
-constexpr int kThreadsTC = kProducers + 32;
 constexpr int kAStages = 2, kBStages = 4, kRawSlots = 2;
 
 enum { kGateUp = 0, kDown = 1 };
@@ -42,9 +44,6 @@ enum { kGateUp = 0, kDown = 1 };
 template <int QT>
 __host__ __device__ constexpr int tc_bn() { return QT == MOE_Q4_K ? 256 : 128; }
 
-__device__ __forceinline__ float nib_f(uint32_t word, int b) {   // byte b (0..15 value) -> float, exact
-    return __int_as_float(__byte_perm(word, 0x4B00u, 0x5440u | (uint32_t)b)) - 8388608.0f;
-}
 __device__ __forceinline__ float s8_f(uint32_t word, int b) {    // signed byte b -> float, exact
     return __int_as_float(__byte_perm(word ^ 0x80808080u, 0x4B00u, 0x5440u | (uint32_t)b)) - 8388736.0f;
 }
@@ -105,17 +104,19 @@ struct TileInfo {
 };
 
 struct TcParams {
+    CUtensorMap tmap_b;          // B rows: GATEUP x16 [T][K] (box 64 x 1, gathered 4 rows at a
+                                 // time); DOWN h16 [P][K] (box 64 x BN); 128-byte swizzle
     const uint8_t* w0;           // gate (GATEUP) or down (DOWN) weights
     const uint8_t* w1;           // up (GATEUP)
     int64_t expert_stride;
     int rows;                    // weight rows per expert (I for GATEUP, H for DOWN)
     int K;                       // H for GATEUP, I for DOWN
     int k;                       // top-k (token of pair = sorted_pairs[i] / k)
-    const __half* bsrc;          // x16 [T][K] (GATEUP) or h16 [P][K] (DOWN)
     const int32_t* sorted_pairs; // GATEUP gather map (NULL: identity)
     const int4* tb_list;         // [0].x = number of token blocks, then (e, tok0, ntok, 0); NULL: identity
     int n_identity;              // identity mode: tokens
     int bn;                      // token-block width of the list (tc_bn)
+    int b_box_rows;              // DOWN: rows of the B box (BN, or P when fewer)
     __half* h_out;               // GATEUP: [P][rows] fp16
     float* y_out;                // DOWN: [P][rows] fp32
     WsHeader* hdr;
@@ -136,14 +137,28 @@ __device__ __forceinline__ bool tile_at(const TcParams& p, int n_mb, int t, int 
     return true;
 }
 
+// Warp layout: producers 0-7, then (DOWN) 4 epilogue warps, then the MMA warp.  DOWN keeps
+// two accumulators in TMEM so that its epilogue overlaps the next tile's main loop; GATEUP
+// needs all 512 columns for one tile (gate and up, 256 tokens each) and lets the producers
+// run its epilogue.
+template <int MODE>
+__host__ __device__ constexpr int tc_epi_warps() { return MODE == kDown ? 4 : 0; }
+template <int MODE>
+__host__ __device__ constexpr int tc_threads() { return kProducers + 32 * tc_epi_warps<MODE>() + 32; }
+
 template <int QT, int MODE>
-__global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(tc_threads<MODE>(), 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
     constexpr int kAStageBytes = (MODE == kGateUp ? 2 : 1) * kBM * 128;
     constexpr int BN = tc_bn<QT>();
     constexpr int kBStageBytes = BN * 128;
     constexpr int kRawBytes = RawCfg<QT, MODE>::kBytes;
     constexpr int kRawSlotBytes = kProducers * kRawBytes;
-    constexpr uint32_t kTmemCols = MODE == kGateUp ? 2 * BN : BN;
+    constexpr int kEpiWarps = tc_epi_warps<MODE>();
+    constexpr int kMmaWarp = kProducerWarps + kEpiWarps;
+    constexpr uint32_t kAccCols = (MODE == kGateUp ? 2 : 1) * BN;
+    constexpr int kAccBufs = kEpiWarps > 0 ? 2 : 1;
+    constexpr uint32_t kTmemCols = kAccCols * kAccBufs;
+    static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation must be a power of two");
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -151,22 +166,24 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
     uint8_t* sB = sA + kAStages * kAStageBytes;
     uint8_t* sRaw = sB + kBStages * kBStageBytes;
     uint64_t* bar = reinterpret_cast<uint64_t*>(sRaw + kRawSlots * kRawSlotBytes);
-    uint64_t* full = bar;            // [4]
+    uint64_t* full = bar;            // [4]: A dequantized (kProducers arrivals) + B landed (tx bytes)
     uint64_t* empty = bar + 4;       // [4]
-    uint64_t* accf = bar + 8;        // [1]
-    uint64_t* drain = bar + 9;       // [1]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 10);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 11);
+    uint64_t* accf = bar + 8;        // [2]: accumulator buffer complete
+    uint64_t* tfree = bar + 10;      // [2]: accumulator buffer read out by the epilogue warps
+    uint64_t* drain = bar + 12;      // [1]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 13);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 14);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int i = 0; i < 4; ++i) { mbar_init(&full[i], kProducers); mbar_init(&empty[i], 1); }
-        mbar_init(accf, 1);
+        for (int i = 0; i < 2; ++i) { mbar_init(&accf[i], 1); mbar_init(&tfree[i], kEpiWarps > 0 ? kEpiWarps : 1); }
         mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tmap_b) : "memory");
     }
-    if (warp == kProducerWarps) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
                      "n"(kTmemCols)
                      : "memory");
@@ -185,7 +202,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
     const int64_t rb = (int64_t)nblk_row * (QT == MOE_Q4_K ? kQ4KBytes : kQ80Bytes);
 
     if (warp < kProducerWarps) {
-        // ======================= producers + epilogue =======================
+        // ======================= producers (+ GATEUP epilogue) =======================
         const int prow = tid & 127;                 // weight row within the tile
         const int psel = tid >> 7;                  // GATEUP: matrix (0 gate, 1 up); DOWN: half of the k-step
         uint32_t g = 0;                             // global k-step counter
@@ -195,28 +212,35 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
             if (!tile_at(p, n_mb, t, n_tb, ti)) break;
             const uint8_t* wrow = (MODE == kGateUp && psel == 1 ? p.w1 : p.w0) + (int64_t)ti.e * p.expert_stride +
                                   (int64_t)(ti.m0 + prow) * rb;
-            // rows of B this thread copies: r = tid/8 + 32*it, 16-byte chunk tid%8
-            constexpr int kBIt = BN / 32;
-            const int bch = tid & 7;
-            int64_t brow[kBIt];
-#pragma unroll
-            for (int it = 0; it < kBIt; ++it) {
-                const int r = (tid >> 3) + 32 * it;
-                int64_t src = -1;
-                if (r < ti.ntok) {
-                    const int i = ti.tok0 + r;
-                    if (MODE == kGateUp) src = p.sorted_pairs ? (int64_t)(p.sorted_pairs[i] / p.k) : (int64_t)i;
-                    else src = i;
-                }
-                brow[it] = src;
+            // GATEUP: the x16 row of column 32 * warp + lane of the block (columns past the block's
+            // tokens take its first token's row; they are never read)
+            int myrow = 0;
+            if (MODE == kGateUp) {
+                const int r = 32 * warp + lane;
+                const int i = ti.tok0 + (r < ti.ntok ? r : 0);
+                myrow = p.sorted_pairs ? p.sorted_pairs[i] / p.k : i;
             }
+            // B of k-step kb into stage `stage`, completing on full[stage]: GATEUP gathers four
+            // x16 rows per TMA (warp w: groups 8w..8w+7 of the rows the block needs), DOWN loads
+            // the BN consecutive h16 rows of the block in one box
             auto issue_b = [&](int kb, int stage) {
                 uint8_t* dst = sB + stage * kBStageBytes;
-                // rows past the block's tokens only feed accumulator columns that are never read
-#pragma unroll
-                for (int it = 0; it < kBIt; ++it) {
-                    const int r = (tid >> 3) + 32 * it;
-                    if (brow[it] >= 0) cp_async16(dst + swz(r, bch), p.bsrc + brow[it] * p.K + kb * kBK + bch * 8, 16u);
+                uint64_t* fb = &full[stage];
+                if (MODE == kGateUp) {
+                    const int ngroups = (ti.ntok + 3) >> 2;
+                    const int mine = min(8, max(0, ngroups - 8 * warp));
+                    if (mine > 0) {
+                        const int src = (4 * lane) & 31;
+                        const int y0 = __shfl_sync(0xffffffffu, myrow, src), y1 = __shfl_sync(0xffffffffu, myrow, src + 1);
+                        const int y2 = __shfl_sync(0xffffffffu, myrow, src + 2), y3 = __shfl_sync(0xffffffffu, myrow, src + 3);
+                        if (lane == 0) mbar_expect_tx(fb, (uint32_t)mine * 512u);
+                        __syncwarp();
+                        if (lane < mine)
+                            tma_gather4(dst + (8 * warp + lane) * 512, &p.tmap_b, kb * kBK, y0, y1, y2, y3, fb);
+                    }
+                } else if (tid == 0) {
+                    mbar_expect_tx(fb, (uint32_t)p.b_box_rows * 128u);
+                    tma_load_2d(dst, &p.tmap_b, kb * kBK, ti.tok0, fb);
                 }
             };
             auto issue_raw = [&](int kb, int slot) {
@@ -236,8 +260,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
                     for (int w = 0; w < 17; ++w) cp_async4(dst + 4 * w, src + 4 * w);
                 }
             };
-            // prologue: groups {raw0, B0}, {raw1, B1}; the group of step kb + 2 is issued right
-            // after step kb's dequantization, into the raw slot it has just read
+            // prologue: raw0 + B0, raw1 + B1; the raw group and B of step kb + 2 are issued right
+            // after step kb's dequantization (stage (g+2)%4 and the raw slot just read are free)
             issue_raw(0, g % kRawSlots);
             if (nk > 0) issue_b(0, g % kBStages);
             cp_commit();
@@ -251,7 +275,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
             for (int kb = 0; kb < nk; ++kb, ++g) {
                 // A stage g%2 and B stage (g+2)%4 were last read by MMA(g-2)
                 if (g >= 2 && !mbar_wait(&empty[(g + 2) & 3], ((g - 2) >> 2) & 1, abort_flag)) { ok = false; break; }
-                cp_wait<1>();                        // raw(kb) and B(kb) have landed
+                cp_wait<1>();                        // raw(kb) has landed
                 // ---- dequantize k-step kb into A stage g%2
                 const uint8_t* raw = sRaw + (g % kRawSlots) * kRawSlotBytes + tid * kRawBytes;
                 uint8_t* arow = sA + (g % kAStages) * kAStageBytes + (MODE == kGateUp ? psel * kBM * 128 : 0);
@@ -323,16 +347,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
             }
             cp_wait_all();
             if (!ok) break;
-            // ---- epilogue: wait for the accumulators of this tile
-            if (!mbar_wait(accf, tile_iter & 1, abort_flag)) break;
-            tc_after();
-            const int q = warp & 3, half = warp >> 2;
-            const int m = q * 32 + lane;
-            for (int c16 = half * 16; c16 < ti.n_inst; c16 += 32) {
-                uint32_t a[16];
-                tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c16, a);
-                if (MODE == kGateUp) {
-                    uint32_t u[16];
+            if constexpr (MODE == kGateUp) {
+                // ---- epilogue: wait for the accumulators of this tile, h = SiLU(gate) * up
+                if (!mbar_wait(&accf[0], tile_iter & 1, abort_flag)) break;
+                tc_after();
+                const int q = warp & 3, half = warp >> 2;
+                const int m = q * 32 + lane;
+                __half* hrow = p.h_out + (int64_t)ti.tok0 * p.rows + ti.m0 + m;
+                for (int c16 = half * 16; c16 < ti.n_inst; c16 += 32) {
+                    uint32_t a[16], u[16];
+                    tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c16, a);
                     tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(BN + c16), u);
                     tmem_ld_wait();
 #pragma unroll
@@ -340,30 +364,57 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
                         const int col = c16 + j;
                         if (col < ti.ntok) {
                             const float gv = __uint_as_float(a[j]), uv = __uint_as_float(u[j]);
-                            const float hv = gv * __frcp_rn(1.0f + __expf(-gv)) * uv;
-                            p.h_out[(int64_t)(ti.tok0 + col) * p.rows + ti.m0 + m] = __float2half_rn(hv);
+                            hrow[(int64_t)col * p.rows] = __float2half_rn(__fdividef(gv, 1.0f + __expf(-gv)) * uv);
                         }
                     }
-                } else {
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int col = c16 + j;
-                        if (col < ti.ntok) p.y_out[(int64_t)(ti.tok0 + col) * p.rows + ti.m0 + m] = __uint_as_float(a[j]);
-                    }
                 }
+                tc_before();
             }
-            tc_before();
         }
         cp_wait_all();
+    } else if (warp < kMmaWarp) {
+        // ======================= DOWN epilogue warps =======================
+        // warp kProducerWarps + q reads TMEM lanes 32q.. (q = warp % 4); y fp32 per pair
+        const int q = warp & 3;
+        const int m = q * 32 + lane;
+        int j = 0;
+        for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x, ++j) {
+            TileInfo ti;
+            if (!tile_at(p, n_mb, t, n_tb, ti)) break;
+            const int b = j & 1;
+            if (!mbar_wait(&accf[b], (j >> 1) & 1, abort_flag)) break;
+            tc_after();
+            float* yrow = p.y_out + (int64_t)ti.tok0 * p.rows + ti.m0 + m;
+            const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)b * kAccCols;
+            for (int c16 = 0; c16 < ti.n_inst; c16 += 16) {
+                uint32_t a[16];
+                tmem_ld16(tb + (uint32_t)c16, a);
+                tmem_ld_wait();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj)
+                    if (c16 + jj < ti.ntok) yrow[(int64_t)(c16 + jj) * p.rows] = __uint_as_float(a[jj]);
+            }
+            tc_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tfree[b]);
+        }
     } else {
-        // ======================= MMA issuer (warp 8) =======================
+        // ======================= MMA issuer =======================
         uint32_t g = 0;
         bool issued = false;
-        for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
+        int j = 0;
+        for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x, ++j) {
             TileInfo ti;
             if (!tile_at(p, n_mb, t, n_tb, ti)) break;
             const uint32_t idesc = idesc_mma(kBM, ti.n_inst, false);
+            const int b = j % kAccBufs;
+            // the accumulator buffer's previous tile has been read out (GATEUP: the producers
+            // only reach this tile's first k-step after their epilogue)
+            if (kEpiWarps > 0 && j >= kAccBufs) {
+                if (!mbar_wait(&tfree[b], ((j / kAccBufs) - 1) & 1, abort_flag)) break;
+                tc_after();
+            }
+            const uint32_t acc = tmem + (uint32_t)b * kAccCols;
             bool ok = true;
             for (int kb = 0; kb < nk; ++kb, ++g) {
                 if (!mbar_wait(&full[g & 3], (g >> 2) & 1, abort_flag)) { ok = false; break; }
@@ -374,12 +425,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t bd = sdesc(b0 + 32 * kk);
-                        mma_f16(tmem, sdesc(a0 + 32 * kk), bd, idesc, (kb | kk) != 0);
+                        mma_f16(acc, sdesc(a0 + 32 * kk), bd, idesc, (kb | kk) != 0);
                         if (MODE == kGateUp)
-                            mma_f16(tmem + BN, sdesc(a0 + kBM * 128 + 32 * kk), bd, idesc, (kb | kk) != 0);
+                            mma_f16(acc + BN, sdesc(a0 + kBM * 128 + 32 * kk), bd, idesc, (kb | kk) != 0);
                     }
                     mma_commit(&empty[g & 3]);
-                    if (kb == nk - 1) mma_commit(accf);
+                    if (kb == nk - 1) mma_commit(&accf[b]);
                 }
                 issued = true;
                 __syncwarp();
@@ -400,7 +451,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_gemm_kernel(const __grid_con
     tc_before();
     __syncthreads();
     tc_after();
-    if (warp == kProducerWarps) {
+    if (*abort_flag) {
+        // after a timeout, give copies still in flight (TMA, cp.async) time to land before the
+        // CTA's shared memory is released
+        const uint64_t t0 = gtime();
+        while (gtime() - t0 < 1000000ull) {
+        }
+    }
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
     }
 }
@@ -461,7 +519,41 @@ size_t tc_smem_bytes() {
     constexpr int a = kAStages * (MODE == kGateUp ? 2 : 1) * kBM * 128;
     constexpr int b = kBStages * tc_bn<QT>() * 128;
     constexpr int r = kRawSlots * kProducers * RawCfg<QT, MODE>::kBytes;
-    return (size_t)a + b + r + 128 + 1024;   // barriers + alignment slack
+    return (size_t)a + b + r + 256 + 1024;   // barriers + alignment slack
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+// Tensor map of an fp16 matrix [rows][cols] (dense rows): boxes of 64 columns (128 bytes) x
+// box_rows rows, 128-byte swizzle, zero fill outside.
+cudaError_t make_tmap_f16(CUtensorMap* m, const __half* base, int64_t rows, int cols, int box_rows) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return cudaErrorNotSupported;
+    if (((uintptr_t)base & 15) != 0 || cols % 64 != 0 || rows <= 0 || box_rows <= 0 || box_rows > 256)
+        return cudaErrorInvalidValue;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * sizeof(__half)};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 int num_sms() {
@@ -482,7 +574,7 @@ cudaError_t launch_tc(const TcParams& p, int max_tiles, cudaStream_t s) {
                                            (int)smem);
     if (err != cudaSuccess) return err;
     const int grid = max(1, min(num_sms(), max_tiles));
-    tc_gemm_kernel<QT, MODE><<<grid, kThreadsTC, smem, s>>>(p);
+    tc_gemm_kernel<QT, MODE><<<grid, tc_threads<MODE>(), smem, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -524,7 +616,8 @@ cudaError_t launch_tc_expert_ffn(const TcFfnArgs& a, cudaStream_t s) {
     }
     TcParams gu{};
     gu.w0 = a.wg; gu.w1 = a.wu; gu.expert_stride = a.stride_gu; gu.rows = a.I; gu.K = a.H; gu.k = a.k;
-    gu.bsrc = a.x16; gu.sorted_pairs = a.identity ? nullptr : a.sorted_pairs;
+    if ((err = make_tmap_f16(&gu.tmap_b, a.x16, a.T, a.H, 1)) != cudaSuccess) return err;
+    gu.sorted_pairs = a.identity ? nullptr : a.sorted_pairs;
     gu.tb_list = a.identity ? nullptr : a.tb_list; gu.n_identity = a.identity ? a.T : 0; gu.bn = bn;
     gu.h_out = a.h16; gu.hdr = a.hdr;
     if (a.ev_before_gateup && (err = cudaEventRecord(a.ev_before_gateup, s)) != cudaSuccess) return err;
@@ -532,7 +625,9 @@ cudaError_t launch_tc_expert_ffn(const TcFfnArgs& a, cudaStream_t s) {
     if (a.ev_after_gateup && (err = cudaEventRecord(a.ev_after_gateup, s)) != cudaSuccess) return err;
     TcParams dn{};
     dn.w0 = a.wd; dn.expert_stride = a.stride_d; dn.rows = a.H; dn.K = a.I; dn.k = a.k;
-    dn.bsrc = a.h16; dn.sorted_pairs = nullptr;
+    dn.b_box_rows = std::min(bn, P);
+    if ((err = make_tmap_f16(&dn.tmap_b, a.h16, P, a.I, dn.b_box_rows)) != cudaSuccess) return err;
+    dn.sorted_pairs = nullptr;
     dn.tb_list = gu.tb_list; dn.n_identity = gu.n_identity; dn.bn = bn;
     dn.y_out = a.y; dn.hdr = a.hdr;
     return launch_tc_q<kDown>(a.qtype, dn, max_tb * (a.H / kBM), s);
