@@ -33,8 +33,11 @@ namespace {
 
 constexpr int kBM = 128, kBK = 64;
 constexpr int kBNMin = 128;                       // token-block width bound used to size the tile list
-constexpr int kProducerWarps = 8;
-constexpr int kProducers = kProducerWarps * 32;
+// Producer warps: 16 for the Q4_K gate/up (a thread dequantizes half of a row's 64-weight
+// k-step, so that enough warps hide the latency of their dependent steps), 8 otherwise (Q4_K
+// down: half a k-step per thread already; Q8_0: its raw blocks need the shared memory).
+template <int QT, int MODE>
+__host__ __device__ constexpr int tc_pw() { return QT == MOE_Q4_K && MODE == 0 ? 16 : 8; }
 constexpr int kAStages = 2, kBStages = 4, kRawSlots = 2;
 
 enum { kGateUp = 0, kDown = 1 };
@@ -96,7 +99,7 @@ __device__ __forceinline__ void q4k_scale_min(const uint4& hd, int j, float& fsc
 // Raw bytes staged per producer thread per k-step.
 template <int QT, int MODE>
 struct RawCfg {
-    static constexpr int kBytes = QT == MOE_Q4_K ? (MODE == kGateUp ? 48 : 32) : 80;
+    static constexpr int kBytes = QT == MOE_Q4_K ? 32 : 80;   // Q4_K: header + up to 16 quant bytes
 };
 
 struct TileInfo {
@@ -143,18 +146,22 @@ __device__ __forceinline__ bool tile_at(const TcParams& p, int n_mb, int t, int 
 // run its epilogue.
 template <int MODE>
 __host__ __device__ constexpr int tc_epi_warps() { return MODE == kDown ? 4 : 0; }
-template <int MODE>
-__host__ __device__ constexpr int tc_threads() { return kProducers + 32 * tc_epi_warps<MODE>() + 32; }
+template <int QT, int MODE>
+__host__ __device__ constexpr int tc_threads() { return 32 * tc_pw<QT, MODE>() + 32 * tc_epi_warps<MODE>() + 32; }
 
 template <int QT, int MODE>
-__global__ void __launch_bounds__(tc_threads<MODE>(), 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
     constexpr int kAStageBytes = (MODE == kGateUp ? 2 : 1) * kBM * 128;
     constexpr int BN = tc_bn<QT>();
     constexpr int kBStageBytes = BN * 128;
     constexpr int kRawBytes = RawCfg<QT, MODE>::kBytes;
-    constexpr int kRawSlotBytes = kProducers * kRawBytes;
+    constexpr int kPW = tc_pw<QT, MODE>();
+    constexpr int kNP = kPW * 32;
+    constexpr int kMats = MODE == kGateUp ? 2 : 1;
+    constexpr int kSplit = kNP / (kBM * kMats);       // threads per (row, matrix) of a k-step
+    constexpr int kRawSlotBytes = kNP * kRawBytes;
     constexpr int kEpiWarps = tc_epi_warps<MODE>();
-    constexpr int kMmaWarp = kProducerWarps + kEpiWarps;
+    constexpr int kMmaWarp = kPW + kEpiWarps;
     constexpr uint32_t kAccCols = (MODE == kGateUp ? 2 : 1) * BN;
     constexpr int kAccBufs = kEpiWarps > 0 ? 2 : 1;
     constexpr uint32_t kTmemCols = kAccCols * kAccBufs;
@@ -166,7 +173,7 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) tc_gemm_kernel(const __
     uint8_t* sB = sA + kAStages * kAStageBytes;
     uint8_t* sRaw = sB + kBStages * kBStageBytes;
     uint64_t* bar = reinterpret_cast<uint64_t*>(sRaw + kRawSlots * kRawSlotBytes);
-    uint64_t* full = bar;            // [4]: A dequantized (kProducers arrivals) + B landed (tx bytes)
+    uint64_t* full = bar;            // [4]: A dequantized (kNP arrivals) + B landed (tx bytes)
     uint64_t* empty = bar + 4;       // [4]
     uint64_t* accf = bar + 8;        // [2]: accumulator buffer complete
     uint64_t* tfree = bar + 10;      // [2]: accumulator buffer read out by the epilogue warps
@@ -176,7 +183,7 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) tc_gemm_kernel(const __
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) { mbar_init(&full[i], kProducers); mbar_init(&empty[i], 1); }
+        for (int i = 0; i < 4; ++i) { mbar_init(&full[i], kNP); mbar_init(&empty[i], 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(&accf[i], 1); mbar_init(&tfree[i], kEpiWarps > 0 ? kEpiWarps : 1); }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -201,84 +208,98 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) tc_gemm_kernel(const __
     const int nblk_row = QT == MOE_Q4_K ? p.K / kQ4KWeights : p.K / kQ80Weights;
     const int64_t rb = (int64_t)nblk_row * (QT == MOE_Q4_K ? kQ4KBytes : kQ80Bytes);
 
-    if (warp < kProducerWarps) {
+    if (warp < kPW) {
         // ======================= producers (+ GATEUP epilogue) =======================
         const int prow = tid & 127;                 // weight row within the tile
-        const int psel = tid >> 7;                  // GATEUP: matrix (0 gate, 1 up); DOWN: half of the k-step
+        const int pmat = MODE == kGateUp ? (tid >> 7) & 1 : 0;   // matrix: 0 gate / down, 1 up
+        const int part = (tid >> 7) / kMats;        // which 1/kSplit of the row's k-step
+        constexpr int kRowsPW = BN / kPW, kGroupsPW = kRowsPW / 4;
+        // ---- issue cursor: runs two k-steps ahead of the dequantization, across tile
+        // boundaries, so that a tile's first raw blocks and token rows are in flight while the
+        // previous tile finishes
+        int is_t = blockIdx.x, is_kb = 0;
+        TileInfo iti{};
+        bool is_valid = false;
+        const uint8_t* is_wrow = nullptr;
+        int is_row = 0;     // GATEUP: lane l < kRowsPW holds the x16 row of column kRowsPW * warp + l
+        auto is_tile = [&]() {
+            is_valid = is_t < n_tiles && tile_at(p, n_mb, is_t, n_tb, iti);
+            if (!is_valid) return;
+            is_wrow = (pmat == 1 ? p.w1 : p.w0) + (int64_t)iti.e * p.expert_stride + (int64_t)(iti.m0 + prow) * rb;
+            if (MODE == kGateUp) {
+                // columns past the block's tokens take its first token's row (never read)
+                const int r = kRowsPW * warp + lane;
+                const int i = iti.tok0 + (r < iti.ntok ? r : 0);
+                is_row = p.sorted_pairs ? p.sorted_pairs[i] / p.k : i;
+            }
+        };
+        // B of the cursor's k-step into stage `stage`, completing on full[stage]: GATEUP gathers
+        // four x16 rows per TMA (warp w: groups kGroupsPW * w.. of the rows the block needs),
+        // DOWN loads the BN consecutive h16 rows of the block in one box
+        auto issue_b = [&](int kb, int stage) {
+            uint8_t* dst = sB + stage * kBStageBytes;
+            uint64_t* fb = &full[stage];
+            if (MODE == kGateUp) {
+                const int ngroups = (iti.ntok + 3) >> 2;
+                const int mine = min(kGroupsPW, max(0, ngroups - kGroupsPW * warp));
+                if (mine > 0) {
+                    const int src = (4 * lane) & (kRowsPW - 1);
+                    const int y0 = __shfl_sync(0xffffffffu, is_row, src), y1 = __shfl_sync(0xffffffffu, is_row, src + 1);
+                    const int y2 = __shfl_sync(0xffffffffu, is_row, src + 2), y3 = __shfl_sync(0xffffffffu, is_row, src + 3);
+                    if (lane == 0) mbar_expect_tx(fb, (uint32_t)mine * 512u);
+                    __syncwarp();
+                    if (lane < mine)
+                        tma_gather4(dst + (kGroupsPW * warp + lane) * 512, &p.tmap_b, kb * kBK, y0, y1, y2, y3, fb);
+                }
+            } else if (tid == 0) {
+                mbar_expect_tx(fb, (uint32_t)p.b_box_rows * 128u);
+                tma_load_2d(dst, &p.tmap_b, kb * kBK, iti.tok0, fb);
+            }
+        };
+        auto issue_raw = [&](int kb, int slot) {
+            uint8_t* dst = sRaw + slot * kRawSlotBytes + tid * kRawBytes;
+            if (QT == MOE_Q4_K) {
+                const uint8_t* blk = is_wrow + (int64_t)(kb >> 2) * kQ4KBytes;
+                cp_async16(dst, blk, 16u);                                    // header
+                const uint8_t* qs = blk + 16 + 32 * (kb & 3) + (32 / kSplit) * part;
+                if constexpr (kSplit == 2) cp_async16(dst + 16, qs, 16u);
+                else cp_async8(dst + 16, qs);
+            } else {
+                const uint8_t* src = is_wrow + (int64_t)kb * 2 * kQ80Bytes;     // two blocks, 68 bytes
+#pragma unroll
+                for (int w = 0; w < 17; ++w) cp_async4(dst + 4 * w, src + 4 * w);
+            }
+        };
+        // issue global k-step gs (the cursor's) and advance the cursor; always one commit group
+        auto issue_next = [&](uint32_t gs) {
+            if (is_valid) {
+                issue_raw(is_kb, gs % kRawSlots);
+                issue_b(is_kb, gs % kBStages);
+                if (++is_kb == nk) {
+                    is_kb = 0;
+                    is_t += gridDim.x;
+                    is_tile();
+                }
+            }
+            cp_commit();
+        };
+        is_tile();
+        issue_next(0);
+        issue_next(1);
+
         uint32_t g = 0;                             // global k-step counter
         int tile_iter = 0;
         for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x, ++tile_iter) {
             TileInfo ti;
             if (!tile_at(p, n_mb, t, n_tb, ti)) break;
-            const uint8_t* wrow = (MODE == kGateUp && psel == 1 ? p.w1 : p.w0) + (int64_t)ti.e * p.expert_stride +
-                                  (int64_t)(ti.m0 + prow) * rb;
-            // GATEUP: the x16 row of column 32 * warp + lane of the block (columns past the block's
-            // tokens take its first token's row; they are never read)
-            int myrow = 0;
-            if (MODE == kGateUp) {
-                const int r = 32 * warp + lane;
-                const int i = ti.tok0 + (r < ti.ntok ? r : 0);
-                myrow = p.sorted_pairs ? p.sorted_pairs[i] / p.k : i;
-            }
-            // B of k-step kb into stage `stage`, completing on full[stage]: GATEUP gathers four
-            // x16 rows per TMA (warp w: groups 8w..8w+7 of the rows the block needs), DOWN loads
-            // the BN consecutive h16 rows of the block in one box
-            auto issue_b = [&](int kb, int stage) {
-                uint8_t* dst = sB + stage * kBStageBytes;
-                uint64_t* fb = &full[stage];
-                if (MODE == kGateUp) {
-                    const int ngroups = (ti.ntok + 3) >> 2;
-                    const int mine = min(8, max(0, ngroups - 8 * warp));
-                    if (mine > 0) {
-                        const int src = (4 * lane) & 31;
-                        const int y0 = __shfl_sync(0xffffffffu, myrow, src), y1 = __shfl_sync(0xffffffffu, myrow, src + 1);
-                        const int y2 = __shfl_sync(0xffffffffu, myrow, src + 2), y3 = __shfl_sync(0xffffffffu, myrow, src + 3);
-                        if (lane == 0) mbar_expect_tx(fb, (uint32_t)mine * 512u);
-                        __syncwarp();
-                        if (lane < mine)
-                            tma_gather4(dst + (8 * warp + lane) * 512, &p.tmap_b, kb * kBK, y0, y1, y2, y3, fb);
-                    }
-                } else if (tid == 0) {
-                    mbar_expect_tx(fb, (uint32_t)p.b_box_rows * 128u);
-                    tma_load_2d(dst, &p.tmap_b, kb * kBK, ti.tok0, fb);
-                }
-            };
-            auto issue_raw = [&](int kb, int slot) {
-                uint8_t* dst = sRaw + slot * kRawSlotBytes + tid * kRawBytes;
-                if (QT == MOE_Q4_K) {
-                    const uint8_t* blk = wrow + (int64_t)(kb >> 2) * kQ4KBytes;
-                    cp_async16(dst, blk, 16u);                                    // header
-                    if (MODE == kGateUp) {
-                        cp_async16(dst + 16, blk + 16 + 32 * (kb & 3), 16u);
-                        cp_async16(dst + 32, blk + 32 + 32 * (kb & 3), 16u);
-                    } else {
-                        cp_async16(dst + 16, blk + 16 + 32 * (kb & 3) + 16 * psel, 16u);
-                    }
-                } else {
-                    const uint8_t* src = wrow + (int64_t)kb * 2 * kQ80Bytes;       // two blocks, 68 bytes
-#pragma unroll
-                    for (int w = 0; w < 17; ++w) cp_async4(dst + 4 * w, src + 4 * w);
-                }
-            };
-            // prologue: raw0 + B0, raw1 + B1; the raw group and B of step kb + 2 are issued right
-            // after step kb's dequantization (stage (g+2)%4 and the raw slot just read are free)
-            issue_raw(0, g % kRawSlots);
-            if (nk > 0) issue_b(0, g % kBStages);
-            cp_commit();
-            if (nk > 1) {
-                issue_raw(1, (g + 1) % kRawSlots);
-                issue_b(1, (g + 1) % kBStages);
-            }
-            cp_commit();
-
             bool ok = true;
             for (int kb = 0; kb < nk; ++kb, ++g) {
                 // A stage g%2 and B stage (g+2)%4 were last read by MMA(g-2)
                 if (g >= 2 && !mbar_wait(&empty[(g + 2) & 3], ((g - 2) >> 2) & 1, abort_flag)) { ok = false; break; }
-                cp_wait<1>();                        // raw(kb) has landed
+                cp_wait<1>();                        // raw(g) has landed (only g + 1 may be pending)
                 // ---- dequantize k-step kb into A stage g%2
                 const uint8_t* raw = sRaw + (g % kRawSlots) * kRawSlotBytes + tid * kRawBytes;
-                uint8_t* arow = sA + (g % kAStages) * kAStageBytes + (MODE == kGateUp ? psel * kBM * 128 : 0);
+                uint8_t* arow = sA + (g % kAStages) * kAStageBytes + pmat * kBM * 128;
                 if (QT == MOE_Q4_K) {
                     const uint4 hd = *reinterpret_cast<const uint4*>(raw);
                     const int c = kb & 3;
@@ -286,33 +307,21 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) tc_gemm_kernel(const __
                     q4k_scale_min(hd, 2 * c, fs0, fm0);
                     q4k_scale_min(hd, 2 * c + 1, fs1, fm1);
                     const Q4H2 hc = q4h2_consts(fs0, fm0, fs1, fm1);
-                    if (MODE == kGateUp) {
-                        const uint4 q0 = *reinterpret_cast<const uint4*>(raw + 16);
-                        const uint4 q1 = *reinterpret_cast<const uint4*>(raw + 32);
-                        const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                        // chunk ch < 4: elements 8ch.. of sub-block 2c (low nibbles of words 2ch, 2ch+1);
-                        // chunk 4 + ch: the same elements of 2c+1 (high nibbles)
+                    // this thread's quant bytes: elements (32 / kSplit) * part .. of sub-blocks 2c (low
+                    // nibbles) and 2c + 1 (high nibbles); each pair of words fills chunk ch (elements
+                    // 8ch..8ch+7 of 2c) and chunk 4 + ch (the same elements of 2c + 1)
+                    constexpr int kWords = 8 / kSplit;
+                    uint32_t qw[kWords];
 #pragma unroll
-                        for (int ch = 0; ch < 4; ++ch) {
-                            uint32_t la[2], ha[2], lb[2], hb[2];
-                            q4_word_h2(qw[2 * ch], hc, la, ha);
-                            q4_word_h2(qw[2 * ch + 1], hc, lb, hb);
-                            *reinterpret_cast<uint4*>(arow + swz(prow, ch)) = make_uint4(la[0], la[1], lb[0], lb[1]);
-                            *reinterpret_cast<uint4*>(arow + swz(prow, 4 + ch)) = make_uint4(ha[0], ha[1], hb[0], hb[1]);
-                        }
-                    } else {
-                        const uint4 q = *reinterpret_cast<const uint4*>(raw + 16);   // bytes 16*psel .. +15
-                        const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
-                        // words 0,1: elements 16*psel + 0..7 (chunk 2*psel), words 2,3: + 8..15 (chunk 2*psel+1)
+                    for (int w = 0; w < kWords; ++w) qw[w] = reinterpret_cast<const uint32_t*>(raw + 16)[w];
 #pragma unroll
-                        for (int part = 0; part < 2; ++part) {
-                            uint32_t la[2], ha[2], lb[2], hb[2];
-                            q4_word_h2(qw[2 * part], hc, la, ha);
-                            q4_word_h2(qw[2 * part + 1], hc, lb, hb);
-                            const int ch = 2 * psel + part;
-                            *reinterpret_cast<uint4*>(arow + swz(prow, ch)) = make_uint4(la[0], la[1], lb[0], lb[1]);
-                            *reinterpret_cast<uint4*>(arow + swz(prow, 4 + ch)) = make_uint4(ha[0], ha[1], hb[0], hb[1]);
-                        }
+                    for (int w2 = 0; w2 < kWords / 2; ++w2) {
+                        uint32_t la[2], ha[2], lb[2], hb[2];
+                        q4_word_h2(qw[2 * w2], hc, la, ha);
+                        q4_word_h2(qw[2 * w2 + 1], hc, lb, hb);
+                        const int ch = part * (kWords / 2) + w2;
+                        *reinterpret_cast<uint4*>(arow + swz(prow, ch)) = make_uint4(la[0], la[1], lb[0], lb[1]);
+                        *reinterpret_cast<uint4*>(arow + swz(prow, 4 + ch)) = make_uint4(ha[0], ha[1], hb[0], hb[1]);
                     }
                 } else {
                     // Q8_0: 68 bytes = d0, q0[32], d1, q1[32]
@@ -323,7 +332,7 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) tc_gemm_kernel(const __
                     const float d1 = __half2float(__ushort_as_half((unsigned short)(wv[8] >> 16)));
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch) {
-                        if (MODE == kDown && (ch >> 2) != psel) continue;     // DOWN: this thread's block only
+                        if (kSplit == 2 && (ch >> 2) != part) continue;       // DOWN: this thread's block only
                         const int b0 = ch < 4 ? 2 + 8 * ch : 36 + 8 * (ch - 4);
                         const float d = ch < 4 ? d0 : d1;
                         float v[8];
@@ -339,22 +348,18 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) tc_gemm_kernel(const __
                 }
                 fence_async_smem();
                 mbar_arrive(&full[g & 3]);
-                if (kb + 2 < nk) {
-                    issue_raw(kb + 2, g % kRawSlots);
-                    issue_b(kb + 2, (g + 2) % kBStages);
-                }
-                cp_commit();
+                issue_next(g + 2);
             }
-            cp_wait_all();
             if (!ok) break;
             if constexpr (MODE == kGateUp) {
                 // ---- epilogue: wait for the accumulators of this tile, h = SiLU(gate) * up
                 if (!mbar_wait(&accf[0], tile_iter & 1, abort_flag)) break;
                 tc_after();
-                const int q = warp & 3, half = warp >> 2;
+                // warp w reads TMEM lanes 32 (w % 4).. and every (kPW / 4)-th group of 16 columns
+                const int q = warp & 3;
                 const int m = q * 32 + lane;
                 __half* hrow = p.h_out + (int64_t)ti.tok0 * p.rows + ti.m0 + m;
-                for (int c16 = half * 16; c16 < ti.n_inst; c16 += 32) {
+                for (int c16 = (warp >> 2) * 16; c16 < ti.n_inst; c16 += 16 * (kPW / 4)) {
                     uint32_t a[16], u[16];
                     tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c16, a);
                     tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(BN + c16), u);
@@ -374,7 +379,7 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1) tc_gemm_kernel(const __
         cp_wait_all();
     } else if (warp < kMmaWarp) {
         // ======================= DOWN epilogue warps =======================
-        // warp kProducerWarps + q reads TMEM lanes 32q.. (q = warp % 4); y fp32 per pair
+        // warp kPW + q reads TMEM lanes 32q.. (q = warp % 4); y fp32 per pair
         const int q = warp & 3;
         const int m = q * 32 + lane;
         int j = 0;
@@ -518,7 +523,7 @@ template <int QT, int MODE>
 size_t tc_smem_bytes() {
     constexpr int a = kAStages * (MODE == kGateUp ? 2 : 1) * kBM * 128;
     constexpr int b = kBStages * tc_bn<QT>() * 128;
-    constexpr int r = kRawSlots * kProducers * RawCfg<QT, MODE>::kBytes;
+    constexpr int r = kRawSlots * 32 * tc_pw<QT, MODE>() * RawCfg<QT, MODE>::kBytes;
     return (size_t)a + b + r + 256 + 1024;   // barriers + alignment slack
 }
 
@@ -574,7 +579,7 @@ cudaError_t launch_tc(const TcParams& p, int max_tiles, cudaStream_t s) {
                                            (int)smem);
     if (err != cudaSuccess) return err;
     const int grid = max(1, min(num_sms(), max_tiles));
-    tc_gemm_kernel<QT, MODE><<<grid, tc_threads<MODE>(), smem, s>>>(p);
+    tc_gemm_kernel<QT, MODE><<<grid, tc_threads<QT, MODE>(), smem, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -72,6 +72,9 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t 
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(su32(dst)), "l"(src), "r"(src_bytes)
                  : "memory");
 }
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(su32(dst)), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(su32(dst)), "l"(src) : "memory");
 }
