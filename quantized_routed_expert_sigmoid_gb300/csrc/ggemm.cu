@@ -55,45 +55,54 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// scale and min of sub-block j (0..7) of a Q4_K block header (words y, z, w = scale bytes 0-11)
 // Eight fp16 weights of one Q4_K word into two 16-byte halves of a chunk: the low nibbles of
 // bytes b0..b3 are elements 0..3 of sub-block 2c, the high nibbles elements 0..3 of 2c+1.
-// A nibble q placed under the fp16 exponent of 1024 reads as 1024 + q (low nibble) or
-// 1024 + 16q (high nibble, left in place); one exact subtraction leaves q (or 16q), and one
-// fp16 FMA applies the sub-block's scale (s, or s/16) and min: w = s*q - m.
+// A low nibble q placed under the fp16 exponent of 1024 reads as 1024 + q; a high nibble,
+// left in place (16q) under the exponent of 64 (one unit in the last place = 1/16), reads as
+// 64 + q.  One exact subtraction leaves q, and one fp16 FMA applies the sub-block's scale and
+// min: w = s*q - m (rounded once).
 struct Q4H2 {
     __half2 s_lo, m_lo, s_hi, m_hi;       // m already negated
 };
-__device__ __forceinline__ Q4H2 q4h2_consts(float fs0, float fm0, float fs1, float fm1) {
-    Q4H2 c;
-    c.s_lo = __float2half2_rn(fs0);
-    c.m_lo = __float2half2_rn(-fm0);
-    c.s_hi = __float2half2_rn(fs1 * 0.0625f);
-    c.m_hi = __float2half2_rn(-fm1);
-    return c;
-}
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 // w -> (lo: elements 0,1 | 2,3 of sub-block 2c) and (hi: the same of 2c+1), as fp16 pairs
 __device__ __forceinline__ void q4_word_h2(uint32_t w, const Q4H2& c, uint32_t (&lo)[2], uint32_t (&hi)[2]) {
-    const __half2 k1024 = __float2half2_rn(1024.0f);
+    const __half2 k1024 = __float2half2_rn(1024.0f), k64 = __float2half2_rn(64.0f);
     const uint32_t t01 = __byte_perm(w, 0u, 0x4140u);        // [b0, 0, b1, 0]
     const uint32_t t23 = __byte_perm(w, 0u, 0x4342u);        // [b2, 0, b3, 0]
     lo[0] = h2u(__hfma2(__hsub2(u2h((t01 & 0x000F000Fu) | 0x64006400u), k1024), c.s_lo, c.m_lo));
     lo[1] = h2u(__hfma2(__hsub2(u2h((t23 & 0x000F000Fu) | 0x64006400u), k1024), c.s_lo, c.m_lo));
-    hi[0] = h2u(__hfma2(__hsub2(u2h((t01 & 0x00F000F0u) | 0x64006400u), k1024), c.s_hi, c.m_hi));
-    hi[1] = h2u(__hfma2(__hsub2(u2h((t23 & 0x00F000F0u) | 0x64006400u), k1024), c.s_hi, c.m_hi));
+    hi[0] = h2u(__hfma2(__hsub2(u2h((t01 & 0x00F000F0u) | 0x54005400u), k64), c.s_hi, c.m_hi));
+    hi[1] = h2u(__hfma2(__hsub2(u2h((t23 & 0x00F000F0u) | 0x54005400u), k64), c.s_hi, c.m_hi));
 }
-__device__ __forceinline__ void q4k_scale_min(const uint4& hd, int j, float& fsc, float& fm) {
-    const float d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
-    const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
-    const int jj = j & 3;
-    const uint32_t by = (hd.y >> (8 * jj)) & 0xFFu, bz = (hd.z >> (8 * jj)) & 0xFFu, bw = (hd.w >> (8 * jj)) & 0xFFu;
-    uint32_t sc, m;
-    if (j < 4) { sc = by & 63u; m = bz & 63u; }
-    else { sc = (bw & 15u) | ((by >> 6) << 4); m = (bw >> 4) | ((bz >> 6) << 4); }
-    fsc = d * (float)sc;
-    fm = dmin * (float)m;
+// Scales and negated mins of the eight sub-blocks of a Q4_K block header as fp16 pairs:
+// sc[c] = (d*sc_2c, d*sc_2c+1) and mn[c] = (-dmin*m_2c, -dmin*m_2c+1) for k-step c of the
+// super-block.  The 6-bit codes (public Q4_K packing: codes 0-3 in the low six bits of scale
+// bytes 0-3 and 4-7, codes 4-7 from the nibbles of bytes 8-11 and the top two bits of bytes
+// 0-7) become exact fp16 integers (1024 + b under the exponent of 1024, minus 1024); each
+// product is rounded once, as the exact product rounded to fp16.
+struct Q4Scales {
+    __half2 sc0, sc1, sc2, sc3, mn0, mn1, mn2, mn3;     // named, so that selecting one stays in registers
+};
+__device__ __forceinline__ Q4Scales q4k_scales_h2(const uint4& hd) {
+    const uint32_t sc_lo = hd.y & 0x3F3F3F3Fu, m_lo = hd.z & 0x3F3F3F3Fu;
+    const uint32_t sc_hi = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
+    const uint32_t m_hi = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
+    const __half2 d2 = u2h(__byte_perm(hd.x, 0u, 0x1010u));                  // (d, d)
+    const __half2 nm2 = u2h(__byte_perm(hd.x, 0u, 0x3232u) ^ 0x80008000u);    // (-dmin, -dmin)
+    const __half2 k1024 = __float2half2_rn(1024.0f);
+    auto pair = [&](uint32_t v, uint32_t sel) { return __hsub2(u2h(__byte_perm(v, 0x64u, sel)), k1024); };
+    Q4Scales r;
+    r.sc0 = __hmul2(pair(sc_lo, 0x4140u), d2);
+    r.sc1 = __hmul2(pair(sc_lo, 0x4342u), d2);
+    r.sc2 = __hmul2(pair(sc_hi, 0x4140u), d2);
+    r.sc3 = __hmul2(pair(sc_hi, 0x4342u), d2);
+    r.mn0 = __hmul2(pair(m_lo, 0x4140u), nm2);
+    r.mn1 = __hmul2(pair(m_lo, 0x4342u), nm2);
+    r.mn2 = __hmul2(pair(m_hi, 0x4140u), nm2);
+    r.mn3 = __hmul2(pair(m_hi, 0x4342u), nm2);
+    return r;
 }
 
 // Raw bytes staged per producer thread per k-step.
@@ -221,16 +230,26 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
         TileInfo iti{};
         bool is_valid = false;
         const uint8_t* is_wrow = nullptr;
-        int is_row = 0;     // GATEUP: lane l < kRowsPW holds the x16 row of column kRowsPW * warp + l
+        // GATEUP: this warp's gathers of the cursor's tile: how many, and the four x16 rows of
+        // the lane's group (lane < is_mine)
+        int is_mine = 0, is_y0 = 0, is_y1 = 0, is_y2 = 0, is_y3 = 0;
         auto is_tile = [&]() {
             is_valid = is_t < n_tiles && tile_at(p, n_mb, is_t, n_tb, iti);
             if (!is_valid) return;
             is_wrow = (pmat == 1 ? p.w1 : p.w0) + (int64_t)iti.e * p.expert_stride + (int64_t)(iti.m0 + prow) * rb;
             if (MODE == kGateUp) {
-                // columns past the block's tokens take its first token's row (never read)
+                // lane l < kRowsPW takes the x16 row of column kRowsPW * warp + l; columns past the
+                // block's tokens take its first token's row (never read)
                 const int r = kRowsPW * warp + lane;
                 const int i = iti.tok0 + (r < iti.ntok ? r : 0);
-                is_row = p.sorted_pairs ? p.sorted_pairs[i] / p.k : i;
+                const int row = p.sorted_pairs ? p.sorted_pairs[i] / p.k : i;
+                const int ngroups = (iti.ntok + 3) >> 2;
+                is_mine = min(kGroupsPW, max(0, ngroups - kGroupsPW * warp));
+                const int src = (4 * lane) & (kRowsPW - 1);
+                is_y0 = __shfl_sync(0xffffffffu, row, src);
+                is_y1 = __shfl_sync(0xffffffffu, row, src + 1);
+                is_y2 = __shfl_sync(0xffffffffu, row, src + 2);
+                is_y3 = __shfl_sync(0xffffffffu, row, src + 3);
             }
         };
         // B of the cursor's k-step into stage `stage`, completing on full[stage]: GATEUP gathers
@@ -240,16 +259,12 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
             uint8_t* dst = sB + stage * kBStageBytes;
             uint64_t* fb = &full[stage];
             if (MODE == kGateUp) {
-                const int ngroups = (iti.ntok + 3) >> 2;
-                const int mine = min(kGroupsPW, max(0, ngroups - kGroupsPW * warp));
-                if (mine > 0) {
-                    const int src = (4 * lane) & (kRowsPW - 1);
-                    const int y0 = __shfl_sync(0xffffffffu, is_row, src), y1 = __shfl_sync(0xffffffffu, is_row, src + 1);
-                    const int y2 = __shfl_sync(0xffffffffu, is_row, src + 2), y3 = __shfl_sync(0xffffffffu, is_row, src + 3);
-                    if (lane == 0) mbar_expect_tx(fb, (uint32_t)mine * 512u);
+                if (is_mine > 0) {
+                    if (lane == 0) mbar_expect_tx(fb, (uint32_t)is_mine * 512u);
                     __syncwarp();
-                    if (lane < mine)
-                        tma_gather4(dst + (kGroupsPW * warp + lane) * 512, &p.tmap_b, kb * kBK, y0, y1, y2, y3, fb);
+                    if (lane < is_mine)
+                        tma_gather4(dst + (kGroupsPW * warp + lane) * 512, &p.tmap_b, kb * kBK, is_y0, is_y1, is_y2,
+                                    is_y3, fb);
                 }
             } else if (tid == 0) {
                 mbar_expect_tx(fb, (uint32_t)p.b_box_rows * 128u);
@@ -260,7 +275,7 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
             uint8_t* dst = sRaw + slot * kRawSlotBytes + tid * kRawBytes;
             if (QT == MOE_Q4_K) {
                 const uint8_t* blk = is_wrow + (int64_t)(kb >> 2) * kQ4KBytes;
-                cp_async16(dst, blk, 16u);                                    // header
+                if ((kb & 3) == 0) cp_async16(dst, blk, 16u);                 // header, once per super-block
                 const uint8_t* qs = blk + 16 + 32 * (kb & 3) + (32 / kSplit) * part;
                 if constexpr (kSplit == 2) cp_async16(dst + 16, qs, 16u);
                 else cp_async8(dst + 16, qs);
@@ -289,6 +304,7 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
 
         uint32_t g = 0;                             // global k-step counter
         int tile_iter = 0;
+        Q4Scales qs4{};                             // Q4_K: scales of the current super-block
         for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x, ++tile_iter) {
             TileInfo ti;
             if (!tile_at(p, n_mb, t, n_tb, ti)) break;
@@ -301,12 +317,13 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
                 const uint8_t* raw = sRaw + (g % kRawSlots) * kRawSlotBytes + tid * kRawBytes;
                 uint8_t* arow = sA + (g % kAStages) * kAStageBytes + pmat * kBM * 128;
                 if (QT == MOE_Q4_K) {
-                    const uint4 hd = *reinterpret_cast<const uint4*>(raw);
+                    // the header (read at the super-block's first k-step) gives the scales of all four
                     const int c = kb & 3;
-                    float fs0, fm0, fs1, fm1;
-                    q4k_scale_min(hd, 2 * c, fs0, fm0);
-                    q4k_scale_min(hd, 2 * c + 1, fs1, fm1);
-                    const Q4H2 hc = q4h2_consts(fs0, fm0, fs1, fm1);
+                    if (c == 0) qs4 = q4k_scales_h2(*reinterpret_cast<const uint4*>(raw));
+                    const uint32_t scp = c == 0 ? h2u(qs4.sc0) : c == 1 ? h2u(qs4.sc1) : c == 2 ? h2u(qs4.sc2) : h2u(qs4.sc3);
+                    const uint32_t mnp = c == 0 ? h2u(qs4.mn0) : c == 1 ? h2u(qs4.mn1) : c == 2 ? h2u(qs4.mn2) : h2u(qs4.mn3);
+                    const Q4H2 hc{u2h(__byte_perm(scp, 0u, 0x1010u)), u2h(__byte_perm(mnp, 0u, 0x1010u)),
+                                  u2h(__byte_perm(scp, 0u, 0x3232u)), u2h(__byte_perm(mnp, 0u, 0x3232u))};
                     // this thread's quant bytes: elements (32 / kSplit) * part .. of sub-blocks 2c (low
                     // nibbles) and 2c + 1 (high nibbles); each pair of words fills chunk ch (elements
                     // 8ch..8ch+7 of 2c) and chunk 4 + ch (the same elements of 2c + 1)
