@@ -542,7 +542,8 @@ moe_status moe_layer_timed(const moe_layer_plan* plan, const void* x, int T, flo
         a.sorted_pairs = sorted; a.offsets = offs;
         a.x16 = at<__half>(workspace, w.x16);
         a.h16 = at<__half>(workspace, w.h);
-        a.y = y;
+        a.y = nullptr;
+        a.y16 = at<__half>(workspace, w.y);          // fp16 per-pair outputs, read by the combine
         a.tb_list = at<int4>(workspace, w.tiles);
         a.hdr = hdr;
         a.ev_before_gateup = evb;
@@ -562,6 +563,7 @@ moe_status moe_layer_timed(const moe_layer_plan* plan, const void* x, int T, flo
             b.ev_before_gateup = b.ev_after_gateup = nullptr;
             b.h16 = at<__half>(workspace, w.sh_h);
             b.y = at<float>(workspace, w.sh_y);
+            b.y16 = nullptr;
             err = launch_tc_expert_ffn(b, s);
             if (err != cudaSuccess) return cuda_fail(err, "tensor-core shared expert kernels");
             shared = b.y;
@@ -582,7 +584,8 @@ moe_status moe_layer_timed(const moe_layer_plan* plan, const void* x, int T, flo
             shared = sy;
         }
     }
-    err = launch_combine(y, gw, ppos, T, k, H, shared, d.accumulate != 0, out, s);
+    err = w.tc ? launch_combine16(at<__half>(workspace, w.y), gw, ppos, T, k, H, shared, d.accumulate != 0, out, s)
+               : launch_combine(y, gw, ppos, T, k, H, shared, d.accumulate != 0, out, s);
     if (err != cudaSuccess) return cuda_fail(err, "combine kernel");
     return MOE_OK;
 }

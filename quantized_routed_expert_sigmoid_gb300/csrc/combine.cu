@@ -14,7 +14,17 @@
 namespace moe {
 namespace {
 
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const float* __restrict__ w,
+__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 load4(const __half* p) {
+    const uint2 r = *reinterpret_cast<const uint2*>(p);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&r.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&r.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// y fp32 (GEMV paths) or fp16 (tensor-core path); the sum is fp32 either way
+template <typename YT>
+__global__ void __launch_bounds__(256) combine_kernel(const YT* __restrict__ y, const float* __restrict__ w,
                                                       const int32_t* __restrict__ pair_pos, int k, int H,
                                                       const float* __restrict__ shared, bool accumulate,
                                                       float* __restrict__ out) {
@@ -26,7 +36,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
         const int pp = pair_pos[(int64_t)t * k + j];
         if (pp < 0) continue;
         const float wj = w[(int64_t)t * k + j];
-        const float4 v = *reinterpret_cast<const float4*>(y + (int64_t)pp * H + n);
+        const float4 v = load4(y + (int64_t)pp * H + n);
         acc.x = fmaf(wj, v.x, acc.x);
         acc.y = fmaf(wj, v.y, acc.y);
         acc.z = fmaf(wj, v.z, acc.z);
@@ -88,7 +98,15 @@ cudaError_t launch_combine(const float* y_pairs, const float* w, const int32_t* 
                            int H, const float* shared_out, bool accumulate, float* out, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
     dim3 grid(T, (H / 4 + 255) / 256);
-    combine_kernel<<<grid, 256, 0, s>>>(y_pairs, w, pair_pos, k, H, shared_out, accumulate, out);
+    combine_kernel<float><<<grid, 256, 0, s>>>(y_pairs, w, pair_pos, k, H, shared_out, accumulate, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine16(const __half* y_pairs, const float* w, const int32_t* pair_pos, int T, int k, int H,
+                             const float* shared_out, bool accumulate, float* out, cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    dim3 grid(T, (H / 4 + 255) / 256);
+    combine_kernel<__half><<<grid, 256, 0, s>>>(y_pairs, w, pair_pos, k, H, shared_out, accumulate, out);
     return cudaGetLastError();
 }
 

@@ -5,23 +5,27 @@
 // 0.3.1", "Why it is fast": prompts as tensor-core GEMMs).  Here each expert's
 // tokens form a dense GEMM against that expert's GGUF weights:
 //   GATEUP: h[i, r] = silu(Wg[e][r] . x_t) * (Wu[e][r] . x_t)     (fp16 out)
-//   DOWN  : y[i, n] = Wd[e][n] . h[i]                             (fp32 out)
-// Tile = 128 weight rows (MMA M) x up to 128 pairs of one expert (MMA N),
-// K in steps of 64.  Weights are dequantized from Q4_K / Q8_0 to fp16 in
-// shared memory (128-byte swizzled K-major tiles); token rows are gathered
-// with cp.async into the same layout; one thread issues tcgen05.mma with the
-// accumulators in TMEM (fp32); the epilogue reads TMEM with tcgen05.ld.
-// Persistent CTAs (one per SM) walk a device-built list of token blocks, so
-// the launch needs no host knowledge of the per-expert counts.
+//   DOWN  : y[i, n] = Wd[e][n] . h[i]     (fp32 out; fp16 for the layer, whose combine sums in fp32)
+// Tile = 128 weight rows (MMA M; gate/up: 128 rows of each) x one token block of the expert
+// (MMA N: up to 256 pairs for Q4_K, 128 for Q8_0), K in steps of 64.  Weights are
+// dequantized from Q4_K / Q8_0 to fp16 in shared memory (128-byte swizzled K-major tiles);
+// token rows arrive by TMA into the same layout (gate/up: gather4 of x16 rows, four per
+// copy; down: one box of consecutive h16 rows); one thread issues tcgen05.mma with the
+// accumulators in TMEM (fp32); tcgen05.ld reads them back for the epilogue.  Persistent CTAs
+// (one per SM) walk a device-built list of token blocks, so the launch needs no host
+// knowledge of the per-expert counts.
 //
-// Warp roles (288 threads): warps 0-7 stage operands (dequant + gather) and
-// run the epilogue; warp 8 owns TMEM and issues the MMAs.  Pipeline per
-// k-step g: producers wait until MMA(g-2) has finished (so A stage g%2 and B
-// stage (g+2)%4 are free), prefetch B(g+2) and the raw blocks of g+3 with
-// cp.async, dequantize g into A stage g%2, and arrive on full[g%4]; the MMA
-// warp waits full[g%4], issues 4 k-substeps, and commits to empty[g%4].
-// Every wait is bounded (globaltimer); on timeout the kernel records
-// MOE_ERR_TIMEOUT, drains its MMAs, frees TMEM and returns.
+// Warp roles: producer warps (16 for the Q4_K gate/up, else 8) copy the raw blocks with
+// cp.async, dequantize them and issue the token-row TMA; gate/up producers also run the
+// SwiGLU epilogue (its accumulators fill all 512 TMEM columns); down has 8 epilogue warps
+// and two accumulator buffers, so its epilogue overlaps the next tile; the last warp owns
+// TMEM and issues the MMAs.  Pipeline per global k-step g: a producer waits until the A
+// stage g%2 is free (MMA(g-2) done), waits for raw(g), dequantizes it, arrives on full[g%4]
+// (which also counts the TMA bytes of B(g)), then issues raw and B of step g + D (D = 2 for
+// gate/up, 3 for down, across tile boundaries); the MMA warp waits full[g%4], issues four
+// k-substeps and commits to empty[g%4].  Every wait is bounded (globaltimer); on timeout
+// the kernel records MOE_ERR_TIMEOUT, drains its MMAs, lets copies in flight land, frees
+// TMEM and returns.
 #include <algorithm>
 #include <cuda.h>   // CUtensorMap and its enums (the encoder is fetched from the driver at run time)
 
@@ -38,7 +42,12 @@ constexpr int kBNMin = 128;                       // token-block width bound use
 // down: half a k-step per thread already; Q8_0: its raw blocks need the shared memory).
 template <int QT, int MODE>
 __host__ __device__ constexpr int tc_pw() { return QT == MOE_Q4_K && MODE == 0 ? 16 : 8; }
-constexpr int kAStages = 2, kBStages = 4, kRawSlots = 2;
+constexpr int kAStages = 2, kBStages = 4;
+// How many k-steps ahead of the dequantization the raw blocks and token rows are issued: 2
+// for gate/up (its shared memory is full), 3 for down (its k-steps are half as long, so two
+// of them do not cover the latency of a DRAM read); one raw slot per step in flight.
+template <int MODE>
+__host__ __device__ constexpr int tc_dist() { return MODE == 0 ? 2 : 3; }
 
 enum { kGateUp = 0, kDown = 1 };
 
@@ -130,7 +139,8 @@ struct TcParams {
     int bn;                      // token-block width of the list (tc_bn)
     int b_box_rows;              // DOWN: rows of the B box (BN, or P when fewer)
     __half* h_out;               // GATEUP: [P][rows] fp16
-    float* y_out;                // DOWN: [P][rows] fp32
+    float* y_out;                // DOWN: [P][rows] fp32, or
+    __half* y16_out;             //       [P][rows] fp16 when set
     WsHeader* hdr;
 };
 
@@ -149,12 +159,12 @@ __device__ __forceinline__ bool tile_at(const TcParams& p, int n_mb, int t, int 
     return true;
 }
 
-// Warp layout: producers 0-7, then (DOWN) 4 epilogue warps, then the MMA warp.  DOWN keeps
+// Warp layout: producers, then (DOWN) 8 epilogue warps, then the MMA warp.  DOWN keeps
 // two accumulators in TMEM so that its epilogue overlaps the next tile's main loop; GATEUP
 // needs all 512 columns for one tile (gate and up, 256 tokens each) and lets the producers
 // run its epilogue.
 template <int MODE>
-__host__ __device__ constexpr int tc_epi_warps() { return MODE == kDown ? 4 : 0; }
+__host__ __device__ constexpr int tc_epi_warps() { return MODE == kDown ? 8 : 0; }
 template <int QT, int MODE>
 __host__ __device__ constexpr int tc_threads() { return 32 * tc_pw<QT, MODE>() + 32 * tc_epi_warps<MODE>() + 32; }
 
@@ -169,6 +179,8 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
     constexpr int kMats = MODE == kGateUp ? 2 : 1;
     constexpr int kSplit = kNP / (kBM * kMats);       // threads per (row, matrix) of a k-step
     constexpr int kRawSlotBytes = kNP * kRawBytes;
+    constexpr int kDist = tc_dist<MODE>();
+    constexpr int kRawSlots = kDist;
     constexpr int kEpiWarps = tc_epi_warps<MODE>();
     constexpr int kMmaWarp = kPW + kEpiWarps;
     constexpr uint32_t kAccCols = (MODE == kGateUp ? 2 : 1) * BN;
@@ -299,8 +311,7 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
             cp_commit();
         };
         is_tile();
-        issue_next(0);
-        issue_next(1);
+        for (int i = 0; i < kDist; ++i) issue_next((uint32_t)i);
 
         uint32_t g = 0;                             // global k-step counter
         int tile_iter = 0;
@@ -310,9 +321,10 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
             if (!tile_at(p, n_mb, t, n_tb, ti)) break;
             bool ok = true;
             for (int kb = 0; kb < nk; ++kb, ++g) {
-                // A stage g%2 and B stage (g+2)%4 were last read by MMA(g-2)
-                if (g >= 2 && !mbar_wait(&empty[(g + 2) & 3], ((g - 2) >> 2) & 1, abort_flag)) { ok = false; break; }
-                cp_wait<1>();                        // raw(g) has landed (only g + 1 may be pending)
+                // A stage g%2 was last read by MMA(g-2) (with kDist == 3 already waited for below)
+                if (kDist == 2 && g >= 2 &&
+                    !mbar_wait(&empty[(g + 2) & 3], ((g - 2) >> 2) & 1, abort_flag)) { ok = false; break; }
+                cp_wait<kDist - 1>();                // raw(g) has landed (only later steps may be pending)
                 // ---- dequantize k-step kb into A stage g%2
                 const uint8_t* raw = sRaw + (g % kRawSlots) * kRawSlotBytes + tid * kRawBytes;
                 uint8_t* arow = sA + (g % kAStages) * kAStageBytes + pmat * kBM * 128;
@@ -365,7 +377,10 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
                 }
                 fence_async_smem();
                 mbar_arrive(&full[g & 3]);
-                issue_next(g + 2);
+                // B stage (g + kDist) % 4 was last read by MMA(g + kDist - 4)
+                if (kDist == 3 && g >= 1 &&
+                    !mbar_wait(&empty[(g - 1) & 3], ((g - 1) >> 2) & 1, abort_flag)) { ok = false; break; }
+                issue_next(g + kDist);
             }
             if (!ok) break;
             if constexpr (MODE == kGateUp) {
@@ -396,9 +411,12 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
         cp_wait_all();
     } else if (warp < kMmaWarp) {
         // ======================= DOWN epilogue warps =======================
-        // warp kPW + q reads TMEM lanes 32q.. (q = warp % 4); y fp32 per pair
+        // epilogue warp e reads TMEM lanes 32q.. (q = warp % 4) and the 64-column chunks
+        // e / 4, e / 4 + 2, ... of the accumulator
         const int q = warp & 3;
+        const int chunk0 = (warp - kPW) >> 2;
         const int m = q * 32 + lane;
+        const bool odd = (lane & 1) != 0;
         int j = 0;
         for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x, ++j) {
             TileInfo ti;
@@ -406,15 +424,38 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
             const int b = j & 1;
             if (!mbar_wait(&accf[b], (j >> 1) & 1, abort_flag)) break;
             tc_after();
-            float* yrow = p.y_out + (int64_t)ti.tok0 * p.rows + ti.m0 + m;
             const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)b * kAccCols;
-            for (int c16 = 0; c16 < ti.n_inst; c16 += 16) {
-                uint32_t a[16];
-                tmem_ld16(tb + (uint32_t)c16, a);
-                tmem_ld_wait();
+            // fp16: lanes 2i, 2i+1 swap one value so that each stores rows (m & ~1, m | 1) of one
+            // column as a pair (even lane: even column, odd lane: odd column)
+            __half* y16row = p.y16_out + (int64_t)(ti.tok0 + (odd ? 1 : 0)) * p.rows + ti.m0 + (m & ~1);
+            float* yrow = p.y_out + (int64_t)ti.tok0 * p.rows + ti.m0 + m;
+            for (int c64 = 64 * chunk0; c64 < ti.n_inst; c64 += 128) {
+                uint32_t a[4][16];
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj)
-                    if (c16 + jj < ti.ntok) yrow[(int64_t)(c16 + jj) * p.rows] = __uint_as_float(a[jj]);
+                for (int i = 0; i < 4; ++i) tmem_ld16(tb + (uint32_t)(c64 + 16 * i), a[i]);
+                tmem_ld_wait();
+                if (p.y16_out) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int jj = 0; jj < 16; jj += 2) {
+                            const float v0 = __uint_as_float(a[i][jj]), v1 = __uint_as_float(a[i][jj + 1]);
+                            const float recv = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+                            const float keep = odd ? v1 : v0;
+                            const __half2 hv = odd ? __floats2half2_rn(recv, keep) : __floats2half2_rn(keep, recv);
+                            const int col = c64 + 16 * i + jj;          // this lane stores column col + odd
+                            if (col + (odd ? 1 : 0) < ti.ntok)
+                                *reinterpret_cast<__half2*>(y16row + (int64_t)col * p.rows) = hv;
+                        }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int col = c64 + 16 * i + jj;
+                            if (col < ti.ntok) yrow[(int64_t)col * p.rows] = __uint_as_float(a[i][jj]);
+                        }
+                }
             }
             tc_before();
             __syncwarp();
@@ -540,7 +581,7 @@ template <int QT, int MODE>
 size_t tc_smem_bytes() {
     constexpr int a = kAStages * (MODE == kGateUp ? 2 : 1) * kBM * 128;
     constexpr int b = kBStages * tc_bn<QT>() * 128;
-    constexpr int r = kRawSlots * 32 * tc_pw<QT, MODE>() * RawCfg<QT, MODE>::kBytes;
+    constexpr int r = tc_dist<MODE>() * 32 * tc_pw<QT, MODE>() * RawCfg<QT, MODE>::kBytes;
     return (size_t)a + b + r + 256 + 1024;   // barriers + alignment slack
 }
 
@@ -651,7 +692,7 @@ cudaError_t launch_tc_expert_ffn(const TcFfnArgs& a, cudaStream_t s) {
     if ((err = make_tmap_f16(&dn.tmap_b, a.h16, P, a.I, dn.b_box_rows)) != cudaSuccess) return err;
     dn.sorted_pairs = nullptr;
     dn.tb_list = gu.tb_list; dn.n_identity = gu.n_identity; dn.bn = bn;
-    dn.y_out = a.y; dn.hdr = a.hdr;
+    dn.y_out = a.y; dn.y16_out = a.y16; dn.hdr = a.hdr;
     return launch_tc_q<kDown>(a.qtype, dn, max_tb * (a.H / kBM), s);
 }
 

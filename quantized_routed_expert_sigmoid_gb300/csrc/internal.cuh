@@ -84,6 +84,8 @@ cudaError_t launch_seg_gemv(bool gateup, const void* vin, bool vin_bf16, const i
                             int64_t expert_stride, float* out, WsHeader* hdr, int max_tokens, cudaStream_t s);
 
 // ---------------------------------------------------------------- combine, norm
+cudaError_t launch_combine16(const __half* y_pairs, const float* w, const int32_t* pair_pos, int T, int k, int H,
+                             const float* shared_out, bool accumulate, float* out, cudaStream_t s);
 cudaError_t launch_combine(const float* y_pairs, const float* w, const int32_t* pair_pos, int T, int k,
                            int H, const float* shared_out, bool accumulate, float* out, cudaStream_t s);
 cudaError_t launch_rmsnorm_bf16(const float* x, const float* gamma, int T, int H, float eps, void* u,
@@ -146,7 +148,8 @@ struct TcFfnArgs {
     const int32_t* offsets;
     __half* x16;                // [T][H]
     __half* h16;                // [P][I]
-    float* y;                   // [P][H]
+    float* y;                   // [P][H] fp32, or
+    __half* y16;                // [P][H] fp16 when set (the layer's combine reads it)
     int4* tb_list;              // token-block list (routed mode)
     WsHeader* hdr;
     cudaEvent_t ev_before_gateup, ev_after_gateup;   // optional timing events
