@@ -344,7 +344,10 @@ def run_ours(args, rank, world):
                 "timing": "CUDA events recorded around the gate/up launch, eager calls"}
     elif gu_ms is not None and not tc_path:
         achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
-        roof = {"kernel": "qgemv_kernel (gate/up + SwiGLU)", "bound": "hbm", "achieved": round(achieved, 1),
+        # Q4_K experts (up to 256 of them) take the persistent segmented kernel, others qgemv
+        kern = ("seg_gateup_kernel (persistent segmented gate/up + SwiGLU)" if shape.qtype == "q4_k" and shape.E <= 256
+                else "qgemv_kernel (gate/up + SwiGLU)")
+        roof = {"kernel": kern, "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
                 "peak_source": peak_kind, "bytes_per_launch": round(gu_bytes), "us_per_launch": round(gu_ms * 1e3, 3)}
     elif gu_ms is not None:

@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
     uint8_t* sB = sA + kAStages * kAStageBytes;
     uint8_t* sRaw = sB + kBStages * kBStageBytes;
     uint64_t* bar = reinterpret_cast<uint64_t*>(sRaw + kRawSlots * kRawSlotBytes);
-    uint64_t* full = bar;            // [4]: A dequantized (kNP arrivals) + B landed (tx bytes)
+    uint64_t* full = bar;            // [4]: A dequantized (one arrival per producer warp) + B landed (tx bytes)
     uint64_t* empty = bar + 4;       // [4]
     uint64_t* accf = bar + 8;        // [2]: accumulator buffer complete
     uint64_t* tfree = bar + 10;      // [2]: accumulator buffer read out by the epilogue warps
@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) { mbar_init(&full[i], kNP); mbar_init(&empty[i], 1); }
+        for (int i = 0; i < 4; ++i) { mbar_init(&full[i], kPW); mbar_init(&empty[i], 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(&accf[i], 1); mbar_init(&tfree[i], kEpiWarps > 0 ? kEpiWarps : 1); }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -375,8 +375,11 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
                                        pack_h2(v[6], v[7]));
                     }
                 }
+                // every thread makes its own A writes visible to the tensor core's (async) proxy;
+                // the warp then arrives once
                 fence_async_smem();
-                mbar_arrive(&full[g & 3]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[g & 3]);
                 // B stage (g + kDist) % 4 was last read by MMA(g + kDist - 4)
                 if (kDist == 3 && g >= 1 &&
                     !mbar_wait(&empty[(g - 1) & 3], ((g - 1) >> 2) & 1, abort_flag)) { ok = false; break; }
