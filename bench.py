@@ -84,7 +84,8 @@ def profiled_traffic(kernel, args):
     since the counters were taken."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            entry = json.load(f).get(f"{kernel} {args.workload}")
+            key = f"{kernel} {args.workload}" + (f" T={args.tokens}" if args.tokens else "")
+        entry = json.load(f).get(key)
         if entry and sources_digest(entry["sources"]) == entry["sources_sha1"]:
             return entry["dram_bytes_per_launch"]
     except (OSError, ValueError, KeyError):
@@ -348,7 +349,8 @@ def run_ours(args, rank, world):
         kern = ("seg_gateup_kernel (persistent segmented gate/up + SwiGLU)" if shape.qtype == "q4_k" and shape.E <= 256
                 else "qgemv_kernel (gate/up + SwiGLU)")
         roof = {"kernel": kern, "bound": "hbm", "achieved": round(achieved, 1),
-                "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                "traffic": profiled_traffic(kern.split(" ")[0], args),
                 "peak_source": peak_kind, "bytes_per_launch": round(gu_bytes), "us_per_launch": round(gu_ms * 1e3, 3)}
     elif gu_ms is not None:
         # the tensor-core gate/up: report the binding roofline (tensor pipe or HBM, whichever
@@ -360,13 +362,13 @@ def run_ours(args, rank, world):
         kern = "tc_gemm_kernel (tcgen05 gate/up + SwiGLU, fp16 operands, fp32 accumulate)"
         if tc_frac >= hbm_frac:
             roof = {"kernel": kern, "bound": "tensor", "achieved": round(tflops, 1), "peak": tc_peak,
-                    "unit": "TFLOP/s", "frac": round(tc_frac, 4), "traffic": None,
+                    "unit": "TFLOP/s", "frac": round(tc_frac, 4), "traffic": profiled_traffic("tc_gemm_kernel", args),
                     "peak_source": peak_kind + " (bf16 burst; fp16 runs at the bf16 rate)",
                     "flops_per_launch": flops, "us_per_launch": round(gu_ms * 1e3, 3),
                     "other": {"bound": "hbm", "achieved": round(gbs, 1), "unit": "GB/s", "frac": round(hbm_frac, 4)}}
         else:
             roof = {"kernel": kern, "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                    "frac": round(hbm_frac, 4), "traffic": None, "peak_source": peak_kind,
+                    "frac": round(hbm_frac, 4), "traffic": profiled_traffic("tc_gemm_kernel", args), "peak_source": peak_kind,
                     "bytes_per_launch": round(gu_bytes), "us_per_launch": round(gu_ms * 1e3, 3),
                     "other": {"bound": "tensor", "achieved": round(tflops, 1), "unit": "TFLOP/s",
                               "frac": round(tc_frac, 4)}}
