@@ -4,7 +4,7 @@
 // exactly into three bf16 parts, W = hi + mid + lo (hi = bf16(W), mid = bf16(W - hi),
 // lo = bf16(W - hi - mid): 24 significant bits together), so every product of a part
 // with a bf16 x is exact in fp32 and the three MMAs accumulate the fp32 dot product.
-// Tile: M = 128 tokens (A = x rows) x N = 64 experts (B = the three parts' rows), K in
+// Tile: M = 128 tokens (A = x rows) x N = 32 experts (B = the three parts' rows), K in
 // steps of 64; 128 producer threads stage A and B with cp.async into 128-byte-swizzled
 // K-major tiles (4 stages), one thread issues the 12 MMAs of a k-step (4 substeps x 3
 // parts) into one TMEM accumulator, the producers then read it and write l fp32.
@@ -14,7 +14,7 @@
 namespace moe {
 namespace {
 
-constexpr int kRM = 128, kRN = 64, kRK = 64;
+constexpr int kRM = 128, kRN = 32, kRK = 64;     // N = 32: T/128 x E/32 CTAs fill the GPU
 constexpr int kRStages = 4;
 constexpr int kRProducers = 128;
 constexpr int kRThreads = kRProducers + 32;
@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kRThreads, 1) router_tc_kernel(const __grid_co
                 cp_async16(st + swz(r, ch), p.x + (ok ? (int64_t)t * p.H + kb * kRK + ch * 8 : 0), ok ? 16u : 0u);
             }
 #pragma unroll
-            for (int i = 0; i < 3 * kRN / 16; ++i) {               // B: 3 parts x 64 rows x 8 chunks
+            for (int i = 0; i < 3 * kRN / 16; ++i) {               // B: 3 parts x kRN rows x 8 chunks
                 const int rr = (tid >> 3) + 16 * i, part = rr / kRN, r = rr - part * kRN, e = e0 + r;
                 const bool ok = e < p.E;
                 const __nv_bfloat16* src =
