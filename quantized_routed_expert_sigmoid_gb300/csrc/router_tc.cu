@@ -6,8 +6,9 @@
 // with a bf16 x is exact in fp32 and the three MMAs accumulate the fp32 dot product.
 // Tile: M = 128 tokens (A = x rows) x N = 32 experts (B = the three parts' rows), K in
 // steps of 64; 128 producer threads stage A and B with cp.async into 128-byte-swizzled
-// K-major tiles (4 stages), one thread issues the 12 MMAs of a k-step (4 substeps x 3
-// parts) into one TMEM accumulator, the producers then read it and write l fp32.
+// K-major tiles (6 stages, loads three k-steps ahead, so a stage is refilled three steps
+// after the MMAs that read it were issued), one thread issues the 12 MMAs of a k-step (4
+// substeps x 3 parts) into one TMEM accumulator, the producers then read it and write l fp32.
 #include "internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -15,7 +16,7 @@ namespace moe {
 namespace {
 
 constexpr int kRM = 128, kRN = 32, kRK = 64;     // N = 32: T/128 x E/32 CTAs fill the GPU
-constexpr int kRStages = 4;
+constexpr int kRStages = 6;                       // loads go 3 k-steps ahead; 3 steps of slack for the MMAs
 constexpr int kRProducers = 128;
 constexpr int kRThreads = kRProducers + 32;
 constexpr int kRAStage = kRM * 128;               // x tile
@@ -97,8 +98,9 @@ __global__ void __launch_bounds__(kRThreads, 1) router_tc_kernel(const __grid_co
         }
         for (int kb = 0; kb < nk; ++kb) {
             if (kb + 3 < nk) {
-                // stage (kb + 3) % 4 was last read by MMA(kb - 1)
-                if (kb >= 1 && !mbar_wait(&empty[(kb + 3) % kRStages], ((kb - 1) / kRStages) & 1, abort_flag)) break;
+                // stage (kb + 3) % kRStages was last read by MMA(kb + 3 - kRStages)
+                const int prev = kb + 3 - kRStages;
+                if (prev >= 0 && !mbar_wait(&empty[(kb + 3) % kRStages], (prev / kRStages) & 1, abort_flag)) break;
                 issue(kb + 3);
             }
             cp_commit();
