@@ -262,19 +262,24 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_gateup_kernel(const __grid_c
 }
 
 // ============================================================================ down
-// unit = 8 rows n0.. of one expert's down matrix; lane = 4 * row + sub takes, in every item
-// (4 blocks of the 8 rows), the group of `sub` in each block; the 4 lanes of a row then sum.
-template <int NT>
+// Narrow rows (I/64 groups not a multiple of 32, e.g. I = 768): unit = 8 rows n0.. of one
+// expert's down matrix; lane = 4 * row + sub takes, in every item (4 blocks of the 8 rows), the
+// group of `sub` in each block; the 4 lanes of a row then sum.
+// Wide rows (kWide: I/64 a multiple of 32, e.g. I = 2048): the gate/up layout -- unit = 4 rows,
+// item = 8 blocks of the 4 rows, lane = group, so every activation load serves 4 rows.
+template <int NT, bool kWide>
 __global__ void __launch_bounds__(kSThreads, 1) seg_down_kernel(const __grid_constant__ SegParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ SegPlan s_plan;
     __shared__ int s_rows[NT];
     __shared__ __align__(8) uint64_t s_bar[kSWarps][2];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int I = p.K, H = p.rows, GI = qd4_groups(I), upe = H / 8;
-    const int nblk = I / kQ4KWeights, ncd = (nblk + kSDownBlocks - 1) / kSDownBlocks;
+    constexpr int kRowsU = kWide ? 4 : 8;           // rows per unit
+    constexpr int kBlocksI = kWide ? kSChunkBlocks : kSDownBlocks;   // blocks of each row per item
+    const int I = p.K, H = p.rows, GI = qd4_groups(I), upe = H / kRowsU;
+    const int nblk = I / kQ4KWeights, ncd = (nblk + kBlocksI - 1) / kBlocksI;
     const int64_t rbI = (int64_t)nblk * kQ4KBytes;
-    const int rs = ncd == 1 ? (int)rbI : kSDownBlocks * kQ4KBytes;     // row stride in a slot
+    const int rs = !kWide && ncd == 1 ? (int)rbI : kBlocksI * kQ4KBytes;   // row stride in a slot
     uint4* X = reinterpret_cast<uint4*>(smem);
     float4* XS = reinterpret_cast<float4*>(X + (size_t)NT * 16 * GI);
     uint8_t* ring = smem + seg_align((size_t)NT * qd4_vec_bytes(I)) + (size_t)warp * 2 * kSSlotBytes;
@@ -307,17 +312,18 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_down_kernel(const __grid_con
             auto issue = [&](int item) {
                 if (lane != 0 || item >= n_items || !ok) return;
                 const int u = u0 + warp + (item / ncd) * kSWarps, ch = item - (item / ncd) * ncd;
-                const int n0 = 8 * u;
-                const int b0 = ch * kSDownBlocks, nb = min(kSDownBlocks, nblk - b0);
+                const int n0 = kRowsU * u;
+                const int b0 = ch * kBlocksI, nb = min(kBlocksI, nblk - b0);
                 const uint32_t slot = (gi + item) & 1u;
                 uint8_t* dst = ring + slot * kSSlotBytes;
                 uint64_t* bar = &s_bar[warp][slot];
                 const uint32_t bytes = (uint32_t)nb * kQ4KBytes;
-                s_expect(bar, 8 * bytes);
-                if (ncd == 1) {
-                    s_bulk(dst, dbase + (int64_t)n0 * rbI, 8 * bytes, bar);
+                s_expect(bar, kRowsU * bytes);
+                if (!kWide && ncd == 1) {
+                    s_bulk(dst, dbase + (int64_t)n0 * rbI, kRowsU * bytes, bar);
                 } else {
-                    for (int r = 0; r < 8; ++r) s_bulk(dst + r * rs, dbase + (int64_t)(n0 + r) * rbI + (int64_t)b0 * kQ4KBytes, bytes, bar);
+                    for (int r = 0; r < kRowsU; ++r)
+                        s_bulk(dst + r * rs, dbase + (int64_t)(n0 + r) * rbI + (int64_t)b0 * kQ4KBytes, bytes, bar);
                 }
             };
             issue(0);
@@ -337,8 +343,24 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_down_kernel(const __grid_con
 #pragma unroll
                         for (int t = 0; t < NT; ++t) acc[r][t] = 0.f;
                 }
-                const int b0 = ch * kSDownBlocks, nb = min(kSDownBlocks, nblk - b0);
-                if (have) {
+                const int b0 = ch * kBlocksI, nb = min(kBlocksI, nblk - b0);
+                if constexpr (kWide) {
+                    // lane = group ch * 32 + lane of the 4 rows (block lane / 4, quant group lane % 4)
+                    if (have) {
+                        const uint8_t* blk = ring + slot * kSSlotBytes + (lane >> 2) * kQ4KBytes;
+                        const int c = lane & 3;
+                        uint4 hd[4], q0[4], q1[4];
+                        const bool live[4] = {true, true, true, true};
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const uint8_t* rb = blk + r * rs;
+                            hd[r] = *reinterpret_cast<const uint4*>(rb);
+                            q0[r] = *reinterpret_cast<const uint4*>(rb + 16 + 32 * c);
+                            q1[r] = *reinterpret_cast<const uint4*>(rb + 32 + 32 * c);
+                        }
+                        qd4_group_math<NT, 4>(hd, q0, q1, live, 0, ch * 32 + lane, GI, X, XS, nt, acc, nullptr);
+                    }
+                } else if (have) {
                     const uint8_t* rb0 = ring + slot * kSSlotBytes + row * rs;
                     for (int i = 0; i < nb; ++i) {
                         const uint8_t* blk = rb0 + i * kQ4KBytes;
@@ -353,13 +375,20 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_down_kernel(const __grid_con
                 __syncwarp();
                 issue(item + 2);
                 if (ch == ncd - 1) {
-                    const int n = 8 * u + row;
+                    if constexpr (kWide) {
+                        constexpr int sh = qd_red_shift<NT>();
+                        const float v = qd_warp_reduce_t<NT>(acc);
+                        const int i = lane >> sh, r = i / NT, t = i - r * NT;
+                        if ((lane & ((1 << sh) - 1)) == 0 && t < nt) p.out[(int64_t)(st + pb + t) * H + 4 * u + r] = v;
+                    } else {
+                        const int n = 8 * u + row;
 #pragma unroll
-                    for (int t = 0; t < NT; ++t) {
-                        float v = acc[0][t];
-                        v += __shfl_xor_sync(0xffffffffu, v, 1);
-                        v += __shfl_xor_sync(0xffffffffu, v, 2);
-                        if (sub == 0 && t < nt) p.out[(int64_t)(st + pb + t) * H + n] = v;
+                        for (int t = 0; t < NT; ++t) {
+                            float v = acc[0][t];
+                            v += __shfl_xor_sync(0xffffffffu, v, 1);
+                            v += __shfl_xor_sync(0xffffffffu, v, 2);
+                            if (sub == 0 && t < nt) p.out[(int64_t)(st + pb + t) * H + n] = v;
+                        }
                     }
                 }
             }
@@ -397,10 +426,17 @@ cudaError_t seg_launch(bool gateup, const SegParams& p, cudaStream_t s) {
             return err;
         seg_gateup_kernel<NT><<<seg_sms(), kSThreads, smem, s>>>(p);
     } else {
-        if ((err = cudaFuncSetAttribute(seg_down_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-            cudaSuccess)
-            return err;
-        seg_down_kernel<NT><<<seg_sms(), kSThreads, smem, s>>>(p);
+        if (qd4_groups(p.K) % 32 == 0) {
+            if ((err = cudaFuncSetAttribute(seg_down_kernel<NT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)smem)) != cudaSuccess)
+                return err;
+            seg_down_kernel<NT, true><<<seg_sms(), kSThreads, smem, s>>>(p);
+        } else {
+            if ((err = cudaFuncSetAttribute(seg_down_kernel<NT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)smem)) != cudaSuccess)
+                return err;
+            seg_down_kernel<NT, false><<<seg_sms(), kSThreads, smem, s>>>(p);
+        }
     }
     return cudaGetLastError();
 }

@@ -111,8 +111,11 @@ def test_permute_zero_tokens():
     assert np.all(off == 0) and status == 0
 
 
+# the Q4_K cases take the segmented kernels; I = 2048 the down kernel's wide-row layout, with
+# up to 20 tokens per expert (three passes of 8)
 @pytest.mark.parametrize("qt,H,I,E,T,k", [(synth.Q8_0, 256, 128, 8, 6, 2), (synth.Q4_K, 2048, 768, 16, 5, 4),
-                                          (synth.Q4_K, 512, 256, 4, 40, 2), (synth.Q8_0, 1024, 512, 4, 9, 2)])
+                                          (synth.Q4_K, 512, 256, 4, 40, 2), (synth.Q8_0, 1024, 512, 4, 9, 2),
+                                          (synth.Q4_K, 1024, 2048, 4, 30, 2)])
 def test_expert_ffn(qt, H, I, E, T, k):
     shape = synth.LayerShape(H=H, E=E, k=k, I=I, qtype=qt, x_dtype="bf16")
     bank = synth.ExpertBank(shape, 9, 0, exact=None, fill_device="cuda")
