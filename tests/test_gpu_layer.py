@@ -52,6 +52,24 @@ def test_decode_q4_k_ragged_batch():
     _check_layer(tl, 37, tc_min_tokens=1 << 30)
 
 
+def test_segmented_gemv_zipf_T120():
+    # GEMV path just below the tensor-core threshold with Zipf-skewed routing: the popular
+    # experts take many passes of 8 tokens (their work spread over many CTAs by cost), some
+    # experts get no token at all; the whole output is compared with the oracle
+    from helpers import SeededLayer, route_oracle, MIN_GAP
+    shape, seed, T = synth.DECODE, 17, 120
+    Wr = synth.router_weight(shape, seed, 0)
+    L = synth.zipf_target_logits(T, shape.E, shape.k, seed)
+    x = synth.activations_for_logits(L, Wr.numpy(), seed)
+    ids, _, gaps = route_oracle(shape, x.double().numpy(), Wr.numpy(), None)
+    assert gaps[:, 0].min() >= MIN_GAP
+    counts = np.bincount(ids.reshape(-1), minlength=shape.E)
+    assert (counts == 0).sum() >= 8 and counts.max() > 40
+    tl = SeededLayer(shape, seed, x, exact=None, Wr=Wr, bias=None)
+    layer, _, _ = _check_layer(tl, T, tc_min_tokens=1 << 30)
+    assert layer.path(T) == "gemv"
+
+
 def test_deepseek_shape_decode_T2():
     tl = make_layer(synth.DEEPSEEK, 4, 2)
     _check_layer(tl, 2)
