@@ -13,12 +13,14 @@
 //   K1 logits   one CTA per expert row: the T router logits of that expert.
 //   K2 gate/up  every CTA selects the top-k of the T tokens itself (identical
 //               results everywhere; CTA 0 publishes them), then a persistent
-//               grid runs (active expert, row pair) units: each warp streams
-//               its units' rows through a two-slot ring in shared memory (bulk
-//               copies, one mbarrier per slot) and computes
-//               h = silu(gate . x) * (up . x) as they land; the shared
-//               expert's rows follow.  Each CTA also requests its share of the
-//               chosen down rows into L2.
+//               grid runs (active expert, row pair) units in rounds of 16 per
+//               CTA: a round's 32 gate rows and 32 up rows of one expert arrive
+//               as two bulk copies into a two-slot ring in shared memory (one
+//               mbarrier per slot), each warp computes h = silu(gate . x) *
+//               (up . x) of one row pair, and the CTA stages the round's 32
+//               values of h (one sub-block) for K3; the shared expert's rows
+//               follow.  Each CTA also requests its share of the chosen down
+//               rows into L2.
 //   K3 down     one CTA per block of output rows: its down rows of every pair
 //               go to shared memory (one bulk copy per pair) while h is
 //               staged, then the dot products and the gate-weighted combine in
@@ -283,14 +285,14 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
     uint4* X = reinterpret_cast<uint4*>(smem);
     float4* XS = reinterpret_cast<float4*>(X + (size_t)T * 16 * G);
     float4* xs_s = reinterpret_cast<float4*>(smem + p.k2_off_xs_s);
-    uint8_t* ring = smem + p.k2_off_ring + (size_t)warp * 2 * kSlotBytes;
-    __shared__ __align__(8) uint64_t s_bar[kK2MaxWarps][2];
-    if (lane == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar[warp][0])) : "memory");
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar[warp][1])) : "memory");
+    uint8_t* cring = smem + p.k2_off_ring;          // two round slots: [32 gate rows][32 up rows]
+    __shared__ __align__(8) uint64_t c_bar[2];
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&c_bar[0])) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&c_bar[1])) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    __syncwarp();
+    __syncthreads();
     const bool xb = p.x_bf16 != 0;
     // ---- x is the input of the whole chain: stage it before waiting
     qd4_stage_par(p.x, xb, false, H, T, nullptr, H, X, XS, tid, nthr);
@@ -308,40 +310,34 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
     const int nact = R.nact;
     const int64_t rbH = (int64_t)(H / kQ4KWeights) * kQ4KBytes;
     const int half_I = I / 2;
-    const int nch = (G + 31) / 32;
     const int Ur = nact * half_I;
     const int Us = has_shared ? p.I_s / 2 : 0;
     const int W = gridDim.x * (nthr / 32);
     const int wg = blockIdx.x * (nthr / 32) + warp;
     const int my_units = wg < Ur ? (Ur - wg + W - 1) / W : 0;
-    const int n_items = my_units * nch;
 
-    auto unit_rows = [&](int u, const uint8_t* (&rowp)[4]) {
-        const int a = u / half_I, r0 = 2 * (u - a * half_I);
-        const uint8_t* gb = p.wg + (int64_t)R.act_e[a] * p.stride_gu + r0 * rbH;
-        const uint8_t* ub = p.wu + (int64_t)R.act_e[a] * p.stride_gu + r0 * rbH;
-        rowp[0] = gb; rowp[1] = ub; rowp[2] = gb + rbH; rowp[3] = ub + rbH;
-    };
-    const int nblk = H / kQ4KWeights;
-    // lane 0 puts item `item` (its 4 rows' blocks [8*ch, 8*ch + 8)) into slot item & 1
-    auto issue = [&](int item) {
-        if (lane != 0 || item >= n_items) return;
-        const int u = wg + (item / nch) * W, ch = item - (item / nch) * nch;
-        const int b0 = ch * kChunkBlocks, nb = min(kChunkBlocks, nblk - b0);
-        const uint32_t bytes = (uint32_t)nb * kQ4KBytes;
-        const uint8_t* rowp[4];
-        unit_rows(u, rowp);
-        uint8_t* dst = ring + (item & 1) * kSlotBytes;
-        uint64_t* bar = &s_bar[warp][item & 1];
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(4 * bytes)
+    // ---- routed units, one round per 16: round r of this CTA covers the units wg0 + r W ..
+    // + 15 (wg0 = 16 * blockIdx.x), i.e. 32 consecutive rows of gate and of up of one expert
+    // (half_I is a multiple of 16) -- one staged sub-block of h.  A round arrives as two bulk
+    // copies (the 32 gate rows, the 32 up rows; rows are whole, H <= 2048) into slot r % 2;
+    // warp w computes the row pair of unit wg0 + r W + w.
+    const int n_rounds = my_units;                 // the same for every warp of the CTA
+    const uint32_t rows_bytes = (uint32_t)(32 * rbH);
+    auto issue_round = [&](int r) {
+        if (tid != 0 || r >= n_rounds) return;
+        const int u0 = blockIdx.x * (nthr / 32) + r * W;
+        const int a = u0 / half_I, row0 = 2 * (u0 - a * half_I);
+        const int64_t off = (int64_t)R.act_e[a] * p.stride_gu + row0 * rbH;
+        uint8_t* dst = cring + (r & 1) * 2 * rows_bytes;
+        uint64_t* bar = &c_bar[r & 1];
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(2 * rows_bytes)
                      : "memory");
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-            bulk_to_smem(dst + r * kChunkBlocks * kQ4KBytes, rowp[r] + (int64_t)b0 * kQ4KBytes, bytes, bar);
+        bulk_to_smem(dst, p.wg + off, rows_bytes, bar);
+        bulk_to_smem(dst + rows_bytes, p.wu + off, rows_bytes, bar);
     };
-    // this warp's first two items go out before anything else
-    issue(0);
-    issue(1);
+    // the CTA's first two rounds go out before anything else
+    issue_round(0);
+    issue_round(1);
     // ---- this CTA's share of the chosen down rows (and the shared expert's) into L2
     {
         const int rows0 = (int)((int64_t)blockIdx.x * H / gridDim.x), rows1 = (int)((int64_t)(blockIdx.x + 1) * H / gridDim.x);
@@ -368,80 +364,68 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
             p.offsets[e] = cnt;
         }
     }
-    // ---- routed units through the ring.  The 16 warps of a CTA take 16 consecutive row pairs
-    // of one expert in each round: 32 rows of h, one staged sub-block, which the CTA stages
-    // itself (the values meet in shared memory) and writes out for the down kernel.  Every
-    // warp runs the same rounds, so the barrier below is reached uniformly, also after a
-    // copy that timed out (the warp then stops computing and issuing, not looping).
+    // ---- the rounds.  Every warp runs all of them, so the barrier below is reached uniformly,
+    // also after a copy that timed out (the CTA then stops computing and issuing, not looping).
     __shared__ float s_hq[2][kCMaxT][32];
     const int vb = 272 * qd4_groups(I);            // bytes of one staged vector of h
     float acc[4][NT];
-    int n = 0, st = 0;
     int vidx[NT];
     bool ok = true;
-    int round = 0, waited = 0, issued = min(2, n_items);
-    for (int item = 0; item < n_items; ++item) {
-        const bool have = ok && mbar_wait(&s_bar[warp][item & 1], (uint32_t)(item >> 1) & 1u);
+    int waited = 0, issued = min(2, n_rounds);
+    for (int r = 0; r < n_rounds; ++r) {
+        const bool have = ok && mbar_wait(&c_bar[r & 1], (uint32_t)(r >> 1) & 1u);
         if (ok && !have) {
             ok = false;
-            if (lane == 0) atomicExch(&p.hdr->status, (int)MOE_ERR_TIMEOUT);
+            if (tid == 0) atomicExch(&p.hdr->status, (int)MOE_ERR_TIMEOUT);
         }
-        if (have) waited = item + 1;
-        const int u = wg + (item / nch) * W, ch = item - (item / nch) * nch;
-        if (ch == 0) {
+        if (have) waited = r + 1;
+        const int u = wg + r * W;
+        const int a = u / half_I, r0 = 2 * (u - a * half_I);
+        const int st = R.act_start[a], n = R.act_n[a];
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
+        for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int t = 0; t < NT; ++t) acc[r][t] = 0.f;
-            const int a = u / half_I;
-            st = R.act_start[a];
-            n = R.act_n[a];
+            for (int t = 0; t < NT; ++t) acc[q][t] = 0.f;
 #pragma unroll
-            for (int t = 0; t < NT; ++t) vidx[t] = R.tok[st + min(t, n - 1)];
-        }
-        const int g = ch * 32 + lane;
-        if (have && g < G) {
-            const uint8_t* blk = ring + (item & 1) * kSlotBytes + (lane >> 2) * kQ4KBytes;
+        for (int t = 0; t < NT; ++t) vidx[t] = R.tok[st + min(t, n - 1)];
+        if (have && lane < G) {
+            // rows 0, 1 = gate, up of row r0; rows 2, 3 = gate, up of row r0 + 1 (slot rows 2w, 2w + 1)
+            const uint8_t* base = cring + (r & 1) * 2 * rows_bytes + (lane >> 2) * kQ4KBytes;
+            const uint8_t* rb[4] = {base + (2 * warp) * rbH, base + rows_bytes + (2 * warp) * rbH,
+                                    base + (2 * warp + 1) * rbH, base + rows_bytes + (2 * warp + 1) * rbH};
             const int c = lane & 3;
             uint4 hd[4], q0[4], q1[4];
             const bool live[4] = {true, true, true, true};
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const uint8_t* rb = blk + r * kChunkBlocks * kQ4KBytes;
-                hd[r] = *reinterpret_cast<const uint4*>(rb);
-                q0[r] = *reinterpret_cast<const uint4*>(rb + 16 + 32 * c);
-                q1[r] = *reinterpret_cast<const uint4*>(rb + 32 + 32 * c);
+            for (int q = 0; q < 4; ++q) {
+                hd[q] = *reinterpret_cast<const uint4*>(rb[q]);
+                q0[q] = *reinterpret_cast<const uint4*>(rb[q] + 16 + 32 * c);
+                q1[q] = *reinterpret_cast<const uint4*>(rb[q] + 32 + 32 * c);
             }
-            qd4_group_math<NT, 4>(hd, q0, q1, live, 0, g, G, X, XS, n, acc, vidx);
+            qd4_group_math<NT, 4>(hd, q0, q1, live, 0, lane, G, X, XS, n, acc, vidx);
         }
-        __syncwarp();                              // every lane is done with the slot
-        if (ok && item + 2 < n_items) {
-            issue(item + 2);
-            issued = item + 3;
+        constexpr int sh = qd_red_shift<NT>();
+        const float gv = qd_warp_reduce_t<NT>(acc);
+        const float uv = __shfl_xor_sync(0xffffffffu, gv, NT << sh);
+        {
+            const int i = lane >> sh, q = i / NT, t = i - q * NT;
+            if ((q & 1) == 0 && (lane & ((1 << sh) - 1)) == 0 && t < n)
+                s_hq[r & 1][t][(r0 & 31) + (q >> 1)] = silu_mul(gv, uv);
         }
-        if (ch == nch - 1) {
-            // rows 0, 1 = gate, up of row r0; rows 2, 3 = gate, up of row r0 + 1
-            constexpr int sh = qd_red_shift<NT>();
-            const float gv = qd_warp_reduce_t<NT>(acc);
-            const float uv = __shfl_xor_sync(0xffffffffu, gv, NT << sh);
-            const int a = u / half_I, r0 = 2 * (u - a * half_I);
-            {
-                const int i = lane >> sh, r = i / NT, t = i - r * NT;
-                if ((r & 1) == 0 && (lane & ((1 << sh) - 1)) == 0 && t < n)
-                    s_hq[round & 1][t][(r0 & 31) + (r >> 1)] = silu_mul(gv, uv);
-            }
-            __syncthreads();
-            if (warp < n)
-                warp_stage_subblock(s_hq[round & 1][warp][lane], p.hq + (size_t)(st + warp) * vb, qd4_groups(I), r0 >> 5,
-                                    lane);
-            ++round;
+        __syncthreads();                           // slot r % 2 read by every warp; s_hq complete
+        if (ok && r + 2 < n_rounds) {
+            issue_round(r + 2);
+            issued = r + 3;
         }
+        if (warp < n)
+            warp_stage_subblock(s_hq[r & 1][warp][lane], p.hq + (size_t)(st + warp) * vb, qd4_groups(I), r0 >> 5, lane);
     }
-    if (!ok && lane == 0) {
+    if (!ok && tid == 0) {
         // let no copy land after the CTA exits: wait (bounded) for the ones still in flight
-        for (int i = waited; i < issued; ++i) mbar_wait(&s_bar[warp][i & 1], (uint32_t)(i >> 1) & 1u);
+        for (int i = waited; i < issued; ++i) mbar_wait(&c_bar[i & 1], (uint32_t)(i >> 1) & 1u);
     }
-    __syncwarp();
+    __syncthreads();
+    int round = n_rounds;                          // the shared expert's sub-blocks continue the s_hq parity
     // ---- the shared expert's row pairs (direct loads)
     if constexpr (has_shared) {
     for (int u = wg + my_units * W; u < Ur + Us; u += W) {
@@ -751,6 +735,9 @@ bool decode_chain_supported(const DecodeArgs& a) {
     if (a.T < 1 || a.T > kCMaxT || P > kCMaxP || a.route.n_experts > kCMaxE) return false;
     if (a.qtype != MOE_Q4_K) return false;
     if (a.H % kQ4KWeights || a.I % kQ4KWeights || a.H / 4 > kK1MaxVec * kK1Threads) return false;
+    // a round of the gate/up kernel copies 32 whole rows of gate and of up: rows of at most
+    // kChunkBlocks super-blocks (the ring's slot size), I/2 a multiple of 16
+    if (a.H > kChunkBlocks * kQ4KWeights || (a.I / 2) % kK2MaxWarps) return false;
     if (a.I_s > 0) {
         if (a.s_qtype == MOE_Q8_0) {
             if (a.I_s % kQ80Weights || a.H % kQ80Weights || a.I_s % 2) return false;
