@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_gateup_kernel(const __grid_c
     const int H = p.K, I = p.rows, G = qd4_groups(H), half_I = I / 2;
     const int nblk = H / kQ4KWeights, nch = (G + 31) / 32;
     const int64_t rbH = (int64_t)nblk * kQ4KBytes;
+    const int rs = nch == 1 ? (int)rbH : kSChunkBlocks * kQ4KBytes;     // row stride in a slot
     uint4* X = reinterpret_cast<uint4*>(smem);
     float4* XS = reinterpret_cast<float4*>(X + (size_t)NT * 16 * G);
     uint8_t* ring = smem + seg_align((size_t)NT * qd4_vec_bytes(H)) + (size_t)warp * 2 * kSSlotBytes;
@@ -202,10 +203,17 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_gateup_kernel(const __grid_c
                 uint8_t* dst = ring + slot * kSSlotBytes;
                 uint64_t* bar = &s_bar[warp][slot];
                 s_expect(bar, 4 * bytes);
-                const uint8_t* rp[4] = {gbase + r0 * rbH, ubase + r0 * rbH, gbase + (r0 + 1) * rbH, ubase + (r0 + 1) * rbH};
+                if (nch == 1) {
+                    // whole rows: gate rows r0, r0 + 1 and up rows r0, r0 + 1 are two contiguous runs;
+                    // slot rows (gate r0, gate r0 + 1, up r0, up r0 + 1) at rs apart
+                    s_bulk(dst, gbase + r0 * rbH, 2 * bytes, bar);
+                    s_bulk(dst + 2 * rs, ubase + r0 * rbH, 2 * bytes, bar);
+                } else {
+                    const uint8_t* rp[4] = {gbase + r0 * rbH, gbase + (r0 + 1) * rbH, ubase + r0 * rbH,
+                                            ubase + (r0 + 1) * rbH};
 #pragma unroll
-                for (int r = 0; r < 4; ++r)
-                    s_bulk(dst + r * kSChunkBlocks * kQ4KBytes, rp[r] + (int64_t)b0 * kQ4KBytes, bytes, bar);
+                    for (int r = 0; r < 4; ++r) s_bulk(dst + r * rs, rp[r] + (int64_t)b0 * kQ4KBytes, bytes, bar);
+                }
             };
             issue(0);
             issue(1);
@@ -230,9 +238,11 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_gateup_kernel(const __grid_c
                     const int c = lane & 3;
                     uint4 hd[4], q0[4], q1[4];
                     const bool live[4] = {true, true, true, true};
+                    // acc rows 0..3 = gate r0, up r0, gate r0 + 1, up r0 + 1 = slot rows 0, 2, 1, 3
+                    constexpr int kSlotRow[4] = {0, 2, 1, 3};
 #pragma unroll
                     for (int r = 0; r < 4; ++r) {
-                        const uint8_t* rb = blk + r * kSChunkBlocks * kQ4KBytes;
+                        const uint8_t* rb = blk + kSlotRow[r] * rs;
                         hd[r] = *reinterpret_cast<const uint4*>(rb);
                         q0[r] = *reinterpret_cast<const uint4*>(rb + 16 + 32 * c);
                         q1[r] = *reinterpret_cast<const uint4*>(rb + 32 + 32 * c);
@@ -279,7 +289,7 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_down_kernel(const __grid_con
     const int I = p.K, H = p.rows, GI = qd4_groups(I), upe = H / kRowsU;
     const int nblk = I / kQ4KWeights, ncd = (nblk + kBlocksI - 1) / kBlocksI;
     const int64_t rbI = (int64_t)nblk * kQ4KBytes;
-    const int rs = !kWide && ncd == 1 ? (int)rbI : kBlocksI * kQ4KBytes;   // row stride in a slot
+    const int rs = ncd == 1 ? (int)rbI : kBlocksI * kQ4KBytes;     // row stride in a slot
     uint4* X = reinterpret_cast<uint4*>(smem);
     float4* XS = reinterpret_cast<float4*>(X + (size_t)NT * 16 * GI);
     uint8_t* ring = smem + seg_align((size_t)NT * qd4_vec_bytes(I)) + (size_t)warp * 2 * kSSlotBytes;
@@ -319,7 +329,7 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_down_kernel(const __grid_con
                 uint64_t* bar = &s_bar[warp][slot];
                 const uint32_t bytes = (uint32_t)nb * kQ4KBytes;
                 s_expect(bar, kRowsU * bytes);
-                if (!kWide && ncd == 1) {
+                if (ncd == 1) {                            // whole rows: one contiguous run
                     s_bulk(dst, dbase + (int64_t)n0 * rbI, kRowsU * bytes, bar);
                 } else {
                     for (int r = 0; r < kRowsU; ++r)
