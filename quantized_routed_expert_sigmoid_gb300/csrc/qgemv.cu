@@ -1,4 +1,6 @@
-// qgemv.cu -- fused dequant-GEMV for the experts at decode sizes.
+// qgemv.cu -- fused dequant-GEMV for the experts at decode sizes where the segmented
+// kernels of gemv_seg.cu do not apply (Q8_0 weights, such as a Q8_0 shared expert, or more
+// than 256 experts).
 //
 // The pages run the card experts on the stored GGUF quantization ("bloomery
 // README 0.3.1", Status table, "Quant types" row; "Why it is fast": kernels
