@@ -83,9 +83,9 @@ def profiled_traffic(kernel, args):
     (profiles/traffic.json), or None when there is none or the kernel's sources changed
     since the counters were taken."""
     try:
+        key = f"{kernel} {args.workload}" + (f" T={args.tokens}" if args.tokens else "")
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            key = f"{kernel} {args.workload}" + (f" T={args.tokens}" if args.tokens else "")
-        entry = json.load(f).get(key)
+            entry = json.load(f).get(key)
         if entry and sources_digest(entry["sources"]) == entry["sources_sha1"]:
             return entry["dram_bytes_per_launch"]
     except (OSError, ValueError, KeyError):
