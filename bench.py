@@ -195,13 +195,13 @@ def algorithmic_bytes(shape, T, offsets_host):
 def launches_per_layer(shape, T, stack=False, path=None):
     P = T * shape.k
     if path == "decode_chain":
-        return 3 + (1 if stack else 0)                # logits, routing + gate/up, down + combine (+ RMSNorm)
+        return 3                                     # logits (+ RMSNorm), routing + gate/up, down + combine
     n = 2 + (1 if P <= 1024 else 2) + 2 + 1          # logits, top-k, permute, gate/up, down, combine
     if T >= 128:
         n += 2                                       # fp16 copy of x, token-block list
     if shape.I_s > 0:
         n += 2
-    return n + (1 if stack else 0)                   # RMSNorm in the stack
+    return n + (1 if stack else 0)                   # the layer's own RMSNorm launch in the stack
 
 
 # ------------------------------------------------------------------ our arm
@@ -225,19 +225,24 @@ def run_ours(args, rank, world):
     for lay in layers:
         lay.ensure_workspace(T, device)
     if stack:
-        import quantized_routed_expert_sigmoid_gb300 as moe_mod
-        for lay in layers:              # the stack adds each layer into the residual stream
-            lay.desc.accumulate = 1
-            lay.rebuild_plan()
+        import quantized_routed_expert_sigmoid_gb300._native as N
         gammas = [synth.gamma(shape.H, seed, l).to(device) for l in range(L)]
+        for lay, gm in zip(layers, gammas):
+            # one call per layer is a residual block: resid += layer(bf16(RMSNorm(resid) * gamma))
+            lay.desc.accumulate = 1
+            lay.desc.x_type = N.MOE_F32
+            lay.desc.norm_gamma = gm.data_ptr()
+            lay.desc.norm_eps = 1e-6
+            lay._keep.append(gm)
+            lay.rebuild_plan()
+            lay.ensure_workspace(T, device)
         resid = x.float().clone()
         u = torch.empty(T, shape.H, dtype=torch.bfloat16, device=device)
 
     def chain(stream=None):
         if stack:
-            for lay, gm in zip(layers, gammas):
-                moe.moe_rmsnorm_bf16(resid, gm, T, shape.H, 1e-6, u, stream)
-                lay(u, out=resid, stream=stream)
+            for lay in layers:
+                lay(resid, out=resid, stream=stream)
             return
         for lay, o in zip(layers, outs):
             lay(x, out=o, stream=stream)
@@ -292,7 +297,13 @@ def run_ours(args, rank, world):
     chain_path = path == "decode_chain"
     gu_ms = None
     if stack:
-        x = u                           # the kernels' input in the stack: the bf16 normalised stream
+        # the gate/up kernel's input: the residual stream for the chain (which normalizes it
+        # itself), the bf16 normalized stream for the other paths
+        if chain_path or tc_path:
+            x = resid.clone()
+        else:
+            moe.moe_rmsnorm_bf16(resid, gammas[0], T, shape.H, 1e-6, u)
+            x = u
     try:
         if tc_path or chain_path:
             gu_ms = time_gateup_events(moe, layers, x, outs, T, args)
@@ -312,9 +323,8 @@ def run_ours(args, rank, world):
         x_dev.copy_(x_host, non_blocking=True)
         if stack:
             resid.copy_(x_dev)
-            for lay, gm in zip(layers, gammas):
-                moe.moe_rmsnorm_bf16(resid, gm, T, shape.H, 1e-6, u)
-                lay(u, out=resid)
+            for lay in layers:
+                lay(resid, out=resid)
             out_stack[0].copy_(resid)
         else:
             for i, lay in enumerate(layers):
@@ -424,12 +434,14 @@ def time_gateup(moe, layers, x, shape, T, device, args):
     """Average duration of the gate/up kernel: one graph of L launches, replayed."""
     k, E, H, I = shape.k, shape.E, shape.H, shape.I
     P = T * k
+    import quantized_routed_expert_sigmoid_gb300._native as N
+    xt = N.MOE_BF16 if x.dtype == torch.bfloat16 else N.MOE_F32   # the kernels read x as it is
     routed = []
     for lay in layers:
         ids = torch.empty(T, k, dtype=torch.int32, device=device)
         w = torch.empty(T, k, device=device)
         lg = torch.empty(T, E, device=device)
-        moe.moe_route(lay.desc.route, x, lay.desc.x_type, T, H, lay.desc.W_router, lay.desc.bias, None, lg, ids, w)
+        moe.moe_route(lay.desc.route, x, xt, T, H, lay.desc.W_router, lay.desc.bias, None, lg, ids, w)
         sp = torch.empty(P, dtype=torch.int32, device=device)
         pp = torch.empty(P, dtype=torch.int32, device=device)
         off = torch.empty(E + 1, dtype=torch.int32, device=device)
@@ -442,7 +454,7 @@ def time_gateup(moe, layers, x, shape, T, device, args):
 
     def run(stream=None):
         for lay, sp, off, h in routed:
-            moe.moe_expert_gateup(lay.desc.gate, lay.desc.up, E, x, lay.desc.x_type, T, H, I, sp, off, k, h,
+            moe.moe_expert_gateup(lay.desc.gate, lay.desc.up, E, x, xt, T, H, I, sp, off, k, h,
                                   stream)
 
     s = torch.cuda.Stream(device=device)

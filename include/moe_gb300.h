@@ -205,6 +205,13 @@ typedef struct {
     int accumulate;               /* 1: out += layer(x) (a residual add); 0: out = layer(x) */
     int tc_min_tokens;            /* T at or above this uses the tensor-core path (0 = default 128) */
     int decode_chain_off;         /* 1: never use the chained decode kernels (T <= 4) */
+    /* Pre-norm (nullable): x is the fp32 residual stream [T][H] (x_type MOE_F32) and the layer's
+     * input is u = bf16(x / sqrt(mean_h x^2 + norm_eps) * norm_gamma), exactly as moe_rmsnorm_bf16
+     * computes it; the chained decode kernels compute u themselves (no extra launch), the other
+     * paths run moe_rmsnorm_bf16 into the workspace first.  With accumulate = 1 and out == x one
+     * call is a whole residual block, out += layer(norm(out)).  norm_gamma: (device) fp32 [H]. */
+    const float* norm_gamma;
+    float norm_eps;
 } moe_layer_desc;
 
 typedef struct moe_layer_plan moe_layer_plan;

@@ -48,7 +48,7 @@ class moe_layer_desc(ctypes.Structure):
                 ("gate", moe_qmat), ("up", moe_qmat), ("down", moe_qmat),
                 ("shared_intermediate", ctypes.c_int), ("s_gate", moe_qmat), ("s_up", moe_qmat),
                 ("s_down", moe_qmat), ("accumulate", ctypes.c_int), ("tc_min_tokens", ctypes.c_int),
-                ("decode_chain_off", ctypes.c_int)]
+                ("decode_chain_off", ctypes.c_int), ("norm_gamma", ctypes.c_void_p), ("norm_eps", ctypes.c_float)]
 
 
 _lock = threading.Lock()

@@ -96,9 +96,15 @@ namespace {
 // Workspace of moe_layer for T tokens (offsets in bytes, all 256-aligned).
 struct LayerWs {
     bool tc;                      // tensor-core path for this T
-    size_t hdr, logits, ids, w, sorted, pair_pos, offsets, chunk, h, y, sh_h, sh_y, x16, tiles, wsplit, hq, hq_s, total;
+    size_t hdr, logits, ids, w, sorted, pair_pos, offsets, chunk, h, y, sh_h, sh_y, x16, tiles, wsplit, hq, hq_s, u,
+        total;
     bool router_tc;               // router logits on the tensor cores
+    bool chain;                   // the chained decode kernels
+    bool norm_in_chain;           // pre-norm computed by the chain itself (else moe_rmsnorm_bf16 into u)
 };
+
+// The layer's input dtype once a pre-norm has run (its output u is bf16).
+bool input_bf16(const moe_layer_desc& d) { return d.x_type == MOE_BF16 || d.norm_gamma != nullptr; }
 
 bool use_tc(const moe_layer_desc& d, int T) {
     if (T < d.tc_min_tokens) return false;
@@ -169,9 +175,13 @@ LayerWs layer_ws(const moe_layer_desc& d, int T) {
     w.tiles = take(w.tc ? tc_tile_list_bytes(T, k, E) : 0);
     // tensor-core router logits only on the tensor-core path: their fp32 accumulation inside the
     // MMA is within that path's tolerance, not within the GEMV path's
-    w.router_tc = w.tc && router_tc_supported(T, H, E, d.x_type == MOE_BF16);
+    w.router_tc = w.tc && router_tc_supported(T, H, E, input_bf16(d));
     w.wsplit = take(w.router_tc ? router_tc_split_bytes(H, E) : 0);
     const bool chain = decode_chain_applies(d, T);
+    w.chain = chain;
+    // the chain normalizes its own input unless its shared expert is Q8_0 (staged from x apart)
+    w.norm_in_chain = chain && d.norm_gamma && !(Is > 0 && d.s_gate.qtype == MOE_Q8_0);
+    w.u = take(d.norm_gamma && !w.norm_in_chain ? (size_t)T * H * 2 : 0);
     w.hq = take(chain ? P * (size_t)(I / 64) * 272 : 0);
     w.hq_s = take(chain && Is > 0 ? (size_t)T * (Is / 64) * 272 : 0);
     w.total = o;
@@ -436,6 +446,12 @@ moe_status moe_layer_plan_create(const moe_layer_desc* desc, moe_layer_plan** pl
     if (d.gate.qtype != d.up.qtype || d.gate.expert_stride_bytes != d.up.expert_stride_bytes)
         return fail(MOE_ERR_INVALID_ARG, "gate and up must share qtype and expert stride");
     if (d.shared_intermediate < 0) return fail(MOE_ERR_INVALID_ARG, "shared_intermediate < 0");
+    if (d.norm_gamma) {
+        if (d.x_type != MOE_F32) return fail(MOE_ERR_INVALID_ARG, "a pre-norm needs the fp32 residual stream as x");
+        if (!aligned(d.norm_gamma, 16)) return fail(MOE_ERR_INVALID_ARG, "norm_gamma not 16-byte aligned");
+        if (H % 4) return fail(MOE_ERR_INVALID_ARG, "a pre-norm needs H %% 4 == 0");
+        if (!(d.norm_eps >= 0.f)) return fail(MOE_ERR_INVALID_ARG, "norm_eps < 0");
+    }
     if (d.shared_intermediate > 0) {
         const int Is = d.shared_intermediate;
         if ((st = check_qmat(&d.s_gate, "s_gate", Is, H, 1)) || (st = check_qmat(&d.s_up, "s_up", Is, H, 1)) ||
@@ -494,7 +510,15 @@ moe_status moe_layer_timed(const moe_layer_plan* plan, const void* x, int T, flo
     if (!aligned(workspace, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace not 256-byte aligned");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int E = d.route.n_experts, k = d.route.top_k, H = d.hidden, I = d.intermediate;
-    const bool xb = d.x_type == MOE_BF16;
+    const void* x_res = x;                         // the call's x (the residual stream with a pre-norm)
+    if (d.norm_gamma && !w.norm_in_chain) {
+        // pre-norm as its own launch: the layer then reads u
+        void* u = at<void>(workspace, w.u);
+        cudaError_t e0 = launch_rmsnorm_bf16(static_cast<const float*>(x), d.norm_gamma, T, H, d.norm_eps, u, s);
+        if (e0 != cudaSuccess) return cuda_fail(e0, "rmsnorm kernel");
+        x = u;
+    }
+    const bool xb = input_bf16(d);
     WsHeader* hdr = at<WsHeader>(workspace, w.hdr);
     float* logits = at<float>(workspace, w.logits);
     int32_t* ids = at<int32_t>(workspace, w.ids);
@@ -503,10 +527,12 @@ moe_status moe_layer_timed(const moe_layer_plan* plan, const void* x, int T, flo
     int32_t* ppos = at<int32_t>(workspace, w.pair_pos);
     int32_t* offs = at<int32_t>(workspace, w.offsets);
     cudaError_t err;
-    if (!w.tc && decode_chain_applies(d, T)) {
+    if (!w.tc && w.chain) {
         DecodeArgs da = decode_shape_args(d, T);
-        da.x = x;
-        da.x_bf16 = xb;
+        da.x = w.norm_in_chain ? x_res : x;
+        da.x_bf16 = w.norm_in_chain ? false : xb;
+        da.norm_gamma = w.norm_in_chain ? d.norm_gamma : nullptr;
+        da.norm_eps = d.norm_eps;
         da.logits = logits; da.ids = ids; da.gw = gw; da.sorted = sorted; da.offsets = offs; da.pair_pos = ppos;
         da.h = at<float>(workspace, w.h);
         da.h_s = at<float>(workspace, w.sh_h);

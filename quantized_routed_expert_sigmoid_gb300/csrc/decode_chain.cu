@@ -54,6 +54,8 @@ struct ChainParams {
     const float* bias;
     const void* x;
     int x_bf16;
+    const float* gamma;                     // pre-norm: x is the fp32 residual stream, the layer input
+    float eps;                              // is bf16(RMSNorm(x) * gamma) (K1 and K2 compute it)
     int T, H, I;
     const uint8_t* wg;
     const uint8_t* wu;
@@ -224,17 +226,22 @@ __global__ void __launch_bounds__(kK1Threads) chain_logits_kernel(const __grid_c
     const int n4 = H / 4;
     // the router row: a weight, independent of the launches before this one
     // (volatile loads: issued here, ahead of the wait, not moved past it)
-    float4 w[kK1MaxVec];
+    float4 w[kK1MaxVec], gm[kK1MaxVec];
 #pragma unroll
     for (int i = 0; i < kK1MaxVec; ++i) {
         const int j = tid + i * kK1Threads;
         w[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        gm[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (j < n4) w[i] = ld_nc_v4(reinterpret_cast<const float4*>(p.Wr + (int64_t)e * H) + j);
+        if (p.gamma && j < n4) gm[i] = ld_nc_v4(reinterpret_cast<const float4*>(p.gamma) + j);
     }
     pdl_wait();                                   // x and the workspace belong to the launches before
     pdl_launch_dependents();
     if (e == 0 && tid == 0) p.hdr->status = MOE_OK;
     const bool xb = p.x_bf16 != 0;
+    // pre-norm: the tokens' RMSNorm scales, by all warps
+    __shared__ float s_r[kCMaxT], s_rpart[kCMaxT][8];
+    if (p.gamma) rms_scales_cta(reinterpret_cast<const float*>(p.x), T, H, p.eps, s_rpart, s_r);
     float acc[kCMaxT];
 #pragma unroll
     for (int t = 0; t < kCMaxT; ++t) acc[t] = 0.f;
@@ -245,7 +252,8 @@ __global__ void __launch_bounds__(kK1Threads) chain_logits_kernel(const __grid_c
 #pragma unroll
             for (int t = 0; t < kCMaxT; ++t) {
                 if (t < T) {
-                    const float4 xv = qd_load_vec4(p.x, xb, (int64_t)t * H + 4 * j);
+                    float4 xv = qd_load_vec4(p.x, xb, (int64_t)t * H + 4 * j);
+                    if (p.gamma) xv = rms_apply4(xv, s_r[t], gm[i]);
                     acc[t] = fmaf(w[i].x, xv.x, acc[t]);
                     acc[t] = fmaf(w[i].y, xv.y, acc[t]);
                     acc[t] = fmaf(w[i].z, xv.z, acc[t]);
@@ -294,8 +302,11 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
     }
     __syncthreads();
     const bool xb = p.x_bf16 != 0;
-    // ---- x is the input of the whole chain: stage it before waiting
-    qd4_stage_par(p.x, xb, false, H, T, nullptr, H, X, XS, tid, nthr);
+    // ---- x is the input of the whole chain: stage it before waiting (with a pre-norm, x is the
+    // residual stream that the layer before finished writing before K1 let this kernel start)
+    __shared__ float s_r[kCMaxT], s_rpart[kCMaxT][8];
+    if (p.gamma) rms_scales_cta(reinterpret_cast<const float*>(p.x), T, H, p.eps, s_rpart, s_r);
+    qd4_stage_par(p.x, xb, false, H, T, nullptr, H, X, XS, tid, nthr, p.gamma, s_r);
     if (kSh == 2) {
         const int slots = p.it_H_s * 256;
         for (int t = 0; t < T; ++t) {
@@ -711,6 +722,7 @@ ChainParams chain_params(const DecodeArgs& a, const ChainLayout& L) {
     p.rc.renorm = a.route.renormalize;
     p.rc.scale = a.route.routed_scale;
     p.Wr = a.Wr; p.bias = a.bias; p.x = a.x; p.x_bf16 = a.x_bf16 ? 1 : 0;
+    p.gamma = a.norm_gamma; p.eps = a.norm_eps;
     p.T = a.T; p.H = a.H; p.I = a.I;
     p.wg = a.wg; p.wu = a.wu; p.wd = a.wd;
     p.stride_gu = a.stride_gu; p.stride_d = a.stride_d;

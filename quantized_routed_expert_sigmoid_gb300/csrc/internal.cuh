@@ -99,6 +99,8 @@ struct DecodeArgs {
     const float* bias;
     const void* x;
     bool x_bf16;
+    const float* norm_gamma;      // pre-norm inside the chain (x fp32 residual stream), or NULL
+    float norm_eps;
     int T, H, I;
     int qtype;
     const uint8_t* wg;

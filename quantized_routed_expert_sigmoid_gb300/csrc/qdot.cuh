@@ -470,12 +470,71 @@ __device__ __forceinline__ void qd4_stage(const void* src, bool bf16, bool coher
     }
 }
 
+// RMSNorm of one fp32 row, r = 1 / sqrt(mean(x^2) + eps), in the summation order of
+// moe_rmsnorm_bf16's kernel: its thread i (of 256) accumulates x[4i + 1024 j .. + 3] with fmaf,
+// each of its 8 warps reduces its 32 partial sums by a xor butterfly, and the 8 warp sums are
+// added in order.  rms_vwarp_sum is that kernel's warp vw (lanes playing threads 32 vw ..
+// 32 vw + 31; every lane gets the sum); rms_scale adds the 8 sums in order.  H <= 2048, so a
+// lane's two loads are issued before any arithmetic.  A layer that normalizes its own input
+// thus gives the bits of the separate kernel.
+__device__ __forceinline__ float rms_vwarp_sum(const float* row, int H, int vw) {
+    const int lane = threadIdx.x & 31;
+    const int h0 = (vw * 32 + lane) * 4;
+    const float4 a = h0 < H ? __ldcg(reinterpret_cast<const float4*>(row + h0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 b = h0 + 1024 < H ? __ldcg(reinterpret_cast<const float4*>(row + h0 + 1024))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    float ss = 0.f;
+    if (h0 < H) {
+        ss = fmaf(a.x, a.x, ss);
+        ss = fmaf(a.y, a.y, ss);
+        ss = fmaf(a.z, a.z, ss);
+        ss = fmaf(a.w, a.w, ss);
+    }
+    if (h0 + 1024 < H) {
+        ss = fmaf(b.x, b.x, ss);
+        ss = fmaf(b.y, b.y, ss);
+        ss = fmaf(b.z, b.z, ss);
+        ss = fmaf(b.w, b.w, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    return ss;
+}
+__device__ __forceinline__ float rms_scale(const float* part8, int H, float eps) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) s += part8[w];
+    return 1.0f / sqrtf(s / (float)H + eps);
+}
+// The scales of T rows of x (stride H) into s_r[t], by all warps of the CTA (part: [T][8]
+// shared scratch).  Every thread of the CTA must call it.
+__device__ __forceinline__ void rms_scales_cta(const float* x, int T, int H, float eps, float (*part)[8],
+                                               float* s_r) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int it = warp; it < T * 8; it += nw) {
+        const float v = rms_vwarp_sum(x + (int64_t)(it >> 3) * H, H, it & 7);
+        if (lane == 0) part[it >> 3][it & 7] = v;
+    }
+    __syncthreads();
+    if ((int)threadIdx.x < T) s_r[threadIdx.x] = rms_scale(part[threadIdx.x], H, eps);
+    __syncthreads();
+}
+// u = bf16(x * r * gamma) per component, as a float (the normalized layer input).
+__device__ __forceinline__ float4 rms_apply4(float4 x, float r, float4 g) {
+    return make_float4(__bfloat162float(__float2bfloat16_rn(x.x * r * g.x)),
+                       __bfloat162float(__float2bfloat16_rn(x.y * r * g.y)),
+                       __bfloat162float(__float2bfloat16_rn(x.z * r * g.z)),
+                       __bfloat162float(__float2bfloat16_rn(x.w * r * g.w)));
+}
+
 // Same layout as qd4_stage.  Work is split in chunks of 32 values (4 sub-blocks of 8
 // threads, 4 values per thread, max and sum by butterfly within the 8); warp w of nw
 // takes chunks w, w + nw, ... with four chunks' loads in flight.  Every lane of every
-// warp in [0, nw) must call it.
+// warp in [0, nw) must call it.  With ngamma, src is fp32 and vector i is staged as its
+// RMSNorm output bf16(x * nscale[i] * gamma) (nscale: the vectors' scales, shared memory).
 __device__ __forceinline__ void qd4_stage_par(const void* src, bool bf16, bool coherent, int64_t row_elems, int n,
-                                              const int* rows, int K, uint4* X, float4* XS, int tid, int nthr) {
+                                              const int* rows, int K, uint4* X, float4* XS, int tid, int nthr,
+                                              const float* ngamma = nullptr, const float* nscale = nullptr) {
     const int G = qd4_groups(K);
     const int lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
     const int cpv = G / 2;                            // chunks per vector (G = K/64 is a multiple of 4)
@@ -506,6 +565,9 @@ __device__ __forceinline__ void qd4_stage_par(const void* src, bool bf16, bool c
                 } else {
                     const float4* p4 = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + e);
                     v[j] = coherent ? __ldcg(p4) : *p4;
+                    if (ngamma)
+                        v[j] = rms_apply4(v[j], nscale[i],
+                                          *reinterpret_cast<const float4*>(ngamma + (e - row * row_elems)));
                 }
             }
         }

@@ -25,11 +25,11 @@ class MoeLayer:
                  bias=None, n_groups: int = 1, topk_groups: int = 1, scale: float = 1.0,
                  renormalize: bool = True, x_dtype: str = "bf16", I_s: int = 0, shared_qtype: str = "q8_0",
                  s_gate=None, s_up=None, s_down=None, accumulate: bool = False, tc_min_tokens: int = 0,
-                 decode_chain: bool = True):
+                 decode_chain: bool = True, norm_gamma=None, norm_eps: float = 1e-6):
         self.E, self.k, self.H, self.I = E, k, H, I
         self.x_dtype = x_dtype
         qt = _QT[qtype]
-        self._keep = [gate, up, down, W_router, bias, s_gate, s_up, s_down]
+        self._keep = [gate, up, down, W_router, bias, s_gate, s_up, s_down, norm_gamma]
         d = N.moe_layer_desc()
         d.route = N.route_cfg(N.MOE_ROUTE_SIGMOID_GROUP if mode == "sigmoid_group" else N.MOE_ROUTE_SOFTMAX,
                               E, k, n_groups, topk_groups, scale, renormalize)
@@ -49,6 +49,9 @@ class MoeLayer:
         d.accumulate = int(accumulate)
         d.tc_min_tokens = tc_min_tokens
         d.decode_chain_off = 0 if decode_chain else 1
+        if norm_gamma is not None:       # pre-norm: x is the fp32 residual stream
+            d.norm_gamma = norm_gamma.data_ptr()
+            d.norm_eps = norm_eps
         self.desc = d
         self.plan = N.moe_layer_plan_create(d)
         self.ws = None
@@ -90,6 +93,7 @@ class MoeLayer:
         """Re-create the plan after editing self.desc."""
         N.moe_layer_plan_destroy(self.plan)
         self.plan = N.moe_layer_plan_create(self.desc)
+        self.ws, self.ws_T = None, -1   # the workspace layout may have changed
 
     def device_status(self, T: int) -> int:
         return N.moe_read_device_status(self.plan, T, self.ws)

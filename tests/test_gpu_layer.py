@@ -70,6 +70,34 @@ def test_segmented_gemv_zipf_T120():
     assert layer.path(T) == "gemv"
 
 
+@pytest.mark.parametrize("T", [1, 2, 4, 8])
+def test_prenorm_equals_separate_rmsnorm(T):
+    # a pre-norm layer on the fp32 residual stream (the chain computes the RMSNorm itself at
+    # T <= 4; the GEMV path runs moe_rmsnorm_bf16 into its workspace) gives the bits of
+    # moe_rmsnorm_bf16 followed by the layer on its bf16 output
+    import quantized_routed_expert_sigmoid_gb300 as moe
+    from quantized_routed_expert_sigmoid_gb300 import MoeLayer
+    shape, seed = synth.DECODE, 41
+    kw = dict(mode="softmax", E=shape.E, k=shape.k, H=shape.H, I=shape.I, qtype=shape.qtype,
+              gate=synth.expert_stack(shape, seed, 0, "gate", "cuda"), up=synth.expert_stack(shape, seed, 0, "up", "cuda"),
+              down=synth.expert_stack(shape, seed, 0, "down", "cuda"),
+              W_router=synth.router_weight(shape, seed, 0).cuda(), accumulate=True)
+    gamma = synth.gamma(shape.H, seed, 0).cuda()
+    fused = MoeLayer(**kw, x_dtype="f32", norm_gamma=gamma, norm_eps=1e-6)
+    plain = MoeLayer(**kw, x_dtype="bf16")
+    assert fused.path(T) == plain.path(T) == ("decode_chain" if T <= 4 else "gemv")
+    x0 = 3.0 * synth.activations(T, shape.H, seed, "bf16").float().cuda()
+    a = x0.clone()
+    fused(a, out=a)
+    b = x0.clone()
+    u = torch.empty(T, shape.H, dtype=torch.bfloat16, device="cuda")
+    moe.moe_rmsnorm_bf16(b, gamma, T, shape.H, 1e-6, u)
+    plain(u, out=b)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert fused.device_status(T) == 0
+
+
 def test_deepseek_shape_decode_T2():
     tl = make_layer(synth.DEEPSEEK, 4, 2)
     _check_layer(tl, 2)

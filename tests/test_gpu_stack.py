@@ -170,6 +170,18 @@ def test_stack_48_layers_graph(T):
         assert err <= 1e-4 + 10 * self_div, f"layer {l}: rel-L2 {err:.3e}, oracle self-divergence {self_div:.3e}"
     eager_final = x.clone()
     assert drift[0][0] <= 1e-4                                         # one layer: the single-layer bar
+    # the same stack with the RMSNorm inside each layer call (pre-norm; the chain computes it
+    # itself): one call per layer on the residual stream, the bits of the separate kernels
+    from quantized_routed_expert_sigmoid_gb300 import MoeLayer
+    fused = [MoeLayer(mode="softmax", E=shape.E, k=shape.k, H=shape.H, I=shape.I, qtype=shape.qtype,
+                      gate=L["gate"], up=L["up"], down=L["down"], W_router=L["Wr"].cuda(), accumulate=True,
+                      x_dtype="f32", norm_gamma=L["gamma"].cuda(), norm_eps=EPS)
+             for L in layers]
+    xf = x0.cuda().contiguous().clone()
+    for m in fused:
+        m(xf, out=xf)
+    torch.cuda.synchronize()
+    assert torch.equal(xf, eager_final), "pre-norm layers differ from RMSNorm + layer"
     # capture the 48 layers once, replay from x0: the same bits as the eager chain
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
