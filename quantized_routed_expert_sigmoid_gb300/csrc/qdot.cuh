@@ -310,20 +310,6 @@ __device__ __forceinline__ void qd_rows4(const uint8_t* const (&rowp)[4], int nb
     }
 }
 
-// Butterfly sum of every accumulator across the warp (fixed order: same bits on every run).
-template <int NT>
-__device__ __forceinline__ void qd_warp_reduce(float (&acc)[4][NT]) {
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            float v = acc[r][t];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            acc[r][t] = v;
-        }
-}
-
 // Transposed warp sum of acc[4][NT] (NT = 1, 2, 4 or 8).  Each halving step sends one half
 // of the lane's entries to the partner lane and keeps the other, so the 4*NT sums cost
 // 4*NT - 1 shuffles plus the butterfly steps left over, not 4*NT*5.  Afterwards lane L
@@ -357,17 +343,6 @@ __device__ __forceinline__ float qd_warp_reduce_t(const float (&acc)[4][NT]) {
     return s;
 }
 
-// acc[r][t] selected by runtime (r, t) without dynamic register indexing.
-template <int NT>
-__device__ __forceinline__ float qd_pick(const float (&acc)[4][NT], int r, int t) {
-    float v = 0.f;
-#pragma unroll
-    for (int tt = 0; tt < NT; ++tt)
-#pragma unroll
-        for (int rr = 0; rr < 4; ++rr)
-            if (tt == t && rr == r) v = acc[rr][tt];
-    return v;
-}
 
 
 // ============================================================================
