@@ -129,3 +129,28 @@ def test_last_error_is_per_thread_message():
     t.start()
     t.join()
     assert seen == [""]
+
+
+def test_prenorm_validation():
+    # a pre-norm reads the fp32 residual stream: other input types, a misaligned gamma or a
+    # negative eps are refused on the host; an accepted one needs room for u in the workspace
+    d = _desc()
+    d.norm_gamma, d.norm_eps = FAKE, 1e-6
+    msg = _expect(N.MOE_ERR_INVALID_ARG, moe.moe_layer_plan_create, d)
+    assert "fp32" in msg
+    d.x_type = N.MOE_F32
+    d.norm_gamma = FAKE + 4
+    _expect(N.MOE_ERR_INVALID_ARG, moe.moe_layer_plan_create, d)
+    d.norm_gamma, d.norm_eps = FAKE, -1.0
+    _expect(N.MOE_ERR_INVALID_ARG, moe.moe_layer_plan_create, d)
+    d.norm_eps = 1e-6
+    plain_d = _desc()
+    plain_d.x_type = N.MOE_F32
+    pre, plain = moe.moe_layer_plan_create(d), moe.moe_layer_plan_create(plain_d)
+    try:
+        for T in (8, 64):
+            # no GPU here, so no decode chain: the normalized input u (bf16 [T][H]) gets its own region
+            assert moe.moe_layer_workspace_size(pre, T) >= moe.moe_layer_workspace_size(plain, T) + T * 2048 * 2
+    finally:
+        moe.moe_layer_plan_destroy(pre)
+        moe.moe_layer_plan_destroy(plain)
