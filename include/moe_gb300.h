@@ -241,9 +241,11 @@ moe_status moe_layer_path(const moe_layer_plan* plan, int T, int* path);
  * read-back, so it can be captured in a CUDA graph; replays give the same
  * bits as eager calls.  The expert path is chosen from T on the host
  * (moe_layer_path tells which): T <= 4 (T*k <= 64, E <= 256, Q4_K routed
- * experts) the chained decode kernels, T < tc_min_tokens the fp32
+ * experts, H <= 2048) the chained decode kernels, T < tc_min_tokens the fp32
  * dequant-GEMV kernels (both fp32 accumulate), larger T the tensor-core
- * grouped GEMM (fp16 operands, fp32 accumulate).
+ * grouped GEMM (fp16 operands, fp32 accumulate; the per-pair down outputs
+ * are rounded to fp16 before the fp32 combine).  out may alias x when
+ * accumulate = 1 (a residual block): x is read before out is written.
  */
 moe_status moe_layer(const moe_layer_plan* plan, const void* x, int T, float* out, void* workspace,
                      size_t ws_bytes, moe_stream_t stream);
