@@ -55,7 +55,7 @@ WORKLOADS = {
                  "MoE layer T=2: H=7168 E=256 sigmoid+bias 8 groups/4 kept top-8 scale 2.5 I=2048 Q4_K, shared I=2048 Q8_0"),
 }
 
-CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+CLOCK_QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -121,29 +121,55 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t_begin=None, t_end=None):
+        """Median SM clock, max clock and active throttle reasons over the samples taken in
+        [t_begin, t_end] (host epoch seconds: the timed region); all samples when none fell in it."""
         if self.proc is None or not self.path or not os.path.exists(self.path):
             return None
-        rows = []
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                rows.append((float(parts[1]), float(parts[2]), parts[4:]))
-            except ValueError:
-                continue
+        rows = parse_clock_samples(open(self.path).read().splitlines())
         os.unlink(self.path)
-        if not rows:
-            return None
-        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = set()
-        for _, _, flags in rows:
-            for n, v in zip(names[1:], flags[1:]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "samples": len(rows), "reasons": sorted(reasons)}
+        return summarize_clocks(rows, t_begin, t_end)
+
+
+def parse_clock_samples(lines):
+    """(epoch seconds or None, sm MHz, max sm MHz, [reason flags]) per nvidia-smi CSV line of
+    CLOCK_QUERY (noheader, nounits)."""
+    import datetime
+    rows = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            ts = None
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                pass
+            rows.append((ts, float(parts[2]), float(parts[3]), parts[5:10]))
+        except ValueError:
+            continue
+    return rows
+
+
+def summarize_clocks(rows, t_begin=None, t_end=None):
+    if not rows:
+        return None
+    window = "timed region"
+    if t_begin is not None and t_end is not None:
+        inside = [r for r in rows if r[0] is not None and t_begin <= r[0] <= t_end]
+        if inside:
+            rows = inside
+        else:
+            window = "whole run (no sample fell in the timed region)"
+    names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = set()
+    for r in rows:
+        for n, v in zip(names[1:], r[3][1:]):
+            if v.lower().startswith("active"):
+                reasons.add(n)
+    return {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": max(r[2] for r in rows),
+            "samples": len(rows), "reasons": sorted(reasons), "window": window}
 
 
 # ------------------------------------------------------------------ workload construction
@@ -276,13 +302,26 @@ def run_ours(args, rank, world):
         torch.distributed.barrier()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     cur = torch.cuda.current_stream(device)          # CUDAGraph.replay() launches on the current stream
+    if args.steps is None:
+        # no --steps given: about a second of timed work, so the clock samples fall inside it
+        t_probe = time.perf_counter()
+        for _ in range(10):
+            graph.replay()
+        torch.cuda.synchronize()
+        per = max((time.perf_counter() - t_probe) / 10, 1e-6)
+        k = torch.tensor([min(20000, max(200, int(1.2 / per) + 1))], device=device)
+        if world > 1:
+            torch.distributed.all_reduce(k, op=torch.distributed.ReduceOp.MAX)
+        args.steps = int(k.item())
     with ClockSampler(device.index) as clk:
         torch.cuda.synchronize()
+        t_begin = time.time()
         ev0.record(cur)
         for _ in range(args.steps):
             graph.replay()
         ev1.record(cur)
         torch.cuda.synchronize()
+        t_end = time.time()
     t_ms = ev0.elapsed_time(ev1)
     if world > 1:
         tt = torch.tensor([t_ms], device=device)
@@ -401,7 +440,7 @@ def run_ours(args, rank, world):
         "roofline": roof,
         "e2e": e2e,
         "gpu_launches": launches_per_layer(shape, T, stack, path) * L * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clk.summary(t_begin, t_end),
     }
     result.update(extra)
     if rank == 0 and not args.no_cpu_baseline:
@@ -555,7 +594,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: about a second of work; the reference arm: 200)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
@@ -569,6 +609,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
+        if args.steps is None:
+            args.steps = 200
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
         return

@@ -55,3 +55,25 @@ def test_changed_source_gives_none(bench):
     mod, csrc = bench
     (csrc / "k.cu").write_bytes(b"kernel source v2\n")
     assert mod.profiled_traffic("k_kernel", types.SimpleNamespace(workload="decode", tokens=0)) is None
+
+
+def test_clock_samples_inside_the_timed_region(bench):
+    # only the samples taken while the timed steps ran count; with none inside, all of them
+    mod, _ = bench
+    lines = [
+        "2026/12/02 10:00:00.000, 0, 1200, 2070, 150.0, Active, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 10:00:00.200, 0, 2070, 2070, 900.0, Active, Not Active, Not Active, Not Active, Active",
+        "2026/12/02 10:00:00.400, 0, 2055, 2070, 950.0, Active, Not Active, Not Active, Not Active, Active",
+        "2026/12/02 10:00:00.600, 0, 1500, 2070, 200.0, Active, Active, Not Active, Not Active, Not Active",
+        "garbage line",
+    ]
+    rows = mod.parse_clock_samples(lines)
+    assert len(rows) == 4
+    t0 = rows[1][0] - 0.05
+    t1 = rows[2][0] + 0.05
+    s = mod.summarize_clocks(rows, t0, t1)
+    assert s["samples"] == 2 and s["sm_mhz"] == (2070 + 2055) / 2 and s["reasons"] == ["sw_power_cap"]
+    assert s["window"] == "timed region"
+    s_all = mod.summarize_clocks(rows, t1 + 10.0, t1 + 11.0)
+    assert s_all["samples"] == 4 and "hw_slowdown" in s_all["reasons"] and s_all["window"].startswith("whole run")
+    assert mod.summarize_clocks([], None, None) is None
