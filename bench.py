@@ -172,6 +172,30 @@ def summarize_clocks(rows, t_begin=None, t_end=None):
             "samples": len(rows), "reasons": sorted(reasons), "window": window}
 
 
+# ------------------------------------------------------------------ replicas (one process per GPU)
+
+def ranks_max(v, world, device):
+    """The largest of the ranks' values of v; v itself for one process.  Every rank calls it."""
+    if world <= 1:
+        return v
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.item()
+
+
+def agree_steps(seconds_per_step, world, device, target_s=1.2, lo=200, hi=20000):
+    """Timed steps for about target_s seconds of work, the same count on every rank (the
+    slowest rank's probe sets it, so no rank's timed region is shorter than target_s)."""
+    k = min(hi, max(lo, int(target_s / max(seconds_per_step, 1e-6)) + 1))
+    return int(ranks_max(k, world, device))
+
+
+def job_tokens_per_s(world, T, L, steps, t_ms):
+    """Whole-job throughput of N replicas: each rank applies L layers to its own T tokens per
+    step, and t_ms, the slowest rank's time for all steps, bounds the job."""
+    return world * T * L * steps / (t_ms / 1e3)
+
+
 # ------------------------------------------------------------------ workload construction
 
 def build_layers(shape, T, L, seed, device, shared_router=False, decode_chain=True):
@@ -308,11 +332,7 @@ def run_ours(args, rank, world):
         for _ in range(10):
             graph.replay()
         torch.cuda.synchronize()
-        per = max((time.perf_counter() - t_probe) / 10, 1e-6)
-        k = torch.tensor([min(20000, max(200, int(1.2 / per) + 1))], device=device)
-        if world > 1:
-            torch.distributed.all_reduce(k, op=torch.distributed.ReduceOp.MAX)
-        args.steps = int(k.item())
+        args.steps = agree_steps((time.perf_counter() - t_probe) / 10, world, device)
     with ClockSampler(device.index) as clk:
         torch.cuda.synchronize()
         t_begin = time.time()
@@ -322,13 +342,9 @@ def run_ours(args, rank, world):
         ev1.record(cur)
         torch.cuda.synchronize()
         t_end = time.time()
-    t_ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        tt = torch.tensor([t_ms], device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_ms = float(tt.item())
+    t_ms = ranks_max(ev0.elapsed_time(ev1), world, device)
     ms_per_step = t_ms / args.steps
-    value = world * T * L * args.steps / (t_ms / 1e3)
+    value = job_tokens_per_s(world, T, L, args.steps, t_ms)
 
     # ---- the dominant kernel alone (the routed gate/up + SwiGLU launch)
     path = layers[0].path(T)           # which kernels the library runs for this T
@@ -373,16 +389,17 @@ def run_ours(args, rank, world):
 
     for _ in range(2):
         e2e_step()
+    if world > 1:
+        torch.distributed.barrier()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         e2e_step()
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    e2e = {"value": T * L / e2e_s * world, "unit": "tokens/s", "h2d_bytes_per_step": x.numel() * x.element_size(),
+    e2e_ms = ranks_max((time.perf_counter() - t0) * 1e3, world, device)
+    e2e = {"value": job_tokens_per_s(world, T, L, e2e_steps, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": x.numel() * x.element_size(),
            "d2h_bytes_per_step": out_stack.numel() * 4, "calls": "moe_layer x %d per step" % L}
 
     hbm_peak, tc_peak, peak_kind = measured_peaks()
     roof = None
-    layer_us_ = ms_per_step * 1e3 / L
     if gu_ms is not None and chain_path:
         # routing + gate/up (+ the shared expert's gate/up rows) of the chain
         cb = gu_bytes + (2 * shape.I_s * synth.row_bytes(shape.shared_qtype, shape.H) if shape.I_s > 0 else 0)
@@ -424,7 +441,7 @@ def run_ours(args, rank, world):
     layer_us = ms_per_step * 1e3 / L
     extra = {}
     if stack:
-        extra["stack_tokens_per_s"] = round(world * T * args.steps / (t_ms / 1e3), 1)
+        extra["stack_tokens_per_s"] = round(job_tokens_per_s(world, T, 1, args.steps, t_ms), 1)
     result = {
         "metric": "MoE-layer tokens/s (decode T=1,2 / prefill T=4096); % of HBM roofline",
         "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
