@@ -27,6 +27,9 @@ _lib = None
 
 Q8_0 = 2
 Q4_K = 3
+Q5_K = 4
+Q6_K = 5
+Q3_K = 6
 ROUTE_SOFTMAX = 0
 ROUTE_SIGMOID_GROUP = 1
 
@@ -113,8 +116,12 @@ def _u8(a) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(a, dtype=np.uint8))
 
 
+_BLOCK = {Q8_0: (32, 34), Q4_K: (256, 144), Q5_K: (256, 176), Q6_K: (256, 210), Q3_K: (256, 110)}
+
+
 def row_bytes(qtype: int, K: int) -> int:
-    return K // 32 * 34 if qtype == Q8_0 else K // 256 * 144
+    weights, nbytes = _BLOCK[qtype]
+    return K // weights * nbytes
 
 
 # --------------------------------------------------------------------------- wrappers

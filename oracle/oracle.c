@@ -33,13 +33,24 @@
  *   Q4_K: 144 bytes per 256 weights: fp16 d, fp16 dmin, 12 bytes of packed
  *         6-bit (scale, min) for 8 sub-blocks of 32, 128 bytes of 4-bit q;
  *         w = d*sc_j*q - dmin*m_j.
+ *   Q5_K: 176 bytes per 256: Q4_K's fields plus 32 bytes of fifth bits;
+ *         q in [0, 31], w = d*sc_j*q - dmin*m_j.
+ *   Q6_K: 210 bytes per 256: 4-bit low and 2-bit high parts, 16 int8
+ *         scales (one per 16 weights), fp16 d last; w = d*sc*(q - 32).
+ *   Q3_K: 110 bytes per 256: high-bit mask, 2-bit low parts, 16 packed
+ *         6-bit scales stored plus 32, fp16 d last; w = d*(sc - 32)*q with
+ *         q = low - 4 where the high bit is clear.
+ * Q5_K, Q6_K and Q3_K are the next expert types the pages list for the card
+ * (Q4_K to Q6_K, and the Q3_K_M files the large model ships in); only the
+ * oracle decodes them so far.
  *
  * Every value is computed in fp64.  Weight matrices are [rows][K/blk blocks],
  * blocks along the input dimension K; experts are laid out one after another
  * at a fixed byte stride.
  *
  * Parity status of each function (pins live in the test suite):
- *   half_to_double, dequant Q8_0 / Q4_K   pinned (hand-built blocks)
+ *   half_to_double, dequant Q8_0 / Q4_K /
+ *   Q5_K / Q6_K / Q3_K                    pinned (hand-built blocks)
  *   router logits                         pinned (integer closed form)
  *   top-k softmax / sigmoid-group         pinned (brute force, special cases)
  *   permute                               pinned (brute force)
@@ -57,6 +68,9 @@
 
 #define ORACLE_Q8_0 2
 #define ORACLE_Q4_K 3
+#define ORACLE_Q5_K 4
+#define ORACLE_Q6_K 5
+#define ORACLE_Q3_K 6
 
 #define ORACLE_ROUTE_SOFTMAX 0
 #define ORACLE_ROUTE_SIGMOID_GROUP 1
@@ -144,10 +158,107 @@ void oracle_dequant_q4_k_row(const uint8_t* row, int64_t K, double* w)
     }
 }
 
+/* Q5_K: 176 bytes per 256 weights: d, dmin and the 12 packed (scale, min)
+ * bytes exactly as in Q4_K, then 32 bytes of fifth bits, then 128 bytes of
+ * low nibbles laid out as the Q4_K quants.  Element i of sub-block j takes
+ * bit j of fifth-bit byte i as its 16s digit:
+ * q = nibble + 16*bit in [0, 31];  w = d*sc_j*q - dmin*m_j.               */
+void oracle_dequant_q5_k_row(const uint8_t* row, int64_t K, double* w)
+{
+    for (int64_t b = 0; b < K / 256; ++b) {
+        const uint8_t* blk = row + b * 176;
+        double d = oracle_half_to_double(read_u16_le(blk));
+        double dmin = oracle_half_to_double(read_u16_le(blk + 2));
+        const uint8_t* S = blk + 4;
+        const uint8_t* QH = blk + 16;
+        const uint8_t* Q = blk + 48;
+        for (int j = 0; j < 8; ++j) {
+            int sc, m;
+            q4k_scale_min(S, j, &sc, &m);
+            int c = j / 2;
+            for (int i = 0; i < 32; ++i) {
+                int byte = Q[32 * c + i];
+                int lo = (j % 2 == 0) ? (byte & 15) : (byte >> 4);
+                int hi = (QH[i] >> j) & 1;
+                int q = lo + 16 * hi;
+                w[b * 256 + 32 * j + i] = d * (double)sc * (double)q - dmin * (double)m;
+            }
+        }
+    }
+}
+
+/* Q6_K: 210 bytes per 256 weights: 128 bytes of low nibbles, 64 bytes of
+ * two-bit high parts, 16 signed 8-bit scales (one per 16 weights), and the
+ * fp16 d last.  The super-block is two halves of 128; in half h, element
+ * e = 32r + l (quarter r < 4, l < 32) takes
+ *   its low nibble from nibble byte 64h + 32(r % 2) + l
+ *     (the low nibble for r < 2, the high nibble for r >= 2),
+ *   its high pair from bits 2r, 2r+1 of high-part byte 32h + l;
+ * q = nibble + 16*pair - 32 in [-32, 31];  w = d * scale[i/16] * q with
+ * i = 128h + e the element's index in the super-block.                   */
+void oracle_dequant_q6_k_row(const uint8_t* row, int64_t K, double* w)
+{
+    for (int64_t b = 0; b < K / 256; ++b) {
+        const uint8_t* blk = row + b * 210;
+        const uint8_t* QL = blk;
+        const uint8_t* QH = blk + 128;
+        const uint8_t* SC = blk + 192;
+        double d = oracle_half_to_double(read_u16_le(blk + 208));
+        for (int i = 0; i < 256; ++i) {
+            int h = i / 128, e = i % 128, r = e / 32, l = e % 32;
+            int byte = QL[64 * h + 32 * (r % 2) + l];
+            int lo = (r < 2) ? (byte & 15) : (byte >> 4);
+            int hi = (QH[32 * h + l] >> (2 * r)) & 3;
+            int q = lo + 16 * hi - 32;
+            int sc = (int)SC[i / 16];
+            if (sc >= 128) sc -= 256;                /* two's-complement int8 */
+            w[b * 256 + i] = d * (double)sc * (double)q;
+        }
+    }
+}
+
+/* Q3_K scale j (of 16) from the 12 packed bytes S, before the offset of 32:
+ * bits 0-3 are the low nibble of S[j] for j < 8 and the high nibble of
+ * S[j-8] for j >= 8; bits 4-5 are bits 2(j/4), 2(j/4)+1 of S[8 + j%4].    */
+static int q3k_scale(const uint8_t* S, int j)
+{
+    int lo = (j < 8) ? (S[j] & 15) : (S[j - 8] >> 4);
+    int hi = (S[8 + j % 4] >> (2 * (j / 4))) & 3;
+    return lo | (hi << 4);
+}
+
+/* Q3_K: 110 bytes per 256 weights: 32 bytes of high bits, 64 bytes of
+ * two-bit low parts, 12 bytes of packed 6-bit scales (one per 16 weights,
+ * stored plus 32), and the fp16 d last.  In half h, element e = 32r + l
+ * (r < 4, l < 32) takes bits 2r, 2r+1 of low-part byte 32h + l and bit
+ * 4h + r of high-bit byte l; q = low - 4 when that bit is clear, else low,
+ * so q is in [-4, 3];  w = d * (scale[i/16] - 32) * q, i = 128h + e.      */
+void oracle_dequant_q3_k_row(const uint8_t* row, int64_t K, double* w)
+{
+    for (int64_t b = 0; b < K / 256; ++b) {
+        const uint8_t* blk = row + b * 110;
+        const uint8_t* HM = blk;
+        const uint8_t* QS = blk + 32;
+        const uint8_t* S = blk + 96;
+        double d = oracle_half_to_double(read_u16_le(blk + 108));
+        for (int i = 0; i < 256; ++i) {
+            int h = i / 128, e = i % 128, r = e / 32, l = e % 32;
+            int lo = (QS[32 * h + l] >> (2 * r)) & 3;
+            int hbit = (HM[l] >> (4 * h + r)) & 1;
+            int q = hbit ? lo : lo - 4;
+            int sc = q3k_scale(S, i / 16) - 32;
+            w[b * 256 + i] = d * (double)sc * (double)q;
+        }
+    }
+}
+
 static int64_t row_bytes(int qtype, int64_t K)
 {
     if (qtype == ORACLE_Q8_0) return K / 32 * 34;
     if (qtype == ORACLE_Q4_K) return K / 256 * 144;
+    if (qtype == ORACLE_Q5_K) return K / 256 * 176;
+    if (qtype == ORACLE_Q6_K) return K / 256 * 210;
+    if (qtype == ORACLE_Q3_K) return K / 256 * 110;
     return -1;
 }
 
@@ -157,8 +268,15 @@ int oracle_dequant_matrix(int qtype, const uint8_t* data, int64_t rows, int64_t 
     int64_t rb = row_bytes(qtype, K);
     if (rb < 0) return -1;
     for (int64_t r = 0; r < rows; ++r) {
-        if (qtype == ORACLE_Q8_0) oracle_dequant_q8_0_row(data + r * rb, K, w + r * K);
-        else oracle_dequant_q4_k_row(data + r * rb, K, w + r * K);
+        const uint8_t* src = data + r * rb;
+        double* dst = w + r * K;
+        switch (qtype) {
+        case ORACLE_Q8_0: oracle_dequant_q8_0_row(src, K, dst); break;
+        case ORACLE_Q4_K: oracle_dequant_q4_k_row(src, K, dst); break;
+        case ORACLE_Q5_K: oracle_dequant_q5_k_row(src, K, dst); break;
+        case ORACLE_Q6_K: oracle_dequant_q6_k_row(src, K, dst); break;
+        default:          oracle_dequant_q3_k_row(src, K, dst); break;
+        }
     }
     return 0;
 }

@@ -2,7 +2,8 @@
 
 This module draws the random tensors (activations, router weights, biases,
 RMSNorm weights, expert weights) and stores expert weights in the GGUF block
-layouts Q8_0 and Q4_K.  It is shared by the tests, the benchmark and the
+layouts Q8_0 and Q4_K (and Q5_K, Q6_K, Q3_K, which only the oracle decodes
+so far).  It is shared by the tests, the benchmark and the
 smoke check, and it holds none of the layer's arithmetic: it never routes,
 never dequantizes and never evaluates an expert.  (Encoding a float matrix
 into blocks is how the stored inputs are made; decoding them is the oracle's
@@ -31,6 +32,12 @@ import torch
 
 Q8_0 = "q8_0"
 Q4_K = "q4_k"
+Q5_K = "q5_k"
+Q6_K = "q6_k"
+Q3_K = "q3_k"
+
+# weights and bytes per block of each stored type
+BLOCK = {Q8_0: (32, 34), Q4_K: (256, 144), Q5_K: (256, 176), Q6_K: (256, 210), Q3_K: (256, 110)}
 
 TAGS = {"x": 1, "router": 2, "bias": 3, "gate": 4, "up": 5, "down": 6, "gamma": 7,
         "s_gate": 8, "s_up": 9, "s_down": 10, "zipf": 11, "fill": 12}
@@ -63,7 +70,8 @@ def normal(shape, std: float, seed: int, device="cpu") -> torch.Tensor:
 
 
 def row_bytes(qtype: str, K: int) -> int:
-    return K // 32 * 34 if qtype == Q8_0 else K // 256 * 144
+    weights, nbytes = BLOCK[qtype]
+    return K // weights * nbytes
 
 
 # --------------------------------------------------------------------------- encoders
@@ -147,8 +155,117 @@ def encode_q4_k(w: torch.Tensor) -> torch.Tensor:
     return blocks.reshape(rows, K // 256 * 144).contiguous()
 
 
+def pack_q5_k(d: torch.Tensor, dmin: torch.Tensor, sc: torch.Tensor, m: torch.Tensor,
+              q: torch.Tensor) -> torch.Tensor:
+    """Pack Q5_K fields into 176-byte blocks: q [..., 256] ints in [0, 31].  The header and
+    the low nibbles are laid out as in Q4_K; byte i of the 32 fifth-bit bytes holds bit 4 of
+    q[32j + i] in its bit j."""
+    q = q.to(torch.int32)
+    base = pack_q4_k(d, dmin, sc, m, q & 15)
+    bits = ((q >> 4) & 1).reshape(*q.shape[:-1], 8, 32)             # [..., j, i]
+    shifts = torch.arange(8, dtype=torch.int32).reshape(8, 1)
+    qh = (bits << shifts).sum(dim=-2).to(torch.uint8)                # [..., 32]
+    return torch.cat([base[..., :16], qh, base[..., 16:]], dim=-1)
+
+
+def encode_q5_k(w: torch.Tensor) -> torch.Tensor:
+    """[rows, K] float -> [rows, K/256*176] uint8 Q5_K blocks: the Q4_K quantizer with 32
+    levels per sub-block instead of 16."""
+    rows, K = w.shape
+    assert K % 256 == 0
+    b = w.reshape(rows, K // 256, 8, 32).float()
+    mn = b.amin(dim=-1).clamp(max=0.0)
+    mx = b.amax(dim=-1)
+    scale = (mx - mn) / 31.0
+    mins = -mn
+    d = (scale.amax(dim=-1) / 63.0).to(torch.float16).float()
+    dmin = (mins.amax(dim=-1) / 63.0).to(torch.float16).float()
+    safe_d = torch.where(d > 0, d, torch.ones_like(d)).unsqueeze(-1)
+    safe_dm = torch.where(dmin > 0, dmin, torch.ones_like(dmin)).unsqueeze(-1)
+    sc = torch.where(d.unsqueeze(-1) > 0, torch.round(scale / safe_d), torch.zeros_like(scale)).clamp(0, 63)
+    m = torch.where(dmin.unsqueeze(-1) > 0, torch.round(mins / safe_dm), torch.zeros_like(mins)).clamp(0, 63)
+    step = (d.unsqueeze(-1) * sc).unsqueeze(-1)
+    off = (dmin.unsqueeze(-1) * m).unsqueeze(-1)
+    safe_step = torch.where(step > 0, step, torch.ones_like(step))
+    q = torch.where(step > 0, torch.round((b + off) / safe_step), torch.zeros_like(b)).clamp(0, 31)
+    blocks = pack_q5_k(d, dmin, sc.to(torch.int32), m.to(torch.int32), q.reshape(rows, K // 256, 256))
+    return blocks.reshape(rows, K // 256 * 176).contiguous()
+
+
+def _signed_group_quant(w: torch.Tensor, qmax: int, smax: int):
+    """Symmetric quantizer shared by Q6_K and Q3_K: per 16-weight group a step s_g =
+    max|w| / qmax; one fp16 d per 256 = max_g s_g / smax; integer group scales
+    sc_g = round(s_g / d) in [0, smax]; q = clamp(round(w / (d sc_g)), -qmax, qmax - 1).
+    w: [rows, nb, 16, 16]."""
+    s = w.abs().amax(dim=-1) / qmax                                  # [rows, nb, 16]
+    d = (s.amax(dim=-1) / smax).to(torch.float16).float()            # [rows, nb]
+    safe_d = torch.where(d > 0, d, torch.ones_like(d)).unsqueeze(-1)
+    sc = torch.where(d.unsqueeze(-1) > 0, torch.round(s / safe_d), torch.zeros_like(s)).clamp(0, smax)
+    step = (d.unsqueeze(-1) * sc).unsqueeze(-1)
+    safe_step = torch.where(step > 0, step, torch.ones_like(step))
+    q = torch.where(step > 0, torch.round(w / safe_step), torch.zeros_like(w)).clamp(-qmax, qmax - 1)
+    return d, sc.to(torch.int32), q.to(torch.int32)
+
+
+def pack_q6_k(d: torch.Tensor, sc: torch.Tensor, q: torch.Tensor) -> torch.Tensor:
+    """Pack Q6_K fields into 210-byte blocks: sc [..., 16] ints in [-128, 127], q [..., 256]
+    ints in [-32, 31].  With u = q + 32, weight 128h + 32r + l puts the low nibble of u in
+    byte 64h + 32(r % 2) + l of the first 128 bytes (low nibble for r < 2, high for r >= 2)
+    and its top two bits in bits 2r..2r+1 of byte 128 + 32h + l; then the 16 scale bytes,
+    then fp16 d."""
+    u = (q.to(torch.int32) + 32).reshape(*q.shape[:-1], 2, 4, 32)   # [..., h, r, l]
+    lo = u & 15
+    ql = torch.cat([lo[..., 0, :] | (lo[..., 2, :] << 4), lo[..., 1, :] | (lo[..., 3, :] << 4)], dim=-1)
+    shifts = (2 * torch.arange(4, dtype=torch.int32)).reshape(4, 1)
+    qh = (((u >> 4) & 3) << shifts).sum(dim=-2)                      # [..., h, 32]
+    lead = q.shape[:-1]
+    scb = (sc.to(torch.int32) & 0xFF).to(torch.uint8)
+    return torch.cat([ql.reshape(*lead, 128).to(torch.uint8), qh.reshape(*lead, 64).to(torch.uint8), scb,
+                      _fp16_bits(d.float())], dim=-1)
+
+
+def encode_q6_k(w: torch.Tensor) -> torch.Tensor:
+    """[rows, K] float -> [rows, K/256*210] uint8 Q6_K blocks (symmetric per 16 weights)."""
+    rows, K = w.shape
+    assert K % 256 == 0
+    d, sc, q = _signed_group_quant(w.reshape(rows, K // 256, 16, 16).float(), 32, 127)
+    blocks = pack_q6_k(d, sc, q.reshape(rows, K // 256, 256))
+    return blocks.reshape(rows, K // 256 * 210).contiguous()
+
+
+def pack_q3_k(d: torch.Tensor, sc: torch.Tensor, q: torch.Tensor) -> torch.Tensor:
+    """Pack Q3_K fields into 110-byte blocks: sc [..., 16] ints in [-32, 31], q [..., 256]
+    ints in [-4, 3].  With v = q + 4, weight 128h + 32r + l puts bit 2 of v in bit 4h + r of
+    byte l (the 32 mask bytes) and bits 0-1 in bits 2r..2r+1 of byte 32 + 32h + l.  Scale j
+    is stored as s = sc_j + 32: bits 0-3 in the low nibble of byte 96 + j (j < 8) or the high
+    nibble of byte 96 + j - 8, bits 4-5 in bits 2(j // 4).. of byte 104 + j % 4; then fp16 d."""
+    lead = q.shape[:-1]
+    v = (q.to(torch.int32) + 4).reshape(*lead, 2, 4, 32)             # [..., h, r, l]
+    hbit = ((v >> 2) & 1).reshape(*lead, 8, 32)                      # [..., 4h + r, l]
+    hm = (hbit << torch.arange(8, dtype=torch.int32).reshape(8, 1)).sum(dim=-2)
+    qs = ((v & 3) << (2 * torch.arange(4, dtype=torch.int32)).reshape(4, 1)).sum(dim=-2)   # [..., h, l]
+    s = sc.to(torch.int32) + 32                                      # [..., 16]
+    nib = (s[..., :8] & 15) | ((s[..., 8:] & 15) << 4)               # [..., 8]
+    top = ((s >> 4) & 3).reshape(*lead, 4, 4)                        # [..., j // 4, j % 4]
+    hi = (top << (2 * torch.arange(4, dtype=torch.int32)).reshape(4, 1)).sum(dim=-2)      # [..., 4]
+    return torch.cat([hm.to(torch.uint8), qs.reshape(*lead, 64).to(torch.uint8), nib.to(torch.uint8),
+                      hi.to(torch.uint8), _fp16_bits(d.float())], dim=-1)
+
+
+def encode_q3_k(w: torch.Tensor) -> torch.Tensor:
+    """[rows, K] float -> [rows, K/256*110] uint8 Q3_K blocks (symmetric per 16 weights)."""
+    rows, K = w.shape
+    assert K % 256 == 0
+    d, sc, q = _signed_group_quant(w.reshape(rows, K // 256, 16, 16).float(), 4, 31)
+    blocks = pack_q3_k(d, sc, q.reshape(rows, K // 256, 256))
+    return blocks.reshape(rows, K // 256 * 110).contiguous()
+
+
+_ENCODERS = {Q8_0: encode_q8_0, Q4_K: encode_q4_k, Q5_K: encode_q5_k, Q6_K: encode_q6_k, Q3_K: encode_q3_k}
+
+
 def encode(qtype: str, w: torch.Tensor) -> torch.Tensor:
-    return encode_q8_0(w) if qtype == Q8_0 else encode_q4_k(w)
+    return _ENCODERS[qtype](w)
 
 
 # --------------------------------------------------------------------------- layer specs

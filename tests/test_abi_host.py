@@ -85,6 +85,8 @@ def test_plan_validation():
     finally:
         moe.moe_layer_plan_destroy(plan)
     _expect(N.MOE_ERR_UNSUPPORTED, moe.moe_layer_plan_create, _desc(qtype=N.MOE_BF16))
+    for other in (4, 5, 6, -1):          # types the library does not decode yet, and garbage
+        _expect(N.MOE_ERR_UNSUPPORTED, moe.moe_layer_plan_create, _desc(qtype=other))
     _expect(N.MOE_ERR_INVALID_ARG, moe.moe_layer_plan_create, _desc(H=2000))          # not a block multiple
     _expect(N.MOE_ERR_INVALID_ARG, moe.moe_layer_plan_create, _desc(data=FAKE + 4))   # misaligned weights
     _expect(N.MOE_ERR_INVALID_ARG, moe.moe_layer_plan_create, _desc(stride=100))      # stride too small

@@ -29,6 +29,30 @@ MUTANTS = [
     ("q4k_scale_high_bits", "((S[j - 4] >> 6) << 4)", "((S[j] >> 6) << 4)", ["q4_k_handbuilt"]),
     ("q4k_min_high_bits", "((S[j] >> 6) << 4);", "((S[j - 4] >> 6) << 4);", ["q4_k_handbuilt"]),
     ("q4k_block_stride", "row + b * 144", "row + b * 128", ["q4_k_multiblock_rows"]),
+    ("q5k_fifth_bit_index", "int hi = (QH[i] >> j) & 1;", "int hi = (QH[i] >> (j / 2)) & 1;",
+     ["q5_k_handbuilt"]),
+    ("q5k_fifth_bit_weight", "int q = lo + 16 * hi;", "int q = lo + 32 * hi;", ["q5_k_handbuilt"]),
+    ("q5k_block_stride", "row + b * 176", "row + b * 160", ["kquant_multiblock_rows"]),
+    ("q6k_offset", "int q = lo + 16 * hi - 32;", "int q = lo + 16 * hi - 31;", ["q6_k_handbuilt"]),
+    ("q6k_quarter_nibble", "int lo = (r < 2) ? (byte & 15) : (byte >> 4);",
+     "int lo = (r % 2 == 0) ? (byte & 15) : (byte >> 4);", ["q6_k_handbuilt"]),
+    ("q6k_low_byte", "QL[64 * h + 32 * (r % 2) + l]", "QL[64 * h + 32 * (r / 2) + l]", ["q6_k_handbuilt"]),
+    ("q6k_high_pair", "(QH[32 * h + l] >> (2 * r)) & 3", "(QH[32 * h + l] >> (2 * (3 - r))) & 3",
+     ["q6_k_handbuilt"]),
+    ("q6k_scale_unsigned", "if (sc >= 128) sc -= 256;", "", ["q6_k_handbuilt"]),
+    ("q6k_scale_group", "(int)SC[i / 16]", "(int)SC[i / 32]", ["q6_k_handbuilt"]),
+    ("q6k_d_first", "read_u16_le(blk + 208)", "read_u16_le(blk)", ["q6_k_handbuilt"]),
+    ("q6k_block_stride", "row + b * 210", "row + b * 208", ["kquant_multiblock_rows"]),
+    ("q3k_high_bit_sense", "int q = hbit ? lo : lo - 4;", "int q = hbit ? lo - 4 : lo;", ["q3_k_handbuilt"]),
+    ("q3k_mask_bit", "(HM[l] >> (4 * h + r)) & 1", "(HM[l] >> (2 * h + r)) & 1", ["q3_k_handbuilt"]),
+    ("q3k_scale_high_bits", "(S[8 + j % 4] >> (2 * (j / 4))) & 3", "(S[8 + j / 4] >> (2 * (j % 4))) & 3",
+     ["q3_k_handbuilt"]),
+    ("q3k_scale_nibbles", "(j < 8) ? (S[j] & 15) : (S[j - 8] >> 4)", "(j < 8) ? (S[j] >> 4) : (S[j - 8] & 15)",
+     ["q3_k_handbuilt"]),
+    ("q3k_scale_offset", "q3k_scale(S, i / 16) - 32", "q3k_scale(S, i / 16) - 31", ["q3_k_handbuilt"]),
+    ("q3k_block_stride", "row + b * 110", "row + b * 108", ["kquant_multiblock_rows"]),
+    ("q6k_row_bytes", "return K / 256 * 210;", "return K / 256 * 208;",
+     ["kquant_multiblock_rows", "ffn_identity_kquants"]),
     ("router_transposed", "(double)Wr[(int64_t)e * H + h]", "(double)Wr[(int64_t)h * E + e]",
      ["router_integer"]),
     ("topk_smallest", "if (sa != sb) return sa > sb;", "if (sa != sb) return sa < sb;",

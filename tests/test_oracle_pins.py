@@ -64,6 +64,46 @@ def pin_q4_k_multiblock_rows(lib):
             assert np.all(got[r, 256 * b:256 * (b + 1)] == 2.0 ** (r + b))
 
 
+def _pin_handbuilt(lib, kind, qtype):
+    weights, nbytes, make = golden.BLOCK_TYPES[kind]
+    fx = golden.read_fixture(kind)
+    for name, (blk, expected) in make().items():
+        assert len(blk) == nbytes, name
+        assert fx[name] == blk, f"fixture {name} differs from the packer"
+        got = oracle.dequant(qtype, np.frombuffer(blk, np.uint8), 1, weights, lib=lib)[0]
+        assert np.array_equal(got, np.array(expected)), name
+
+
+def pin_q5_k_handbuilt(lib):
+    _pin_handbuilt(lib, "Q5_K", oracle.Q5_K)
+
+
+def pin_q6_k_handbuilt(lib):
+    _pin_handbuilt(lib, "Q6_K", oracle.Q6_K)
+
+
+def pin_q3_k_handbuilt(lib):
+    _pin_handbuilt(lib, "Q3_K", oracle.Q3_K)
+
+
+def pin_kquant_multiblock_rows(lib):
+    # for each of Q5_K, Q6_K, Q3_K: two rows of two super-blocks; block (r, b) has d = 2^(r+b)
+    # and every other field chosen so that each weight decodes to d
+    d_bits = {0: 0x3C00, 1: 0x4000, 2: 0x4400}
+    blocks = {
+        oracle.Q5_K: lambda db: golden.q5_k_block(db, 0, [1] * 8, [0] * 8, [1] * 256),
+        oracle.Q6_K: lambda db: golden.q6_k_block(db, [1] * 16, [1] * 256),
+        oracle.Q3_K: lambda db: golden.q3_k_block(db, [1] * 16, [1] * 256),
+    }
+    for qtype, make in blocks.items():
+        data = b"".join(make(d_bits[r + b]) for r in range(2) for b in range(2))
+        assert len(data) == 2 * oracle.row_bytes(qtype, 512)
+        got = oracle.dequant(qtype, np.frombuffer(data, np.uint8), 2, 512, lib=lib)
+        for r in range(2):
+            for b in range(2):
+                assert np.all(got[r, 256 * b:256 * (b + 1)] == 2.0 ** (r + b)), (qtype, r, b)
+
+
 def test_half_to_double(olib):
     pin_half_to_double(olib)
 
@@ -80,6 +120,22 @@ def test_q4_k_multiblock_rows(olib):
     pin_q4_k_multiblock_rows(olib)
 
 
+def test_q5_k_handbuilt(olib):
+    pin_q5_k_handbuilt(olib)
+
+
+def test_q6_k_handbuilt(olib):
+    pin_q6_k_handbuilt(olib)
+
+
+def test_q3_k_handbuilt(olib):
+    pin_q3_k_handbuilt(olib)
+
+
+def test_kquant_multiblock_rows(olib):
+    pin_kquant_multiblock_rows(olib)
+
+
 def test_synth_packer_matches_handbuilt_packer():
     """The synthetic-input encoder lays out bytes exactly as the hand packer."""
     rng = np.random.default_rng(1)
@@ -91,6 +147,48 @@ def test_synth_packer_matches_handbuilt_packer():
         got = synth.pack_q4_k(torch.tensor(1.0), torch.tensor(0.5), torch.tensor(sc),
                               torch.tensor(m), torch.tensor(q)).numpy().tobytes()
         assert got == ref
+
+
+def test_synth_kquant_packers_match_handbuilt_packers():
+    """The Q5_K, Q6_K and Q3_K encoders of the synthetic inputs lay out bytes exactly as the
+    hand packers (written separately, byte by byte) on random fields."""
+    rng = np.random.default_rng(2)
+    one, half = torch.tensor(1.0), torch.tensor(0.5)
+    for _ in range(20):
+        sc8 = rng.integers(0, 64, 8).tolist()
+        m8 = rng.integers(0, 64, 8).tolist()
+        q5 = rng.integers(0, 32, 256).tolist()
+        ref = golden.q5_k_block(0x3C00, 0x3800, sc8, m8, q5)
+        got = synth.pack_q5_k(one, half, torch.tensor(sc8), torch.tensor(m8), torch.tensor(q5))
+        assert got.numpy().tobytes() == ref
+        s6 = rng.integers(-128, 128, 16).tolist()
+        q6 = rng.integers(-32, 32, 256).tolist()
+        ref = golden.q6_k_block(0x3800, s6, q6)
+        assert synth.pack_q6_k(half, torch.tensor(s6), torch.tensor(q6)).numpy().tobytes() == ref
+        s3 = rng.integers(-32, 32, 16).tolist()
+        q3 = rng.integers(-4, 4, 256).tolist()
+        ref = golden.q3_k_block(0x3C00, s3, q3)
+        assert synth.pack_q3_k(one, torch.tensor(s3), torch.tensor(q3)).numpy().tobytes() == ref
+
+
+def test_synth_kquant_encoders_round_trip(olib):
+    """Encoded Q5_K / Q6_K / Q3_K blocks decode (oracle) close to the source weights.  The
+    bounds are the quantizers' own: half a step per weight plus the rounding of the group
+    scales, which for N(0, 0.02) weights gives these relative L2 errors with margin."""
+    w = synth.normal((16, 1024), 0.02, 321)
+    ref = w.double().numpy()
+    for qt, oq, rel_max in ((synth.Q5_K, oracle.Q5_K, 0.06), (synth.Q6_K, oracle.Q6_K, 0.04),
+                            (synth.Q3_K, oracle.Q3_K, 0.25)):
+        blk = synth.encode(qt, w).numpy()
+        assert blk.shape == (16, oracle.row_bytes(oq, 1024))
+        deq = oracle.dequant(oq, blk, 16, 1024, lib=olib)
+        rel = np.linalg.norm(deq - ref) / np.linalg.norm(ref)
+        assert rel < rel_max, (qt, rel)
+    # more bits, less error: Q6_K < Q5_K < Q4_K < Q3_K on the same weights
+    errs = [np.linalg.norm(oracle.dequant(oq, synth.encode(qt, w).numpy(), 16, 1024, lib=olib) - ref)
+            for qt, oq in ((synth.Q6_K, oracle.Q6_K), (synth.Q5_K, oracle.Q5_K), (synth.Q4_K, oracle.Q4_K),
+                           (synth.Q3_K, oracle.Q3_K))]
+    assert errs == sorted(errs), errs
 
 
 def test_synth_encoders_round_trip(olib):
@@ -293,6 +391,38 @@ def test_ffn_identity(olib):
     pin_ffn_identity(olib)
 
 
+def pin_ffn_identity_kquants(lib):
+    # the identity expert stored as Q5_K, Q6_K and Q3_K (n = 512: two super-blocks a row):
+    # every weight decodes to 0 except a 1 on the diagonal, so h = y = silu(x) * x
+    n = 512
+    x = np.linspace(-3.0, 3.0, n)
+    silu_x = x / (1.0 + np.exp(-x))
+
+    def eye(make):
+        rows = []
+        for i in range(n):
+            q = [0] * n
+            q[i] = 1
+            rows.append(b"".join(make(q[256 * b:256 * (b + 1)]) for b in range(n // 256)))
+        return np.frombuffer(b"".join(rows), np.uint8)
+
+    makers = {
+        oracle.Q5_K: lambda q: golden.q5_k_block(0x3C00, 0, [1] * 8, [0] * 8, q),
+        oracle.Q6_K: lambda q: golden.q6_k_block(0x3C00, [1] * 16, q),
+        oracle.Q3_K: lambda q: golden.q3_k_block(0x3C00, [1] * 16, q),
+    }
+    for qtype, make in makers.items():
+        m = eye(make)
+        assert m.size == n * oracle.row_bytes(qtype, n)
+        y, h = oracle.expert_ffn(qtype, m, m, m, n, n, x, lib=lib)
+        assert np.allclose(h, silu_x * x, rtol=1e-15, atol=1e-300), qtype
+        assert np.allclose(y, silu_x * x, rtol=1e-15, atol=1e-300), qtype
+
+
+def test_ffn_identity_kquants(olib):
+    pin_ffn_identity_kquants(olib)
+
+
 def _tiny_spec(seed=0, shared=False, mode=oracle.ROUTE_SOFTMAX, E=8, k=2, H=256, I=128, G=1, Gk=1,
                identical=False):
     qt = synth.Q8_0
@@ -463,6 +593,10 @@ PINS = {
     "q8_0_handbuilt": pin_q8_0_handbuilt,
     "q4_k_handbuilt": pin_q4_k_handbuilt,
     "q4_k_multiblock_rows": pin_q4_k_multiblock_rows,
+    "q5_k_handbuilt": pin_q5_k_handbuilt,
+    "q6_k_handbuilt": pin_q6_k_handbuilt,
+    "q3_k_handbuilt": pin_q3_k_handbuilt,
+    "kquant_multiblock_rows": pin_kquant_multiblock_rows,
     "router_integer": pin_router_integer,
     "softmax_topk_bruteforce": pin_softmax_topk_bruteforce,
     "softmax_special": pin_softmax_special,
@@ -470,6 +604,7 @@ PINS = {
     "sigmoid_group_special": pin_sigmoid_group_special,
     "permute_bruteforce": pin_permute_bruteforce,
     "ffn_identity": pin_ffn_identity,
+    "ffn_identity_kquants": pin_ffn_identity_kquants,
     "dense_masked_equals_sparse": pin_dense_masked_equals_sparse,
     "identical_experts_ignore_routing": pin_identical_experts_ignore_routing,
     "token_permutation": pin_token_permutation,
