@@ -246,6 +246,7 @@ moe_status moe_layer_path(const moe_layer_plan* plan, int T, int* path);
  * grouped GEMM (fp16 operands, fp32 accumulate; the per-pair down outputs
  * are rounded to fp16 before the fp32 combine).  out may alias x when
  * accumulate = 1 (a residual block): x is read before out is written.
+ * T = 0 is a no-op that launches nothing (x, out and workspace may be NULL).
  */
 moe_status moe_layer(const moe_layer_plan* plan, const void* x, int T, float* out, void* workspace,
                      size_t ws_bytes, moe_stream_t stream);

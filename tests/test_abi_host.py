@@ -81,6 +81,8 @@ def test_plan_validation():
             assert moe.moe_layer_workspace_size(plan, T) > 0
         assert moe.moe_layer_workspace_size(plan, 4096) > moe.moe_layer_workspace_size(plan, 1)
         _expect(N.MOE_ERR_WORKSPACE, moe.moe_layer, plan, FAKE, 4, FAKE, FAKE, 16, 0)
+        moe.moe_layer(plan, None, 0, None, None, 0, 0)     # T = 0: a no-op, nothing launched
+        _expect(N.MOE_ERR_INVALID_ARG, moe.moe_layer, plan, FAKE, -1, FAKE, FAKE, 1 << 30, 0)
         _expect(N.MOE_ERR_INVALID_ARG, moe.moe_layer, plan, FAKE + 8, 4, FAKE, FAKE, 1 << 30, 0)
     finally:
         moe.moe_layer_plan_destroy(plan)
