@@ -243,14 +243,17 @@ def algorithmic_bytes(shape, T, offsets_host):
 
 
 def launches_per_layer(shape, T, stack=False, path=None):
+    """Kernel launches of one moe_layer call on the given path (the library's own launch order)."""
     P = T * shape.k
     if path == "decode_chain":
         return 3                                     # logits (+ RMSNorm), routing + gate/up, down + combine
     n = 2 + (1 if P <= 1024 else 2) + 2 + 1          # logits, top-k, permute, gate/up, down, combine
-    if T >= 128:
+    if path == "tensor":
         n += 2                                       # fp16 copy of x, token-block list
+        if shape.x_dtype == "bf16" and T > 32 and shape.H % 64 == 0 and shape.E % 4 == 0 and shape.E <= 1024:
+            n += 1                                   # router logits on tcgen05: W_r split into bf16 parts first
     if shape.I_s > 0:
-        n += 2
+        n += 2                                       # the shared expert's gate/up and down
     return n + (1 if stack else 0)                   # the layer's own RMSNorm launch in the stack
 
 

@@ -77,3 +77,38 @@ def test_clock_samples_inside_the_timed_region(bench):
     s_all = mod.summarize_clocks(rows, t1 + 10.0, t1 + 11.0)
     assert s_all["samples"] == 4 and "hw_slowdown" in s_all["reasons"] and s_all["window"].startswith("whole run")
     assert mod.summarize_clocks([], None, None) is None
+
+
+def test_launch_count_per_layer(bench):
+    mod, _ = bench
+    import synth
+    # the three chained decode kernels
+    assert mod.launches_per_layer(synth.DECODE, 1, path="decode_chain") == 3
+    # prefill T=4096, as listed by ncu: router split, router logits, top-k, permute (two
+    # launches above 1024 pairs), fp16 copy of x, token-block list, gate/up, down, combine
+    assert mod.launches_per_layer(synth.DECODE, 4096, path="tensor") == 10
+    # stack at T=64 on the GEMV path: RMSNorm, logits, top-k, permute, gate/up, down, combine
+    assert mod.launches_per_layer(synth.DECODE, 64, stack=True, path="gemv") == 7
+    # DeepSeek-shaped T=2 on the GEMV path: + the shared expert's gate/up and down
+    assert mod.launches_per_layer(synth.DEEPSEEK, 2, path="gemv") == 8
+    # DeepSeek-shaped T=512 on the tensor cores: 4096 pairs, router on tcgen05, shared expert
+    assert mod.launches_per_layer(synth.DEEPSEEK, 512, path="tensor") == 12
+
+
+def test_algorithmic_bytes_of_the_decode_layer(bench):
+    mod, _ = bench
+    import numpy as np
+    import synth
+    # T = 1 with 8 distinct experts: 8 x 2,654,208 B of Q4_K rows, the fp32 router (1 MiB),
+    # the bf16 token in and the fp32 row out
+    offs = np.array([0] * 5 + list(range(1, 9)) + [8] * 116)
+    assert len(offs) == 129
+    total, gu, u = mod.algorithmic_bytes(synth.DECODE, 1, offs)
+    assert u == 8
+    assert synth.bytes_per_expert(synth.DECODE) == 2654208
+    assert total == 8 * 2654208 + 128 * 2048 * 4 + 2048 * 2 + 2048 * 4
+    # gate/up: 2 x 768 rows of 8 Q4_K blocks per chosen expert, the token, and h (fp32, k x I)
+    assert gu == 8 * 2 * 768 * 8 * 144 + 2048 * 2 + 8 * 768 * 4
+    # the DeepSeek-shaped layer: a routed expert of 24,772,608 B, a Q8_0 shared expert of 46.8 MB
+    assert synth.bytes_per_expert(synth.DEEPSEEK) == 24772608
+    assert synth.shared_bytes(synth.DEEPSEEK) == 46792704
