@@ -60,6 +60,7 @@ class _Layer(ctypes.Structure):
         ("Wr", ctypes.c_void_p), ("bias", ctypes.c_void_p),
         ("shared_qtype", ctypes.c_int), ("I_s", ctypes.c_int),
         ("s_gate", ctypes.c_void_p), ("s_up", ctypes.c_void_p), ("s_down", ctypes.c_void_p),
+        ("qtype_down", ctypes.c_int),
     ]
 
 
@@ -88,6 +89,8 @@ def _declare(lib):
     lib.oracle_permute.restype = I32
     lib.oracle_expert_ffn.argtypes = [I32, P, P, P, I32, I32, P, P, P]
     lib.oracle_expert_ffn.restype = I32
+    lib.oracle_expert_ffn_mixed.argtypes = [I32, I32, P, P, P, I32, I32, P, P, P]
+    lib.oracle_expert_ffn_mixed.restype = I32
     lib.oracle_moe_layer.argtypes = [ctypes.POINTER(_Layer), P, I32, P, P, P, P, P, P, I32]
     lib.oracle_moe_layer.restype = I32
     lib.oracle_rmsnorm.argtypes = [P, I32, I32, P, D, P]
@@ -179,14 +182,19 @@ def permute(ids, E: int, lib=None):
     return sp, off, pp
 
 
-def expert_ffn(qtype: int, gate, up, down, H: int, I: int, x, lib=None):
-    """One SwiGLU expert on one token; returns (y [H], h [I])."""
+def expert_ffn(qtype: int, gate, up, down, H: int, I: int, x, lib=None, qtype_down: int | None = None):
+    """One SwiGLU expert on one token; returns (y [H], h [I]).  qtype_down (default: qtype)
+    is the type of the down matrix when it differs from gate and up."""
     gate, up, down = _u8(gate), _u8(up), _u8(down)
     x = _f64(x)
     y = np.empty(H, dtype=np.float64)
     h = np.empty(I, dtype=np.float64)
-    rc = (lib or load()).oracle_expert_ffn(qtype, _ptr(gate), _ptr(up), _ptr(down), H, I,
-                                           _ptr(x), _ptr(y), _ptr(h))
+    lib = lib or load()
+    if qtype_down is None:
+        rc = lib.oracle_expert_ffn(qtype, _ptr(gate), _ptr(up), _ptr(down), H, I, _ptr(x), _ptr(y), _ptr(h))
+    else:
+        rc = lib.oracle_expert_ffn_mixed(qtype, qtype_down, _ptr(gate), _ptr(up), _ptr(down), H, I,
+                                         _ptr(x), _ptr(y), _ptr(h))
     assert rc == 0
     return y, h
 
@@ -194,14 +202,15 @@ def expert_ffn(qtype: int, gate, up, down, H: int, I: int, x, lib=None):
 class LayerSpec:
     """Host-side description of one MoE layer's stored tensors (numpy arrays).
 
-    gate/up: uint8 [E, I, row_bytes(H)]; down: uint8 [E, H, row_bytes(I)];
-    Wr fp32 [E, H]; bias fp32 [E] or None; shared_* uint8 or None.
+    gate/up: uint8 [E, I, row_bytes(H)] in qtype; down: uint8 [E, H, row_bytes(I)] in
+    qtype_down (default: qtype); Wr fp32 [E, H]; bias fp32 [E] or None; shared_* uint8 or None.
     """
 
     def __init__(self, *, mode, E, k, H, I, qtype, gate, up, down, Wr, bias=None,
                  n_groups=1, topk_groups=1, renormalize=True, scale=1.0,
-                 shared_qtype=Q8_0, I_s=0, s_gate=None, s_up=None, s_down=None):
+                 shared_qtype=Q8_0, I_s=0, s_gate=None, s_up=None, s_down=None, qtype_down=None):
         self.mode, self.E, self.k, self.H, self.I, self.qtype = mode, E, k, H, I, qtype
+        self.qtype_down = qtype if qtype_down is None else qtype_down
         self.gate, self.up, self.down = _u8(gate), _u8(up), _u8(down)
         self.Wr = np.ascontiguousarray(Wr, dtype=np.float32)
         self.bias = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
@@ -219,10 +228,11 @@ class LayerSpec:
             scale=float(self.scale), H=self.H, I=self.I, qtype=self.qtype,
             gate=_ptr(self.gate), up=_ptr(self.up), down=_ptr(self.down),
             expert_stride_gu=self.I * row_bytes(self.qtype, self.H),
-            expert_stride_d=self.H * row_bytes(self.qtype, self.I),
+            expert_stride_d=self.H * row_bytes(self.qtype_down, self.I),
             Wr=_ptr(self.Wr), bias=_ptr(self.bias),
             shared_qtype=self.shared_qtype, I_s=self.I_s,
             s_gate=_ptr(self.s_gate), s_up=_ptr(self.s_up), s_down=_ptr(self.s_down),
+            qtype_down=self.qtype_down,
         )
 
 

@@ -485,24 +485,27 @@ int oracle_permute(const int32_t* ids, int T, int k, int E,
 /* ------------------------------------------------------------------ */
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 
-int oracle_expert_ffn(int qtype, const uint8_t* gate, const uint8_t* up, const uint8_t* down,
-                      int H, int I, const double* x, double* y, double* hout)
+/* gate and up stored as qtype_gu, down as qtype_d (a file may mix them,
+ * e.g. 3-bit gate/up with 4-bit down).                                  */
+int oracle_expert_ffn_mixed(int qtype_gu, int qtype_d, const uint8_t* gate, const uint8_t* up,
+                            const uint8_t* down, int H, int I, const double* x, double* y,
+                            double* hout)
 {
-    int64_t rb_in = row_bytes(qtype, H), rb_mid = row_bytes(qtype, I);
+    int64_t rb_in = row_bytes(qtype_gu, H), rb_mid = row_bytes(qtype_d, I);
     if (rb_in < 0 || rb_mid < 0) return -1;
     double* wrow = (double*)malloc(sizeof(double) * (size_t)(H > I ? H : I));
     double* h = (double*)malloc(sizeof(double) * (size_t)I);
     for (int i = 0; i < I; ++i) {
         double g = 0.0, u = 0.0;
-        oracle_dequant_matrix(qtype, gate + (int64_t)i * rb_in, 1, H, wrow);
+        oracle_dequant_matrix(qtype_gu, gate + (int64_t)i * rb_in, 1, H, wrow);
         for (int c = 0; c < H; ++c) g += wrow[c] * x[c];
-        oracle_dequant_matrix(qtype, up + (int64_t)i * rb_in, 1, H, wrow);
+        oracle_dequant_matrix(qtype_gu, up + (int64_t)i * rb_in, 1, H, wrow);
         for (int c = 0; c < H; ++c) u += wrow[c] * x[c];
         h[i] = silu(g) * u;
     }
     for (int n = 0; n < H; ++n) {
         double acc = 0.0;
-        oracle_dequant_matrix(qtype, down + (int64_t)n * rb_mid, 1, I, wrow);
+        oracle_dequant_matrix(qtype_d, down + (int64_t)n * rb_mid, 1, I, wrow);
         for (int i = 0; i < I; ++i) acc += wrow[i] * h[i];
         y[n] = acc;
     }
@@ -510,6 +513,12 @@ int oracle_expert_ffn(int qtype, const uint8_t* gate, const uint8_t* up, const u
     free(wrow);
     free(h);
     return 0;
+}
+
+int oracle_expert_ffn(int qtype, const uint8_t* gate, const uint8_t* up, const uint8_t* down,
+                      int H, int I, const double* x, double* y, double* hout)
+{
+    return oracle_expert_ffn_mixed(qtype, qtype, gate, up, down, H, I, x, y, hout);
 }
 
 /* ------------------------------------------------------------------ */
@@ -520,7 +529,7 @@ typedef struct {
     int E, k, n_groups, topk_groups, renormalize;
     double scale;
     int H, I;
-    int qtype;             /* routed experts */
+    int qtype;             /* routed experts' gate and up */
     const uint8_t* gate;   /* expert e at gate + e*expert_stride_gu */
     const uint8_t* up;
     const uint8_t* down;   /* expert e at down + e*expert_stride_d */
@@ -532,6 +541,7 @@ typedef struct {
     const uint8_t* s_gate;
     const uint8_t* s_up;
     const uint8_t* s_down;
+    int qtype_down;        /* routed experts' down (may differ from qtype) */
 } oracle_layer;
 
 /* out[T][H] = combine of the routed experts (+ shared) for the T tokens.
@@ -561,10 +571,11 @@ int oracle_moe_layer(const oracle_layer* L, const double* x, int T, const double
     for (int64_t p = 0; p < P; ++p) {
         int t = (int)(p / k);
         int e = ids[p];
-        oracle_expert_ffn(L->qtype, L->gate + (int64_t)e * L->expert_stride_gu,
-                          L->up + (int64_t)e * L->expert_stride_gu,
-                          L->down + (int64_t)e * L->expert_stride_d, H, L->I,
-                          x + (int64_t)t * H, y + p * H, NULL);
+        oracle_expert_ffn_mixed(L->qtype, L->qtype_down,
+                                L->gate + (int64_t)e * L->expert_stride_gu,
+                                L->up + (int64_t)e * L->expert_stride_gu,
+                                L->down + (int64_t)e * L->expert_stride_d, H, L->I,
+                                x + (int64_t)t * H, y + p * H, NULL);
     }
 #ifdef _OPENMP
 #pragma omp parallel for schedule(dynamic, 1) if (n_threads > 1)

@@ -53,6 +53,12 @@ MUTANTS = [
     ("q3k_block_stride", "row + b * 110", "row + b * 108", ["kquant_multiblock_rows"]),
     ("q6k_row_bytes", "return K / 256 * 210;", "return K / 256 * 208;",
      ["kquant_multiblock_rows", "ffn_identity_kquants"]),
+    ("ffn_down_decoded_as_gate_type", "oracle_dequant_matrix(qtype_d, down", "oracle_dequant_matrix(qtype_gu, down",
+     ["ffn_mixed_types", "layer_mixed_types"]),
+    ("ffn_down_rows_of_gate_type", "rb_mid = row_bytes(qtype_d, I)", "rb_mid = row_bytes(qtype_gu, I)",
+     ["ffn_mixed_types"]),
+    ("layer_down_type_ignored", "oracle_expert_ffn_mixed(L->qtype, L->qtype_down,",
+     "oracle_expert_ffn_mixed(L->qtype, L->qtype,", ["layer_mixed_types"]),
     ("router_transposed", "(double)Wr[(int64_t)e * H + h]", "(double)Wr[(int64_t)h * E + e]",
      ["router_integer"]),
     ("topk_smallest", "if (sa != sb) return sa > sb;", "if (sa != sb) return sa < sb;",

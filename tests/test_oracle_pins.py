@@ -423,6 +423,60 @@ def test_ffn_identity_kquants(olib):
     pin_ffn_identity_kquants(olib)
 
 
+def _eye_blocks(n: int, make) -> np.ndarray:
+    """The n x n identity stored as 256-weight blocks built by make(q[256])."""
+    rows = []
+    for i in range(n):
+        q = [0] * n
+        q[i] = 1
+        rows.append(b"".join(make(q[256 * b:256 * (b + 1)]) for b in range(n // 256)))
+    return np.stack([np.frombuffer(r, np.uint8) for r in rows])
+
+
+def pin_ffn_mixed_types(lib):
+    # gate/up and down stored in different types: identity gate/up, down = c * identity
+    n = 256
+    x = np.linspace(-3.0, 3.0, n)
+    sx = x / (1.0 + np.exp(-x)) * x
+    eye3 = _eye_blocks(n, lambda q: golden.q3_k_block(0x3C00, [1] * 16, q))
+    down8 = _identity_q8_0(n, 0x4000)                                   # 2 * identity, Q8_0
+    y, h = oracle.expert_ffn(oracle.Q3_K, eye3, eye3, down8, n, n, x, lib=lib, qtype_down=oracle.Q8_0)
+    assert np.allclose(h, sx, rtol=1e-15, atol=1e-300)
+    assert np.allclose(y, 2 * sx, rtol=1e-15, atol=1e-300)
+    eye8 = _identity_q8_0(n)
+    down6 = _eye_blocks(n, lambda q: golden.q6_k_block(0x4200, [1] * 16, q))   # 3 * identity, Q6_K
+    y, _ = oracle.expert_ffn(oracle.Q8_0, eye8, eye8, down6, n, n, x, lib=lib, qtype_down=oracle.Q6_K)
+    assert np.allclose(y, 3 * sx, rtol=1e-15, atol=1e-300)
+
+
+def test_ffn_mixed_types(olib):
+    pin_ffn_mixed_types(olib)
+
+
+def pin_layer_mixed_types(lib):
+    # E = 4 experts with Q3_K identity gate/up and Q4_K down = 2^e * identity; the logits are
+    # given (0, 1, 2, 3 for every token), so top-2 = {2, 3} with softmax gates over (2, 3):
+    # out = (4 g_2 + 8 g_3) * silu(x) x
+    n, E = 256, 4
+    eye3 = _eye_blocks(n, lambda q: golden.q3_k_block(0x3C00, [1] * 16, q))
+    d_bits = [0x3C00, 0x4000, 0x4400, 0x4800]                          # 1, 2, 4, 8
+    downs = [_eye_blocks(n, lambda q, db=db: golden.q4_k_block(db, 0, [1] * 8, [0] * 8, q)) for db in d_bits]
+    spec = oracle.LayerSpec(mode=oracle.ROUTE_SOFTMAX, E=E, k=2, H=n, I=n, qtype=oracle.Q3_K,
+                            qtype_down=oracle.Q4_K, gate=np.stack([eye3] * E), up=np.stack([eye3] * E),
+                            down=np.stack(downs), Wr=np.zeros((E, n), np.float32))
+    x = np.stack([np.linspace(-3.0, 3.0, n), np.linspace(2.0, -1.0, n)])
+    logits = np.tile(np.arange(E, dtype=np.float64), (2, 1))
+    res = oracle.moe_layer(spec, x, logits=logits, lib=lib)
+    assert np.array_equal(res["ids"], [[2, 3], [2, 3]])
+    g2, g3 = np.exp(2.0) / (np.exp(2.0) + np.exp(3.0)), np.exp(3.0) / (np.exp(2.0) + np.exp(3.0))
+    expect = (4 * g2 + 8 * g3) * (x / (1.0 + np.exp(-x)) * x)
+    assert np.allclose(res["out"], expect, rtol=1e-13, atol=1e-300)
+
+
+def test_layer_mixed_types(olib):
+    pin_layer_mixed_types(olib)
+
+
 def _tiny_spec(seed=0, shared=False, mode=oracle.ROUTE_SOFTMAX, E=8, k=2, H=256, I=128, G=1, Gk=1,
                identical=False):
     qt = synth.Q8_0
@@ -605,6 +659,8 @@ PINS = {
     "permute_bruteforce": pin_permute_bruteforce,
     "ffn_identity": pin_ffn_identity,
     "ffn_identity_kquants": pin_ffn_identity_kquants,
+    "ffn_mixed_types": pin_ffn_mixed_types,
+    "layer_mixed_types": pin_layer_mixed_types,
     "dense_masked_equals_sparse": pin_dense_masked_equals_sparse,
     "identical_experts_ignore_routing": pin_identical_experts_ignore_routing,
     "token_permutation": pin_token_permutation,
