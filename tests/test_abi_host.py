@@ -2,7 +2,6 @@
 and rejects invalid arguments on the host before any launch (no GPU needed)."""
 from __future__ import annotations
 
-import ctypes
 import re
 
 import pytest
