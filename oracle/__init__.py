@@ -30,6 +30,7 @@ Q4_K = 3
 Q5_K = 4
 Q6_K = 5
 Q3_K = 6
+MXFP4 = 7
 ROUTE_SOFTMAX = 0
 ROUTE_SIGMOID_GROUP = 1
 
@@ -79,6 +80,8 @@ def _declare(lib):
     P, I64, I32, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
     lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
     lib.oracle_half_to_double.restype = D
+    lib.oracle_e2m1_to_double.argtypes = [I32]
+    lib.oracle_e2m1_to_double.restype = D
     lib.oracle_dequant_matrix.argtypes = [I32, P, I64, I64, P]
     lib.oracle_dequant_matrix.restype = I32
     lib.oracle_router_logits.argtypes = [P, I32, I32, P, I32, P]
@@ -119,7 +122,8 @@ def _u8(a) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(a, dtype=np.uint8))
 
 
-_BLOCK = {Q8_0: (32, 34), Q4_K: (256, 144), Q5_K: (256, 176), Q6_K: (256, 210), Q3_K: (256, 110)}
+_BLOCK = {Q8_0: (32, 34), Q4_K: (256, 144), Q5_K: (256, 176), Q6_K: (256, 210), Q3_K: (256, 110),
+          MXFP4: (32, 17)}
 
 
 def row_bytes(qtype: int, K: int) -> int:
@@ -131,6 +135,10 @@ def row_bytes(qtype: int, K: int) -> int:
 
 def half_to_double(bits: int, lib=None) -> float:
     return (lib or load()).oracle_half_to_double(int(bits))
+
+
+def e2m1_to_double(nibble: int, lib=None) -> float:
+    return (lib or load()).oracle_e2m1_to_double(int(nibble))
 
 
 def dequant(qtype: int, data, rows: int, K: int, lib=None) -> np.ndarray:

@@ -40,9 +40,11 @@
  *   Q3_K: 110 bytes per 256: high-bit mask, 2-bit low parts, 16 packed
  *         6-bit scales stored plus 32, fp16 d last; w = d*(sc - 32)*q with
  *         q = low - 4 where the high bit is clear.
- * Q5_K, Q6_K and Q3_K are the next expert types the pages list for the card
- * (Q4_K to Q6_K, and the Q3_K_M files the large model ships in); only the
- * oracle decodes them so far.
+ *   MXFP4: 17 bytes per 32: an E8M0 scale byte, then 16 bytes of E2M1
+ *         nibbles (OCP Microscaling formats); w = 2^(e-127) * e2m1(q).
+ * Q5_K, Q6_K, Q3_K and MXFP4 are the next expert types the pages list for
+ * the card (Q4_K to Q6_K, the Q3_K_M files the large model ships in, and
+ * MXFP4); only the oracle decodes them so far.
  *
  * Every value is computed in fp64.  Weight matrices are [rows][K/blk blocks],
  * blocks along the input dimension K; experts are laid out one after another
@@ -50,7 +52,8 @@
  *
  * Parity status of each function (pins live in the test suite):
  *   half_to_double, dequant Q8_0 / Q4_K /
- *   Q5_K / Q6_K / Q3_K                    pinned (hand-built blocks)
+ *   Q5_K / Q6_K / Q3_K / MXFP4            pinned (hand-built blocks; E2M1
+ *                                         against the format's value list)
  *   router logits                         pinned (integer closed form)
  *   top-k softmax / sigmoid-group         pinned (brute force, special cases)
  *   permute                               pinned (brute force)
@@ -71,6 +74,7 @@
 #define ORACLE_Q5_K 4
 #define ORACLE_Q6_K 5
 #define ORACLE_Q3_K 6
+#define ORACLE_MXFP4 7
 
 #define ORACLE_ROUTE_SOFTMAX 0
 #define ORACLE_ROUTE_SIGMOID_GROUP 1
@@ -180,8 +184,8 @@ void oracle_dequant_q5_k_row(const uint8_t* row, int64_t K, double* w)
                 int byte = Q[32 * c + i];
                 int lo = (j % 2 == 0) ? (byte & 15) : (byte >> 4);
                 int hi = (QH[i] >> j) & 1;
-                int q = lo + 16 * hi;
-                w[b * 256 + 32 * j + i] = d * (double)sc * (double)q - dmin * (double)m;
+                double qv = (double)(lo + 16 * hi);
+                w[b * 256 + 32 * j + i] = d * (double)sc * qv - dmin * (double)m;
             }
         }
     }
@@ -252,6 +256,34 @@ void oracle_dequant_q3_k_row(const uint8_t* row, int64_t K, double* w)
     }
 }
 
+/* FP4 E2M1 (OCP Microscaling formats): sign bit 3, exponent bits 2-1 with
+ * bias 1, mantissa bit 0; exponent 0 is subnormal (m * 0.5), otherwise
+ * (1 + m/2) * 2^(exp - 1).  No infinities or NaNs.                      */
+double oracle_e2m1_to_double(int nibble)
+{
+    int sign = (nibble >> 3) & 1;
+    int expo = (nibble >> 1) & 3;
+    int man = nibble & 1;
+    double mag = (expo == 0) ? 0.5 * (double)man : ldexp(1.0 + 0.5 * (double)man, expo - 1);
+    return sign ? -mag : mag;
+}
+
+/* MXFP4: 17 bytes per 32 weights: one E8M0 scale byte e (2^(e-127); 255 is
+ * NaN), then 16 bytes whose byte j holds element j in its low nibble and
+ * element j+16 in its high nibble, each an E2M1 value;  w = 2^(e-127) * v. */
+void oracle_dequant_mxfp4_row(const uint8_t* row, int64_t K, double* w)
+{
+    for (int64_t b = 0; b < K / 32; ++b) {
+        const uint8_t* blk = row + b * 17;
+        int e = blk[0];
+        double scale = (e == 255) ? NAN : ldexp(1.0, e - 127);
+        for (int j = 0; j < 16; ++j) {
+            w[b * 32 + j] = scale * oracle_e2m1_to_double(blk[1 + j] & 15);
+            w[b * 32 + j + 16] = scale * oracle_e2m1_to_double(blk[1 + j] >> 4);
+        }
+    }
+}
+
 static int64_t row_bytes(int qtype, int64_t K)
 {
     if (qtype == ORACLE_Q8_0) return K / 32 * 34;
@@ -259,6 +291,7 @@ static int64_t row_bytes(int qtype, int64_t K)
     if (qtype == ORACLE_Q5_K) return K / 256 * 176;
     if (qtype == ORACLE_Q6_K) return K / 256 * 210;
     if (qtype == ORACLE_Q3_K) return K / 256 * 110;
+    if (qtype == ORACLE_MXFP4) return K / 32 * 17;
     return -1;
 }
 
@@ -275,7 +308,8 @@ int oracle_dequant_matrix(int qtype, const uint8_t* data, int64_t rows, int64_t 
         case ORACLE_Q4_K: oracle_dequant_q4_k_row(src, K, dst); break;
         case ORACLE_Q5_K: oracle_dequant_q5_k_row(src, K, dst); break;
         case ORACLE_Q6_K: oracle_dequant_q6_k_row(src, K, dst); break;
-        default:          oracle_dequant_q3_k_row(src, K, dst); break;
+        case ORACLE_Q3_K: oracle_dequant_q3_k_row(src, K, dst); break;
+        default:          oracle_dequant_mxfp4_row(src, K, dst); break;
         }
     }
     return 0;

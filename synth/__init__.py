@@ -2,8 +2,8 @@
 
 This module draws the random tensors (activations, router weights, biases,
 RMSNorm weights, expert weights) and stores expert weights in the GGUF block
-layouts Q8_0 and Q4_K (and Q5_K, Q6_K, Q3_K, which only the oracle decodes
-so far).  It is shared by the tests, the benchmark and the
+layouts Q8_0 and Q4_K (and Q5_K, Q6_K, Q3_K and MXFP4, which only the
+oracle decodes so far).  It is shared by the tests, the benchmark and the
 smoke check, and it holds none of the layer's arithmetic: it never routes,
 never dequantizes and never evaluates an expert.  (Encoding a float matrix
 into blocks is how the stored inputs are made; decoding them is the oracle's
@@ -35,9 +35,11 @@ Q4_K = "q4_k"
 Q5_K = "q5_k"
 Q6_K = "q6_k"
 Q3_K = "q3_k"
+MXFP4 = "mxfp4"
 
 # weights and bytes per block of each stored type
-BLOCK = {Q8_0: (32, 34), Q4_K: (256, 144), Q5_K: (256, 176), Q6_K: (256, 210), Q3_K: (256, 110)}
+BLOCK = {Q8_0: (32, 34), Q4_K: (256, 144), Q5_K: (256, 176), Q6_K: (256, 210), Q3_K: (256, 110),
+         MXFP4: (32, 17)}
 
 TAGS = {"x": 1, "router": 2, "bias": 3, "gate": 4, "up": 5, "down": 6, "gamma": 7,
         "s_gate": 8, "s_up": 9, "s_down": 10, "zipf": 11, "fill": 12}
@@ -261,7 +263,34 @@ def encode_q3_k(w: torch.Tensor) -> torch.Tensor:
     return blocks.reshape(rows, K // 256 * 110).contiguous()
 
 
-_ENCODERS = {Q8_0: encode_q8_0, Q4_K: encode_q4_k, Q5_K: encode_q5_k, Q6_K: encode_q6_k, Q3_K: encode_q3_k}
+def pack_mxfp4(e: torch.Tensor, codes: torch.Tensor) -> torch.Tensor:
+    """Pack MXFP4 fields into 17-byte blocks: e [...] E8M0 scale bytes, codes [..., 32] E2M1
+    codes in [0, 15]; byte 1 + j holds codes[j] (low nibble) and codes[j + 16] (high)."""
+    c = codes.to(torch.int32)
+    qs = (c[..., :16] | (c[..., 16:] << 4)).to(torch.uint8)
+    return torch.cat([e.to(torch.int32).unsqueeze(-1).to(torch.uint8), qs], dim=-1)
+
+
+def encode_mxfp4(w: torch.Tensor) -> torch.Tensor:
+    """[rows, K] float -> [rows, K/32*17] uint8 MXFP4 blocks.  Per block of 32 the shared scale
+    is 2^(floor(log2 max|w|) - 2) (the largest E2M1 magnitude, 6, has exponent 2); each weight
+    takes the nearest E2M1 magnitude of w / scale (the lower one on a tie), clamped to 6."""
+    rows, K = w.shape
+    assert K % 32 == 0
+    b = w.reshape(rows, K // 32, 32).float()
+    amax = b.abs().amax(dim=-1)
+    E = torch.where(amax > 0, torch.floor(torch.log2(torch.where(amax > 0, amax, torch.ones_like(amax)))) - 2,
+                    torch.full_like(amax, -127.0)).clamp(-127, 127)
+    v = b / torch.exp2(E).unsqueeze(-1)
+    mags = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    idx = (v.abs().clamp(max=6.0).unsqueeze(-1) - mags).abs().argmin(dim=-1)
+    codes = torch.where((v < 0) & (idx > 0), idx + 8, idx)
+    blocks = pack_mxfp4((E + 127).to(torch.int32), codes)
+    return blocks.reshape(rows, K // 32 * 17).contiguous()
+
+
+_ENCODERS = {Q8_0: encode_q8_0, Q4_K: encode_q4_k, Q5_K: encode_q5_k, Q6_K: encode_q6_k, Q3_K: encode_q3_k,
+             MXFP4: encode_mxfp4}
 
 
 def encode(qtype: str, w: torch.Tensor) -> torch.Tensor:

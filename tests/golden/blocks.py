@@ -1,8 +1,8 @@
 """Hand-built GGUF blocks with values known in closed form.
 
 The bloomery pages name the block types the card experts use (Q4_K..Q6_K,
-Q8_0, and the Q3_K_M files of the large model: "bloomery README 0.3.1",
-Status table, "Quant types" row) but print no
+Q8_0, MXFP4, and the Q3_K_M files of the large model: "bloomery README
+0.3.1", Status table, "Quant types" row) but print no
 block bytes and no worked example.  These blocks are built by hand from the
 public GGUF layout, byte by byte, with a packer written here on its own (it
 shares nothing with the synthetic-input encoder or the oracle), so that the
@@ -258,6 +258,41 @@ def q3_k_cases():
     return cases
 
 
+# ---------------------------------------------------------------- MXFP4 (17 B / 32)
+
+# FP4 E2M1 magnitudes of codes 0..7, as listed by the OCP Microscaling formats specification;
+# codes 8..15 are the same magnitudes negated.
+E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def e2m1_value(code: int) -> float:
+    v = E2M1[code & 7]
+    return -v if code & 8 else v
+
+
+def mxfp4_block(e: int, codes: list[int]) -> bytes:
+    """One block: the E8M0 scale byte e, then byte j = codes[j] | codes[j + 16] << 4."""
+    assert 0 <= e < 256 and len(codes) == 32 and all(0 <= c < 16 for c in codes)
+    return bytes([e]) + bytes(codes[j] | (codes[j + 16] << 4) for j in range(16))
+
+
+def mxfp4_cases():
+    cases = {}
+    # every code once in each half, the second half reversed: element order is visible
+    codes = [i for i in range(16)] + [15 - i for i in range(16)]
+    vals = [e2m1_value(c) for c in codes]
+    cases["codes_scale1"] = (mxfp4_block(127, codes), vals)
+    cases["codes_scale8"] = (mxfp4_block(130, codes), [8.0 * v for v in vals])
+    cases["codes_scale_2^-27"] = (mxfp4_block(100, codes), [v * 2.0 ** -27 for v in vals])
+    cases["codes_min_scale"] = (mxfp4_block(0, codes), [v * 2.0 ** -127 for v in vals])
+    cases["codes_max_scale"] = (mxfp4_block(254, codes), [v * 2.0 ** 127 for v in vals])
+    # low and high nibbles of each byte differ: 0.5 in the first half, -6 in the second
+    cases["halves"] = (mxfp4_block(127, [1] * 16 + [15] * 16), [0.5] * 16 + [-6.0] * 16)
+    # e = 255 is not a number; every element decodes to NaN
+    cases["nan_scale"] = (mxfp4_block(255, codes), [float("nan")] * 32)
+    return cases
+
+
 BLOCK_TYPES = {
     # name -> (weights per block, bytes per block, cases)
     "Q8_0": (32, 34, q8_0_cases),
@@ -265,6 +300,7 @@ BLOCK_TYPES = {
     "Q5_K": (256, 176, q5_k_cases),
     "Q6_K": (256, 210, q6_k_cases),
     "Q3_K": (256, 110, q3_k_cases),
+    "MXFP4": (32, 17, mxfp4_cases),
 }
 
 

@@ -22,16 +22,20 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 MUTANTS = [
     ("fp16_exponent_bias", "expo - 15", "expo - 14", ["half_to_double", "q8_0_handbuilt"]),
     ("q8_0_unsigned", "if (q >= 128) q -= 256;", "", ["q8_0_handbuilt"]),
-    ("q4k_nibbles_swapped", "(j % 2 == 0) ? (byte & 15) : (byte >> 4)",
-     "(j % 2 == 1) ? (byte & 15) : (byte >> 4)", ["q4_k_handbuilt"]),
-    ("q4k_min_dropped", "- dmin * (double)m;", ";", ["q4_k_handbuilt"]),
-    ("q4k_min_sign", "- dmin * (double)m;", "+ dmin * (double)m;", ["q4_k_handbuilt"]),
+    ("q4k_nibbles_swapped", "int q = (j % 2 == 0) ? (byte & 15) : (byte >> 4)",
+     "int q = (j % 2 == 1) ? (byte & 15) : (byte >> 4)", ["q4_k_handbuilt"]),
+    ("q4k_min_dropped", "(double)q - dmin * (double)m;", "(double)q;", ["q4_k_handbuilt"]),
+    ("q4k_min_sign", "(double)q - dmin * (double)m;", "(double)q + dmin * (double)m;", ["q4_k_handbuilt"]),
     ("q4k_scale_high_bits", "((S[j - 4] >> 6) << 4)", "((S[j] >> 6) << 4)", ["q4_k_handbuilt"]),
     ("q4k_min_high_bits", "((S[j] >> 6) << 4);", "((S[j - 4] >> 6) << 4);", ["q4_k_handbuilt"]),
     ("q4k_block_stride", "row + b * 144", "row + b * 128", ["q4_k_multiblock_rows"]),
     ("q5k_fifth_bit_index", "int hi = (QH[i] >> j) & 1;", "int hi = (QH[i] >> (j / 2)) & 1;",
      ["q5_k_handbuilt"]),
-    ("q5k_fifth_bit_weight", "int q = lo + 16 * hi;", "int q = lo + 32 * hi;", ["q5_k_handbuilt"]),
+    ("q5k_fifth_bit_weight", "double qv = (double)(lo + 16 * hi);", "double qv = (double)(lo + 32 * hi);",
+     ["q5_k_handbuilt"]),
+    ("q5k_min_sign", "qv - dmin * (double)m;", "qv + dmin * (double)m;", ["q5_k_handbuilt"]),
+    ("q5k_nibbles_swapped", "int lo = (j % 2 == 0) ? (byte & 15) : (byte >> 4);",
+     "int lo = (j % 2 == 1) ? (byte & 15) : (byte >> 4);", ["q5_k_handbuilt"]),
     ("q5k_block_stride", "row + b * 176", "row + b * 160", ["kquant_multiblock_rows"]),
     ("q6k_offset", "int q = lo + 16 * hi - 32;", "int q = lo + 16 * hi - 31;", ["q6_k_handbuilt"]),
     ("q6k_quarter_nibble", "int lo = (r < 2) ? (byte & 15) : (byte >> 4);",
@@ -53,6 +57,16 @@ MUTANTS = [
     ("q3k_block_stride", "row + b * 110", "row + b * 108", ["kquant_multiblock_rows"]),
     ("q6k_row_bytes", "return K / 256 * 210;", "return K / 256 * 208;",
      ["kquant_multiblock_rows", "ffn_identity_kquants"]),
+    ("e2m1_sign_ignored", "return sign ? -mag : mag;", "return mag;", ["e2m1", "mxfp4_handbuilt"]),
+    ("e2m1_no_subnormal", "(expo == 0) ? 0.5 * (double)man :", "(expo == -1) ? 0.5 * (double)man :",
+     ["e2m1", "mxfp4_handbuilt"]),
+    ("e2m1_exponent_bias", "ldexp(1.0 + 0.5 * (double)man, expo - 1)", "ldexp(1.0 + 0.5 * (double)man, expo - 2)",
+     ["e2m1"]),
+    ("mxfp4_scale_bias", "ldexp(1.0, e - 127)", "ldexp(1.0, e - 128)", ["mxfp4_handbuilt"]),
+    ("mxfp4_nibble_halves_swapped", "oracle_e2m1_to_double(blk[1 + j] & 15);\n            w[b * 32 + j + 16]",
+     "oracle_e2m1_to_double(blk[1 + j] >> 4);\n            w[b * 32 + j + 16]", ["mxfp4_handbuilt"]),
+    ("mxfp4_nan_scale_finite", "(e == 255) ? NAN :", "(e == 256) ? NAN :", ["mxfp4_handbuilt"]),
+    ("mxfp4_block_stride", "row + b * 17;", "row + b * 16;", ["mxfp4_multiblock_rows"]),
     ("ffn_down_decoded_as_gate_type", "oracle_dequant_matrix(qtype_d, down", "oracle_dequant_matrix(qtype_gu, down",
      ["ffn_mixed_types", "layer_mixed_types"]),
     ("ffn_down_rows_of_gate_type", "rb_mid = row_bytes(qtype_d, I)", "rb_mid = row_bytes(qtype_gu, I)",
@@ -84,7 +98,7 @@ MUTANTS = [
 
 def _build_mutant(name, find, repl, tmp):
     src = open(SRC).read()
-    assert src.count(find) >= 1, f"mutation {name}: pattern not found"
+    assert src.count(find) == 1, f"mutation {name}: pattern must occur exactly once"
     mutated = src.replace(find, repl, 1)
     path = os.path.join(tmp, f"{name}.c")
     with open(path, "w") as f:

@@ -71,7 +71,7 @@ def _pin_handbuilt(lib, kind, qtype):
         assert len(blk) == nbytes, name
         assert fx[name] == blk, f"fixture {name} differs from the packer"
         got = oracle.dequant(qtype, np.frombuffer(blk, np.uint8), 1, weights, lib=lib)[0]
-        assert np.array_equal(got, np.array(expected)), name
+        assert np.array_equal(got, np.array(expected), equal_nan=True), name
 
 
 def pin_q5_k_handbuilt(lib):
@@ -84,6 +84,27 @@ def pin_q6_k_handbuilt(lib):
 
 def pin_q3_k_handbuilt(lib):
     _pin_handbuilt(lib, "Q3_K", oracle.Q3_K)
+
+
+def pin_e2m1(lib):
+    # the 16 FP4 E2M1 codes against the format's value list, signed zero included
+    for code in range(16):
+        got = oracle.e2m1_to_double(code, lib=lib)
+        assert got == golden.e2m1_value(code), code
+        assert np.signbit(got) == bool(code & 8), code
+
+
+def pin_mxfp4_handbuilt(lib):
+    _pin_handbuilt(lib, "MXFP4", oracle.MXFP4)
+
+
+def pin_mxfp4_multiblock_rows(lib):
+    # two rows of three blocks; block (r, b) has e = 127 + r + b and every code 2 (= 1.0)
+    data = b"".join(golden.mxfp4_block(127 + r + b, [2] * 32) for r in range(2) for b in range(3))
+    got = oracle.dequant(oracle.MXFP4, np.frombuffer(data, np.uint8), 2, 96, lib=lib)
+    for r in range(2):
+        for b in range(3):
+            assert np.all(got[r, 32 * b:32 * (b + 1)] == 2.0 ** (r + b)), (r, b)
 
 
 def pin_kquant_multiblock_rows(lib):
@@ -136,6 +157,18 @@ def test_kquant_multiblock_rows(olib):
     pin_kquant_multiblock_rows(olib)
 
 
+def test_e2m1(olib):
+    pin_e2m1(olib)
+
+
+def test_mxfp4_handbuilt(olib):
+    pin_mxfp4_handbuilt(olib)
+
+
+def test_mxfp4_multiblock_rows(olib):
+    pin_mxfp4_multiblock_rows(olib)
+
+
 def test_synth_packer_matches_handbuilt_packer():
     """The synthetic-input encoder lays out bytes exactly as the hand packer."""
     rng = np.random.default_rng(1)
@@ -169,6 +202,10 @@ def test_synth_kquant_packers_match_handbuilt_packers():
         q3 = rng.integers(-4, 4, 256).tolist()
         ref = golden.q3_k_block(0x3C00, s3, q3)
         assert synth.pack_q3_k(one, torch.tensor(s3), torch.tensor(q3)).numpy().tobytes() == ref
+        e = int(rng.integers(0, 256))
+        c4 = rng.integers(0, 16, 32).tolist()
+        ref = golden.mxfp4_block(e, c4)
+        assert synth.pack_mxfp4(torch.tensor(e), torch.tensor(c4)).numpy().tobytes() == ref
 
 
 def test_synth_kquant_encoders_round_trip(olib):
@@ -178,7 +215,7 @@ def test_synth_kquant_encoders_round_trip(olib):
     w = synth.normal((16, 1024), 0.02, 321)
     ref = w.double().numpy()
     for qt, oq, rel_max in ((synth.Q5_K, oracle.Q5_K, 0.06), (synth.Q6_K, oracle.Q6_K, 0.04),
-                            (synth.Q3_K, oracle.Q3_K, 0.25)):
+                            (synth.Q3_K, oracle.Q3_K, 0.25), (synth.MXFP4, oracle.MXFP4, 0.15)):
         blk = synth.encode(qt, w).numpy()
         assert blk.shape == (16, oracle.row_bytes(oq, 1024))
         deq = oracle.dequant(oq, blk, 16, 1024, lib=olib)
@@ -651,6 +688,9 @@ PINS = {
     "q6_k_handbuilt": pin_q6_k_handbuilt,
     "q3_k_handbuilt": pin_q3_k_handbuilt,
     "kquant_multiblock_rows": pin_kquant_multiblock_rows,
+    "e2m1": pin_e2m1,
+    "mxfp4_handbuilt": pin_mxfp4_handbuilt,
+    "mxfp4_multiblock_rows": pin_mxfp4_multiblock_rows,
     "router_integer": pin_router_integer,
     "softmax_topk_bruteforce": pin_softmax_topk_bruteforce,
     "softmax_special": pin_softmax_special,
