@@ -198,10 +198,11 @@ def job_tokens_per_s(world, T, L, steps, t_ms):
 
 # ------------------------------------------------------------------ workload construction
 
-def build_layers(shape, T, L, seed, device, shared_router=False, decode_chain=True):
+def build_layers(shape, T, L, seed, device, shared_router=False, decode_chain=True, tc_min_tokens=0):
     """L layers with distinct expert weights.  Router weights and biases are drawn on the
     CPU (small) so that a workload built around them (the Zipf prefill) sees the same values;
-    shared_router gives every layer layer 0's router."""
+    shared_router gives every layer layer 0's router.  tc_min_tokens (0: the library's
+    default) is the smallest T that takes the tensor-core path."""
     from quantized_routed_expert_sigmoid_gb300 import MoeLayer
     layers = []
     for l in range(L):
@@ -220,7 +221,8 @@ def build_layers(shape, T, L, seed, device, shared_router=False, decode_chain=Tr
                                topk_groups=shape.topk_groups, scale=shape.scale, renormalize=shape.renormalize,
                                x_dtype=shape.x_dtype, I_s=shape.I_s, shared_qtype=shape.shared_qtype,
                                s_gate=sh[0] if sh else None, s_up=sh[1] if sh else None,
-                               s_down=sh[2] if sh else None, decode_chain=decode_chain))
+                               s_down=sh[2] if sh else None, decode_chain=decode_chain,
+                               tc_min_tokens=tc_min_tokens))
     return layers
 
 
@@ -272,7 +274,7 @@ def run_ours(args, rank, world):
         L = args.layers
         desc = desc.replace("16 distinct layers", f"{L} distinct layers")
     layers = build_layers(shape, T, L, seed + 1000 * rank, device, shared_router=(args.workload == "prefill"),
-                          decode_chain=not args.separate_decode)
+                          decode_chain=not args.separate_decode, tc_min_tokens=args.tc_min_tokens)
     x = make_x(shape, T, seed + 1000 * rank, device, args.workload)
     outs = [torch.empty(T, shape.H, dtype=torch.float32, device=device) for _ in range(L)]
     for lay in layers:
@@ -452,7 +454,8 @@ def run_ours(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": desc, "T": T, "layers_per_step": L, "H": shape.H, "E": shape.E, "k": shape.k,
                    "I": shape.I, "qtype": shape.qtype, "l2": "inputs larger than L2 (distinct weights per layer)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU", "path": path},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU", "path": path,
+                   **({"tc_min_tokens": args.tc_min_tokens} if args.tc_min_tokens else {})},
         "layer": {"us_per_layer": round(layer_us, 3), "algorithmic_bytes": round(layer_bytes),
                   "GBps": round(layer_bytes / (layer_us * 1e-6) / 1e9, 1),
                   "frac_hbm": round(layer_bytes / (layer_us * 1e-6) / 1e9 / hbm_peak, 4),
@@ -623,6 +626,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="override the layers per step (default per workload)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (tokens per layer call)")
+    ap.add_argument("--tc-min-tokens", type=int, default=0,
+                    help="smallest T that takes the tensor-core path (default: the library's, 128)")
     ap.add_argument("--separate-decode", action="store_true",
                     help="decode sizes: run the separate route/permute/GEMV/combine kernels, not the single-launch layer")
     args = ap.parse_args()
