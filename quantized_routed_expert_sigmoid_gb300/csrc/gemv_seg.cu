@@ -10,7 +10,9 @@
 // per slot) and computes them against the staged tokens: the weight bytes come from HBM
 // once and from L2 on the later passes, with many units in flight per SM.
 //   gate/up: unit = rows 2rp, 2rp+1 of gate and up of one expert -> h fp32 [P][I]
-//   down:    unit = 8 rows of one expert's down matrix           -> y fp32 [P][H]
+//   down:    unit = 8 rows of one expert's down matrix, 4 lanes a row (rows of fewer
+//            than 32 activation groups), or 4 rows with one group a lane (the gate/up
+//            layout, rows of 32 groups or more)                  -> y fp32 [P][H]
 // Pairs are in sorted (expert-major) order; the combine kernel gathers them per token.
 // Dot products use the integer Q4_K walk of qdot.cuh in a fixed order.
 #include <algorithm>
