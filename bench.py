@@ -95,13 +95,69 @@ def profiled_traffic(kernel, args):
 
 # ------------------------------------------------------------------ clocks
 
+class NvmlClocks:
+    """Read-only NVML queries (SM clock, max SM clock, clock-event reasons, power) through
+    ctypes on libnvidia-ml; None when the library or the device is not available."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index: int):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sample(self):
+        ct = self.ct
+        mhz, mx, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz))          # NVML_CLOCK_SM
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ct.byref(mx))
+        self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw))
+        self.reasons_fn(self.h, ct.byref(rs))
+        return time.time(), float(mhz.value), float(mx.value), mw.value / 1000.0, int(rs.value)
+
+
 class ClockSampler:
-    def __init__(self, device_index: int):
+    """Samples the SM clock every `period_s` on a thread (NVML), or through nvidia-smi every
+    200 ms when NVML is not available; summary() keeps the samples of the timed region."""
+
+    def __init__(self, device_index: int, period_s: float = 0.002):
+        self.dev = device_index
+        self.period = period_s
+        self.rows = []
         self.proc = None
         self.path = None
-        self.dev = device_index
+        self.thread = None
+        self.stop = False
+        self.source = "nvml"
+
+    def _loop(self, nv):
+        while not self.stop:
+            try:
+                t, mhz, mx, w, bits = nv.sample()
+                self.rows.append((t, mhz, mx, [n for b, n in NvmlClocks.REASONS.items() if bits & b]))
+            except Exception:
+                pass
+            time.sleep(self.period)
 
     def __enter__(self):
+        import threading
+        try:
+            nv = NvmlClocks(self.dev)
+            nv.sample()
+            self.thread = threading.Thread(target=self._loop, args=(nv,), daemon=True)
+            self.thread.start()
+            time.sleep(3 * self.period)
+            return self
+        except Exception:
+            self.thread = None
+        self.source = "nvidia-smi"
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
@@ -114,6 +170,10 @@ class ClockSampler:
         return self
 
     def __exit__(self, *a):
+        if self.thread is not None:
+            time.sleep(2 * self.period)
+            self.stop = True
+            self.thread.join(timeout=2)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -124,11 +184,21 @@ class ClockSampler:
     def summary(self, t_begin=None, t_end=None):
         """Median SM clock, max clock and active throttle reasons over the samples taken in
         [t_begin, t_end] (host epoch seconds: the timed region); all samples when none fell in it."""
-        if self.proc is None or not self.path or not os.path.exists(self.path):
-            return None
-        rows = parse_clock_samples(open(self.path).read().splitlines())
-        os.unlink(self.path)
-        return summarize_clocks(rows, t_begin, t_end)
+        if self.thread is not None:
+            rows = [(t, mhz, mx, ["active"] + [("Active" if n in rs else "Not Active") for n in
+                                                ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                                 "sw_power_cap")])
+                    for t, mhz, mx, rs in self.rows]
+            out = summarize_clocks(rows, t_begin, t_end)
+        else:
+            if self.proc is None or not self.path or not os.path.exists(self.path):
+                return None
+            rows = parse_clock_samples(open(self.path).read().splitlines())
+            os.unlink(self.path)
+            out = summarize_clocks(rows, t_begin, t_end)
+        if out is not None:
+            out["source"] = self.source
+        return out
 
 
 def parse_clock_samples(lines):
@@ -213,17 +283,45 @@ def build_layers(shape, T, L, seed, device, shared_router=False, decode_chain=Tr
         Wr = synth.router_weight(shape, seed, lr).to(device)
         b = synth.bias(shape, seed, lr)
         b = None if b is None else b.to(device)
-        sh = None
+        sh, sh_run, sq = None, None, shape.shared_qtype
         if shape.I_s > 0:
             sh = [synth.expert_matrix(shape, seed, l, n, 0, device) for n in ("s_gate", "s_up", "s_down")]
-        layers.append(MoeLayer(mode=shape.mode, E=shape.E, k=shape.k, H=shape.H, I=shape.I, qtype=shape.qtype,
-                               gate=gate, up=up, down=down, W_router=Wr, bias=b, n_groups=shape.n_groups,
-                               topk_groups=shape.topk_groups, scale=shape.scale, renormalize=shape.renormalize,
-                               x_dtype=shape.x_dtype, I_s=shape.I_s, shared_qtype=shape.shared_qtype,
-                               s_gate=sh[0] if sh else None, s_up=sh[1] if sh else None,
-                               s_down=sh[2] if sh else None, decode_chain=decode_chain,
-                               tc_min_tokens=tc_min_tokens))
+            sh_run = sh
+            if shape.shared_qtype == synth.Q8_0:
+                # a Q8_0 shared expert is prepared once (moe_weights_prepare), as a user would
+                from quantized_routed_expert_sigmoid_gb300.layer import prepare_q8_0
+                sh_run = [prepare_q8_0(sh[0], shape.I_s, shape.H), prepare_q8_0(sh[1], shape.I_s, shape.H),
+                          prepare_q8_0(sh[2], shape.H, shape.I_s)]
+                sq = "q8_0_r"
+        lay = MoeLayer(mode=shape.mode, E=shape.E, k=shape.k, H=shape.H, I=shape.I, qtype=shape.qtype,
+                       gate=gate, up=up, down=down, W_router=Wr, bias=b, n_groups=shape.n_groups,
+                       topk_groups=shape.topk_groups, scale=shape.scale, renormalize=shape.renormalize,
+                       x_dtype=shape.x_dtype, I_s=shape.I_s, shared_qtype=sq,
+                       s_gate=sh_run[0] if sh else None, s_up=sh_run[1] if sh else None,
+                       s_down=sh_run[2] if sh else None, decode_chain=decode_chain, tc_min_tokens=tc_min_tokens)
+        lay.stored_shared = sh                   # the GGUF bytes, for the oracle
+        layers.append(lay)
     return layers
+
+
+def resolve_workload(args):
+    """(shape, T, layers per step, seed, description) of args.workload with --tokens / --layers."""
+    shape, T, L, seed, desc = WORKLOADS[args.workload]
+    if args.tokens:
+        T = args.tokens
+        desc = desc.replace("T=1:", f"T={T}:").replace("T=2:", f"T={T}:")
+    if args.layers:
+        L = args.layers
+        desc = desc.replace("16 distinct layers", f"{L} distinct layers")
+    return shape, T, L, seed, desc
+
+
+def workload_config(args, shape, T, L, desc, world):
+    """The `config` of a bench line: the workload and its sizes (the same on both arms)."""
+    return {"workload": desc, "T": T, "layers_per_step": L, "H": shape.H, "E": shape.E, "k": shape.k,
+            "I": shape.I, "qtype": shape.qtype, "l2": "inputs larger than L2 (distinct weights per layer)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            **({"tc_min_tokens": args.tc_min_tokens} if args.tc_min_tokens else {})}
 
 
 def make_x(shape, T, seed, device, workload):
@@ -261,18 +359,36 @@ def launches_per_layer(shape, T, stack=False, path=None):
 
 # ------------------------------------------------------------------ our arm
 
+SUB_WORKLOADS = ("decode2", "prefill")       # the metric's other two points, measured beside the headline
+
+
 def run_ours(args, rank, world):
+    """The headline line (decode T=1) with the metric's other points (decode T=2, prefill
+    T=4096) as sub-records measured in the same run, each with its own timing, roofline and
+    end-to-end figure."""
+    import copy
+    steps_given = args.steps
+    head = measure(args, rank, world)
+    if args.workload == "decode" and not (args.tokens or args.layers or args.no_sub):
+        subs = {}
+        for name in SUB_WORKLOADS:
+            torch.cuda.empty_cache()
+            a = copy.copy(args)
+            a.workload, a.steps, a.no_cpu_baseline = name, steps_given, True
+            r = measure(a, rank, world)
+            subs[name] = {k: r[k] for k in ("value", "unit", "steps", "ms_per_step", "config", "layer", "roofline",
+                                            "e2e", "gpu_launches", "clocks") if k in r}
+        head["workloads"] = subs
+    return head
+
+
+def measure(args, rank, world):
+    """One workload: build its layers, capture one step as a CUDA graph, time K steps."""
     import quantized_routed_expert_sigmoid_gb300 as moe
     device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(device)
-    shape, T, L, seed, desc = WORKLOADS[args.workload]
-    if args.tokens:
-        T = args.tokens
-        desc = desc.replace("T=1:", f"T={T}:").replace("T=2:", f"T={T}:")
+    shape, T, L, seed, desc = resolve_workload(args)
     stack = args.workload == "stack"
-    if args.layers:
-        L = args.layers
-        desc = desc.replace("16 distinct layers", f"{L} distinct layers")
     layers = build_layers(shape, T, L, seed + 1000 * rank, device, shared_router=(args.workload == "prefill"),
                           decode_chain=not args.separate_decode, tc_min_tokens=args.tc_min_tokens)
     x = make_x(shape, T, seed + 1000 * rank, device, args.workload)
@@ -452,10 +568,7 @@ def run_ours(args, rank, world):
         "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": desc, "T": T, "layers_per_step": L, "H": shape.H, "E": shape.E, "k": shape.k,
-                   "I": shape.I, "qtype": shape.qtype, "l2": "inputs larger than L2 (distinct weights per layer)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU", "path": path,
-                   **({"tc_min_tokens": args.tc_min_tokens} if args.tc_min_tokens else {})},
+        "config": workload_config(args, shape, T, L, desc, world), "path": path,
         "layer": {"us_per_layer": round(layer_us, 3), "algorithmic_bytes": round(layer_bytes),
                   "GBps": round(layer_bytes / (layer_us * 1e-6) / 1e9, 1),
                   "frac_hbm": round(layer_bytes / (layer_us * 1e-6) / 1e9 / hbm_peak, 4),
@@ -477,7 +590,7 @@ def time_gateup_events(moe, layers, x, outs, T, args):
     is never the bottleneck)."""
     import quantized_routed_expert_sigmoid_gb300._native as N
     durations = []
-    rounds = max(3, min(args.steps, 10))
+    rounds = max(5, min(args.steps, 20))
     for _ in range(rounds):
         evs = []
         torch.cuda._sleep(20_000_000)
@@ -489,7 +602,9 @@ def time_gateup_events(moe, layers, x, outs, T, args):
             evs.append((eb, ea))
         torch.cuda.synchronize()
         durations += [eb.elapsed_time(ea) for eb, ea in evs]
-    return statistics.median(durations)
+    # the events tick in steps of about 1 us: the mean over many launches (whose start times
+    # fall anywhere within a tick) estimates the duration without the rounding of a median
+    return statistics.fmean(durations)
 
 
 def time_gateup(moe, layers, x, shape, T, device, args):
@@ -565,7 +680,7 @@ def cpu_baseline(workload, layer, x, shape, T, budget_s=10.0):
     spec = oracle_layer_spec(shape, (gate.cpu().numpy(), up.cpu().numpy(), down.cpu().numpy(), Wr.cpu().numpy(),
                                      None if b is None else b.cpu().numpy()))
     if shape.I_s > 0:
-        sg, su, sd = layer._keep[5], layer._keep[6], layer._keep[7]
+        sg, su, sd = layer.stored_shared
         spec.shared_qtype, spec.I_s = oracle.Q8_0, shape.I_s
         spec.s_gate, spec.s_up, spec.s_down = sg.cpu().numpy(), su.cpu().numpy(), sd.cpu().numpy()
     xs = x.float().cpu().double().numpy()
@@ -586,7 +701,7 @@ def cpu_baseline(workload, layer, x, shape, T, budget_s=10.0):
 def run_reference(args):
     """The fp64 oracle timed on the host cores on this workload (no GPU)."""
     import oracle
-    shape, T, L, seed, desc = WORKLOADS[args.workload]
+    shape, T, L, seed, desc = resolve_workload(args)
     tensors = (synth.expert_stack(shape, seed, 0, "gate").numpy(), synth.expert_stack(shape, seed, 0, "up").numpy(),
                synth.expert_stack(shape, seed, 0, "down").numpy(), synth.router_weight(shape, seed, 0).numpy(),
                None if shape.bias_std <= 0 else synth.bias(shape, seed, 0).numpy())
@@ -608,7 +723,7 @@ def run_reference(args):
     return {"impl": "reference", "metric": "MoE-layer tokens/s (decode T=1,2 / prefill T=4096); % of HBM roofline",
             "value": round(value, 3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f64", "data": "synthetic", "config": {"workload": desc, "T": T},
+            "dtype": "f64", "data": "synthetic", "config": workload_config(args, shape, T, L, desc, 1),
             "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
                              "sample": f"each step: one oracle call on {n_sample} token(s) of one layer"},
             "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -628,6 +743,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=0, help="override T (tokens per layer call)")
     ap.add_argument("--tc-min-tokens", type=int, default=0,
                     help="smallest T that takes the tensor-core path (default: the library's, 128)")
+    ap.add_argument("--no-sub", action="store_true",
+                    help="decode: skip the sub-records of decode T=2 and prefill T=4096")
     ap.add_argument("--separate-decode", action="store_true",
                     help="decode sizes: run the separate route/permute/GEMV/combine kernels, not the single-launch layer")
     args = ap.parse_args()
