@@ -40,7 +40,7 @@ def test_tiny_q8_0(T):
     _check_layer(tl, T)
 
 
-@pytest.mark.parametrize("T", [1, 2])
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
 def test_decode_q4_k(T):
     tl = make_layer(synth.DECODE, 2, T)
     _check_layer(tl, T)
@@ -152,10 +152,28 @@ def test_accumulate_is_residual_add():
 
 # ---------------------------------------------------------------- tensor-core path (T >= tc_min_tokens)
 
-def _check_sampled(tl, T, sample, tol, tc_min_tokens=0, n_threads=8):
+def tile_sample(ref_ids, E, bn):
+    """Tokens that put at least one checked pair in every (expert, token block) tile of the
+    tensor-core GEMM -- the first and the last pair of each block of up to bn pairs of an
+    expert's sorted run, so every ragged tail's last pair is among them -- and the number of
+    tiles.  The blocks follow from the routing alone (the permutation is bit-exact)."""
+    k = ref_ids.shape[1]
+    sorted_pairs, offsets, _ = oracle.permute(ref_ids, E)
+    tokens, n_tiles = set(), 0
+    for e in range(E):
+        for p0 in range(int(offsets[e]), int(offsets[e + 1]), bn):
+            p1 = min(int(offsets[e + 1]), p0 + bn) - 1
+            tokens.add(int(sorted_pairs[p0]) // k)
+            tokens.add(int(sorted_pairs[p1]) // k)
+            n_tiles += 1
+    return np.array(sorted(tokens)), n_tiles
+
+
+def _check_sampled(tl, T, sample, tol, tc_min_tokens=0, n_threads=None):
     """Whole-layer run on the GPU; routing ids of every token and the outputs of the
     sampled tokens against the oracle (tokens are independent, so the oracle runs on
-    the sample alone)."""
+    the sample alone).  sample=None takes tile_sample of the routing."""
+    n_threads = n_threads or oracle.max_threads()
     layer = tl.moe_layer(tc_min_tokens=tc_min_tokens)
     x = tl.x.cuda()
     out = layer(x)
@@ -167,6 +185,9 @@ def _check_sampled(tl, T, sample, tol, tc_min_tokens=0, n_threads=8):
     assert np.array_equal(ids.numpy(), ref_ids), "routing ids differ"
     _, ref_off, _ = oracle.permute(ref_ids, tl.shape.E)
     assert np.array_equal(offs.numpy(), ref_off), "expert offsets differ"
+    n_tiles = None
+    if sample is None:
+        sample, n_tiles = tile_sample(ref_ids, tl.shape.E, 256 if tl.shape.qtype == synth.Q4_K else 128)
     sample = np.asarray(sample)
     need = sorted(set(ref_ids[sample].reshape(-1).tolist()))
     assert set(need) <= tl.exact
@@ -174,6 +195,8 @@ def _check_sampled(tl, T, sample, tol, tc_min_tokens=0, n_threads=8):
     err = rel_l2(out.cpu().numpy()[sample], ref["out"])
     assert err <= tol, f"rel-L2 {err:.3e} > {tol}"
     assert layer.device_status(T) == 0
+    print(f"T={T}: {len(sample)} tokens checked against the oracle"
+          + (f", covering all {n_tiles} (expert, token block) tiles" if n_tiles else "") + f", rel-L2 {err:.2e}")
     return layer, out, err
 
 
@@ -188,7 +211,7 @@ def test_tc_decode_shape_ragged():
     from helpers import TOL_TC
     T = 300                                 # 2400 pairs: many token blocks, a ragged tail per expert
     tl = make_layer(synth.DECODE, 30, T, exact_all=True)
-    _check_sampled(tl, T, np.arange(0, T, 13), TOL_TC)
+    _check_sampled(tl, T, None, TOL_TC)
 
 
 def test_tc_prefill_zipf_T4096():
@@ -203,14 +226,19 @@ def test_tc_prefill_zipf_T4096():
     counts = np.bincount(ids.reshape(-1), minlength=shape.E)
     assert (counts == 0).sum() >= 8 and counts.max() > 1000          # uneven, some experts empty
     tl = SeededLayer(shape, seed, x, exact=None, Wr=Wr, bias=None)
-    _check_sampled(tl, T, np.arange(0, T, 257), TOL_TC)
+    layer, o_tc, _ = _check_sampled(tl, T, None, TOL_TC)
+    # the whole output against the fp32 GEMV path on the same layer and tokens
+    o_gv = tl.moe_layer(tc_min_tokens=1 << 30)(tl.x.cuda())
+    torch.cuda.synchronize()
+    err = rel_l2(o_tc.cpu().numpy(), o_gv.cpu().double().numpy())
+    assert err <= TOL_TC, f"tensor-core vs GEMV path, all {T} tokens: rel-L2 {err:.3e}"
 
 
 def test_tc_deepseek_shape_verify_T512():
     from helpers import TOL_TC
     T = 512
     tl = make_layer(synth.DEEPSEEK, 4, T, exact_all=True)
-    _check_sampled(tl, T, np.arange(0, T, 43), TOL_TC)
+    _check_sampled(tl, T, None, TOL_TC)
 
 
 def test_tc_deterministic_and_graph_replay():
@@ -292,3 +320,30 @@ def test_decode_chain_q4k_shared_expert():
     tl = make_layer(shape, 63, 3, exact_all=True)
     _chain_vs_separate(tl, 3)
     _check_layer(tl, 3)
+
+
+def test_tc_fp16_range_is_reported():
+    """The tensor-core path multiplies fp16 operands: an activation or an intermediate value
+    beyond the fp16 range is reported in the status word (MOE_ERR_DEVICE_CHECK), not hidden."""
+    from quantized_routed_expert_sigmoid_gb300 import _native as N
+    T = 160
+    tl = make_layer(synth.DECODE, 33, T, exact_all=True)
+    layer = tl.moe_layer()
+    assert layer.path(T) == "tensor"
+    x = tl.x.cuda()
+    layer(x)
+    torch.cuda.synchronize()
+    assert layer.device_status(T) == N.MOE_OK
+    big = x.clone()
+    big[3, 5] = 1.0e5                                 # a bf16 value with no fp16 counterpart
+    layer(big)
+    torch.cuda.synchronize()
+    assert layer.device_status(T) == N.MOE_ERR_DEVICE_CHECK
+    loud = (x.float() * 400.0).to(torch.bfloat16)     # x in range; silu(gate) * up beyond 65504
+    assert loud.float().abs().max().item() < 6e4
+    layer(loud)
+    torch.cuda.synchronize()
+    assert layer.device_status(T) == N.MOE_ERR_DEVICE_CHECK
+    layer(x)
+    torch.cuda.synchronize()
+    assert layer.device_status(T) == N.MOE_OK

@@ -1,13 +1,24 @@
-"""The 48-layer stack: x <- x + MoE_l(bf16(RMSNorm_l(x))), captured as one CUDA graph.
+"""The 48-layer stack: x <- x + MoE_l(bf16(RMSNorm_l(x))), one residual block per layer call.
 
 Each layer is the decode-shaped layer (hidden 2048, 128 experts, top-8, I=768,
-Q4_K).  The oracle runs its own chain in fp64 (it never sees a GPU value);
-routing ids must match at every layer whose routing the oracle's own reruns
-leave unchanged, the first layer must meet the single-layer tolerance, and the
-drift after every later layer must stay within a bound the oracle measures for
-itself (see the test).  A layer whose routing margin
-(measured on the oracle chain) falls below 1e-3 gets its router redrawn from a
-new seed before the chain continues.
+Q4_K); every token count of the sweep T in {1, 2, 4, 8, 16, 32, 64} runs all 48
+layers.  Layer l's router is drawn so that the oracle's own chain keeps a 1e-3
+routing margin (a layer whose margin falls below it on the oracle chain gets its
+router redrawn from a new seed before the chain continues).
+
+Parity is checked per layer with teacher forcing: the oracle's layer l runs on
+the GPU's own bf16 input to layer l (the GPU's RMSNorm output of the GPU's
+residual stream -- an input of the check, never a compared result):
+  - routing ids bit-exact for every token whose top-k margin, measured by the
+    oracle in fp64 on that input, is at least 1e-3; a token under the margin may
+    pick another expert set only if that set is a valid top-k within the margin;
+  - the layer's MoE output within rel-L2 1e-4 of the oracle's on that input
+    (tokens with identical ids).
+The residual add, the pre-norm inside the layer call and the CUDA graph are
+then checked bit for bit against their parts.  The distance of the whole GPU
+chain from the oracle's own chain is reported beside the oracle's distance from
+itself under flipped bf16 roundings; it is not a pass/fail bar, because past the
+first layers it measures how depth amplifies rounding steps, not the GPU.
 """
 from __future__ import annotations
 
@@ -17,174 +28,181 @@ import torch
 
 import oracle
 import synth
-from helpers import MIN_GAP, OQ, oracle_mode, rel_l2
+from helpers import MIN_GAP, OQ, TOL_GEMV, oracle_mode, rel_l2
 
 pytestmark = pytest.mark.gpu
 
 N_LAYERS = 48
 EPS = 1e-6
+SHAPE = synth.DECODE
+STACK_T = [1, 2, 4, 8, 16, 32, 64]
+
+_WEIGHTS: dict[int, dict] = {}
 
 
-def _bf16_neighbours(u):
-    """The two bf16 values around each element of u (fp64), and the midpoint between them."""
+def _weights(l: int) -> dict:
+    """Layer l's RMSNorm weight and expert tensors (GPU), shared by every T of the sweep."""
+    if l not in _WEIGHTS:
+        lseed = 5000 + l
+        _WEIGHTS[l] = dict(gamma=synth.gamma(SHAPE.H, lseed, l),
+                           gate=synth.expert_stack(SHAPE, lseed, l, "gate", "cuda"),
+                           up=synth.expert_stack(SHAPE, lseed, l, "up", "cuda"),
+                           down=synth.expert_stack(SHAPE, lseed, l, "down", "cuda"))
+    return _WEIGHTS[l]
+
+
+def _spec(W: dict, Wr: torch.Tensor, experts) -> oracle.LayerSpec:
+    """The oracle's view of one layer; only `experts` carry their bytes (the rest are zero)."""
+    s = SHAPE
+    rb_h, rb_i = synth.row_bytes(s.qtype, s.H), synth.row_bytes(s.qtype, s.I)
+    g = np.zeros((s.E, s.I, rb_h), np.uint8)
+    u = np.zeros((s.E, s.I, rb_h), np.uint8)
+    d = np.zeros((s.E, s.H, rb_i), np.uint8)
+    idx = np.asarray(sorted(set(int(e) for e in np.asarray(experts).reshape(-1))), dtype=np.int64)
+    ti = torch.from_numpy(idx).cuda()
+    g[idx] = W["gate"].index_select(0, ti).cpu().numpy()
+    u[idx] = W["up"].index_select(0, ti).cpu().numpy()
+    d[idx] = W["down"].index_select(0, ti).cpu().numpy()
+    return oracle.LayerSpec(mode=oracle_mode(s), E=s.E, k=s.k, H=s.H, I=s.I, qtype=OQ[s.qtype],
+                            gate=g, up=u, down=d, Wr=Wr.numpy())
+
+
+def _round_bf16(u):
+    return np.vectorize(oracle.round_bf16)(u)
+
+
+def _bf16_midpoint_flips(u, rel=1e-6):
+    """bf16(u), except that elements within rel of a rounding midpoint take the other
+    neighbour (a less precise RMSNorm may land on either side there)."""
+    r = _round_bf16(u)
     f = np.abs(u).astype(np.float32)
     lo_bits = f.view(np.uint32) & np.uint32(0xFFFF0000)
     lo = lo_bits.view(np.float32).astype(np.float64)
     hi = (lo_bits + np.uint32(0x10000)).view(np.float32).astype(np.float64)
-    return lo, hi, 0.5 * (lo + hi)
-
-
-def _round_other_way(u, rel=1e-6):
-    """bf16(u), except that elements within rel of a rounding midpoint take the other
-    neighbour: a computation of u in lower precision may land on either side there."""
-    r = np.vectorize(oracle.round_bf16)(u)
-    lo, hi, mid = _bf16_neighbours(u)
+    mid = 0.5 * (lo + hi)
     amb = np.abs(np.abs(u) - mid) <= rel * np.abs(u)
     other = np.where(np.abs(r) == lo, hi, lo) * np.sign(u)
     return np.where(amb, other, r)
 
 
-def _oracle_chain(layers, shape, x, flip_rel=0.0):
-    """The oracle's own chain from x (fp64), returning x and the routing ids after every
-    layer.  flip_rel > 0 rounds the RMSNorm outputs that sit within flip_rel of a bf16
-    rounding midpoint the other way (the rounding a less precise RMSNorm may legitimately
-    take)."""
+def _oracle_chain(layers, x, rounding=_round_bf16, n_threads=None):
+    """The oracle's chain from x (fp64): the residual stream after every layer and the ids."""
+    n_threads = n_threads or oracle.max_threads()
     xs, ids = [], []
-    for L in layers:
-        u = oracle.rmsnorm(x, L["gamma"].numpy(), EPS)
-        u = _round_other_way(u, flip_rel) if flip_rel > 0 else np.vectorize(oracle.round_bf16)(u)
-        r = oracle.moe_layer(L["spec"], u, n_threads=8)
-        x = x + r["out"]
+    for l, L in enumerate(layers):
+        W = _weights(l)
+        u = rounding(oracle.rmsnorm(x, W["gamma"].numpy(), EPS))
+        lg = oracle.router_logits(u, L["Wr"].numpy())
+        sel, _, _ = oracle.route(oracle_mode(SHAPE), lg, SHAPE.k)
+        x = x + oracle.moe_layer(_spec(W, L["Wr"], sel), u, logits=lg, n_threads=n_threads)["out"]
         xs.append(x)
-        ids.append(r["ids"])
+        ids.append(sel)
     return xs, ids
 
 
-def _first_rerouted(layers, *id_chains):
-    """First layer at which any rerun of the oracle chain routes differently from the
-    reference chain (len(layers) if none does)."""
-    for l, L in enumerate(layers):
-        if any(not np.array_equal(ch[l], L["ids"]) for ch in id_chains):
-            return l
-    return len(layers)
-
-
-def _build_stack(T, seed=5, n_layers=N_LAYERS):
-    shape = synth.DECODE
-    x0 = synth.activations(T, shape.H, seed, "bf16").float()
+def _build_stack(T: int, seed: int = 5):
+    """x0 and the 48 layers' routers, each drawn so that the oracle's own chain keeps the
+    routing margin at that layer; also the oracle chain's state after every layer."""
+    x0 = synth.activations(T, SHAPE.H, seed, "bf16").float()
     x = x0.double().numpy()
     layers = []
-    for l in range(n_layers):
-        lseed = 5000 + l
-        gamma = synth.gamma(shape.H, lseed, l)
-        u = oracle.rmsnorm(x, gamma.numpy(), EPS)
-        u = np.vectorize(oracle.round_bf16)(u)
+    nt = oracle.max_threads()
+    for l in range(N_LAYERS):
+        W = _weights(l)
+        u = _round_bf16(oracle.rmsnorm(x, W["gamma"].numpy(), EPS))
         for attempt in range(50):
-            Wr = synth.router_weight(shape, lseed, l, attempt=attempt)
+            Wr = synth.router_weight(SHAPE, 5000 + l, l, attempt=attempt)
             lg = oracle.router_logits(u, Wr.numpy())
-            ids, w, gaps = oracle.route(oracle_mode(shape), lg, shape.k)
+            ids, _, gaps = oracle.route(oracle_mode(SHAPE), lg, SHAPE.k)
             if gaps[:, 0].min() >= MIN_GAP:
                 break
         else:
             raise RuntimeError("no router draw met the margin")
-        gate = synth.expert_stack(shape, lseed, l, "gate", "cuda")
-        up = synth.expert_stack(shape, lseed, l, "up", "cuda")
-        down = synth.expert_stack(shape, lseed, l, "down", "cuda")
-        used = sorted(set(ids.reshape(-1).tolist()))
-        rb_h, rb_i = synth.row_bytes(shape.qtype, shape.H), synth.row_bytes(shape.qtype, shape.I)
-        g_np = np.zeros((shape.E, shape.I, rb_h), np.uint8)
-        u_np = np.zeros_like(g_np)
-        d_np = np.zeros((shape.E, shape.H, rb_i), np.uint8)
-        for e in used:
-            g_np[e], u_np[e], d_np[e] = gate[e].cpu().numpy(), up[e].cpu().numpy(), down[e].cpu().numpy()
-        spec = oracle.LayerSpec(mode=oracle_mode(shape), E=shape.E, k=shape.k, H=shape.H, I=shape.I,
-                                qtype=OQ[shape.qtype], gate=g_np, up=u_np, down=d_np, Wr=Wr.numpy())
-        y = oracle.moe_layer(spec, u, n_threads=8)["out"]
-        x = x + y
-        layers.append(dict(gamma=gamma, Wr=Wr, gate=gate, up=up, down=down, ids=ids, spec=spec, x_after=x))
-    return shape, x0, layers, x
+        x = x + oracle.moe_layer(_spec(W, Wr, ids), u, logits=lg, n_threads=nt)["out"]
+        layers.append(dict(Wr=Wr, ids=ids, x_after=x))
+    return x0, layers
 
 
-def _gpu_stack(shape, x0, layers, T):
+def _gpu_layers(layers):
+    """Per layer: the production residual block (pre-norm inside the call, out == x) and the
+    plain layer on a bf16 input (no residual add) that the teacher-forced check reads."""
     from quantized_routed_expert_sigmoid_gb300 import MoeLayer
+    fused, plain = [], []
+    for l, L in enumerate(layers):
+        W = _weights(l)
+        kw = dict(mode="softmax", E=SHAPE.E, k=SHAPE.k, H=SHAPE.H, I=SHAPE.I, qtype=SHAPE.qtype,
+                  gate=W["gate"], up=W["up"], down=W["down"], W_router=L["Wr"].cuda())
+        fused.append(MoeLayer(**kw, accumulate=True, x_dtype="f32", norm_gamma=W["gamma"].cuda(), norm_eps=EPS))
+        plain.append(MoeLayer(**kw, accumulate=False, x_dtype="bf16"))
+    return fused, plain
+
+
+def _valid_topk(lg_row, chosen, k, tol):
+    """chosen is a top-k of lg_row up to tol: no unchosen logit exceeds a chosen one by more."""
+    mask = np.zeros(lg_row.shape[0], bool)
+    mask[np.asarray(chosen)] = True
+    return len(set(int(c) for c in chosen)) == k and lg_row[mask].min() >= lg_row[~mask].max() - tol
+
+
+@pytest.mark.parametrize("T", STACK_T)
+def test_stack_48_layers(T):
+    """Teacher-forced per-layer parity over 48 layers, then the chaining checked bit for bit:
+    the residual block equals x + layer(norm(x)) exactly, the pre-norm call routes like the
+    plain layer, and the captured graph of 48 calls replays the eager chain's bits.  The
+    distance of the whole chain from the oracle's own chain is printed, not bounded."""
     import quantized_routed_expert_sigmoid_gb300 as moe
-    mls = [MoeLayer(mode="softmax", E=shape.E, k=shape.k, H=shape.H, I=shape.I, qtype=shape.qtype,
-                    gate=L["gate"], up=L["up"], down=L["down"], W_router=L["Wr"].cuda(), accumulate=True)
-           for L in layers]
-    gammas = [L["gamma"].cuda() for L in layers]
-    for m in mls:
-        m.ensure_workspace(T)
-    x = x0.cuda().contiguous()
-    u = torch.empty(T, shape.H, dtype=torch.bfloat16, device="cuda")
-
-    def run(stream=None):
-        for m, g in zip(mls, gammas):
-            moe.moe_rmsnorm_bf16(x, g, T, shape.H, EPS, u, stream)
-            m(u, out=x, stream=stream)
-
-    return mls, x, run
-
-
-@pytest.mark.parametrize("T", [1, 2])
-def test_stack_48_layers_graph(T):
-    """Ids bit-exact where the oracle's routing is decided; drift within a bound the oracle sets.
-
-    The stack is a deep residual chain whose bf16 rounding of each layer's input
-    is a discontinuous step, so tiny differences grow with depth.  The bound on
-    the GPU's distance from the oracle after layer l is derived from the oracle
-    alone, from two reruns of its chain: one from an input perturbed by 1e-6
-    (relative), and one that rounds every RMSNorm output lying within 1e-6 of a
-    bf16 rounding midpoint to the other neighbour (the GPU computes RMSNorm in
-    fp32, so such elements may round either way).  The larger of the two
-    divergences after layer l, times 10, plus the single-layer tolerance, is the
-    allowed distance.  The same reruns say how far down the routing is decided: from
-    the first layer at which either of them picks other experts than the reference
-    chain, a 1e-6 change of the input already reroutes the oracle itself, so from there
-    on only the drift bound applies (the reference keeps a 1e-3 margin on its own
-    inputs, but the drift of any chain grows with depth).  At least the first 32 layers
-    must stay decided, so the test keeps checking ids over two thirds of the stack.
-    """
-    shape, x0, layers, x_ref = _build_stack(T)
-    rng = np.random.default_rng(7)
-    x0_64 = x0.double().numpy()
-    pert, pert_ids = _oracle_chain(layers, shape, x0_64 * (1.0 + 1e-6 * rng.standard_normal(x0_64.shape)))
-    flip, flip_ids = _oracle_chain(layers, shape, x0_64, flip_rel=1e-6)
-    decided = _first_rerouted(layers, pert_ids, flip_ids)
-    assert decided >= 32, f"the oracle's own reruns reroute at layer {decided}"
-    mls, x, run = _gpu_stack(shape, x0, layers, T)
-    # eager, layer by layer: the GPU chain next to the oracle chain (never fed into it)
-    import quantized_routed_expert_sigmoid_gb300 as moe
-    u = torch.empty(T, shape.H, dtype=torch.bfloat16, device="cuda")
-    x.copy_(x0.cuda())
-    drift = []
-    for l, (m, L) in enumerate(zip(mls, layers)):
-        moe.moe_rmsnorm_bf16(x, L["gamma"].cuda(), T, shape.H, EPS, u)
-        m(u, out=x)
+    x0, layers = _build_stack(T)
+    fused, plain = _gpu_layers(layers)
+    H, k = SHAPE.H, SHAPE.k
+    x = x0.cuda().contiguous().clone()
+    u = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    inputs, moe_out, gpu_ids, after = [], [], [], []
+    for l in range(N_LAYERS):
+        W = _weights(l)
+        x_in = x.clone()
+        moe.moe_rmsnorm_bf16(x, W["gamma"].cuda(), T, H, EPS, u)
+        m = plain[l](u)
+        fused[l](x, out=x)
         torch.cuda.synchronize()
-        ids, _, _ = m.debug_views(T)
-        if l < decided:
-            assert np.array_equal(ids.numpy(), L["ids"]), f"layer {l}: routing ids differ"
-        err = rel_l2(x.cpu().numpy(), L["x_after"])
-        self_div = max(rel_l2(pert[l], L["x_after"]), rel_l2(flip[l], L["x_after"]))
-        drift.append((err, self_div))
-        assert err <= 1e-4 + 10 * self_div, f"layer {l}: rel-L2 {err:.3e}, oracle self-divergence {self_div:.3e}"
+        assert torch.equal(x, x_in + m), f"layer {l}: the residual block is not x + layer(norm(x))"
+        ids_p, _, _ = plain[l].debug_views(T)
+        ids_f, _, _ = fused[l].debug_views(T)
+        assert torch.equal(ids_p, ids_f), f"layer {l}: pre-norm call routes differently"
+        assert fused[l].device_status(T) == 0 and plain[l].device_status(T) == 0
+        inputs.append(u.float().cpu().double().numpy())
+        moe_out.append(m.cpu().double().numpy())
+        gpu_ids.append(ids_p.numpy())
+        after.append(x.cpu().double().numpy())
+
+    # ---- teacher forcing: the oracle's layer l on the GPU's input to layer l
+    nt = oracle.max_threads()
+    worst, undecided, rerouted = 0.0, 0, 0
+    for l in range(N_LAYERS):
+        ul = inputs[l]
+        lg = oracle.router_logits(ul, layers[l]["Wr"].numpy())
+        ref_ids, _, gaps = oracle.route(oracle_mode(SHAPE), lg, k)
+        decided = gaps[:, 0] >= MIN_GAP
+        same = np.all(gpu_ids[l] == ref_ids, axis=1)
+        assert np.all(same[decided]), f"layer {l}: routing ids differ on decided tokens {np.where(~same & decided)[0]}"
+        for t in np.where(~same)[0]:
+            assert _valid_topk(lg[t], gpu_ids[l][t], k, MIN_GAP), f"layer {l} token {t}: not a top-{k}"
+        undecided += int((~decided).sum())
+        rerouted += int((~same).sum())
+        ref = oracle.moe_layer(_spec(_weights(l), layers[l]["Wr"], ref_ids), ul, logits=lg, n_threads=nt)["out"]
+        err = rel_l2(moe_out[l][same], ref[same])
+        worst = max(worst, err)
+        assert err <= TOL_GEMV, f"layer {l}: teacher-forced rel-L2 {err:.3e} > {TOL_GEMV}"
+
+    # ---- the whole stack as one captured graph: the eager chain's bits
     eager_final = x.clone()
-    assert drift[0][0] <= 1e-4                                         # one layer: the single-layer bar
-    # the same stack with the RMSNorm inside each layer call (pre-norm; the chain computes it
-    # itself): one call per layer on the residual stream, the bits of the separate kernels
-    from quantized_routed_expert_sigmoid_gb300 import MoeLayer
-    fused = [MoeLayer(mode="softmax", E=shape.E, k=shape.k, H=shape.H, I=shape.I, qtype=shape.qtype,
-                      gate=L["gate"], up=L["up"], down=L["down"], W_router=L["Wr"].cuda(), accumulate=True,
-                      x_dtype="f32", norm_gamma=L["gamma"].cuda(), norm_eps=EPS)
-             for L in layers]
-    xf = x0.cuda().contiguous().clone()
-    for m in fused:
-        m(xf, out=xf)
-    torch.cuda.synchronize()
-    assert torch.equal(xf, eager_final), "pre-norm layers differ from RMSNorm + layer"
-    # capture the 48 layers once, replay from x0: the same bits as the eager chain
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
+
+    def run(stream=None):
+        for m in fused:
+            m(x, out=x, stream=stream)
+
+    x.copy_(x0.cuda())
     with torch.cuda.stream(s):
         run(stream=s)
     torch.cuda.current_stream().wait_stream(s)
@@ -195,9 +213,18 @@ def test_stack_48_layers_graph(T):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(x, eager_final), "graph replay differs from the eager chain"
-    for l, (m, L) in enumerate(zip(mls[:decided], layers)):
-        ids, _, _ = m.debug_views(T)
-        assert np.array_equal(ids.numpy(), L["ids"]), f"replay, layer {l}: routing ids differ"
-    print(f"routing decided through layer {decided - 1};",
-          "stack drift (gpu vs oracle, oracle self-divergence) per 8 layers:",
-          [(f"{a:.1e}", f"{b:.1e}") for a, b in drift[::8]], "final", f"{drift[-1][0]:.2e}")
+    for l in range(N_LAYERS):
+        ids_f, _, _ = fused[l].debug_views(T)
+        assert np.array_equal(ids_f.numpy(), gpu_ids[l]), f"replay, layer {l}: routing ids differ"
+
+    # ---- end-to-end distance from the oracle's own chain: reported, not a pass/fail bar.  The
+    # checks above make the GPU chain, layer by layer, the oracle's layer evaluated on the GPU's
+    # own input plus a local error below 1e-4 (measured ~1e-6), composed bit for bit; what
+    # separates the two chains after many layers is the oracle's own response to a slightly
+    # different input (each bf16 rounding of a layer input is a step, and depth amplifies the
+    # steps), which the oracle's rerun with midpoint-flipped roundings shows beside it.
+    flip, _ = _oracle_chain(layers, x0.double().numpy(), rounding=_bf16_midpoint_flips)
+    drift = [(rel_l2(after[l], layers[l]["x_after"]), rel_l2(flip[l], layers[l]["x_after"])) for l in range(N_LAYERS)]
+    print(f"T={T}: teacher-forced worst rel-L2 {worst:.2e}; tokens under the margin {undecided}, "
+          f"of them rerouted {rerouted}; distance from the oracle chain (gpu, oracle flip rerun) every 8 layers:",
+          [(f"{a:.1e}", f"{b:.1e}") for a, b in drift[::8]], f"final {drift[-1][0]:.2e}")
