@@ -33,6 +33,7 @@
  *    weights (fp16 d, 32 x int8 q; w = d*q).  Q4_K: 144 bytes per 256
  *    weights (fp16 d, fp16 dmin, 12 bytes of packed 6-bit scales/mins for 8
  *    sub-blocks of 32, 128 bytes of 4-bit q; w = d*sc_j*q - dmin*m_j).
+ *    MOE_Q8_0_R: the same Q8_0 values in moe_weights_prepare's row layout.
  *    For gate/up: rows = I, cols = H.  For down: rows = H, cols = I.
  *    Expert e of a stacked tensor starts at data + e * expert_stride_bytes.
  *  - Token-expert pairs: p = t*k + j for token t and its j-th chosen expert.
@@ -59,13 +60,16 @@ typedef enum {
     MOE_ERR_TIMEOUT = 6        /* a bounded device-side wait ran out (see *_read_device_status) */
 } moe_status;
 
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_Q8_0 = 2, MOE_Q4_K = 3 } moe_dtype;
+/* MOE_Q8_0_R: Q8_0 weights after moe_weights_prepare -- per row of K weights, the int8
+ * quants of its K/32 blocks (32 bytes each, in order), then their fp16 scales, padded to
+ * a multiple of 16 bytes: 32*(K/32) + roundup16(2*(K/32)) bytes a row. */
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_Q8_0 = 2, MOE_Q4_K = 3, MOE_Q8_0_R = 4 } moe_dtype;
 
 typedef enum { MOE_ROUTE_SOFTMAX = 0, MOE_ROUTE_SIGMOID_GROUP = 1 } moe_route_mode;
 
 /* One quantized weight tensor, possibly a stack of experts. */
 typedef struct {
-    moe_dtype qtype;             /* MOE_Q8_0 or MOE_Q4_K */
+    moe_dtype qtype;             /* MOE_Q8_0, MOE_Q4_K or MOE_Q8_0_R */
     const void* data;            /* (device) 16-byte aligned */
     int64_t rows, cols;          /* per expert; cols = input dimension */
     int64_t expert_stride_bytes; /* bytes from expert e to e+1 (multiple of 16) */
@@ -80,6 +84,28 @@ typedef struct {
     float routed_scale;          /* gates are multiplied by this (1.0 = none) */
     int renormalize;             /* 1: gates renormalised over the chosen k */
 } moe_route_cfg;
+
+/* ---------------------------------------------------------------- weights */
+
+/*
+ * moe_weights_prepare -- one-time repack of a stored Q8_0 tensor (n_experts stacked
+ * matrices) into MOE_Q8_0_R, the layout the kernels stream with 16-byte loads: a GGUF
+ * Q8_0 block is 34 bytes, so its quants never start on a 16-byte boundary.  The values
+ * are unchanged (w = d*q of the same bytes); only their place moves.  The pages' large
+ * model stores its shared experts in Q8_0 ("bloomery early V4.1 README", model file
+ * notes; "bloomery V4.1 README", quant-mix notes); this call lets those be read at the
+ * rate of the Q4_K experts.
+ *   in_out (host): the tensor to repack (qtype MOE_Q8_0, data device, 16-byte aligned,
+ *     rows, cols = K a multiple of 32, expert_stride_bytes >= rows * 34 * K/32 when
+ *     n_experts > 1).  On success it is rewritten to describe the repacked tensor:
+ *     qtype MOE_Q8_0_R, data = dst, expert_stride_bytes = rows * row bytes.  A MOE_Q4_K
+ *     tensor is used as stored: in_out is left unchanged and nothing is written.
+ *   dst (device, 16-byte aligned): at least moe_weights_prepare_size() bytes, owned by
+ *     the caller; it must not overlap the source.
+ * One kernel on `stream`; the source may be freed once the stream has passed it.
+ */
+moe_status moe_weights_prepare_size(const moe_qmat* in, int n_experts, size_t* bytes);
+moe_status moe_weights_prepare(moe_qmat* in_out, int n_experts, void* dst, size_t dst_bytes, moe_stream_t stream);
 
 /* ---------------------------------------------------------------- steps */
 
@@ -130,8 +156,9 @@ moe_status moe_permute(const int32_t* topk_ids, int T, int k, int E, int32_t* so
  * a fixed 262,400-byte array inside the library that every GPU which loads
  * the library keeps until the process exits.  Limit: T*k <= 65536 pairs
  * (larger sizes return MOE_ERR_INVALID_ARG); E <= 1024 as for moe_permute.
- * The first call on each device looks up that array's device address (with
- * the device current); make that first call outside any stream capture.
+ * Every call looks up that array's address in the current context; the first
+ * call in a context may load the library's device code, so make it outside
+ * any stream capture.
  * Every call on a device shares the array and zeroes its header first, so
  * two calls whose kernels overlap on the GPU (different streams, no ordering)
  * race: order them on one stream or with events.  Out-of-range ids are
@@ -270,6 +297,36 @@ moe_status moe_read_device_status(const moe_layer_plan* plan, int T, void* works
                                   moe_stream_t stream);
 moe_status moe_permute_read_device_status(int T, int k, int E, void* workspace, int32_t* code,
                                           moe_stream_t stream);
+
+/*
+ * moe_debug_set_waits -- test hook for the bounded device-side waits; off by
+ * default.  Every wait of the library's kernels on a copy or an MMA gives up
+ * after limit_ns nanoseconds (0 restores the default of 2 s), records
+ * MOE_ERR_TIMEOUT in the workspace status word, waits (within the same limit)
+ * for the copies its CTA still has in flight, releases what it holds and
+ * returns; the call's outputs are then undefined and moe_read_device_status
+ * reports the code.  stall = 1 makes the first wait of the chained decode,
+ * segmented GEMV and tensor-core kernels wait on a barrier that nothing
+ * completes, so that a test can run this path without a faulty input.
+ * Applies to calls launched after it, from any host thread (a graph keeps the
+ * setting it was captured with).  The failure reporting follows the pages'
+ * refusals by name with named exit codes ("bloomery README 0.3.11").
+ */
+moe_status moe_debug_set_waits(uint64_t limit_ns, int stall);
+
+/*
+ * moe_debug_set_stamps -- timing hook of the chained decode kernels (T <= 4); off by
+ * default (buf = NULL).  With a device buffer of at least 3*256*8*8 = 49,152 bytes, every
+ * chained call launched afterwards has thread 0 of CTA c (c < 256) of kernel n (0 router
+ * logits, 1 routing + gate/up, 2 down + combine) write the GPU's global nanosecond clock
+ * at phase ph into buf[(n*256 + c)*8 + ph] (uint64): n = 0: start, after the wait for the
+ * previous launch, end; n = 1: start, activations staged, after the wait, routed, first
+ * unit computed, units done, CTA done; n = 2: start, after the wait, inputs in shared
+ * memory, CTA done.  Calls overwrite the same slots; a graph keeps the setting it was
+ * captured with.  For measuring where a decode layer's time goes; the results are
+ * unchanged.
+ */
+moe_status moe_debug_set_stamps(void* buf, size_t bytes);
 
 /* The reason for the last non-MOE_OK status returned on this host thread. */
 const char* moe_last_error(void);

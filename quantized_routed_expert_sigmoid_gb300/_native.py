@@ -18,7 +18,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "moe_gb300.h")
 
 (MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE_CHECK,
  MOE_ERR_TIMEOUT) = range(7)
-MOE_F32, MOE_BF16, MOE_Q8_0, MOE_Q4_K = range(4)
+MOE_F32, MOE_BF16, MOE_Q8_0, MOE_Q4_K, MOE_Q8_0_R = range(5)
 MOE_ROUTE_SOFTMAX, MOE_ROUTE_SIGMOID_GROUP = range(2)
 
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
@@ -97,6 +97,10 @@ def _declare(lib):
         "moe_layer_debug_views": [P, I, P, ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P)],
         "moe_read_device_status": [P, I, P, ctypes.POINTER(ctypes.c_int32), P],
         "moe_permute_read_device_status": [I, I, I, P, ctypes.POINTER(ctypes.c_int32), P],
+        "moe_debug_set_waits": [ctypes.c_uint64, I],
+        "moe_debug_set_stamps": [P, S],
+        "moe_weights_prepare_size": [ctypes.POINTER(moe_qmat), I, PS],
+        "moe_weights_prepare": [ctypes.POINTER(moe_qmat), I, P, S, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -253,6 +257,27 @@ def moe_permute_read_device_status(T, k, E, workspace, stream=None) -> int:
     code = ctypes.c_int32(0)
     _check(load().moe_permute_read_device_status(T, k, E, _p(workspace), ctypes.byref(code), _stream(stream)))
     return code.value
+
+
+def moe_weights_prepare_size(m: moe_qmat, n_experts: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().moe_weights_prepare_size(ctypes.byref(m), n_experts, ctypes.byref(n)))
+    return n.value
+
+
+def moe_weights_prepare(m: moe_qmat, n_experts: int, dst, dst_bytes: int, stream=None) -> moe_qmat:
+    """Repacks m (Q8_0) into dst; returns the moe_qmat that describes the prepared tensor."""
+    out = moe_qmat(m.qtype, m.data, m.rows, m.cols, m.expert_stride_bytes)
+    _check(load().moe_weights_prepare(ctypes.byref(out), n_experts, _p(dst), dst_bytes, _stream(stream)))
+    return out
+
+
+def moe_debug_set_stamps(buf, nbytes: int):
+    _check(load().moe_debug_set_stamps(_p(buf), int(nbytes)))
+
+
+def moe_debug_set_waits(limit_ns: int, stall: int):
+    _check(load().moe_debug_set_waits(int(limit_ns), int(stall)))
 
 
 def moe_last_error() -> str:

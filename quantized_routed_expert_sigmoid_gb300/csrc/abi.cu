@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <new>
 #include <vector>
 
@@ -31,15 +32,16 @@ moe_status cuda_fail(cudaError_t err, const char* what) {
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 int64_t row_bytes(moe_dtype q, int64_t cols) {
-    if (q == MOE_Q4_K) return cols / kQ4KWeights * kQ4KBytes;
-    if (q == MOE_Q8_0) return cols / kQ80Weights * kQ80Bytes;
+    if (q == MOE_Q4_K || q == MOE_Q8_0 || q == MOE_Q8_0_R) return q_row_bytes(q, cols);
     return -1;
 }
+// The kernels' view of a weight type: Q8_0 in either layout is MOE_Q8_0, the layout a flag.
+int kernel_qtype(moe_dtype q) { return q == MOE_Q8_0_R ? (int)MOE_Q8_0 : (int)q; }
 
 moe_status check_qmat(const moe_qmat* m, const char* name, int64_t rows, int64_t cols, int E) {
     if (!m) return fail(MOE_ERR_INVALID_ARG, "%s: NULL matrix", name);
-    if (m->qtype != MOE_Q4_K && m->qtype != MOE_Q8_0)
-        return fail(MOE_ERR_UNSUPPORTED, "%s: qtype %d (supported: Q8_0, Q4_K)", name, (int)m->qtype);
+    if (m->qtype != MOE_Q4_K && m->qtype != MOE_Q8_0 && m->qtype != MOE_Q8_0_R)
+        return fail(MOE_ERR_UNSUPPORTED, "%s: qtype %d (supported: Q8_0, Q8_0_R, Q4_K)", name, (int)m->qtype);
     if (!m->data) return fail(MOE_ERR_INVALID_ARG, "%s: NULL data", name);
     if (!aligned(m->data, 16)) return fail(MOE_ERR_INVALID_ARG, "%s: data not 16-byte aligned", name);
     if (m->rows != rows || m->cols != cols)
@@ -87,6 +89,19 @@ FfnWs ffn_ws(int T, int k, int I) {
 
 moe_status moe::report(moe_status st, const char* msg) { return fail(st, "%s", msg); }
 
+namespace {
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_wait_stall{0};
+}  // namespace
+
+WaitCfg moe::wait_cfg() { return WaitCfg{g_wait_ns.load(), g_wait_stall.load()}; }
+
+namespace {
+std::atomic<void*> g_stamps{nullptr};
+}  // namespace
+
+void* moe::debug_stamps() { return g_stamps.load(); }
+
 struct moe_layer_plan {
     moe_layer_desc d;
 };
@@ -125,7 +140,7 @@ DecodeArgs decode_shape_args(const moe_layer_desc& d, int T) {
     da.Wr = d.W_router;
     da.bias = d.bias;
     da.T = T; da.H = d.hidden; da.I = d.intermediate;
-    da.qtype = d.gate.qtype;
+    da.qtype = kernel_qtype(d.gate.qtype);
     da.wg = static_cast<const uint8_t*>(d.gate.data);
     da.wu = static_cast<const uint8_t*>(d.up.data);
     da.wd = static_cast<const uint8_t*>(d.down.data);
@@ -133,7 +148,8 @@ DecodeArgs decode_shape_args(const moe_layer_desc& d, int T) {
     da.stride_d = d.down.expert_stride_bytes;
     da.I_s = d.shared_intermediate;
     if (da.I_s > 0) {
-        da.s_qtype = d.s_gate.qtype;
+        da.s_qtype = kernel_qtype(d.s_gate.qtype);
+        da.s_q80r = d.s_gate.qtype == MOE_Q8_0_R;
         da.sg = static_cast<const uint8_t*>(d.s_gate.data);
         da.su = static_cast<const uint8_t*>(d.s_up.data);
         da.sd = static_cast<const uint8_t*>(d.s_down.data);
@@ -180,7 +196,7 @@ LayerWs layer_ws(const moe_layer_desc& d, int T) {
     const bool chain = decode_chain_applies(d, T);
     w.chain = chain;
     // the chain normalizes its own input unless its shared expert is Q8_0 (staged from x apart)
-    w.norm_in_chain = chain && d.norm_gamma && !(Is > 0 && d.s_gate.qtype == MOE_Q8_0);
+    w.norm_in_chain = chain && d.norm_gamma && !(Is > 0 && kernel_qtype(d.s_gate.qtype) == MOE_Q8_0);
     w.u = take(d.norm_gamma && !w.norm_in_chain ? (size_t)T * H * 2 : 0);
     w.hq = take(chain ? P * (size_t)(I / 64) * 272 : 0);
     w.hq_s = take(chain && Is > 0 ? (size_t)T * (Is / 64) * 272 : 0);
@@ -196,7 +212,8 @@ T* at(void* base, size_t off) {
 GemvArgs gemv_args(const moe_qmat& m0, const moe_qmat* m1, int E, const void* vin, bool vin_bf16, int rows,
                    int K, const int32_t* sorted, const int32_t* offsets, int k, int n_pairs, float* out) {
     GemvArgs g{};
-    g.qtype = m0.qtype;
+    g.qtype = kernel_qtype(m0.qtype);
+    g.q80r = m0.qtype == MOE_Q8_0_R;
     g.gateup = m1 != nullptr;
     g.w0 = static_cast<const uint8_t*>(m0.data);
     g.w1 = m1 ? static_cast<const uint8_t*>(m1->data) : nullptr;
@@ -258,7 +275,58 @@ moe_status run_ffn(const moe_qmat& gate, const moe_qmat& up, const moe_qmat& dow
 extern "C" {
 
 const char* moe_last_error(void) { return g_err; }
+
+moe_status moe_debug_set_stamps(void* buf, size_t bytes) {
+    if (buf && (bytes < kStampBytes || !aligned(buf, 8)))
+        return fail(MOE_ERR_INVALID_ARG, "stamp buffer: %zu bytes (need %zu, 8-byte aligned)", bytes, kStampBytes);
+    g_stamps.store(buf);
+    return MOE_OK;
+}
+
+moe_status moe_debug_set_waits(uint64_t limit_ns, int stall) {
+    if (stall != 0 && stall != 1) return fail(MOE_ERR_INVALID_ARG, "stall must be 0 or 1");
+    g_wait_ns.store(limit_ns == 0 ? kDefaultWaitNs : limit_ns);
+    g_wait_stall.store(stall);
+    return MOE_OK;
+}
 const char* moe_version(void) { return "moe_gb300 0.1 (sm_103a)"; }
+
+moe_status moe_weights_prepare_size(const moe_qmat* in, int n_experts, size_t* bytes) {
+    if (!in || !bytes) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    if (n_experts < 1) return fail(MOE_ERR_INVALID_ARG, "n_experts = %d < 1", n_experts);
+    if (in->qtype == MOE_Q4_K) { *bytes = 0; return MOE_OK; }
+    if (in->qtype != MOE_Q8_0)
+        return fail(MOE_ERR_UNSUPPORTED, "moe_weights_prepare: qtype %d (it repacks Q8_0; Q4_K is used as stored)",
+                    (int)in->qtype);
+    if (in->rows < 1 || in->cols < kQ80Weights || in->cols % kQ80Weights)
+        return fail(MOE_ERR_INVALID_ARG, "shape %lldx%lld (cols a positive multiple of 32)", (long long)in->rows,
+                    (long long)in->cols);
+    *bytes = (size_t)n_experts * (size_t)in->rows * (size_t)q80r_row_bytes(in->cols);
+    return MOE_OK;
+}
+
+moe_status moe_weights_prepare(moe_qmat* in_out, int n_experts, void* dst, size_t dst_bytes, moe_stream_t stream) {
+    size_t need = 0;
+    moe_status st = moe_weights_prepare_size(in_out, n_experts, &need);
+    if (st) return st;
+    if (in_out->qtype == MOE_Q4_K) return MOE_OK;
+    if ((st = check_qmat(in_out, "in", in_out->rows, in_out->cols, n_experts))) return st;
+    if (!dst || !aligned(dst, 16)) return fail(MOE_ERR_INVALID_ARG, "dst NULL or not 16-byte aligned");
+    if (dst_bytes < need) return fail(MOE_ERR_WORKSPACE, "dst %zu bytes, need %zu", dst_bytes, need);
+    const uintptr_t s0 = (uintptr_t)in_out->data, d0 = (uintptr_t)dst;
+    const uintptr_t s1 = s0 + (size_t)(n_experts - 1) * (size_t)in_out->expert_stride_bytes +
+                         (size_t)in_out->rows * (size_t)row_bytes(MOE_Q8_0, in_out->cols);
+    if (d0 < s1 && s0 < d0 + need) return fail(MOE_ERR_INVALID_ARG, "dst overlaps the source");
+    const int64_t rb = q80r_row_bytes(in_out->cols);
+    cudaError_t err = launch_q80_repack(static_cast<const uint8_t*>(in_out->data), in_out->expert_stride_bytes,
+                                        n_experts, in_out->rows, in_out->cols, static_cast<uint8_t*>(dst),
+                                        reinterpret_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return cuda_fail(err, "repack kernel");
+    in_out->qtype = MOE_Q8_0_R;
+    in_out->data = dst;
+    in_out->expert_stride_bytes = in_out->rows * rb;
+    return MOE_OK;
+}
 
 moe_status moe_route(const moe_route_cfg* cfg, const void* x, moe_dtype x_type, int T, int H,
                      const float* W_router, const float* bias, const float* logits_in, float* logits_out,
@@ -556,7 +624,8 @@ moe_status moe_layer_timed(const moe_layer_plan* plan, const void* x, int T, flo
     const float* shared = nullptr;
     if (w.tc) {
         TcFfnArgs a{};
-        a.qtype = d.gate.qtype;
+        a.qtype = kernel_qtype(d.gate.qtype);
+        a.q80r = d.gate.qtype == MOE_Q8_0_R;
         a.wg = static_cast<const uint8_t*>(d.gate.data);
         a.wu = static_cast<const uint8_t*>(d.up.data);
         a.wd = static_cast<const uint8_t*>(d.down.data);
@@ -578,7 +647,8 @@ moe_status moe_layer_timed(const moe_layer_plan* plan, const void* x, int T, flo
         if (err != cudaSuccess) return cuda_fail(err, "tensor-core expert kernels");
         if (d.shared_intermediate > 0) {
             TcFfnArgs b = a;
-            b.qtype = d.s_gate.qtype;
+            b.qtype = kernel_qtype(d.s_gate.qtype);
+            b.q80r = d.s_gate.qtype == MOE_Q8_0_R;
             b.wg = static_cast<const uint8_t*>(d.s_gate.data);
             b.wu = static_cast<const uint8_t*>(d.s_up.data);
             b.wd = static_cast<const uint8_t*>(d.s_down.data);

@@ -42,10 +42,10 @@ constexpr int kCMaxP = 64;
 constexpr int kCMaxE = 256;
 constexpr int kK1Threads = 128;
 constexpr int kK3Threads = 256;
-constexpr int kK1MaxVec = 16;              // float4 of a router row per K1 thread: H <= 8192
+constexpr int kK1MaxVec = 4;               // float4 of a router row per K1 thread: H <= 2048
 constexpr int kChunkBlocks = 8;            // ring item: 8 Q4_K blocks (32 groups) of 4 rows
 constexpr int kSlotBytes = 4 * kChunkBlocks * kQ4KBytes;
-constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kStampCtas = 256, kStampPhases = 8;   // the timing hook's buffer: [3][256][8] uint64
 constexpr int kK2MaxWarps = 16;
 
 struct ChainParams {
@@ -62,6 +62,7 @@ struct ChainParams {
     const uint8_t* wd;
     int64_t stride_gu, stride_d;
     int I_s, s_q8;                          // shared expert: intermediate, 1 if Q8_0 (else Q4_K)
+    int s_q80r;                             // its Q8_0 rows in the repacked layout
     const uint8_t* sg;
     const uint8_t* su;
     const uint8_t* sd;
@@ -83,6 +84,9 @@ struct ChainParams {
     int rows_per_cta;                       // K3 output rows per CTA (multiple of 8)
     int k3_prefetch;                        // K3 copies its down rows to shared memory
     int k3_off_hs_s, k3_off_y, k3_off_w;    // K3 dynamic shared-memory offsets (bytes)
+    uint64_t wait_ns;                       // limit of every bounded wait
+    int stall;                              // test setting: K2's first wait never completes
+    uint64_t* stamps;                       // timing hook (NULL: off): [kernel][CTA][phase] globaltimer
 };
 
 // The routing every K2 CTA derives from the logits (shared memory).
@@ -142,6 +146,11 @@ __device__ __forceinline__ uint64_t gtime() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+// Timing hook: thread 0 of CTA c records the global time of phase ph of kernel kn.
+__device__ __forceinline__ void stamp(const ChainParams& p, int kn, int ph) {
+    if (p.stamps && threadIdx.x == 0 && blockIdx.x < kStampCtas)
+        p.stamps[((size_t)kn * kStampCtas + blockIdx.x) * kStampPhases + ph] = gtime();
+}
 __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
     uint32_t ok;
     // the suspend-time hint lets the warp sleep until the phase completes (or ~0.1 ms pass)
@@ -151,12 +160,12 @@ __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
                  : "memory");
     return ok != 0;
 }
-// Waits for the phase of parity `parity` to complete; false after kWaitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
+// Waits for the phase of parity `parity` to complete; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, uint64_t limit_ns) {
     if (mbar_test(b, parity)) return true;
     const uint64_t t0 = gtime();
     while (!mbar_test(b, parity))
-        if (gtime() - t0 > kWaitNs) return false;
+        if (gtime() - t0 > limit_ns) return false;
     return true;
 }
 // A bulk copy global -> shared whose bytes complete the transaction count of bar.
@@ -177,6 +186,7 @@ __device__ void cta_route(const ChainParams& p, CtaRoute& R) {
         warp_topk(p.rc, p.logits + (int64_t)warp * E, p.bias, R.sel[warp], R.sel[warp] + E, R.ids + warp * k,
                   R.w + warp * k);
     __syncthreads();
+    stamp(p, 1, 7);
     if (warp == 0) {
         for (int i = lane; i < P; i += 32) {
             const int ei = R.ids[i];
@@ -219,6 +229,9 @@ __device__ void cta_route(const ChainParams& p, CtaRoute& R) {
 }
 
 // ============================================================================ K1: router logits
+// The loops run over exactly NT tokens and H/512 <= kK1MaxVec float4 per thread: the kernel
+// runs once per layer on every SM, mostly waiting, so short straight code matters.
+template <int NT>
 __global__ void __launch_bounds__(kK1Threads) chain_logits_kernel(const __grid_constant__ ChainParams p) {
     __shared__ float s_part[kK1Threads / 32][kCMaxT];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -235,22 +248,24 @@ __global__ void __launch_bounds__(kK1Threads) chain_logits_kernel(const __grid_c
         if (j < n4) w[i] = ld_nc_v4(reinterpret_cast<const float4*>(p.Wr + (int64_t)e * H) + j);
         if (p.gamma && j < n4) gm[i] = ld_nc_v4(reinterpret_cast<const float4*>(p.gamma) + j);
     }
+    stamp(p, 0, 0);
     pdl_wait();                                   // x and the workspace belong to the launches before
     pdl_launch_dependents();
+    stamp(p, 0, 1);
     if (e == 0 && tid == 0) p.hdr->status = MOE_OK;
     const bool xb = p.x_bf16 != 0;
     // pre-norm: the tokens' RMSNorm scales, by all warps
     __shared__ float s_r[kCMaxT], s_rpart[kCMaxT][8];
     if (p.gamma) rms_scales_cta(reinterpret_cast<const float*>(p.x), T, H, p.eps, s_rpart, s_r);
-    float acc[kCMaxT];
+    float acc[NT];
 #pragma unroll
-    for (int t = 0; t < kCMaxT; ++t) acc[t] = 0.f;
+    for (int t = 0; t < NT; ++t) acc[t] = 0.f;
 #pragma unroll
     for (int i = 0; i < kK1MaxVec; ++i) {
         const int j = tid + i * kK1Threads;
         if (j < n4) {
 #pragma unroll
-            for (int t = 0; t < kCMaxT; ++t) {
+            for (int t = 0; t < NT; ++t) {
                 if (t < T) {
                     float4 xv = qd_load_vec4(p.x, xb, (int64_t)t * H + 4 * j);
                     if (p.gamma) xv = rms_apply4(xv, s_r[t], gm[i]);
@@ -263,17 +278,19 @@ __global__ void __launch_bounds__(kK1Threads) chain_logits_kernel(const __grid_c
         }
     }
 #pragma unroll
-    for (int t = 0; t < kCMaxT; ++t) {
+    for (int t = 0; t < NT; ++t) {
         const float v = warp_sum(acc[t]);
         if (lane == 0) s_part[warp][t] = v;
     }
     __syncthreads();
+    stamp(p, 0, 2);
     if (tid < T) {
         float s = 0.f;
 #pragma unroll
         for (int wi = 0; wi < kK1Threads / 32; ++wi) s += s_part[wi][tid];
         p.logits[(int64_t)tid * E + e] = s;
     }
+    stamp(p, 0, 3);
 }
 
 // ============================================================================ K2: routing + gate/up
@@ -294,10 +311,11 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
     float4* XS = reinterpret_cast<float4*>(X + (size_t)T * 16 * G);
     float4* xs_s = reinterpret_cast<float4*>(smem + p.k2_off_xs_s);
     uint8_t* cring = smem + p.k2_off_ring;          // two round slots: [32 gate rows][32 up rows]
-    __shared__ __align__(8) uint64_t c_bar[2];
+    __shared__ __align__(8) uint64_t c_bar[3];     // two ring slots; [2]: the test stall (never arrived on)
+    stamp(p, 1, 0);
     if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&c_bar[0])) : "memory");
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&c_bar[1])) : "memory");
+        for (int i = 0; i < 3; ++i)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&c_bar[i])) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -315,9 +333,12 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
             qd_stage<MOE_Q8_0>(src, xb, false, H, p.it_H_s, xs_s + (size_t)t * slots, tid, nthr);
         }
     }
+    stamp(p, 1, 1);
     pdl_wait();                                   // the logits of K1
     pdl_launch_dependents();
+    stamp(p, 1, 2);
     cta_route(p, R);
+    stamp(p, 1, 3);
     const int nact = R.nact;
     const int64_t rbH = (int64_t)(H / kQ4KWeights) * kQ4KBytes;
     const int half_I = I / 2;
@@ -356,7 +377,7 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
         if (warp == 0 && lane < nact && rows1 > rows0)
             prefetch_l2(p.wd + (int64_t)R.act_e[lane] * p.stride_d + rows0 * rbI, (int64_t)(rows1 - rows0) * rbI);
         if (warp == 0 && lane == 31 && has_shared && rows1 > rows0) {
-            const int64_t rbS = p.s_q8 ? (int64_t)(p.I_s / kQ80Weights) * kQ80Bytes
+            const int64_t rbS = p.s_q8 ? (p.s_q80r ? q80r_row_bytes(p.I_s) : (int64_t)(p.I_s / kQ80Weights) * kQ80Bytes)
                                        : (int64_t)(p.I_s / kQ4KWeights) * kQ4KBytes;
             if ((rbS % 16) == 0) prefetch_l2(p.sd + rows0 * rbS, (int64_t)(rows1 - rows0) * rbS);
         }
@@ -384,7 +405,9 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
     bool ok = true;
     int waited = 0, issued = min(2, n_rounds);
     for (int r = 0; r < n_rounds; ++r) {
-        const bool have = ok && mbar_wait(&c_bar[r & 1], (uint32_t)(r >> 1) & 1u);
+        // (test stall: the first round waits on a barrier that never completes)
+        const bool have = ok && (p.stall && r == 0 ? mbar_wait(&c_bar[2], 0u, p.wait_ns)
+                                                   : mbar_wait(&c_bar[r & 1], (uint32_t)(r >> 1) & 1u, p.wait_ns));
         if (ok && !have) {
             ok = false;
             if (tid == 0) atomicExch(&p.hdr->status, (int)MOE_ERR_TIMEOUT);
@@ -430,10 +453,12 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
         }
         if (warp < n)
             warp_stage_subblock(s_hq[r & 1][warp][lane], p.hq + (size_t)(st + warp) * vb, qd4_groups(I), r0 >> 5, lane);
+        if (r == 0) stamp(p, 1, 4);
     }
+    stamp(p, 1, 5);
     if (!ok && tid == 0) {
         // let no copy land after the CTA exits: wait (bounded) for the ones still in flight
-        for (int i = waited; i < issued; ++i) mbar_wait(&c_bar[i & 1], (uint32_t)(i >> 1) & 1u);
+        for (int i = waited; i < issued; ++i) mbar_wait(&c_bar[i & 1], (uint32_t)(i >> 1) & 1u, p.wait_ns);
     }
     __syncthreads();
     int round = n_rounds;                          // the shared expert's sub-blocks continue the s_hq parity
@@ -451,11 +476,12 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
 #pragma unroll
         for (int t = 0; t < NT; ++t) sv[t] = min(t, T - 1);
         if (kSh == 2) {
-            const int64_t rbS = (int64_t)(H / kQ80Weights) * kQ80Bytes;
+            const int64_t rbS = p.s_q80r ? q80r_row_bytes(H) : (int64_t)(H / kQ80Weights) * kQ80Bytes;
             const uint8_t* const rowp[4] = {p.sg + r0 * rbS, p.sg + (r0 + 1) * rbS, p.su + r0 * rbS,
                                             p.su + (r0 + 1) * rbS};
             qd_rows4<MOE_Q8_0, NT, false>(rowp, H / kQ80Weights, p.it_H_s, xs_s, p.it_H_s * 256,
-                                          reinterpret_cast<const float2*>(xs_s), 0, T, lane, sacc, sv);
+                                          reinterpret_cast<const float2*>(xs_s), 0, T, lane, sacc, sv,
+                                          p.s_q80r != 0);
         } else {
             const uint8_t* const rowp[4] = {p.sg + r0 * rbH, p.sg + (r0 + 1) * rbH, p.su + r0 * rbH,
                                             p.su + (r0 + 1) * rbH};
@@ -478,6 +504,10 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
             ++round;
         }
     }
+    }
+    if (p.stamps) {                               // (timing hook) the whole CTA is done
+        __syncthreads();
+        stamp(p, 1, 6);
     }
 }
 
@@ -503,8 +533,10 @@ __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_con
     uint4* SX = reinterpret_cast<uint4*>(smem + p.k3_off_hs_s);          // Q4_K shared expert: [T][16 GS] uint4
     const int GS = kSh == 1 ? qd4_groups(p.I_s) : 1;
     float4* SXS = reinterpret_cast<float4*>(SX + (size_t)T * 16 * GS);   // then [T][GS] float4
+    stamp(p, 2, 0);
     pdl_wait();                                   // h and the routing of K2
     pdl_launch_dependents();
+    stamp(p, 2, 1);
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_wbar)) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -515,6 +547,7 @@ __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_con
         s_w[i] = __ldcg(p.gw + i);
     }
     __syncthreads();
+    stamp(p, 2, 2);
     // ---- bulk copies into shared memory, all completing on one mbarrier: the CTA's down rows
     // of every pair (rows n0.. of one expert are contiguous: one copy per pair), and every
     // pair's h, which the gate/up kernel wrote already staged (one copy per pair)
@@ -545,16 +578,18 @@ __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_con
         float4* hs = reinterpret_cast<float4*>(smem + p.k3_off_hs_s);
         qd_stage_many_f32<MOE_Q8_0>(p.h_s, p.I_s, T, p.I_s, p.it_Is_s, hs, tid, kK3Threads);
     }
-    const bool landed = mbar_wait(&s_wbar, 0u);
+    stamp(p, 2, 3);
+    const bool landed = mbar_wait(&s_wbar, 0u, p.wait_ns);
     if (__syncthreads_or(!landed)) {
         // the copies did not complete in time: report it; let none land after the CTA exits
         if (tid == 0) {
             atomicExch(&p.hdr->status, (int)MOE_ERR_TIMEOUT);
-            mbar_wait(&s_wbar, 0u);
+            mbar_wait(&s_wbar, 0u, p.wait_ns);
         }
         __syncthreads();
         return;
     }
+    stamp(p, 2, 4);
     const int nsub = R / 8;
     const int n_routed = P * nsub;
     const int n_shared = has_shared ? R / 4 : 0;
@@ -591,13 +626,14 @@ __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_con
 #pragma unroll
             for (int t = 0; t < NT; ++t) vidx[t] = min(t, T - 1);
             if (kSh == 2) {
-                const int64_t rbS = (int64_t)(p.I_s / kQ80Weights) * kQ80Bytes;
+                const int64_t rbS = p.s_q80r ? q80r_row_bytes(p.I_s) : (int64_t)(p.I_s / kQ80Weights) * kQ80Bytes;
                 const uint8_t* rowp[4];
 #pragma unroll
                 for (int r = 0; r < 4; ++r) rowp[r] = nb + r < H ? p.sd + (int64_t)(nb + r) * rbS : nullptr;
                 const float4* hs = reinterpret_cast<const float4*>(smem + p.k3_off_hs_s);
                 qd_rows4<MOE_Q8_0, NT, false>(rowp, p.I_s / kQ80Weights, p.it_Is_s, hs, p.it_Is_s * 256,
-                                              reinterpret_cast<const float2*>(hs), 0, T, lane, acc, vidx);
+                                              reinterpret_cast<const float2*>(hs), 0, T, lane, acc, vidx,
+                                              p.s_q80r != 0);
             } else {
                 const int64_t rbS = (int64_t)(p.I_s / kQ4KWeights) * kQ4KBytes;
                 const uint8_t* rowp[4];
@@ -612,6 +648,7 @@ __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_con
         }
     }
     __syncthreads();
+    stamp(p, 2, 5);
     // ---- combine: out[t][n] = ((sum_j w_tj * y_(t,j)[n]) + shared) (+ old out)
     for (int idx = tid; idx < T * R; idx += kK3Threads) {
         const int t = idx / R, nl = idx - t * R, n = n0 + nl;
@@ -622,6 +659,10 @@ __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_con
         float* o = p.out + (int64_t)t * H + n;
         if (p.accumulate) acc += *o;
         *o = acc;
+    }
+    if (p.stamps) {                               // (timing hook) the whole CTA is done
+        __syncthreads();
+        stamp(p, 2, 6);
     }
 }
 
@@ -693,7 +734,7 @@ cudaError_t launch_chain_nt(const ChainParams& p, const ChainLayout& L, int E, c
     cfg.gridDim = dim3(E);
     cfg.blockDim = dim3(kK1Threads);
     cfg.dynamicSmemBytes = 0;
-    if ((err = cudaLaunchKernelEx(&cfg, chain_logits_kernel, p)) != cudaSuccess) return err;
+    if ((err = cudaLaunchKernelEx(&cfg, chain_logits_kernel<NT>, p)) != cudaSuccess) return err;
     if (evb && (err = cudaEventRecord(evb, s)) != cudaSuccess) return err;
     if ((err = cudaFuncSetAttribute(chain_gateup_kernel<NT, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)L.k2_smem)) != cudaSuccess)
@@ -727,6 +768,7 @@ ChainParams chain_params(const DecodeArgs& a, const ChainLayout& L) {
     p.wg = a.wg; p.wu = a.wu; p.wd = a.wd;
     p.stride_gu = a.stride_gu; p.stride_d = a.stride_d;
     p.I_s = a.I_s; p.s_q8 = (a.I_s > 0 && a.s_qtype == MOE_Q8_0) ? 1 : 0;
+    p.s_q80r = (p.s_q8 && a.s_q80r) ? 1 : 0;
     p.sg = a.sg; p.su = a.su; p.sd = a.sd;
     p.logits = a.logits; p.ids = a.ids; p.gw = a.gw; p.sorted = a.sorted; p.offsets = a.offsets;
     p.pair_pos = a.pair_pos;
@@ -736,6 +778,9 @@ ChainParams chain_params(const DecodeArgs& a, const ChainLayout& L) {
     p.k2_warps = L.k2_warps; p.k2_off_xs_s = L.k2_off_xs_s; p.k2_off_ring = L.k2_off_ring;
     p.rows_per_cta = L.rows_per_cta; p.k3_prefetch = L.k3_prefetch;
     p.k3_off_hs_s = L.k3_off_hs_s; p.k3_off_y = L.k3_off_y; p.k3_off_w = L.k3_off_w;
+    const WaitCfg wc = wait_cfg();
+    p.wait_ns = wc.limit_ns; p.stall = wc.stall;
+    p.stamps = static_cast<uint64_t*>(debug_stamps());
     return p;
 }
 

@@ -29,7 +29,6 @@ constexpr int kSMaxE = 256;
 constexpr int kSChunkBlocks = 8;                       // gate/up item: 8 blocks of 4 rows
 constexpr int kSSlotBytes = 4 * kSChunkBlocks * kQ4KBytes;
 constexpr int kSDownBlocks = 4;                        // down item: 4 blocks of 8 rows
-constexpr uint64_t kSWaitNs = 2000000000ull;
 
 struct SegParams {
     const void* vin;                 // gate/up: x [T][H] (bf16 or fp32); down: h fp32 [P][I]
@@ -43,6 +42,8 @@ struct SegParams {
     float* out;                      // gate/up: h [P][I]; down: y [P][H]
     WsHeader* hdr;
     int nt_max;                      // tokens per staging pass (<= NT)
+    uint64_t wait_ns;                // limit of every bounded wait
+    int stall;                       // test setting: each warp's first wait never completes
 };
 
 __host__ __device__ inline size_t seg_align(size_t v) { return (v + 127) & ~(size_t)127; }
@@ -60,11 +61,11 @@ __device__ __forceinline__ bool s_test(uint64_t* b, uint32_t parity) {
                  : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ bool s_wait(uint64_t* b, uint32_t parity) {
+__device__ __forceinline__ bool s_wait(uint64_t* b, uint32_t parity, uint64_t limit_ns) {
     if (s_test(b, parity)) return true;
     const uint64_t t0 = s_time();
     while (!s_test(b, parity))
-        if (s_time() - t0 > kSWaitNs) return false;
+        if (s_time() - t0 > limit_ns) return false;
     return true;
 }
 __device__ __forceinline__ void s_bulk(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -169,9 +170,11 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_gateup_kernel(const __grid_c
     uint4* X = reinterpret_cast<uint4*>(smem);
     float4* XS = reinterpret_cast<float4*>(X + (size_t)NT * 16 * G);
     uint8_t* ring = smem + seg_align((size_t)NT * qd4_vec_bytes(H)) + (size_t)warp * 2 * kSSlotBytes;
+    __shared__ __align__(8) uint64_t s_never;          // test stall: initialized, never arrived on
     if (lane == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s_u32(&s_bar[warp][0])) : "memory");
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s_u32(&s_bar[warp][1])) : "memory");
+        if (warp == 0) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s_u32(&s_never)) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     seg_plan(p.offsets, p.E, half_I, p.nt_max, s_plan);
@@ -195,8 +198,11 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_gateup_kernel(const __grid_c
             __syncthreads();
             qd4_stage_par(p.vin, p.vin_bf16 != 0, false, H, nt, s_rows, H, X, XS, tid, kSThreads);
             __syncthreads();
+            int issued = 0, waited = 0;                    // items copied / landed in this pass
             auto issue = [&](int item) {
-                if (lane != 0 || item >= n_items || !ok) return;
+                if (item >= n_items || !ok) return;
+                issued = item + 1;
+                if (lane != 0) return;
                 const int u = u0 + warp + (item / nch) * kSWarps, ch = item - (item / nch) * nch;
                 const int r0 = 2 * u;
                 const int b0 = ch * kSChunkBlocks, nb = min(kSChunkBlocks, nblk - b0);
@@ -222,7 +228,10 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_gateup_kernel(const __grid_c
             float acc[4][NT];
             for (int item = 0; item < n_items; ++item) {
                 const uint32_t slot = (gi + item) & 1u, par = ((gi + item) >> 1) & 1u;
-                const bool have = ok && s_wait(&s_bar[warp][slot], par);
+                // (test stall: the warp's first wait is on a barrier that never completes)
+                uint64_t* wbar = p.stall && gi + item == 0 ? &s_never : &s_bar[warp][slot];
+                const bool have = ok && s_wait(wbar, wbar == &s_never ? 0u : par, p.wait_ns);
+                if (have) waited = item + 1;
                 if (ok && !have) {
                     ok = false;
                     if (lane == 0 && p.hdr) atomicExch(&p.hdr->status, (int)MOE_ERR_TIMEOUT);
@@ -264,8 +273,9 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_gateup_kernel(const __grid_c
                 }
             }
             // the items of this pass are all consumed (or, after a timeout, waited for below)
+            // after a timeout: wait (bounded) for the copies this warp issued and never saw land
             if (!ok && lane == 0)
-                for (int i = 0; i < n_items; ++i) s_wait(&s_bar[warp][(gi + i) & 1u], ((gi + i) >> 1) & 1u);
+                for (int i = waited; i < issued; ++i) s_wait(&s_bar[warp][(gi + i) & 1u], ((gi + i) >> 1) & 1u, p.wait_ns);
             gi += ok ? n_items : 0;
             __syncwarp();
         }
@@ -295,9 +305,11 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_down_kernel(const __grid_con
     uint4* X = reinterpret_cast<uint4*>(smem);
     float4* XS = reinterpret_cast<float4*>(X + (size_t)NT * 16 * GI);
     uint8_t* ring = smem + seg_align((size_t)NT * qd4_vec_bytes(I)) + (size_t)warp * 2 * kSSlotBytes;
+    __shared__ __align__(8) uint64_t s_never;          // test stall: initialized, never arrived on
     if (lane == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s_u32(&s_bar[warp][0])) : "memory");
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s_u32(&s_bar[warp][1])) : "memory");
+        if (warp == 0) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s_u32(&s_never)) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     seg_plan(p.offsets, p.E, upe, p.nt_max, s_plan);
@@ -321,8 +333,11 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_down_kernel(const __grid_con
             __syncthreads();
             qd4_stage_par(p.vin, false, true, I, nt, s_rows, I, X, XS, tid, kSThreads);
             __syncthreads();
+            int issued = 0, waited = 0;                    // items copied / landed in this pass
             auto issue = [&](int item) {
-                if (lane != 0 || item >= n_items || !ok) return;
+                if (item >= n_items || !ok) return;
+                issued = item + 1;
+                if (lane != 0) return;
                 const int u = u0 + warp + (item / ncd) * kSWarps, ch = item - (item / ncd) * ncd;
                 const int n0 = kRowsU * u;
                 const int b0 = ch * kBlocksI, nb = min(kBlocksI, nblk - b0);
@@ -343,7 +358,10 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_down_kernel(const __grid_con
             float acc[4][NT];
             for (int item = 0; item < n_items; ++item) {
                 const uint32_t slot = (gi + item) & 1u, par = ((gi + item) >> 1) & 1u;
-                const bool have = ok && s_wait(&s_bar[warp][slot], par);
+                // (test stall: the warp's first wait is on a barrier that never completes)
+                uint64_t* wbar = p.stall && gi + item == 0 ? &s_never : &s_bar[warp][slot];
+                const bool have = ok && s_wait(wbar, wbar == &s_never ? 0u : par, p.wait_ns);
+                if (have) waited = item + 1;
                 if (ok && !have) {
                     ok = false;
                     if (lane == 0 && p.hdr) atomicExch(&p.hdr->status, (int)MOE_ERR_TIMEOUT);
@@ -404,8 +422,9 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_down_kernel(const __grid_con
                     }
                 }
             }
+            // after a timeout: wait (bounded) for the copies this warp issued and never saw land
             if (!ok && lane == 0)
-                for (int i = 0; i < n_items; ++i) s_wait(&s_bar[warp][(gi + i) & 1u], ((gi + i) >> 1) & 1u);
+                for (int i = waited; i < issued; ++i) s_wait(&s_bar[warp][(gi + i) & 1u], ((gi + i) >> 1) & 1u, p.wait_ns);
             gi += ok ? n_items : 0;
             __syncwarp();
         }
@@ -467,6 +486,8 @@ cudaError_t launch_seg_gemv(bool gateup, const void* vin, bool vin_bf16, const i
     p.vin = vin; p.vin_bf16 = vin_bf16 ? 1 : 0; p.sorted_pairs = sorted_pairs; p.offsets = offsets;
     p.E = E; p.k = k; p.K = K; p.rows = rows; p.w0 = w0; p.w1 = w1; p.expert_stride = expert_stride;
     p.out = out; p.hdr = hdr;
+    const WaitCfg wc = wait_cfg();
+    p.wait_ns = wc.limit_ns; p.stall = wc.stall;
     // tokens per staging pass: the largest of 8, 4, 2, 1 whose staged vectors fit, and not
     // more than one expert can hold
     const int cap = std::max(1, max_tokens);

@@ -24,8 +24,8 @@
 // (which also counts the TMA bytes of B(g)), then issues raw and B of step g + D (D = 2 for
 // gate/up, 3 for down, across tile boundaries); the MMA warp waits full[g%4], issues four
 // k-substeps and commits to empty[g%4].  Every wait is bounded (globaltimer); on timeout
-// the kernel records MOE_ERR_TIMEOUT, drains its MMAs, lets copies in flight land, frees
-// TMEM and returns.
+// the kernel records MOE_ERR_TIMEOUT, drains its MMAs, waits (bounded) on the barriers of
+// the copies still in flight, frees TMEM and returns.
 #include <algorithm>
 #include <cuda.h>   // CUtensorMap and its enums (the encoder is fetched from the driver at run time)
 
@@ -62,6 +62,12 @@ __device__ __forceinline__ float s8_f(uint32_t word, int b) {    // signed byte 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+// fp16 operands and outputs: a value that rounds to inf (or is NaN) is reported, not hidden.
+__device__ __forceinline__ bool half_finite(__half h) { return (__half_as_ushort(h) & 0x7C00u) != 0x7C00u; }
+// One report per warp: the status word becomes MOE_ERR_DEVICE_CHECK unless it holds an error.
+__device__ __forceinline__ void report_out_of_range(bool bad, int lane, WsHeader* hdr) {
+    if (__any_sync(0xffffffffu, bad) && lane == 0 && hdr) atomicCAS(&hdr->status, (int)MOE_OK, (int)MOE_ERR_DEVICE_CHECK);
 }
 
 // Eight fp16 weights of one Q4_K word into two 16-byte halves of a chunk: the low nibbles of
@@ -142,6 +148,8 @@ struct TcParams {
     float* y_out;                // DOWN: [P][rows] fp32, or
     __half* y16_out;             //       [P][rows] fp16 when set
     WsHeader* hdr;
+    uint64_t wait_ns;            // limit of every bounded wait
+    int stall;                   // test setting: the MMA warp's first wait never completes
 };
 
 // The full tile description for tile index t.
@@ -201,13 +209,17 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
     uint64_t* drain = bar + 12;      // [1]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 13);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 14);
+    uint64_t* never = bar + 15;      // [1]: the test stall (initialized, never arrived on)
+    int* max_issued = reinterpret_cast<int*>(bar + 16);   // k-steps the producers issued (abort drain)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int i = 0; i < 4; ++i) { mbar_init(&full[i], kPW); mbar_init(&empty[i], 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(&accf[i], 1); mbar_init(&tfree[i], kEpiWarps > 0 ? kEpiWarps : 1); }
         mbar_init(drain, 1);
+        mbar_init(never, 1);
         *abort_flag = 0;
+        *max_issued = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tmap_b) : "memory");
     }
@@ -227,8 +239,10 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
     const int n_tiles = n_tb * n_mb;
     const int nk = p.K / kBK;
     const int nblk_row = QT == MOE_Q4_K ? p.K / kQ4KWeights : p.K / kQ80Weights;
-    const int64_t rb = (int64_t)nblk_row * (QT == MOE_Q4_K ? kQ4KBytes : kQ80Bytes);
+    const int64_t rb = QT == MOE_Q4_K ? (int64_t)nblk_row * kQ4KBytes
+                                      : (QT == MOE_Q8_0_R ? q80r_row_bytes(p.K) : (int64_t)nblk_row * kQ80Bytes);
 
+    int n_issued = 0, n_arrived = 0;                // producers: k-steps issued / arrived on full[]
     if (warp < kPW) {
         // ======================= producers (+ GATEUP epilogue) =======================
         const int prow = tid & 127;                 // weight row within the tile
@@ -291,6 +305,12 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
                 const uint8_t* qs = blk + 16 + 32 * (kb & 3) + (32 / kSplit) * part;
                 if constexpr (kSplit == 2) cp_async16(dst + 16, qs, 16u);
                 else cp_async8(dst + 16, qs);
+            } else if (QT == MOE_Q8_0_R) {
+                // repacked: the k-step's 64 quants (16-byte aligned), then its two scales
+                const uint8_t* qsrc = is_wrow + (int64_t)kb * 64;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) cp_async16(dst + 16 * w, qsrc + 16 * w, 16u);
+                cp_async4(dst + 64, is_wrow + (int64_t)nblk_row * 32 + 4 * kb);
             } else {
                 const uint8_t* src = is_wrow + (int64_t)kb * 2 * kQ80Bytes;     // two blocks, 68 bytes
 #pragma unroll
@@ -299,6 +319,7 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
         };
         // issue global k-step gs (the cursor's) and advance the cursor; always one commit group
         auto issue_next = [&](uint32_t gs) {
+            n_issued = (int)gs + 1;
             if (is_valid) {
                 issue_raw(is_kb, gs % kRawSlots);
                 issue_b(is_kb, gs % kBStages);
@@ -323,7 +344,7 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
             for (int kb = 0; kb < nk; ++kb, ++g) {
                 // A stage g%2 was last read by MMA(g-2) (with kDist == 3 already waited for below)
                 if (kDist == 2 && g >= 2 &&
-                    !mbar_wait(&empty[(g + 2) & 3], ((g - 2) >> 2) & 1, abort_flag)) { ok = false; break; }
+                    !mbar_wait(&empty[(g + 2) & 3], ((g - 2) >> 2) & 1, abort_flag, p.wait_ns)) { ok = false; break; }
                 cp_wait<kDist - 1>();                // raw(g) has landed (only later steps may be pending)
                 // ---- dequantize k-step kb into A stage g%2
                 const uint8_t* raw = sRaw + (g % kRawSlots) * kRawSlotBytes + tid * kRawBytes;
@@ -353,17 +374,17 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
                         *reinterpret_cast<uint4*>(arow + swz(prow, 4 + ch)) = make_uint4(ha[0], ha[1], hb[0], hb[1]);
                     }
                 } else {
-                    // Q8_0: 68 bytes = d0, q0[32], d1, q1[32]
+                    // Q8_0: 68 bytes = d0, q0[32], d1, q1[32]; repacked: q0[32], q1[32], d0, d1
                     uint32_t wv[17];
 #pragma unroll
                     for (int w = 0; w < 17; ++w) wv[w] = reinterpret_cast<const uint32_t*>(raw)[w];
-                    const float d0 = __half2float(__ushort_as_half((unsigned short)(wv[0] & 0xFFFFu)));
-                    const float d1 = __half2float(__ushort_as_half((unsigned short)(wv[8] >> 16)));
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        if (kSplit == 2 && (ch >> 2) != part) continue;       // DOWN: this thread's block only
-                        const int b0 = ch < 4 ? 2 + 8 * ch : 36 + 8 * (ch - 4);
-                        const float d = ch < 4 ? d0 : d1;
+                    const uint32_t dw0 = QT == MOE_Q8_0_R ? wv[16] & 0xFFFFu : wv[0] & 0xFFFFu;
+                    const uint32_t dw1 = QT == MOE_Q8_0_R ? wv[16] >> 16 : wv[8] >> 16;
+                    const float d0 = __half2float(__ushort_as_half((unsigned short)dw0));
+                    const float d1 = __half2float(__ushort_as_half((unsigned short)dw1));
+                    // 8 weights (chunk ch of the k-step) from byte b0 of the 68 with scale d; the byte
+                    // offsets stay compile-time constants, so wv stays in registers
+                    auto chunk = [&](int ch, int b0, float d) {
                         float v[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
@@ -373,6 +394,19 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
                         *reinterpret_cast<uint4*>(arow + swz(prow, ch)) =
                             make_uint4(pack_h2(v[0], v[1]), pack_h2(v[2], v[3]), pack_h2(v[4], v[5]),
                                        pack_h2(v[6], v[7]));
+                    };
+                    if (QT == MOE_Q8_0_R) {
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch) {
+                            if (kSplit == 2 && (ch >> 2) != part) continue;   // DOWN: this thread's block only
+                            chunk(ch, 8 * ch, ch < 4 ? d0 : d1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch) {
+                            if (kSplit == 2 && (ch >> 2) != part) continue;
+                            chunk(ch, ch < 4 ? 2 + 8 * ch : 36 + 8 * (ch - 4), ch < 4 ? d0 : d1);
+                        }
                     }
                 }
                 // every thread makes its own A writes visible to the tensor core's (async) proxy;
@@ -380,20 +414,22 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
                 fence_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full[g & 3]);
+                n_arrived = (int)g + 1;
                 // B stage (g + kDist) % 4 was last read by MMA(g + kDist - 4)
                 if (kDist == 3 && g >= 1 &&
-                    !mbar_wait(&empty[(g - 1) & 3], ((g - 1) >> 2) & 1, abort_flag)) { ok = false; break; }
+                    !mbar_wait(&empty[(g - 1) & 3], ((g - 1) >> 2) & 1, abort_flag, p.wait_ns)) { ok = false; break; }
                 issue_next(g + kDist);
             }
             if (!ok) break;
             if constexpr (MODE == kGateUp) {
                 // ---- epilogue: wait for the accumulators of this tile, h = SiLU(gate) * up
-                if (!mbar_wait(&accf[0], tile_iter & 1, abort_flag)) break;
+                if (!mbar_wait(&accf[0], tile_iter & 1, abort_flag, p.wait_ns)) break;
                 tc_after();
                 // warp w reads TMEM lanes 32 (w % 4).. and every (kPW / 4)-th group of 16 columns
                 const int q = warp & 3;
                 const int m = q * 32 + lane;
                 __half* hrow = p.h_out + (int64_t)ti.tok0 * p.rows + ti.m0 + m;
+                bool out_of_range = false;               // an h value beyond the fp16 range
                 for (int c16 = (warp >> 2) * 16; c16 < ti.n_inst; c16 += 16 * (kPW / 4)) {
                     uint32_t a[16], u[16];
                     tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c16, a);
@@ -404,14 +440,18 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
                         const int col = c16 + j;
                         if (col < ti.ntok) {
                             const float gv = __uint_as_float(a[j]), uv = __uint_as_float(u[j]);
-                            hrow[(int64_t)col * p.rows] = __float2half_rn(__fdividef(gv, 1.0f + __expf(-gv)) * uv);
+                            const __half hv = __float2half_rn(__fdividef(gv, 1.0f + __expf(-gv)) * uv);
+                            out_of_range |= !half_finite(hv);
+                            hrow[(int64_t)col * p.rows] = hv;
                         }
                     }
                 }
+                report_out_of_range(out_of_range, lane, p.hdr);
                 tc_before();
             }
         }
         cp_wait_all();
+        if (lane == 0) atomicMax(max_issued, n_issued);
     } else if (warp < kMmaWarp) {
         // ======================= DOWN epilogue warps =======================
         // epilogue warp e reads TMEM lanes 32q.. (q = warp % 4) and the 64-column chunks
@@ -425,13 +465,14 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
             TileInfo ti;
             if (!tile_at(p, n_mb, t, n_tb, ti)) break;
             const int b = j & 1;
-            if (!mbar_wait(&accf[b], (j >> 1) & 1, abort_flag)) break;
+            if (!mbar_wait(&accf[b], (j >> 1) & 1, abort_flag, p.wait_ns)) break;
             tc_after();
             const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)b * kAccCols;
             // fp16: lanes 2i, 2i+1 swap one value so that each stores rows (m & ~1, m | 1) of one
             // column as a pair (even lane: even column, odd lane: odd column)
             __half* y16row = p.y16_out + (int64_t)(ti.tok0 + (odd ? 1 : 0)) * p.rows + ti.m0 + (m & ~1);
             float* yrow = p.y_out + (int64_t)ti.tok0 * p.rows + ti.m0 + m;
+            bool out_of_range = false;                   // a y value beyond the fp16 range
             for (int c64 = 64 * chunk0; c64 < ti.n_inst; c64 += 128) {
                 uint32_t a[4][16];
 #pragma unroll
@@ -447,8 +488,10 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
                             const float keep = odd ? v1 : v0;
                             const __half2 hv = odd ? __floats2half2_rn(recv, keep) : __floats2half2_rn(keep, recv);
                             const int col = c64 + 16 * i + jj;          // this lane stores column col + odd
-                            if (col + (odd ? 1 : 0) < ti.ntok)
+                            if (col + (odd ? 1 : 0) < ti.ntok) {
+                                out_of_range |= !half_finite(__low2half(hv)) || !half_finite(__high2half(hv));
                                 *reinterpret_cast<__half2*>(y16row + (int64_t)col * p.rows) = hv;
+                            }
                         }
                 } else {
 #pragma unroll
@@ -460,6 +503,7 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
                         }
                 }
             }
+            report_out_of_range(out_of_range, lane, p.hdr);
             tc_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tfree[b]);
@@ -477,13 +521,14 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
             // the accumulator buffer's previous tile has been read out (GATEUP: the producers
             // only reach this tile's first k-step after their epilogue)
             if (kEpiWarps > 0 && j >= kAccBufs) {
-                if (!mbar_wait(&tfree[b], ((j / kAccBufs) - 1) & 1, abort_flag)) break;
+                if (!mbar_wait(&tfree[b], ((j / kAccBufs) - 1) & 1, abort_flag, p.wait_ns)) break;
                 tc_after();
             }
             const uint32_t acc = tmem + (uint32_t)b * kAccCols;
             bool ok = true;
             for (int kb = 0; kb < nk; ++kb, ++g) {
-                if (!mbar_wait(&full[g & 3], (g >> 2) & 1, abort_flag)) { ok = false; break; }
+                uint64_t* fb = p.stall && g == 0 ? never : &full[g & 3];     // (test stall)
+                if (!mbar_wait(fb, fb == never ? 0u : (g >> 2) & 1, abort_flag, p.wait_ns)) { ok = false; break; }
                 tc_after();
                 if (lane == 0) {
                     const uint32_t a0 = su32(sA + (g % kAStages) * kAStageBytes);
@@ -507,22 +552,30 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
         if (issued) {
             if (lane == 0) mma_commit(drain);
             __syncwarp();
-            const uint64_t t0 = gtime();
-            while (!mbar_test(drain, 0)) {
-                if (gtime() - t0 > kWaitLimitNs) break;
-            }
+            mbar_wait_for(drain, 0, p.wait_ns);
         }
     }
-    if (*abort_flag && tid == 0) atomicCAS(&p.hdr->status, (int)MOE_OK, (int)MOE_ERR_TIMEOUT);
     tc_before();
     __syncthreads();
     tc_after();
     if (*abort_flag) {
-        // after a timeout, give copies still in flight (TMA, cp.async) time to land before the
-        // CTA's shared memory is released
-        const uint64_t t0 = gtime();
-        while (gtime() - t0 < 1000000ull) {
+        // every thread has left its loop.  The producers' raw copies (cp.async) are waited for;
+        // the token rows (TMA) of the last k-steps may still be in flight.  Each producer warp
+        // arrives on full[] for the k-steps it has not arrived on, up to the last one any warp
+        // issued, so that the phase of each such step completes exactly when its bytes land.
+        // Steps older than the last four completed already: a producer issues step s only after
+        // the MMAs of step s - 4, which waited for its phase.
+        if (warp < kPW && lane == 0)
+            for (int s = n_arrived; s < *max_issued; ++s) mbar_arrive(&full[s & 3]);
+        __syncthreads();
+        if (tid == 0) {
+            atomicCAS(&p.hdr->status, (int)MOE_OK, (int)MOE_ERR_TIMEOUT);
+            const int last = *max_issued;
+            for (int s = max(0, last - 4); s < last; ++s) mbar_wait_for(&full[s & 3], (uint32_t)(s >> 2) & 1u, p.wait_ns);
         }
+        tc_before();
+        __syncthreads();
+        tc_after();
     }
     if (warp == kMmaWarp) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
@@ -565,19 +618,27 @@ __global__ void __launch_bounds__(1024) tile_list_kernel(const int32_t* __restri
     if (threadIdx.x == 0) list[0] = make_int4(total, 0, 0, 0);
 }
 
-__global__ void to_half_kernel(const void* __restrict__ x, bool bf16, int64_t n, __half* __restrict__ out) {
+__global__ void to_half_kernel(const void* __restrict__ x, bool bf16, int64_t n, __half* __restrict__ out,
+                               WsHeader* hdr) {
     const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
-    if (i >= n) return;
-    float v[4];
-    if (bf16) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(x) + i);
-        v[0] = __uint_as_float(raw.x << 16); v[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-        v[2] = __uint_as_float(raw.y << 16); v[3] = __uint_as_float(raw.y & 0xFFFF0000u);
-    } else {
-        const float4 f = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(x) + i);
-        v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    bool bad = false;
+    if (i < n) {
+        float v[4];
+        if (bf16) {
+            const uint2 raw = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(x) + i);
+            v[0] = __uint_as_float(raw.x << 16); v[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+            v[2] = __uint_as_float(raw.y << 16); v[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+        } else {
+            const float4 f = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(x) + i);
+            v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+        }
+        const uint2 h = make_uint2(pack_h2(v[0], v[1]), pack_h2(v[2], v[3]));
+        *reinterpret_cast<uint2*>(out + i) = h;
+        // x beyond the fp16 range (or not finite) has no fp16 operand: report it
+        bad = ((h.x & 0x7C00u) == 0x7C00u) || ((h.x & 0x7C000000u) == 0x7C000000u) ||
+              ((h.y & 0x7C00u) == 0x7C00u) || ((h.y & 0x7C000000u) == 0x7C000000u);
     }
-    *reinterpret_cast<uint2*>(out + i) = make_uint2(pack_h2(v[0], v[1]), pack_h2(v[2], v[3]));
+    report_out_of_range(bad, threadIdx.x & 31, hdr);
 }
 
 template <int QT, int MODE>
@@ -644,9 +705,11 @@ cudaError_t launch_tc(const TcParams& p, int max_tiles, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// The weight type as a template: Q4_K, Q8_0 in GGUF blocks, or Q8_0 repacked (MOE_Q8_0_R).
 template <int MODE>
-cudaError_t launch_tc_q(int qtype, const TcParams& p, int max_tiles, cudaStream_t s) {
-    return qtype == MOE_Q4_K ? launch_tc<MOE_Q4_K, MODE>(p, max_tiles, s) : launch_tc<MOE_Q8_0, MODE>(p, max_tiles, s);
+cudaError_t launch_tc_q(int qtype, bool q80r, const TcParams& p, int max_tiles, cudaStream_t s) {
+    if (qtype == MOE_Q4_K) return launch_tc<MOE_Q4_K, MODE>(p, max_tiles, s);
+    return q80r ? launch_tc<MOE_Q8_0_R, MODE>(p, max_tiles, s) : launch_tc<MOE_Q8_0, MODE>(p, max_tiles, s);
 }
 
 }  // namespace
@@ -657,7 +720,7 @@ size_t tc_tile_list_bytes(int T, int k, int E) {
 }
 
 bool tc_supported(int qtype, int rows_gu, int K_gu) {
-    return (qtype == MOE_Q4_K || qtype == MOE_Q8_0) && rows_gu % kBM == 0 && K_gu % kBK == 0 &&
+    return (qtype == MOE_Q4_K || qtype == MOE_Q8_0 || qtype == MOE_Q8_0_R) && rows_gu % kBM == 0 && K_gu % kBK == 0 &&
            (qtype != MOE_Q4_K || K_gu % kQ4KWeights == 0);
 }
 
@@ -668,7 +731,7 @@ cudaError_t launch_tc_expert_ffn(const TcFfnArgs& a, cudaStream_t s) {
     // x -> fp16 copy (once per layer; the caller may share it between routed and shared experts)
     if (a.convert_x) {
         const int64_t n = (int64_t)a.T * a.H;
-        to_half_kernel<<<(unsigned)((n / 4 + 255) / 256), 256, 0, s>>>(a.x, a.x_bf16, n, a.x16);
+        to_half_kernel<<<(unsigned)((n / 4 + 255) / 256), 256, 0, s>>>(a.x, a.x_bf16, n, a.x16, a.hdr);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     const int bn = a.qtype == MOE_Q4_K ? tc_bn<MOE_Q4_K>() : tc_bn<MOE_Q8_0>();
@@ -686,8 +749,10 @@ cudaError_t launch_tc_expert_ffn(const TcFfnArgs& a, cudaStream_t s) {
     gu.sorted_pairs = a.identity ? nullptr : a.sorted_pairs;
     gu.tb_list = a.identity ? nullptr : a.tb_list; gu.n_identity = a.identity ? a.T : 0; gu.bn = bn;
     gu.h_out = a.h16; gu.hdr = a.hdr;
+    const WaitCfg wc = wait_cfg();
+    gu.wait_ns = wc.limit_ns; gu.stall = wc.stall;
     if (a.ev_before_gateup && (err = cudaEventRecord(a.ev_before_gateup, s)) != cudaSuccess) return err;
-    if ((err = launch_tc_q<kGateUp>(a.qtype, gu, max_tb * (a.I / kBM), s)) != cudaSuccess) return err;
+    if ((err = launch_tc_q<kGateUp>(a.qtype, a.q80r, gu, max_tb * (a.I / kBM), s)) != cudaSuccess) return err;
     if (a.ev_after_gateup && (err = cudaEventRecord(a.ev_after_gateup, s)) != cudaSuccess) return err;
     TcParams dn{};
     dn.w0 = a.wd; dn.expert_stride = a.stride_d; dn.rows = a.H; dn.K = a.I; dn.k = a.k;
@@ -696,7 +761,8 @@ cudaError_t launch_tc_expert_ffn(const TcFfnArgs& a, cudaStream_t s) {
     dn.sorted_pairs = nullptr;
     dn.tb_list = gu.tb_list; dn.n_identity = gu.n_identity; dn.bn = bn;
     dn.y_out = a.y; dn.y16_out = a.y16; dn.hdr = a.hdr;
-    return launch_tc_q<kDown>(a.qtype, dn, max_tb * (a.H / kBM), s);
+    dn.wait_ns = wc.limit_ns; dn.stall = wc.stall;
+    return launch_tc_q<kDown>(a.qtype, a.q80r, dn, max_tb * (a.H / kBM), s);
 }
 
 }  // namespace moe

@@ -18,6 +18,18 @@ constexpr int kQ4KWeights = 256;
 constexpr int kQ80Bytes = 34;      // fp16 d, 32 x int8
 constexpr int kQ80Weights = 32;
 
+// MOE_Q8_0_R row: the quants of its K/32 blocks, then their fp16 scales padded to 16 bytes.
+__host__ __device__ inline int64_t q80r_row_bytes(int64_t K) {
+    const int64_t nb = K / kQ80Weights;
+    return 32 * nb + (2 * nb + 15) / 16 * 16;
+}
+// Bytes of one row of K weights stored as qtype (Q8_0, Q8_0_R or Q4_K).
+__host__ __device__ inline int64_t q_row_bytes(int qtype, int64_t K) {
+    if (qtype == MOE_Q4_K) return K / kQ4KWeights * kQ4KBytes;
+    if (qtype == MOE_Q8_0_R) return q80r_row_bytes(K);
+    return K / kQ80Weights * kQ80Bytes;
+}
+
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kPermuteChunk = 1024;  // pairs per permute CTA
@@ -33,8 +45,29 @@ constexpr size_t kHeaderBytes = 256;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Bounded device-side waits.  Every wait on an mbarrier (bulk copies, TMA, MMA completion)
+// gives up after limit_ns, records MOE_ERR_TIMEOUT in the status word, waits (again within
+// limit_ns) for the copies its CTA still has in flight and returns.  stall = 1 is a test
+// setting: the first wait of the chained, segmented and tensor-core kernels then waits on a
+// barrier that nothing completes, so that this path runs.  Set by moe_debug_set_waits.
+struct WaitCfg {
+    uint64_t limit_ns;
+    int stall;
+};
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;   // 2 s: far above any legitimate wait
+WaitCfg wait_cfg();
+// Timing hook of the chained decode kernels (moe_debug_set_stamps): a device buffer of
+// kStampBytes, or NULL (off).
+constexpr size_t kStampBytes = (size_t)3 * 256 * 8 * sizeof(uint64_t);
+void* debug_stamps();
+
 // Records `msg` as this host thread's moe_last_error() text and returns `st`.
 moe_status report(moe_status st, const char* msg);
+
+// ---------------------------------------------------------------- weights
+// Q8_0 [n_rows][K] (34-byte blocks) -> the MOE_Q8_0_R row layout, one launch.
+cudaError_t launch_q80_repack(const uint8_t* src, int64_t src_stride, int E, int64_t rows, int64_t K, uint8_t* dst,
+                              cudaStream_t s);
 
 // ---------------------------------------------------------------- route
 cudaError_t launch_router_logits(const void* x, bool x_bf16, int T, int H, const float* W, int E,
@@ -60,7 +93,8 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* sor
 //   DOWN  : y[i, n] = Wd[e][n] . v_i                               (rows n < H)
 // with v_i = x[sorted_pairs[i] / k] (GATEUP) or h[i] (DOWN).
 struct GemvArgs {
-    int qtype;                  // MOE_Q8_0 / MOE_Q4_K
+    int qtype;                  // MOE_Q8_0 / MOE_Q4_K (MOE_Q8_0_R arrives as MOE_Q8_0 with q80r)
+    bool q80r;                  // Q8_0 weights in the repacked row layout
     bool gateup;
     const uint8_t* w0;          // gate (GATEUP) or down (DOWN)
     const uint8_t* w1;          // up (GATEUP) or NULL
@@ -107,7 +141,8 @@ struct DecodeArgs {
     const uint8_t* wu;
     const uint8_t* wd;
     int64_t stride_gu, stride_d;
-    int I_s, s_qtype;
+    int I_s, s_qtype;             // shared expert (s_qtype MOE_Q8_0_R arrives as MOE_Q8_0 with s_q80r)
+    bool s_q80r;
     const uint8_t* sg;
     const uint8_t* su;
     const uint8_t* sd;
@@ -137,6 +172,7 @@ cudaError_t launch_decode_chain(const DecodeArgs& a, cudaStream_t s, cudaEvent_t
 // identity mode used by a shared expert).
 struct TcFfnArgs {
     int qtype;                  // MOE_Q4_K or MOE_Q8_0 (gate, up and down share it)
+    bool q80r;                  // Q8_0 weights in the repacked row layout
     const uint8_t* wg;
     const uint8_t* wu;
     const uint8_t* wd;

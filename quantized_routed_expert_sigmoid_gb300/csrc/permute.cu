@@ -10,7 +10,6 @@
 // offsets and per-chunk bases), then a stable scatter inside each chunk
 // (warp match for the rank inside a warp, per-warp counts for the rank
 // across warps).  A single chunk does both steps in one launch.
-#include <mutex>
 
 #include "internal.cuh"
 
@@ -196,25 +195,16 @@ constexpr size_t kNoallocWords = kHeaderBytes / sizeof(int32_t) + (size_t)kNoall
 // GPU that loads the library until the process exits.
 static __device__ __align__(256) int32_t g_permute_scratch[kNoallocWords];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// The device address of g_permute_scratch on the current device, looked up
-// once per device (host code cannot use the symbol itself as an address).
-cudaError_t scratch_for_current_device(void** out) {
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
+// The device address of g_permute_scratch in the current context.  Host code cannot use the
+// symbol itself as an address.  The lookup runs on every call: after the first call in a
+// context (which may load the library's device code, so it must not run under stream capture)
+// it is a host-side table lookup, and it stays right when the caller switches contexts or a
+// context is destroyed and created again, where a cached address would go stale.
+cudaError_t scratch_for_current_context(void** out) {
+    void* p = nullptr;
+    const cudaError_t err = cudaGetSymbolAddress(&p, g_permute_scratch);
     if (err != cudaSuccess) return err;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        err = cudaGetSymbolAddress(&p, g_permute_scratch);
-        if (err != cudaSuccess) return err;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return cudaSuccess;
 }
 
@@ -232,7 +222,7 @@ extern "C" moe_status moe_permute_noalloc(const int32_t* topk_ids, int T, int k,
     if (!offsets) return report(MOE_ERR_INVALID_ARG, "offsets is NULL");
     if (T > 0 && (!topk_ids || !sorted_pairs || !pair_pos)) return report(MOE_ERR_INVALID_ARG, "NULL array");
     void* scratch = nullptr;
-    cudaError_t err = scratch_for_current_device(&scratch);
+    cudaError_t err = scratch_for_current_context(&scratch);
     if (err != cudaSuccess) return report(MOE_ERR_CUDA, "moe_permute_noalloc: scratch lookup failed");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     WsHeader* hdr = reinterpret_cast<WsHeader*>(scratch);

@@ -188,10 +188,12 @@ __device__ __forceinline__ uint32_t qd_ld2(const uint8_t* p) {
     return qd_ldg_u16(p);
 }
 
+// Q8_0 rows are GGUF blocks (34 bytes, read as halfwords), or with q80r the repacked row
+// layout (the block's 32 quants at 32*b, 16-byte aligned; its scale at 32*nblk + 2*b).
 template <int QT, int NT, bool kSmemRows = false>
 __device__ __forceinline__ void qd_rows4(const uint8_t* const (&rowp)[4], int nblk, int iters, const float4* xs,
                                          int vstride, const float2* xsum, int sstride, int nt, int lane,
-                                         float (&acc)[4][NT], const int* vidx = nullptr) {
+                                         float (&acc)[4][NT], const int* vidx = nullptr, bool q80r = false) {
     for (int it = 0; it < iters; ++it) {
         const int b = Walk<QT>::blk(it, lane);
         if (b >= nblk) continue;
@@ -270,7 +272,15 @@ __device__ __forceinline__ void qd_rows4(const uint8_t* const (&rowp)[4], int nb
             float dd[4];
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
-                if (rowp[r]) {
+                if (rowp[r] && q80r) {
+                    const uint8_t* qp = rowp[r] + (int64_t)b * 32;
+                    dd[r] = __half2float(__ushort_as_half((unsigned short)qd_ld2<kSmemRows>(rowp[r] + (int64_t)nblk * 32 + 2 * b)));
+                    const uint4 a0 = qd_ld16<kSmemRows>(qp), a1 = qd_ld16<kSmemRows>(qp + 16);
+                    qw[r][0] = a0.x ^ 0x80808080u; qw[r][1] = a0.y ^ 0x80808080u;   // int8 + 128 as bytes
+                    qw[r][2] = a0.z ^ 0x80808080u; qw[r][3] = a0.w ^ 0x80808080u;
+                    qw[r][4] = a1.x ^ 0x80808080u; qw[r][5] = a1.y ^ 0x80808080u;
+                    qw[r][6] = a1.z ^ 0x80808080u; qw[r][7] = a1.w ^ 0x80808080u;
+                } else if (rowp[r]) {
                     const uint8_t* bp = rowp[r] + (int64_t)b * kQ80Bytes;
                     dd[r] = __half2float(__ushort_as_half((unsigned short)qd_ld2<kSmemRows>(bp)));
 #pragma unroll

@@ -1,6 +1,6 @@
 // qgemv.cu -- fused dequant-GEMV for the experts at decode sizes where the segmented
-// kernels of gemv_seg.cu do not apply (Q8_0 weights, such as a Q8_0 shared expert, or more
-// than 256 experts).
+// kernels of gemv_seg.cu do not apply (Q8_0 weights, such as a Q8_0 shared expert, in the
+// stored GGUF blocks or repacked by moe_weights_prepare, or more than 256 experts).
 //
 // The pages run the card experts on the stored GGUF quantization ("bloomery
 // README 0.3.1", Status table, "Quant types" row; "Why it is fast": kernels
@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kThreads, 2) qgemv_kernel(GemvArgs a, int iter
     const int start = s_start, n_tot = s_n;
 
     const int nblk = a.K / Walk<QT>::kBlockWeights;
-    const int64_t rb = (int64_t)nblk * Walk<QT>::kBlockBytes;
+    const int64_t rb = QT == MOE_Q8_0 && a.q80r ? q80r_row_bytes(a.K) : (int64_t)nblk * Walk<QT>::kBlockBytes;
     const uint8_t* w0 = a.w0 + (int64_t)e * a.expert_stride;
     const uint8_t* w1 = GATEUP ? a.w1 + (int64_t)e * a.expert_stride : nullptr;
     const int n_units = a.rows / (GATEUP ? 2 : 4);
@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 2) qgemv_kernel(GemvArgs a, int iter
             for (int r = 0; r < 4; ++r)
 #pragma unroll
                 for (int t = 0; t < NT; ++t) acc[r][t] = 0.f;
-            qd_rows4<QT, NT>(rowp, nblk, iters, xs, slots, xsum, iters * 32, nt, lane, acc);
+            qd_rows4<QT, NT>(rowp, nblk, iters, xs, slots, xsum, iters * 32, nt, lane, acc, nullptr, a.q80r);
             qd_store_units<NT, GATEUP>(acc, lane, nt, a.out + (int64_t)(start + pb) * a.rows, a.rows, unit);
         }
         __syncthreads();

@@ -29,6 +29,7 @@ struct RouterTcParams {
     float* logits;                   // [T][E]
     int T, H, E;
     WsHeader* clear_hdr;
+    uint64_t wait_ns;                // limit of every bounded wait
 };
 
 __global__ void router_split_kernel(const float* __restrict__ W, int64_t n, __nv_bfloat16* __restrict__ w3) {
@@ -100,7 +101,7 @@ __global__ void __launch_bounds__(kRThreads, 1) router_tc_kernel(const __grid_co
             if (kb + 3 < nk) {
                 // stage (kb + 3) % kRStages was last read by MMA(kb + 3 - kRStages)
                 const int prev = kb + 3 - kRStages;
-                if (prev >= 0 && !mbar_wait(&empty[(kb + 3) % kRStages], (prev / kRStages) & 1, abort_flag)) break;
+                if (prev >= 0 && !mbar_wait(&empty[(kb + 3) % kRStages], (prev / kRStages) & 1, abort_flag, p.wait_ns)) break;
                 issue(kb + 3);
             }
             cp_commit();
@@ -110,7 +111,7 @@ __global__ void __launch_bounds__(kRThreads, 1) router_tc_kernel(const __grid_co
         }
         cp_wait_all();
         // ---- epilogue: lane = token row, 64 expert columns
-        if (!*abort_flag && mbar_wait(&accf, 0, abort_flag)) {
+        if (!*abort_flag && mbar_wait(&accf, 0, abort_flag, p.wait_ns)) {
             tc_after();
             const int t = t0 + warp * 32 + lane;
 #pragma unroll
@@ -136,7 +137,7 @@ __global__ void __launch_bounds__(kRThreads, 1) router_tc_kernel(const __grid_co
         const uint32_t idesc = idesc_mma(kRM, kRN, true);
         bool issued = false;
         for (int kb = 0; kb < nk; ++kb) {
-            if (!mbar_wait(&full[kb % kRStages], (kb / kRStages) & 1, abort_flag)) break;
+            if (!mbar_wait(&full[kb % kRStages], (kb / kRStages) & 1, abort_flag, p.wait_ns)) break;
             tc_after();
             if (lane == 0) {
                 const uint32_t a0 = su32(smem + (kb % kRStages) * kRStageBytes);
@@ -157,9 +158,7 @@ __global__ void __launch_bounds__(kRThreads, 1) router_tc_kernel(const __grid_co
             // let every issued MMA finish before the accumulator is freed
             if (lane == 0) mma_commit(&accf);
             __syncwarp();
-            const uint64_t ts = gtime();
-            while (!mbar_test(&accf, 0) && gtime() - ts < kWaitLimitNs) {
-            }
+            mbar_wait_for(&accf, 0, p.wait_ns);
         }
     }
     if (*abort_flag && tid == 0 && p.clear_hdr) atomicCAS(&p.clear_hdr->status, (int)MOE_OK, (int)MOE_ERR_TIMEOUT);
@@ -195,6 +194,7 @@ cudaError_t launch_router_tc(const void* x, int T, int H, const float* W, int E,
     p.logits = logits;
     p.T = T; p.H = H; p.E = E;
     p.clear_hdr = clear_hdr;
+    p.wait_ns = wait_cfg().limit_ns;
     router_tc_kernel<<<dim3((T + kRM - 1) / kRM, (E + kRN - 1) / kRN), kRThreads, smem, s>>>(p);
     return cudaGetLastError();
 }

@@ -8,8 +8,6 @@
 namespace moe {
 namespace {
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
-
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 __device__ __forceinline__ uint64_t gtime() {
@@ -35,14 +33,22 @@ __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait for the completion of the phase with the given parity.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
+// Bounded wait for the completion of the phase with the given parity: false when another
+// thread of the CTA raised abort_flag, or (raising it) after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag, uint64_t limit_ns) {
     if (mbar_test(b, parity)) return true;
     const uint64_t t0 = gtime();
     while (!mbar_test(b, parity)) {
         if (*abort_flag) return false;
-        if (gtime() - t0 > kWaitLimitNs) { *abort_flag = 1; return false; }
+        if (gtime() - t0 > limit_ns) { *abort_flag = 1; return false; }
     }
+    return true;
+}
+// Bounded wait that ignores abort_flag (the drain after an abort).
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* b, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = gtime();
+    while (!mbar_test(b, parity))
+        if (gtime() - t0 > limit_ns) return false;
     return true;
 }
 

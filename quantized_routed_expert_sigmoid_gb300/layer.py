@@ -11,24 +11,40 @@ import torch
 
 from . import _native as N
 
-_QT = {"q8_0": N.MOE_Q8_0, "q4_k": N.MOE_Q4_K}
+_QT = {"q8_0": N.MOE_Q8_0, "q4_k": N.MOE_Q4_K, "q8_0_r": N.MOE_Q8_0_R}
 
 
 def row_bytes(qtype: int, cols: int) -> int:
+    if qtype == N.MOE_Q8_0_R:                     # quants, then fp16 scales padded to 16 bytes
+        nb = cols // 32
+        return 32 * nb + (2 * nb + 15) // 16 * 16
     return cols // 32 * 34 if qtype == N.MOE_Q8_0 else cols // 256 * 144
 
 
+def prepare_q8_0(t, rows: int, cols: int, n_experts: int = 1):
+    """A Q8_0 tensor (uint8, [n_experts, rows, rb] or [rows, rb] on the GPU) repacked by
+    moe_weights_prepare into a new uint8 tensor of the MOE_Q8_0_R layout (qtype "q8_0_r")."""
+    m = N.qmat(N.MOE_Q8_0, t, rows, cols, rows * row_bytes(N.MOE_Q8_0, cols))
+    nbytes = N.moe_weights_prepare_size(m, n_experts)
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=t.device)
+    N.moe_weights_prepare(m, n_experts, dst, nbytes)
+    shape = (n_experts, rows, row_bytes(N.MOE_Q8_0_R, cols)) if t.dim() == 3 else (rows, row_bytes(N.MOE_Q8_0_R, cols))
+    return dst.view(*shape)
+
+
 class MoeLayer:
-    """gate/up: uint8 [E, I, rb(H)], down: uint8 [E, H, rb(I)] on the GPU."""
+    """gate/up: uint8 [E, I, rb(H)], down: uint8 [E, H, rb(I)] on the GPU (qtype, or
+    qtype_down for down); shared expert matrices in shared_qtype."""
 
     def __init__(self, *, mode: str, E: int, k: int, H: int, I: int, qtype: str, gate, up, down, W_router,
                  bias=None, n_groups: int = 1, topk_groups: int = 1, scale: float = 1.0,
                  renormalize: bool = True, x_dtype: str = "bf16", I_s: int = 0, shared_qtype: str = "q8_0",
                  s_gate=None, s_up=None, s_down=None, accumulate: bool = False, tc_min_tokens: int = 0,
-                 decode_chain: bool = True, norm_gamma=None, norm_eps: float = 1e-6):
+                 decode_chain: bool = True, norm_gamma=None, norm_eps: float = 1e-6, qtype_down: str | None = None):
         self.E, self.k, self.H, self.I = E, k, H, I
         self.x_dtype = x_dtype
         qt = _QT[qtype]
+        qd = _QT[qtype_down] if qtype_down else qt      # the down matrix may be stored in another type
         self._keep = [gate, up, down, W_router, bias, s_gate, s_up, s_down, norm_gamma]
         d = N.moe_layer_desc()
         d.route = N.route_cfg(N.MOE_ROUTE_SIGMOID_GROUP if mode == "sigmoid_group" else N.MOE_ROUTE_SOFTMAX,
@@ -39,7 +55,7 @@ class MoeLayer:
         d.bias = bias.data_ptr() if bias is not None else None
         d.gate = N.qmat(qt, gate, I, H, I * row_bytes(qt, H))
         d.up = N.qmat(qt, up, I, H, I * row_bytes(qt, H))
-        d.down = N.qmat(qt, down, H, I, H * row_bytes(qt, I))
+        d.down = N.qmat(qd, down, H, I, H * row_bytes(qd, I))
         d.shared_intermediate = I_s
         if I_s > 0:
             sq = _QT[shared_qtype]

@@ -65,7 +65,8 @@ def _desc(qtype=N.MOE_Q4_K, H=2048, I=768, E=128, data=FAKE, stride=None, mode=N
     d.route = moe.route_cfg(mode, E, 8, 8 if mode else 1, 4 if mode else 1, 1.0, True)
     d.hidden, d.intermediate, d.x_type = H, I, N.MOE_BF16
     d.W_router = FAKE
-    rb = (lambda K: K // 256 * 144) if qtype == N.MOE_Q4_K else (lambda K: K // 32 * 34)
+    from quantized_routed_expert_sigmoid_gb300.layer import row_bytes
+    rb = (lambda K: row_bytes(qtype, K)) if qtype in (N.MOE_Q4_K, N.MOE_Q8_0, N.MOE_Q8_0_R) else (lambda K: K // 32 * 34)
     sgu = stride if stride is not None else I * rb(H)
     d.gate = moe.qmat(qtype, data, I, H, sgu)
     d.up = moe.qmat(qtype, data, I, H, sgu)
@@ -86,7 +87,7 @@ def test_plan_validation():
     finally:
         moe.moe_layer_plan_destroy(plan)
     _expect(N.MOE_ERR_UNSUPPORTED, moe.moe_layer_plan_create, _desc(qtype=N.MOE_BF16))
-    for other in (4, 5, 6, -1):          # types the library does not decode yet, and garbage
+    for other in (5, 6, 7, -1):          # types the library does not decode yet, and garbage
         _expect(N.MOE_ERR_UNSUPPORTED, moe.moe_layer_plan_create, _desc(qtype=other))
     _expect(N.MOE_ERR_INVALID_ARG, moe.moe_layer_plan_create, _desc(H=2000))          # not a block multiple
     _expect(N.MOE_ERR_INVALID_ARG, moe.moe_layer_plan_create, _desc(data=FAKE + 4))   # misaligned weights
@@ -157,3 +158,35 @@ def test_prenorm_validation():
     finally:
         moe.moe_layer_plan_destroy(pre)
         moe.moe_layer_plan_destroy(plain)
+
+
+def test_debug_waits_setting_is_validated():
+    lib = N.load()
+    assert lib.moe_debug_set_waits(1000, 2) == N.MOE_ERR_INVALID_ARG
+    assert lib.moe_debug_set_waits(0, 0) == N.MOE_OK
+
+
+def test_weights_prepare_size_and_validation():
+    # Q8_0 rows of K weights repack to 32 * K/32 quant bytes + the K/32 fp16 scales padded to 16
+    m = N.qmat(N.MOE_Q8_0, FAKE, 2048, 7168, 2048 * 7168 // 32 * 34)
+    assert N.moe_weights_prepare_size(m, 1) == 2048 * (7168 + 448)
+    assert N.moe_weights_prepare_size(m, 3) == 3 * 2048 * (7168 + 448)
+    m2 = N.qmat(N.MOE_Q8_0, FAKE, 4, 96, 4 * 102)         # 3 blocks: scales 6 bytes -> 16
+    assert N.moe_weights_prepare_size(m2, 1) == 4 * (96 + 16)
+    q4 = N.qmat(N.MOE_Q4_K, FAKE, 768, 2048, 768 * 1152)  # used as stored
+    assert N.moe_weights_prepare_size(q4, 128) == 0
+    out = N.moe_weights_prepare(q4, 128, None, 0, 0)
+    assert out.qtype == N.MOE_Q4_K and out.data == FAKE
+    _expect(N.MOE_ERR_UNSUPPORTED, N.moe_weights_prepare_size, N.qmat(N.MOE_Q8_0_R, FAKE, 4, 96, 0), 1)
+    _expect(N.MOE_ERR_INVALID_ARG, N.moe_weights_prepare_size, N.qmat(N.MOE_Q8_0, FAKE, 4, 100, 0), 1)
+    _expect(N.MOE_ERR_INVALID_ARG, N.moe_weights_prepare_size, m, 0)
+    _expect(N.MOE_ERR_WORKSPACE, N.moe_weights_prepare, m2, 1, FAKE * 16, 16, 0)
+    _expect(N.MOE_ERR_INVALID_ARG, N.moe_weights_prepare, m2, 1, FAKE + 8, 1 << 20, 0)
+    _expect(N.MOE_ERR_INVALID_ARG, N.moe_weights_prepare, m2, 1, FAKE + 16, 1 << 20, 0)   # overlaps the source
+
+
+def test_layer_accepts_repacked_q8_0():
+    from quantized_routed_expert_sigmoid_gb300.layer import row_bytes
+    assert row_bytes(N.MOE_Q8_0_R, 256) == 256 + 16
+    plan = moe.moe_layer_plan_create(_desc(qtype=N.MOE_Q8_0_R))
+    moe.moe_layer_plan_destroy(plan)

@@ -59,7 +59,9 @@ def _no_alloc(ids, E):
 def test_noalloc_matches_workspace_permute_twice():
     # first call: many chunks (exercises the arrival ticket and per-chunk bases);
     # second call: a different size on the same scratch, which must start clean
-    for (T, k, E, seed) in ((3000, 8, 128, 1), (700, 8, 256, 2), (1, 8, 128, 3)):
+    # the largest accepted size (65,536 pairs in 64 chunks over 1024 experts) fills every
+    # chunk-base word of the fixed array
+    for (T, k, E, seed) in ((3000, 8, 128, 1), (700, 8, 256, 2), (1, 8, 128, 3), (8192, 8, 1024, 4)):
         ids = _ids(T, k, E, seed)
         ref = _with_workspace(ids, E)
         got = _no_alloc(ids, E)
