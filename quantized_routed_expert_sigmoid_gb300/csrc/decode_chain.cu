@@ -595,25 +595,35 @@ __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_con
     const int n_shared = has_shared ? R / 4 : 0;
     for (int task = warp; task < n_routed + n_shared; task += kK3Threads / 32) {
         if (task < n_routed) {
+            // each 16-lane half takes 4 of the task's 8 rows; lane = one 64-weight group of all 4
+            // rows (groups gl, gl + 16, ...), so each activation load serves 4 rows and the lane
+            // has 4 rows' independent integer sums in flight
             const int s = task / nsub, sb = task - s * nsub;
-            const int row = lane >> 2, sub = lane & 3;
-            const int rl = 8 * sb + row, n = n0 + rl;
+            const int half = lane >> 4, gl = lane & 15;
+            const int rl0 = 8 * sb + 4 * half;
             float acc[4][1] = {{0.f}, {0.f}, {0.f}, {0.f}};
             const uint4* Xs = reinterpret_cast<const uint4*>(hsm + (size_t)s * vb);
             const float4* XSs = reinterpret_cast<const float4*>(hsm + (size_t)s * vb + 256 * GI);
-            if (p.k3_prefetch) {
-                const uint8_t* const rowp[4] = {n < H ? wbuf + ((int64_t)s * R + rl) * rbI : nullptr, nullptr, nullptr,
-                                                nullptr};
-                for (int g = sub; g < GI; g += 4) qd4_group<1, 1, true>(rowp, 0, g, GI, Xs, XSs, 1, acc, nullptr);
-            } else {
-                const uint8_t* const rowp[4] = {n < H ? p.wd + (int64_t)s_e[s] * p.stride_d + (int64_t)n * rbI : nullptr,
-                                                nullptr, nullptr, nullptr};
-                for (int g = sub; g < GI; g += 4) qd4_group<1, 1, false>(rowp, 0, g, GI, Xs, XSs, 1, acc, nullptr);
+            const uint8_t* rowp[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int n = n0 + rl0 + r;
+                rowp[r] = n >= H ? nullptr
+                          : p.k3_prefetch ? wbuf + ((int64_t)s * R + rl0 + r) * rbI
+                                          : p.wd + (int64_t)s_e[s] * p.stride_d + (int64_t)n * rbI;
             }
-            float v = acc[0][0];
-            v += __shfl_xor_sync(0xffffffffu, v, 1);
-            v += __shfl_xor_sync(0xffffffffu, v, 2);
-            if (sub == 0) ybuf[s * R + rl] = v;
+            if (p.k3_prefetch) {
+                for (int g = gl; g < GI; g += 16) qd4_group<1, 4, true>(rowp, 0, g, GI, Xs, XSs, 1, acc, nullptr);
+            } else {
+                for (int g = gl; g < GI; g += 16) qd4_group<1, 4, false>(rowp, 0, g, GI, Xs, XSs, 1, acc, nullptr);
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                float v = acc[r][0];
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (gl == 0 && n0 + rl0 + r < H) ybuf[s * R + rl0 + r] = v;
+            }
         } else if constexpr (has_shared) {
             const int q = task - n_routed;
             const int nb = n0 + 4 * q;
