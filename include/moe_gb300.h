@@ -120,6 +120,10 @@ moe_status moe_weights_prepare(moe_qmat* in_out, int n_experts, void* dst, size_
  *     them; gates = s_j / sum s (renormalize=1) or s_j; the bias never enters
  *     a gate.  Gates are then multiplied by routed_scale.
  * Chosen ids are written in ascending expert id per token.
+ * Pages: the router's top-k ids are integer outputs that an engine must
+ * reproduce exactly outside tie bands ("bloomery early V4.1 README", "Oracle
+ * sets against ik_llama.cpp"; "bloomery V4.1 README", "Against ik_llama.cpp");
+ * the scoring itself is not printed there and is the definition above.
  * x (device) [T][H] in x_type (MOE_F32 or MOE_BF16); W_router (device) fp32
  * [E][H]; bias (device, nullable) fp32 [E]; logits_in (device, nullable)
  * fp32 [T][E] replaces the router product; logits_out (device, nullable) fp32
@@ -139,6 +143,9 @@ moe_status moe_route(const moe_route_cfg* cfg, const void* x, moe_dtype x_type, 
  * device status word in the workspace to MOE_ERR_DEVICE_CHECK and the pair is
  * dropped); sorted_pairs, pair_pos (device) int32 [P]; offsets (device) int32
  * [E+1]; workspace (device) of moe_permute_workspace_size() bytes.
+ * Pages: a prompt batch runs each expert over all of its tokens at once
+ * ("bloomery V4.1 README", feature list, "Batched prompts"); this call builds
+ * that per-expert work list.  Integer work: the same bits on every run.
  */
 moe_status moe_permute_workspace_size(int T, int k, int E, size_t* bytes);
 moe_status moe_permute(const int32_t* topk_ids, int T, int k, int E, int32_t* sorted_pairs,
@@ -178,6 +185,12 @@ moe_status moe_permute_noalloc(const int32_t* topk_ids, int T, int k, int E, int
  * i.  With sorted_pairs = NULL and offsets = NULL (then E = 1, k = 1) the
  * expert runs on every token in order, as a shared expert does.
  * fp32 accumulation, fp32 h, for every T.
+ * Pages: routed experts run on the card over the file's stored block
+ * quantization, Q4_K among the card types ("bloomery README 0.3.1", Status
+ * table, "Quant types" row), each expert over its grouped tokens ("bloomery
+ * V4.1 README", feature list, "Batched prompts").  The SwiGLU form and the
+ * block layouts are not printed on the pages; they are the definitions above
+ * and in the conventions at the top of this file.
  */
 moe_status moe_expert_ffn_workspace_size(int T, int k, int E, int H, int I, size_t* bytes);
 moe_status moe_expert_ffn(const moe_qmat* gate, const moe_qmat* up, const moe_qmat* down, int E,
@@ -204,6 +217,9 @@ moe_status moe_expert_down(const moe_qmat* down, int E, const float* h, int T, i
  *                           (+ shared_out[t,n]) (+ old out[t,n] if accumulate),
  * summed in ascending j, then the shared term, then the old value: the same
  * bits on every run.  y_pairs, shared_out (nullable), out: fp32 (device).
+ * Pages: no formula for the combine is printed; its fixed summation order
+ * serves the requirement that a replay equal the eager run bit for bit
+ * ("bloomery early V4.1 README", "Bit gates").
  */
 moe_status moe_combine(const float* y_pairs, const float* topk_w, const int32_t* pair_pos, int T,
                        int k, int H, const float* shared_out, int accumulate, float* out,
@@ -213,6 +229,8 @@ moe_status moe_combine(const float* y_pairs, const float* topk_w, const int32_t*
  * moe_rmsnorm_bf16 -- u[t,h] = bf16( x[t,h] / sqrt(mean_h x[t,:]^2 + eps) * gamma[h] )
  * (fp32 arithmetic, round to nearest even).  x fp32 [T][H], gamma fp32 [H],
  * u bf16 [T][H] (device).  Used between stacked layers.
+ * Pages: none of the normalisation is printed; this is the plain RMSNorm
+ * definition, and the bf16 rounding is the layer input's storage type.
  */
 moe_status moe_rmsnorm_bf16(const float* x, const float* gamma, int T, int H, float eps, void* u,
                             moe_stream_t stream);
@@ -243,7 +261,10 @@ typedef struct {
 
 typedef struct moe_layer_plan moe_layer_plan;
 
-/* Validates the description once and keeps a host copy of it. */
+/* Validates the description once and keeps a host copy of it.  Plans, workspace
+ * sizes and path choice are host-side only, so the per-step launches can be
+ * recorded once and replayed ("bloomery README 0.3.11", list of why it is fast:
+ * one CUDA graph a decode step). */
 moe_status moe_layer_plan_create(const moe_layer_desc* desc, moe_layer_plan** plan);
 moe_status moe_layer_plan_destroy(moe_layer_plan* plan);
 /* Bytes of device workspace moe_layer needs for up to T tokens. */
@@ -274,6 +295,11 @@ moe_status moe_layer_path(const moe_layer_plan* plan, int T, int* path);
  * are rounded to fp16 before the fp32 combine).  out may alias x when
  * accumulate = 1 (a residual block): x is read before out is written.
  * T = 0 is a no-op that launches nothing (x, out and workspace may be NULL).
+ * Pages: one CUDA graph per decode step ("bloomery README 0.3.11", list of why
+ * it is fast), prompts as tensor-core GEMMs (same list) over experts grouped by
+ * token ("bloomery V4.1 README", feature list, "Batched prompts"), and a graph
+ * replay that equals the eager run bit for bit ("bloomery early V4.1 README",
+ * "Bit gates").
  */
 moe_status moe_layer(const moe_layer_plan* plan, const void* x, int T, float* out, void* workspace,
                      size_t ws_bytes, moe_stream_t stream);
@@ -292,7 +318,8 @@ moe_status moe_layer_debug_views(const moe_layer_plan* plan, int T, void* worksp
 
 /* Copies the device status word of a workspace (MOE_OK or a MOE_ERR_* code
  * raised by a device-side check) to *code and clears it.  Synchronizes the
- * stream first; call it outside graph capture. */
+ * stream first; call it outside graph capture.  Pages: a bad request is
+ * refused by name rather than run ("bloomery README 0.3.11", limits list). */
 moe_status moe_read_device_status(const moe_layer_plan* plan, int T, void* workspace, int32_t* code,
                                   moe_stream_t stream);
 moe_status moe_permute_read_device_status(int T, int k, int E, void* workspace, int32_t* code,
@@ -319,16 +346,19 @@ moe_status moe_debug_set_waits(uint64_t limit_ns, int stall);
  * default (buf = NULL).  With a device buffer of at least 3*256*8*8 = 49,152 bytes, every
  * chained call launched afterwards has thread 0 of CTA c (c < 256) of kernel n (0 router
  * logits, 1 routing + gate/up, 2 down + combine) write the GPU's global nanosecond clock
- * at phase ph into buf[(n*256 + c)*8 + ph] (uint64): n = 0: start, after the wait for the
- * previous launch, end; n = 1: start, activations staged, after the wait, routed, first
- * unit computed, units done, CTA done; n = 2: start, after the wait, inputs in shared
- * memory, CTA done.  Calls overwrite the same slots; a graph keeps the setting it was
+ * at phase ph into buf[(n*256 + c)*8 + ph] (uint64): n = 0: 0 start, 1 after the wait for
+ * the previous launch, 2 router dot products done, 3 end; n = 1: 0 start, 1 activations
+ * staged, 2 after the wait, 3 routing read, 4 first unit computed, 5 units done, 6 CTA
+ * done, 7 top-k written (the CTA that routes); n = 2: 0 start, 1 after the wait, 2 ids
+ * read, 3 copies issued, 4 copies landed, 5 dot products done, 6 CTA done.  Calls overwrite the same slots; a graph keeps the setting it was
  * captured with.  For measuring where a decode layer's time goes; the results are
- * unchanged.
+ * unchanged.  Pages: step times there are quoted with their instrumentation state
+ * ("bloomery early V4.1 README", caveats of the depth measurement).
  */
 moe_status moe_debug_set_stamps(void* buf, size_t bytes);
 
-/* The reason for the last non-MOE_OK status returned on this host thread. */
+/* The reason for the last non-MOE_OK status returned on this host thread
+ * (refusals by name: "bloomery README 0.3.11", limits list). */
 const char* moe_last_error(void);
 /* Library version string. */
 const char* moe_version(void);

@@ -138,6 +138,7 @@ DecodeArgs decode_shape_args(const moe_layer_desc& d, int T) {
     DecodeArgs da{};
     da.route = d.route;
     da.Wr = d.W_router;
+    da.x_bf16 = input_bf16(d);    // the values the chain stages (the launch sets the buffers)
     da.bias = d.bias;
     da.T = T; da.H = d.hidden; da.I = d.intermediate;
     da.qtype = kernel_qtype(d.gate.qtype);

@@ -108,8 +108,9 @@ __device__ __forceinline__ void prefetch_l2(const uint8_t* src, int64_t bytes) {
 }
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 // One warp stages the 32 consecutive values v (lane = element) of sub-block sb of a vector
-// of G groups into dst: the layout qd4_stage gives a staged vector (X: 16 x G uint4 of byte
-// planes {hi, mid, lo, 0} of 4 values, then XS: G float4 {scale lo, scale hi, sum lo, sum hi}).
+// of G groups into dst as three byte planes: the layout qd4_stage_par gives a staged vector
+// with NPL = 3 (X: 16 x G uint4 of planes {hi, mid, lo, 0} of 4 values, then XS: G float4
+// {scale lo, scale hi, sum lo, sum hi}).
 __device__ __forceinline__ void warp_stage_subblock(float v, uint8_t* dst, int G, int sb, int lane) {
     float m = fabsf(v), sum = v;
 #pragma unroll
@@ -117,21 +118,20 @@ __device__ __forceinline__ void warp_stage_subblock(float v, uint8_t* dst, int G
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         sum += __shfl_xor_sync(0xffffffffu, sum, o);
     }
-    const float inv = m > 0.f ? 8388607.0f / m : 0.f;
-    int x24 = __float2int_rn(v * inv);
-    x24 = max(-8388607, min(8388607, x24));
-    uint32_t hb = ((uint32_t)x24 >> 16) & 0xFFu, mb = ((uint32_t)x24 >> 8) & 0xFFu, lb = (uint32_t)x24 & 0xFFu;
+    const float2 sc = qx_scale<3>(m);
+    const int x = qx_int<3>(v, sc.x);
+    uint32_t w[3];
 #pragma unroll
-    for (int b = 1; b < 4; ++b) {
-        hb |= __shfl_down_sync(0xffffffffu, ((uint32_t)x24 >> 16) & 0xFFu, b) << (8 * b);
-        mb |= __shfl_down_sync(0xffffffffu, ((uint32_t)x24 >> 8) & 0xFFu, b) << (8 * b);
-        lb |= __shfl_down_sync(0xffffffffu, (uint32_t)x24 & 0xFFu, b) << (8 * b);
+    for (int pl = 0; pl < 3; ++pl) {
+        w[pl] = qx_plane<3>(x, pl);
+#pragma unroll
+        for (int b = 1; b < 4; ++b) w[pl] |= __shfl_down_sync(0xffffffffu, qx_plane<3>(x, pl), b) << (8 * b);
     }
     const int g = sb >> 1, hh = sb & 1;
-    if ((lane & 3) == 0) reinterpret_cast<uint4*>(dst)[(hh * 8 + (lane >> 2)) * G + g] = make_uint4(hb, mb, lb, 0u);
+    if ((lane & 3) == 0) reinterpret_cast<uint4*>(dst)[(hh * 8 + (lane >> 2)) * G + g] = make_uint4(w[0], w[1], w[2], 0u);
     if (lane == 0) {
         float* xs = reinterpret_cast<float*>(dst + (size_t)16 * G * 16) + 4 * g;
-        xs[hh] = m / 8388607.0f;
+        xs[hh] = sc.y;
         xs[2 + hh] = sum;
     }
 }
@@ -311,10 +311,12 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
     float4* XS = reinterpret_cast<float4*>(X + (size_t)T * 16 * G);
     float4* xs_s = reinterpret_cast<float4*>(smem + p.k2_off_xs_s);
     uint8_t* cring = smem + p.k2_off_ring;          // two round slots: [32 gate rows][32 up rows]
-    __shared__ __align__(8) uint64_t c_bar[3];     // two ring slots; [2]: the test stall (never arrived on)
+    // two ring slots of four quarters (8 gate + 8 up rows each, for warps 4q .. 4q + 3); [8]: the
+    // test stall (never arrived on)
+    __shared__ __align__(8) uint64_t c_bar[9];
     stamp(p, 1, 0);
     if (tid == 0) {
-        for (int i = 0; i < 3; ++i)
+        for (int i = 0; i < 9; ++i)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&c_bar[i])) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -324,7 +326,7 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
     // residual stream that the layer before finished writing before K1 let this kernel start)
     __shared__ float s_r[kCMaxT], s_rpart[kCMaxT][8];
     if (p.gamma) rms_scales_cta(reinterpret_cast<const float*>(p.x), T, H, p.eps, s_rpart, s_r);
-    qd4_stage_par(p.x, xb, false, H, T, nullptr, H, X, XS, tid, nthr, p.gamma, s_r);
+    qd4_stage_par<2>(p.x, xb, false, H, T, nullptr, H, X, XS, tid, nthr, p.gamma, s_r);   // bf16 values
     if (kSh == 2) {
         const int slots = p.it_H_s * 256;
         for (int t = 0; t < T; ++t) {
@@ -350,22 +352,26 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
 
     // ---- routed units, one round per 16: round r of this CTA covers the units wg0 + r W ..
     // + 15 (wg0 = 16 * blockIdx.x), i.e. 32 consecutive rows of gate and of up of one expert
-    // (half_I is a multiple of 16) -- one staged sub-block of h.  A round arrives as two bulk
-    // copies (the 32 gate rows, the 32 up rows; rows are whole, H <= 2048) into slot r % 2;
-    // warp w computes the row pair of unit wg0 + r W + w.
+    // (half_I is a multiple of 16) -- one staged sub-block of h.  A round arrives in slot r % 2
+    // as four quarters, each two bulk copies (8 gate rows, 8 up rows; rows are whole, H <= 2048)
+    // on its own mbarrier; warp w computes the row pair of unit wg0 + r W + w as soon as its
+    // quarter w / 4 has landed, while the rest of the round still streams in.
     const int n_rounds = my_units;                 // the same for every warp of the CTA
     const uint32_t rows_bytes = (uint32_t)(32 * rbH);
+    const uint32_t qbytes = (uint32_t)(8 * rbH);
     auto issue_round = [&](int r) {
         if (tid != 0 || r >= n_rounds) return;
         const int u0 = blockIdx.x * (nthr / 32) + r * W;
         const int a = u0 / half_I, row0 = 2 * (u0 - a * half_I);
         const int64_t off = (int64_t)R.act_e[a] * p.stride_gu + row0 * rbH;
         uint8_t* dst = cring + (r & 1) * 2 * rows_bytes;
-        uint64_t* bar = &c_bar[r & 1];
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(2 * rows_bytes)
-                     : "memory");
-        bulk_to_smem(dst, p.wg + off, rows_bytes, bar);
-        bulk_to_smem(dst + rows_bytes, p.wu + off, rows_bytes, bar);
+        for (int q = 0; q < 4; ++q) {
+            uint64_t* bar = &c_bar[(r & 1) * 4 + q];
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(2 * qbytes)
+                         : "memory");
+            bulk_to_smem(dst + q * qbytes, p.wg + off + q * qbytes, qbytes, bar);
+            bulk_to_smem(dst + rows_bytes + q * qbytes, p.wu + off + q * qbytes, qbytes, bar);
+        }
     };
     // the CTA's first two rounds go out before anything else
     issue_round(0);
@@ -403,16 +409,16 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
     float acc[4][NT];
     int vidx[NT];
     bool ok = true;
-    int waited = 0, issued = min(2, n_rounds);
+    int issued = min(2, n_rounds);
     for (int r = 0; r < n_rounds; ++r) {
         // (test stall: the first round waits on a barrier that never completes)
-        const bool have = ok && (p.stall && r == 0 ? mbar_wait(&c_bar[2], 0u, p.wait_ns)
-                                                   : mbar_wait(&c_bar[r & 1], (uint32_t)(r >> 1) & 1u, p.wait_ns));
+        const bool have = ok && (p.stall && r == 0 ? mbar_wait(&c_bar[8], 0u, p.wait_ns)
+                                                   : mbar_wait(&c_bar[(r & 1) * 4 + (warp >> 2)], (uint32_t)(r >> 1) & 1u,
+                                                               p.wait_ns));
         if (ok && !have) {
             ok = false;
             if (tid == 0) atomicExch(&p.hdr->status, (int)MOE_ERR_TIMEOUT);
         }
-        if (have) waited = r + 1;
         const int u = wg + r * W;
         const int a = u / half_I, r0 = 2 * (u - a * half_I);
         const int st = R.act_start[a], n = R.act_n[a];
@@ -436,7 +442,7 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
                 q0[q] = *reinterpret_cast<const uint4*>(rb[q] + 16 + 32 * c);
                 q1[q] = *reinterpret_cast<const uint4*>(rb[q] + 32 + 32 * c);
             }
-            qd4_group_math<NT, 4>(hd, q0, q1, live, 0, lane, G, X, XS, n, acc, vidx);
+            qd4_group_math<NT, 4, 2>(hd, q0, q1, live, 0, lane, G, X, XS, n, acc, vidx);
         }
         constexpr int sh = qd_red_shift<NT>();
         const float gv = qd_warp_reduce_t<NT>(acc);
@@ -458,7 +464,8 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
     stamp(p, 1, 5);
     if (!ok && tid == 0) {
         // let no copy land after the CTA exits: wait (bounded) for the ones still in flight
-        for (int i = waited; i < issued; ++i) mbar_wait(&c_bar[i & 1], (uint32_t)(i >> 1) & 1u, p.wait_ns);
+        for (int i = max(0, issued - 2); i < issued; ++i)      // at most two rounds are in flight
+            for (int q = 0; q < 4; ++q) mbar_wait(&c_bar[(i & 1) * 4 + q], (uint32_t)(i >> 1) & 1u, p.wait_ns);
     }
     __syncthreads();
     int round = n_rounds;                          // the shared expert's sub-blocks continue the s_hq parity
@@ -485,7 +492,7 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
         } else {
             const uint8_t* const rowp[4] = {p.sg + r0 * rbH, p.sg + (r0 + 1) * rbH, p.su + r0 * rbH,
                                             p.su + (r0 + 1) * rbH};
-            qd4_rows4<NT, false>(rowp, H / kQ4KWeights, X, XS, T, lane, sacc, sv);
+            qd4_rows4<NT, false, 2>(rowp, H / kQ4KWeights, X, XS, T, lane, sacc, sv);
         }
         // rows 0, 1 = gate of rows r0, r0 + 1; rows 2, 3 = up of the same rows
         constexpr int sh = qd_red_shift<NT>();
@@ -613,9 +620,9 @@ __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_con
                                           : p.wd + (int64_t)s_e[s] * p.stride_d + (int64_t)n * rbI;
             }
             if (p.k3_prefetch) {
-                for (int g = gl; g < GI; g += 16) qd4_group<1, 4, true>(rowp, 0, g, GI, Xs, XSs, 1, acc, nullptr);
+                for (int g = gl; g < GI; g += 16) qd4_group<1, 4, true, 3>(rowp, 0, g, GI, Xs, XSs, 1, acc, nullptr);
             } else {
-                for (int g = gl; g < GI; g += 16) qd4_group<1, 4, false>(rowp, 0, g, GI, Xs, XSs, 1, acc, nullptr);
+                for (int g = gl; g < GI; g += 16) qd4_group<1, 4, false, 3>(rowp, 0, g, GI, Xs, XSs, 1, acc, nullptr);
             }
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
@@ -649,7 +656,7 @@ __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_con
                 const uint8_t* rowp[4];
 #pragma unroll
                 for (int r = 0; r < 4; ++r) rowp[r] = nb + r < H ? p.sd + (int64_t)(nb + r) * rbS : nullptr;
-                qd4_rows4<NT, false>(rowp, p.I_s / kQ4KWeights, SX, SXS, T, lane, acc, vidx);
+                qd4_rows4<NT, false, 3>(rowp, p.I_s / kQ4KWeights, SX, SXS, T, lane, acc, vidx);
             }
             constexpr int sh = qd_red_shift<NT>();
             const float v = qd_warp_reduce_t<NT>(acc);
@@ -801,6 +808,7 @@ bool decode_chain_supported(const DecodeArgs& a) {
     const int P = a.T * a.route.top_k;
     if (a.T < 1 || a.T > kCMaxT || P > kCMaxP || a.route.n_experts > kCMaxE) return false;
     if (a.qtype != MOE_Q4_K) return false;
+    if (!a.x_bf16 && !a.norm_gamma) return false;   // x is staged as bf16 values (two planes)
     if (a.H % kQ4KWeights || a.I % kQ4KWeights || a.H / 4 > kK1MaxVec * kK1Threads) return false;
     // a round of the gate/up kernel copies 32 whole rows of gate and of up: rows of at most
     // kChunkBlocks super-blocks (the ring's slot size), I/2 a multiple of 16

@@ -156,7 +156,8 @@ __device__ void seg_plan(const int32_t* offsets, int E, int U, int ntm, SegPlan&
 }
 
 // ============================================================================ gate/up
-template <int NT>
+// NPL: activation planes (2 for bf16 x, 3 for fp32 x)
+template <int NT, int NPL>
 __global__ void __launch_bounds__(kSThreads, 1) seg_gateup_kernel(const __grid_constant__ SegParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ SegPlan s_plan;
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_gateup_kernel(const __grid_c
             __syncthreads();                               // the previous segment is done with X
             if (tid < nt) s_rows[tid] = __ldcg(p.sorted_pairs + st + pb + tid) / p.k;
             __syncthreads();
-            qd4_stage_par(p.vin, p.vin_bf16 != 0, false, H, nt, s_rows, H, X, XS, tid, kSThreads);
+            qd4_stage_par<NPL>(p.vin, p.vin_bf16 != 0, false, H, nt, s_rows, H, X, XS, tid, kSThreads);
             __syncthreads();
             int issued = 0, waited = 0;                    // items copied / landed in this pass
             auto issue = [&](int item) {
@@ -258,7 +259,7 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_gateup_kernel(const __grid_c
                         q0[r] = *reinterpret_cast<const uint4*>(rb + 16 + 32 * c);
                         q1[r] = *reinterpret_cast<const uint4*>(rb + 32 + 32 * c);
                     }
-                    qd4_group_math<NT, 4>(hd, q0, q1, live, 0, g, G, X, XS, nt, acc, nullptr);
+                    qd4_group_math<NT, 4, NPL>(hd, q0, q1, live, 0, g, G, X, XS, nt, acc, nullptr);
                 }
                 __syncwarp();
                 issue(item + 2);
@@ -331,7 +332,7 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_down_kernel(const __grid_con
             __syncthreads();
             if (tid < nt) s_rows[tid] = st + pb + tid;
             __syncthreads();
-            qd4_stage_par(p.vin, false, true, I, nt, s_rows, I, X, XS, tid, kSThreads);
+            qd4_stage_par<3>(p.vin, false, true, I, nt, s_rows, I, X, XS, tid, kSThreads);
             __syncthreads();
             int issued = 0, waited = 0;                    // items copied / landed in this pass
             auto issue = [&](int item) {
@@ -388,7 +389,7 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_down_kernel(const __grid_con
                             q0[r] = *reinterpret_cast<const uint4*>(rb + 16 + 32 * c);
                             q1[r] = *reinterpret_cast<const uint4*>(rb + 32 + 32 * c);
                         }
-                        qd4_group_math<NT, 4>(hd, q0, q1, live, 0, ch * 32 + lane, GI, X, XS, nt, acc, nullptr);
+                        qd4_group_math<NT, 4, 3>(hd, q0, q1, live, 0, ch * 32 + lane, GI, X, XS, nt, acc, nullptr);
                     }
                 } else if (have) {
                     const uint8_t* rb0 = ring + slot * kSSlotBytes + row * rs;
@@ -399,7 +400,7 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_down_kernel(const __grid_con
                         hd[0] = *reinterpret_cast<const uint4*>(blk);
                         q0[0] = *reinterpret_cast<const uint4*>(blk + 16 + 32 * sub);
                         q1[0] = *reinterpret_cast<const uint4*>(blk + 32 + 32 * sub);
-                        qd4_group_math<NT, 1>(hd, q0, q1, live, 0, (b0 + i) * 4 + sub, GI, X, XS, nt, acc, nullptr);
+                        qd4_group_math<NT, 1, 3>(hd, q0, q1, live, 0, (b0 + i) * 4 + sub, GI, X, XS, nt, acc, nullptr);
                     }
                 }
                 __syncwarp();
@@ -452,10 +453,10 @@ cudaError_t seg_launch(bool gateup, const SegParams& p, cudaStream_t s) {
     const size_t smem = seg_smem<NT>(p.K);
     cudaError_t err;
     if (gateup) {
-        if ((err = cudaFuncSetAttribute(seg_gateup_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-            cudaSuccess)
+        auto* kern = p.vin_bf16 ? seg_gateup_kernel<NT, 2> : seg_gateup_kernel<NT, 3>;
+        if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
             return err;
-        seg_gateup_kernel<NT><<<seg_sms(), kSThreads, smem, s>>>(p);
+        kern<<<seg_sms(), kSThreads, smem, s>>>(p);
     } else {
         if (qd4_groups(p.K) % 32 == 0) {
             if ((err = cudaFuncSetAttribute(seg_down_kernel<NT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -356,30 +356,72 @@ __device__ __forceinline__ float qd_warp_reduce_t(const float (&acc)[4][NT]) {
 
 
 // ============================================================================
-// Q4_K against 24-bit integer activations (the path both GEMV kernels use).
+// Q4_K against integer activations (the path both GEMV kernels use).
 //
 // A row is walked in groups of 64 weights: group g = (super-block b, quant group
 // c), i.e. 32 quant bytes holding sub-blocks 2c (low nibbles) and 2c+1 (high
 // nibbles).  One lane takes one (row, group) item, so it decodes its two
 // sub-block scales once per 64 weights.  Each activation sub-block of 32 values
-// is scaled to 24-bit integers, x24 = round(x * (2^23-1) / max|x|), stored as
-// three byte planes (signed high byte, then two unsigned bytes); the lane
-// multiplies its 4-bit codes with dp4a (exact integer sums), recombines the
-// planes and applies the scales in fp32:
-//   dot_j = (65536*sum(q*hi) + 256*sum(q*mid) + sum(q*lo)) * sx_j
+// (largest magnitude m) is scaled to integers and stored as NPL byte planes (the
+// signed high byte first, then unsigned bytes):
+//   NPL = 3, any input: x24 = round(x * (2^23-1) / m), planes {hi, mid, lo};
+//   NPL = 2, bf16 input: x16 = round(x * 2^(15-e)) with 2^(e-1) <= m < 2^e, planes
+//     {hi, lo}.  The step is a power of two, so a bf16 value (8 significant bits)
+//     within 7 binades of m is held exactly; only smaller ones round, by at most
+//     2^-16 of 2^e.
+// The lane multiplies its 4-bit codes with dp4a (exact integer sums), recombines
+// the planes and applies the scales in fp32:
+//   dot_j = (65536*sum(q*hi) + 256*sum(q*mid) + sum(q*lo)) * sx_j      (NPL = 3)
+//   dot_j = (256*sum(q*hi) + sum(q*lo)) * sx_j                         (NPL = 2)
 //   row . x += d*sc_j*dot_j - dmin*m_j*sum(x over sub-block j)
 // The high nibbles enter dp4a unshifted (byte = 16 q), so their sums are 16x the
-// codes' sums and the factor 1/16 joins the sub-block scale (exact).  The high and
-// middle plane sums are joined in integers (|256*hi + mid| < 2^31, and < 2^24 for
-// the low nibbles) before the one conversion to fp32.
-// The 24-bit rounding is far below fp32 accumulation noise (2^-23 of the block
-// maximum per value).
+// codes' sums and the factor 1/16 joins the sub-block scale (exact).  Plane sums
+// are joined in integers (|256*hi + next| < 2^31) before the conversion to fp32.
+// The sums over sub-block j carry the unrounded values, so the min term is exact;
+// the rounding of x is at most 2^-24 (NPL = 3) or 2^-16 (NPL = 2, bf16 values
+// more than 7 binades below m only) of the sub-block's range.
 // Staged vector layout (G = K/64 groups): X[q*G + g] (q = 0..15) holds the
-// planes {hi, mid, lo, 0} of 4 values: q < 8 values 4q.. of sub-block 2c,
-// q >= 8 values 4(q-8).. of sub-block 2c+1; XS[g] = {sx_lo, sx_hi, sum_lo, sum_hi}.
+// planes {hi, mid, lo, 0} or {hi, lo, 0, 0} of 4 values: q < 8 values 4q.. of
+// sub-block 2c, q >= 8 values 4(q-8).. of sub-block 2c+1;
+// XS[g] = {sx_lo, sx_hi, sum_lo, sum_hi}.
 // ============================================================================
 
 __host__ __device__ inline int qd4_groups(int K) { return K / 64; }
+// Staging of one sub-block with largest magnitude m (NPL planes, see above): the
+// factor inv that maps a value to its integer and the step sx that maps it back.
+template <int NPL>
+__device__ __forceinline__ float2 qx_scale(float m) {
+    if (!(m > 0.f)) return make_float2(0.f, 0.f);
+    if constexpr (NPL == 3) {
+        return make_float2(8388607.0f / m, m / 8388607.0f);
+    } else {
+        int e;
+        (void)frexpf(m, &e);                         // m = f * 2^e, 1/2 <= f < 1
+        return make_float2(ldexpf(1.0f, 15 - e), ldexpf(1.0f, e - 15));
+    }
+}
+template <int NPL>
+__device__ __forceinline__ int qx_int(float v, float inv) {
+    constexpr int kLim = NPL == 3 ? 8388607 : 32767;
+    return max(-kLim, min(kLim, __float2int_rn(v * inv)));
+}
+// byte plane p (0 = the signed high byte) of a staged integer
+template <int NPL>
+__device__ __forceinline__ uint32_t qx_plane(int x, int p) {
+    return ((uint32_t)x >> (8 * (NPL - 1 - p))) & 0xFFu;
+}
+// the staged uint4 of 4 values (planes in .x, .y[, .z])
+template <int NPL>
+__device__ __forceinline__ uint4 qx_pack4(const float (&v)[4], float inv) {
+    uint32_t w[3] = {0u, 0u, 0u};
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const int x = qx_int<NPL>(v[b], inv);
+#pragma unroll
+        for (int pl = 0; pl < NPL; ++pl) w[pl] |= qx_plane<NPL>(x, pl) << (8 * b);
+    }
+    return make_uint4(w[0], w[1], NPL == 3 ? w[2] : 0u, 0u);
+}
 // bytes of one staged vector
 __host__ __device__ inline size_t qd4_vec_bytes(int K) { return (size_t)qd4_groups(K) * 17 * 16; }
 
@@ -392,67 +434,6 @@ __device__ __forceinline__ int qd_dp4a_uu(uint32_t a, uint32_t b, int c) {
     int d;
     asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
-}
-
-// Stage n vectors (vector i at src + row*row_elems, bf16 or fp32; `coherent` reads
-// fp32 through L2) into X + i*16*G, XS + i*G.  One task = one 32-value sub-block.
-// rows (nullable): vector i is source row rows[i] instead of row i.
-__device__ __forceinline__ void qd4_stage(const void* src, bool bf16, bool coherent, int64_t row_elems, int n,
-                                          const int* rows, int K, uint4* X, float4* XS, int tid, int nthr) {
-    const int G = qd4_groups(K);
-    const int tasks = n * G * 2;
-    for (int s = tid; s < tasks; s += nthr) {
-        const int i = s / (2 * G), r = s - i * 2 * G, g = r >> 1, hh = r & 1;
-        const int64_t row = rows ? rows[i] : i;
-        const int64_t e0 = row * row_elems + (g >> 2) * 256 + (2 * (g & 3) + hh) * 32;
-        float v[32];
-        if (bf16) {
-            const uint4* p4 = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(src) + e0);
-            uint4 raw[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) raw[j] = p4[j];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
-#pragma unroll
-                for (int h2 = 0; h2 < 4; ++h2) {
-                    v[8 * j + 2 * h2] = __uint_as_float(w[h2] << 16);
-                    v[8 * j + 2 * h2 + 1] = __uint_as_float(w[h2] & 0xFFFF0000u);
-                }
-            }
-        } else {
-            const float4* p4 = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + e0);
-            float4 raw[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) raw[j] = coherent ? __ldcg(p4 + j) : p4[j];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                v[4 * j] = raw[j].x; v[4 * j + 1] = raw[j].y; v[4 * j + 2] = raw[j].z; v[4 * j + 3] = raw[j].w;
-            }
-        }
-        float m = 0.f, sum = 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) { m = fmaxf(m, fabsf(v[j])); sum += v[j]; }
-        const float inv = m > 0.f ? 8388607.0f / m : 0.f;
-        const float sx = m / 8388607.0f;
-        uint4* Xi = X + (size_t)i * 16 * G;
-#pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) {
-            uint32_t hw = 0, mw = 0, lw = 0;
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                int x24 = __float2int_rn(v[4 * q8 + b] * inv);
-                x24 = max(-8388607, min(8388607, x24));
-                hw |= ((uint32_t)(x24 >> 16) & 0xFFu) << (8 * b);
-                mw |= ((uint32_t)(x24 >> 8) & 0xFFu) << (8 * b);
-                lw |= ((uint32_t)x24 & 0xFFu) << (8 * b);
-            }
-            Xi[(hh * 8 + q8) * G + g] = make_uint4(hw, mw, lw, 0u);
-        }
-        float* xsf = reinterpret_cast<float*>(XS + (size_t)i * G + g);
-        xsf[hh] = sx;
-        xsf[2 + hh] = sum;
-    }
 }
 
 // RMSNorm of one fp32 row, r = 1 / sqrt(mean(x^2) + eps), in the summation order of
@@ -512,11 +493,15 @@ __device__ __forceinline__ float4 rms_apply4(float4 x, float r, float4 g) {
                        __bfloat162float(__float2bfloat16_rn(x.w * r * g.w)));
 }
 
-// Same layout as qd4_stage.  Work is split in chunks of 32 values (4 sub-blocks of 8
-// threads, 4 values per thread, max and sum by butterfly within the 8); warp w of nw
-// takes chunks w, w + nw, ... with four chunks' loads in flight.  Every lane of every
-// warp in [0, nw) must call it.  With ngamma, src is fp32 and vector i is staged as its
-// RMSNorm output bf16(x * nscale[i] * gamma) (nscale: the vectors' scales, shared memory).
+// Stage n vectors (vector i at src + row*row_elems, bf16 or fp32; `coherent` reads fp32
+// through L2; rows (nullable): vector i is source row rows[i]) into X + i*16*G, XS + i*G
+// as NPL planes (NPL = 2 only for bf16 values: bf16 src, or the normalized input below).
+// Work is split in chunks of 32 values (4 sub-blocks of 8 threads, 4 values per thread,
+// max and sum by butterfly within the 8); warp w of nw takes chunks w, w + nw, ... with
+// four chunks' loads in flight.  Every lane of every warp in [0, nw) must call it.  With
+// ngamma, src is fp32 and vector i is staged as its RMSNorm output bf16(x * nscale[i] *
+// gamma) (nscale: the vectors' scales, shared memory).
+template <int NPL>
 __device__ __forceinline__ void qd4_stage_par(const void* src, bool bf16, bool coherent, int64_t row_elems, int n,
                                               const int* rows, int K, uint4* X, float4* XS, int tid, int nthr,
                                               const float* ngamma = nullptr, const float* nscale = nullptr) {
@@ -567,21 +552,12 @@ __device__ __forceinline__ void qd4_stage_par(const void* src, bool bf16, bool c
                 sum += __shfl_xor_sync(0xffffffffu, sum, o);
             }
             const int i = iv[j], sb = sbv[j], g = sb >> 1, hh = sb & 1;
-            const float inv = m > 0.f ? 8388607.0f / m : 0.f;
+            const float2 sc = qx_scale<NPL>(m);
             const float vv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-            uint32_t hw = 0, mw = 0, lw = 0;
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                int x24 = __float2int_rn(vv[b] * inv);
-                x24 = max(-8388607, min(8388607, x24));
-                hw |= ((uint32_t)(x24 >> 16) & 0xFFu) << (8 * b);
-                mw |= ((uint32_t)(x24 >> 8) & 0xFFu) << (8 * b);
-                lw |= ((uint32_t)x24 & 0xFFu) << (8 * b);
-            }
-            X[(size_t)i * 16 * G + (hh * 8 + q8) * G + g] = make_uint4(hw, mw, lw, 0u);
+            X[(size_t)i * 16 * G + (hh * 8 + q8) * G + g] = qx_pack4<NPL>(vv, sc.x);
             if (q8 == 0) {
                 float* xsf = reinterpret_cast<float*>(XS + (size_t)i * G + g);
-                xsf[hh] = m / 8388607.0f;
+                xsf[hh] = sc.y;
                 xsf[2 + hh] = sum;
             }
         }
@@ -616,7 +592,7 @@ __device__ __forceinline__ void qd4_scales(const uint4& hd, int c, float (&fs)[2
 // RPL rows whose bytes are already loaded: hd = the 16-byte block header, q0/q1 = the
 // 32 quant bytes of the group.  acc[r0 + i][t] += row i . vector vidx[t] (t < nt); the
 // activation planes of the group are read once and serve every row.
-template <int NT, int RPL>
+template <int NT, int RPL, int NPL>
 __device__ __forceinline__ void qd4_group_math(const uint4 (&hd)[RPL], const uint4 (&q0)[RPL], const uint4 (&q1)[RPL],
                                                const bool (&live)[RPL], int r0, int g, int G, const uint4* X,
                                                const float4* XS, int nt, float (&acc)[4][NT], const int* vidx) {
@@ -635,7 +611,7 @@ __device__ __forceinline__ void qd4_group_math(const uint4 (&hd)[RPL], const uin
         if (t < nt) {
             const int v = vidx ? vidx[t] : t;
             const uint4* Xv = X + (size_t)v * 16 * G + g;
-            int ah[RPL][2], am[RPL][2], al[RPL][2];
+            int ah[RPL][2], am[RPL][2], al[RPL][2];       // am: the middle plane (NPL = 3)
 #pragma unroll
             for (int i = 0; i < RPL; ++i) ah[i][0] = ah[i][1] = am[i][0] = am[i][1] = al[i][0] = al[i][1] = 0;
 #pragma unroll
@@ -645,19 +621,30 @@ __device__ __forceinline__ void qd4_group_math(const uint4 (&hd)[RPL], const uin
                 for (int i = 0; i < RPL; ++i) {
                     const uint32_t ql = qw[i][qd] & 0x0F0F0F0Fu, qh = qw[i][qd] & 0xF0F0F0F0u;
                     ah[i][0] = qd_dp4a_us(ql, xl.x, ah[i][0]);
-                    am[i][0] = qd_dp4a_uu(ql, xl.y, am[i][0]);
-                    al[i][0] = qd_dp4a_uu(ql, xl.z, al[i][0]);
                     ah[i][1] = qd_dp4a_us(qh, xh.x, ah[i][1]);
-                    am[i][1] = qd_dp4a_uu(qh, xh.y, am[i][1]);
-                    al[i][1] = qd_dp4a_uu(qh, xh.z, al[i][1]);
+                    if constexpr (NPL == 3) {
+                        am[i][0] = qd_dp4a_uu(ql, xl.y, am[i][0]);
+                        am[i][1] = qd_dp4a_uu(qh, xh.y, am[i][1]);
+                        al[i][0] = qd_dp4a_uu(ql, xl.z, al[i][0]);
+                        al[i][1] = qd_dp4a_uu(qh, xh.z, al[i][1]);
+                    } else {
+                        al[i][0] = qd_dp4a_uu(ql, xl.y, al[i][0]);
+                        al[i][1] = qd_dp4a_uu(qh, xh.y, al[i][1]);
+                    }
                 }
             }
             const float4 xs = XS[(size_t)v * G + g];
 #pragma unroll
             for (int i = 0; i < RPL; ++i) {
                 if (live[i]) {
-                    const float d0 = fmaf((float)(ah[i][0] * 256 + am[i][0]), 256.0f, (float)al[i][0]) * xs.x;
-                    const float d1 = fmaf((float)(ah[i][1] * 256 + am[i][1]), 256.0f, (float)al[i][1]) * xs.y;
+                    float d0, d1;
+                    if constexpr (NPL == 3) {
+                        d0 = fmaf((float)(ah[i][0] * 256 + am[i][0]), 256.0f, (float)al[i][0]) * xs.x;
+                        d1 = fmaf((float)(ah[i][1] * 256 + am[i][1]), 256.0f, (float)al[i][1]) * xs.y;
+                    } else {
+                        d0 = (float)(ah[i][0] * 256 + al[i][0]) * xs.x;
+                        d1 = (float)(ah[i][1] * 256 + al[i][1]) * xs.y;
+                    }
                     float part = fs[i][0] * d0;
                     part = fmaf(fs[i][1], d1, part);
                     part = fmaf(-fm[i][0], xs.z, part);
@@ -672,7 +659,7 @@ __device__ __forceinline__ void qd4_group_math(const uint4 (&hd)[RPL], const uin
 }
 
 // qd4_group_math with the rows' bytes read here (rows r0..r0+RPL-1 of rowp; NULL rows skipped).
-template <int NT, int RPL, bool kSmemRows>
+template <int NT, int RPL, bool kSmemRows, int NPL>
 __device__ __forceinline__ void qd4_group(const uint8_t* const (&rowp)[4], int r0, int g, int G, const uint4* X,
                                           const float4* XS, int nt, float (&acc)[4][NT], const int* vidx) {
     const int b = g >> 2, c = g & 3;
@@ -691,26 +678,26 @@ __device__ __forceinline__ void qd4_group(const uint8_t* const (&rowp)[4], int r
             hd[i] = q0[i] = q1[i] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
-    qd4_group_math<NT, RPL>(hd, q0, q1, live, r0, g, G, X, XS, nt, acc, vidx);
+    qd4_group_math<NT, RPL, NPL>(hd, q0, q1, live, r0, g, G, X, XS, nt, acc, vidx);
 }
 
 // acc[r][t] += row r . vector vidx[t] (t < nt) for 4 Q4_K rows of nblk super-blocks.
 // Rows may be NULL (skipped).  Vector v lives at X + v*16*G, XS + v*G.  Lanes split
 // into row subsets so that every lane reuses one group's activations over 4, 2 or 1
 // rows (long rows: 4; 12-23 groups: 2; shorter: 1).
-template <int NT, bool kSmemRows = false>
+template <int NT, bool kSmemRows, int NPL>
 __device__ __forceinline__ void qd4_rows4(const uint8_t* const (&rowp)[4], int nblk, const uint4* X,
                                           const float4* XS, int nt, int lane, float (&acc)[4][NT],
                                           const int* vidx = nullptr) {
     const int G = nblk * 4;
     if (G >= 24) {
-        for (int g = lane; g < G; g += 32) qd4_group<NT, 4, kSmemRows>(rowp, 0, g, G, X, XS, nt, acc, vidx);
+        for (int g = lane; g < G; g += 32) qd4_group<NT, 4, kSmemRows, NPL>(rowp, 0, g, G, X, XS, nt, acc, vidx);
     } else if (G >= 12) {
         const int rs = lane >> 4;
-        for (int g = lane & 15; g < G; g += 16) qd4_group<NT, 2, kSmemRows>(rowp, 2 * rs, g, G, X, XS, nt, acc, vidx);
+        for (int g = lane & 15; g < G; g += 16) qd4_group<NT, 2, kSmemRows, NPL>(rowp, 2 * rs, g, G, X, XS, nt, acc, vidx);
     } else {
         const int rs = lane >> 3;
-        for (int g = lane & 7; g < G; g += 8) qd4_group<NT, 1, kSmemRows>(rowp, rs, g, G, X, XS, nt, acc, vidx);
+        for (int g = lane & 7; g < G; g += 8) qd4_group<NT, 1, kSmemRows, NPL>(rowp, rs, g, G, X, XS, nt, acc, vidx);
     }
 }
 

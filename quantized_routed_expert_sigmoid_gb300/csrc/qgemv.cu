@@ -51,7 +51,8 @@ __device__ __forceinline__ void qd_store_units(const float (&acc)[4][NT], int la
     }
 }
 
-template <int QT, bool GATEUP, int NT>
+// NPL: activation planes of the Q4_K path (2 for bf16 input, 3 otherwise; unused for Q8_0)
+template <int QT, bool GATEUP, int NT, int NPL>
 __global__ void __launch_bounds__(kThreads, 2) qgemv_kernel(GemvArgs a, int iters, int units_per_warp) {
     extern __shared__ float4 xs[];                    // [NT][iters*256] float4
     float2* xsum = reinterpret_cast<float2*>(xs + (size_t)NT * iters * 256);  // [NT][iters*32]
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 2) qgemv_kernel(GemvArgs a, int iter
     for (int pb = 0; pb < n_tot; pb += NT) {
         const int nt = min(NT, n_tot - pb);
         if (QT == MOE_Q4_K) {
-            // ---- stage the activation vectors as 24-bit integer planes (qdot.cuh)
+            // ---- stage the activation vectors as 16-bit integer planes (qdot.cuh)
             uint4* X = reinterpret_cast<uint4*>(xs);
             float4* XS = reinterpret_cast<float4*>(X + (size_t)NT * 16 * qd4_groups(a.K));
             if (threadIdx.x < nt) {
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 2) qgemv_kernel(GemvArgs a, int iter
                 s_rows[threadIdx.x] = (GATEUP && a.sorted_pairs) ? a.sorted_pairs[i] / a.k : i;
             }
             __syncthreads();
-            qd4_stage_par(a.vin, a.vin_bf16, false, a.K, nt, s_rows, a.K, X, XS, threadIdx.x, kThreads);
+            qd4_stage_par<NPL>(a.vin, a.vin_bf16, false, a.K, nt, s_rows, a.K, X, XS, threadIdx.x, kThreads);
             __syncthreads();
             for (int ui = 0; ui < units_per_warp; ++ui) {
                 const int unit = (blockIdx.x * kWarps + warp) * units_per_warp + ui;
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 2) qgemv_kernel(GemvArgs a, int iter
                 for (int r = 0; r < 4; ++r)
 #pragma unroll
                     for (int t = 0; t < NT; ++t) acc[r][t] = 0.f;
-                qd4_rows4<NT>(rowp, nblk, X, XS, nt, lane, acc);
+                qd4_rows4<NT, false, NPL>(rowp, nblk, X, XS, nt, lane, acc);
                 qd_store_units<NT, GATEUP>(acc, lane, nt, a.out + (int64_t)(start + pb) * a.rows, a.rows, unit);
             }
             __syncthreads();
@@ -187,12 +188,12 @@ __global__ void __launch_bounds__(kThreads, 2) qgemv_kernel(GemvArgs a, int iter
     }
 }
 
-template <int QT, bool GU, int NT>
+template <int QT, bool GU, int NT, int NPL>
 cudaError_t launch_one(const GemvArgs& a, int iters, int grid_y, cudaStream_t s) {
     const size_t smem = QT == MOE_Q4_K ? (size_t)NT * qd4_vec_bytes(a.K)
                                        : (size_t)NT * iters * 256 * sizeof(float4) + (size_t)NT * iters * 32 * sizeof(float2);
     if (smem > 48 * 1024) {
-        cudaError_t err = cudaFuncSetAttribute(qgemv_kernel<QT, GU, NT>,
+        cudaError_t err = cudaFuncSetAttribute(qgemv_kernel<QT, GU, NT, NPL>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
     }
@@ -204,17 +205,17 @@ cudaError_t launch_one(const GemvArgs& a, int iters, int grid_y, cudaStream_t s)
     const int64_t target_warps = (int64_t)kWarps * 4 * (sms > 0 ? sms : 152);
     const int upw = (int)std::max<int64_t>(1, ((int64_t)n_units * grid_y + target_warps - 1) / target_warps);
     const int grid_x = (n_units + kWarps * upw - 1) / (kWarps * upw);
-    qgemv_kernel<QT, GU, NT><<<dim3(grid_x, grid_y), kThreads, smem, s>>>(a, iters, upw);
+    qgemv_kernel<QT, GU, NT, NPL><<<dim3(grid_x, grid_y), kThreads, smem, s>>>(a, iters, upw);
     return cudaGetLastError();
 }
 
-template <int QT, bool GU>
+template <int QT, bool GU, int NPL>
 cudaError_t launch_nt(const GemvArgs& a, int nt, int iters, int grid_y, cudaStream_t s) {
     switch (nt) {
-        case 1: return launch_one<QT, GU, 1>(a, iters, grid_y, s);
-        case 2: return launch_one<QT, GU, 2>(a, iters, grid_y, s);
-        case 4: return launch_one<QT, GU, 4>(a, iters, grid_y, s);
-        default: return launch_one<QT, GU, 8>(a, iters, grid_y, s);
+        case 1: return launch_one<QT, GU, 1, NPL>(a, iters, grid_y, s);
+        case 2: return launch_one<QT, GU, 2, NPL>(a, iters, grid_y, s);
+        case 4: return launch_one<QT, GU, 4, NPL>(a, iters, grid_y, s);
+        default: return launch_one<QT, GU, 8, NPL>(a, iters, grid_y, s);
     }
 }
 
@@ -230,11 +231,13 @@ cudaError_t launch_qgemv(const GemvArgs& a, cudaStream_t s) {
     int nt = 8;
     while (nt > 1 && ((size_t)nt * per_vec > 64 * 1024 || nt / 2 >= per_expert_max)) nt /= 2;
     const int grid_y = a.offsets ? (a.n_pairs < a.E ? a.n_pairs : a.E) : 1;
-    if (a.qtype == MOE_Q4_K)
-        return a.gateup ? launch_nt<MOE_Q4_K, true>(a, nt, iters, grid_y, s)
-                        : launch_nt<MOE_Q4_K, false>(a, nt, iters, grid_y, s);
-    return a.gateup ? launch_nt<MOE_Q8_0, true>(a, nt, iters, grid_y, s)
-                    : launch_nt<MOE_Q8_0, false>(a, nt, iters, grid_y, s);
+    if (a.qtype == MOE_Q4_K) {
+        if (!a.gateup) return launch_nt<MOE_Q4_K, false, 3>(a, nt, iters, grid_y, s);   // h is fp32
+        return a.vin_bf16 ? launch_nt<MOE_Q4_K, true, 2>(a, nt, iters, grid_y, s)
+                          : launch_nt<MOE_Q4_K, true, 3>(a, nt, iters, grid_y, s);
+    }
+    return a.gateup ? launch_nt<MOE_Q8_0, true, 3>(a, nt, iters, grid_y, s)
+                    : launch_nt<MOE_Q8_0, false, 3>(a, nt, iters, grid_y, s);
 }
 
 }  // namespace moe

@@ -5,6 +5,8 @@ must be within rel-L2 1e-4 of the oracle on the fp32 GEMV path.
 """
 from __future__ import annotations
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -44,6 +46,16 @@ def test_tiny_q8_0(T):
 def test_decode_q4_k(T):
     tl = make_layer(synth.DECODE, 2, T)
     _check_layer(tl, T)
+
+
+@pytest.mark.parametrize("T", [2, 9, 40])
+def test_decode_q4_k_fp32_activations(T):
+    # fp32 x: the Q4_K kernels stage it as three byte planes (bf16 x takes two); the chained
+    # decode kernels take bf16 values only, so T = 2 runs the separate kernels as well
+    shape = dataclasses.replace(synth.DECODE, x_dtype="fp32")
+    tl = make_layer(shape, 23, T)
+    layer, _, _ = _check_layer(tl, T, tc_min_tokens=1 << 30)
+    assert layer.path(T) == "gemv"
 
 
 def test_decode_q4_k_ragged_batch():
