@@ -742,7 +742,7 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="override the layers per step (default per workload)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (tokens per layer call)")
     ap.add_argument("--tc-min-tokens", type=int, default=0,
-                    help="smallest T that takes the tensor-core path (default: the library's, 128)")
+                    help="smallest T that takes the tensor-core path (default: the library's, 65)")
     ap.add_argument("--no-sub", action="store_true",
                     help="decode: skip the sub-records of decode T=2 and prefill T=4096")
     ap.add_argument("--separate-decode", action="store_true",

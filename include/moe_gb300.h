@@ -248,7 +248,7 @@ typedef struct {
     int shared_intermediate;      /* I_s, 0 = no shared expert */
     moe_qmat s_gate, s_up, s_down;/* shared expert (single matrices) */
     int accumulate;               /* 1: out += layer(x) (a residual add); 0: out = layer(x) */
-    int tc_min_tokens;            /* T at or above this uses the tensor-core path (0 = default 128) */
+    int tc_min_tokens;            /* T at or above this uses the tensor-core path (0 = default 65) */
     int decode_chain_off;         /* 1: never use the chained decode kernels (T <= 4) */
     /* Pre-norm (nullable): x is the fp32 residual stream [T][H] (x_type MOE_F32) and the layer's
      * input is u = bf16(x / sqrt(mean_h x^2 + norm_eps) * norm_gamma), exactly as moe_rmsnorm_bf16
@@ -349,8 +349,9 @@ moe_status moe_debug_set_waits(uint64_t limit_ns, int stall);
  * at phase ph into buf[(n*256 + c)*8 + ph] (uint64): n = 0: 0 start, 1 after the wait for
  * the previous launch, 2 router dot products done, 3 end; n = 1: 0 start, 1 activations
  * staged, 2 after the wait, 3 routing read, 4 first unit computed, 5 units done, 6 CTA
- * done, 7 top-k written (the CTA that routes); n = 2: 0 start, 1 after the wait, 2 ids
- * read, 3 copies issued, 4 copies landed, 5 dot products done, 6 CTA done.  Calls overwrite the same slots; a graph keeps the setting it was
+ * done, 7 top-k written; n = 2: 0 start, 2 routing read and down rows requested (before
+ * the wait), 1 after the wait, 3 h copies issued, 4 copies landed, 5 dot products done, 6 CTA
+ * done.  Calls overwrite the same slots; a graph keeps the setting it was
  * captured with.  For measuring where a decode layer's time goes; the results are
  * unchanged.  Pages: step times there are quoted with their instrumentation state
  * ("bloomery early V4.1 README", caveats of the depth measurement).

@@ -531,7 +531,7 @@ moe_status moe_layer_plan_create(const moe_layer_desc* desc, moe_layer_plan** pl
     moe_layer_plan* p = new (std::nothrow) moe_layer_plan;
     if (!p) return fail(MOE_ERR_INVALID_ARG, "out of host memory");
     p->d = d;
-    if (p->d.tc_min_tokens <= 0) p->d.tc_min_tokens = 128;
+    if (p->d.tc_min_tokens <= 0) p->d.tc_min_tokens = 65;      // T > 64: the grouped GEMM
     *plan = p;
     return MOE_OK;
 }

@@ -252,7 +252,10 @@ __global__ void __launch_bounds__(kK1Threads) chain_logits_kernel(const __grid_c
     pdl_wait();                                   // x and the workspace belong to the launches before
     pdl_launch_dependents();
     stamp(p, 0, 1);
-    if (e == 0 && tid == 0) p.hdr->status = MOE_OK;
+    if (e == 0 && tid == 0) {
+        p.hdr->status = MOE_OK;
+        p.hdr->route_ready = 0u;
+    }
     const bool xb = p.x_bf16 != 0;
     // pre-norm: the tokens' RMSNorm scales, by all warps
     __shared__ float s_r[kCMaxT], s_rpart[kCMaxT][8];
@@ -376,13 +379,11 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
     // the CTA's first two rounds go out before anything else
     issue_round(0);
     issue_round(1);
-    // ---- this CTA's share of the chosen down rows (and the shared expert's) into L2
-    {
+    // ---- this CTA's share of the shared expert's down rows into L2 (the routed down rows are
+    // fetched by the down kernel itself, which starts on the SMs this kernel leaves early)
+    if constexpr (has_shared) {
         const int rows0 = (int)((int64_t)blockIdx.x * H / gridDim.x), rows1 = (int)((int64_t)(blockIdx.x + 1) * H / gridDim.x);
-        const int64_t rbI = (int64_t)(I / kQ4KWeights) * kQ4KBytes;
-        if (warp == 0 && lane < nact && rows1 > rows0)
-            prefetch_l2(p.wd + (int64_t)R.act_e[lane] * p.stride_d + rows0 * rbI, (int64_t)(rows1 - rows0) * rbI);
-        if (warp == 0 && lane == 31 && has_shared && rows1 > rows0) {
+        if (warp == 0 && lane == 31 && rows1 > rows0) {
             const int64_t rbS = p.s_q8 ? (p.s_q80r ? q80r_row_bytes(p.I_s) : (int64_t)(p.I_s / kQ80Weights) * kQ80Bytes)
                                        : (int64_t)(p.I_s / kQ4KWeights) * kQ4KBytes;
             if ((rbS % 16) == 0) prefetch_l2(p.sd + rows0 * rbS, (int64_t)(rows1 - rows0) * rbS);
@@ -400,6 +401,11 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
             int cnt = 0;
             for (int i = 0; i < P; ++i) cnt += R.ids[i] < e ? 1 : 0;
             p.offsets[e] = cnt;
+        }
+        __syncthreads();
+        if (tid == 0) {                            // the down kernel may read the routing from here on
+            __threadfence();
+            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(&p.hdr->route_ready), "r"(1u) : "memory");
         }
     }
     // ---- the rounds.  Every warp runs all of them, so the barrier below is reached uniformly,
@@ -526,7 +532,8 @@ __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_con
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ int32_t s_e[kCMaxP], s_pos[kCMaxP];
     __shared__ float s_w[kCMaxP];
-    __shared__ __align__(8) uint64_t s_wbar;
+    __shared__ __align__(8) uint64_t s_wbar, s_hbar;
+    __shared__ int s_route_ok;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = p.T, H = p.H, I = p.I, k = p.rc.k, P = T * k;
     const int GI = qd4_groups(I);
@@ -541,44 +548,70 @@ __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_con
     const int GS = kSh == 1 ? qd4_groups(p.I_s) : 1;
     float4* SXS = reinterpret_cast<float4*>(SX + (size_t)T * 16 * GS);   // then [T][GS] float4
     stamp(p, 2, 0);
-    pdl_wait();                                   // h and the routing of K2
-    pdl_launch_dependents();
-    stamp(p, 2, 1);
+    // ---- the routing, which CTA 0 of the gate/up kernel publishes ahead of its units: read it
+    // (and fetch the down rows it selects) while the gate/up kernel still computes h
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_wbar)) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_hbar)) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    for (int i = tid; i < P; i += kK3Threads) {
-        s_e[i] = __ldcg(p.ids + i);
-        s_pos[i] = __ldcg(p.pair_pos + i);
-        s_w[i] = __ldcg(p.gw + i);
+        uint32_t ready = 0u;
+        const uint64_t t0 = gtime();
+        for (;;) {
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(ready) : "l"(&p.hdr->route_ready) : "memory");
+            if (ready || gtime() - t0 > p.wait_ns) break;
+            __nanosleep(64);
+        }
+        s_route_ok = ready != 0u;
+        if (!ready) atomicExch(&p.hdr->status, (int)MOE_ERR_TIMEOUT);
     }
     __syncthreads();
+    const bool route_ok = s_route_ok != 0;
+    if (route_ok)
+        for (int i = tid; i < P; i += kK3Threads) {
+            s_e[i] = __ldcg(p.ids + i);
+            s_pos[i] = __ldcg(p.pair_pos + i);
+            s_w[i] = __ldcg(p.gw + i);
+        }
+    __syncthreads();
     stamp(p, 2, 2);
-    // ---- bulk copies into shared memory, all completing on one mbarrier: the CTA's down rows
-    // of every pair (rows n0.. of one expert are contiguous: one copy per pair), and every
-    // pair's h, which the gate/up kernel wrote already staged (one copy per pair)
     const int nrows = min(R, H - n0);
-    const bool wcopy = p.k3_prefetch && nrows > 0;
+    const bool wcopy = route_ok && p.k3_prefetch && nrows > 0;
+    if (route_ok && !p.k3_prefetch && nrows > 0 && warp == 0)   // rows read in place later: into L2 now
+        for (int s = lane; s < P; s += 32)
+            prefetch_l2(p.wd + (int64_t)s_e[s] * p.stride_d + (int64_t)n0 * rbI, (int64_t)nrows * rbI);
+    if (wcopy) {
+        if (tid == 0)
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&s_wbar)),
+                         "r"((uint32_t)(P * nrows * rbI))
+                         : "memory");
+        __syncthreads();
+        if (warp == 0)
+            for (int s = lane; s < P; s += 32)
+                bulk_to_smem(wbuf + (int64_t)s * R * rbI, p.wd + (int64_t)s_e[s] * p.stride_d + (int64_t)n0 * rbI,
+                             (uint32_t)(nrows * rbI), &s_wbar);
+    }
+    pdl_wait();                                   // h of K2
+    pdl_launch_dependents();
+    stamp(p, 2, 1);
+    if (!route_ok) return;
+    // ---- every pair's h, which the gate/up kernel wrote already staged (one bulk copy per
+    // pair); the CTA's down rows of every pair (rows n0.. of one expert are contiguous: one
+    // copy per pair) were requested above, on their own mbarrier
     if (tid == 0) {
         uint32_t total = (uint32_t)P * vb;
-        if (wcopy) total += (uint32_t)(P * nrows * rbI);
         if (kSh == 1) total += (uint32_t)T * 272 * GS;
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&s_wbar)), "r"(total)
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&s_hbar)), "r"(total)
                      : "memory");
     }
-    if (warp == 0 && wcopy) {
+    __syncthreads();
+    if (warp == 1) {
         for (int s = lane; s < P; s += 32)
-            bulk_to_smem(wbuf + (int64_t)s * R * rbI, p.wd + (int64_t)s_e[s] * p.stride_d + (int64_t)n0 * rbI,
-                         (uint32_t)(nrows * rbI), &s_wbar);
-    } else if (warp == 1) {
-        for (int s = lane; s < P; s += 32)
-            bulk_to_smem(hsm + (size_t)s * vb, p.hq + (size_t)s_pos[s] * vb, (uint32_t)vb, &s_wbar);
+            bulk_to_smem(hsm + (size_t)s * vb, p.hq + (size_t)s_pos[s] * vb, (uint32_t)vb, &s_hbar);
     } else if (warp == 2 && kSh == 1) {
         for (int t = lane; t < T; t += 32) {
             const uint8_t* src = p.hq_s + (size_t)t * 272 * GS;
-            bulk_to_smem(SX + (size_t)t * 16 * GS, src, (uint32_t)(256 * GS), &s_wbar);
-            bulk_to_smem(SXS + (size_t)t * GS, src + 256 * GS, (uint32_t)(16 * GS), &s_wbar);
+            bulk_to_smem(SX + (size_t)t * 16 * GS, src, (uint32_t)(256 * GS), &s_hbar);
+            bulk_to_smem(SXS + (size_t)t * GS, src + 256 * GS, (uint32_t)(16 * GS), &s_hbar);
         }
     }
     if constexpr (kSh == 2) {                          // Q8_0 shared expert: its h is fp32
@@ -586,12 +619,13 @@ __global__ void __launch_bounds__(kK3Threads) chain_down_kernel(const __grid_con
         qd_stage_many_f32<MOE_Q8_0>(p.h_s, p.I_s, T, p.I_s, p.it_Is_s, hs, tid, kK3Threads);
     }
     stamp(p, 2, 3);
-    const bool landed = mbar_wait(&s_wbar, 0u, p.wait_ns);
+    const bool landed = mbar_wait(&s_hbar, 0u, p.wait_ns) && (!wcopy || mbar_wait(&s_wbar, 0u, p.wait_ns));
     if (__syncthreads_or(!landed)) {
         // the copies did not complete in time: report it; let none land after the CTA exits
         if (tid == 0) {
             atomicExch(&p.hdr->status, (int)MOE_ERR_TIMEOUT);
-            mbar_wait(&s_wbar, 0u, p.wait_ns);
+            mbar_wait(&s_hbar, 0u, p.wait_ns);
+            if (wcopy) mbar_wait(&s_wbar, 0u, p.wait_ns);
         }
         __syncthreads();
         return;
@@ -703,6 +737,7 @@ int sm_count() {
 }
 
 constexpr size_t kChainSmemCap = 200 * 1024;   // dynamic; the kernels' static shared memory is < 12 KB
+constexpr size_t kK3TwoPerSm = 108 * 1024;     // dynamic shared memory of a down CTA that still fits twice
 
 ChainLayout chain_layout(const DecodeArgs& a) {
     ChainLayout L{};
@@ -731,8 +766,10 @@ ChainLayout chain_layout(const DecodeArgs& a) {
     L.k3_off_y = (int)align_up(o, 16);
     o = L.k3_off_y + (size_t)(P + T) * R * 4;
     L.k3_off_w = (int)align_up(o, 16);
+    // the down rows are copied into shared memory only while two CTAs still fit an SM (the
+    // grid is about two CTAs per SM); otherwise they are read in place, from L2
     const size_t wbytes = (size_t)P * R * (size_t)(I / kQ4KWeights) * kQ4KBytes;
-    L.k3_prefetch = L.k3_off_w + wbytes <= kChainSmemCap ? 1 : 0;
+    L.k3_prefetch = L.k3_off_w + wbytes <= kK3TwoPerSm ? 1 : 0;
     L.k3_smem = L.k3_off_w + (L.k3_prefetch ? wbytes : 0);
     return L;
 }

@@ -39,6 +39,7 @@ constexpr int kPermuteChunk = 1024;  // pairs per permute CTA
 struct WsHeader {
     int32_t status;
     uint32_t ticket;
+    uint32_t route_ready;    // chained decode: the routing is in the workspace (cleared by the logits kernel)
 };
 constexpr size_t kHeaderBytes = 256;
 

@@ -30,6 +30,55 @@ struct RouteCfgDev {
     float scale;
 };
 
+// Sigmoid-group scoring of one token (whole warp): sv[e] = s = 1/(1+exp(-l)), sel[e] = s + b
+// for the experts of the topk_groups best groups (a group scored by the sum of its two largest
+// sel, ties to the lower group), sel[e] = -inf outside them.  Kept out of line: the chained
+// decode kernel inlines only the softmax scoring, the common case there.
+static __device__ __noinline__ void warp_scores_sigmoid_group(const RouteCfgDev& c, const float* lrow, const float* bias,
+                                                       float* sel, float* sv) {
+    const int lane = threadIdx.x & 31;
+    const int E = c.E;
+    for (int e0 = 0; e0 < E; e0 += 8 * 32) {
+        float l[8], b[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = e0 + i * 32 + lane;
+            l[i] = e < E ? __ldcg(lrow + e) : 0.f;
+            b[i] = (bias && e < E) ? __ldg(bias + e) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = e0 + i * 32 + lane;
+            if (e < E) {
+                const float s = 1.0f / (1.0f + expf(-l[i]));
+                sv[e] = s;
+                sel[e] = s + b[i];
+            }
+        }
+    }
+    __syncwarp();
+    const int per = E / c.G;
+    float gs = -INFINITY;
+    if (lane < c.G) {
+        float b1 = -INFINITY, b2 = -INFINITY;
+        for (int i = 0; i < per; ++i) {
+            const float v = sel[lane * per + i];
+            if (v > b1) { b2 = b1; b1 = v; } else if (v > b2) { b2 = v; }
+        }
+        gs = per >= 2 ? b1 + b2 : b1;
+    }
+    uint32_t keep = 0u;
+    for (int r = 0; r < c.Gk; ++r) {
+        float v = (lane < c.G && !((keep >> lane) & 1u)) ? gs : -INFINITY;
+        int id = (lane < c.G && !((keep >> lane) & 1u)) ? lane : 0x7fffffff;
+        warp_argmax(v, id);
+        if (id < 32) keep |= 1u << id;
+    }
+    for (int e = lane; e < E; e += 32)
+        if (!((keep >> (e / per)) & 1u)) sel[e] = -INFINITY;
+    __syncwarp();
+}
+
 // The whole warp selects token `lrow`'s k experts and writes them in ascending id
 // order to ids[0..k) with their gates w[0..k).  sel, sv: 2*E floats of per-warp
 // shared memory.  lrow is read through L2 (it may have been written by other CTAs
@@ -40,52 +89,24 @@ __device__ __forceinline__ void warp_topk_n(const RouteCfgDev& c, const float* l
     const int lane = threadIdx.x & 31;
     const int E = c.E, k = c.k;
     const bool sig = (c.mode == MOE_ROUTE_SIGMOID_GROUP);
-    // all loads of a chunk are issued before its stores (the shared-memory stores could
-    // otherwise alias the global loads and serialise one L2 round trip per element)
-    for (int e0 = 0; e0 < E; e0 += 8 * 32) {
-        float l[8], b[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = e0 + i * 32 + lane;
-            l[i] = e < E ? __ldcg(lrow + e) : 0.f;
-            b[i] = (sig && bias && e < E) ? __ldg(bias + e) : 0.f;
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = e0 + i * 32 + lane;
-            if (e < E) {
-                if (sig) {
-                    const float s = 1.0f / (1.0f + expf(-l[i]));
-                    sv[e] = s;
-                    sel[e] = s + b[i];
-                } else {
-                    sv[e] = l[i];
-                    sel[e] = l[i];
-                }
-            }
-        }
-    }
-    __syncwarp();
     if (sig) {
-        const int per = E / c.G;
-        float gs = -INFINITY;
-        if (lane < c.G) {
-            float b1 = -INFINITY, b2 = -INFINITY;
-            for (int i = 0; i < per; ++i) {
-                const float v = sel[lane * per + i];
-                if (v > b1) { b2 = b1; b1 = v; } else if (v > b2) { b2 = v; }
+        warp_scores_sigmoid_group(c, lrow, bias, sel, sv);
+    } else {
+        // all loads of a chunk are issued before its stores (the shared-memory stores could
+        // otherwise alias the global loads and serialise one L2 round trip per element)
+        for (int e0 = 0; e0 < E; e0 += 8 * 32) {
+            float l[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = e0 + i * 32 + lane;
+                l[i] = e < E ? __ldcg(lrow + e) : 0.f;
             }
-            gs = per >= 2 ? b1 + b2 : b1;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = e0 + i * 32 + lane;
+                if (e < E) sv[e] = sel[e] = l[i];
+            }
         }
-        uint32_t keep = 0u;
-        for (int r = 0; r < c.Gk; ++r) {
-            float v = (lane < c.G && !((keep >> lane) & 1u)) ? gs : -INFINITY;
-            int id = (lane < c.G && !((keep >> lane) & 1u)) ? lane : 0x7fffffff;
-            warp_argmax(v, id);
-            if (id < 32) keep |= 1u << id;
-        }
-        for (int e = lane; e < E; e += 32)
-            if (!((keep >> (e / per)) & 1u)) sel[e] = -INFINITY;
         __syncwarp();
     }
     // k rounds of arg-max over sel (larger first, ties to the lower id); lane r keeps the
@@ -104,6 +125,7 @@ __device__ __forceinline__ void warp_topk_n(const RouteCfgDev& c, const float* l
         kv[i] = key;
     }
     int my_id = 0x7fffffff;
+#pragma unroll 1                                      // rounds are serial: no gain from copies
     for (int r = 0; r < k; ++r) {
         uint32_t best = 0u;
         int bid = 0x7fffffff;
@@ -135,6 +157,7 @@ __device__ __forceinline__ void warp_topk_n(const RouteCfgDev& c, const float* l
         }
     }
     int rank = 0;
+#pragma unroll 1
     for (int j = 0; j < k; ++j) {
         const int oid = __shfl_sync(0xffffffffu, my_id, j);
         rank += (oid < my_id) ? 1 : 0;
@@ -146,12 +169,22 @@ __device__ __forceinline__ void warp_topk_n(const RouteCfgDev& c, const float* l
     __syncwarp();
 }
 
-// Same, with the key registers sized for E (E <= 1024).
+// Out-of-line instances for the wider key arrays (E > 128).
+static __device__ __noinline__ void warp_topk_256(const RouteCfgDev& c, const float* lrow, const float* bias, float* sel,
+                                           float* sv, int32_t* ids, float* w) {
+    warp_topk_n<8>(c, lrow, bias, sel, sv, ids, w);
+}
+static __device__ __noinline__ void warp_topk_1024(const RouteCfgDev& c, const float* lrow, const float* bias, float* sel,
+                                            float* sv, int32_t* ids, float* w) {
+    warp_topk_n<32>(c, lrow, bias, sel, sv, ids, w);
+}
+
+// Same, with the key registers sized for E (E <= 1024); E <= 128 inline.
 __device__ __forceinline__ void warp_topk(const RouteCfgDev& c, const float* lrow, const float* bias, float* sel,
                                           float* sv, int32_t* ids, float* w) {
     if (c.E <= 128) warp_topk_n<4>(c, lrow, bias, sel, sv, ids, w);
-    else if (c.E <= 256) warp_topk_n<8>(c, lrow, bias, sel, sv, ids, w);
-    else warp_topk_n<32>(c, lrow, bias, sel, sv, ids, w);
+    else if (c.E <= 256) warp_topk_256(c, lrow, bias, sel, sv, ids, w);
+    else warp_topk_1024(c, lrow, bias, sel, sv, ids, w);
 }
 
 }  // namespace moe

@@ -219,6 +219,16 @@ def test_tc_tiny_q8_0():
         _check_sampled(tl, T, np.arange(T), TOL_TC, tc_min_tokens=1)
 
 
+def test_default_threshold_T64_T65():
+    # the default crossover: T <= 64 takes the GEMV kernels, T = 65 the tensor cores (one
+    # token block per expert, every block ragged); both against the oracle on every token
+    from helpers import TOL_TC
+    for T, path, tol in ((64, "gemv", TOL_GEMV), (65, "tensor", TOL_TC)):
+        tl = make_layer(synth.DECODE, 34, T, exact_all=True)
+        layer, _, _ = _check_sampled(tl, T, np.arange(T), tol)
+        assert layer.path(T) == path
+
+
 def test_tc_decode_shape_ragged():
     from helpers import TOL_TC
     T = 300                                 # 2400 pairs: many token blocks, a ragged tail per expert

@@ -6,19 +6,20 @@ layers.  Layer l's router is drawn so that the oracle's own chain keeps a 1e-3
 routing margin (a layer whose margin falls below it on the oracle chain gets its
 router redrawn from a new seed before the chain continues).
 
-Parity is checked per layer with teacher forcing: the oracle's layer l runs on
-the GPU's own bf16 input to layer l (the GPU's RMSNorm output of the GPU's
-residual stream -- an input of the check, never a compared result):
-  - routing ids bit-exact for every token whose top-k margin, measured by the
-    oracle in fp64 on that input, is at least 1e-3; a token under the margin may
-    pick another expert set only if that set is a valid top-k within the margin;
-  - the layer's MoE output within rel-L2 1e-4 of the oracle's on that input
-    (tokens with identical ids).
-The residual add, the pre-norm inside the layer call and the CUDA graph are
-then checked bit for bit against their parts.  The distance of the whole GPU
-chain from the oracle's own chain is reported beside the oracle's distance from
-itself under flipped bf16 roundings; it is not a pass/fail bar, because past the
-first layers it measures how depth amplifies rounding steps, not the GPU.
+Parity is checked per layer with teacher forcing in the oracle's direction: the
+GPU's layer l runs on the oracle chain's own input to layer l (the oracle's bf16
+RMSNorm output, exact bf16 values), so no GPU value ever enters the oracle:
+  - routing ids bit-exact at every layer and token (the router draw keeps the
+    1e-3 margin on exactly these inputs);
+  - the layer's MoE output within rel-L2 1e-4 of the oracle's.
+The GPU's own chain (pre-norm inside the call, residual add, 48 calls in one
+CUDA graph) is then checked bit for bit against its parts: each residual block
+equals x + layer(bf16(RMSNorm(x))) computed by the separate kernels, the pre-norm
+call routes like the plain layer, and the graph replays the eager chain.  The
+distance of the whole GPU chain from the oracle's own chain is reported beside
+the oracle's distance from itself under flipped bf16 roundings; it is not a
+pass/fail bar, because past the first layers it measures how depth amplifies
+rounding steps, not the GPU.
 """
 from __future__ import annotations
 
@@ -118,14 +119,15 @@ def _build_stack(T: int, seed: int = 5):
                 break
         else:
             raise RuntimeError("no router draw met the margin")
-        x = x + oracle.moe_layer(_spec(W, Wr, ids), u, logits=lg, n_threads=nt)["out"]
-        layers.append(dict(Wr=Wr, ids=ids, x_after=x))
+        y = oracle.moe_layer(_spec(W, Wr, ids), u, logits=lg, n_threads=nt)["out"]
+        x = x + y
+        layers.append(dict(Wr=Wr, ids=ids, u=u, y=y, x_after=x))
     return x0, layers
 
 
 def _gpu_layers(layers):
     """Per layer: the production residual block (pre-norm inside the call, out == x) and the
-    plain layer on a bf16 input (no residual add) that the teacher-forced check reads."""
+    plain layer on a bf16 input (no residual add)."""
     from quantized_routed_expert_sigmoid_gb300 import MoeLayer
     fused, plain = [], []
     for l, L in enumerate(layers):
@@ -137,26 +139,34 @@ def _gpu_layers(layers):
     return fused, plain
 
 
-def _valid_topk(lg_row, chosen, k, tol):
-    """chosen is a top-k of lg_row up to tol: no unchosen logit exceeds a chosen one by more."""
-    mask = np.zeros(lg_row.shape[0], bool)
-    mask[np.asarray(chosen)] = True
-    return len(set(int(c) for c in chosen)) == k and lg_row[mask].min() >= lg_row[~mask].max() - tol
-
-
 @pytest.mark.parametrize("T", STACK_T)
 def test_stack_48_layers(T):
-    """Teacher-forced per-layer parity over 48 layers, then the chaining checked bit for bit:
-    the residual block equals x + layer(norm(x)) exactly, the pre-norm call routes like the
-    plain layer, and the captured graph of 48 calls replays the eager chain's bits.  The
-    distance of the whole chain from the oracle's own chain is printed, not bounded."""
+    """Per-layer parity on the oracle chain's inputs over 48 layers, then the GPU chain checked
+    bit for bit: the residual block equals x + layer(norm(x)) exactly, the pre-norm call routes
+    like the plain layer, and the captured graph of 48 calls replays the eager chain's bits.
+    The distance of the whole chain from the oracle's own chain is printed, not bounded."""
     import quantized_routed_expert_sigmoid_gb300 as moe
     x0, layers = _build_stack(T)
     fused, plain = _gpu_layers(layers)
-    H, k = SHAPE.H, SHAPE.k
+    H = SHAPE.H
+
+    # ---- teacher forcing: the GPU's layer l on the oracle's input to layer l
+    worst = 0.0
+    for l in range(N_LAYERS):
+        ul = torch.from_numpy(layers[l]["u"]).to(torch.bfloat16).cuda()     # exact: bf16 values
+        m = plain[l](ul)
+        torch.cuda.synchronize()
+        ids, _, _ = plain[l].debug_views(T)
+        assert np.array_equal(ids.numpy(), layers[l]["ids"]), f"layer {l}: routing ids differ"
+        assert plain[l].device_status(T) == 0
+        err = rel_l2(m.cpu().double().numpy(), layers[l]["y"])
+        worst = max(worst, err)
+        assert err <= TOL_GEMV, f"layer {l}: rel-L2 {err:.3e} > {TOL_GEMV}"
+
+    # ---- the GPU's own chain: each residual block against its parts
     x = x0.cuda().contiguous().clone()
     u = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
-    inputs, moe_out, gpu_ids, after = [], [], [], []
+    gpu_ids, after = [], []
     for l in range(N_LAYERS):
         W = _weights(l)
         x_in = x.clone()
@@ -169,29 +179,8 @@ def test_stack_48_layers(T):
         ids_f, _, _ = fused[l].debug_views(T)
         assert torch.equal(ids_p, ids_f), f"layer {l}: pre-norm call routes differently"
         assert fused[l].device_status(T) == 0 and plain[l].device_status(T) == 0
-        inputs.append(u.float().cpu().double().numpy())
-        moe_out.append(m.cpu().double().numpy())
         gpu_ids.append(ids_p.numpy())
         after.append(x.cpu().double().numpy())
-
-    # ---- teacher forcing: the oracle's layer l on the GPU's input to layer l
-    nt = oracle.max_threads()
-    worst, undecided, rerouted = 0.0, 0, 0
-    for l in range(N_LAYERS):
-        ul = inputs[l]
-        lg = oracle.router_logits(ul, layers[l]["Wr"].numpy())
-        ref_ids, _, gaps = oracle.route(oracle_mode(SHAPE), lg, k)
-        decided = gaps[:, 0] >= MIN_GAP
-        same = np.all(gpu_ids[l] == ref_ids, axis=1)
-        assert np.all(same[decided]), f"layer {l}: routing ids differ on decided tokens {np.where(~same & decided)[0]}"
-        for t in np.where(~same)[0]:
-            assert _valid_topk(lg[t], gpu_ids[l][t], k, MIN_GAP), f"layer {l} token {t}: not a top-{k}"
-        undecided += int((~decided).sum())
-        rerouted += int((~same).sum())
-        ref = oracle.moe_layer(_spec(_weights(l), layers[l]["Wr"], ref_ids), ul, logits=lg, n_threads=nt)["out"]
-        err = rel_l2(moe_out[l][same], ref[same])
-        worst = max(worst, err)
-        assert err <= TOL_GEMV, f"layer {l}: teacher-forced rel-L2 {err:.3e} > {TOL_GEMV}"
 
     # ---- the whole stack as one captured graph: the eager chain's bits
     eager_final = x.clone()
@@ -218,13 +207,13 @@ def test_stack_48_layers(T):
         assert np.array_equal(ids_f.numpy(), gpu_ids[l]), f"replay, layer {l}: routing ids differ"
 
     # ---- end-to-end distance from the oracle's own chain: reported, not a pass/fail bar.  The
-    # checks above make the GPU chain, layer by layer, the oracle's layer evaluated on the GPU's
-    # own input plus a local error below 1e-4 (measured ~1e-6), composed bit for bit; what
-    # separates the two chains after many layers is the oracle's own response to a slightly
-    # different input (each bf16 rounding of a layer input is a step, and depth amplifies the
-    # steps), which the oracle's rerun with midpoint-flipped roundings shows beside it.
+    # checks above give every GPU layer within 1e-4 of the oracle's on the same input and the
+    # GPU chain composed of those layers bit for bit; what separates the two chains after many
+    # layers is each chain's response to slightly different inputs (each bf16 rounding of a
+    # layer input is a step, and depth amplifies the steps), which the oracle's rerun with
+    # midpoint-flipped roundings shows beside it.
     flip, _ = _oracle_chain(layers, x0.double().numpy(), rounding=_bf16_midpoint_flips)
     drift = [(rel_l2(after[l], layers[l]["x_after"]), rel_l2(flip[l], layers[l]["x_after"])) for l in range(N_LAYERS)]
-    print(f"T={T}: teacher-forced worst rel-L2 {worst:.2e}; tokens under the margin {undecided}, "
-          f"of them rerouted {rerouted}; distance from the oracle chain (gpu, oracle flip rerun) every 8 layers:",
+    print(f"T={T}: per-layer worst rel-L2 {worst:.2e}; distance from the oracle chain (gpu, oracle flip rerun) "
+          f"every 8 layers:",
           [(f"{a:.1e}", f"{b:.1e}") for a, b in drift[::8]], f"final {drift[-1][0]:.2e}")
