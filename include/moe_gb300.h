@@ -62,14 +62,25 @@ typedef enum {
 
 /* MOE_Q8_0_R: Q8_0 weights after moe_weights_prepare -- per row of K weights, the int8
  * quants of its K/32 blocks (32 bytes each, in order), then their fp16 scales, padded to
- * a multiple of 16 bytes: 32*(K/32) + roundup16(2*(K/32)) bytes a row. */
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_Q8_0 = 2, MOE_Q4_K = 3, MOE_Q8_0_R = 4 } moe_dtype;
+ * a multiple of 16 bytes: 32*(K/32) + roundup16(2*(K/32)) bytes a row.
+ * MOE_Q5_K: 176 bytes per 256 weights -- Q4_K's 16-byte header (fp16 d, fp16 dmin, 12 bytes
+ * of 6-bit scales and mins), 32 bytes whose byte i holds in bit j the 16s digit of element i
+ * of sub-block j, then Q4_K's 128 nibble bytes; q in [0, 31], w = d*sc_j*q - dmin*m_j.
+ * MOE_Q6_K: 210 bytes per 256 weights -- 128 bytes of low nibbles, 64 bytes of 2-bit high
+ * parts, 16 int8 scales (one per 16 weights), fp16 d; element 128h + 32r + l (r < 4) takes
+ * the low (r < 2) or high (r >= 2) nibble of byte 64h + 32(r % 2) + l and bits 2r, 2r + 1 of
+ * byte 128 + 32h + l, u = nibble + 16 * those bits, w = d * sc[element / 16] * (u - 32).
+ * Both are the public GGUF K-quant layouts; the pages list them among the card-expert types
+ * ("bloomery README 0.3.1", Status table, "Quant types" row).  They run on the GEMV kernels
+ * at every T (moe_layer_path reports MOE_PATH_GEMV). */
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_Q8_0 = 2, MOE_Q4_K = 3, MOE_Q8_0_R = 4, MOE_Q5_K = 5,
+               MOE_Q6_K = 6 } moe_dtype;
 
 typedef enum { MOE_ROUTE_SOFTMAX = 0, MOE_ROUTE_SIGMOID_GROUP = 1 } moe_route_mode;
 
 /* One quantized weight tensor, possibly a stack of experts. */
 typedef struct {
-    moe_dtype qtype;             /* MOE_Q8_0, MOE_Q4_K or MOE_Q8_0_R */
+    moe_dtype qtype;             /* MOE_Q8_0, MOE_Q4_K, MOE_Q8_0_R, MOE_Q5_K or MOE_Q6_K */
     const void* data;            /* (device) 16-byte aligned */
     int64_t rows, cols;          /* per expert; cols = input dimension */
     int64_t expert_stride_bytes; /* bytes from expert e to e+1 (multiple of 16) */
@@ -99,7 +110,8 @@ typedef struct {
  *     rows, cols = K a multiple of 32, expert_stride_bytes >= rows * 34 * K/32 when
  *     n_experts > 1).  On success it is rewritten to describe the repacked tensor:
  *     qtype MOE_Q8_0_R, data = dst, expert_stride_bytes = rows * row bytes.  A MOE_Q4_K
- *     tensor is used as stored: in_out is left unchanged and nothing is written.
+ *     tensor (and a MOE_Q5_K or MOE_Q6_K one) is used as stored: in_out is left unchanged and
+ *     nothing is written.
  *   dst (device, 16-byte aligned): at least moe_weights_prepare_size() bytes, owned by
  *     the caller; it must not overlap the source.
  * One kernel on `stream`; the source may be freed once the stream has passed it.

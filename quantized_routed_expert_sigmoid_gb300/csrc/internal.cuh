@@ -26,6 +26,8 @@ __host__ __device__ inline int64_t q80r_row_bytes(int64_t K) {
 // Bytes of one row of K weights stored as qtype (Q8_0, Q8_0_R or Q4_K).
 __host__ __device__ inline int64_t q_row_bytes(int qtype, int64_t K) {
     if (qtype == MOE_Q4_K) return K / kQ4KWeights * kQ4KBytes;
+    if (qtype == MOE_Q5_K) return K / 256 * 176;
+    if (qtype == MOE_Q6_K) return K / 256 * 210;
     if (qtype == MOE_Q8_0_R) return q80r_row_bytes(K);
     return K / kQ80Weights * kQ80Bytes;
 }

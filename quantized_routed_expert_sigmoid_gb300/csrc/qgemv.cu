@@ -18,6 +18,7 @@
 
 #include "internal.cuh"
 #include "qdot.cuh"
+#include "qdot_k56.cuh"
 
 namespace moe {
 namespace {
@@ -111,8 +112,8 @@ __global__ void __launch_bounds__(kThreads, 2) qgemv_kernel(GemvArgs a, int iter
     __shared__ int s_rows[NT];
     for (int pb = 0; pb < n_tot; pb += NT) {
         const int nt = min(NT, n_tot - pb);
-        if (QT == MOE_Q4_K) {
-            // ---- stage the activation vectors as 16-bit integer planes (qdot.cuh)
+        if constexpr (QT == MOE_Q4_K || QT == MOE_Q5_K || QT == MOE_Q6_K) {
+            // ---- stage the activation vectors as integer planes (qdot.cuh)
             uint4* X = reinterpret_cast<uint4*>(xs);
             float4* XS = reinterpret_cast<float4*>(X + (size_t)NT * 16 * qd4_groups(a.K));
             if (threadIdx.x < nt) {
@@ -141,12 +142,12 @@ __global__ void __launch_bounds__(kThreads, 2) qgemv_kernel(GemvArgs a, int iter
                 for (int r = 0; r < 4; ++r)
 #pragma unroll
                     for (int t = 0; t < NT; ++t) acc[r][t] = 0.f;
-                qd4_rows4<NT, false, NPL>(rowp, nblk, X, XS, nt, lane, acc);
+                if constexpr (QT == MOE_Q4_K) qd4_rows4<NT, false, NPL>(rowp, nblk, X, XS, nt, lane, acc);
+                else qd56_rows4<QT, NT, NPL>(rowp, nblk, X, XS, nt, lane, acc);
                 qd_store_units<NT, GATEUP>(acc, lane, nt, a.out + (int64_t)(start + pb) * a.rows, a.rows, unit);
             }
             __syncthreads();
-            continue;
-        }
+        } else {
         // ---- stage the activation vectors of pairs start+pb .. +nt in walk order
         for (int t = 0; t < nt; ++t) {
             const int i = start + pb + t;
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 2) qgemv_kernel(GemvArgs a, int iter
             qd_stage<QT>(src, a.vin_bf16, false, a.K, iters, xs + (size_t)t * slots, threadIdx.x, kThreads);
         }
         __syncthreads();
-        if (QT == MOE_Q4_K) {
+        if constexpr (QT == MOE_Q4_K) {
             for (int t = 0; t < nt; ++t)
                 qd_stage_sums(xs + (size_t)t * slots, xsum + (size_t)t * iters * 32, iters, threadIdx.x, kThreads);
             __syncthreads();
@@ -185,12 +186,13 @@ __global__ void __launch_bounds__(kThreads, 2) qgemv_kernel(GemvArgs a, int iter
             qd_store_units<NT, GATEUP>(acc, lane, nt, a.out + (int64_t)(start + pb) * a.rows, a.rows, unit);
         }
         __syncthreads();
+        }
     }
 }
 
 template <int QT, bool GU, int NT, int NPL>
 cudaError_t launch_one(const GemvArgs& a, int iters, int grid_y, cudaStream_t s) {
-    const size_t smem = QT == MOE_Q4_K ? (size_t)NT * qd4_vec_bytes(a.K)
+    const size_t smem = QT != MOE_Q8_0 ? (size_t)NT * qd4_vec_bytes(a.K)
                                        : (size_t)NT * iters * 256 * sizeof(float4) + (size_t)NT * iters * 32 * sizeof(float2);
     if (smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(qgemv_kernel<QT, GU, NT, NPL>,
@@ -211,11 +213,15 @@ cudaError_t launch_one(const GemvArgs& a, int iters, int grid_y, cudaStream_t s)
 
 template <int QT, bool GU, int NPL>
 cudaError_t launch_nt(const GemvArgs& a, int nt, int iters, int grid_y, cudaStream_t s) {
-    switch (nt) {
-        case 1: return launch_one<QT, GU, 1, NPL>(a, iters, grid_y, s);
-        case 2: return launch_one<QT, GU, 2, NPL>(a, iters, grid_y, s);
-        case 4: return launch_one<QT, GU, 4, NPL>(a, iters, grid_y, s);
-        default: return launch_one<QT, GU, 8, NPL>(a, iters, grid_y, s);
+    if constexpr (QT == MOE_Q5_K || QT == MOE_Q6_K) {   // their codes take registers: two vectors a pass
+        return nt == 1 ? launch_one<QT, GU, 1, NPL>(a, iters, grid_y, s) : launch_one<QT, GU, 2, NPL>(a, iters, grid_y, s);
+    } else {
+        switch (nt) {
+            case 1: return launch_one<QT, GU, 1, NPL>(a, iters, grid_y, s);
+            case 2: return launch_one<QT, GU, 2, NPL>(a, iters, grid_y, s);
+            case 4: return launch_one<QT, GU, 4, NPL>(a, iters, grid_y, s);
+            default: return launch_one<QT, GU, 8, NPL>(a, iters, grid_y, s);
+        }
     }
 }
 
@@ -223,19 +229,22 @@ cudaError_t launch_nt(const GemvArgs& a, int nt, int iters, int grid_y, cudaStre
 
 cudaError_t launch_qgemv(const GemvArgs& a, cudaStream_t s) {
     if (a.n_pairs <= 0) return cudaSuccess;
-    const int iters = a.qtype == MOE_Q4_K ? walk_iters<MOE_Q4_K>(a.K) : walk_iters<MOE_Q8_0>(a.K);
+    const int iters = a.qtype == MOE_Q8_0 ? walk_iters<MOE_Q8_0>(a.K) : walk_iters<MOE_Q4_K>(a.K);
     // Tokens per pass: at most the pairs one expert can hold (distinct ids per
     // token: <= tokens), at most 8, and a staged tile of at most ~64 KB.
     const int per_expert_max = a.sorted_pairs ? (a.n_pairs / a.k) : a.n_pairs;
-    const size_t per_vec = a.qtype == MOE_Q4_K ? qd4_vec_bytes(a.K) : (size_t)iters * 4096;
+    const size_t per_vec = a.qtype != MOE_Q8_0 ? qd4_vec_bytes(a.K) : (size_t)iters * 4096;
     int nt = 8;
     while (nt > 1 && ((size_t)nt * per_vec > 64 * 1024 || nt / 2 >= per_expert_max)) nt /= 2;
     const int grid_y = a.offsets ? (a.n_pairs < a.E ? a.n_pairs : a.E) : 1;
-    if (a.qtype == MOE_Q4_K) {
-        if (!a.gateup) return launch_nt<MOE_Q4_K, false, 3>(a, nt, iters, grid_y, s);   // h is fp32
-        return a.vin_bf16 ? launch_nt<MOE_Q4_K, true, 2>(a, nt, iters, grid_y, s)
-                          : launch_nt<MOE_Q4_K, true, 3>(a, nt, iters, grid_y, s);
-    }
+    auto planes = [&](auto qt) -> cudaError_t {
+        constexpr int Q = decltype(qt)::value;
+        if (!a.gateup) return launch_nt<Q, false, 3>(a, nt, iters, grid_y, s);   // h is fp32
+        return a.vin_bf16 ? launch_nt<Q, true, 2>(a, nt, iters, grid_y, s) : launch_nt<Q, true, 3>(a, nt, iters, grid_y, s);
+    };
+    if (a.qtype == MOE_Q4_K) return planes(std::integral_constant<int, MOE_Q4_K>{});
+    if (a.qtype == MOE_Q5_K) return planes(std::integral_constant<int, MOE_Q5_K>{});
+    if (a.qtype == MOE_Q6_K) return planes(std::integral_constant<int, MOE_Q6_K>{});
     return a.gateup ? launch_nt<MOE_Q8_0, true, 3>(a, nt, iters, grid_y, s)
                     : launch_nt<MOE_Q8_0, false, 3>(a, nt, iters, grid_y, s);
 }

@@ -11,14 +11,16 @@ import torch
 
 from . import _native as N
 
-_QT = {"q8_0": N.MOE_Q8_0, "q4_k": N.MOE_Q4_K, "q8_0_r": N.MOE_Q8_0_R}
+_QT = {"q8_0": N.MOE_Q8_0, "q4_k": N.MOE_Q4_K, "q8_0_r": N.MOE_Q8_0_R, "q5_k": N.MOE_Q5_K, "q6_k": N.MOE_Q6_K}
 
 
 def row_bytes(qtype: int, cols: int) -> int:
     if qtype == N.MOE_Q8_0_R:                     # quants, then fp16 scales padded to 16 bytes
         nb = cols // 32
         return 32 * nb + (2 * nb + 15) // 16 * 16
-    return cols // 32 * 34 if qtype == N.MOE_Q8_0 else cols // 256 * 144
+    if qtype == N.MOE_Q8_0:
+        return cols // 32 * 34
+    return cols // 256 * {N.MOE_Q4_K: 144, N.MOE_Q5_K: 176, N.MOE_Q6_K: 210}[qtype]
 
 
 def prepare_q8_0(t, rows: int, cols: int, n_experts: int = 1):

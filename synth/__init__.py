@@ -165,7 +165,7 @@ def pack_q5_k(d: torch.Tensor, dmin: torch.Tensor, sc: torch.Tensor, m: torch.Te
     q = q.to(torch.int32)
     base = pack_q4_k(d, dmin, sc, m, q & 15)
     bits = ((q >> 4) & 1).reshape(*q.shape[:-1], 8, 32)             # [..., j, i]
-    shifts = torch.arange(8, dtype=torch.int32).reshape(8, 1)
+    shifts = torch.arange(8, dtype=torch.int32, device=q.device).reshape(8, 1)
     qh = (bits << shifts).sum(dim=-2).to(torch.uint8)                # [..., 32]
     return torch.cat([base[..., :16], qh, base[..., 16:]], dim=-1)
 
@@ -218,7 +218,7 @@ def pack_q6_k(d: torch.Tensor, sc: torch.Tensor, q: torch.Tensor) -> torch.Tenso
     u = (q.to(torch.int32) + 32).reshape(*q.shape[:-1], 2, 4, 32)   # [..., h, r, l]
     lo = u & 15
     ql = torch.cat([lo[..., 0, :] | (lo[..., 2, :] << 4), lo[..., 1, :] | (lo[..., 3, :] << 4)], dim=-1)
-    shifts = (2 * torch.arange(4, dtype=torch.int32)).reshape(4, 1)
+    shifts = (2 * torch.arange(4, dtype=torch.int32, device=q.device)).reshape(4, 1)
     qh = (((u >> 4) & 3) << shifts).sum(dim=-2)                      # [..., h, 32]
     lead = q.shape[:-1]
     scb = (sc.to(torch.int32) & 0xFF).to(torch.uint8)
@@ -244,12 +244,12 @@ def pack_q3_k(d: torch.Tensor, sc: torch.Tensor, q: torch.Tensor) -> torch.Tenso
     lead = q.shape[:-1]
     v = (q.to(torch.int32) + 4).reshape(*lead, 2, 4, 32)             # [..., h, r, l]
     hbit = ((v >> 2) & 1).reshape(*lead, 8, 32)                      # [..., 4h + r, l]
-    hm = (hbit << torch.arange(8, dtype=torch.int32).reshape(8, 1)).sum(dim=-2)
-    qs = ((v & 3) << (2 * torch.arange(4, dtype=torch.int32)).reshape(4, 1)).sum(dim=-2)   # [..., h, l]
+    hm = (hbit << torch.arange(8, dtype=torch.int32, device=q.device).reshape(8, 1)).sum(dim=-2)
+    qs = ((v & 3) << (2 * torch.arange(4, dtype=torch.int32, device=q.device)).reshape(4, 1)).sum(dim=-2)   # [..., h, l]
     s = sc.to(torch.int32) + 32                                      # [..., 16]
     nib = (s[..., :8] & 15) | ((s[..., 8:] & 15) << 4)               # [..., 8]
     top = ((s >> 4) & 3).reshape(*lead, 4, 4)                        # [..., j // 4, j % 4]
-    hi = (top << (2 * torch.arange(4, dtype=torch.int32)).reshape(4, 1)).sum(dim=-2)      # [..., 4]
+    hi = (top << (2 * torch.arange(4, dtype=torch.int32, device=q.device)).reshape(4, 1)).sum(dim=-2)      # [..., 4]
     return torch.cat([hm.to(torch.uint8), qs.reshape(*lead, 64).to(torch.uint8), nib.to(torch.uint8),
                       hi.to(torch.uint8), _fp16_bits(d.float())], dim=-1)
 
@@ -282,7 +282,7 @@ def encode_mxfp4(w: torch.Tensor) -> torch.Tensor:
     E = torch.where(amax > 0, torch.floor(torch.log2(torch.where(amax > 0, amax, torch.ones_like(amax)))) - 2,
                     torch.full_like(amax, -127.0)).clamp(-127, 127)
     v = b / torch.exp2(E).unsqueeze(-1)
-    mags = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    mags = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], device=b.device)
     idx = (v.abs().clamp(max=6.0).unsqueeze(-1) - mags).abs().argmin(dim=-1)
     codes = torch.where((v < 0) & (idx > 0), idx + 8, idx)
     blocks = pack_mxfp4((E + 127).to(torch.int32), codes)
