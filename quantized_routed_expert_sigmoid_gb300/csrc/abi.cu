@@ -32,8 +32,8 @@ moe_status cuda_fail(cudaError_t err, const char* what) {
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 int64_t row_bytes(moe_dtype q, int64_t cols) {
-    if (q == MOE_Q4_K || q == MOE_Q8_0 || q == MOE_Q8_0_R || q == MOE_Q5_K || q == MOE_Q6_K)
-        return q_row_bytes(q, cols);
+    if (q == MOE_Q3_K) return cols / 256 * 110;
+    if (q == MOE_Q4_K || q == MOE_Q8_0 || q == MOE_Q8_0_R || q == MOE_Q5_K || q == MOE_Q6_K) return q_row_bytes(q, cols);
     return -1;
 }
 // The kernels' view of a weight type: Q8_0 in either layout is MOE_Q8_0, the layout a flag.
@@ -42,8 +42,8 @@ int kernel_qtype(moe_dtype q) { return q == MOE_Q8_0_R ? (int)MOE_Q8_0 : (int)q;
 moe_status check_qmat(const moe_qmat* m, const char* name, int64_t rows, int64_t cols, int E) {
     if (!m) return fail(MOE_ERR_INVALID_ARG, "%s: NULL matrix", name);
     if (m->qtype != MOE_Q4_K && m->qtype != MOE_Q8_0 && m->qtype != MOE_Q8_0_R && m->qtype != MOE_Q5_K &&
-        m->qtype != MOE_Q6_K)
-        return fail(MOE_ERR_UNSUPPORTED, "%s: qtype %d (supported: Q8_0, Q8_0_R, Q4_K, Q5_K, Q6_K)", name,
+        m->qtype != MOE_Q6_K && m->qtype != MOE_Q3_K)
+        return fail(MOE_ERR_UNSUPPORTED, "%s: qtype %d (supported: Q8_0, Q8_0_R, Q4_K, Q5_K, Q6_K, Q3_K)", name,
                     (int)m->qtype);
     if (!m->data) return fail(MOE_ERR_INVALID_ARG, "%s: NULL data", name);
     if (!aligned(m->data, 16)) return fail(MOE_ERR_INVALID_ARG, "%s: data not 16-byte aligned", name);
@@ -298,7 +298,10 @@ const char* moe_version(void) { return "moe_gb300 0.1 (sm_103a)"; }
 moe_status moe_weights_prepare_size(const moe_qmat* in, int n_experts, size_t* bytes) {
     if (!in || !bytes) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
     if (n_experts < 1) return fail(MOE_ERR_INVALID_ARG, "n_experts = %d < 1", n_experts);
-    if (in->qtype == MOE_Q4_K || in->qtype == MOE_Q5_K || in->qtype == MOE_Q6_K) { *bytes = 0; return MOE_OK; }
+    if (in->qtype == MOE_Q4_K || in->qtype == MOE_Q5_K || in->qtype == MOE_Q6_K || in->qtype == MOE_Q3_K) {
+        *bytes = 0;
+        return MOE_OK;
+    }
     if (in->qtype != MOE_Q8_0)
         return fail(MOE_ERR_UNSUPPORTED, "moe_weights_prepare: qtype %d (it repacks Q8_0; Q4_K is used as stored)",
                     (int)in->qtype);
@@ -313,7 +316,9 @@ moe_status moe_weights_prepare(moe_qmat* in_out, int n_experts, void* dst, size_
     size_t need = 0;
     moe_status st = moe_weights_prepare_size(in_out, n_experts, &need);
     if (st) return st;
-    if (in_out->qtype == MOE_Q4_K || in_out->qtype == MOE_Q5_K || in_out->qtype == MOE_Q6_K) return MOE_OK;
+    if (in_out->qtype == MOE_Q4_K || in_out->qtype == MOE_Q5_K || in_out->qtype == MOE_Q6_K ||
+        in_out->qtype == MOE_Q3_K)
+        return MOE_OK;
     if ((st = check_qmat(in_out, "in", in_out->rows, in_out->cols, n_experts))) return st;
     if (!dst || !aligned(dst, 16)) return fail(MOE_ERR_INVALID_ARG, "dst NULL or not 16-byte aligned");
     if (dst_bytes < need) return fail(MOE_ERR_WORKSPACE, "dst %zu bytes, need %zu", dst_bytes, need);

@@ -1,7 +1,8 @@
-// qdot_k56.cuh -- Q5_K and Q6_K rows against integer activation planes (the GEMV kernels).
+// qdot_k56.cuh -- Q5_K, Q6_K and Q3_K rows against integer activation planes (the GEMV kernels).
 //
-// Both types are the next card-expert types the pages list after Q4_K ("bloomery README
-// 0.3.1", Status table, "Quant types" row: card experts in Q4_K-Q6_K).  The activations are
+// These are the next card-expert types the pages list after Q4_K ("bloomery README 0.3.1",
+// Status table, "Quant types" row: card experts in Q4_K-Q6_K; "bloomery README 0.3.11", limits
+// list: the large model's routed experts as Q3_K gate and up with a Q4_K down).  The activations are
 // the staged vectors of qdot.cuh (per 32-value sub-block: NPL byte planes, an fp32 step and the
 // sub-block sum; group g = values 64g .. 64g + 63 = sub-blocks 2c, 2c + 1 of super-block g/4,
 // c = g % 4).  A lane takes one (row, group) item, builds the weights' integer codes as bytes
@@ -21,6 +22,13 @@
 // most 2 bytes before a field and funnel-shifted into place; no read leaves the block's row
 // past its end.  The codes u - 32 enter dp4a as signed bytes; the two 16-weight halves of a
 // sub-block have their own scales, so their integer sums are kept apart.
+//
+// Q3_K (110 bytes per 256 weights): 32 bytes hmask, 64 bytes of 2-bit low parts, 12 bytes of
+// sixteen 6-bit scales stored + 32, fp16 d.  Element 128h + 32r + l takes bits 2r, 2r + 1 of
+// byte 32 + 32h + l and bit 4h + r of byte l; v = low + 4 * bit, q = v - 4 in [-4, 3]; scale j
+// has its low nibble in byte 96 + j (j < 8, low) or 96 + j - 8 (high nibble) and bits 4-5 in bits
+// 2(j / 4), 2(j / 4) + 1 of byte 104 + j % 4; w = d * (s_j - 32) * q.  Read and multiplied as
+// Q6_K (2-byte aligned blocks, signed codes, one scale per 16 weights).
 #pragma once
 
 #include <type_traits>
@@ -31,6 +39,7 @@ namespace moe {
 
 constexpr int kQ5KBytes = 176;
 constexpr int kQ6KBytes = 210;
+constexpr int kQ3KBytes = 110;
 
 template <>
 struct Walk<MOE_Q5_K> {
@@ -41,6 +50,11 @@ template <>
 struct Walk<MOE_Q6_K> {
     static constexpr int kBlockWeights = 256;
     static constexpr int kBlockBytes = kQ6KBytes;
+};
+template <>
+struct Walk<MOE_Q3_K> {
+    static constexpr int kBlockWeights = 256;
+    static constexpr int kBlockBytes = kQ3KBytes;
 };
 
 __device__ __forceinline__ int qd_dp4a_ss(uint32_t a, uint32_t b, int c) {
@@ -155,40 +169,77 @@ __device__ __forceinline__ void q6_words(const uint8_t* p, uint32_t (&out)[N]) {
     for (int j = 0; j < N; ++j) out[j] = __funnelshift_r(a[j], a[j + 1], 8u * mis);
 }
 
-template <int NT, int RPL, int NPL>
-__device__ __forceinline__ void qd6_group(const uint8_t* const (&rowp)[4], int r0, int g, int G, const uint4* X,
-                                          const float4* XS, int nt, float (&acc)[4][NT], const int* vidx) {
-    const int b = g >> 2, c = g & 3, h = c >> 1, rlo = 2 * (c & 1);    // sub-block 2c: r = rlo; 2c+1: rlo+1
-    uint32_t cw[RPL][2][8];                          // (u - 32) as signed bytes, sub-blocks 2c, 2c + 1
-    float sd[RPL][4];                                // d * sc for the four 16-weight quarters of the group
-    bool live[RPL];
-#pragma unroll
-    for (int i = 0; i < RPL; ++i) {
-        const uint8_t* rp = rowp[r0 + i];
-        live[i] = rp != nullptr;
+// Signed codes (as bytes) of sub-blocks 2c and 2c + 1 of group g of one row, and d * scale of the
+// group's four 16-weight quarters.  Q6_K: u - 32 from a nibble and two high bits; Q3_K: v - 4
+// from two low bits and a high bit, with 6-bit scales stored + 32.
+template <int QT>
+__device__ __forceinline__ void q_signed_codes(const uint8_t* rp, int g, uint32_t (&cw)[2][8], float (&sd)[4]) {
+    const int b = g >> 2, c = g & 3, h = c >> 1, rlo = 2 * (c & 1);   // sub-block 2c: r = rlo; 2c+1: rlo+1
+    if constexpr (QT == MOE_Q6_K) {
+        const uint8_t* blk = rp + (int64_t)b * kQ6KBytes;
         uint32_t l0[8], l1[8], hb[8], sw[1];
-        if (live[i]) {
-            const uint8_t* blk = rp + (int64_t)b * kQ6KBytes;
-            q6_words<8>(blk + 64 * h, l0);
-            q6_words<8>(blk + 64 * h + 32, l1);
-            q6_words<8>(blk + 128 + 32 * h, hb);
-            q6_words<1>(blk + 192 + 4 * c, sw);
-            const float d = __half2float(__ushort_as_half((unsigned short)qd_ldg_u16(blk + 208)));
+        q6_words<8>(blk + 64 * h, l0);
+        q6_words<8>(blk + 64 * h + 32, l1);
+        q6_words<8>(blk + 128 + 32 * h, hb);
+        q6_words<1>(blk + 192 + 4 * c, sw);
+        const float d = __half2float(__ushort_as_half((unsigned short)qd_ldg_u16(blk + 208)));
 #pragma unroll
-            for (int j = 0; j < 4; ++j) sd[i][j] = d * (float)(int8_t)((sw[0] >> (8 * j)) & 0xFFu);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) l0[j] = l1[j] = hb[j] = 0u;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) sd[i][j] = 0.f;
-        }
+        for (int j = 0; j < 4; ++j) sd[j] = d * (float)(int8_t)((sw[0] >> (8 * j)) & 0xFFu);
         const int ns = 4 * (c & 1);                  // nibble: low for r < 2, high for r >= 2
 #pragma unroll
         for (int qd = 0; qd < 8; ++qd) {
             const uint32_t u0 = ((l0[qd] >> ns) & 0x0F0F0F0Fu) | (((hb[qd] >> (2 * rlo)) & 0x03030303u) << 4);
             const uint32_t u1 = ((l1[qd] >> ns) & 0x0F0F0F0Fu) | (((hb[qd] >> (2 * rlo + 2)) & 0x03030303u) << 4);
-            cw[i][0][qd] = __vsub4(u0, 0x20202020u);
-            cw[i][1][qd] = __vsub4(u1, 0x20202020u);
+            cw[0][qd] = __vsub4(u0, 0x20202020u);
+            cw[1][qd] = __vsub4(u1, 0x20202020u);
+        }
+    } else {                                         // MOE_Q3_K, 110 bytes
+        const uint8_t* blk = rp + (int64_t)b * kQ3KBytes;
+        uint32_t hm[8], qs[8], sw[3];
+        q6_words<8>(blk, hm);                        // bit 4h + r of byte l: the high bit of element 128h + 32r + l
+        q6_words<8>(blk + 32 + 32 * h, qs);          // bits 2r, 2r + 1 of byte 32h + l: its low bits
+        q6_words<3>(blk + 96, sw);
+        const float d = __half2float(__ushort_as_half((unsigned short)qd_ldg_u16(blk + 108)));
+        auto S = [&](int i) -> int {                  // scale byte i (registers, no indexed array)
+            const uint32_t w = i < 4 ? sw[0] : i < 8 ? sw[1] : sw[2];
+            return (int)((w >> (8 * (i & 3))) & 0xFFu);
+        };
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int j = 4 * c + jj;
+            const int lo4 = j < 8 ? (S(j) & 15) : (S(j - 8) >> 4);
+            const int hi2 = (S(8 + (j & 3)) >> (2 * (j >> 2))) & 3;
+            sd[jj] = d * (float)((lo4 | (hi2 << 4)) - 32);
+        }
+#pragma unroll
+        for (int qd = 0; qd < 8; ++qd) {
+            const uint32_t v0 = ((qs[qd] >> (2 * rlo)) & 0x03030303u) | (((hm[qd] >> (4 * h + rlo)) & 0x01010101u) << 2);
+            const uint32_t v1 =
+                ((qs[qd] >> (2 * rlo + 2)) & 0x03030303u) | (((hm[qd] >> (4 * h + rlo + 1)) & 0x01010101u) << 2);
+            cw[0][qd] = __vsub4(v0, 0x04040404u);
+            cw[1][qd] = __vsub4(v1, 0x04040404u);
+        }
+    }
+}
+
+// Rows of signed codes with one scale per 16 weights (Q6_K, Q3_K) over group g.
+template <int QT, int NT, int RPL, int NPL>
+__device__ __forceinline__ void qd_signed_group(const uint8_t* const (&rowp)[4], int r0, int g, int G, const uint4* X,
+                                                const float4* XS, int nt, float (&acc)[4][NT], const int* vidx) {
+    uint32_t cw[RPL][2][8];                          // signed code bytes, sub-blocks 2c, 2c + 1
+    float sd[RPL][4];                                // d * scale of the group's four 16-weight quarters
+    bool live[RPL];
+#pragma unroll
+    for (int i = 0; i < RPL; ++i) {
+        const uint8_t* rp = rowp[r0 + i];
+        live[i] = rp != nullptr;
+        if (live[i]) {
+            q_signed_codes<QT>(rp, g, cw[i], sd[i]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) cw[i][0][j] = cw[i][1][j] = 0u;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sd[i][j] = 0.f;
         }
     }
 #pragma unroll
@@ -237,7 +288,7 @@ __device__ __forceinline__ void qd6_group(const uint8_t* const (&rowp)[4], int r
 }
 
 // acc[r][t] += row r . vector vidx[t] (t < nt) for 4 rows of nblk super-blocks of type QT
-// (MOE_Q5_K or MOE_Q6_K), lanes split into row subsets as in qd4_rows4.
+// (MOE_Q5_K, MOE_Q6_K or MOE_Q3_K), lanes split into row subsets as in qd4_rows4.
 template <int QT, int NT, int NPL>
 __device__ __forceinline__ void qd56_rows4(const uint8_t* const (&rowp)[4], int nblk, const uint4* X,
                                            const float4* XS, int nt, int lane, float (&acc)[4][NT]) {
@@ -245,7 +296,7 @@ __device__ __forceinline__ void qd56_rows4(const uint8_t* const (&rowp)[4], int 
     auto grp = [&](auto rpl, int r0, int g) {
         constexpr int RPL = decltype(rpl)::value;
         if constexpr (QT == MOE_Q5_K) qd5_group<NT, RPL, NPL>(rowp, r0, g, G, X, XS, nt, acc, nullptr);
-        else qd6_group<NT, RPL, NPL>(rowp, r0, g, G, X, XS, nt, acc, nullptr);
+        else qd_signed_group<QT, NT, RPL, NPL>(rowp, r0, g, G, X, XS, nt, acc, nullptr);
     };
     if (G >= 24) {
         for (int g = lane; g < G; g += 32) grp(std::integral_constant<int, 4>{}, 0, g);

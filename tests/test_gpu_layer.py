@@ -58,24 +58,53 @@ def test_decode_q4_k_fp32_activations(T):
     assert layer.path(T) == "gemv"
 
 
-@pytest.mark.parametrize("qt", [synth.Q5_K, synth.Q6_K])
+@pytest.mark.parametrize("qt", [synth.Q5_K, synth.Q6_K, synth.Q3_K])
 @pytest.mark.parametrize("T", [1, 3, 9, 70])
 def test_decode_shape_q5_k_q6_k(qt, T):
     # the next K-quants on the GEMV kernels (every T): gate/up rows of 8 super-blocks, down rows
-    # of 3, so Q6_K's 210-byte blocks start 2 bytes off a 4-byte boundary in every other row
+    # of 3, so Q6_K's 210-byte and Q3_K's 110-byte blocks start 2 bytes off a 4-byte boundary in
+    # every other row
     shape = dataclasses.replace(synth.DECODE, qtype=qt)
     tl = make_layer(shape, 24, T)
     layer, _, _ = _check_layer(tl, T)
     assert layer.path(T) == "gemv"
 
 
-@pytest.mark.parametrize("qt", [synth.Q5_K, synth.Q6_K])
+@pytest.mark.parametrize("qt", [synth.Q5_K, synth.Q6_K, synth.Q3_K])
 def test_small_q5_k_q6_k_fp32(qt):
     # one super-block per row (the short-row lane split) and fp32 activations (three planes)
     shape = synth.LayerShape(H=256, E=8, k=2, I=256, qtype=qt, x_dtype="fp32")
     for T in (1, 4, 13):
         tl = make_layer(shape, 25, T, exact_all=True)
         _check_layer(tl, T)
+
+
+@pytest.mark.parametrize("T", [1, 9, 70])
+def test_q3_k_gate_up_with_q4_k_down(T):
+    # the large model's routed-expert mix: Q3_K gate and up, Q4_K down (GEMV kernels at every T;
+    # the down matrix takes the segmented Q4_K kernel)
+    from quantized_routed_expert_sigmoid_gb300 import MoeLayer
+    from helpers import OQ, oracle_mode
+    shape = dataclasses.replace(synth.DECODE, qtype=synth.Q3_K)
+    seed = 26
+    tl = make_layer(shape, seed, T, exact_all=True)
+    dshape = dataclasses.replace(shape, qtype=synth.Q4_K)
+    down4 = torch.stack([synth.expert_matrix(dshape, seed, 0, "down", e, "cuda") for e in range(shape.E)])
+    spec = tl.spec()
+    spec = oracle.LayerSpec(mode=oracle_mode(shape), E=shape.E, k=shape.k, H=shape.H, I=shape.I, qtype=OQ[shape.qtype],
+                            gate=spec.gate, up=spec.up, down=down4.cpu().numpy(), Wr=tl.Wr.numpy(),
+                            qtype_down=oracle.Q4_K)
+    ref = oracle.moe_layer(spec, tl.x.double().numpy(), n_threads=oracle.max_threads())
+    layer = MoeLayer(mode="softmax", E=shape.E, k=shape.k, H=shape.H, I=shape.I, qtype=shape.qtype,
+                     gate=tl.bank.gate, up=tl.bank.up, down=down4, W_router=tl.Wr.cuda(), qtype_down="q4_k")
+    assert layer.path(T) == "gemv"
+    out = layer(tl.x.cuda())
+    torch.cuda.synchronize()
+    ids, _, _ = layer.debug_views(T)
+    assert np.array_equal(ids.numpy(), ref["ids"])
+    err = rel_l2(out.cpu().numpy(), ref["out"])
+    assert err <= TOL_GEMV, f"rel-L2 {err:.3e}"
+    assert layer.device_status(T) == 0
 
 
 def test_decode_q4_k_ragged_batch():
