@@ -286,8 +286,9 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_gateup_kernel(const __grid_c
 
 // ============================================================================ down
 // Narrow rows (I/64 groups not a multiple of 32, e.g. I = 768): unit = 8 rows n0.. of one
-// expert's down matrix; lane = 4 * row + sub takes, in every item (4 blocks of the 8 rows), the
-// group of `sub` in each block; the 4 lanes of a row then sum.
+// expert's down matrix; in every item (at most 4 blocks = 16 groups of the 8 rows) lane = 16 *
+// half + gl takes group gl of rows 4 half .. 4 half + 3, so every activation load serves 4 rows;
+// the 16 lanes of a half then sum.
 // Wide rows (kWide: I/64 a multiple of 32, e.g. I = 2048): the gate/up layout -- unit = 4 rows,
 // item = 8 blocks of the 4 rows, lane = group, so every activation load serves 4 rows.
 template <int NT, bool kWide>
@@ -314,7 +315,7 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_down_kernel(const __grid_con
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     seg_plan(p.offsets, p.E, upe, p.nt_max, s_plan);
-    const int row = lane >> 2, sub = lane & 3;
+    const int half = lane >> 4, gl = lane & 15;
     bool ok = true;
     uint32_t gi = 0;
     int a = s_plan.a_lo;
@@ -391,17 +392,20 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_down_kernel(const __grid_con
                         }
                         qd4_group_math<NT, 4, 3>(hd, q0, q1, live, 0, ch * 32 + lane, GI, X, XS, nt, acc, nullptr);
                     }
-                } else if (have) {
-                    const uint8_t* rb0 = ring + slot * kSSlotBytes + row * rs;
-                    for (int i = 0; i < nb; ++i) {
-                        const uint8_t* blk = rb0 + i * kQ4KBytes;
-                        uint4 hd[1], q0[1], q1[1];
-                        const bool live[1] = {true};
-                        hd[0] = *reinterpret_cast<const uint4*>(blk);
-                        q0[0] = *reinterpret_cast<const uint4*>(blk + 16 + 32 * sub);
-                        q1[0] = *reinterpret_cast<const uint4*>(blk + 32 + 32 * sub);
-                        qd4_group_math<NT, 1, 3>(hd, q0, q1, live, 0, (b0 + i) * 4 + sub, GI, X, XS, nt, acc, nullptr);
+                } else if (have && gl < 4 * nb) {
+                    // rows 4 half .. 4 half + 3, group gl of the item: block gl / 4, quant group gl % 4
+                    const uint8_t* blk = ring + slot * kSSlotBytes + (4 * half) * rs + (gl >> 2) * kQ4KBytes;
+                    const int c = gl & 3;
+                    uint4 hd[4], q0[4], q1[4];
+                    const bool live[4] = {true, true, true, true};
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const uint8_t* rb = blk + r * rs;
+                        hd[r] = *reinterpret_cast<const uint4*>(rb);
+                        q0[r] = *reinterpret_cast<const uint4*>(rb + 16 + 32 * c);
+                        q1[r] = *reinterpret_cast<const uint4*>(rb + 32 + 32 * c);
                     }
+                    qd4_group_math<NT, 4, 3>(hd, q0, q1, live, 0, b0 * 4 + gl, GI, X, XS, nt, acc, nullptr);
                 }
                 __syncwarp();
                 issue(item + 2);
@@ -412,13 +416,17 @@ __global__ void __launch_bounds__(kSThreads, 1) seg_down_kernel(const __grid_con
                         const int i = lane >> sh, r = i / NT, t = i - r * NT;
                         if ((lane & ((1 << sh) - 1)) == 0 && t < nt) p.out[(int64_t)(st + pb + t) * H + 4 * u + r] = v;
                     } else {
-                        const int n = 8 * u + row;
+                        // the 16 lanes of a half: butterfly over gl, lane gl = 0 writes its 4 rows
 #pragma unroll
                         for (int t = 0; t < NT; ++t) {
-                            float v = acc[0][t];
-                            v += __shfl_xor_sync(0xffffffffu, v, 1);
-                            v += __shfl_xor_sync(0xffffffffu, v, 2);
-                            if (sub == 0 && t < nt) p.out[(int64_t)(st + pb + t) * H + n] = v;
+                            if (t >= nt) break;                 // warp-uniform: the pass's tokens only
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) {
+                                float v = acc[r][t];
+#pragma unroll
+                                for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                                if (gl == 0) p.out[(int64_t)(st + pb + t) * H + 8 * u + 4 * half + r] = v;
+                            }
                         }
                     }
                 }
