@@ -75,19 +75,22 @@ typedef enum {
  * 2r + 1 of byte 32 + 32h + l and bit 4h + r of byte l, q = low + 4 * bit - 4 in [-4, 3]; scale
  * j: low nibble of byte 96 + j (j < 8) or high nibble of byte 96 + j - 8, bits 4-5 from bits
  * 2(j / 4).. of byte 104 + j % 4; w = d * (s_j - 32) * q.
- * These are the public GGUF K-quant layouts; the pages list them among the card-expert types
+ * MOE_MXFP4: 17 bytes per 32 weights (OCP Microscaling) -- an E8M0 scale byte e, then 16 bytes
+ * whose byte j holds the FP4 E2M1 element j (low nibble) and j + 16 (high nibble);
+ * w = 2^(e - 127) * e2m1 (e = 255 is NaN).  cols must be a multiple of 128.
+ * These are the public GGUF layouts; the pages list them among the card-expert types
  * ("bloomery README 0.3.1", Status table, "Quant types" row), and their large model keeps its
  * routed experts as Q3_K gate and up with a Q4_K down ("bloomery README 0.3.11", limits list;
  * desc.down may have another type than gate and up).  They run on the GEMV kernels at every T
  * (moe_layer_path reports MOE_PATH_GEMV). */
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_Q8_0 = 2, MOE_Q4_K = 3, MOE_Q8_0_R = 4, MOE_Q5_K = 5,
-               MOE_Q6_K = 6, MOE_Q3_K = 7 } moe_dtype;
+               MOE_Q6_K = 6, MOE_Q3_K = 7, MOE_MXFP4 = 8 } moe_dtype;
 
 typedef enum { MOE_ROUTE_SOFTMAX = 0, MOE_ROUTE_SIGMOID_GROUP = 1 } moe_route_mode;
 
 /* One quantized weight tensor, possibly a stack of experts. */
 typedef struct {
-    moe_dtype qtype;             /* MOE_Q8_0, MOE_Q4_K, MOE_Q8_0_R, MOE_Q5_K, MOE_Q6_K or MOE_Q3_K */
+    moe_dtype qtype;             /* MOE_Q8_0, MOE_Q4_K, MOE_Q8_0_R, MOE_Q5_K, MOE_Q6_K, MOE_Q3_K or MOE_MXFP4 */
     const void* data;            /* (device) 16-byte aligned */
     int64_t rows, cols;          /* per expert; cols = input dimension */
     int64_t expert_stride_bytes; /* bytes from expert e to e+1 (multiple of 16) */
@@ -117,7 +120,7 @@ typedef struct {
  *     rows, cols = K a multiple of 32, expert_stride_bytes >= rows * 34 * K/32 when
  *     n_experts > 1).  On success it is rewritten to describe the repacked tensor:
  *     qtype MOE_Q8_0_R, data = dst, expert_stride_bytes = rows * row bytes.  A MOE_Q4_K
- *     tensor (and a MOE_Q5_K, MOE_Q6_K or MOE_Q3_K one) is used as stored: in_out is left unchanged and
+ *     tensor (and a MOE_Q5_K, MOE_Q6_K, MOE_Q3_K or MOE_MXFP4 one) is used as stored: in_out is left unchanged and
  *     nothing is written.
  *   dst (device, 16-byte aligned): at least moe_weights_prepare_size() bytes, owned by
  *     the caller; it must not overlap the source.

@@ -44,7 +44,7 @@
  *         nibbles (OCP Microscaling formats); w = 2^(e-127) * e2m1(q).
  * Q5_K, Q6_K, Q3_K and MXFP4 are the next expert types the pages list for
  * the card (Q4_K to Q6_K, the Q3_K_M files the large model ships in, and
- * MXFP4); only the oracle decodes them so far.
+ * MXFP4).
  *
  * Every value is computed in fp64.  Weight matrices are [rows][K/blk blocks],
  * blocks along the input dimension K; experts are laid out one after another

@@ -18,7 +18,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "moe_gb300.h")
 
 (MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE_CHECK,
  MOE_ERR_TIMEOUT) = range(7)
-MOE_F32, MOE_BF16, MOE_Q8_0, MOE_Q4_K, MOE_Q8_0_R, MOE_Q5_K, MOE_Q6_K, MOE_Q3_K = range(8)
+MOE_F32, MOE_BF16, MOE_Q8_0, MOE_Q4_K, MOE_Q8_0_R, MOE_Q5_K, MOE_Q6_K, MOE_Q3_K, MOE_MXFP4 = range(9)
 MOE_ROUTE_SOFTMAX, MOE_ROUTE_SIGMOID_GROUP = range(2)
 
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",

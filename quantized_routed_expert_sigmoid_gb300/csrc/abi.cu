@@ -33,6 +33,7 @@ bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 int64_t row_bytes(moe_dtype q, int64_t cols) {
     if (q == MOE_Q3_K) return cols / 256 * 110;
+    if (q == MOE_MXFP4) return cols / 32 * 17;
     if (q == MOE_Q4_K || q == MOE_Q8_0 || q == MOE_Q8_0_R || q == MOE_Q5_K || q == MOE_Q6_K) return q_row_bytes(q, cols);
     return -1;
 }
@@ -42,15 +43,17 @@ int kernel_qtype(moe_dtype q) { return q == MOE_Q8_0_R ? (int)MOE_Q8_0 : (int)q;
 moe_status check_qmat(const moe_qmat* m, const char* name, int64_t rows, int64_t cols, int E) {
     if (!m) return fail(MOE_ERR_INVALID_ARG, "%s: NULL matrix", name);
     if (m->qtype != MOE_Q4_K && m->qtype != MOE_Q8_0 && m->qtype != MOE_Q8_0_R && m->qtype != MOE_Q5_K &&
-        m->qtype != MOE_Q6_K && m->qtype != MOE_Q3_K)
-        return fail(MOE_ERR_UNSUPPORTED, "%s: qtype %d (supported: Q8_0, Q8_0_R, Q4_K, Q5_K, Q6_K, Q3_K)", name,
+        m->qtype != MOE_Q6_K && m->qtype != MOE_Q3_K && m->qtype != MOE_MXFP4)
+        return fail(MOE_ERR_UNSUPPORTED, "%s: qtype %d (supported: Q8_0, Q8_0_R, Q4_K, Q5_K, Q6_K, Q3_K, MXFP4)", name,
                     (int)m->qtype);
     if (!m->data) return fail(MOE_ERR_INVALID_ARG, "%s: NULL data", name);
     if (!aligned(m->data, 16)) return fail(MOE_ERR_INVALID_ARG, "%s: data not 16-byte aligned", name);
     if (m->rows != rows || m->cols != cols)
         return fail(MOE_ERR_INVALID_ARG, "%s: shape %lldx%lld, expected %lldx%lld", name, (long long)m->rows,
                     (long long)m->cols, (long long)rows, (long long)cols);
-    const int blk = (m->qtype == MOE_Q8_0 || m->qtype == MOE_Q8_0_R) ? kQ80Weights : kQ4KWeights;
+    // MXFP4: 17-byte blocks, rows kept to a multiple of 4 bytes (the kernels' aligned word loads)
+    const int blk = (m->qtype == MOE_Q8_0 || m->qtype == MOE_Q8_0_R) ? kQ80Weights : m->qtype == MOE_MXFP4 ? 128
+                                                                                     : kQ4KWeights;
     if (cols % blk) return fail(MOE_ERR_INVALID_ARG, "%s: cols %lld not a multiple of %d", name, (long long)cols, blk);
     const int64_t need = rows * row_bytes(m->qtype, cols);
     if (E > 1 && (m->expert_stride_bytes < need || m->expert_stride_bytes % 16))
@@ -298,7 +301,8 @@ const char* moe_version(void) { return "moe_gb300 0.1 (sm_103a)"; }
 moe_status moe_weights_prepare_size(const moe_qmat* in, int n_experts, size_t* bytes) {
     if (!in || !bytes) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
     if (n_experts < 1) return fail(MOE_ERR_INVALID_ARG, "n_experts = %d < 1", n_experts);
-    if (in->qtype == MOE_Q4_K || in->qtype == MOE_Q5_K || in->qtype == MOE_Q6_K || in->qtype == MOE_Q3_K) {
+    if (in->qtype == MOE_Q4_K || in->qtype == MOE_Q5_K || in->qtype == MOE_Q6_K || in->qtype == MOE_Q3_K ||
+        in->qtype == MOE_MXFP4) {
         *bytes = 0;
         return MOE_OK;
     }
@@ -317,7 +321,7 @@ moe_status moe_weights_prepare(moe_qmat* in_out, int n_experts, void* dst, size_
     moe_status st = moe_weights_prepare_size(in_out, n_experts, &need);
     if (st) return st;
     if (in_out->qtype == MOE_Q4_K || in_out->qtype == MOE_Q5_K || in_out->qtype == MOE_Q6_K ||
-        in_out->qtype == MOE_Q3_K)
+        in_out->qtype == MOE_Q3_K || in_out->qtype == MOE_MXFP4)
         return MOE_OK;
     if ((st = check_qmat(in_out, "in", in_out->rows, in_out->cols, n_experts))) return st;
     if (!dst || !aligned(dst, 16)) return fail(MOE_ERR_INVALID_ARG, "dst NULL or not 16-byte aligned");

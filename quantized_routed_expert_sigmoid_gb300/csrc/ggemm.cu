@@ -16,17 +16,16 @@
 // knowledge of the per-expert counts.
 //
 // Warp roles: producer warps (16 for the Q4_K gate/up, else 8) copy the raw blocks with
-// cp.async and dequantize them; gate/up producers also run the SwiGLU epilogue (its
-// accumulators fill all 512 TMEM columns); down has 8 epilogue warps and two accumulator
-// buffers, so its epilogue overlaps the next tile; the last warp owns TMEM and issues the
-// MMAs.  Pipeline per global k-step g, operand stage g % S (S = 3 for gate/up, 4 for down): a
-// producer warp waits until the MMAs of step g - S have completed (empty), arms bfull with
-// the bytes of its token rows of B(g) and issues their TMA, waits for raw(g), dequantizes it
-// into A, arrives on afull, then issues raw(g + D) (D = 2 for gate/up, 3 for down, across tile
-// boundaries); the MMA warp waits afull and bfull, issues four k-substeps and commits to
-// empty.  Producers thus run up to S - 1 k-steps ahead of the MMAs.  Every wait is bounded
-// (globaltimer); on timeout the kernel records MOE_ERR_TIMEOUT, drains its MMAs, waits
-// (bounded) on the bfull phases of the token rows still in flight, frees TMEM and returns.
+// cp.async, dequantize them and issue the token-row TMA; gate/up producers also run the
+// SwiGLU epilogue (its accumulators fill all 512 TMEM columns); down has 8 epilogue warps
+// and two accumulator buffers, so its epilogue overlaps the next tile; the last warp owns
+// TMEM and issues the MMAs.  Pipeline per global k-step g: a producer waits until the A
+// stage g%2 is free (MMA(g-2) done), waits for raw(g), dequantizes it, arrives on full[g%4]
+// (which also counts the TMA bytes of B(g)), then issues raw and B of step g + D (D = 2 for
+// gate/up, 3 for down, across tile boundaries); the MMA warp waits full[g%4], issues four
+// k-substeps and commits to empty[g%4].  Every wait is bounded (globaltimer); on timeout
+// the kernel records MOE_ERR_TIMEOUT, drains its MMAs, waits (bounded) on the barriers of
+// the copies still in flight, frees TMEM and returns.
 #include <algorithm>
 #include <cuda.h>   // CUtensorMap and its enums (the encoder is fetched from the driver at run time)
 
@@ -39,21 +38,16 @@ namespace {
 constexpr int kBM = 128, kBK = 64;
 constexpr int kBNMin = 128;                       // token-block width bound used to size the tile list
 // Producer warps: 16 for the Q4_K gate/up (a thread dequantizes half of a row's 64-weight
-// k-step, so that enough warps hide the latency of their dependent steps; 8 warps with whole
-// k-steps per thread measured 12 % slower), 8 otherwise (Q4_K down: half a k-step per thread
-// already; Q8_0: its raw blocks need the shared memory).
+// k-step, so that enough warps hide the latency of their dependent steps), 8 otherwise (Q4_K
+// down: half a k-step per thread already; Q8_0: its raw blocks need the shared memory).
 template <int QT, int MODE>
 __host__ __device__ constexpr int tc_pw() { return QT == MOE_Q4_K && MODE == 0 ? 16 : 8; }
-// How many k-steps ahead of the dequantization a producer issues its raw blocks: 2 for gate/up
-// (its shared memory is full), 3 for down (its k-steps are half as long, so two of them do not
-// cover the latency of a DRAM read); one raw slot per step in flight.
+constexpr int kAStages = 2, kBStages = 4;
+// How many k-steps ahead of the dequantization the raw blocks and token rows are issued: 2
+// for gate/up (its shared memory is full), 3 for down (its k-steps are half as long, so two
+// of them do not cover the latency of a DRAM read); one raw slot per step in flight.
 template <int MODE>
 __host__ __device__ constexpr int tc_dist() { return MODE == 0 ? 2 : 3; }
-// Operand stages: A (dequantized weights) and B (token rows) of k-step g live in stage g % S.
-// Gate/up: 3 (A 32 KB + B 32 KB each; the producers may run two k-steps ahead of the MMAs);
-// down: 4 (A 16 KB + B 32 KB each).
-template <int MODE>
-__host__ __device__ constexpr int tc_stages() { return MODE == 0 ? 3 : 4; }
 
 enum { kGateUp = 0, kDown = 1 };
 
@@ -129,8 +123,7 @@ __device__ __forceinline__ Q4Scales q4k_scales_h2(const uint4& hd) {
 // Raw bytes staged per producer thread per k-step.
 template <int QT, int MODE>
 struct RawCfg {
-    static constexpr int kSplit = 32 * tc_pw<QT, MODE>() / (kBM * (MODE == 0 ? 2 : 1));   // threads per row
-    static constexpr int kBytes = QT == MOE_Q4_K ? 16 + 32 / kSplit : 80;   // Q4_K: header + the thread's quants
+    static constexpr int kBytes = QT == MOE_Q4_K ? 32 : 80;   // Q4_K: header + up to 16 quant bytes
 };
 
 struct TileInfo {
@@ -174,14 +167,14 @@ __device__ __forceinline__ bool tile_at(const TcParams& p, int n_mb, int t, int 
     return true;
 }
 
-// Warp layout: producers, then (DOWN) 8 epilogue warps, then the MMA warp.  DOWN keeps two
-// accumulators in TMEM so that its epilogue overlaps the next tile's main loop; GATEUP needs
-// all 512 columns for one tile (gate and up, 256 tokens each) and lets the producers run its
-// epilogue.
+// Warp layout: producers, then (DOWN) 8 epilogue warps, then the MMA warp.  DOWN keeps
+// two accumulators in TMEM so that its epilogue overlaps the next tile's main loop; GATEUP
+// needs all 512 columns for one tile (gate and up, 256 tokens each) and lets the producers
+// run its epilogue.
 template <int MODE>
 __host__ __device__ constexpr int tc_epi_warps() { return MODE == kDown ? 8 : 0; }
 template <int QT, int MODE>
-__host__ __device__ constexpr int tc_threads() { return 32 * (tc_pw<QT, MODE>() + tc_epi_warps<MODE>() + 1); }
+__host__ __device__ constexpr int tc_threads() { return 32 * tc_pw<QT, MODE>() + 32 * tc_epi_warps<MODE>() + 32; }
 
 template <int QT, int MODE>
 __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
@@ -196,7 +189,6 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
     constexpr int kRawSlotBytes = kNP * kRawBytes;
     constexpr int kDist = tc_dist<MODE>();
     constexpr int kRawSlots = kDist;
-    constexpr int kS = tc_stages<MODE>();
     constexpr int kEpiWarps = tc_epi_warps<MODE>();
     constexpr int kMmaWarp = kPW + kEpiWarps;
     constexpr uint32_t kAccCols = (MODE == kGateUp ? 2 : 1) * BN;
@@ -207,30 +199,27 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
-    uint8_t* sB = sA + kS * kAStageBytes;
-    uint8_t* sRaw = sB + kS * kBStageBytes;
+    uint8_t* sB = sA + kAStages * kAStageBytes;
+    uint8_t* sRaw = sB + kBStages * kBStageBytes;
     uint64_t* bar = reinterpret_cast<uint64_t*>(sRaw + kRawSlots * kRawSlotBytes);
-    uint64_t* afull = bar;           // [kS]: A dequantized (one arrival per producer warp)
-    uint64_t* bfull = bar + 4;       // [kS]: B landed (one arrival per producer warp + the TMA bytes)
-    uint64_t* empty = bar + 8;       // [kS]: the MMAs of the stage completed
-    uint64_t* accf = bar + 12;       // [2]: accumulator buffer complete
-    uint64_t* tfree = bar + 14;      // [2]: accumulator buffer read out by the epilogue warps
-    uint64_t* drain = bar + 16;      // [1]
-    uint64_t* never = bar + 17;      // [1]: the test stall (initialized, never arrived on)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 18);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 19);
-    int* b_issued = reinterpret_cast<int*>(bar + 20);    // k-steps whose bfull a producer warp armed (abort drain)
-    auto sidx = [](uint32_t g) { return (int)(g % kS); };
-    auto spar = [](uint32_t g) { return (uint32_t)(g / kS) & 1u; };
+    uint64_t* full = bar;            // [4]: A dequantized (one arrival per producer warp) + B landed (tx bytes)
+    uint64_t* empty = bar + 4;       // [4]
+    uint64_t* accf = bar + 8;        // [2]: accumulator buffer complete
+    uint64_t* tfree = bar + 10;      // [2]: accumulator buffer read out by the epilogue warps
+    uint64_t* drain = bar + 12;      // [1]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 13);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 14);
+    uint64_t* never = bar + 15;      // [1]: the test stall (initialized, never arrived on)
+    int* max_issued = reinterpret_cast<int*>(bar + 16);   // k-steps the producers issued (abort drain)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
-        for (int i = 0; i < kS; ++i) { mbar_init(&afull[i], kPW); mbar_init(&bfull[i], kPW); mbar_init(&empty[i], 1); }
+        for (int i = 0; i < 4; ++i) { mbar_init(&full[i], kPW); mbar_init(&empty[i], 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(&accf[i], 1); mbar_init(&tfree[i], kEpiWarps > 0 ? kEpiWarps : 1); }
         mbar_init(drain, 1);
         mbar_init(never, 1);
         *abort_flag = 0;
-        *b_issued = 0;
+        *max_issued = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tmap_b) : "memory");
     }
@@ -253,59 +242,60 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
     const int64_t rb = QT == MOE_Q4_K ? (int64_t)nblk_row * kQ4KBytes
                                       : (QT == MOE_Q8_0_R ? q80r_row_bytes(p.K) : (int64_t)nblk_row * kQ80Bytes);
 
-    int n_armed_out = 0;                            // producers: the k-steps whose bfull this warp armed
+    int n_issued = 0, n_arrived = 0;                // producers: k-steps issued / arrived on full[]
     if (warp < kPW) {
         // ======================= producers (+ GATEUP epilogue) =======================
         const int prow = tid & 127;                 // weight row within the tile
         const int pmat = MODE == kGateUp ? (tid >> 7) & 1 : 0;   // matrix: 0 gate / down, 1 up
         const int part = (tid >> 7) / kMats;        // which 1/kSplit of the row's k-step
-        // ---- raw-block cursor: runs kDist k-steps ahead of the dequantization, across tile
-        // boundaries, so that a tile's first raw blocks are in flight while the previous tile
-        // finishes
+        constexpr int kRowsPW = BN / kPW, kGroupsPW = kRowsPW / 4;
+        // ---- issue cursor: runs two k-steps ahead of the dequantization, across tile
+        // boundaries, so that a tile's first raw blocks and token rows are in flight while the
+        // previous tile finishes
         int is_t = blockIdx.x, is_kb = 0;
         TileInfo iti{};
         bool is_valid = false;
         const uint8_t* is_wrow = nullptr;
+        // GATEUP: this warp's gathers of the cursor's tile: how many, and the four x16 rows of
+        // the lane's group (lane < is_mine)
+        int is_mine = 0, is_y0 = 0, is_y1 = 0, is_y2 = 0, is_y3 = 0;
         auto is_tile = [&]() {
             is_valid = is_t < n_tiles && tile_at(p, n_mb, is_t, n_tb, iti);
             if (!is_valid) return;
             is_wrow = (pmat == 1 ? p.w1 : p.w0) + (int64_t)iti.e * p.expert_stride + (int64_t)(iti.m0 + prow) * rb;
-        };
-        // ---- token rows of the current tile: GATEUP warp w gathers groups kGroupsPW * w ..
-        // (four x16 rows per TMA; rows past the block's tokens take its first token's row,
-        // whose columns are computed and never stored); DOWN: warp 0 loads the block's
-        // consecutive h16 rows in one box.  Every producer warp arrives on bfull once per step.
-        constexpr int kRowsPW = BN / kPW, kGroupsPW = kRowsPW / 4;
-        int b_mine = 0, b_y0 = 0, b_y1 = 0, b_y2 = 0, b_y3 = 0, b_tok0 = 0, n_armed = 0;
-        auto b_tile = [&](const TileInfo& ti) {
-            b_tok0 = ti.tok0;
             if (MODE == kGateUp) {
+                // lane l < kRowsPW takes the x16 row of column kRowsPW * warp + l; columns past the
+                // block's tokens take its first token's row (never read)
                 const int r = kRowsPW * warp + lane;
-                const int i = ti.tok0 + (r < ti.ntok ? r : 0);
+                const int i = iti.tok0 + (r < iti.ntok ? r : 0);
                 const int row = p.sorted_pairs ? p.sorted_pairs[i] / p.k : i;
-                const int ngroups = (ti.ntok + 3) >> 2;
-                b_mine = min(kGroupsPW, max(0, ngroups - kGroupsPW * warp));
+                const int ngroups = (iti.ntok + 3) >> 2;
+                is_mine = min(kGroupsPW, max(0, ngroups - kGroupsPW * warp));
                 const int src = (4 * lane) & (kRowsPW - 1);
-                b_y0 = __shfl_sync(0xffffffffu, row, src);
-                b_y1 = __shfl_sync(0xffffffffu, row, src + 1);
-                b_y2 = __shfl_sync(0xffffffffu, row, src + 2);
-                b_y3 = __shfl_sync(0xffffffffu, row, src + 3);
+                is_y0 = __shfl_sync(0xffffffffu, row, src);
+                is_y1 = __shfl_sync(0xffffffffu, row, src + 1);
+                is_y2 = __shfl_sync(0xffffffffu, row, src + 2);
+                is_y3 = __shfl_sync(0xffffffffu, row, src + 3);
             }
         };
-        auto issue_b = [&](uint32_t g, int kb) {
-            uint8_t* dst = sB + sidx(g) * kBStageBytes;
-            uint64_t* fb = &bfull[sidx(g)];
-            const uint32_t bytes = MODE == kGateUp ? (uint32_t)b_mine * 512u : (warp == 0 ? (uint32_t)p.b_box_rows * 128u : 0u);
-            if (lane == 0)
-                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(fb)), "r"(bytes) : "memory");
-            __syncwarp();
+        // B of the cursor's k-step into stage `stage`, completing on full[stage]: GATEUP gathers
+        // four x16 rows per TMA (warp w: groups kGroupsPW * w.. of the rows the block needs),
+        // DOWN loads the BN consecutive h16 rows of the block in one box
+        auto issue_b = [&](int kb, int stage) {
+            uint8_t* dst = sB + stage * kBStageBytes;
+            uint64_t* fb = &full[stage];
             if (MODE == kGateUp) {
-                if (lane < b_mine)
-                    tma_gather4(dst + (kGroupsPW * warp + lane) * 512, &p.tmap_b, kb * kBK, b_y0, b_y1, b_y2, b_y3, fb);
-            } else if (warp == 0 && lane == 0) {
-                tma_load_2d(dst, &p.tmap_b, kb * kBK, b_tok0, fb);
+                if (is_mine > 0) {
+                    if (lane == 0) mbar_expect_tx(fb, (uint32_t)is_mine * 512u);
+                    __syncwarp();
+                    if (lane < is_mine)
+                        tma_gather4(dst + (kGroupsPW * warp + lane) * 512, &p.tmap_b, kb * kBK, is_y0, is_y1, is_y2,
+                                    is_y3, fb);
+                }
+            } else if (tid == 0) {
+                mbar_expect_tx(fb, (uint32_t)p.b_box_rows * 128u);
+                tma_load_2d(dst, &p.tmap_b, kb * kBK, iti.tok0, fb);
             }
-            n_armed = (int)g + 1;
         };
         auto issue_raw = [&](int kb, int slot) {
             uint8_t* dst = sRaw + slot * kRawSlotBytes + tid * kRawBytes;
@@ -313,14 +303,8 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
                 const uint8_t* blk = is_wrow + (int64_t)(kb >> 2) * kQ4KBytes;
                 if ((kb & 3) == 0) cp_async16(dst, blk, 16u);                 // header, once per super-block
                 const uint8_t* qs = blk + 16 + 32 * (kb & 3) + (32 / kSplit) * part;
-                if constexpr (kSplit == 1) {
-                    cp_async16(dst + 16, qs, 16u);
-                    cp_async16(dst + 32, qs + 16, 16u);
-                } else if constexpr (kSplit == 2) {
-                    cp_async16(dst + 16, qs, 16u);
-                } else {
-                    cp_async8(dst + 16, qs);
-                }
+                if constexpr (kSplit == 2) cp_async16(dst + 16, qs, 16u);
+                else cp_async8(dst + 16, qs);
             } else if (QT == MOE_Q8_0_R) {
                 // repacked: the k-step's 64 quants (16-byte aligned), then its two scales
                 const uint8_t* qsrc = is_wrow + (int64_t)kb * 64;
@@ -335,8 +319,10 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
         };
         // issue global k-step gs (the cursor's) and advance the cursor; always one commit group
         auto issue_next = [&](uint32_t gs) {
+            n_issued = (int)gs + 1;
             if (is_valid) {
                 issue_raw(is_kb, gs % kRawSlots);
+                issue_b(is_kb, gs % kBStages);
                 if (++is_kb == nk) {
                     is_kb = 0;
                     is_t += gridDim.x;
@@ -354,20 +340,15 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
         for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x, ++tile_iter) {
             TileInfo ti;
             if (!tile_at(p, n_mb, t, n_tb, ti)) break;
-            b_tile(ti);
             bool ok = true;
             for (int kb = 0; kb < nk; ++kb, ++g) {
-                // stage g % kS (A and B) was last read by MMA(g - kS); then this warp's token rows
-                // of the step go out first, to land while the step is dequantized
-                if (g >= (uint32_t)kS && !mbar_wait(&empty[sidx(g)], spar(g - kS), abort_flag, p.wait_ns)) {
-                    ok = false;
-                    break;
-                }
-                issue_b(g, kb);
+                // A stage g%2 was last read by MMA(g-2) (with kDist == 3 already waited for below)
+                if (kDist == 2 && g >= 2 &&
+                    !mbar_wait(&empty[(g + 2) & 3], ((g - 2) >> 2) & 1, abort_flag, p.wait_ns)) { ok = false; break; }
                 cp_wait<kDist - 1>();                // raw(g) has landed (only later steps may be pending)
                 // ---- dequantize k-step kb into A stage g%2
                 const uint8_t* raw = sRaw + (g % kRawSlots) * kRawSlotBytes + tid * kRawBytes;
-                uint8_t* arow = sA + sidx(g) * kAStageBytes + pmat * kBM * 128;
+                uint8_t* arow = sA + (g % kAStages) * kAStageBytes + pmat * kBM * 128;
                 if (QT == MOE_Q4_K) {
                     // the header (read at the super-block's first k-step) gives the scales of all four
                     const int c = kb & 3;
@@ -432,7 +413,11 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
                 // the warp then arrives once
                 fence_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&afull[sidx(g)]);
+                if (lane == 0) mbar_arrive(&full[g & 3]);
+                n_arrived = (int)g + 1;
+                // B stage (g + kDist) % 4 was last read by MMA(g + kDist - 4)
+                if (kDist == 3 && g >= 1 &&
+                    !mbar_wait(&empty[(g - 1) & 3], ((g - 1) >> 2) & 1, abort_flag, p.wait_ns)) { ok = false; break; }
                 issue_next(g + kDist);
             }
             if (!ok) break;
@@ -466,9 +451,7 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
             }
         }
         cp_wait_all();
-        if (lane == 0) atomicMax(b_issued, n_armed);
-        // (abort drain, below: this warp arrives on the bfull phases it did not arm)
-        n_armed_out = n_armed;
+        if (lane == 0) atomicMax(max_issued, n_issued);
     } else if (warp < kMmaWarp) {
         // ======================= DOWN epilogue warps =======================
         // epilogue warp e reads TMEM lanes 32q.. (q = warp % 4) and the 64-column chunks
@@ -544,16 +527,12 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
             const uint32_t acc = tmem + (uint32_t)b * kAccCols;
             bool ok = true;
             for (int kb = 0; kb < nk; ++kb, ++g) {
-                uint64_t* fa = p.stall && g == 0 ? never : &afull[sidx(g)];   // (test stall)
-                if (!mbar_wait(fa, fa == never ? 0u : spar(g), abort_flag, p.wait_ns) ||
-                    !mbar_wait(&bfull[sidx(g)], spar(g), abort_flag, p.wait_ns)) {
-                    ok = false;
-                    break;
-                }
+                uint64_t* fb = p.stall && g == 0 ? never : &full[g & 3];     // (test stall)
+                if (!mbar_wait(fb, fb == never ? 0u : (g >> 2) & 1, abort_flag, p.wait_ns)) { ok = false; break; }
                 tc_after();
                 if (lane == 0) {
-                    const uint32_t a0 = su32(sA + sidx(g) * kAStageBytes);
-                    const uint32_t b0 = su32(sB + sidx(g) * kBStageBytes);
+                    const uint32_t a0 = su32(sA + (g % kAStages) * kAStageBytes);
+                    const uint32_t b0 = su32(sB + (g % kBStages) * kBStageBytes);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t bd = sdesc(b0 + 32 * kk);
@@ -561,7 +540,7 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
                         if (MODE == kGateUp)
                             mma_f16(acc + BN, sdesc(a0 + kBM * 128 + 32 * kk), bd, idesc, (kb | kk) != 0);
                     }
-                    mma_commit(&empty[sidx(g)]);
+                    mma_commit(&empty[g & 3]);
                     if (kb == nk - 1) mma_commit(&accf[b]);
                 }
                 issued = true;
@@ -580,20 +559,19 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
     __syncthreads();
     tc_after();
     if (*abort_flag) {
-        // every thread has left its loop and the producers' raw copies (cp.async) are waited for;
+        // every thread has left its loop.  The producers' raw copies (cp.async) are waited for;
         // the token rows (TMA) of the last k-steps may still be in flight.  Each producer warp
-        // arrives on the bfull phases it did not arm, up to the last step any warp armed, so that
-        // each such phase completes exactly when its bytes land; steps older than the last kS
-        // completed already (a warp arms step s only after the MMAs of step s - kS, which waited
-        // for its phase).
-        const int last = *b_issued;
+        // arrives on full[] for the k-steps it has not arrived on, up to the last one any warp
+        // issued, so that the phase of each such step completes exactly when its bytes land.
+        // Steps older than the last four completed already: a producer issues step s only after
+        // the MMAs of step s - 4, which waited for its phase.
         if (warp < kPW && lane == 0)
-            for (int s2 = n_armed_out; s2 < last; ++s2) mbar_arrive(&bfull[sidx((uint32_t)s2)]);
+            for (int s = n_arrived; s < *max_issued; ++s) mbar_arrive(&full[s & 3]);
         __syncthreads();
         if (tid == 0) {
             atomicCAS(&p.hdr->status, (int)MOE_OK, (int)MOE_ERR_TIMEOUT);
-            for (int s2 = max(0, last - kS); s2 < last; ++s2)
-                mbar_wait_for(&bfull[sidx((uint32_t)s2)], spar((uint32_t)s2), p.wait_ns);
+            const int last = *max_issued;
+            for (int s = max(0, last - 4); s < last; ++s) mbar_wait_for(&full[s & 3], (uint32_t)(s >> 2) & 1u, p.wait_ns);
         }
         tc_before();
         __syncthreads();
@@ -665,8 +643,8 @@ __global__ void to_half_kernel(const void* __restrict__ x, bool bf16, int64_t n,
 
 template <int QT, int MODE>
 size_t tc_smem_bytes() {
-    constexpr int a = tc_stages<MODE>() * (MODE == kGateUp ? 2 : 1) * kBM * 128;
-    constexpr int b = tc_stages<MODE>() * tc_bn<QT>() * 128;
+    constexpr int a = kAStages * (MODE == kGateUp ? 2 : 1) * kBM * 128;
+    constexpr int b = kBStages * tc_bn<QT>() * 128;
     constexpr int r = tc_dist<MODE>() * 32 * tc_pw<QT, MODE>() * RawCfg<QT, MODE>::kBytes;
     return (size_t)a + b + r + 256 + 1024;   // barriers + alignment slack
 }

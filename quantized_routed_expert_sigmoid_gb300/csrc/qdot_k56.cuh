@@ -29,6 +29,12 @@
 // has its low nibble in byte 96 + j (j < 8, low) or 96 + j - 8 (high nibble) and bits 4-5 in bits
 // 2(j / 4), 2(j / 4) + 1 of byte 104 + j % 4; w = d * (s_j - 32) * q.  Read and multiplied as
 // Q6_K (2-byte aligned blocks, signed codes, one scale per 16 weights).
+//
+// MXFP4 (17 bytes per 32 weights, OCP Microscaling): an E8M0 scale byte e, then 16 bytes whose
+// byte j holds E2M1 element j (low nibble) and j + 16 (high nibble); w = 2^(e - 127) * value.
+// The codes enter dp4a as signed bytes of twice their value (exact integers), one scale per
+// block, i.e. per staged sub-block of x.  Rows must be a multiple of 4 bytes (K % 128 == 0), so
+// that the aligned word loads of the byte-aligned blocks stay inside the row.
 #pragma once
 
 #include <type_traits>
@@ -40,6 +46,7 @@ namespace moe {
 constexpr int kQ5KBytes = 176;
 constexpr int kQ6KBytes = 210;
 constexpr int kQ3KBytes = 110;
+constexpr int kMxfp4Bytes = 17;
 
 template <>
 struct Walk<MOE_Q5_K> {
@@ -55,6 +62,11 @@ template <>
 struct Walk<MOE_Q3_K> {
     static constexpr int kBlockWeights = 256;
     static constexpr int kBlockBytes = kQ3KBytes;
+};
+template <>
+struct Walk<MOE_MXFP4> {
+    static constexpr int kBlockWeights = 32;
+    static constexpr int kBlockBytes = kMxfp4Bytes;
 };
 
 __device__ __forceinline__ int qd_dp4a_ss(uint32_t a, uint32_t b, int c) {
@@ -172,8 +184,52 @@ __device__ __forceinline__ void q6_words(const uint8_t* p, uint32_t (&out)[N]) {
 // Signed codes (as bytes) of sub-blocks 2c and 2c + 1 of group g of one row, and d * scale of the
 // group's four 16-weight quarters.  Q6_K: u - 32 from a nibble and two high bits; Q3_K: v - 4
 // from two low bits and a high bit, with 6-bit scales stored + 32.
+// n consecutive 4-byte words from byte p at any alignment (aligned loads, funnel-shifted).
+// Reads stay inside [p & ~3, p + 4n) and, when p is not 4-byte aligned, up to the next
+// 4-byte boundary after p + 4n - 1.
+template <int N>
+__device__ __forceinline__ void q_words_any(const uint8_t* p, uint32_t (&out)[N]) {
+    const uint32_t mis = (uint32_t)(reinterpret_cast<uintptr_t>(p) & 3u);
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(p - mis);
+    uint32_t a[N + 1];
+#pragma unroll
+    for (int j = 0; j < N; ++j) a[j] = __ldg(w + j);
+    a[N] = mis ? __ldg(w + N) : 0u;
+#pragma unroll
+    for (int j = 0; j < N; ++j) out[j] = __funnelshift_r(a[j], a[j + 1], 8u * mis);
+}
+
+// Four E2M1 codes (one per byte, low nibble) as signed bytes of twice their value: magnitudes
+// 0, 0.5, 1, 1.5, 2, 3, 4, 6 become 0, 1, 2, 3, 4, 6, 8, 12 (byte permutes from two 8-byte
+// tables, the negative table chosen by the sign bit).
+__device__ __forceinline__ uint32_t e2m1x2_bytes(uint32_t nib) {
+    const uint32_t mag = nib & 0x07070707u;
+    const uint32_t sel = (mag & 0x7u) | ((mag >> 4) & 0x70u) | ((mag >> 8) & 0x700u) | ((mag >> 12) & 0x7000u);
+    const uint32_t pos = __byte_perm(0x03020100u, 0x0C080604u, sel);
+    const uint32_t neg = __byte_perm(0xFDFEFF00u, 0xF4F8FAFCu, sel);
+    const uint32_t sgn = ((nib >> 3) & 0x01010101u) * 0xFFu;
+    return (pos & ~sgn) | (neg & sgn);
+}
+
 template <int QT>
 __device__ __forceinline__ void q_signed_codes(const uint8_t* rp, int g, uint32_t (&cw)[2][8], float (&sd)[4]) {
+    if constexpr (QT == MOE_MXFP4) {
+        // group g = blocks 2g (sub-block 0) and 2g + 1: an E8M0 scale byte, then byte j holds
+        // element j (low nibble) and element j + 16 (high nibble); codes are twice the value, so
+        // the scale is 2^(e - 128) (e = 255: NaN)
+#pragma unroll
+        for (int sb = 0; sb < 2; ++sb) {
+            const uint8_t* blk = rp + (int64_t)(2 * g + sb) * kMxfp4Bytes;
+            const uint32_t e = __ldg(blk);
+            const float s = e == 255u ? __int_as_float(0x7FC00000) : ldexpf(0.5f, (int)e - 127);
+            sd[2 * sb] = sd[2 * sb + 1] = s;
+            uint32_t q[4];
+            q_words_any<4>(blk + 1, q);
+#pragma unroll
+            for (int qd = 0; qd < 8; ++qd)
+                cw[sb][qd] = e2m1x2_bytes(qd < 4 ? (q[qd] & 0x0F0F0F0Fu) : ((q[qd - 4] >> 4) & 0x0F0F0F0Fu));
+        }
+    } else {
     const int b = g >> 2, c = g & 3, h = c >> 1, rlo = 2 * (c & 1);   // sub-block 2c: r = rlo; 2c+1: rlo+1
     if constexpr (QT == MOE_Q6_K) {
         const uint8_t* blk = rp + (int64_t)b * kQ6KBytes;
@@ -219,6 +275,7 @@ __device__ __forceinline__ void q_signed_codes(const uint8_t* rp, int g, uint32_
             cw[0][qd] = __vsub4(v0, 0x04040404u);
             cw[1][qd] = __vsub4(v1, 0x04040404u);
         }
+    }
     }
 }
 
@@ -287,12 +344,12 @@ __device__ __forceinline__ void qd_signed_group(const uint8_t* const (&rowp)[4],
     }
 }
 
-// acc[r][t] += row r . vector vidx[t] (t < nt) for 4 rows of nblk super-blocks of type QT
-// (MOE_Q5_K, MOE_Q6_K or MOE_Q3_K), lanes split into row subsets as in qd4_rows4.
+// acc[r][t] += row r . vector vidx[t] (t < nt) for 4 rows of nblk blocks of type QT
+// (MOE_Q5_K, MOE_Q6_K, MOE_Q3_K or MOE_MXFP4), lanes split into row subsets as in qd4_rows4.
 template <int QT, int NT, int NPL>
 __device__ __forceinline__ void qd56_rows4(const uint8_t* const (&rowp)[4], int nblk, const uint4* X,
                                            const float4* XS, int nt, int lane, float (&acc)[4][NT]) {
-    const int G = nblk * 4;
+    const int G = QT == MOE_MXFP4 ? nblk / 2 : nblk * 4;        // groups of 64 weights
     auto grp = [&](auto rpl, int r0, int g) {
         constexpr int RPL = decltype(rpl)::value;
         if constexpr (QT == MOE_Q5_K) qd5_group<NT, RPL, NPL>(rowp, r0, g, G, X, XS, nt, acc, nullptr);

@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 2) qgemv_kernel(GemvArgs a, int iter
     __shared__ int s_rows[NT];
     for (int pb = 0; pb < n_tot; pb += NT) {
         const int nt = min(NT, n_tot - pb);
-        if constexpr (QT == MOE_Q4_K || QT == MOE_Q5_K || QT == MOE_Q6_K || QT == MOE_Q3_K) {
+        if constexpr (QT != MOE_Q8_0) {                     // K-quants and MXFP4: integer planes
             // ---- stage the activation vectors as integer planes (qdot.cuh)
             uint4* X = reinterpret_cast<uint4*>(xs);
             float4* XS = reinterpret_cast<float4*>(X + (size_t)NT * 16 * qd4_groups(a.K));
@@ -213,7 +213,7 @@ cudaError_t launch_one(const GemvArgs& a, int iters, int grid_y, cudaStream_t s)
 
 template <int QT, bool GU, int NPL>
 cudaError_t launch_nt(const GemvArgs& a, int nt, int iters, int grid_y, cudaStream_t s) {
-    if constexpr (QT == MOE_Q5_K || QT == MOE_Q6_K || QT == MOE_Q3_K) {   // codes take registers: two vectors a pass
+    if constexpr (QT == MOE_Q5_K || QT == MOE_Q6_K || QT == MOE_Q3_K || QT == MOE_MXFP4) {   // codes take registers
         return nt == 1 ? launch_one<QT, GU, 1, NPL>(a, iters, grid_y, s) : launch_one<QT, GU, 2, NPL>(a, iters, grid_y, s);
     } else {
         switch (nt) {
@@ -246,6 +246,7 @@ cudaError_t launch_qgemv(const GemvArgs& a, cudaStream_t s) {
     if (a.qtype == MOE_Q5_K) return planes(std::integral_constant<int, MOE_Q5_K>{});
     if (a.qtype == MOE_Q6_K) return planes(std::integral_constant<int, MOE_Q6_K>{});
     if (a.qtype == MOE_Q3_K) return planes(std::integral_constant<int, MOE_Q3_K>{});
+    if (a.qtype == MOE_MXFP4) return planes(std::integral_constant<int, MOE_MXFP4>{});
     return a.gateup ? launch_nt<MOE_Q8_0, true, 3>(a, nt, iters, grid_y, s)
                     : launch_nt<MOE_Q8_0, false, 3>(a, nt, iters, grid_y, s);
 }

@@ -12,7 +12,7 @@ import torch
 from . import _native as N
 
 _QT = {"q8_0": N.MOE_Q8_0, "q4_k": N.MOE_Q4_K, "q8_0_r": N.MOE_Q8_0_R, "q5_k": N.MOE_Q5_K, "q6_k": N.MOE_Q6_K,
-       "q3_k": N.MOE_Q3_K}
+       "q3_k": N.MOE_Q3_K, "mxfp4": N.MOE_MXFP4}
 
 
 def row_bytes(qtype: int, cols: int) -> int:
@@ -21,6 +21,8 @@ def row_bytes(qtype: int, cols: int) -> int:
         return 32 * nb + (2 * nb + 15) // 16 * 16
     if qtype == N.MOE_Q8_0:
         return cols // 32 * 34
+    if qtype == N.MOE_MXFP4:
+        return cols // 32 * 17
     return cols // 256 * {N.MOE_Q4_K: 144, N.MOE_Q5_K: 176, N.MOE_Q6_K: 210, N.MOE_Q3_K: 110}[qtype]
 
 

@@ -2,8 +2,8 @@
 
 This module draws the random tensors (activations, router weights, biases,
 RMSNorm weights, expert weights) and stores expert weights in the GGUF block
-layouts Q8_0 and Q4_K (and Q5_K, Q6_K, Q3_K and MXFP4, which only the
-oracle decodes so far).  It is shared by the tests, the benchmark and the
+layouts Q8_0, Q4_K, Q5_K, Q6_K, Q3_K and MXFP4.  It is shared by the tests,
+the benchmark and the
 smoke check, and it holds none of the layer's arithmetic: it never routes,
 never dequantizes and never evaluates an expert.  (Encoding a float matrix
 into blocks is how the stored inputs are made; decoding them is the oracle's

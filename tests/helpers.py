@@ -19,7 +19,7 @@ TOL_GEMV = 1e-4      # rel-L2 bound, fp32-accumulate dequant-GEMV path
 TOL_TC = 5e-3        # rel-L2 bound, fp16-operand tensor-core path
 
 OQ = {synth.Q8_0: oracle.Q8_0, synth.Q4_K: oracle.Q4_K, synth.Q5_K: oracle.Q5_K, synth.Q6_K: oracle.Q6_K,
-      synth.Q3_K: oracle.Q3_K}
+      synth.Q3_K: oracle.Q3_K, synth.MXFP4: oracle.MXFP4}
 
 
 def rel_l2(got, ref) -> float:

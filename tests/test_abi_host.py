@@ -67,7 +67,7 @@ def _desc(qtype=N.MOE_Q4_K, H=2048, I=768, E=128, data=FAKE, stride=None, mode=N
     d.W_router = FAKE
     from quantized_routed_expert_sigmoid_gb300.layer import row_bytes
     rb = ((lambda K: row_bytes(qtype, K)) if qtype in (N.MOE_Q4_K, N.MOE_Q8_0, N.MOE_Q8_0_R, N.MOE_Q5_K, N.MOE_Q6_K,
-                                                       N.MOE_Q3_K)
+                                                       N.MOE_Q3_K, N.MOE_MXFP4)
           else (lambda K: K // 32 * 34))
     sgu = stride if stride is not None else I * rb(H)
     d.gate = moe.qmat(qtype, data, I, H, sgu)
@@ -89,9 +89,9 @@ def test_plan_validation():
     finally:
         moe.moe_layer_plan_destroy(plan)
     _expect(N.MOE_ERR_UNSUPPORTED, moe.moe_layer_plan_create, _desc(qtype=N.MOE_BF16))
-    for other in (8, 9, -1):             # types the library does not decode, and garbage
+    for other in (9, 10, -1):            # types the library does not decode, and garbage
         _expect(N.MOE_ERR_UNSUPPORTED, moe.moe_layer_plan_create, _desc(qtype=other))
-    for qt in (N.MOE_Q5_K, N.MOE_Q6_K, N.MOE_Q3_K):   # K-quants beyond Q4_K: on the GEMV kernels at every T
+    for qt in (N.MOE_Q5_K, N.MOE_Q6_K, N.MOE_Q3_K, N.MOE_MXFP4):   # beyond Q4_K/Q8_0: GEMV kernels at every T
         plan = moe.moe_layer_plan_create(_desc(qtype=qt))
         try:
             assert all(moe.moe_layer_path(plan, T) == 0 for T in (1, 2, 64, 4096))

@@ -58,19 +58,19 @@ def test_decode_q4_k_fp32_activations(T):
     assert layer.path(T) == "gemv"
 
 
-@pytest.mark.parametrize("qt", [synth.Q5_K, synth.Q6_K, synth.Q3_K])
+@pytest.mark.parametrize("qt", [synth.Q5_K, synth.Q6_K, synth.Q3_K, synth.MXFP4])
 @pytest.mark.parametrize("T", [1, 3, 9, 70])
 def test_decode_shape_q5_k_q6_k(qt, T):
-    # the next K-quants on the GEMV kernels (every T): gate/up rows of 8 super-blocks, down rows
-    # of 3, so Q6_K's 210-byte and Q3_K's 110-byte blocks start 2 bytes off a 4-byte boundary in
-    # every other row
+    # the next expert types on the GEMV kernels (every T): gate/up rows of 2048 weights, down rows
+    # of 768, so Q6_K's 210-byte and Q3_K's 110-byte blocks start 2 bytes off a 4-byte boundary in
+    # every other row and MXFP4's 17-byte blocks at every byte offset
     shape = dataclasses.replace(synth.DECODE, qtype=qt)
     tl = make_layer(shape, 24, T)
     layer, _, _ = _check_layer(tl, T)
     assert layer.path(T) == "gemv"
 
 
-@pytest.mark.parametrize("qt", [synth.Q5_K, synth.Q6_K, synth.Q3_K])
+@pytest.mark.parametrize("qt", [synth.Q5_K, synth.Q6_K, synth.Q3_K, synth.MXFP4])
 def test_small_q5_k_q6_k_fp32(qt):
     # one super-block per row (the short-row lane split) and fp32 activations (three planes)
     shape = synth.LayerShape(H=256, E=8, k=2, I=256, qtype=qt, x_dtype="fp32")
