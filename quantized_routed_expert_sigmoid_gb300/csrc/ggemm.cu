@@ -9,23 +9,24 @@
 // Tile = 128 weight rows (MMA M; gate/up: 128 rows of each) x one token block of the expert
 // (MMA N: up to 256 pairs for Q4_K, 128 for Q8_0), K in steps of 64.  Weights are
 // dequantized from Q4_K / Q8_0 to fp16 in shared memory (128-byte swizzled K-major tiles);
-// token rows arrive by TMA into the same layout (gate/up: gather4 of x16 rows, four per
-// copy; down: one box of consecutive h16 rows); one thread issues tcgen05.mma with the
+// token rows arrive in the same layout (gate/up: the producers copy the block's x16 rows,
+// found through the pair order, 16 bytes a thread with cp.async; down: one TMA box of
+// consecutive h16 rows); one thread issues tcgen05.mma with the
 // accumulators in TMEM (fp32); tcgen05.ld reads them back for the epilogue.  Persistent CTAs
 // (one per SM) walk a device-built list of token blocks, so the launch needs no host
 // knowledge of the per-expert counts.
 //
 // Warp roles: producer warps (16 for the Q4_K gate/up, else 8) copy the raw blocks with
-// cp.async, dequantize them and issue the token-row TMA; gate/up producers also run the
+// cp.async, dequantize them and issue the token rows; gate/up producers also run the
 // SwiGLU epilogue (its accumulators fill all 512 TMEM columns); down has 8 epilogue warps
 // and two accumulator buffers, so its epilogue overlaps the next tile; the last warp owns
 // TMEM and issues the MMAs.  Pipeline per global k-step g: a producer waits until the A
-// stage g%2 is free (MMA(g-2) done), waits for raw(g), dequantizes it, arrives on full[g%4]
-// (which also counts the TMA bytes of B(g)), then issues raw and B of step g + D (D = 2 for
-// gate/up, 3 for down, across tile boundaries); the MMA warp waits full[g%4], issues four
-// k-substeps and commits to empty[g%4].  Every wait is bounded (globaltimer); on timeout
-// the kernel records MOE_ERR_TIMEOUT, drains its MMAs, waits (bounded) on the barriers of
-// the copies still in flight, frees TMEM and returns.
+// stage g%2 is free (MMA(g-2) done), waits for raw(g) (and, gate/up, B(g)), dequantizes it,
+// arrives on full[g%4] (down: which also counts the TMA bytes of B(g)), then issues raw and
+// B of step g + D (D = 2 for gate/up, 3 for down, across tile boundaries); the MMA warp
+// waits full[g%4], issues four k-substeps and commits to empty[g%4].  Every wait is bounded
+// (globaltimer); on timeout the kernel records MOE_ERR_TIMEOUT, drains its MMAs, waits
+// (bounded) on the barriers of the copies still in flight, frees TMEM and returns.
 #include <algorithm>
 #include <cuda.h>   // CUtensorMap and its enums (the encoder is fetched from the driver at run time)
 
@@ -65,6 +66,12 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 }
 // fp16 operands and outputs: a value that rounds to inf (or is NaN) is reported, not hidden.
 __device__ __forceinline__ bool half_finite(__half h) { return (__half_as_ushort(h) & 0x7C00u) != 0x7C00u; }
+// max that keeps NaN (so that a NaN h is reported like an overflow)
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
 // One report per warp: the status word becomes MOE_ERR_DEVICE_CHECK unless it holds an error.
 __device__ __forceinline__ void report_out_of_range(bool bad, int lane, WsHeader* hdr) {
     if (__any_sync(0xffffffffu, bad) && lane == 0 && hdr) atomicCAS(&hdr->status, (int)MOE_OK, (int)MOE_ERR_DEVICE_CHECK);
@@ -131,8 +138,7 @@ struct TileInfo {
 };
 
 struct TcParams {
-    CUtensorMap tmap_b;          // B rows: GATEUP x16 [T][K] (box 64 x 1, gathered 4 rows at a
-                                 // time); DOWN h16 [P][K] (box 64 x BN); 128-byte swizzle
+    CUtensorMap tmap_b;          // DOWN: B rows h16 [P][K] (box 64 x BN, 128-byte swizzle)
     const uint8_t* w0;           // gate (GATEUP) or down (DOWN) weights
     const uint8_t* w1;           // up (GATEUP)
     int64_t expert_stride;
@@ -140,6 +146,7 @@ struct TcParams {
     int K;                       // H for GATEUP, I for DOWN
     int k;                       // top-k (token of pair = sorted_pairs[i] / k)
     const int32_t* sorted_pairs; // GATEUP gather map (NULL: identity)
+    const __half* x16;           // GATEUP: token rows [T][K] fp16 (copied 16 bytes a thread)
     const int4* tb_list;         // [0].x = number of token blocks, then (e, tok0, ntok, 0); NULL: identity
     int n_identity;              // identity mode: tokens
     int bn;                      // token-block width of the list (tc_bn)
@@ -221,7 +228,7 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
         *abort_flag = 0;
         *max_issued = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tmap_b) : "memory");
+        if (MODE == kDown) asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tmap_b) : "memory");
     }
     if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
@@ -248,7 +255,6 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
         const int prow = tid & 127;                 // weight row within the tile
         const int pmat = MODE == kGateUp ? (tid >> 7) & 1 : 0;   // matrix: 0 gate / down, 1 up
         const int part = (tid >> 7) / kMats;        // which 1/kSplit of the row's k-step
-        constexpr int kRowsPW = BN / kPW, kGroupsPW = kRowsPW / 4;
         // ---- issue cursor: runs two k-steps ahead of the dequantization, across tile
         // boundaries, so that a tile's first raw blocks and token rows are in flight while the
         // previous tile finishes
@@ -256,42 +262,41 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
         TileInfo iti{};
         bool is_valid = false;
         const uint8_t* is_wrow = nullptr;
-        // GATEUP: this warp's gathers of the cursor's tile: how many, and the four x16 rows of
-        // the lane's group (lane < is_mine)
-        int is_mine = 0, is_y0 = 0, is_y1 = 0, is_y2 = 0, is_y3 = 0;
+        // GATEUP: the x16 rows this thread copies for the cursor's tile (NULL past its tokens)
+        constexpr int kBRowsPass = kNP / 8, kBPass = BN / kBRowsPass;
+        static_assert(kBPass * kBRowsPass == BN, "B rows per producer pass");
+        const uint8_t* is_xb[kBPass];
         auto is_tile = [&]() {
             is_valid = is_t < n_tiles && tile_at(p, n_mb, is_t, n_tb, iti);
             if (!is_valid) return;
             is_wrow = (pmat == 1 ? p.w1 : p.w0) + (int64_t)iti.e * p.expert_stride + (int64_t)(iti.m0 + prow) * rb;
             if (MODE == kGateUp) {
-                // lane l < kRowsPW takes the x16 row of column kRowsPW * warp + l; columns past the
-                // block's tokens take its first token's row (never read)
-                const int r = kRowsPW * warp + lane;
-                const int i = iti.tok0 + (r < iti.ntok ? r : 0);
-                const int row = p.sorted_pairs ? p.sorted_pairs[i] / p.k : i;
-                const int ngroups = (iti.ntok + 3) >> 2;
-                is_mine = min(kGroupsPW, max(0, ngroups - kGroupsPW * warp));
-                const int src = (4 * lane) & (kRowsPW - 1);
-                is_y0 = __shfl_sync(0xffffffffu, row, src);
-                is_y1 = __shfl_sync(0xffffffffu, row, src + 1);
-                is_y2 = __shfl_sync(0xffffffffu, row, src + 2);
-                is_y3 = __shfl_sync(0xffffffffu, row, src + 3);
+                // thread t copies 16-byte chunk t % 8 of columns t / 8 + kBRowsPass * j of the block
+#pragma unroll
+                for (int j = 0; j < kBPass; ++j) {
+                    const int r = (tid >> 3) + kBRowsPass * j;
+                    if (r < iti.ntok) {
+                        const int i = iti.tok0 + r;
+                        const int row = p.sorted_pairs ? p.sorted_pairs[i] / p.k : i;
+                        is_xb[j] = reinterpret_cast<const uint8_t*>(p.x16 + (int64_t)row * p.K) + 16 * (tid & 7);
+                    } else {
+                        is_xb[j] = nullptr;
+                    }
+                }
             }
         };
-        // B of the cursor's k-step into stage `stage`, completing on full[stage]: GATEUP gathers
-        // four x16 rows per TMA (warp w: groups kGroupsPW * w.. of the rows the block needs),
-        // DOWN loads the BN consecutive h16 rows of the block in one box
+        // B of the cursor's k-step into stage `stage`: GATEUP copies the block's x16 rows 16 bytes
+        // a thread (cp.async into the 128-byte-swizzled layout, in the same commit group as the
+        // raw blocks, so the wait before the dequantization covers both; columns past the block's
+        // tokens are not loaded and never stored), DOWN loads its BN consecutive h16 rows in one
+        // TMA box that completes on full[stage]
         auto issue_b = [&](int kb, int stage) {
             uint8_t* dst = sB + stage * kBStageBytes;
             uint64_t* fb = &full[stage];
             if (MODE == kGateUp) {
-                if (is_mine > 0) {
-                    if (lane == 0) mbar_expect_tx(fb, (uint32_t)is_mine * 512u);
-                    __syncwarp();
-                    if (lane < is_mine)
-                        tma_gather4(dst + (kGroupsPW * warp + lane) * 512, &p.tmap_b, kb * kBK, is_y0, is_y1, is_y2,
-                                    is_y3, fb);
-                }
+#pragma unroll
+                for (int j = 0; j < kBPass; ++j)
+                    if (is_xb[j]) cp_async16(dst + swz((tid >> 3) + kBRowsPass * j, tid & 7), is_xb[j] + kb * 128, 16u);
             } else if (tid == 0) {
                 mbar_expect_tx(fb, (uint32_t)p.b_box_rows * 128u);
                 tma_load_2d(dst, &p.tmap_b, kb * kBK, iti.tok0, fb);
@@ -425,28 +430,37 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
                 // ---- epilogue: wait for the accumulators of this tile, h = SiLU(gate) * up
                 if (!mbar_wait(&accf[0], tile_iter & 1, abort_flag, p.wait_ns)) break;
                 tc_after();
-                // warp w reads TMEM lanes 32 (w % 4).. and every (kPW / 4)-th group of 16 columns
+                // warp w reads TMEM lanes 32 (w % 4).. and every (kPW / 4)-th group of 16 columns;
+                // lanes 2i and 2i + 1 trade one value of each column pair, so that each stores two
+                // adjacent rows of one column as a half2 (even lane: even column, odd: odd column)
                 const int q = warp & 3;
                 const int m = q * 32 + lane;
-                __half* hrow = p.h_out + (int64_t)ti.tok0 * p.rows + ti.m0 + m;
-                bool out_of_range = false;               // an h value beyond the fp16 range
+                const bool odd = (lane & 1) != 0;
+                __half* hrow = p.h_out + (int64_t)(ti.tok0 + (odd ? 1 : 0)) * p.rows + ti.m0 + (m & ~1);
+                float amax = 0.0f;                       // largest |h| of the block's columns (NaN kept)
                 for (int c16 = (warp >> 2) * 16; c16 < ti.n_inst; c16 += 16 * (kPW / 4)) {
                     uint32_t a[16], u[16];
                     tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c16, a);
                     tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(BN + c16), u);
                     tmem_ld_wait();
+                    const int nv = ti.ntok - c16;       // columns of this group that hold tokens
+                    float h[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const int col = c16 + j;
-                        if (col < ti.ntok) {
-                            const float gv = __uint_as_float(a[j]), uv = __uint_as_float(u[j]);
-                            const __half hv = __float2half_rn(__fdividef(gv, 1.0f + __expf(-gv)) * uv);
-                            out_of_range |= !half_finite(hv);
-                            hrow[(int64_t)col * p.rows] = hv;
-                        }
+                        const float gv = __uint_as_float(a[j]), uv = __uint_as_float(u[j]);
+                        h[j] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+                        if (j < nv) amax = fmax_nan(amax, fabsf(h[j]));
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; j += 2) {
+                        const float recv = __shfl_xor_sync(0xffffffffu, odd ? h[j] : h[j + 1], 1);
+                        const float keep = odd ? h[j + 1] : h[j];
+                        const __half2 hv = odd ? __floats2half2_rn(recv, keep) : __floats2half2_rn(keep, recv);
+                        if (j + (odd ? 1 : 0) < nv) *reinterpret_cast<__half2*>(hrow + (int64_t)(c16 + j) * p.rows) = hv;
                     }
                 }
-                report_out_of_range(out_of_range, lane, p.hdr);
+                // a value at or beyond 65520 rounds to inf in fp16
+                report_out_of_range(!(amax < 65520.0f), lane, p.hdr);
                 tc_before();
             }
         }
@@ -559,8 +573,8 @@ __global__ void __launch_bounds__(tc_threads<QT, MODE>(), 1) tc_gemm_kernel(cons
     __syncthreads();
     tc_after();
     if (*abort_flag) {
-        // every thread has left its loop.  The producers' raw copies (cp.async) are waited for;
-        // the token rows (TMA) of the last k-steps may still be in flight.  Each producer warp
+        // every thread has left its loop.  The producers' copies (cp.async) are waited for; the
+        // DOWN token rows (TMA) of the last k-steps may still be in flight.  Each producer warp
         // arrives on full[] for the k-steps it has not arrived on, up to the last one any warp
         // issued, so that the phase of each such step completes exactly when its bytes land.
         // Steps older than the last four completed already: a producer issues step s only after
@@ -745,8 +759,9 @@ cudaError_t launch_tc_expert_ffn(const TcFfnArgs& a, cudaStream_t s) {
     }
     TcParams gu{};
     gu.w0 = a.wg; gu.w1 = a.wu; gu.expert_stride = a.stride_gu; gu.rows = a.I; gu.K = a.H; gu.k = a.k;
-    if ((err = make_tmap_f16(&gu.tmap_b, a.x16, a.T, a.H, 1)) != cudaSuccess) return err;
+    if (((uintptr_t)a.x16 & 15) != 0 || a.H % 64 != 0) return cudaErrorInvalidValue;   // 16-byte row copies
     gu.sorted_pairs = a.identity ? nullptr : a.sorted_pairs;
+    gu.x16 = a.x16;
     gu.tb_list = a.identity ? nullptr : a.tb_list; gu.n_identity = a.identity ? a.T : 0; gu.bn = bn;
     gu.h_out = a.h16; gu.hdr = a.hdr;
     const WaitCfg wc = wait_cfg();

@@ -63,16 +63,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
         ::"r"(su32(dst)), "l"(tmap), "r"(x), "r"(y), "r"(su32(bar))
         : "memory");
 }
-// TMA gather: rows y0..y3 (any order) of a 2-D tensor map whose box is one row high,
-// columns x.. of the box width, into four consecutive box rows of shared memory.
-__device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, int x, int y0, int y1, int y2, int y3,
-                                            uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
-        ::"r"(su32(dst)), "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(su32(bar))
-        : "memory");
-}
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(su32(dst)), "l"(src), "r"(src_bytes)
