@@ -90,6 +90,8 @@ def _declare(lib):
     lib.oracle_route.restype = I32
     lib.oracle_permute.argtypes = [P, I32, I32, I32, P, P, P]
     lib.oracle_permute.restype = I32
+    lib.oracle_expert_counts.argtypes = [P, I64, I32, P]
+    lib.oracle_expert_counts.restype = I32
     lib.oracle_expert_ffn.argtypes = [I32, P, P, P, I32, I32, P, P, P]
     lib.oracle_expert_ffn.restype = I32
     lib.oracle_expert_ffn_mixed.argtypes = [I32, I32, P, P, P, I32, I32, P, P, P]
@@ -188,6 +190,19 @@ def permute(ids, E: int, lib=None):
     if rc != 0:
         raise ValueError("oracle_permute: expert id out of range")
     return sp, off, pp
+
+
+def expert_counts(ids, E: int, counts=None, lib=None) -> np.ndarray:
+    """The running routing histogram: counts (uint64 [E], zeros when None) plus, for each
+    expert, the number of pairs of ids routed to it.  Returns the updated counts."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32).reshape(-1)
+    out = np.zeros(E, dtype=np.uint64) if counts is None else np.array(counts, dtype=np.uint64, copy=True)
+    if out.shape != (E,):
+        raise ValueError("counts must have E entries")
+    rc = (lib or load()).oracle_expert_counts(_ptr(ids), ids.size, E, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_expert_counts: expert id out of range")
+    return out
 
 
 def expert_ffn(qtype: int, gate, up, down, H: int, I: int, x, lib=None, qtype_down: int | None = None):

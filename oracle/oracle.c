@@ -23,6 +23,7 @@
  *                experts scored by the sum of their two largest sel; keep the
  *                best G_k groups; top-k sel inside them; gates = scale*s/sum s
  *   permute      counts, exclusive offsets, pairs p = t*k+j sorted by (id, p)
+ *   histogram    running per-expert count of routed pairs over many calls
  *   expert FFN   y = Wd * ( silu(Wg x) (.) (Wu x) ),  silu(z) = z/(1+e^-z)
  *   combine      out[t] = sum_j w[t,j] * y[t,j]  (+ shared expert, unweighted)
  *   RMSNorm      u = x / sqrt(mean(x^2) + eps) * gamma
@@ -57,6 +58,8 @@
  *   router logits                         pinned (integer closed form)
  *   top-k softmax / sigmoid-group         pinned (brute force, special cases)
  *   permute                               pinned (brute force)
+ *   expert counts (routing histogram)     pinned (hand-counted example,
+ *                                         brute force, invariants)
  *   expert FFN, layer, combine            pinned (identity-expert closed form,
  *                                         dense-masked equals sparse)
  *   RMSNorm, bf16 rounding, stack         pinned (closed forms)
@@ -509,6 +512,27 @@ int oracle_permute(const int32_t* ids, int T, int k, int E,
         pair_pos[p] = i;
     }
     free(cursor);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Routing histogram: the engine counts its own routing so that the     */
+/* experts it calls most can be moved to the fast tier between steps    */
+/* ("bloomery README 0.3.1", opening feature list: MoE models larger    */
+/* than the card; "bloomery V4.1 README", feature list, "Adaptive       */
+/* residency").  counts[e] += #{p : ids[p] = e} over the P = T*k pairs  */
+/* of one call; counts carries over from call to call.                  */
+/* ------------------------------------------------------------------ */
+int oracle_expert_counts(const int32_t* ids, int64_t P, int E, uint64_t* counts)
+{
+    for (int64_t p = 0; p < P; ++p)
+        if (ids[p] < 0 || ids[p] >= E) return -1;
+    for (int e = 0; e < E; ++e) {
+        uint64_t n = 0;
+        for (int64_t p = 0; p < P; ++p)
+            if (ids[p] == e) n += 1;
+        counts[e] += n;
+    }
     return 0;
 }
 

@@ -85,6 +85,8 @@ MUTANTS = [
      ["sigmoid_group_bruteforce", "sigmoid_group_special"]),
     ("permute_unstable", "for (int64_t p = 0; p < P; ++p) {\n        int32_t i = cursor[ids[p]]++;",
      "for (int64_t p = P - 1; p >= 0; --p) {\n        int32_t i = cursor[ids[p]]++;", ["permute_bruteforce"]),
+    ("counts_reset_each_call", "counts[e] += n;", "counts[e] = n;", ["expert_counts"]),
+    ("counts_off_by_one_expert", "if (ids[p] == e) n += 1;", "if (ids[p] == e + 1) n += 1;", ["expert_counts"]),
     ("silu_sign", "return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));", ["ffn_identity"]),
     ("gate_up_swapped_in_h", "h[i] = silu(g) * u;", "h[i] = g * silu(u);", ["ffn_identity"]),
     ("combine_drops_weights", "o[n] += w[(int64_t)t * k + j] * yp[n];", "o[n] += yp[n];",

@@ -394,6 +394,41 @@ def test_permute_rejects_bad_ids(olib):
         oracle.permute(np.array([[0, 9]], dtype=np.int32), 8, lib=olib)
 
 
+def pin_expert_counts(lib):
+    # a hand-counted example: two calls of T=3, k=2 over E=4
+    c = oracle.expert_counts(np.array([[0, 2], [2, 3], [0, 2]]), 4, lib=lib)
+    assert c.tolist() == [2, 0, 3, 1]
+    c = oracle.expert_counts(np.array([[1, 3], [3, 0], [2, 1]]), 4, counts=c, lib=lib)
+    assert c.tolist() == [3, 2, 4, 3]
+    # brute force over many calls, and the total is the number of pairs routed
+    rng = np.random.default_rng(17)
+    E = 37
+    c = np.zeros(E, dtype=np.uint64)
+    want = [0] * E
+    pairs = 0
+    for T, k in ((1, 8), (5, 3), (64, 8), (9, 1)):
+        ids = rng.integers(0, E, size=(T, k)).astype(np.int32)
+        c = oracle.expert_counts(ids, E, counts=c, lib=lib)
+        for v in ids.reshape(-1):
+            want[int(v)] += 1
+        pairs += T * k
+    assert c.tolist() == want
+    assert int(c.sum()) == pairs
+    # the permutation's offsets are one call's counts
+    ids = rng.integers(0, E, size=(33, 4)).astype(np.int32)
+    _, off, _ = oracle.permute(ids, E, lib=lib)
+    assert oracle.expert_counts(ids, E, lib=lib).tolist() == np.diff(off).tolist()
+
+
+def test_expert_counts(olib):
+    pin_expert_counts(olib)
+
+
+def test_expert_counts_rejects_bad_ids(olib):
+    with pytest.raises(ValueError):
+        oracle.expert_counts(np.array([[0, 4]], dtype=np.int32), 4, lib=olib)
+
+
 # ---------------------------------------------------------------- expert FFN and layer
 
 def _identity_q8_0(n: int, d_bits: int = 0x3C00) -> np.ndarray:
@@ -697,6 +732,7 @@ PINS = {
     "sigmoid_group_bruteforce": pin_sigmoid_group_bruteforce,
     "sigmoid_group_special": pin_sigmoid_group_special,
     "permute_bruteforce": pin_permute_bruteforce,
+    "expert_counts": pin_expert_counts,
     "ffn_identity": pin_ffn_identity,
     "ffn_identity_kquants": pin_ffn_identity_kquants,
     "ffn_mixed_types": pin_ffn_mixed_types,
