@@ -198,6 +198,20 @@ moe_status moe_permute_noalloc(const int32_t* topk_ids, int T, int k, int E, int
                                int32_t* offsets, int32_t* pair_pos, moe_stream_t stream);
 
 /*
+ * moe_expert_counts_add -- the running routing histogram for callers of moe_permute.
+ *   Pages: the engine counts its own routing and moves the experts it calls most to the fast
+ *   tier between steps ("bloomery README 0.3.1", opening feature list, MoE models larger than
+ *   the card; "bloomery V4.1 README", feature list, "Adaptive residency").
+ * counts[e] += offsets[e+1] - offsets[e] for e < E, one launch on `stream`.
+ *   offsets (device): int32 [E+1], a moe_permute / moe_permute_noalloc result (non-decreasing);
+ *   counts (device): uint64 [E], owned by the caller, read and cleared by it between calls.
+ *   Atomic adds: calls on several streams may share one counts array.
+ * Errors: MOE_ERR_INVALID_ARG for E outside 1..1024 or a NULL array; MOE_ERR_CUDA when the
+ * launch fails.  moe_layer keeps the same histogram itself (moe_layer_desc.expert_counts).
+ */
+moe_status moe_expert_counts_add(const int32_t* offsets, int E, unsigned long long* counts, moe_stream_t stream);
+
+/*
  * moe_expert_ffn -- the SwiGLU experts over the grouped pairs.
  *   for sorted position i with pair p = sorted_pairs[i], token t = p / k,
  *   expert e (offsets[e] <= i < offsets[e+1]):
@@ -271,7 +285,7 @@ typedef struct {
     moe_qmat s_gate, s_up, s_down;/* shared expert (single matrices) */
     int accumulate;               /* 1: out += layer(x) (a residual add); 0: out = layer(x) */
     int tc_min_tokens;            /* T at or above this uses the tensor-core path (0 = default 65) */
-    int decode_chain_off;         /* 1: never use the chained decode kernels (T <= 4) */
+    int decode_chain_off;         /* 1: never use the chained decode kernels (T <= 8) */
     /* Pre-norm (nullable): x is the fp32 residual stream [T][H] (x_type MOE_F32) and the layer's
      * input is u = bf16(x / sqrt(mean_h x^2 + norm_eps) * norm_gamma), exactly as moe_rmsnorm_bf16
      * computes it; the chained decode kernels compute u themselves (no extra launch), the other
@@ -279,6 +293,13 @@ typedef struct {
      * call is a whole residual block, out += layer(norm(out)).  norm_gamma: (device) fp32 [H]. */
     const float* norm_gamma;
     float norm_eps;
+    /* Routing histogram (nullable): (device) uint64 [E], owned by the caller.  Every moe_layer
+     * call adds, for each expert, the number of its T*k pairs routed to that expert, inside
+     * the kernels that already order the pairs (no extra launch); the caller reads or clears it
+     * between calls.  The pages' engine counts its own routing and moves the experts it calls
+     * most to the fast tier ("bloomery README 0.3.1", opening feature list, MoE models larger
+     * than the card; "bloomery V4.1 README", feature list, "Adaptive residency"). */
+    unsigned long long* expert_counts;
 } moe_layer_desc;
 
 typedef struct moe_layer_plan moe_layer_plan;
@@ -310,8 +331,9 @@ moe_status moe_layer_path(const moe_layer_plan* plan, int T, int* path);
  * [T][H]).  Enqueued on `stream` with no host synchronization and no host
  * read-back, so it can be captured in a CUDA graph; replays give the same
  * bits as eager calls.  The expert path is chosen from T on the host
- * (moe_layer_path tells which): T <= 4 (T*k <= 64, E <= 256, Q4_K routed
- * experts, H <= 2048) the chained decode kernels, T < tc_min_tokens the fp32
+ * (moe_layer_path tells which): T <= 8 (T*k <= 64, E <= 256, Q4_K routed
+ * experts, H <= 2048, the staged x and the gate/up rings within the kernel's
+ * shared memory: T <= 6 at H = 2048) the chained decode kernels, T < tc_min_tokens the fp32
  * dequant-GEMV kernels (both fp32 accumulate), larger T the tensor-core
  * grouped GEMM (fp16 operands, fp32 accumulate; the per-pair down outputs
  * are rounded to fp16 before the fp32 combine).  out may alias x when
@@ -364,7 +386,7 @@ moe_status moe_permute_read_device_status(int T, int k, int E, void* workspace, 
 moe_status moe_debug_set_waits(uint64_t limit_ns, int stall);
 
 /*
- * moe_debug_set_stamps -- timing hook of the chained decode kernels (T <= 4); off by
+ * moe_debug_set_stamps -- timing hook of the chained decode kernels (T <= 8); off by
  * default (buf = NULL).  With a device buffer of at least 3*256*8*8 = 49,152 bytes, every
  * chained call launched afterwards has thread 0 of CTA c (c < 256) of kernel n (0 router
  * logits, 1 routing + gate/up, 2 down + combine) write the GPU's global nanosecond clock

@@ -48,7 +48,8 @@ class moe_layer_desc(ctypes.Structure):
                 ("gate", moe_qmat), ("up", moe_qmat), ("down", moe_qmat),
                 ("shared_intermediate", ctypes.c_int), ("s_gate", moe_qmat), ("s_up", moe_qmat),
                 ("s_down", moe_qmat), ("accumulate", ctypes.c_int), ("tc_min_tokens", ctypes.c_int),
-                ("decode_chain_off", ctypes.c_int), ("norm_gamma", ctypes.c_void_p), ("norm_eps", ctypes.c_float)]
+                ("decode_chain_off", ctypes.c_int), ("norm_gamma", ctypes.c_void_p), ("norm_eps", ctypes.c_float),
+                ("expert_counts", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -82,6 +83,7 @@ def _declare(lib):
         "moe_permute_workspace_size": [I, I, I, PS],
         "moe_permute": [P, I, I, I, P, P, P, P, S, P],
         "moe_permute_noalloc": [P, I, I, I, P, P, P, P],
+        "moe_expert_counts_add": [P, I, P, P],
         "moe_expert_ffn_workspace_size": [I, I, I, I, I, PS],
         "moe_expert_ffn": [ctypes.POINTER(moe_qmat)] * 3 + [I, P, I, I, I, I, P, P, I, P, P, S, P],
         "moe_expert_gateup": [ctypes.POINTER(moe_qmat)] * 2 + [I, P, I, I, I, I, P, P, I, P, P],
@@ -162,6 +164,11 @@ def moe_permute_workspace_size(T, k, E) -> int:
 def moe_permute(topk_ids, T, k, E, sorted_pairs, offsets, pair_pos, workspace, ws_bytes, stream=None):
     _check(load().moe_permute(_p(topk_ids), T, k, E, _p(sorted_pairs), _p(offsets), _p(pair_pos),
                               _p(workspace), ws_bytes, _stream(stream)))
+
+
+def moe_expert_counts_add(offsets, E, counts, stream=None):
+    """counts[e] += offsets[e+1] - offsets[e] (counts: int64 [E] on the device, a running histogram)."""
+    _check(load().moe_expert_counts_add(_p(offsets), E, _p(counts), _stream(stream)))
 
 
 def moe_permute_noalloc(topk_ids, T, k, E, sorted_pairs, offsets, pair_pos, stream=None):

@@ -161,6 +161,7 @@ DecodeArgs decode_shape_args(const moe_layer_desc& d, int T) {
         da.su = static_cast<const uint8_t*>(d.s_up.data);
         da.sd = static_cast<const uint8_t*>(d.s_down.data);
     }
+    da.counts = d.expert_counts;
     return da;
 }
 
@@ -631,7 +632,7 @@ moe_status moe_layer_timed(const moe_layer_plan* plan, const void* x, int T, flo
     if (err != cudaSuccess) return cuda_fail(err, "router logits kernel");
     err = launch_topk(d.route, logits, d.bias, T, ids, gw, nullptr, s);
     if (err != cudaSuccess) return cuda_fail(err, "top-k kernel");
-    err = launch_permute(ids, T, k, E, sorted, offs, ppos, hdr, at<int32_t>(workspace, w.chunk), s);
+    err = launch_permute(ids, T, k, E, sorted, offs, ppos, hdr, at<int32_t>(workspace, w.chunk), s, d.expert_counts);
     if (err != cudaSuccess) return cuda_fail(err, "permute kernel");
     float* y = at<float>(workspace, w.y);
     const float* shared = nullptr;

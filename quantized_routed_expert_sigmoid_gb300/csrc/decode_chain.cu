@@ -1,4 +1,5 @@
-// decode_chain.cu -- the MoE layer at T <= 4 tokens as three chained launches.
+// decode_chain.cu -- the MoE layer at T <= 8 tokens as three chained launches (as many as
+// the gate/up kernel's staged x and its 16 warps' rings fit: T <= 6 at hidden 2048).
 //
 // The pages run a decode step as one captured CUDA graph with the routed
 // experts on the card ("bloomery README 0.3.1", "Why it is fast").  At a few
@@ -37,7 +38,7 @@
 namespace moe {
 namespace {
 
-constexpr int kCMaxT = 4;
+constexpr int kCMaxT = 8;
 constexpr int kCMaxP = 64;
 constexpr int kCMaxE = 256;
 constexpr int kK1Threads = 128;
@@ -77,6 +78,7 @@ struct ChainParams {
     float* h_s;                             // [T][I_s] fp32: the shared expert's h (Q8_0 shared expert)
     float* out;
     int accumulate;
+    unsigned long long* counts;             // nullable [E]: the running routing histogram
     WsHeader* hdr;
     int it_H_s, it_Is_s;                    // Q8_0 walk iterations of the shared expert
     int k2_warps;                           // K2 warps per CTA (<= kK2MaxWarps)
@@ -89,13 +91,15 @@ struct ChainParams {
     uint64_t* stamps;                       // timing hook (NULL: off): [kernel][CTA][phase] globaltimer
 };
 
-// The routing every K2 CTA derives from the logits (shared memory).
+// The routing every K2 CTA derives from the logits (shared memory); the top-k scratch is
+// sized for the kernel's NT tokens.
+template <int NT>
 struct CtaRoute {
     int32_t ids[kCMaxP], sorted[kCMaxP], ppos[kCMaxP], tok[kCMaxP];
     float w[kCMaxP];
     int act_e[kCMaxP], act_start[kCMaxP], act_n[kCMaxP];
     int nact;
-    float sel[kCMaxT][2 * kCMaxE];
+    float sel[NT][2 * kCMaxE];
 };
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -179,7 +183,8 @@ __device__ __forceinline__ void bulk_to_smem(void* dst, const void* src, uint32_
 // Every thread of the CTA calls this.  Warp t < T selects token t's experts from the
 // logits (read through L2: another grid wrote them); warp 0 then orders the pairs by
 // expert (stable) and lists the active experts with their runs of sorted positions.
-__device__ void cta_route(const ChainParams& p, CtaRoute& R) {
+template <int NT>
+__device__ void cta_route(const ChainParams& p, CtaRoute<NT>& R) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int E = p.rc.E, k = p.rc.k, P = p.T * k;
     if (warp < p.T)
@@ -304,7 +309,7 @@ __global__ void __launch_bounds__(kK1Threads) chain_logits_kernel(const __grid_c
 template <int NT, int kSh>
 __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const __grid_constant__ ChainParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ CtaRoute R;
+    __shared__ CtaRoute<NT> R;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nthr = blockDim.x;
     const int T = p.T, H = p.H, I = p.I, k = p.rc.k, E = p.rc.E, P = T * k;
@@ -398,9 +403,14 @@ __global__ void __launch_bounds__(kK2MaxWarps * 32, 1) chain_gateup_kernel(const
             p.pair_pos[i] = R.ppos[i];
         }
         for (int e = tid; e <= E; e += nthr) {
-            int cnt = 0;
-            for (int i = 0; i < P; ++i) cnt += R.ids[i] < e ? 1 : 0;
+            int cnt = 0, mine = 0;
+            for (int i = 0; i < P; ++i) {
+                cnt += R.ids[i] < e ? 1 : 0;
+                mine += R.ids[i] == e ? 1 : 0;
+            }
             p.offsets[e] = cnt;
+            // the running routing histogram (nullable), from the same pass
+            if (p.counts && e < E && mine > 0) atomicAdd(&p.counts[e], (unsigned long long)mine);
         }
         __syncthreads();
         if (tid == 0) {                            // the down kernel may read the routing from here on
@@ -736,7 +746,7 @@ int sm_count() {
     return g_sms;
 }
 
-constexpr size_t kChainSmemCap = 200 * 1024;   // dynamic; the kernels' static shared memory is < 12 KB
+constexpr size_t kChainSmemCap = 200 * 1024;   // dynamic; the kernels' static shared memory is < 21 KB
 constexpr size_t kK3TwoPerSm = 108 * 1024;     // dynamic shared memory of a down CTA that still fits twice
 
 ChainLayout chain_layout(const DecodeArgs& a) {
@@ -827,7 +837,7 @@ ChainParams chain_params(const DecodeArgs& a, const ChainLayout& L) {
     p.logits = a.logits; p.ids = a.ids; p.gw = a.gw; p.sorted = a.sorted; p.offsets = a.offsets;
     p.pair_pos = a.pair_pos;
     p.hq = a.hq; p.hq_s = a.hq_s; p.h_s = a.h_s; p.out = a.out; p.accumulate = a.accumulate ? 1 : 0;
-    p.hdr = a.hdr;
+    p.hdr = a.hdr; p.counts = a.counts;
     p.it_H_s = L.it_H_s; p.it_Is_s = L.it_Is_s;
     p.k2_warps = L.k2_warps; p.k2_off_xs_s = L.k2_off_xs_s; p.k2_off_ring = L.k2_off_ring;
     p.rows_per_cta = L.rows_per_cta; p.k3_prefetch = L.k3_prefetch;
@@ -877,7 +887,8 @@ cudaError_t launch_decode_chain(const DecodeArgs& a, cudaStream_t s, cudaEvent_t
     switch (a.T) {
         case 1: return go(std::integral_constant<int, 1>{});
         case 2: return go(std::integral_constant<int, 2>{});
-        default: return go(std::integral_constant<int, 4>{});
+        case 3: case 4: return go(std::integral_constant<int, 4>{});
+        default: return go(std::integral_constant<int, 8>{});
     }
 }
 

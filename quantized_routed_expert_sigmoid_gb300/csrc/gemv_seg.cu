@@ -1,6 +1,6 @@
 // gemv_seg.cu -- the routed experts' gate/up and down for 5 <= T < 128 tokens.
 //
-// Between the decode chain (T <= 4) and the tensor-core GEMM the layer is still a
+// Between the decode chain (T <= 6 at hidden 2048) and the tensor-core GEMM the layer is still a
 // dequant-GEMV bound by the weight bytes, but each chosen expert now serves a few
 // tokens.  A persistent grid (one 16-warp CTA per SM) walks the active experts' units,
 // once per pass of at most NT of the expert's tokens; CTA c owns a contiguous range of

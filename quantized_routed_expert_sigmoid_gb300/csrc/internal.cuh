@@ -86,9 +86,10 @@ cudaError_t launch_topk(const moe_route_cfg& cfg, const float* logits, const flo
 
 // ---------------------------------------------------------------- permute
 size_t permute_scratch_bytes(int T, int k, int E);
+// counts (nullable, [E]): the running routing histogram, += this call's per-expert pair counts
 cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* sorted_pairs,
                            int32_t* offsets, int32_t* pair_pos, WsHeader* hdr, int32_t* chunk_base,
-                           cudaStream_t s);
+                           cudaStream_t s, unsigned long long* counts = nullptr);
 
 // ---------------------------------------------------------------- decode GEMV experts
 // One launch computes, for every active expert e and each of its pairs, either
@@ -161,6 +162,7 @@ struct DecodeArgs {
     uint8_t* hq_s;                // chain: the Q4_K shared expert's h, staged (T vectors)
     float* out;
     bool accumulate;
+    unsigned long long* counts;   // nullable [E]: += the call's per-expert pair counts
     WsHeader* hdr;
 };
 // The layer as three launches chained by programmatic dependent launch (decode_chain.cu).

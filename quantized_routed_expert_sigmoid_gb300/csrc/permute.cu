@@ -55,7 +55,8 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const int32_t* __rest
                                                            int nchunks, int32_t* __restrict__ sorted_pairs,
                                                            int32_t* __restrict__ offsets,
                                                            int32_t* __restrict__ pair_pos, WsHeader* hdr,
-                                                           int32_t* __restrict__ chunk_base, bool scatter) {
+                                                           int32_t* __restrict__ chunk_base, bool scatter,
+                                                           unsigned long long* __restrict__ counts) {
     extern __shared__ int smem[];
     int* base = smem;                 // [E]
     int* wcnt = smem + E;             // [32][E]
@@ -101,6 +102,8 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const int32_t* __rest
                 }
             }
         }
+        // the running routing histogram comes for free: these are the call's per-expert counts
+        if (counts && tot > 0) atomicAdd(&counts[threadIdx.x], (unsigned long long)tot);
         // E <= 1024 = blockDim, so one value per thread.
         const int ex = block_exclusive_scan(tot, warp_tot, &total);
         if (threadIdx.x < E) {
@@ -156,7 +159,7 @@ size_t permute_scratch_bytes(int T, int k, int E) {
 
 cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* sorted_pairs,
                            int32_t* offsets, int32_t* pair_pos, WsHeader* hdr, int32_t* chunk_base,
-                           cudaStream_t s) {
+                           cudaStream_t s, unsigned long long* counts) {
     const int P = T * k;
     if (P == 0) return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s);
     const int nchunks = (P + kPermuteChunk - 1) / kPermuteChunk;
@@ -165,15 +168,15 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int32_t* sor
     if (nchunks == 1) {
         if ((err = set_smem(permute_kernel<true>, sm)) != cudaSuccess) return err;
         permute_kernel<true><<<1, kThreads, sm, s>>>(ids, P, E, 1, sorted_pairs, offsets, pair_pos, hdr,
-                                                     chunk_base, false);
+                                                     chunk_base, false, counts);
         return cudaGetLastError();
     }
     if ((err = set_smem(permute_kernel<false>, sm)) != cudaSuccess) return err;
     permute_kernel<false><<<nchunks, kThreads, sm, s>>>(ids, P, E, nchunks, sorted_pairs, offsets, pair_pos,
-                                                        hdr, chunk_base, false);
+                                                        hdr, chunk_base, false, counts);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     permute_kernel<false><<<nchunks, kThreads, sm, s>>>(ids, P, E, nchunks, sorted_pairs, offsets, pair_pos,
-                                                        hdr, chunk_base, true);
+                                                        hdr, chunk_base, true, nullptr);
     return cudaGetLastError();
 }
 
@@ -232,5 +235,33 @@ extern "C" moe_status moe_permute_noalloc(const int32_t* topk_ids, int T, int k,
     int32_t* chunk_base = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(scratch) + kHeaderBytes);
     err = launch_permute(topk_ids, T, k, E, sorted_pairs, offsets, pair_pos, hdr, chunk_base, s);
     if (err != cudaSuccess) return report(MOE_ERR_CUDA, "moe_permute_noalloc: kernel launch failed");
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// moe_expert_counts_add: the running routing histogram for callers of
+// moe_permute (moe_layer keeps it inside its own permute).
+// ---------------------------------------------------------------------------
+namespace moe {
+namespace {
+
+__global__ void counts_add_kernel(const int32_t* __restrict__ offsets, int E, unsigned long long* __restrict__ counts) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e < E) {
+        const int n = offsets[e + 1] - offsets[e];
+        if (n > 0) atomicAdd(&counts[e], (unsigned long long)n);
+    }
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_expert_counts_add(const int32_t* offsets, int E, unsigned long long* counts,
+                                            moe_stream_t stream) {
+    using namespace moe;
+    if (E < 1 || E > kMaxExperts) return report(MOE_ERR_INVALID_ARG, "bad E");
+    if (!offsets || !counts) return report(MOE_ERR_INVALID_ARG, "NULL array");
+    counts_add_kernel<<<(E + 255) / 256, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(offsets, E, counts);
+    if (cudaGetLastError() != cudaSuccess) return report(MOE_ERR_CUDA, "moe_expert_counts_add: kernel launch failed");
     return MOE_OK;
 }

@@ -45,12 +45,13 @@ class MoeLayer:
                  bias=None, n_groups: int = 1, topk_groups: int = 1, scale: float = 1.0,
                  renormalize: bool = True, x_dtype: str = "bf16", I_s: int = 0, shared_qtype: str = "q8_0",
                  s_gate=None, s_up=None, s_down=None, accumulate: bool = False, tc_min_tokens: int = 0,
-                 decode_chain: bool = True, norm_gamma=None, norm_eps: float = 1e-6, qtype_down: str | None = None):
+                 decode_chain: bool = True, norm_gamma=None, norm_eps: float = 1e-6, qtype_down: str | None = None,
+                 expert_counts=None):
         self.E, self.k, self.H, self.I = E, k, H, I
         self.x_dtype = x_dtype
         qt = _QT[qtype]
         qd = _QT[qtype_down] if qtype_down else qt      # the down matrix may be stored in another type
-        self._keep = [gate, up, down, W_router, bias, s_gate, s_up, s_down, norm_gamma]
+        self._keep = [gate, up, down, W_router, bias, s_gate, s_up, s_down, norm_gamma, expert_counts]
         d = N.moe_layer_desc()
         d.route = N.route_cfg(N.MOE_ROUTE_SIGMOID_GROUP if mode == "sigmoid_group" else N.MOE_ROUTE_SOFTMAX,
                               E, k, n_groups, topk_groups, scale, renormalize)
@@ -73,6 +74,10 @@ class MoeLayer:
         if norm_gamma is not None:       # pre-norm: x is the fp32 residual stream
             d.norm_gamma = norm_gamma.data_ptr()
             d.norm_eps = norm_eps
+        if expert_counts is not None:    # running routing histogram: int64 [E] on the device
+            if expert_counts.dtype != torch.int64 or expert_counts.numel() != E or not expert_counts.is_cuda:
+                raise ValueError("expert_counts must be an int64 CUDA tensor of E entries")
+            d.expert_counts = expert_counts.data_ptr()
         self.desc = d
         self.plan = N.moe_layer_plan_create(d)
         self.ws = None

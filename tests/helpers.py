@@ -87,7 +87,7 @@ class SeededLayer:
                                 n_groups=s.n_groups, topk_groups=s.topk_groups, renormalize=s.renormalize,
                                 scale=s.scale, **kw)
 
-    def moe_layer(self, accumulate=False, tc_min_tokens=0):
+    def moe_layer(self, accumulate=False, tc_min_tokens=0, expert_counts=None):
         from quantized_routed_expert_sigmoid_gb300 import MoeLayer
         s = self.shape
         sh = self.bank.shared
@@ -97,7 +97,7 @@ class SeededLayer:
                         topk_groups=s.topk_groups, scale=s.scale, renormalize=s.renormalize, x_dtype=s.x_dtype,
                         I_s=s.I_s, shared_qtype=s.shared_qtype, s_gate=sh[0] if sh else None,
                         s_up=sh[1] if sh else None, s_down=sh[2] if sh else None, accumulate=accumulate,
-                        tc_min_tokens=tc_min_tokens)
+                        tc_min_tokens=tc_min_tokens, expert_counts=expert_counts)
 
 
 def make_layer(shape: synth.LayerShape, seed: int, T: int, exact_all: bool = False, device="cuda"):

@@ -42,10 +42,18 @@ def test_tiny_q8_0(T):
     _check_layer(tl, T)
 
 
-@pytest.mark.parametrize("T", [1, 2, 3, 4])
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 6, 7])
 def test_decode_q4_k(T):
     tl = make_layer(synth.DECODE, 2, T)
     _check_layer(tl, T)
+
+
+def test_decode_chain_token_range():
+    # at hidden 2048 the chain's staged x and its 16 warps' rings fit up to T = 6 tokens; T = 7
+    # and 8 take the GEMV kernels
+    tl = make_layer(synth.DECODE, 2, 1)
+    layer = tl.moe_layer()
+    assert [layer.path(T) for T in range(1, 10)] == ["decode_chain"] * 6 + ["gemv"] * 3
 
 
 @pytest.mark.parametrize("T", [2, 9, 40])
