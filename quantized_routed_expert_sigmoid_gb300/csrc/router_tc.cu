@@ -9,6 +9,11 @@
 // K-major tiles (6 stages, loads three k-steps ahead, so a stage is refilled three steps
 // after the MMAs that read it were issued), one thread issues the 12 MMAs of a k-step (4
 // substeps x 3 parts) into one TMEM accumulator, the producers then read it and write l fp32.
+// When T/128 x E/32 tiles leave most SMs idle (few tokens, or a long K), K is split over S
+// CTAs per tile (grid z); each writes its fp32 partial sums and a second launch adds the S
+// partials in split order, so a replay gives the same bits.
+#include <algorithm>
+
 #include "internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -26,8 +31,9 @@ constexpr int kRStageBytes = kRAStage + kRBStage;
 struct RouterTcParams {
     const __nv_bfloat16* x;          // [T][H]
     const __nv_bfloat16* w3;         // [3][E][H]: hi, mid, lo
-    float* logits;                   // [T][E]
+    float* logits;                   // [T][E], or the split's partial sums [S][T][E] when S > 1
     int T, H, E;
+    int nsplit;                      // S: K splits per tile (grid z)
     WsHeader* clear_hdr;
     uint64_t wait_ns;                // limit of every bounded wait
 };
@@ -54,13 +60,20 @@ __global__ void __launch_bounds__(kRThreads, 1) router_tc_kernel(const __grid_co
     volatile int* abort_flag = &abort_s;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t0 = blockIdx.x * kRM, e0 = blockIdx.y * kRN;
-    const int nk = p.H / kRK;
+    // this CTA's k-steps: kb0 .. kb0 + nk - 1 of the H / 64
+    const int nk_all = p.H / kRK, z = blockIdx.z;
+    const int kb0 = (int)((int64_t)nk_all * z / p.nsplit);
+    const int nk = (int)((int64_t)nk_all * (z + 1) / p.nsplit) - kb0;
+    float* const out = p.logits + (size_t)z * p.T * p.E;
     if (tid == 0) {
         for (int i = 0; i < kRStages; ++i) { mbar_init(&full[i], kRProducers); mbar_init(&empty[i], 1); }
         mbar_init(&accf, 1);
         abort_s = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        if (p.clear_hdr && blockIdx.x == 0 && blockIdx.y == 0) { p.clear_hdr->status = MOE_OK; p.clear_hdr->ticket = 0u; }
+        if (p.clear_hdr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
+            p.clear_hdr->status = MOE_OK;
+            p.clear_hdr->ticket = 0u;
+        }
     }
     if (warp == kRProducers / 32) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_slot)),
@@ -82,14 +95,14 @@ __global__ void __launch_bounds__(kRThreads, 1) router_tc_kernel(const __grid_co
             for (int i = 0; i < kRM / 16; ++i) {                   // A: 128 rows x 8 chunks
                 const int r = (tid >> 3) + 16 * i, t = t0 + r;
                 const bool ok = t < p.T;
-                cp_async16(st + swz(r, ch), p.x + (ok ? (int64_t)t * p.H + kb * kRK + ch * 8 : 0), ok ? 16u : 0u);
+                cp_async16(st + swz(r, ch), p.x + (ok ? (int64_t)t * p.H + (kb0 + kb) * kRK + ch * 8 : 0), ok ? 16u : 0u);
             }
 #pragma unroll
             for (int i = 0; i < 3 * kRN / 16; ++i) {               // B: 3 parts x kRN rows x 8 chunks
                 const int rr = (tid >> 3) + 16 * i, part = rr / kRN, r = rr - part * kRN, e = e0 + r;
                 const bool ok = e < p.E;
                 const __nv_bfloat16* src =
-                    p.w3 + (ok ? ((int64_t)part * p.E + e) * p.H + kb * kRK + ch * 8 : 0);
+                    p.w3 + (ok ? ((int64_t)part * p.E + e) * p.H + (kb0 + kb) * kRK + ch * 8 : 0);
                 cp_async16(st + kRAStage + part * kRN * 128 + swz(r, ch), src, ok ? 16u : 0u);
             }
         };
@@ -120,7 +133,7 @@ __global__ void __launch_bounds__(kRThreads, 1) router_tc_kernel(const __grid_co
                 tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c16, a);
                 tmem_ld_wait();
                 if (t < p.T) {
-                    float* dst = p.logits + (int64_t)t * p.E + e0 + c16;
+                    float* dst = out + (int64_t)t * p.E + e0 + c16;
                     if (e0 + c16 + 16 <= p.E) {
 #pragma unroll
                         for (int j = 0; j < 16; j += 4)
@@ -169,13 +182,51 @@ __global__ void __launch_bounds__(kRThreads, 1) router_tc_kernel(const __grid_co
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kRN) : "memory");
 }
 
+// logits = the S partial sums, added in split order (one thread per logit)
+__global__ void router_reduce_kernel(const float* __restrict__ partial, int64_t n, int S, float* __restrict__ logits) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    float v = partial[i];
+    for (int z = 1; z < S; ++z) v += partial[(size_t)z * n + i];
+    logits[i] = v;
+}
+
+// Partial sums of a split launch: S * T_pad * E_pad fp32 with S * (T_pad / 128) * (E_pad / 32)
+// <= 152 tiles, so at most 152 * 128 * 32 * 4 bytes whatever T and E are.
+constexpr size_t kRPartialCap = (size_t)152 * kRM * kRN * sizeof(float);
+
+int router_sms() {
+    static int n = 0;
+    if (n <= 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            n = 0;
+    }
+    return n > 0 ? n : 152;
+}
+
+// K splits for a launch of T tokens: doubled while the split tiles still fit the SMs once, each
+// split keeps at least four k-steps, and the partial sums fit their buffer.
+int router_splits(int T, int H, int E) {
+    const int tiles = ((T + kRM - 1) / kRM) * ((E + kRN - 1) / kRN);
+    const int sms = std::min(router_sms(), 152);
+    int S = 1;
+    while (S < 8 && tiles * 2 * S <= sms && H / kRK >= 4 * 2 * S &&
+           (size_t)2 * S * T * E * sizeof(float) <= kRPartialCap)
+        S *= 2;
+    return S;
+}
+
 }  // namespace
 
 bool router_tc_supported(int T, int H, int E, bool x_bf16) {
     return x_bf16 && T > 32 && H % kRK == 0 && E % 4 == 0 && E <= 1024;
 }
 
-size_t router_tc_split_bytes(int H, int E) { return (size_t)3 * E * H * sizeof(__nv_bfloat16); }
+// the three bf16 parts of W, then room for the partial sums of a split launch
+size_t router_tc_split_bytes(int H, int E) {
+    return align_up((size_t)3 * E * H * sizeof(__nv_bfloat16), 256) + kRPartialCap;
+}
 
 cudaError_t launch_router_tc(const void* x, int T, int H, const float* W, int E, float* logits, void* w3,
                              WsHeader* clear_hdr, cudaStream_t s) {
@@ -188,14 +239,20 @@ cudaError_t launch_router_tc(const void* x, int T, int H, const float* W, int E,
     if ((err = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
         cudaSuccess)
         return err;
+    const int S = router_splits(T, H, E);
+    float* partial = reinterpret_cast<float*>(static_cast<uint8_t*>(w3) + align_up((size_t)3 * n * sizeof(__nv_bfloat16), 256));
     RouterTcParams p{};
     p.x = static_cast<const __nv_bfloat16*>(x);
     p.w3 = parts;
-    p.logits = logits;
+    p.logits = S > 1 ? partial : logits;
     p.T = T; p.H = H; p.E = E;
+    p.nsplit = S;
     p.clear_hdr = clear_hdr;
     p.wait_ns = wait_cfg().limit_ns;
-    router_tc_kernel<<<dim3((T + kRM - 1) / kRM, (E + kRN - 1) / kRN), kRThreads, smem, s>>>(p);
+    router_tc_kernel<<<dim3((T + kRM - 1) / kRM, (E + kRN - 1) / kRN, S), kRThreads, smem, s>>>(p);
+    if ((err = cudaGetLastError()) != cudaSuccess || S == 1) return err;
+    const int64_t nl = (int64_t)T * E;
+    router_reduce_kernel<<<(unsigned)((nl + 255) / 256), 256, 0, s>>>(partial, nl, S, logits);
     return cudaGetLastError();
 }
 
