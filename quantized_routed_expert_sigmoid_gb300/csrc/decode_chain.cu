@@ -765,15 +765,20 @@ ChainLayout chain_layout(const DecodeArgs& a) {
     while (warps > 1 && L.k2_off_ring + warps * per_warp > kChainSmemCap) --warps;
     L.k2_warps = warps;
     L.k2_smem = L.k2_off_ring + warps * per_warp;
-    // K3: about two CTAs per SM, 8-row multiples
+    // K3: about two CTAs per SM, 8-row multiples; one CTA per SM with twice the rows when the
+    // staged h leaves room for only one (many pairs), so that each SM stages h once
     const int sms = std::max(1, sm_count());
-    int R = (H + 2 * sms - 1) / (2 * sms);
-    R = std::max(8, (R + 7) / 8 * 8);
-    L.rows_per_cta = R;
     o = (size_t)P * qd4_vec_bytes(I);
     L.k3_off_hs_s = (int)align_up(o, 16);
     if (sh) o = L.k3_off_hs_s + (q8 ? (size_t)T * L.it_Is_s * 4096 : (size_t)T * qd4_vec_bytes(a.I_s));
     L.k3_off_y = (int)align_up(o, 16);
+    int R = (H + 2 * sms - 1) / (2 * sms);
+    R = std::max(8, (R + 7) / 8 * 8);
+    if (L.k3_off_y + (size_t)(P + T) * R * 4 > kK3TwoPerSm) {
+        R = (H + sms - 1) / sms;
+        R = std::max(8, (R + 7) / 8 * 8);
+    }
+    L.rows_per_cta = R;
     o = L.k3_off_y + (size_t)(P + T) * R * 4;
     L.k3_off_w = (int)align_up(o, 16);
     // the down rows are copied into shared memory only while two CTAs still fit an SM (the
